@@ -1,0 +1,128 @@
+// plan.h - layout of parameters and of the activation arena, shared by the
+// host planner (host.cu) and the megakernel (mega.cuh).
+//
+// The arena holds every value that crosses a phase boundary of the update
+// (the "planned GPU-memory arena" of "How a training megakernel works",
+// section "4 - Scheduling and storage").  Offsets are fixed per dimensions,
+// so one plan serves every launch with the same hyperparameters.
+#pragma once
+#include <stdint.h>
+#include <cuda.h>
+
+#define MT_TILE_M 128           // routing pads each expert segment to this many rows
+#define MT_NMAPS 32
+
+// parameter tensors, in flat-buffer order
+enum ParamId {
+  P_EMB = 0, P_ATTN_NORM, P_WQKV, P_WO, P_MOE_NORM, P_ROUTER, P_WGATE, P_WUP, P_WDOWN,
+  P_FINAL_NORM, P_LM_HEAD, P_COUNT
+};
+
+// arena buffers
+enum ArenaId {
+  A_HDR = 0,   // control header (ArenaHdr)
+  A_ROPE,      // fp32 [S][hd/2][2] cos, sin
+  A_X,         // fp32 [L+1][T][d] residual stream entering each layer (L: final)
+  A_XM,        // fp32 [L][T][d] residual stream after attention
+  A_INV1,      // fp32 [L][T] attention RMSNorm 1/rms
+  A_INV2,      // fp32 [L][T] expert RMSNorm 1/rms
+  A_R,         // op   [L][T][d] attention RMSNorm output
+  A_QKV,       // op   [L][T][3hq] q,k after RoPE, v
+  A_O,         // op   [L][T][hq] attention output
+  A_LSE,       // fp32 [L][B*H][S] attention row log-sum-exp
+  A_R2,        // op   [L][T][d] expert RMSNorm output
+  A_Z,         // fp32 [L][T][E] router logits
+  A_IDX,       // i32  [L][T][K] chosen experts (slot 0 best)
+  A_WGT,       // fp32 [L][T][K] renormalised router weights
+  A_CNT,       // i32  [L][NCH][E] per-chunk expert counts
+  A_OFFS,      // i32  [L][E+1] padded segment starts
+  A_PERM,      // i32  [L][Pmax] assignment at each sorted row (-1 pad)
+  A_INVM,      // i32  [L][T*K] sorted row of each assignment
+  A_XS,        // op   [L][Pmax][d] expert inputs in expert order
+  A_GU,        // op   [L][Pmax][2F] gate and up pre-activations [g | u]
+  A_ACT,       // op   [L][Pmax][F] silu(g) * u
+  A_Y,         // fp32 [L][Pmax][d] expert outputs
+  A_RF,        // op   [T][d] final RMSNorm output
+  A_INVF,      // fp32 [T]
+  A_LOGITS,    // fp32 [T][V]
+  A_DLOGITS,   // op   [T][V]
+  A_TOKLOSS,   // fp32 [T]
+  A_DX,        // fp32 [T][d] gradient wrt the residual stream
+  A_DXO,       // op   [T][d] operand copy of A_DX
+  A_DY,        // op   [Pmax][d] gradient wrt expert outputs
+  A_DZ,        // fp32 [T][E] gradient wrt router logits
+  A_DGU,       // op   [Pmax][2F] gradient wrt [g | u]
+  A_DXS,       // fp32 [Pmax][d] gradient wrt expert inputs
+  A_DR2,       // fp32 [T][d] gradient wrt expert RMSNorm output
+  A_DO,        // op   [T][hq] gradient wrt attention output
+  A_DQKV,      // op   [T][3hq] gradient wrt q,k,v (before RoPE)
+  A_DR,        // fp32 [T][d] gradient wrt attention RMSNorm output
+  A_DRF,       // fp32 [T][d] gradient wrt final RMSNorm output
+  A_PART,      // fp32 [NCH][E+1][d] column-reduction partials
+  A_NORMPART,  // fp32 [NCH] squared-norm partials (double precision accumulate)
+  A_TRACE,     // i64  [NCH][MAXPH][2]
+  A_COUNT
+};
+
+#define MT_MAX_PHASES 512
+
+// TMA tensor maps (bf16 operands of the tensor-core products), one per 2-D
+// buffer; per-layer and per-expert tensors are addressed through the outer
+// coordinate of a map over the whole stack.
+enum MapId {
+  MAP_R = 0, MAP_WQKV, MAP_O, MAP_WO, MAP_XS, MAP_WGATE, MAP_WUP, MAP_ACT, MAP_WDOWN, MAP_RF,
+  MAP_WLM, MAP_DLOGITS, MAP_DY, MAP_DGU, MAP_DXO, MAP_DQKV, MAP_COUNT
+};
+
+struct MtDims {
+  int V, d, L, H, hd, hq, E, K, F, B, S, T;
+  int Pmax;    // rows of expert-ordered buffers: T*K + E*(MT_TILE_M-1), rounded up to MT_TILE_M
+  int nch;     // maximum number of CTAs (chunks) the arena was sized for
+  int op_bytes;
+};
+
+// Control header at the start of the arena.  Each word the barrier spins on
+// sits in its own 128-byte line.
+struct ArenaHdr {
+  unsigned int bar_count; unsigned int pad0[31];
+  unsigned int bar_gen;   unsigned int pad1[31];
+  int status; int error_site; int pad2[30];
+  // outputs (mirrors mt_outputs)
+  int micro_index, optimizer_ran;
+  float loss, loss_update, grad_norm, clip_coef;
+  int n_ctas, n_phases;
+  int expert_counts[16 * 64];
+};
+
+struct KArgs {
+  MtDims D;
+  float lr, beta1, beta2, eps, wd, clip, clip_eps, norm_eps, coef, rope_theta;
+  float bc1, bc2;               // 1 - beta^t, computed on the host in double
+  int micro_index, micro_count, run_opt;
+  unsigned int flags;
+  long long timeout_ns;
+  long long n_params;
+  float* master;
+  void* shadow;
+  float* grads;
+  float* adam_m;
+  float* adam_v;
+  const int* tokens;
+  char* arena;
+  long long poff[P_COUNT];      // element offsets of each tensor in the flat buffers
+  long long aoff[A_COUNT];      // byte offsets of each arena buffer
+  int use_tc;                   // tcgen05 GEMMs (bf16 only)
+  int use_tc_attn;              // tensor-core attention (bf16 only)
+  CUtensorMap maps[MT_NMAPS];
+};
+
+// host-side plan (host.cu)
+struct MtPlan {
+  MtDims D;
+  long long aoff[A_COUNT];
+  long long abytes[A_COUNT];
+  long long arena_bytes;
+  long long poff[P_COUNT];
+  long long pnumel[P_COUNT];
+  long long n_params;
+};

@@ -1,0 +1,345 @@
+"""Benchmark of the GB300 training-update megakernel.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config b32] [--impl ours|reference]
+
+One step is one complete training update (forward, cross-entropy, backward,
+global-norm clip, AdamW) of the ~219M-parameter top-2-of-16 MoE on synthetic
+tokens: one persistent-kernel launch per microbatch.  Prints one JSON line.
+Multi-GPU runs (torchrun) are independent replicas (weak scaling): the
+update has no data-parallel exchange in this single-GPU design.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import moe_inputs as mi  # noqa: E402
+
+WORKLOADS = {
+    "b32": "32 x 1024 tokens, one microbatch, 219M-param top-2-of-16 MoE (d 768, 8 layers, V 32000)",
+    "b2": "2 x 1024 tokens, one microbatch, 219M-param top-2-of-16 MoE (d 768, 8 layers, V 32000)",
+    "accum16": "16 microbatches of 8 x 1024 tokens, one optimizer step, 219M-param MoE",
+    "top8": "1 x 4096 Zipf tokens, top-8-of-32 experts d_ff 256, 219M-param MoE",
+    "tiny": "2 x 32 tokens, tiny fp32 MoE (d 64, 2 layers, 4 experts)",
+}
+METRIC = "MoE train-update ms & tokens/s (B2x1024, B32x1024); % bf16 tensor peak"
+ARENA_HDR_BYTES = 4512   # mt_read_outputs copies the arena's control header
+
+
+def flops_per_update(cfg) -> float:
+    """6 x active matmul parameters x tokens + causal attention (3 x 2 B S^2 d L)."""
+    d, L, hq = cfg.d_model, cfg.n_layers, cfg.n_heads * cfg.head_dim
+    per_layer = 3 * hq * d + hq * d + cfg.n_experts * d + cfg.top_k * 3 * cfg.d_ff * d
+    active = L * per_layer + cfg.vocab * d
+    toks = cfg.tokens_per_update
+    attn = 3 * 2 * cfg.batch * cfg.seq ** 2 * hq * L * cfg.micro_count
+    return 6.0 * active * toks + attn
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(bf16=d.get("bf16_tflops", 1900.0), bf16_sustained=d.get("bf16_tflops_sustained", 1700.0),
+                    hbm=d.get("hbm_gbs", 6800.0), source="measured")
+    return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_uuid: str | None):
+        self.dev = dev_uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if self.dev:
+                cmd += ["-i", self.dev]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 7:
+                    try:
+                        rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+                    except ValueError:
+                        pass
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ---------------------------------------------------------------------------
+def oracle_sample_time(cfg, params, tokens, seq_tokens: int) -> tuple[float, str]:
+    """Time the oracle, as it stands, on one sequence prefix of `seq_tokens`
+    positions (forward + backward) plus the matching share of the clip+AdamW
+    sweep.  Returns (seconds, description)."""
+    import oracle
+    D = oracle.Dims.of(cfg)
+    tok = tokens[0][:1, :seq_tokens]
+    share = seq_tokens / cfg.tokens_per_update
+    t0 = time.perf_counter()
+    P = oracle.to64(params)
+    grads = {k: np.zeros_like(v) for k, v in P.items()}
+    oracle.forward_backward(P, tok, D, 1.0 / oracle.n_targets(*tok.shape), grads)
+    sl = {k: v.reshape(-1)[: max(1, int(v.size * share))] for k, v in P.items()}
+    gs = {k: grads[k].reshape(-1)[: sl[k].size] for k in sl}
+    z = {k: np.zeros_like(v) for k, v in sl.items()}
+    oracle.clip_adamw(sl, gs, z, z, lr=cfg.lr, beta1=cfg.beta1, beta2=cfg.beta2, eps=cfg.eps,
+                      weight_decay=cfg.weight_decay, clip_norm=cfg.clip_norm, clip_eps=cfg.clip_eps,
+                      step=1)
+    dt = time.perf_counter() - t0
+    desc = (f"oracle (NumPy float64) forward+backward of one {seq_tokens}-token sequence of the "
+            f"workload plus {share:.4%} of the clip+AdamW sweep; tokens/s = {seq_tokens}/time")
+    return dt, desc
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, cfg, rank):
+    """The oracle as the reference arm: rank 0 only, host cores."""
+    if rank != 0:
+        return
+    params = mi.make_params(cfg)
+    toks = mi.make_update_tokens(cfg)
+    seq_tokens = min(cfg.seq, args.ref_tokens)
+    for _ in range(args.warmup):
+        oracle_sample_time(cfg, params, toks, seq_tokens)
+    times = []
+    desc = ""
+    for _ in range(args.steps):
+        dt, desc = oracle_sample_time(cfg, params, toks, seq_tokens)
+        times.append(dt)
+    tot = sum(times)
+    tps = seq_tokens * len(times) / tot
+    ms_update = cfg.tokens_per_update / tps * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_update,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{args.config}: {WORKLOADS[args.config]}"},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, cfg, rank, world):
+    import torch
+    from adamw_persistent_sm_gb300 import binding as B
+    from adamw_persistent_sm_gb300.trainer import MoETrainer
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    B.load(build_if_missing=True)
+    params = mi.make_params(cfg)
+    host_toks = mi.make_update_tokens(cfg)
+    tr = MoETrainer(cfg, dev)
+    tr.load_params(params)
+    dtoks = [torch.as_tensor(t).to(dev) for t in host_toks]
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def one_update(step):
+        tr.update(dtoks, step=step)
+
+    step = 1
+    for _ in range(args.warmup):
+        one_update(step)
+        step += 1
+    out = tr.outputs()
+    if out.status != B.MT_OK:
+        raise RuntimeError(f"device status {B.status_string(out.status)} site {out.error_site}")
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    barrier()
+    clocks.start()
+    time.sleep(0.3)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    per_launch = []
+    ev0.record(stream)
+    for _ in range(args.steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one_update(step)
+        b.record(stream)
+        per_launch.append((a, b))
+        step += 1
+    ev1.record(stream)
+    barrier()
+    clock_info = clocks.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    upd_ms = [a.elapsed_time(b) for a, b in per_launch]
+    out = tr.outputs()
+    if out.status != B.MT_OK:
+        raise RuntimeError(f"device status {B.status_string(out.status)} site {out.error_site}")
+    ms = ms_total / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the public API: pinned host tokens in, loss out --
+    e2e = None
+    if not args.no_e2e:
+        pinned = [torch.as_tensor(t).pin_memory() for t in host_toks]
+        h2d = sum(t.numel() * 4 for t in pinned)
+        barrier()
+        t0 = time.perf_counter()
+        n_e2e = max(1, min(args.steps, 5))
+        for _ in range(n_e2e):
+            for i, p in enumerate(pinned):
+                dtoks[i].copy_(p, non_blocking=True)
+            one_update(step)
+            step += 1
+            o = tr.outputs()           # synchronises and reads the loss back
+            if o.status != B.MT_OK:
+                raise RuntimeError(B.status_string(o.status))
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+        e2e = {"value": cfg.tokens_per_update * world / (e2e_ms / 1e3), "unit": "tokens/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ARENA_HDR_BYTES}
+
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    flops = flops_per_update(cfg)
+    launch_ms = statistics.mean(upd_ms) / cfg.micro_count
+    achieved = flops / cfg.micro_count / (launch_ms / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16"], "traffic": None,
+            "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)",
+            "kernel": "mt_megakernel<__nv_bfloat16> (the only kernel of the step)"}
+    cpu = None
+    if not args.no_cpu_baseline:
+        dt, desc = oracle_sample_time(cfg, params, host_toks, min(cfg.seq, args.cpu_tokens))
+        tps = min(cfg.seq, args.cpu_tokens) / dt
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC,
+        "value": cfg.tokens_per_update * world / (ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "ms_per_step_min": min(upd_ms),
+        "ms_per_step_median": statistics.median(upd_ms),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if cfg.precision == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{args.config}: {WORKLOADS[args.config]}",
+                   "tokens_per_update": cfg.tokens_per_update,
+                   "flops_per_update": flops,
+                   "l2": "inputs larger than L2 (arena %.1f GB, params %.2f GB)" % (
+                       tr.arena_bytes / 1e9, tr.n_params * 4 / 1e9),
+                   "replicas": world,
+                   "context_h100_ms_per_update": {"b2": [13.63, 13.77], "b32": [68.27, 68.61]}.get(args.config)},
+        "tflops": achieved,
+        "gpu_launches": args.steps * cfg.micro_count,
+        "launches_per_update": cfg.micro_count,
+        "grid_barriers_per_launch": out.n_phases,
+        "roofline": roof,
+        "clocks": clock_info,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "loss": out.loss_update,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="b32", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--ref-tokens", type=int, default=256)
+    args = ap.parse_args()
+    cfg = mi.get_config(args.config)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, cfg, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,188 @@
+/*
+ * moe_train.h - C ABI of the GB300 training-update megakernel.
+ *
+ * One call of mt_train_update() runs one microbatch of a complete training
+ * update of a top-K-of-E mixture-of-experts transformer as ONE persistent
+ * cooperative CUDA kernel resident on every SM: forward pass, next-token
+ * cross-entropy, backward pass and - after the last microbatch of an update -
+ * global-norm clipping and AdamW.  This is the operation described by the
+ * Latch pages: "How a training megakernel works", sections "One training
+ * update" (forward, loss, backward, optimizer), "From two weights to 200
+ * million" (TinyMoE: attention + expert layers, top-2 of 16 routing, AdamW),
+ * "1 - Describe the model and update" (bf16 attention, token_topk,
+ * route_order, ragged_mm, global-norm clipping, AdamW), "4 - Scheduling and
+ * storage" (phases across all SMs, grid-wide barriers, a planned activation
+ * arena, FP32 master weights and Adam moments with BF16 matrix products) and
+ * "How GPUs usually run it" (16 microbatches, one kernel per microbatch, one
+ * optimizer update after the last).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller (allocated
+ *    e.g. through torch).  The library never allocates device memory and
+ *    never frees caller memory.  Pointers must be 256-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Work is enqueued asynchronously on it; the call returns after the launch.
+ *  - Every entry point returns an mt_status (0 = MT_OK).  Argument errors are
+ *    detected on the host before anything is enqueued.  Device-side failures
+ *    (a bounded wait that ran out) are reported in the arena's status word,
+ *    read with mt_read_outputs().
+ *  - Thread safety: calls on different arenas may run concurrently; calls
+ *    that share an arena must be ordered on one stream.
+ */
+#ifndef MOE_TRAIN_H_
+#define MOE_TRAIN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mt_status {
+  MT_OK = 0,
+  MT_ERR_ARG = 1,             /* null / misaligned pointer, bad size or hyperparameter */
+  MT_ERR_UNSUPPORTED = 2,     /* dimensions outside what the kernels implement */
+  MT_ERR_ARENA_SMALL = 3,     /* arena_bytes < mt_arena_bytes(hp) */
+  MT_ERR_LAUNCH = 4,          /* CUDA error at launch (e.g. cooperative grid too large) */
+  MT_ERR_DEVICE_TIMEOUT = 5,  /* a device-side bounded wait ran out (status word) */
+  MT_ERR_DEVICE_BOUNDS = 6,   /* a device-side index check failed (status word) */
+  MT_ERR_CUDA = 7             /* other CUDA runtime error */
+} mt_status;
+
+enum { MT_PREC_FP32 = 0, MT_PREC_BF16 = 1 };
+
+/* hp.flags bits */
+enum {
+  MT_FLAG_TRACE = 1u << 0,        /* record per-CTA phase timestamps in the arena */
+  MT_FLAG_SIMT_GEMM = 1u << 1,    /* bf16 mode: use the CUDA-core GEMM instead of tcgen05 */
+  MT_FLAG_SIMT_ATTN = 1u << 2,    /* bf16 mode: use the CUDA-core attention */
+  MT_FLAG_NO_OPTIMIZER = 1u << 3, /* skip clip + AdamW even on the last microbatch */
+  MT_FLAG_TEST_STALL = 1u << 4    /* test only: CTA 0 never arrives at the first grid
+                                     barrier, so the others' bounded waits run out */
+};
+
+/*
+ * Hyperparameters and dimensions of one microbatch launch (host struct,
+ * copied at call time).  Model: vocab V, d_model d, n_layers L, n_heads H of
+ * head_dim hd (H*hd may differ from d), n_experts E, top_k K, expert width
+ * d_ff F; this microbatch holds batch x seq tokens.
+ */
+typedef struct mt_hparams {
+  int32_t vocab, d_model, n_layers, n_heads, head_dim, n_experts, top_k, d_ff;
+  int32_t batch, seq;
+  int32_t precision;          /* MT_PREC_FP32 (exact fp32 FMAs, no TF32) | MT_PREC_BF16 */
+  int32_t micro_index;        /* 0 overwrites the gradients, > 0 adds into them */
+  int32_t micro_count;        /* optimizer runs when micro_index == micro_count - 1 */
+  uint32_t flags;
+  int64_t step;               /* AdamW step t (1-based) used for bias correction */
+  float lr, beta1, beta2, eps, weight_decay;
+  float clip_norm, clip_eps;  /* c = min(1, clip_norm / (||g|| + clip_eps)) */
+  float norm_eps;             /* RMSNorm epsilon */
+  float rope_theta;           /* rotary base */
+  float loss_coef;            /* per-target CE coefficient; 0 -> 1/(batch*(seq-1)*micro_count) */
+  int64_t wait_timeout_ns;    /* bound on every device-side wait; 0 -> 4e9 ns */
+} mt_hparams;
+
+/* One parameter tensor inside the flat fp32 parameter buffer. */
+typedef struct mt_tensor_desc {
+  char name[24];
+  int64_t offset;             /* element offset into the flat buffer (multiple of 64) */
+  int64_t numel;
+  int32_t ndim;
+  int64_t shape[4];
+  int32_t weight_decay;       /* 1: AdamW decay applies (every tensor, by design) */
+} mt_tensor_desc;
+
+#define MT_MAX_LAYERS 16
+#define MT_MAX_EXPERTS 64
+#define MT_MAX_CTAS 512
+
+/* Results of the last launch on an arena (see mt_read_outputs). */
+typedef struct mt_outputs {
+  int32_t status;             /* mt_status of the device side (0 = ok) */
+  int32_t error_site;         /* which wait / check failed (internal code) */
+  int32_t micro_index;        /* microbatch the values below belong to */
+  int32_t optimizer_ran;      /* 1 if clip + AdamW ran in this launch */
+  float loss;                 /* this microbatch's sum of coef * CE */
+  float loss_update;          /* running sum over the microbatches of this update */
+  float grad_norm;            /* ||g||_2 before clipping (valid if optimizer_ran) */
+  float clip_coef;            /* min(1, clip/(norm+eps))  (valid if optimizer_ran) */
+  int32_t n_ctas;             /* grid size of the launch */
+  int32_t n_phases;           /* grid-wide barriers passed */
+  int32_t expert_counts[MT_MAX_LAYERS * MT_MAX_EXPERTS]; /* tokens routed to [layer][expert] */
+} mt_outputs;
+
+/* Number of parameters (elements of the flat fp32 buffers params/grads/m/v). */
+int64_t mt_param_count(const mt_hparams* hp);
+
+/* Fill out[0..min(cap, n)-1] with the parameter layout; returns the number of
+ * tensors n (11) or a negative mt_status.  Order: emb [V,d], attn_norm [L,d],
+ * wqkv [L,3*H*hd,d], wo [L,d,H*hd], moe_norm [L,d], router [L,E,d],
+ * w_gate [L,E,F,d], w_up [L,E,F,d], w_down [L,E,d,F], final_norm [d],
+ * lm_head [V,d]; every matrix is [out, in]. */
+int32_t mt_param_layout(const mt_hparams* hp, mt_tensor_desc* out, int32_t cap);
+
+/* Bytes of caller-provided device arena the launch needs (worst case over
+ * routing), or a negative mt_status. */
+int64_t mt_arena_bytes(const mt_hparams* hp);
+
+/* Zero the arena's control header (barrier and status words).  Call once after
+ * allocating an arena, and again after a device-side error. */
+int32_t mt_arena_init(void* arena, int64_t arena_bytes, void* stream);
+
+/* Write the bf16 compute copy of the fp32 master parameters:
+ * shadow[i] = bf16(master[i]) for i < n (round to nearest even). */
+int32_t mt_sync_shadow(const float* master, void* shadow_bf16, int64_t n, void* stream);
+
+/*
+ * One microbatch of the training update, as one persistent kernel launch.
+ *   params  fp32 [n]   master weights (updated in place by the optimizer)
+ *   shadow  bf16 [n]   compute copy (read by bf16 products, rewritten by AdamW);
+ *                      may be NULL when hp->precision == MT_PREC_FP32
+ *   grads   fp32 [n]   gradient sum over the update's microbatches
+ *                      (overwritten when micro_index == 0)
+ *   adam_m, adam_v fp32 [n]  Adam moments (updated by the optimizer)
+ *   tokens  int32 [batch, seq] token ids in [0, vocab), device memory
+ *   arena   device scratch of arena_bytes >= mt_arena_bytes(hp), 256-B aligned,
+ *           initialised once with mt_arena_init; holds activations, routing
+ *           buffers, the status word and the outputs block.
+ * Position s of each sequence is trained to predict token s+1; the last
+ * position has no target.
+ */
+int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m,
+                        float* adam_v, const int32_t* tokens, const mt_hparams* hp,
+                        void* arena, int64_t arena_bytes, void* stream);
+
+/* Synchronise `stream` and copy the outputs block of the arena to *out.
+ * Returns out->status (MT_OK if the device side succeeded). */
+int32_t mt_read_outputs(const void* arena, mt_outputs* out, void* stream);
+
+/* Debug views into the arena after a launch (device pointers into the arena).
+ * which: see MT_VIEW_* ; layer selects the layer for per-layer buffers. */
+enum {
+  MT_VIEW_ROUTER_LOGITS = 0,  /* fp32 [T, E] */
+  MT_VIEW_TOPK_IDX = 1,       /* int32 [T, K] */
+  MT_VIEW_TOPK_W = 2,         /* fp32 [T, K] */
+  MT_VIEW_ROUTE_OFFS = 3,     /* int32 [E+1] padded segment starts (multiples of 128) */
+  MT_VIEW_ROUTE_PERM = 4,     /* int32 [Pmax] assignment t*K+k at each sorted row, -1 = pad */
+  MT_VIEW_TOK_LOSS = 5,       /* fp32 [T] coef * CE per position */
+  MT_VIEW_TRACE = 6,          /* int64 [n_ctas, n_phases, 2] (t_arrive, t_leave) ns */
+  MT_VIEW_HIDDEN = 7,         /* fp32 [T, d] residual stream entering `layer` (layer = L: final) */
+  MT_VIEW_LOGITS = 8          /* fp32 [T, V] */
+};
+typedef struct mt_view {
+  void* ptr;
+  int64_t numel;
+  int32_t elem_bytes;
+} mt_view;
+int32_t mt_debug_view(const void* arena, const mt_hparams* hp, int32_t which, int32_t layer,
+                      mt_view* out);
+
+/* Stable text for a status code. */
+const char* mt_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_TRAIN_H_ */

@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI: the library loads, exports every entry
+point the header declares, reports the parameter layout of the seeded inputs,
+sizes the arena monotonically, and rejects bad arguments before touching a
+GPU.  No compute call is made."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import moe_inputs as mi
+from adamw_persistent_sm_gb300 import binding as B
+from adamw_persistent_sm_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return B.load(build_if_missing=True)
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "moe_train.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\**\s*(mt_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_function(lib):
+    names = header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_library_is_in_tree(lib):
+    assert os.path.dirname(_build.LIB) == os.path.join(ROOT, "adamw_persistent_sm_gb300")
+
+
+@pytest.mark.parametrize("name", ["tiny", "b2", "top8"])
+def test_param_layout_matches_inputs(lib, name):
+    cfg = mi.get_config(name)
+    hp = B.hparams(cfg)
+    assert B.mt_param_count(hp) == mi.param_count(cfg)
+    lay = B.mt_param_layout(hp)
+    shapes = mi.param_shapes(cfg)
+    assert [t["name"] for t in lay] == [n for n, _ in shapes]
+    for t, (_, s) in zip(lay, shapes):
+        assert t["shape"] == s
+        assert t["offset"] % 64 == 0
+        assert t["weight_decay"] == 1
+    ends = [t["offset"] + t["numel"] for t in lay]
+    assert all(e <= o for e, o in zip(ends, [t["offset"] for t in lay][1:]))
+
+
+def test_param_count_of_published_stand_in(lib):
+    # 219,132,672 with an untied head (the page quotes 199,837,056 for TinyMoE)
+    assert B.mt_param_count(B.hparams(mi.get_config("b2"))) == 219_132_672
+    # 8 x (2d + 4d^2 + E d + 3 E F d) + 2 V d + d with E=32, F=256
+    assert B.mt_param_count(B.hparams(mi.get_config("top8"))) == 219_230_976
+
+
+def test_arena_grows_with_tokens(lib):
+    cfg = mi.get_config("b2")
+    sizes = [B.mt_arena_bytes(B.hparams(cfg.replace(batch=b))) for b in (1, 2, 4, 8)]
+    assert all(s > 0 for s in sizes)
+    assert sizes == sorted(sizes) and len(set(sizes)) == 4
+
+
+def _bad(cfg, **kw):
+    return B.hparams(cfg.replace(**kw)) if kw else B.hparams(cfg)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(vocab=0), B.MT_ERR_ARG),
+    (dict(head_dim=32), B.MT_ERR_UNSUPPORTED),
+    (dict(top_k=9, n_experts=16), B.MT_ERR_UNSUPPORTED),
+    (dict(n_experts=65), B.MT_ERR_UNSUPPORTED),
+    (dict(d_ff=100), B.MT_ERR_UNSUPPORTED),
+    (dict(seq=1), B.MT_ERR_UNSUPPORTED),
+    (dict(lr=float("nan")), B.MT_ERR_ARG),
+    (dict(beta2=1.0), B.MT_ERR_ARG),
+    (dict(micro_count=0), B.MT_ERR_ARG),
+])
+def test_bad_hparams_are_rejected(lib, kw, code):
+    hp = _bad(mi.get_config("tiny"), **kw)
+    assert B.mt_param_count(hp) == -code
+    assert B.mt_arena_bytes(hp) == -code
+
+
+def test_train_update_argument_checks(lib):
+    cfg = mi.get_config("tiny")
+    hp = B.hparams(cfg)
+    need = B.mt_arena_bytes(hp)
+    fake = 1 << 20                      # aligned, never dereferenced: checks fail first
+    args = [fake, 0, fake, fake, fake, fake]
+    assert B.mt_train_update(0, 0, fake, fake, fake, fake, hp, fake, need) == B.MT_ERR_ARG
+    assert B.mt_train_update(*args, hp, fake + 4, need) == B.MT_ERR_ARG          # misaligned arena
+    assert B.mt_train_update(*args, hp, fake, need - 1) == B.MT_ERR_ARENA_SMALL
+    hb = B.hparams(mi.get_config("b2"))
+    assert B.mt_train_update(*args, hb, fake, B.mt_arena_bytes(hb)) == B.MT_ERR_ARG   # bf16 needs shadow
+    hp.micro_index = 1
+    assert B.mt_train_update(*args, hp, fake, need) == B.MT_ERR_ARG               # index >= count
+    assert B.mt_arena_init(0, 1024) == B.MT_ERR_ARG
+    assert B.status_string(B.MT_ERR_DEVICE_TIMEOUT) == "device-side wait timed out"
+
+
+def test_struct_sizes_match_header(lib):
+    assert C.sizeof(B.mt_hparams) == 112
+    assert C.sizeof(B.mt_outputs) == 40 + 4 * 16 * 64
