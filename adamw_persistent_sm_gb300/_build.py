@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmt_gb300.so")
-UNITS = ["host.cu", "tmaps.cu", "mega_f32.cu", "mega_bf16.cu"]
+UNITS = ["host.cu", "tmaps.cu", "mega_f32.cu", "mega_bf16.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-diag-suppress", "186"]
 

@@ -87,6 +87,10 @@ _SIGNATURES = {
     "mt_read_outputs": (C.c_int32, [_P, C.POINTER(mt_outputs), _P]),
     "mt_debug_view": (C.c_int32, [_P, C.POINTER(mt_hparams), C.c_int32, C.c_int32, C.POINTER(mt_view)]),
     "mt_status_string": (C.c_char_p, [C.c_int32]),
+    "mt_train_update_noalloc": (C.c_int32, [_P, _P, _P, _P, _P, _P, C.POINTER(mt_hparams),
+                                            C.POINTER(mt_outputs), _P]),
+    "mt_debug_gemm": (C.c_int32, [_P, C.c_int32, _P, C.c_int32, _P, C.c_int32, C.c_int32, C.c_int32,
+                                  C.c_int32, _P, C.c_int32, C.c_int32, C.c_int32, _P, C.c_int64, _P]),
 }
 
 _lib = None
@@ -168,6 +172,18 @@ def mt_train_update(params: int, shadow: int, grads: int, adam_m: int, adam_v: i
                                   arena, arena_bytes, stream)
 
 
+MT_NOALLOC_ARENA_BYTES = 16 << 20
+
+
+def mt_train_update_noalloc(params: int, shadow: int, grads: int, adam_m: int, adam_v: int,
+                            tokens: int, hp: mt_hparams, out: mt_outputs | None = None,
+                            stream: int = 0) -> int:
+    """Training-update launch whose scratch arena is the library's fixed
+    device array (no device allocation by the caller or the library)."""
+    return load().mt_train_update_noalloc(params, shadow, grads, adam_m, adam_v, tokens, C.byref(hp),
+                                          C.byref(out) if out is not None else None, stream)
+
+
 def mt_read_outputs(arena: int, stream: int = 0) -> mt_outputs:
     out = mt_outputs()
     load().mt_read_outputs(arena, C.byref(out), stream)
@@ -180,6 +196,13 @@ def mt_debug_view(arena: int, hp: mt_hparams, which: int, layer: int = 0) -> mt_
     if st != MT_OK:
         raise ValueError(f"mt_debug_view: {status_string(st)}")
     return v
+
+
+def mt_debug_gemm(A: int, a_mn: int, B_: int, b_mn: int, C_: int, M: int, N: int, K: int, rag: int,
+                  offs: int, nseg: int, precision: int, use_tc: int, arena: int, arena_bytes: int,
+                  stream: int = 0) -> int:
+    return load().mt_debug_gemm(A, a_mn, B_, b_mn, C_, M, N, K, rag, offs, nseg, precision, use_tc,
+                                arena, arena_bytes, stream)
 
 
 def status_string(st: int) -> str:

@@ -179,6 +179,64 @@ typedef struct mt_view {
 int32_t mt_debug_view(const void* arena, const mt_hparams* hp, int32_t which, int32_t layer,
                       mt_view* out);
 
+/*
+ * mt_train_update_noalloc - the same launch as mt_train_update, but with no
+ * arena argument: the scratch arena is a fixed array of MT_NOALLOC_ARENA_BYTES
+ * that this library keeps in device memory.  The paper has no counterpart to
+ * this entry point.
+ *
+ * Who it is for: callers that are handed pointers to their tensors but may not
+ * allocate device memory themselves - for example a plug-in running inside a
+ * host application whose device memory is all owned by that application's
+ * own pool, or a service that has fixed its device-memory budget at start-up
+ * and may not call cudaMalloc (which can also block on device-wide work) while
+ * it serves.  The caller still passes every input and output (params, shadow,
+ * grads, adam_m, adam_v, tokens, out); this call makes no device allocation.
+ *
+ * Limits and behaviour:
+ *  - Only models with mt_arena_bytes(hp) <= MT_NOALLOC_ARENA_BYTES (16 MiB,
+ *    e.g. the tiny configuration, which needs about 8.8 MiB) are accepted;
+ *    larger ones return MT_ERR_ARENA_SMALL and nothing is enqueued.
+ *  - The array occupies MT_NOALLOC_ARENA_BYTES on every device where the
+ *    library's code is loaded, until the process exits.
+ *  - The first call on a device looks up the array's device address (with that
+ *    device current) and caches it; make that first call before any stream
+ *    capture.
+ *  - Every call uses the same array, which keeps what the previous call left
+ *    in it; each call clears the barrier and status words it needs at zero.
+ *    Calls whose execution overlaps on the GPU (different streams, or
+ *    different host threads on one device) race on the array and must be
+ *    serialised by the caller.
+ *  - out (host pointer, may be NULL): when given, the call synchronises
+ *    `stream` and copies the launch's outputs block to *out, returning
+ *    out->status; when NULL the call returns after the launch is enqueued.
+ */
+#define MT_NOALLOC_ARENA_BYTES (16u << 20)
+int32_t mt_train_update_noalloc(float* params, void* shadow, float* grads, float* adam_m, float* adam_v,
+                                const int32_t* tokens, const mt_hparams* hp, mt_outputs* out, void* stream);
+
+/*
+ * Test harness: one matrix product C = A * B^T through the megakernel's product
+ * engine (tcgen05 tensor cores when precision == MT_PREC_BF16 and use_tc != 0,
+ * CUDA cores otherwise), fp32 accumulation, fp32 C.  Used by the tests to check
+ * every operand layout of the update's products ("1 - Describe the model and
+ * update": dense products and ragged_mm) in isolation.
+ *   rag = 0: A is [M,K] (a_mn = 0) or [K,M] (a_mn = 1); B is [N,K] (b_mn = 0)
+ *            or [K,N] (b_mn = 1); C is [M,N].
+ *   rag = 1: ragged rows.  A [M,K] (a_mn must be 0) is split into nseg row
+ *            segments at offs (device int32 [nseg+1], multiples of 128, the
+ *            last <= M); segment e multiplies B[e] ([nseg][N][K] or
+ *            [nseg][K][N]); rows past offs[nseg] are not written.
+ *   rag = 2: ragged reduction.  A [K,M], B [K,N] (a_mn = b_mn = 1); segment e
+ *            reduces rows offs[e]..offs[e+1] into C[e] ([nseg][M][N]).
+ * A and B are bf16 (MT_PREC_BF16) or fp32 (MT_PREC_FP32) device arrays.  The
+ * tensor-core path needs M and N multiples of 128 and K a multiple of 64.
+ * arena: >= 4 KiB device scratch initialised with mt_arena_init.
+ */
+int32_t mt_debug_gemm(const void* A, int32_t a_mn, const void* B, int32_t b_mn, float* C, int32_t M, int32_t N,
+                      int32_t K, int32_t rag, const int32_t* offs, int32_t nseg, int32_t precision, int32_t use_tc,
+                      void* arena, int64_t arena_bytes, void* stream);
+
 /* Stable text for a status code. */
 const char* mt_status_string(int32_t status);
 
