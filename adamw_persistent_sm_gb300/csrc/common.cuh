@@ -20,6 +20,7 @@ enum ErrSite {
   SITE_TC_ACC_FULL = 12,
   SITE_TC_ACC_EMPTY = 13,
   SITE_TC_DRAIN = 14,
+  SITE_TC_ALIGN = 15,
   SITE_TEST_STALL = 20
 };
 

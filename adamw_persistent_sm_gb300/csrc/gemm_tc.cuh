@@ -1,24 +1,519 @@
-// gemm_tc.cuh - tensor-core (tcgen05) matrix products.  Placeholder until
-// the tcgen05 path lands: the CUDA-core path runs every product.
+// gemm_tc.cuh - tensor-core matrix products (tcgen05 + TMEM + TMA) inside
+// the persistent kernel, for the bf16-product policy.
+//
+// Tile 128 x 128 x 64.  Per GEMM job:
+//   warp 0 (one lane)  - TMA producer: two 64x64 boxes of A and two of B per
+//                        stage into a 6-stage ring of 128B-swizzled tiles;
+//   warp 1 (one lane)  - MMA issuer: 4 x tcgen05.mma (K = 16) per stage into
+//                        one of two TMEM accumulators (128 lanes x 128 fp32
+//                        columns each), tcgen05.commit frees the stage;
+//   warps 4..7         - epilogue: tcgen05.ld of the accumulator rows (warp
+//                        w reads TMEM lanes 32*(w-4)..), fused epilogue, store.
+// A and B may each be K-major or MN-major in memory (forward, dgrad and
+// wgrad products read the same buffers without transposed copies); the
+// shared-memory descriptors describe either layout.  Every mbarrier wait is
+// bounded: on expiry the status word records the site and the job drains.
 #pragma once
 #include "common.cuh"
 #include "gemm.cuh"
 
+#define TC_BM 128
+#define TC_BN 128
+#define TC_BK 64
+#define TC_STAGES 6
+#define TC_BOX_BYTES (64 * 64 * 2)
+#define TC_STAGE_BYTES (4 * TC_BOX_BYTES)
+#define TC_RING_OFF 1024
+#define MT_TC_SMEM (TC_RING_OFF + TC_STAGES * TC_STAGE_BYTES)
+#define TC_TMEM_COLS 256
+#define MT_TC_AVAILABLE 1
+
 struct TcState {
-  unsigned tmem_base;
-  unsigned long long iters;
+  uint32_t tmem_base;
 };
 
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of parity `parity` to complete; false after timeout_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if ((long long)(globaltimer() - t0) > timeout_ns) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"((unsigned long long)map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle.
+//   K-major : rows of 128 B, 8-row groups 1024 B apart (SBO); LBO unused.
+//   MN-major: 64-element MN chunks LBO apart, 8-row K groups 1024 B apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo & 0x3FFFFu) >> 4) << 16) |
+         ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// setup / teardown (once per kernel)
+// ---------------------------------------------------------------------------
 template <class OP>
 __device__ __forceinline__ void tc_setup(const KArgs& a, char* smem, TcState& tc) {
   tc.tmem_base = 0;
-  tc.iters = 0;
+  if constexpr (sizeof(OP) == 2) {
+    if (!a.use_tc) return;
+    uint32_t slot = smem_u32(smem + 256);
+    if ((threadIdx.x >> 5) == 0) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                   "r"(TC_TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tc.tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + 256);
+    __syncthreads();
+  }
 }
+
 template <class OP>
-__device__ __forceinline__ void tc_teardown(const KArgs& a, char* smem, TcState& tc) {}
+__device__ __forceinline__ void tc_teardown(const KArgs& a, char* smem, TcState& tc) {
+  if constexpr (sizeof(OP) == 2) {
+    if (!a.use_tc) return;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if ((threadIdx.x >> 5) == 0)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tc.tmem_base), "r"(TC_TMEM_COLS)
+                   : "memory");
+  }
+}
 
-__device__ __forceinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& g, Sched& s, char* smem,
-                                            TcState& tc) {}
+// ---------------------------------------------------------------------------
+// tiles
+// ---------------------------------------------------------------------------
+struct TcTile {
+  int m0, n0, seg, kbeg, nk;
+};
 
-#define MT_TC_AVAILABLE 0
-#define MT_TC_SMEM 0
+__device__ __forceinline__ TcTile tc_tile(const GemmDesc& g, int t, int nt) {
+  TcTile ti;
+  if (g.rag == RAG_K) {
+    const int mt = g.M / TC_BM;
+    ti.seg = t / (mt * nt);
+    const int rem = t % (mt * nt);
+    ti.m0 = (rem / nt) * TC_BM;
+    ti.n0 = (rem % nt) * TC_BN;
+    ti.kbeg = g.offs[ti.seg];
+    ti.nk = (g.offs[ti.seg + 1] - ti.kbeg) / TC_BK;
+  } else {
+    ti.m0 = (t / nt) * TC_BM;
+    ti.n0 = (t % nt) * TC_BN;
+    ti.seg = (g.rag == RAG_M) ? seg_of_row(g.offs, g.nseg, ti.m0) : 0;
+    ti.kbeg = 0;
+    ti.nk = g.K / TC_BK;
+  }
+  return ti;
+}
+
+// Load the A (rows m0..m0+127) or B (rows n0..n0+127) operand slice of one
+// 64-wide K block as two 64 x 64 boxes.
+__device__ __forceinline__ void tc_load_operand(const KArgs& a, const GOperand& o, int r0, int k0, int yseg_off,
+                                                uint32_t dst, uint32_t bar) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const CUtensorMap* map = &a.maps[o.map0];
+    int x, y;
+    if (!o.mn) {
+      // element (r, k) at row y0 + r, column k
+      int rr = r0 + 64 * i;
+      if (o.two == 1) {            // rows interleaved by 64 between two sources
+        map = &a.maps[i ? o.map1 : o.map0];
+        rr = (r0 >> 1);            // r0 is a multiple of 128: source row block r0/2
+      }
+      x = k0;
+      y = o.y0 + yseg_off + rr;
+    } else {
+      // element (r, k) at row y0 + k, column r
+      int kk = k0;
+      if (o.two == 2 && k0 >= o.split) {
+        map = &a.maps[o.map1];
+        kk = k0 - o.split;
+      }
+      x = r0 + 64 * i;
+      y = o.y0 + yseg_off + kk;
+    }
+    tma_load_2d(dst + i * TC_BOX_BYTES, map, x, y, bar);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// epilogue helpers: one thread owns one output row of the tile
+// ---------------------------------------------------------------------------
+template <int N>
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v) {
+#pragma unroll
+  for (int i = 0; i < N; i += 8) {
+    uint4 u;
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[i], v[i + 1]);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[i + 2], v[i + 3]);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[i + 4], v[i + 5]);
+    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[i + 6], v[i + 7]);
+    u.x = *reinterpret_cast<uint32_t*>(&h0);
+    u.y = *reinterpret_cast<uint32_t*>(&h1);
+    u.z = *reinterpret_cast<uint32_t*>(&h2);
+    u.w = *reinterpret_cast<uint32_t*>(&h3);
+    *reinterpret_cast<uint4*>(dst + i) = u;
+  }
+}
+template <int N>
+__device__ __forceinline__ void store_row_f32(float* dst, const float* v) {
+#pragma unroll
+  for (int i = 0; i < N; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+}
+template <int N>
+__device__ __forceinline__ void load_row_bf16(const __nv_bfloat16* src, float* v) {
+#pragma unroll
+  for (int i = 0; i < N; i += 8) {
+    uint4 u = *reinterpret_cast<const uint4*>(src + i);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float2 f = __bfloat1622float2(h[j]);
+      v[i + 2 * j] = f.x;
+      v[i + 2 * j + 1] = f.y;
+    }
+  }
+}
+
+static __device__ __noinline__ void tc_epilogue(const GemmDesc& g, const TcTile& ti, uint32_t trow, int m) {
+  typedef __nv_bfloat16 bf;
+  switch (g.epi) {
+    case EPI_ROPE: {
+      // hd == 64: columns [64h, 64h+32) pair with [64h+32, 64h+64)
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float x[64];
+        tmem_ld32(trow + h2 * 64, x);
+        tmem_ld32(trow + h2 * 64 + 32, x + 32);
+        const int n = ti.n0 + h2 * 64;
+        if (n < 2 * g.hq) {
+          const int pos = m % g.S;
+          const float* tab = g.rope + (long long)pos * 32 * 2;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float c = tab[2 * i], s = tab[2 * i + 1];
+            const float x1 = x[i], x2 = x[i + 32];
+            x[i] = x1 * c - x2 * s;
+            x[i + 32] = x2 * c + x1 * s;
+          }
+        }
+        store_row_bf16<64>((bf*)g.out + (long long)m * g.ldo + n, x);
+      }
+      break;
+    }
+    case EPI_SWIGLU: {
+      // tile columns [0,64) = gate, [64,128) = up of expert rows f0..f0+63
+      const int f0 = (ti.n0 >> 7) * 64;
+      for (int c = 0; c < 2; ++c) {
+        float gg[32], uu[32];
+        tmem_ld32(trow + c * 32, gg);
+        tmem_ld32(trow + 64 + c * 32, uu);
+        const int f = f0 + c * 32;
+        bf* gu = (bf*)g.out + (long long)m * g.ldo;
+        store_row_bf16<32>(gu + f, gg);
+        store_row_bf16<32>(gu + g.F + f, uu);
+        float act[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) act[i] = silu_f(gg[i]) * uu[i];
+        store_row_bf16<32>((bf*)g.out2 + (long long)m * g.ldo2 + f, act);
+      }
+      break;
+    }
+    case EPI_SWIGLU_BWD: {
+      const bf* gu = (const bf*)g.aux + (long long)m * g.ldaux;
+      bf* dgu = (bf*)g.out + (long long)m * g.ldo;
+      for (int c = 0; c < 4; ++c) {
+        float da[32], gg[32], uu[32], dg[32], du[32];
+        tmem_ld32(trow + c * 32, da);
+        const int n = ti.n0 + c * 32;
+        load_row_bf16<32>(gu + n, gg);
+        load_row_bf16<32>(gu + g.F + n, uu);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          dg[i] = da[i] * uu[i] * silu_grad_f(gg[i]);
+          du[i] = da[i] * silu_f(gg[i]);
+        }
+        store_row_bf16<32>(dgu + n, dg);
+        store_row_bf16<32>(dgu + g.F + n, du);
+      }
+      break;
+    }
+    case EPI_STORE_OP:
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(trow + c * 32, v);
+        store_row_bf16<32>((bf*)g.out + (long long)m * g.ldo + ti.n0 + c * 32, v);
+      }
+      break;
+    case EPI_STORE_F32:
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(trow + c * 32, v);
+        store_row_f32<32>((float*)g.out + (long long)m * g.ldo + ti.n0 + c * 32, v);
+      }
+      break;
+    case EPI_RESID:
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(trow + c * 32, v);
+        const float* r = (const float*)g.aux + (long long)m * g.ldaux + ti.n0 + c * 32;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 q = *reinterpret_cast<const float4*>(r + i);
+          v[i] += q.x; v[i + 1] += q.y; v[i + 2] += q.z; v[i + 3] += q.w;
+        }
+        store_row_f32<32>((float*)g.out + (long long)m * g.ldo + ti.n0 + c * 32, v);
+      }
+      break;
+    case EPI_GRAD: {
+      float* out = (float*)g.out;
+      int mm = m;
+      if (g.osplit > 0 && m >= g.osplit) { out = (float*)g.out1; mm = m - g.osplit; }
+      out += (long long)ti.seg * g.oseg + (long long)mm * g.ldo + ti.n0;
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(trow + c * 32, v);
+        float* p = out + c * 32;
+        if (g.accumulate) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 q = *reinterpret_cast<const float4*>(p + i);
+            v[i] += q.x; v[i + 1] += q.y; v[i + 2] += q.z; v[i + 3] += q.w;
+          }
+        }
+        store_row_f32<32>(p, v);
+      }
+      break;
+    }
+  }
+}
+
+// A weight-gradient tile whose expert received no rows: zero (or keep) the output.
+__device__ __forceinline__ void tc_epilogue_empty(const GemmDesc& g, const TcTile& ti, int m) {
+  if (g.epi != EPI_GRAD || g.accumulate) return;
+  float* out = (float*)g.out;
+  int mm = m;
+  if (g.osplit > 0 && m >= g.osplit) { out = (float*)g.out1; mm = m - g.osplit; }
+  out += (long long)ti.seg * g.oseg + (long long)mm * g.ldo + ti.n0;
+  for (int i = 0; i < TC_BN; i += 4) *reinterpret_cast<float4*>(out + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ---------------------------------------------------------------------------
+// the job
+// ---------------------------------------------------------------------------
+static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& g, Sched& s, char* smem, TcState& tc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t full = sbase, empty = sbase + 64, accf = sbase + 128, acce = sbase + 144;
+  const uint32_t ring = sbase + TC_RING_OFF;
+  ArenaHdr* hdr = reinterpret_cast<ArenaHdr*>(a.arena + a.aoff[A_HDR]);
+  const long long tmo = a.timeout_ns;
+  if (sbase & 1023u) {
+    // 128-byte swizzled tiles need 1024-byte aligned shared memory
+    if (threadIdx.x == 0) set_error(hdr, MT_ERR_DEVICE_BOUNDS, SITE_TC_ALIGN);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < TC_STAGES; ++i) {
+      mbar_init(full + 8 * i, 1);
+      mbar_init(empty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(accf + 8 * i, 1);
+      mbar_init(acce + 8 * i, 4);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  const int nt = g.N / TC_BN;
+  const int items = gemm_items(g, TC_BM, TC_BN);
+  const int first = s.first(), G = s.G;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // make the generic-proxy writes of earlier phases visible to TMA reads
+      asm volatile("fence.proxy.async;" ::: "memory");
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = first; t < items && ok; t += G) {
+        const TcTile ti = tc_tile(g, t, nt);
+        const int bseg = (g.rag == RAG_M) ? ti.seg * g.B.yseg : 0;
+        for (int kb = 0; kb < ti.nk; ++kb, ++it) {
+          const int st = it % TC_STAGES;
+          const uint32_t ph = (it / TC_STAGES) & 1;
+          if (!mbar_wait(empty + 8 * st, ph ^ 1, tmo)) {
+            set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_EMPTY);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full + 8 * st;
+          const uint32_t sa = ring + st * TC_STAGE_BYTES, sb = sa + 2 * TC_BOX_BYTES;
+          const int k0 = ti.kbeg + kb * TC_BK;
+          mbar_expect_tx(fb, TC_STAGE_BYTES);
+          tc_load_operand(a, g.A, ti.m0, k0, 0, sa, fb);
+          tc_load_operand(a, g.B, ti.n0, k0, bseg, sb, fb);
+        }
+      }
+      // drain: every issued stage must have landed before smem is reused
+      const uint32_t lo = it > TC_STAGES ? it - TC_STAGES : 0;
+      for (uint32_t j = lo; j < it; ++j)
+        if (!mbar_wait(full + 8 * (j % TC_STAGES), (j / TC_STAGES) & 1, tmo)) {
+          set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_DRAIN);
+          break;
+        }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(TC_BM, TC_BN, g.A.mn, g.B.mn);
+      const uint32_t a_lbo = g.A.mn ? TC_BOX_BYTES : 16, b_lbo = g.B.mn ? TC_BOX_BYTES : 16;
+      const uint32_t a_kstep = g.A.mn ? 16 * 128 : 32, b_kstep = g.B.mn ? 16 * 128 : 32;
+      uint32_t it = 0, tcount = 0;
+      bool ok = true;
+      uint32_t last_bar = 0, last_par = 0;
+      for (int t = first; t < items && ok; t += G) {
+        const TcTile ti = tc_tile(g, t, nt);
+        if (ti.nk == 0) continue;
+        const int ab = tcount & 1;
+        const uint32_t aph = (tcount >> 1) & 1;
+        if (!mbar_wait(acce + 8 * ab, aph ^ 1, tmo)) {
+          set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_ACC_EMPTY);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dt = tc.tmem_base + ab * TC_BN;
+        for (int kb = 0; kb < ti.nk; ++kb, ++it) {
+          const int st = it % TC_STAGES;
+          const uint32_t ph = (it / TC_STAGES) & 1;
+          if (!mbar_wait(full + 8 * st, ph, tmo)) {
+            set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_FULL);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = ring + st * TC_STAGE_BYTES, sb = sa + 2 * TC_BOX_BYTES;
+#pragma unroll
+          for (int j = 0; j < TC_BK / 16; ++j) {
+            const uint64_t ad = sdesc(sa + j * a_kstep, a_lbo, 1024);
+            const uint64_t bd = sdesc(sb + j * b_kstep, b_lbo, 1024);
+            mma_bf16(dt, ad, bd, idesc, (kb > 0 || j > 0) ? 1u : 0u);
+          }
+          mma_commit(empty + 8 * st);
+          last_bar = empty + 8 * st;
+          last_par = ph;
+        }
+        if (!ok) break;
+        mma_commit(accf + 8 * ab);
+        ++tcount;
+      }
+      // the tensor core must be idle before the job returns
+      if (last_bar && !mbar_wait(last_bar, last_par, tmo)) set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    const int q = warp - 4;
+    uint32_t tcount = 0;
+    for (int t = first; t < items; t += G) {
+      const TcTile ti = tc_tile(g, t, nt);
+      const int m = ti.m0 + q * 32 + lane;
+      if (ti.nk == 0) {
+        tc_epilogue_empty(g, ti, m);
+        continue;
+      }
+      const int ab = tcount & 1;
+      const uint32_t aph = (tcount >> 1) & 1;
+      if (!mbar_wait(accf + 8 * ab, aph, tmo)) {
+        set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_ACC_FULL);
+        break;
+      }
+      __syncwarp();
+      tc_fence_after();
+      const uint32_t trow = tc.tmem_base + ab * TC_BN + ((uint32_t)(q * 32) << 16);
+      tc_epilogue(g, ti, trow, m);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce + 8 * ab);
+      ++tcount;
+    }
+  }
+  __syncthreads();
+  s.next(items);
+}

@@ -57,7 +57,7 @@ bool tc_shapes_ok(const mt_hparams* hp) {
   const long long T = (long long)hp->batch * hp->seq;
   const int hq = hp->n_heads * hp->head_dim;
   return T % 128 == 0 && hp->d_model % 128 == 0 && hq % 128 == 0 && hp->vocab % 128 == 0 &&
-         hp->d_ff % 128 == 0;
+         hp->d_ff % 128 == 0 && hp->head_dim == 64;
 }
 
 void make_plan(const mt_hparams* hp, MtPlan* P) {
@@ -162,6 +162,32 @@ size_t smem_bytes(const MtDims& D, bool tc) {
   return need;
 }
 
+
+// Set the kernel's shared-memory limit (once per size and device) and return
+// the cooperative grid: one CTA per SM.
+int prepare_launch(bool bf16, size_t smem, int* grid) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MT_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& ds = g_dev[dev];
+  if (!ds.sms) {
+    if (cudaDeviceGetAttribute(&ds.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MT_ERR_CUDA;
+  }
+  int* bps = bf16 ? &ds.bps_bf16 : &ds.bps_f32;
+  size_t& prepared = bf16 ? ds.smem_bf16 : ds.smem_f32;
+  if (prepared != smem) {
+    cudaError_t e = bf16 ? mt_prepare_mega_bf16(smem, bps) : mt_prepare_mega_f32(smem, bps);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return MT_ERR_LAUNCH;
+    }
+    prepared = smem;
+  }
+  if (*bps < 1) return MT_ERR_LAUNCH;
+  *grid = ds.sms < kNch ? ds.sms : kNch;
+  return MT_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,30 +255,10 @@ int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m
   const bool want_tc = bf16 && !(hp->flags & MT_FLAG_SIMT_GEMM) && MT_TC_AVAILABLE;
   if (want_tc && !tc_shapes_ok(hp)) return MT_ERR_UNSUPPORTED;
 
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MT_ERR_CUDA;
-  const size_t smem = smem_bytes(P.D, want_tc);
   int grid = 0;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    DevState& ds = g_dev[dev];
-    if (!ds.sms) {
-      if (cudaDeviceGetAttribute(&ds.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MT_ERR_CUDA;
-    }
-    int* bps = bf16 ? &ds.bps_bf16 : &ds.bps_f32;
-    size_t& prepared = bf16 ? ds.smem_bf16 : ds.smem_f32;
-    if (prepared != smem) {
-      cudaError_t e = bf16 ? mt_prepare_mega_bf16(smem, bps) : mt_prepare_mega_f32(smem, bps);
-      if (e != cudaSuccess) {
-        cudaGetLastError();
-        return MT_ERR_LAUNCH;
-      }
-      prepared = smem;
-    }
-    if (*bps < 1) return MT_ERR_LAUNCH;
-    grid = ds.sms;   // one CTA per SM
-  }
-  if (grid > kNch) grid = kNch;
+  st = prepare_launch(bf16, smem_bytes(P.D, want_tc), &grid);
+  if (st) return st;
+  const size_t smem = smem_bytes(P.D, want_tc);
 
   KArgs* a = new KArgs();
   memset(a, 0, sizeof(KArgs));
@@ -343,6 +349,49 @@ int32_t mt_debug_view(const void* arena, const mt_hparams* hp, int32_t which, in
       *out = {base + P.aoff[A_LOGITS], T * D.V, 4}; break;
     default:
       return MT_ERR_ARG;
+  }
+  return MT_OK;
+}
+
+int32_t mt_debug_gemm(const void* A, int32_t a_mn, const void* B, int32_t b_mn, float* C, int32_t M, int32_t N,
+                      int32_t K, int32_t rag, const int32_t* offs, int32_t nseg, int32_t precision, int32_t use_tc,
+                      void* arena, int64_t arena_bytes, void* stream) {
+  if (!A || !B || !C || !arena || M <= 0 || N <= 0 || K <= 0) return MT_ERR_ARG;
+  if (arena_bytes < (int64_t)sizeof(ArenaHdr) || !aligned(arena, 256)) return MT_ERR_ARG;
+  if (precision != MT_PREC_FP32 && precision != MT_PREC_BF16) return MT_ERR_ARG;
+  if (rag < 0 || rag > 2 || (rag && (!offs || nseg <= 0))) return MT_ERR_ARG;
+  if (rag == 1 && a_mn) return MT_ERR_ARG;
+  if (rag == 2 && !(a_mn && b_mn)) return MT_ERR_ARG;
+  const bool bf16 = precision == MT_PREC_BF16;
+  const bool tc = bf16 && use_tc && MT_TC_AVAILABLE;
+  if (tc && (M % 128 || N % 128 || K % 64)) return MT_ERR_UNSUPPORTED;
+  if (tc && (!aligned(A, 16) || !aligned(B, 16))) return MT_ERR_ARG;
+  const size_t smem = tc ? (size_t)MT_TC_SMEM : (size_t)SG_BM * SG_CPAD * 4;
+  int grid = 0;
+  int st = prepare_launch(bf16, smem, &grid);
+  if (st) return st;
+  KArgs* a = new KArgs();
+  memset(a, 0, sizeof(KArgs));
+  a->arena = (char*)arena;
+  a->timeout_ns = 4000000000LL;
+  a->debug_gemm = 1;
+  a->dbg_a = A; a->dbg_b = B; a->dbg_c = C;
+  a->dbg_m = M; a->dbg_n = N; a->dbg_k = K; a->dbg_a_mn = a_mn; a->dbg_b_mn = b_mn;
+  a->dbg_rag = rag; a->dbg_nseg = rag ? nseg : 0; a->dbg_offs = offs;
+  a->use_tc = tc ? 1 : 0;
+  if (tc) {
+    const long long segs = rag == 1 ? nseg : 1;
+    const long long ar = a_mn ? K : M, ac = a_mn ? M : K;
+    const long long br = (b_mn ? K : N) * segs, bc = b_mn ? N : K;
+    int ms = mt_build_debug_maps(a, A, ar, ac, B, br, bc);
+    if (ms != MT_OK) { delete a; return ms; }
+  }
+  cudaError_t e = bf16 ? mt_launch_mega_bf16(*a, grid, smem, (cudaStream_t)stream)
+                       : mt_launch_mega_f32(*a, grid, smem, (cudaStream_t)stream);
+  delete a;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MT_ERR_LAUNCH;
   }
   return MT_OK;
 }

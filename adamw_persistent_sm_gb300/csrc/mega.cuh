@@ -908,27 +908,25 @@ __device__ __forceinline__ void run_attn_bwd(const KArgs& a, int l, Sched& s, ch
 // ===========================================================================
 // the program
 // ===========================================================================
+// One microbatch: forward, loss, backward, and on the last microbatch the
+// optimizer.  Returns early (every CTA) when a grid barrier reports an error.
 template <class OP>
-__global__ void __launch_bounds__(MT_THREADS, 1) mt_megakernel(const __grid_constant__ KArgs a) {
-  extern __shared__ __align__(1024) char smem[];
+__device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   const MtDims& D = a.D;
   ArenaHdr* hdr = abuf<ArenaHdr>(a, A_HDR);
   const unsigned G = gridDim.x;
   const bool trace = (a.flags & MT_FLAG_TRACE) != 0;
   long long* tr = trace ? abuf<long long>(a, A_TRACE) + (long long)blockIdx.x * MT_MAX_PHASES * 2 : nullptr;
   int phase = 0;
-  Sched s{(int)blockIdx.x, (int)G, 0};
-  TcState tc;
-  tc_setup<OP>(a, smem, tc);
   Gemms<OP> gm(a);
-  bool stall = (a.flags & MT_FLAG_TEST_STALL) && blockIdx.x == 0;
+  const bool stall = (a.flags & MT_FLAG_TEST_STALL) && blockIdx.x == 0;
 
-#define MT_SYNC()                                                                          \
-  do {                                                                                     \
+#define MT_SYNC()                                                                                      \
+  do {                                                                                                 \
     if (!grid_barrier(hdr, G, a.timeout_ns, (tr && phase < MT_MAX_PHASES) ? tr + 2 * phase : nullptr, \
-                      stall))                                                              \
-      goto done;                                                                           \
-    ++phase;                                                                               \
+                      stall))                                                                          \
+      return;                                                                                          \
+    ++phase;                                                                                           \
   } while (0)
 
   // ---------------- forward ----------------
@@ -1031,6 +1029,41 @@ __global__ void __launch_bounds__(MT_THREADS, 1) mt_megakernel(const __grid_cons
     hdr->n_phases = phase;
   }
 #undef MT_SYNC
-done:
+}
+
+// Test harness: one product C = A B^T (fp32 out) described by the debug
+// fields of the arguments; A in map MAP_R, B in map MAP_WQKV.
+template <class OP>
+__device__ void run_debug_gemm(const KArgs& a, char* smem, TcState& tc, Sched& s) {
+  GemmDesc g;
+  g.M = a.dbg_m; g.N = a.dbg_n; g.K = a.dbg_k; g.rag = a.dbg_rag; g.offs = a.dbg_offs; g.nseg = a.dbg_nseg;
+  g.epi = (g.rag == RAG_K) ? EPI_GRAD : EPI_STORE_F32;
+  g.out = a.dbg_c; g.out1 = nullptr; g.out2 = nullptr; g.ldo = g.N; g.ldo2 = 0; g.osplit = 0;
+  g.oseg = (long long)g.M * g.N; g.aux = nullptr; g.ldaux = 0; g.accumulate = 0;
+  g.F = 0; g.S = 1; g.hd = 64; g.hq = 0; g.rope = nullptr;
+  GOperand A, B;
+  A.p0 = a.dbg_a; A.p1 = nullptr; A.mn = a.dbg_a_mn; A.ld = A.mn ? g.M : g.K; A.seg = 0; A.two = 0;
+  A.split = 0; A.map0 = MAP_R; A.map1 = -1; A.y0 = 0; A.yseg = 0;
+  B.p0 = a.dbg_b; B.p1 = nullptr; B.mn = a.dbg_b_mn; B.ld = B.mn ? g.N : g.K;
+  B.seg = (long long)g.N * g.K; B.two = 0; B.split = 0; B.map0 = MAP_WQKV; B.map1 = -1; B.y0 = 0;
+  B.yseg = B.mn ? g.K : g.N;
+  g.A = A;
+  g.B = B;
+  run_gemm<OP>(a, g, s, smem, tc);
+  ArenaHdr* hdr = abuf<ArenaHdr>(a, A_HDR);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    hdr->n_ctas = (int)gridDim.x;
+    hdr->n_phases = 0;
+  }
+}
+
+template <class OP>
+__global__ void __launch_bounds__(MT_THREADS, 1) mt_megakernel(const __grid_constant__ KArgs a) {
+  extern __shared__ __align__(1024) char smem[];
+  Sched s{(int)blockIdx.x, (int)gridDim.x, 0};
+  TcState tc;
+  tc_setup<OP>(a, smem, tc);
+  if (a.debug_gemm) run_debug_gemm<OP>(a, smem, tc, s);
+  else run_update<OP>(a, smem, tc, s);
   tc_teardown<OP>(a, smem, tc);
 }

@@ -111,6 +111,10 @@ struct KArgs {
   char* arena;
   long long poff[P_COUNT];      // element offsets of each tensor in the flat buffers
   long long aoff[A_COUNT];      // byte offsets of each arena buffer
+  int debug_gemm;               // test harness: run only the product described below
+  const void* dbg_a; const void* dbg_b; float* dbg_c;
+  int dbg_m, dbg_n, dbg_k, dbg_a_mn, dbg_b_mn, dbg_rag, dbg_nseg;
+  const int* dbg_offs;
   int use_tc;                   // tcgen05 GEMMs (bf16 only)
   int use_tc_attn;              // tensor-core attention (bf16 only)
   CUtensorMap maps[MT_NMAPS];

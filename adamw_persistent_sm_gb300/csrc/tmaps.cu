@@ -48,8 +48,6 @@ int mt_build_tensor_maps(KArgs* a, void* shadow) {
   const MtDims& D = a->D;
   const long long L = D.L, T = D.T, d = D.d, hq = D.hq, E = D.E, F = D.F, V = D.V, Pm = D.Pmax;
   char* ar = a->arena;
-  const __nv_bfloat16_raw* sh = (const __nv_bfloat16_raw*)shadow;
-  (void)sh;
   const char* w = (const char*)shadow;
   auto P = [&](int pid) { return (const void*)(w + a->poff[pid] * 2); };
   auto A = [&](int id) { return (const void*)(ar + a->aoff[id]); };
@@ -70,5 +68,14 @@ int mt_build_tensor_maps(KArgs* a, void* shadow) {
   ok &= encode(&a->maps[MAP_DGU], A(A_DGU), Pm, 2 * F);
   ok &= encode(&a->maps[MAP_DXO], A(A_DXO), T, d);
   ok &= encode(&a->maps[MAP_DQKV], A(A_DQKV), T, 3 * hq);
+  return ok ? MT_OK : MT_ERR_ARG;
+}
+
+int mt_build_debug_maps(KArgs* a, const void* A, long long a_rows, long long a_cols, const void* B,
+                        long long b_rows, long long b_cols) {
+  std::call_once(g_once, resolve);
+  if (!g_encode) return MT_ERR_CUDA;
+  bool ok = encode(&a->maps[MAP_R], A, a_rows, a_cols);
+  ok &= encode(&a->maps[MAP_WQKV], B, b_rows, b_cols);
   return ok ? MT_OK : MT_ERR_ARG;
 }

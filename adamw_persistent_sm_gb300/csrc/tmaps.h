@@ -5,3 +5,7 @@
 // Fill a->maps[] for every MapId; `shadow` is the bf16 parameter copy.
 // Returns an mt_status.
 int mt_build_tensor_maps(KArgs* a, void* shadow);
+
+// Maps of the single-product test harness: A in MAP_R, B in MAP_WQKV.
+int mt_build_debug_maps(KArgs* a, const void* A, long long a_rows, long long a_cols, const void* B,
+                        long long b_rows, long long b_cols);

@@ -345,7 +345,10 @@ def forward_backward(P: dict, tokens: np.ndarray, D: Dims, coef: float, grads: d
     tok_loss = np.where(has_target, coef * (lse - logits[np.arange(T), target]), 0.0)
     loss = float(np.sum(tok_loss))
     if not backward:
-        return loss, tok_loss, dict(lse=lse, logits=logits, rf=rf)
+        dbg = dict(lse=lse, logits=logits, rf=rf)
+        if keep_cache:
+            dbg["caches"] = caches
+        return loss, tok_loss, dbg
     dlogits = np.exp(logits - lse[:, None])
     dlogits[np.arange(T), target] -= 1.0
     dlogits *= np.where(has_target, coef, 0.0)[:, None]
