@@ -20,7 +20,9 @@ enum EpiKind {
   EPI_ROPE,           // out(op) = acc with rotary embedding on the q and k columns
   EPI_SWIGLU,         // tile = [64 gate | 64 up] columns -> g, u (out) and silu(g)*u (out2)
   EPI_SWIGLU_BWD,     // acc = d(silu(g)*u); aux = [g | u] -> out = [dg | du]
-  EPI_GRAD            // out(f32) = acc (+ out if accumulate); rows >= osplit go to out1
+  EPI_GRAD,           // out(f32) = acc (+ out if accumulate); rows >= osplit go to out1
+  EPI_STORE_OP_D      // out(op) = acc, and out2(f32)[m][head] = sum over the head's 64 columns of
+                      // op(acc) * aux(op)  (attention's D = rowsum(dO * O))
 };
 
 enum RagKind { RAG_NONE = 0, RAG_M = 1, RAG_K = 2 };
@@ -174,6 +176,29 @@ __device__ void gemm_simt_tile(const GemmDesc& g, int seg, int m0, int n0, int k
     }
   __syncthreads();
   const int warp = tid >> 5, lane = tid & 31;
+  if (g.epi == EPI_STORE_OP_D) {
+    // 64-column heads: lane owns columns lane, lane+32 of each head
+    for (int r = warp; r < SG_BM; r += MT_WARPS) {
+      const int m = m0 + r;
+      if (m >= mmax) continue;
+      const float* crow = Cs + r * SG_CPAD;
+      for (int hh = 0; hh < SG_BN / 64; ++hh) {
+        float dot = 0.f;
+        for (int c = hh * 64 + lane; c < hh * 64 + 64; c += 32) {
+          const int n = n0 + c;
+          if (n >= g.N) continue;
+          const OP q = from_f<OP>(crow[c]);
+          ((OP*)g.out)[(long long)m * g.ldo + n] = q;
+          dot = fmaf(to_f(q), to_f(((const OP*)g.aux)[(long long)m * g.ldaux + n]), dot);
+        }
+        dot = warp_sum(dot);
+        const int n = n0 + hh * 64;
+        if (lane == 0 && n < g.N) ((float*)g.out2)[(long long)m * g.ldo2 + n / 64] = dot;
+      }
+    }
+    __syncthreads();
+    return;
+  }
   for (int r = warp; r < SG_BM; r += MT_WARPS) {
     const int m = m0 + r;
     if (m >= mmax) continue;

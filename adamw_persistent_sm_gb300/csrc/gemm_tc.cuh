@@ -322,6 +322,22 @@ static __device__ __noinline__ void tc_epilogue(const GemmDesc& g, const TcTile&
         store_row_bf16<32>((bf*)g.out + (long long)m * g.ldo + ti.n0 + c * 32, v);
       }
       break;
+    case EPI_STORE_OP_D: {
+      // two 64-column heads per tile
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float x[64], o[64];
+        tmem_ld32(trow + h2 * 64, x);
+        tmem_ld32(trow + h2 * 64 + 32, x + 32);
+        const int n = ti.n0 + h2 * 64;
+        store_row_bf16<64>((bf*)g.out + (long long)m * g.ldo + n, x);
+        load_row_bf16<64>((const bf*)g.aux + (long long)m * g.ldaux + n, o);
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) dot = fmaf(__bfloat162float(__float2bfloat16_rn(x[i])), o[i], dot);
+        ((float*)g.out2)[(long long)m * g.ldo2 + n / 64] = dot;
+      }
+      break;
+    }
     case EPI_STORE_F32:
       for (int c = 0; c < 4; ++c) {
         float v[32];

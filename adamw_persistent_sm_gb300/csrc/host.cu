@@ -46,6 +46,7 @@ int check_hparams(const mt_hparams* hp) {
   if (hp->d_model % 32 != 0 || hp->d_model > 2048) return MT_ERR_UNSUPPORTED;
   if (hp->d_ff % 64 != 0) return MT_ERR_UNSUPPORTED;
   if (hp->seq < 2) return MT_ERR_UNSUPPORTED;
+  if (hp->vocab % 4 != 0) return MT_ERR_UNSUPPORTED;
   const long long T = (long long)hp->batch * hp->seq;
   if (T * hp->top_k + (long long)hp->n_experts * MT_TILE_M > (1LL << 30)) return MT_ERR_UNSUPPORTED;
   if ((long long)hp->vocab * T > (1LL << 40)) return MT_ERR_UNSUPPORTED;
@@ -105,6 +106,7 @@ void make_plan(const mt_hparams* hp, MtPlan* P) {
   sz[A_DXS] = Pm * d * 4;
   sz[A_DR2] = T * d * 4;
   sz[A_DO] = T * D.hq * ob;
+  sz[A_DSUM] = T * D.H * 4;
   sz[A_DQKV] = T * 3 * D.hq * ob;
   sz[A_DR] = T * d * 4;
   sz[A_DRF] = T * d * 4;
@@ -282,7 +284,7 @@ int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m
   memcpy(a->poff, P.poff, sizeof(a->poff));
   memcpy(a->aoff, P.aoff, sizeof(a->aoff));
   a->use_tc = want_tc ? 1 : 0;
-  a->use_tc_attn = bf16 && !(hp->flags & MT_FLAG_SIMT_ATTN);
+  a->use_tc_attn = bf16 && !(hp->flags & MT_FLAG_SIMT_ATTN) && hp->head_dim == 64 && hp->seq % 128 == 0;
   if (want_tc) {
     int ms = mt_build_tensor_maps(a, shadow);
     if (ms != MT_OK) { delete a; return ms; }

@@ -16,6 +16,9 @@
 #include "gemm.cuh"
 #include "attn_simt.cuh"
 #include "gemm_tc.cuh"
+#include "attn_tc.cuh"
+#include "rows.cuh"
+#include <type_traits>
 
 template <class T>
 __device__ __forceinline__ T* abuf(const KArgs& a, int id) {
@@ -59,27 +62,30 @@ __device__ void job_embed(const KArgs& a, Sched& s) {
     rope[2 * e] = (float)cv;
     rope[2 * e + 1] = (float)sv;
   }
-  const int lane = threadIdx.x & 31;
   ArenaHdr* hdr = abuf<ArenaHdr>(a, A_HDR);
   const float* emb = pmaster(a, P_EMB);
-  const float* g = pmaster(a, P_ATTN_NORM);
   float* X = abuf<float>(a, A_X);
   OP* R = abuf<OP>(a, A_R);
   float* inv1 = abuf<float>(a, A_INV1);
-  const int nw = s.G * MT_WARPS;
-  for (int t = me * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
-    int v = a.tokens[t];
-    if (v < 0 || v >= D.V) {
-      if (lane == 0) set_error(hdr, MT_ERR_DEVICE_BOUNDS, SITE_TOKEN_RANGE);
-      v = 0;
+  const int n4 = D.d / 4, nw = s.G * MT_WARPS, lane = threadIdx.x & 31;
+  with_nc(D.d, [&](auto NCc) {
+    constexpr int NC = decltype(NCc)::value;
+    Row<NC> g, x, r;
+    row_ld(g, pmaster(a, P_ATTN_NORM), n4);
+    for (int t = me * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
+      int v = a.tokens[t];
+      if (v < 0 || v >= D.V) {
+        if (lane == 0) set_error(hdr, MT_ERR_DEVICE_BOUNDS, SITE_TOKEN_RANGE);
+        v = 0;
+      }
+      row_ld(x, emb + (long long)v * D.d, n4);
+      row_st(X + (long long)t * D.d, x, n4);
+      const float inv = row_rms_inv(x, D.d, a.norm_eps);
+      row_norm_apply(r, x, inv, g);
+      row_st_op(R + (long long)t * D.d, r, n4);
+      if (lane == 0) inv1[t] = inv;
     }
-    float* x = X + (long long)t * D.d;
-    const float* er = emb + (long long)v * D.d;
-    for (int i = lane; i < D.d; i += 32) x[i] = er[i];
-    const float inv = warp_rms_inv(x, D.d, a.norm_eps);
-    for (int i = lane; i < D.d; i += 32) R[(long long)t * D.d + i] = from_f<OP>(x[i] * inv * g[i]);
-    if (lane == 0) inv1[t] = inv;
-  }
+  });
   s.next(s.G);
 }
 
@@ -113,27 +119,25 @@ __device__ void job_router(const KArgs& a, int l, float* sm) {
   float* WGT = abuf<float>(a, A_WGT) + (long long)l * D.T * D.K;
   const float* g = pmaster(a, P_MOE_NORM) + (long long)l * D.d;
   const float* Wr = pmaster(a, P_ROUTER) + (long long)l * D.E * D.d;
-  float* row = sm + warp * D.d;
+  (void)sm;
+  const int n4 = D.d / 4;
+  with_nc(D.d, [&](auto NCc) {
+  constexpr int NC = decltype(NCc)::value;
+  Row<NC> gr, x, r, w;
+  row_ld(gr, g, n4);
   for (int t = t0 + warp; t < t1; t += MT_WARPS) {
-    const float* x = XM + (long long)t * D.d;
-    const float inv = warp_rms_inv(x, D.d, a.norm_eps);
-    for (int i = lane; i < D.d; i += 32) {
-      const float r = x[i] * inv * g[i];
-      row[i] = r;
-      R2[(long long)t * D.d + i] = from_f<OP>(r);
-    }
-    __syncwarp();
+    row_ld(x, XM + (long long)t * D.d, n4);
+    const float inv = row_rms_inv(x, D.d, a.norm_eps);
+    row_norm_apply(r, x, inv, gr);
+    row_st_op(R2 + (long long)t * D.d, r, n4);
     if (lane == 0) inv2[t] = inv;
     float z0 = -INFINITY, z1 = -INFINITY;   // experts lane and lane + 32
     for (int e = 0; e < D.E; ++e) {
-      const float* w = Wr + (long long)e * D.d;
-      float acc = 0.f;
-      for (int i = lane; i < D.d; i += 32) acc = fmaf(row[i], w[i], acc);
-      acc = warp_sum(acc);
+      row_ld(w, Wr + (long long)e * D.d, n4);
+      const float acc = row_dot(r, w);
       if (e == lane) z0 = acc;
       if (e == lane + 32) z1 = acc;
     }
-    __syncwarp();
     if (lane < D.E) Z[(long long)t * D.E + lane] = z0;
     if (lane + 32 < D.E) Z[(long long)t * D.E + lane + 32] = z1;
     const float zmax = warp_max(fmaxf(z0, z1));
@@ -163,6 +167,7 @@ __device__ void job_router(const KArgs& a, int l, float* sm) {
       }
     }
   }
+  });
   __syncthreads();
   if (t0 < D.T) {
     int* CNT = abuf<int>(a, A_CNT) + ((long long)l * D.nch + c) * D.E;
@@ -267,32 +272,37 @@ __device__ void job_route(const KArgs& a, int l, int* ism) {
 template <class OP>
 __device__ void job_combine(const KArgs& a, int l, Sched& s) {
   const MtDims& D = a.D;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, n4 = D.d / 4;
   const float* XM = abuf<float>(a, A_XM) + (long long)l * D.T * D.d;
   const float* Y = abuf<float>(a, A_Y) + (long long)l * D.Pmax * D.d;
   const float* WGT = abuf<float>(a, A_WGT) + (long long)l * D.T * D.K;
   const int* INVM = abuf<int>(a, A_INVM) + (long long)l * D.T * D.K;
   float* Xn = abuf<float>(a, A_X) + (long long)(l + 1) * D.T * D.d;
   const bool last = (l + 1 == D.L);
-  const float* g = last ? pmaster(a, P_FINAL_NORM) : pmaster(a, P_ATTN_NORM) + (long long)(l + 1) * D.d;
+  const float* gp = last ? pmaster(a, P_FINAL_NORM) : pmaster(a, P_ATTN_NORM) + (long long)(l + 1) * D.d;
   OP* Rn = last ? abuf<OP>(a, A_RF) : abuf<OP>(a, A_R) + (long long)(l + 1) * D.T * D.d;
   float* invn = last ? abuf<float>(a, A_INVF) : abuf<float>(a, A_INV1) + (long long)(l + 1) * D.T;
   const int nw = s.G * MT_WARPS;
-  for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
-    float* x = Xn + (long long)t * D.d;
-    const float* xm = XM + (long long)t * D.d;
-    for (int i = lane; i < D.d; i += 32) {
-      float acc = 0.f;
+  with_nc(D.d, [&](auto NCc) {
+    constexpr int NC = decltype(NCc)::value;
+    Row<NC> g, x, acc, y, r;
+    row_ld(g, gp, n4);
+    for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
+      row_ld(x, XM + (long long)t * D.d, n4);
+      row_scale(acc, x, 0.f);
       for (int k = 0; k < D.K; ++k) {
         const int p = INVM[(long long)t * D.K + k];
-        acc = fmaf(WGT[(long long)t * D.K + k], Y[(long long)p * D.d + i], acc);
+        row_ld(y, Y + (long long)p * D.d, n4);
+        row_axpy(acc, y, WGT[(long long)t * D.K + k]);
       }
-      x[i] = xm[i] + acc;
+      row_add(x, acc);
+      row_st(Xn + (long long)t * D.d, x, n4);
+      const float inv = row_rms_inv(x, D.d, a.norm_eps);
+      row_norm_apply(r, x, inv, g);
+      row_st_op(Rn + (long long)t * D.d, r, n4);
+      if (lane == 0) invn[t] = inv;
     }
-    const float inv = warp_rms_inv(x, D.d, a.norm_eps);
-    for (int i = lane; i < D.d; i += 32) Rn[(long long)t * D.d + i] = from_f<OP>(x[i] * inv * g[i]);
-    if (lane == 0) invn[t] = inv;
-  }
+  });
   s.next(s.G);
 }
 
@@ -300,6 +310,15 @@ __device__ void job_combine(const KArgs& a, int l, Sched& s) {
 // vocabulary, loss = coef * (lse - logit[target]) and
 // dlogits = coef * (softmax - onehot).  Position s predicts token s+1; the
 // last position of a sequence has no target (zero loss and gradient).
+// One warp per position; float4 loads, eight in flight per lane.
+__device__ __forceinline__ void ce_store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void ce_store4(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
 template <class OP>
 __device__ void job_ce(const KArgs& a, Sched& s) {
   const MtDims& D = a.D;
@@ -308,32 +327,67 @@ __device__ void job_ce(const KArgs& a, Sched& s) {
   OP* DL = abuf<OP>(a, A_DLOGITS);
   float* TL = abuf<float>(a, A_TOKLOSS);
   const int nw = s.G * MT_WARPS;
+  const int v4 = D.V / 4;                 // V % 4 == 0 (checked on the host)
+  constexpr int U = 8;
   for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
-    const float* lg = LOG + (long long)t * D.V;
+    const float4* lg = reinterpret_cast<const float4*>(LOG + (long long)t * D.V);
     OP* dl = DL + (long long)t * D.V;
     const bool has = (t % D.S) != D.S - 1;
     if (!has) {
-      for (int j = lane; j < D.V; j += 32) dl[j] = from_f<OP>(0.f);
+      for (int j = lane; j < v4; j += 32) ce_store4(dl + 4 * j, make_float4(0.f, 0.f, 0.f, 0.f));
       if (lane == 0) TL[t] = 0.f;
       continue;
     }
     int target = a.tokens[t + 1];
     if (target < 0 || target >= D.V) target = 0;   // reported by job_embed; never read outside the row
     float m = -INFINITY, sum = 0.f;
-    for (int j = lane; j < D.V; j += 32) {
-      const float v = lg[j];
-      if (v > m) { sum = sum * expf(m - v) + 1.f; m = v; }
-      else sum += expf(v - m);
+    for (int j0 = 0; j0 < v4; j0 += 32 * U) {
+      float4 q[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + lane + 32 * u;
+        q[u] = (j < v4) ? lg[j] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+      float bm = m;
+#pragma unroll
+      for (int u = 0; u < U; ++u) bm = fmaxf(bm, fmaxf(fmaxf(q[u].x, q[u].y), fmaxf(q[u].z, q[u].w)));
+      if (bm == -INFINITY) continue;
+      float bs = 0.f;
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        bs += __expf(q[u].x - bm) + __expf(q[u].y - bm) + __expf(q[u].z - bm) + __expf(q[u].w - bm);
+      sum = sum * __expf(m - bm) + bs;
+      m = bm;
     }
     const float M = warp_max(m);
-    sum = (m == -INFINITY) ? 0.f : sum * expf(m - M);
+    sum = (m == -INFINITY) ? 0.f : sum * __expf(m - M);
     sum = warp_sum(sum);
     const float lse = M + logf(sum);
-    for (int j = lane; j < D.V; j += 32) {
-      const float p = expf(lg[j] - lse);
-      dl[j] = from_f<OP>(a.coef * (p - (j == target ? 1.f : 0.f)));
+    for (int j0 = 0; j0 < v4; j0 += 32 * U) {
+      float4 q[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + lane + 32 * u;
+        if (j < v4) q[u] = lg[j];
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + lane + 32 * u;
+        if (j < v4) {
+          float4 p = make_float4(a.coef * __expf(q[u].x - lse), a.coef * __expf(q[u].y - lse),
+                                 a.coef * __expf(q[u].z - lse), a.coef * __expf(q[u].w - lse));
+          if ((target >> 2) == j) {
+            const int c = target & 3;
+            if (c == 0) p.x -= a.coef;
+            else if (c == 1) p.y -= a.coef;
+            else if (c == 2) p.z -= a.coef;
+            else p.w -= a.coef;
+          }
+          ce_store4(dl + 4 * j, p);
+        }
+      }
     }
-    if (lane == 0) TL[t] = a.coef * (lse - lg[target]);
+    if (lane == 0) TL[t] = a.coef * (lse - LOG[(long long)t * D.V + target]);
   }
   s.next(s.G);
 }
@@ -341,20 +395,6 @@ __device__ void job_ce(const KArgs& a, Sched& s) {
 // ===========================================================================
 // backward row jobs
 // ===========================================================================
-// RMSNorm backward of one row: dx = inv * (a - xh * mean(a * xh)), a = dy*g.
-// Adds into out (or overwrites when add == false).
-__device__ __forceinline__ void warp_rmsnorm_bwd(const float* dy, const float* x, float inv,
-                                                 const float* g, int d, float* out, bool add) {
-  const int lane = threadIdx.x & 31;
-  float dot = 0.f;
-  for (int i = lane; i < d; i += 32) dot = fmaf(dy[i] * g[i], x[i] * inv, dot);
-  dot = warp_sum(dot) / (float)d;
-  for (int i = lane; i < d; i += 32) {
-    const float v = inv * (dy[i] * g[i] - x[i] * inv * dot);
-    out[i] = add ? out[i] + v : v;
-  }
-}
-
 // dx = d(final RMSNorm) from d rf.
 template <class OP>
 __device__ void job_final_norm_bwd(const KArgs& a, Sched& s) {
@@ -362,12 +402,19 @@ __device__ void job_final_norm_bwd(const KArgs& a, Sched& s) {
   const float* DRF = abuf<float>(a, A_DRF);
   const float* X = abuf<float>(a, A_X) + (long long)D.L * D.T * D.d;
   const float* inv = abuf<float>(a, A_INVF);
-  const float* g = pmaster(a, P_FINAL_NORM);
   float* DX = abuf<float>(a, A_DX);
-  const int nw = s.G * MT_WARPS;
-  for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw)
-    warp_rmsnorm_bwd(DRF + (long long)t * D.d, X + (long long)t * D.d, inv[t], g, D.d,
-                     DX + (long long)t * D.d, false);
+  const int n4 = D.d / 4, nw = s.G * MT_WARPS;
+  with_nc(D.d, [&](auto NCc) {
+    constexpr int NC = decltype(NCc)::value;
+    Row<NC> g, dy, x, dx;
+    row_ld(g, pmaster(a, P_FINAL_NORM), n4);
+    for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
+      row_ld(dy, DRF + (long long)t * D.d, n4);
+      row_ld(x, X + (long long)t * D.d, n4);
+      row_norm_bwd(dx, dy, x, inv[t], g, D.d);
+      row_st(DX + (long long)t * D.d, dx, n4);
+    }
+  });
   s.next(s.G);
 }
 
@@ -378,7 +425,7 @@ __device__ void job_final_norm_bwd(const KArgs& a, Sched& s) {
 template <class OP>
 __device__ void job_moe_bwd1(const KArgs& a, int l, Sched& s) {
   const MtDims& D = a.D;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, n4 = D.d / 4;
   const float* DX = abuf<float>(a, A_DX);
   const float* Y = abuf<float>(a, A_Y) + (long long)l * D.Pmax * D.d;
   const float* WGT = abuf<float>(a, A_WGT) + (long long)l * D.T * D.K;
@@ -390,37 +437,36 @@ __device__ void job_moe_bwd1(const KArgs& a, int l, Sched& s) {
   float* DZ = abuf<float>(a, A_DZ);
   const int nw = s.G * MT_WARPS;
   const int me = s.first() * MT_WARPS + (threadIdx.x >> 5);
-  for (int t = me; t < D.T; t += nw) {
-    const float* dx = DX + (long long)t * D.d;
-    float dw[8], w[8];
-    for (int k = 0; k < D.K; ++k) {
-      const int p = INVM[(long long)t * D.K + k];
-      w[k] = WGT[(long long)t * D.K + k];
-      const float* y = Y + (long long)p * D.d;
-      OP* dy = DY + (long long)p * D.d;
-      float acc = 0.f;
-      for (int i = lane; i < D.d; i += 32) {
-        acc = fmaf(dx[i], y[i], acc);
-        dy[i] = from_f<OP>(w[k] * dx[i]);
+  with_nc(D.d, [&](auto NCc) {
+    constexpr int NC = decltype(NCc)::value;
+    Row<NC> dx, y, dy;
+    for (int t = me; t < D.T; t += nw) {
+      row_ld(dx, DX + (long long)t * D.d, n4);
+      float dw[8], w[8];
+      for (int k = 0; k < D.K; ++k) {
+        const int p = INVM[(long long)t * D.K + k];
+        w[k] = WGT[(long long)t * D.K + k];
+        row_ld(y, Y + (long long)p * D.d, n4);
+        dw[k] = row_dot(dx, y);
+        row_scale(dy, dx, w[k]);
+        row_st_op(DY + (long long)p * D.d, dy, n4);
       }
-      dw[k] = warp_sum(acc);
+      float mean = 0.f;
+      for (int k = 0; k < D.K; ++k) mean = fmaf(w[k], dw[k], mean);
+      for (int e = lane; e < D.E; e += 32) {
+        float v = 0.f;
+        for (int k = 0; k < D.K; ++k)
+          if (IDX[(long long)t * D.K + k] == e) v = w[k] * (dw[k] - mean);
+        DZ[(long long)t * D.E + e] = v;
+      }
     }
-    float mean = 0.f;
-    for (int k = 0; k < D.K; ++k) mean = fmaf(w[k], dw[k], mean);
-    for (int e = lane; e < D.E; e += 32) {
-      float v = 0.f;
-      for (int k = 0; k < D.K; ++k)
-        if (IDX[(long long)t * D.K + k] == e) v = w[k] * (dw[k] - mean);
-      DZ[(long long)t * D.E + e] = v;
-    }
-  }
-  // pad rows of dY: PERM == -1 inside [0, OFFS[E])
-  const int nrows = OFFS[D.E];
-  for (int p = me; p < nrows; p += nw) {
-    if (PERM[p] >= 0) continue;
-    OP* dy = DY + (long long)p * D.d;
-    for (int i = lane; i < D.d; i += 32) dy[i] = from_f<OP>(0.f);
-  }
+    // pad rows of dY: PERM == -1 inside [0, OFFS[E])
+#pragma unroll
+    for (int i = 0; i < NC; ++i) dy.v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int nrows = OFFS[D.E];
+    for (int p = me; p < nrows; p += nw)
+      if (PERM[p] < 0) row_st_op(DY + (long long)p * D.d, dy, n4);
+  });
   s.next(s.G);
 }
 
@@ -431,34 +477,44 @@ __device__ void job_moe_bwd1(const KArgs& a, int l, Sched& s) {
 template <class OP>
 __device__ void job_moe_bwd2(const KArgs& a, int l, Sched& s) {
   const MtDims& D = a.D;
-  const int lane = threadIdx.x & 31;
+  const int n4 = D.d / 4;
   const float* DXS = abuf<float>(a, A_DXS);
   const float* DZ = abuf<float>(a, A_DZ);
   const int* INVM = abuf<int>(a, A_INVM) + (long long)l * D.T * D.K;
   const float* Wr = pmaster(a, P_ROUTER) + (long long)l * D.E * D.d;
   const float* XM = abuf<float>(a, A_XM) + (long long)l * D.T * D.d;
   const float* inv2 = abuf<float>(a, A_INV2) + (long long)l * D.T;
-  const float* g = pmaster(a, P_MOE_NORM) + (long long)l * D.d;
   float* DR2 = abuf<float>(a, A_DR2);
   float* DX = abuf<float>(a, A_DX);
   OP* DXO = abuf<OP>(a, A_DXO);
   const int nw = s.G * MT_WARPS;
-  for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
-    float* dr2 = DR2 + (long long)t * D.d;
-    const float* dz = DZ + (long long)t * D.E;
-    for (int i = lane; i < D.d; i += 32) {
-      float acc = 0.f;
-      for (int k = 0; k < D.K; ++k) acc += DXS[(long long)INVM[(long long)t * D.K + k] * D.d + i];
-      float rz = 0.f;
-      for (int e = 0; e < D.E; ++e) rz = fmaf(dz[e], Wr[(long long)e * D.d + i], rz);
-      dr2[i] = acc + rz;
+  with_nc(D.d, [&](auto NCc) {
+    constexpr int NC = decltype(NCc)::value;
+    Row<NC> g, dr2, tmp, x, dx, dxm;
+    row_ld(g, pmaster(a, P_MOE_NORM) + (long long)l * D.d, n4);
+    for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
+      row_scale(dr2, g, 0.f);
+      for (int k = 0; k < D.K; ++k) {
+        row_ld(tmp, DXS + (long long)INVM[(long long)t * D.K + k] * D.d, n4);
+        row_add(dr2, tmp);
+      }
+      const float* dz = DZ + (long long)t * D.E;
+      for (int e = 0; e < D.E; ++e) {
+        const float ze = dz[e];
+        if (ze != 0.f) {
+          row_ld(tmp, Wr + (long long)e * D.d, n4);
+          row_axpy(dr2, tmp, ze);
+        }
+      }
+      row_st(DR2 + (long long)t * D.d, dr2, n4);
+      row_ld(x, XM + (long long)t * D.d, n4);
+      row_ld(dx, DX + (long long)t * D.d, n4);
+      row_norm_bwd(dxm, dr2, x, inv2[t], g, D.d);
+      row_add(dx, dxm);
+      row_st(DX + (long long)t * D.d, dx, n4);
+      row_st_op(DXO + (long long)t * D.d, dx, n4);
     }
-    __syncwarp();
-    float* dx = DX + (long long)t * D.d;
-    warp_rmsnorm_bwd(dr2, XM + (long long)t * D.d, inv2[t], g, D.d, dx, true);
-    __syncwarp();
-    for (int i = lane; i < D.d; i += 32) DXO[(long long)t * D.d + i] = from_f<OP>(dx[i]);
-  }
+  });
   s.next(s.G);
 }
 
@@ -469,12 +525,21 @@ __device__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s) {
   const float* DR = abuf<float>(a, A_DR);
   const float* X = abuf<float>(a, A_X) + (long long)l * D.T * D.d;
   const float* inv = abuf<float>(a, A_INV1) + (long long)l * D.T;
-  const float* g = pmaster(a, P_ATTN_NORM) + (long long)l * D.d;
   float* DX = abuf<float>(a, A_DX);
-  const int nw = s.G * MT_WARPS;
-  for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw)
-    warp_rmsnorm_bwd(DR + (long long)t * D.d, X + (long long)t * D.d, inv[t], g, D.d,
-                     DX + (long long)t * D.d, true);
+  const int n4 = D.d / 4, nw = s.G * MT_WARPS;
+  with_nc(D.d, [&](auto NCc) {
+    constexpr int NC = decltype(NCc)::value;
+    Row<NC> g, dy, x, dx, acc;
+    row_ld(g, pmaster(a, P_ATTN_NORM) + (long long)l * D.d, n4);
+    for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
+      row_ld(dy, DR + (long long)t * D.d, n4);
+      row_ld(x, X + (long long)t * D.d, n4);
+      row_ld(acc, DX + (long long)t * D.d, n4);
+      row_norm_bwd(dx, dy, x, inv[t], g, D.d);
+      row_add(acc, dx);
+      row_st(DX + (long long)t * D.d, acc, n4);
+    }
+  });
   s.next(s.G);
 }
 
@@ -494,45 +559,74 @@ struct ColArgs {
   int row0;           // first PART row written
 };
 
-static __device__ void job_colpart(const KArgs& a, const ColArgs& c, Sched& s) {
+static __device__ void job_colpart(const KArgs& a, const ColArgs& c, Sched& s, float* sm) {
   const MtDims& D = a.D;
   const int G = s.G;
   const int ch = chunk_len(D, G);
   const int ncb = (D.d + 127) / 128;
   const int items = G * ncb;
-  const int nrows = (c.kind == COL_MOE) ? D.E + 1 : 1;
+  const bool moe = (c.kind == COL_MOE);
+  const int nrows = moe ? D.E + 1 : 1;
   float* PART = abuf<float>(a, A_PART);
-  const int col_l = threadIdx.x & 127, rg = threadIdx.x >> 7;   // 2 row groups
+  const int col_l = threadIdx.x & 127, rg = threadIdx.x >> 7;   // two row groups
+  const int jmax = (nrows - rg + 1) / 2;                         // rows rg, rg+2, ... < nrows
+  constexpr int SUB = 256;                                       // tokens staged at a time
+  float* s_inv = sm;               // [SUB]
+  float* s_dz = sm + SUB;          // [SUB][E]
   for (int it = s.first(); it < items; it += G) {
     const int chunk = it / ncb, cb = it % ncb;
     const int col = cb * 128 + col_l;
     const int t0 = chunk * ch, t1 = min(D.T, t0 + ch);
     float acc[33];
 #pragma unroll
-    for (int r = 0; r < 33; ++r) acc[r] = 0.f;
-    if (col < D.d) {
-      for (int t = t0; t < t1; ++t) {
-        const float xh = c.x[(long long)t * D.d + col] * c.inv[t];
-        if (c.kind == COL_GAIN) {
-          if (rg == 0) acc[0] = fmaf(c.dy[(long long)t * D.d + col], xh, acc[0]);
-        } else {
-          const float r2 = xh * c.g[col];
+    for (int j = 0; j < 33; ++j) acc[j] = 0.f;
+    const float gcol = (moe && col < D.d) ? c.g[col] : 0.f;
+    for (int s0 = t0; s0 < t1; s0 += SUB) {
+      const int n = min(SUB, t1 - s0);
+      __syncthreads();
+      for (int i = threadIdx.x; i < n; i += MT_THREADS) s_inv[i] = c.inv[s0 + i];
+      if (moe)
+        for (int i = threadIdx.x; i < n * D.E; i += MT_THREADS) s_dz[i] = c.dz[(long long)s0 * D.E + i];
+      __syncthreads();
+      if (col >= D.d) continue;
+      for (int tb = 0; tb < n; tb += 8) {
+        float xv[8], dyv[8];
 #pragma unroll
-          for (int j = 0; j < 33; ++j) {
-            const int e = rg + 2 * j;
-            if (e < D.E) acc[j] = fmaf(c.dz[(long long)t * D.E + e], r2, acc[j]);
-            else if (e == D.E) acc[j] = fmaf(c.dy[(long long)t * D.d + col], xh, acc[j]);
+        for (int u = 0; u < 8; ++u) {
+          const bool ok = tb + u < n;
+          const long long off = (long long)(s0 + tb + u) * D.d + col;
+          xv[u] = ok ? c.x[off] : 0.f;
+          dyv[u] = ok ? c.dy[off] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (tb + u >= n) break;
+          const float xh = xv[u] * s_inv[tb + u];
+          if (!moe) {
+            acc[0] = fmaf(dyv[u], xh, acc[0]);
+          } else {
+            const float r2 = xh * gcol;
+            const float* dz = s_dz + (tb + u) * D.E;
+#pragma unroll
+            for (int j = 0; j < 33; ++j) {
+              if (j >= jmax) break;
+              const int e = rg + 2 * j;
+              acc[j] = fmaf(e < D.E ? dz[e] : dyv[u], e < D.E ? r2 : xh, acc[j]);
+            }
           }
         }
       }
+    }
+    if (col < D.d) {
       float* out = PART + ((long long)chunk * (D.E + 2) + c.row0) * D.d + col;
 #pragma unroll
       for (int j = 0; j < 33; ++j) {
         const int r = rg + 2 * j;
-        if (r < nrows) out[(long long)r * D.d] = acc[j];
+        if (r < nrows && (moe || rg == 0)) out[(long long)r * D.d] = acc[j];
       }
     }
   }
+  __syncthreads();
   s.next(items);
 }
 
@@ -836,11 +930,13 @@ struct Gemms {
     return g;
   }
   __device__ GemmDesc wo_dgrad(int l) const {
-    GemmDesc g = base(D.T, D.hq, D.d, EPI_STORE_OP);
+    GemmDesc g = base(D.T, D.hq, D.d, EPI_STORE_OP_D);
     g.A = opnd(abuf<OP>(a, A_DXO), D.d, 0); g.A.map0 = MAP_DXO;
     g.B = opnd(pweight<OP>(a, P_WO) + (long long)l * D.d * D.hq, D.hq, 1);
     g.B.map0 = MAP_WO; g.B.y0 = l * D.d;
     g.out = abuf<OP>(a, A_DO); g.ldo = D.hq;
+    g.aux = abuf<OP>(a, A_O) + (long long)l * D.T * D.hq; g.ldaux = D.hq;
+    g.out2 = abuf<float>(a, A_DSUM); g.ldo2 = D.H;
     return g;
   }
   __device__ GemmDesc wo_wgrad(int l) const {
@@ -893,13 +989,35 @@ __device__ __forceinline__ AttnArgs attn_args(const KArgs& a, int l) {
 }
 
 template <class OP>
+__device__ __forceinline__ attn_tc::Args attn_tc_args(const KArgs& a, int l) {
+  const MtDims& D = a.D;
+  attn_tc::Args t;
+  t.qkv = abuf<__nv_bfloat16>(a, A_QKV) + (long long)l * D.T * 3 * D.hq;
+  t.o = abuf<__nv_bfloat16>(a, A_O) + (long long)l * D.T * D.hq;
+  t.lse = abuf<float>(a, A_LSE) + (long long)l * D.B * D.H * D.S;
+  t.dout = abuf<__nv_bfloat16>(a, A_DO);
+  t.dsum = abuf<float>(a, A_DSUM);
+  t.dqkv = abuf<__nv_bfloat16>(a, A_DQKV);
+  t.rope = abuf<float>(a, A_ROPE);
+  t.B = D.B; t.H = D.H; t.S = D.S; t.hq = D.hq;
+  t.scale = 1.0f / sqrtf((float)D.hd);
+  return t;
+}
+
+template <class OP>
 __device__ __forceinline__ void run_attn_fwd(const KArgs& a, int l, Sched& s, char* smem) {
+  if constexpr (sizeof(OP) == 2) {
+    if (a.use_tc_attn) { attn_tc_fwd_job<OP>(attn_tc_args<OP>(a, l), s, smem); return; }
+  }
   const AttnArgs t = attn_args<OP>(a, l);
   if (a.D.hd == 64) attn_fwd_job<OP, 64>(t, s, (float*)smem);
   else attn_fwd_job<OP, 16>(t, s, (float*)smem);
 }
 template <class OP>
 __device__ __forceinline__ void run_attn_bwd(const KArgs& a, int l, Sched& s, char* smem) {
+  if constexpr (sizeof(OP) == 2) {
+    if (a.use_tc_attn) { attn_tc_bwd_job<OP>(attn_tc_args<OP>(a, l), s, smem); return; }
+  }
   const AttnArgs t = attn_args<OP>(a, l);
   if (a.D.hd == 64) attn_bwd_job<OP, 64>(t, s, (float*)smem);
   else attn_bwd_job<OP, 16>(t, s, (float*)smem);
@@ -966,7 +1084,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     // final-norm gain partials (DRF stays valid until the next LM-head use)
     ColArgs c{COL_GAIN, abuf<float>(a, A_DRF), abuf<float>(a, A_X) + (long long)D.L * D.T * D.d,
               abuf<float>(a, A_INVF), nullptr, nullptr, D.E + 1};
-    job_colpart(a, c, s);
+    job_colpart(a, c, s, (float*)smem);
   }
   for (int l = D.L - 1; l >= 0; --l) {
     job_moe_bwd1<OP>(a, l, s);
@@ -974,7 +1092,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
       // attention-norm gain partials of layer l+1 (DR of layer l+1 is still live)
       ColArgs c{COL_GAIN, abuf<float>(a, A_DR), abuf<float>(a, A_X) + (long long)(l + 1) * D.T * D.d,
                 abuf<float>(a, A_INV1) + (long long)(l + 1) * D.T, nullptr, nullptr, D.E + 1};
-      job_colpart(a, c, s);
+      job_colpart(a, c, s, (float*)smem);
     }
     MT_SYNC();
     if (l == D.L - 1) job_colfinal(a, D.E + 1, 1, pgrad(a, P_FINAL_NORM), nullptr, 0, s);
@@ -991,7 +1109,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
       ColArgs c{COL_MOE, abuf<float>(a, A_DR2), abuf<float>(a, A_XM) + (long long)l * D.T * D.d,
                 abuf<float>(a, A_INV2) + (long long)l * D.T, pmaster(a, P_MOE_NORM) + (long long)l * D.d,
                 abuf<float>(a, A_DZ), 0};
-      job_colpart(a, c, s);
+      job_colpart(a, c, s, (float*)smem);
     }
     run_gemm<OP>(a, gm.wo_dgrad(l), s, smem, tc);
     run_gemm<OP>(a, gm.wo_wgrad(l), s, smem, tc);
@@ -1009,7 +1127,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   {
     ColArgs c{COL_GAIN, abuf<float>(a, A_DR), abuf<float>(a, A_X), abuf<float>(a, A_INV1), nullptr,
               nullptr, D.E + 1};
-    job_colpart(a, c, s);
+    job_colpart(a, c, s, (float*)smem);
   }
   job_embed_bwd(a, (int*)smem);
   MT_SYNC();
