@@ -1,12 +1,12 @@
 // gemm_tc.cuh - tensor-core matrix products (tcgen05 + TMEM + TMA) inside
 // the persistent kernel, for the bf16-product policy.
 //
-// Tile 128 x 128 x 64.  Per GEMM job:
-//   warp 0 (one lane)  - TMA producer: two 64x64 boxes of A and two of B per
-//                        stage into a 6-stage ring of 128B-swizzled tiles;
-//   warp 1 (one lane)  - MMA issuer: 4 x tcgen05.mma (K = 16) per stage into
-//                        one of two TMEM accumulators (128 lanes x 128 fp32
-//                        columns each), tcgen05.commit frees the stage;
+// Tile 128 x 256 x 64.  Per GEMM job:
+//   warp 0 (one lane)  - TMA producer: two 64x64 boxes of A and four of B per
+//                        stage into a 4-stage ring of 128B-swizzled tiles;
+//   warp 1 (one lane)  - MMA issuer: 4 x tcgen05.mma (128 x 256 x 16) per
+//                        stage into one of two TMEM accumulators (128 lanes x
+//                        256 fp32 columns each), tcgen05.commit frees the stage;
 //   warps 4..7         - epilogue: tcgen05.ld of the accumulator rows (warp
 //                        w reads TMEM lanes 32*(w-4)..), fused epilogue, store.
 // A and B may each be K-major or MN-major in memory (forward, dgrad and
@@ -18,14 +18,14 @@
 #include "gemm.cuh"
 
 #define TC_BM 128
-#define TC_BN 128
+#define TC_BN 256
 #define TC_BK 64
-#define TC_STAGES 6
+#define TC_STAGES 4
 #define TC_BOX_BYTES (64 * 64 * 2)
-#define TC_STAGE_BYTES (4 * TC_BOX_BYTES)
+#define TC_STAGE_BYTES ((TC_BM + TC_BN) / 64 * TC_BOX_BYTES)
 #define TC_RING_OFF 1024
 #define MT_TC_SMEM (TC_RING_OFF + TC_STAGES * TC_STAGE_BYTES)
-#define TC_TMEM_COLS 256
+#define TC_TMEM_COLS 512
 #define MT_TC_AVAILABLE 1
 
 struct TcState {
@@ -163,8 +163,20 @@ struct TcTile {
   int m0, n0, seg, kbeg, nk;
 };
 
-__device__ __forceinline__ TcTile tc_tile(const GemmDesc& g, int t, int nt) {
+// Loop-invariant shape of a product, copied into registers by each role.
+struct TcShape {
+  int rag, M, K, nseg, nt;
+  const int* offs;
+};
+__device__ __forceinline__ TcShape tc_shape(const GemmDesc& g) {
+  TcShape sh;
+  sh.rag = g.rag; sh.M = g.M; sh.K = g.K; sh.nseg = g.nseg; sh.nt = g.N / TC_BN; sh.offs = g.offs;
+  return sh;
+}
+
+__device__ __forceinline__ TcTile tc_tile(const TcShape& g, int t) {
   TcTile ti;
+  const int nt = g.nt;
   if (g.rag == RAG_K) {
     const int mt = g.M / TC_BM;
     ti.seg = t / (mt * nt);
@@ -183,20 +195,37 @@ __device__ __forceinline__ TcTile tc_tile(const GemmDesc& g, int t, int nt) {
   return ti;
 }
 
-// Load the A (rows m0..m0+127) or B (rows n0..n0+127) operand slice of one
-// 64-wide K block as two 64 x 64 boxes.
-__device__ __forceinline__ void tc_load_operand(const KArgs& a, const GOperand& o, int r0, int k0, int yseg_off,
-                                                uint32_t dst, uint32_t bar) {
+// Loop-invariant TMA state of one operand.
+struct TmaOp {
+  const CUtensorMap* m0;
+  const CUtensorMap* m1;
+  int mn, two, split, y0, yseg;
+};
+__device__ __forceinline__ TmaOp tma_op(const KArgs& a, const GOperand& o) {
+  TmaOp t;
+  t.m0 = &a.maps[o.map0];
+  t.m1 = (o.map1 >= 0) ? &a.maps[o.map1] : t.m0;
+  t.mn = o.mn; t.two = o.two; t.split = o.split; t.y0 = o.y0; t.yseg = o.yseg;
+  return t;
+}
+
+// Load the A (rows m0..m0+127) or B (rows n0..n0+255) operand slice of one
+// 64-wide K block as NBOX 64 x 64 boxes.
+template <int NBOX>
+__device__ __forceinline__ void tc_load_operand(const TmaOp& o, int r0, int k0, int yseg_off, uint32_t dst,
+                                                uint32_t bar) {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const CUtensorMap* map = &a.maps[o.map0];
+  for (int i = 0; i < NBOX; ++i) {
+    const CUtensorMap* map = o.m0;
     int x, y;
     if (!o.mn) {
       // element (r, k) at row y0 + r, column k
       int rr = r0 + 64 * i;
-      if (o.two == 1) {            // rows interleaved by 64 between two sources
-        map = &a.maps[i ? o.map1 : o.map0];
-        rr = (r0 >> 1);            // r0 is a multiple of 128: source row block r0/2
+      if (o.two == 1) {
+        // columns interleaved by 64 between two sources: box i is block
+        // r0/64 + i, even blocks from m0, odd from m1, row (block/2)*64
+        map = (i & 1) ? o.m1 : o.m0;
+        rr = (r0 >> 1) + (i >> 1) * 64;
       }
       x = k0;
       y = o.y0 + yseg_off + rr;
@@ -204,7 +233,7 @@ __device__ __forceinline__ void tc_load_operand(const KArgs& a, const GOperand& 
       // element (r, k) at row y0 + k, column r
       int kk = k0;
       if (o.two == 2 && k0 >= o.split) {
-        map = &a.maps[o.map1];
+        map = o.m1;
         kk = k0 - o.split;
       }
       x = r0 + 64 * i;
@@ -255,10 +284,11 @@ __device__ __forceinline__ void load_row_bf16(const __nv_bfloat16* src, float* v
 
 static __device__ __noinline__ void tc_epilogue(const GemmDesc& g, const TcTile& ti, uint32_t trow, int m) {
   typedef __nv_bfloat16 bf;
+  constexpr int NCH = TC_BN / 32;     // 32-column chunks per row
   switch (g.epi) {
     case EPI_ROPE: {
       // hd == 64: columns [64h, 64h+32) pair with [64h+32, 64h+64)
-      for (int h2 = 0; h2 < 2; ++h2) {
+      for (int h2 = 0; h2 < TC_BN / 64; ++h2) {
         float x[64];
         tmem_ld32(trow + h2 * 64, x);
         tmem_ld32(trow + h2 * 64 + 32, x + 32);
@@ -279,27 +309,29 @@ static __device__ __noinline__ void tc_epilogue(const GemmDesc& g, const TcTile&
       break;
     }
     case EPI_SWIGLU: {
-      // tile columns [0,64) = gate, [64,128) = up of expert rows f0..f0+63
-      const int f0 = (ti.n0 >> 7) * 64;
-      for (int c = 0; c < 2; ++c) {
-        float gg[32], uu[32];
-        tmem_ld32(trow + c * 32, gg);
-        tmem_ld32(trow + 64 + c * 32, uu);
-        const int f = f0 + c * 32;
-        bf* gu = (bf*)g.out + (long long)m * g.ldo;
-        store_row_bf16<32>(gu + f, gg);
-        store_row_bf16<32>(gu + g.F + f, uu);
-        float act[32];
+      // each 128-column half = [64 gate | 64 up] of expert rows f0..f0+63
+      for (int half = 0; half < TC_BN / 128; ++half) {
+        const int f0 = ((ti.n0 >> 7) + half) * 64;
+        for (int c = 0; c < 2; ++c) {
+          float gg[32], uu[32];
+          tmem_ld32(trow + half * 128 + c * 32, gg);
+          tmem_ld32(trow + half * 128 + 64 + c * 32, uu);
+          const int f = f0 + c * 32;
+          bf* gu = (bf*)g.out + (long long)m * g.ldo;
+          store_row_bf16<32>(gu + f, gg);
+          store_row_bf16<32>(gu + g.F + f, uu);
+          float act[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) act[i] = silu_f(gg[i]) * uu[i];
-        store_row_bf16<32>((bf*)g.out2 + (long long)m * g.ldo2 + f, act);
+          for (int i = 0; i < 32; ++i) act[i] = silu_f(gg[i]) * uu[i];
+          store_row_bf16<32>((bf*)g.out2 + (long long)m * g.ldo2 + f, act);
+        }
       }
       break;
     }
     case EPI_SWIGLU_BWD: {
       const bf* gu = (const bf*)g.aux + (long long)m * g.ldaux;
       bf* dgu = (bf*)g.out + (long long)m * g.ldo;
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < NCH; ++c) {
         float da[32], gg[32], uu[32], dg[32], du[32];
         tmem_ld32(trow + c * 32, da);
         const int n = ti.n0 + c * 32;
@@ -316,15 +348,15 @@ static __device__ __noinline__ void tc_epilogue(const GemmDesc& g, const TcTile&
       break;
     }
     case EPI_STORE_OP:
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < NCH; ++c) {
         float v[32];
         tmem_ld32(trow + c * 32, v);
         store_row_bf16<32>((bf*)g.out + (long long)m * g.ldo + ti.n0 + c * 32, v);
       }
       break;
     case EPI_STORE_OP_D: {
-      // two 64-column heads per tile
-      for (int h2 = 0; h2 < 2; ++h2) {
+      // 64-column heads
+      for (int h2 = 0; h2 < TC_BN / 64; ++h2) {
         float x[64], o[64];
         tmem_ld32(trow + h2 * 64, x);
         tmem_ld32(trow + h2 * 64 + 32, x + 32);
@@ -339,14 +371,14 @@ static __device__ __noinline__ void tc_epilogue(const GemmDesc& g, const TcTile&
       break;
     }
     case EPI_STORE_F32:
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < NCH; ++c) {
         float v[32];
         tmem_ld32(trow + c * 32, v);
         store_row_f32<32>((float*)g.out + (long long)m * g.ldo + ti.n0 + c * 32, v);
       }
       break;
     case EPI_RESID:
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < NCH; ++c) {
         float v[32];
         tmem_ld32(trow + c * 32, v);
         const float* r = (const float*)g.aux + (long long)m * g.ldaux + ti.n0 + c * 32;
@@ -363,7 +395,7 @@ static __device__ __noinline__ void tc_epilogue(const GemmDesc& g, const TcTile&
       int mm = m;
       if (g.osplit > 0 && m >= g.osplit) { out = (float*)g.out1; mm = m - g.osplit; }
       out += (long long)ti.seg * g.oseg + (long long)mm * g.ldo + ti.n0;
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < NCH; ++c) {
         float v[32];
         tmem_ld32(trow + c * 32, v);
         float* p = out + c * 32;
@@ -419,7 +451,7 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
-  const int nt = g.N / TC_BN;
+  const TcShape sh = tc_shape(g);
   const int items = gemm_items(g, TC_BM, TC_BN);
   const int first = s.first(), G = s.G;
 
@@ -427,11 +459,12 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
     if (lane == 0) {
       // make the generic-proxy writes of earlier phases visible to TMA reads
       asm volatile("fence.proxy.async;" ::: "memory");
+      const TmaOp oa = tma_op(a, g.A), ob = tma_op(a, g.B);
       uint32_t it = 0;
       bool ok = true;
       for (int t = first; t < items && ok; t += G) {
-        const TcTile ti = tc_tile(g, t, nt);
-        const int bseg = (g.rag == RAG_M) ? ti.seg * g.B.yseg : 0;
+        const TcTile ti = tc_tile(sh, t);
+        const int bseg = (sh.rag == RAG_M) ? ti.seg * ob.yseg : 0;
         for (int kb = 0; kb < ti.nk; ++kb, ++it) {
           const int st = it % TC_STAGES;
           const uint32_t ph = (it / TC_STAGES) & 1;
@@ -444,8 +477,8 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
           const uint32_t sa = ring + st * TC_STAGE_BYTES, sb = sa + 2 * TC_BOX_BYTES;
           const int k0 = ti.kbeg + kb * TC_BK;
           mbar_expect_tx(fb, TC_STAGE_BYTES);
-          tc_load_operand(a, g.A, ti.m0, k0, 0, sa, fb);
-          tc_load_operand(a, g.B, ti.n0, k0, bseg, sb, fb);
+          tc_load_operand<TC_BM / 64>(oa, ti.m0, k0, 0, sa, fb);
+          tc_load_operand<TC_BN / 64>(ob, ti.n0, k0, bseg, sb, fb);
         }
       }
       // drain: every issued stage must have landed before smem is reused
@@ -466,7 +499,7 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
       bool ok = true;
       uint32_t last_bar = 0, last_par = 0;
       for (int t = first; t < items && ok; t += G) {
-        const TcTile ti = tc_tile(g, t, nt);
+        const TcTile ti = tc_tile(sh, t);
         if (ti.nk == 0) continue;
         const int ab = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
@@ -508,7 +541,7 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
     const int q = warp - 4;
     uint32_t tcount = 0;
     for (int t = first; t < items; t += G) {
-      const TcTile ti = tc_tile(g, t, nt);
+      const TcTile ti = tc_tile(sh, t);
       const int m = ti.m0 + q * 32 + lane;
       if (ti.nk == 0) {
         tc_epilogue_empty(g, ti, m);

@@ -57,8 +57,9 @@ int check_hparams(const mt_hparams* hp) {
 bool tc_shapes_ok(const mt_hparams* hp) {
   const long long T = (long long)hp->batch * hp->seq;
   const int hq = hp->n_heads * hp->head_dim;
-  return T % 128 == 0 && hp->d_model % 128 == 0 && hq % 128 == 0 && hp->vocab % 128 == 0 &&
-         hp->d_ff % 128 == 0 && hp->head_dim == 64;
+  // 128-row tiles over tokens and expert rows, 256-column tiles over features
+  return T % 128 == 0 && hp->d_model % 256 == 0 && hq % 256 == 0 && hp->vocab % 256 == 0 &&
+         hp->d_ff % 256 == 0 && hp->head_dim == 64;
 }
 
 void make_plan(const mt_hparams* hp, MtPlan* P) {
@@ -366,7 +367,7 @@ int32_t mt_debug_gemm(const void* A, int32_t a_mn, const void* B, int32_t b_mn, 
   if (rag == 2 && !(a_mn && b_mn)) return MT_ERR_ARG;
   const bool bf16 = precision == MT_PREC_BF16;
   const bool tc = bf16 && use_tc && MT_TC_AVAILABLE;
-  if (tc && (M % 128 || N % 128 || K % 64)) return MT_ERR_UNSUPPORTED;
+  if (tc && (M % 128 || N % 256 || K % 64)) return MT_ERR_UNSUPPORTED;
   if (tc && (!aligned(A, 16) || !aligned(B, 16))) return MT_ERR_ARG;
   const size_t smem = tc ? (size_t)MT_TC_SMEM : (size_t)SG_BM * SG_CPAD * 4;
   int grid = 0;

@@ -230,7 +230,8 @@ int32_t mt_train_update_noalloc(float* params, void* shadow, float* grads, float
  *   rag = 2: ragged reduction.  A [K,M], B [K,N] (a_mn = b_mn = 1); segment e
  *            reduces rows offs[e]..offs[e+1] into C[e] ([nseg][M][N]).
  * A and B are bf16 (MT_PREC_BF16) or fp32 (MT_PREC_FP32) device arrays.  The
- * tensor-core path needs M and N multiples of 128 and K a multiple of 64.
+ * tensor-core path needs M a multiple of 128, N a multiple of 256 and K a
+ * multiple of 64.
  * arena: >= 4 KiB device scratch initialised with mt_arena_init.
  */
 int32_t mt_debug_gemm(const void* A, int32_t a_mn, const void* B, int32_t b_mn, float* C, int32_t M, int32_t N,

@@ -43,7 +43,7 @@ def _rel(a, b):
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
 def test_dense_layouts(use_tc, a_mn, b_mn):
     torch.manual_seed(0)
-    M, N, K = 384, 256, 448
+    M, N, K = 384, 512, 448
     a = torch.randn(M, K, device="cuda").bfloat16()
     b = torch.randn(N, K, device="cuda").bfloat16()
     A = a.t().contiguous() if a_mn else a
@@ -78,7 +78,7 @@ def test_ragged_reduction(use_tc):
     """Weight-gradient shape: C[e] = A_e^T B_e over segment e's rows; an
     empty segment gives zeros."""
     torch.manual_seed(2)
-    nseg, M, N = 3, 256, 384
+    nseg, M, N = 3, 256, 512
     counts = [256, 0, 384]
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     K = int(offs[-1])
