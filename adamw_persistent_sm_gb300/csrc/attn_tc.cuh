@@ -152,82 +152,97 @@ struct Args {
   float scale;
 };
 
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // ---------------------------------------------------------------------------
+// Every loop below double-buffers its streamed tiles: block i+1 is fetched
+// with cp.async while block i is multiplied.
 static __device__ void fwd_item(const Args& a, int b, int h, int qb, char* smem) {
-  const uint32_t sQ = s_u32(smem), sK = sQ + 128 * 128, sV = sK + 64 * 128;
+  const uint32_t sQ = s_u32(smem);
+  const uint32_t sKV = sQ + 128 * 128;                 // [2][K 64 rows | V 64 rows]
   const int warp = threadIdx.x >> 5, l = threadIdx.x & 31, g = l >> 2, t = l & 3;
   const long long ld = 3LL * a.hq;
   const bf* base = a.qkv + (long long)b * a.S * ld;
   const int q0 = qb * 128, qw = q0 + warp * 16;
+  const int nkb = (q0 + 128) / 64;
+  auto fetch = [&](int kb) {
+    const uint32_t buf = sKV + (kb & 1) * (2 * 64 * 128);
+    load_tile(buf, base + (long long)kb * 64 * ld + a.hq + h * HD, ld, 64);
+    load_tile(buf + 64 * 128, base + (long long)kb * 64 * ld + 2 * a.hq + h * HD, ld, 64);
+    cp_async_commit();
+  };
   load_tile(sQ, base + (long long)q0 * ld + h * HD, ld, 128);
-  cp_async_wait_all();
-  __syncthreads();
+  fetch(0);
   uint32_t qa[4][4];
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) frag_a(sQ, warp * 16, kk * 16, qa[kk]);
   float o[8][4];
   zero(o);
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const float sc = a.scale * LOG2E;
-  const int nkb = (q0 + 128) / 64;
   for (int kb = 0; kb < nkb; ++kb) {
+    if (kb + 1 < nkb) { fetch(kb + 1); cp_async_wait<1>(); }
+    else cp_async_wait<0>();
+    __syncthreads();
+    if (kb == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) frag_a(sQ, warp * 16, kk * 16, qa[kk]);
+    }
     const int k0 = kb * 64;
-    __syncthreads();
-    load_tile(sK, base + (long long)k0 * ld + a.hq + h * HD, ld, 64);
-    load_tile(sV, base + (long long)k0 * ld + 2 * a.hq + h * HD, ld, 64);
-    cp_async_wait_all();
-    __syncthreads();
-    if (k0 > qw + 15) continue;            // every key of this block is after this warp's rows
-    float s[8][4];
-    zero(s);
-    mm16x64x64<false>(s, qa, sK);
-    const bool diag = (k0 + 63 > qw);
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+    const uint32_t sK = sKV + (kb & 1) * (2 * 64 * 128), sV = sK + 64 * 128;
+    if (k0 <= qw + 15) {                 // some key of this block precedes this warp's rows
+      float s[8][4];
+      zero(s);
+      mm16x64x64<false>(s, qa, sK);
+      const bool diag = (k0 + 63 > qw);
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < 8; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = s[j][e] * sc;
-        if (diag) {
-          const int key = k0 + j * 8 + 2 * t + (e & 1);
-          const int row = qw + g + ((e >> 1) << 3);
-          if (key > row) v = -INFINITY;
+        for (int e = 0; e < 4; ++e) {
+          float v = s[j][e] * sc;
+          if (diag) {
+            const int key = k0 + j * 8 + 2 * t + (e & 1);
+            const int row = qw + g + ((e >> 1) << 3);
+            if (key > row) v = -INFINITY;
+          }
+          s[j][e] = v;
+          if (e < 2) mx0 = fmaxf(mx0, v); else mx1 = fmaxf(mx1, v);
         }
-        s[j][e] = v;
-        if (e < 2) mx0 = fmaxf(mx0, v); else mx1 = fmaxf(mx1, v);
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
+      const float c0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - nm0);
+      const float c1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - nm1);
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        s[j][0] = exp2f(s[j][0] - nm0);
+        s[j][1] = exp2f(s[j][1] - nm0);
+        s[j][2] = exp2f(s[j][2] - nm1);
+        s[j][3] = exp2f(s[j][3] - nm1);
+        ls0 += s[j][0] + s[j][1];
+        ls1 += s[j][2] + s[j][3];
       }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
-    const float c0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - nm0);
-    const float c1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - nm1);
-    float ls0 = 0.f, ls1 = 0.f;
+      ls0 += __shfl_xor_sync(0xffffffffu, ls0, 1);
+      ls0 += __shfl_xor_sync(0xffffffffu, ls0, 2);
+      ls1 += __shfl_xor_sync(0xffffffffu, ls1, 1);
+      ls1 += __shfl_xor_sync(0xffffffffu, ls1, 2);
+      l0 = l0 * c0 + ls0;
+      l1 = l1 * c1 + ls1;
+      m0 = nm0;
+      m1 = nm1;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      s[j][0] = exp2f(s[j][0] - nm0);
-      s[j][1] = exp2f(s[j][1] - nm0);
-      s[j][2] = exp2f(s[j][2] - nm1);
-      s[j][3] = exp2f(s[j][3] - nm1);
-      ls0 += s[j][0] + s[j][1];
-      ls1 += s[j][2] + s[j][3];
+      for (int j = 0; j < 8; ++j) {
+        o[j][0] *= c0; o[j][1] *= c0; o[j][2] *= c1; o[j][3] *= c1;
+      }
+      uint32_t pa[4][4];
+      c_to_a(s, pa);
+      mm16x64x64<true>(o, pa, sV);
     }
-    ls0 += __shfl_xor_sync(0xffffffffu, ls0, 1);
-    ls0 += __shfl_xor_sync(0xffffffffu, ls0, 2);
-    ls1 += __shfl_xor_sync(0xffffffffu, ls1, 1);
-    ls1 += __shfl_xor_sync(0xffffffffu, ls1, 2);
-    l0 = l0 * c0 + ls0;
-    l1 = l1 * c1 + ls1;
-    m0 = nm0;
-    m1 = nm1;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      o[j][0] *= c0; o[j][1] *= c0; o[j][2] *= c1; o[j][3] *= c1;
-    }
-    uint32_t pa[4][4];
-    c_to_a(s, pa);
-    mm16x64x64<true>(o, pa, sV);
+    __syncthreads();                     // buffer kb & 1 is refilled by the next iteration's fetch
   }
   const float i0 = 1.f / l0, i1 = 1.f / l1;
 #pragma unroll
@@ -244,56 +259,65 @@ static __device__ void fwd_item(const Args& a, int b, int h, int qb, char* smem)
 
 // dQ for 128 query rows
 static __device__ void dq_item(const Args& a, int b, int h, int qb, char* smem) {
-  const uint32_t sQ = s_u32(smem), sD = sQ + 128 * 128, sK = sD + 128 * 128, sV = sK + 64 * 128;
+  const uint32_t sQ = s_u32(smem), sD = sQ + 128 * 128;
+  const uint32_t sKV = sD + 128 * 128;                 // [2][K 64 rows | V 64 rows]
   const int warp = threadIdx.x >> 5, l = threadIdx.x & 31, g = l >> 2, t = l & 3;
   const long long ld = 3LL * a.hq;
   const bf* base = a.qkv + (long long)b * a.S * ld;
   const int q0 = qb * 128, qw = q0 + warp * 16;
+  const int nkb = (q0 + 128) / 64;
+  auto fetch = [&](int kb) {
+    const uint32_t buf = sKV + (kb & 1) * (2 * 64 * 128);
+    load_tile(buf, base + (long long)kb * 64 * ld + a.hq + h * HD, ld, 64);
+    load_tile(buf + 64 * 128, base + (long long)kb * 64 * ld + 2 * a.hq + h * HD, ld, 64);
+    cp_async_commit();
+  };
   load_tile(sQ, base + (long long)q0 * ld + h * HD, ld, 128);
   load_tile(sD, a.dout + ((long long)b * a.S + q0) * a.hq + h * HD, a.hq, 128);
-  cp_async_wait_all();
-  __syncthreads();
-  uint32_t qa[4][4], da[4][4];
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    frag_a(sQ, warp * 16, kk * 16, qa[kk]);
-    frag_a(sD, warp * 16, kk * 16, da[kk]);
-  }
+  fetch(0);
   const float* Lr = a.lse + ((long long)b * a.H + h) * a.S;
   const float lse0 = Lr[qw + g] * LOG2E, lse1 = Lr[qw + g + 8] * LOG2E;
   const float* Dr = a.dsum + ((long long)b * a.S) * a.H + h;
   const float D0 = Dr[(long long)(qw + g) * a.H], D1 = Dr[(long long)(qw + g + 8) * a.H];
+  uint32_t qa[4][4], da[4][4];
   float dq[8][4];
   zero(dq);
   const float sc = a.scale * LOG2E;
-  const int nkb = (q0 + 128) / 64;
   for (int kb = 0; kb < nkb; ++kb) {
-    const int k0 = kb * 64;
+    if (kb + 1 < nkb) { fetch(kb + 1); cp_async_wait<1>(); }
+    else cp_async_wait<0>();
     __syncthreads();
-    load_tile(sK, base + (long long)k0 * ld + a.hq + h * HD, ld, 64);
-    load_tile(sV, base + (long long)k0 * ld + 2 * a.hq + h * HD, ld, 64);
-    cp_async_wait_all();
-    __syncthreads();
-    if (k0 > qw + 15) continue;
-    float s[8][4], dp[8][4];
-    zero(s);
-    zero(dp);
-    mm16x64x64<false>(s, qa, sK);
-    mm16x64x64<false>(dp, da, sV);
-    const bool diag = (k0 + 63 > qw);
+    if (kb == 0) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = k0 + j * 8 + 2 * t + (e & 1);
-        const int row = qw + g + ((e >> 1) << 3);
-        float p = exp2f(s[j][e] * sc - ((e >> 1) ? lse1 : lse0));
-        if (diag && key > row) p = 0.f;
-        s[j][e] = p * (dp[j][e] - ((e >> 1) ? D1 : D0));
+      for (int kk = 0; kk < 4; ++kk) {
+        frag_a(sQ, warp * 16, kk * 16, qa[kk]);
+        frag_a(sD, warp * 16, kk * 16, da[kk]);
       }
-    uint32_t sa[4][4];
-    c_to_a(s, sa);
-    mm16x64x64<true>(dq, sa, sK);
+    }
+    const int k0 = kb * 64;
+    const uint32_t sK = sKV + (kb & 1) * (2 * 64 * 128), sV = sK + 64 * 128;
+    if (k0 <= qw + 15) {
+      float s[8][4], dp[8][4];
+      zero(s);
+      zero(dp);
+      mm16x64x64<false>(s, qa, sK);
+      mm16x64x64<false>(dp, da, sV);
+      const bool diag = (k0 + 63 > qw);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = k0 + j * 8 + 2 * t + (e & 1);
+          const int row = qw + g + ((e >> 1) << 3);
+          float p = exp2f(s[j][e] * sc - ((e >> 1) ? lse1 : lse0));
+          if (diag && key > row) p = 0.f;
+          s[j][e] = p * (dp[j][e] - ((e >> 1) ? D1 : D0));
+        }
+      uint32_t sa[4][4];
+      c_to_a(s, sa);
+      mm16x64x64<true>(dq, sa, sK);
+    }
+    __syncthreads();
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -305,63 +329,76 @@ static __device__ void dq_item(const Args& a, int b, int h, int qb, char* smem) 
 
 // dK and dV for 128 keys
 static __device__ void dkdv_item(const Args& a, int b, int h, int kb, char* smem) {
-  const uint32_t sK = s_u32(smem), sV = sK + 128 * 128, sQ = sV + 128 * 128, sD = sQ + 64 * 128;
-  float* sL = reinterpret_cast<float*>(smem + 2 * 128 * 128 + 2 * 64 * 128);   // [64] lse * log2e
-  float* sDs = sL + 64;                                                         // [64] D
+  const uint32_t sK = s_u32(smem), sV = sK + 128 * 128;
+  const uint32_t sQD = sV + 128 * 128;                  // [2][Q 64 rows | dO 64 rows]
+  float* sLD = reinterpret_cast<float*>(smem + 2 * 128 * 128 + 2 * 2 * 64 * 128);   // [2][lse 64 | D 64]
   const int warp = threadIdx.x >> 5, l = threadIdx.x & 31, g = l >> 2, t = l & 3;
   const long long ld = 3LL * a.hq;
   const bf* base = a.qkv + (long long)b * a.S * ld;
   const int k0 = kb * 128, kw = k0 + warp * 16;
+  const float* Lr = a.lse + ((long long)b * a.H + h) * a.S;
+  const float* Dr = a.dsum + ((long long)b * a.S) * a.H + h;
+  const int nqb = (a.S - k0) / 64;
+  auto fetch = [&](int i) {
+    const int q0 = k0 + i * 64;
+    const uint32_t buf = sQD + (i & 1) * (2 * 64 * 128);
+    load_tile(buf, base + (long long)q0 * ld + h * HD, ld, 64);
+    load_tile(buf + 64 * 128, a.dout + ((long long)b * a.S + q0) * a.hq + h * HD, a.hq, 64);
+    cp_async_commit();
+    float* ldbuf = sLD + (i & 1) * 128;
+    if (threadIdx.x < 64) {
+      ldbuf[threadIdx.x] = Lr[q0 + threadIdx.x] * LOG2E;
+      ldbuf[64 + threadIdx.x] = Dr[(long long)(q0 + threadIdx.x) * a.H];
+    }
+  };
   load_tile(sK, base + (long long)k0 * ld + a.hq + h * HD, ld, 128);
   load_tile(sV, base + (long long)k0 * ld + 2 * a.hq + h * HD, ld, 128);
-  cp_async_wait_all();
-  __syncthreads();
+  fetch(0);
   uint32_t ka[4][4], va[4][4];
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    frag_a(sK, warp * 16, kk * 16, ka[kk]);
-    frag_a(sV, warp * 16, kk * 16, va[kk]);
-  }
   float dk[8][4], dv[8][4];
   zero(dk);
   zero(dv);
   const float sc = a.scale * LOG2E;
-  const float* Lr = a.lse + ((long long)b * a.H + h) * a.S;
-  const float* Dr = a.dsum + ((long long)b * a.S) * a.H + h;
-  for (int q0 = k0; q0 < a.S; q0 += 64) {
+  for (int i = 0; i < nqb; ++i) {
+    if (i + 1 < nqb) { fetch(i + 1); cp_async_wait<1>(); }
+    else cp_async_wait<0>();
     __syncthreads();
-    load_tile(sQ, base + (long long)q0 * ld + h * HD, ld, 64);
-    load_tile(sD, a.dout + ((long long)b * a.S + q0) * a.hq + h * HD, a.hq, 64);
-    if (threadIdx.x < 64) {
-      sL[threadIdx.x] = Lr[q0 + threadIdx.x] * LOG2E;
-      sDs[threadIdx.x] = Dr[(long long)(q0 + threadIdx.x) * a.H];
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    if (q0 + 63 < kw) continue;            // every query of this block precedes this warp's keys
-    // S^T (16 keys x 64 queries) and dP^T
-    float s[8][4], dp[8][4];
-    zero(s);
-    zero(dp);
-    mm16x64x64<false>(s, ka, sQ);
-    mm16x64x64<false>(dp, va, sD);
-    const bool diag = (q0 < kw + 15);
+    if (i == 0) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int qi = j * 8 + 2 * t + (e & 1);
-        const int key = kw + g + ((e >> 1) << 3);
-        float p = exp2f(s[j][e] * sc - sL[qi]);
-        if (diag && q0 + qi < key) p = 0.f;
-        s[j][e] = p;
-        dp[j][e] = p * (dp[j][e] - sDs[qi]);
+      for (int kk = 0; kk < 4; ++kk) {
+        frag_a(sK, warp * 16, kk * 16, ka[kk]);
+        frag_a(sV, warp * 16, kk * 16, va[kk]);
       }
-    uint32_t pa[4][4], dsa[4][4];
-    c_to_a(s, pa);
-    c_to_a(dp, dsa);
-    mm16x64x64<true>(dv, pa, sD);
-    mm16x64x64<true>(dk, dsa, sQ);
+    }
+    const int q0 = k0 + i * 64;
+    const uint32_t sQ = sQD + (i & 1) * (2 * 64 * 128), sD = sQ + 64 * 128;
+    const float* sL = sLD + (i & 1) * 128;
+    const float* sDs = sL + 64;
+    if (q0 + 63 >= kw) {                 // some query of this block follows this warp's keys
+      float s[8][4], dp[8][4];
+      zero(s);
+      zero(dp);
+      mm16x64x64<false>(s, ka, sQ);      // S^T: keys x queries
+      mm16x64x64<false>(dp, va, sD);     // dP^T
+      const bool diag = (q0 < kw + 15);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int qi = j * 8 + 2 * t + (e & 1);
+          const int key = kw + g + ((e >> 1) << 3);
+          float p = exp2f(s[j][e] * sc - sL[qi]);
+          if (diag && q0 + qi < key) p = 0.f;
+          s[j][e] = p;
+          dp[j][e] = p * (dp[j][e] - sDs[qi]);
+        }
+      uint32_t pa[4][4], dsa[4][4];
+      c_to_a(s, pa);
+      c_to_a(dp, dsa);
+      mm16x64x64<true>(dv, pa, sD);
+      mm16x64x64<true>(dk, dsa, sQ);
+    }
+    __syncthreads();
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {

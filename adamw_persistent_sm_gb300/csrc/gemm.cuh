@@ -21,8 +21,10 @@ enum EpiKind {
   EPI_SWIGLU,         // tile = [64 gate | 64 up] columns -> g, u (out) and silu(g)*u (out2)
   EPI_SWIGLU_BWD,     // acc = d(silu(g)*u); aux = [g | u] -> out = [dg | du]
   EPI_GRAD,           // out(f32) = acc (+ out if accumulate); rows >= osplit go to out1
-  EPI_STORE_OP_D      // out(op) = acc, and out2(f32)[m][head] = sum over the head's 64 columns of
+  EPI_STORE_OP_D,     // out(op) = acc, and out2(f32)[m][head] = sum over the head's 64 columns of
                       // op(acc) * aux(op)  (attention's D = rowsum(dO * O))
+  EPI_LOGITS          // out(op) = acc (LM-head logits); per row and column tile, (max, sum exp(acc -
+                      // max)) into cepart[m][n0 / tile width]; the target token's fp32 logit into cetgt[m]
 };
 
 enum RagKind { RAG_NONE = 0, RAG_M = 1, RAG_K = 2 };
@@ -58,7 +60,20 @@ struct GemmDesc {
   int F;                                      // expert width (swiglu epilogues)
   int S, hd, hq;                              // EPI_ROPE
   const float* rope;                          // [S][hd/2][2] cos, sin
+  const int* tok;                             // EPI_LOGITS: token ids (target of row m = tok[m + 1])
+  float* cepart;                              // EPI_LOGITS: [M][ceparts][2]
+  float* cetgt;                               // EPI_LOGITS: [M]
+  int ceparts;
+  int ksplit;                                 // tensor-core path, dense products: the K range is cut
+                                              // into ksplit slices, slice s writes out + s * oseg
 };
+
+// Target column of logits row m (next token), or -1 for the last position.
+__device__ __forceinline__ int ce_target(const GemmDesc& g, int m) {
+  if (m % g.S == g.S - 1) return -1;
+  const int v = g.tok[m + 1];
+  return (v >= 0 && v < g.N) ? v : 0;
+}
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 __device__ __forceinline__ float silu_grad_f(float g) {
@@ -176,6 +191,34 @@ __device__ void gemm_simt_tile(const GemmDesc& g, int seg, int m0, int n0, int k
     }
   __syncthreads();
   const int warp = tid >> 5, lane = tid & 31;
+  if (g.epi == EPI_LOGITS) {
+    for (int r = warp; r < SG_BM; r += MT_WARPS) {
+      const int m = m0 + r;
+      if (m >= mmax) continue;
+      const float* crow = Cs + r * SG_CPAD;
+      const int tgt = ce_target(g, m);
+      float mx = -INFINITY;
+      for (int c = lane; c < SG_BN; c += 32) {
+        const int n = n0 + c;
+        if (n >= g.N) continue;
+        ((OP*)g.out)[(long long)m * g.ldo + n] = from_f<OP>(crow[c]);
+        mx = fmaxf(mx, crow[c]);
+        if (n == tgt) g.cetgt[m] = crow[c];
+      }
+      mx = warp_max(mx);
+      float sm = 0.f;
+      for (int c = lane; c < SG_BN; c += 32)
+        if (n0 + c < g.N) sm += expf(crow[c] - mx);
+      sm = warp_sum(sm);
+      if (lane == 0) {
+        float* pp = g.cepart + ((long long)m * g.ceparts + n0 / SG_BN) * 2;
+        pp[0] = mx;
+        pp[1] = sm;
+      }
+    }
+    __syncthreads();
+    return;
+  }
   if (g.epi == EPI_STORE_OP_D) {
     // 64-column heads: lane owns columns lane, lane+32 of each head
     for (int r = warp; r < SG_BM; r += MT_WARPS) {

@@ -165,12 +165,13 @@ struct TcTile {
 
 // Loop-invariant shape of a product, copied into registers by each role.
 struct TcShape {
-  int rag, M, K, nseg, nt;
+  int rag, M, K, nseg, nt, ksplit;
   const int* offs;
 };
 __device__ __forceinline__ TcShape tc_shape(const GemmDesc& g) {
   TcShape sh;
   sh.rag = g.rag; sh.M = g.M; sh.K = g.K; sh.nseg = g.nseg; sh.nt = g.N / TC_BN; sh.offs = g.offs;
+  sh.ksplit = (g.rag == RAG_NONE && g.ksplit > 1) ? g.ksplit : 1;
   return sh;
 }
 
@@ -185,6 +186,16 @@ __device__ __forceinline__ TcTile tc_tile(const TcShape& g, int t) {
     ti.n0 = (rem % nt) * TC_BN;
     ti.kbeg = g.offs[ti.seg];
     ti.nk = (g.offs[ti.seg + 1] - ti.kbeg) / TC_BK;
+  } else if (g.ksplit > 1) {
+    // slice s of the reduction; the output of slice s is redirected by seg
+    const int mt = g.M / TC_BM;
+    ti.seg = t / (mt * nt);
+    const int rem = t % (mt * nt);
+    ti.m0 = (rem / nt) * TC_BM;
+    ti.n0 = (rem % nt) * TC_BN;
+    const int kc = g.K / g.ksplit;
+    ti.kbeg = ti.seg * kc;
+    ti.nk = kc / TC_BK;
   } else {
     ti.m0 = (t / nt) * TC_BM;
     ti.n0 = (t % nt) * TC_BN;
@@ -282,26 +293,53 @@ __device__ __forceinline__ void load_row_bf16(const __nv_bfloat16* src, float* v
   }
 }
 
-static __device__ __noinline__ void tc_epilogue(const GemmDesc& g, const TcTile& ti, uint32_t trow, int m) {
+// Epilogue parameters copied into registers once per job: stores through
+// the output pointers can then not force re-reads of the descriptor.
+struct EpiRegs {
+  int epi, S, hq, F, accumulate, osplit, ceparts, N;
+  long long ldo, ldo2, ldaux, oseg;
+  void* out;
+  void* out1;
+  void* out2;
+  const void* aux;
+  const float* rope;
+  const int* tok;
+  float* cepart;
+  float* cetgt;
+};
+__device__ __forceinline__ EpiRegs epi_regs(const GemmDesc& g) {
+  EpiRegs e;
+  e.epi = g.epi; e.S = g.S; e.hq = g.hq; e.F = g.F; e.accumulate = g.accumulate; e.osplit = g.osplit;
+  e.ceparts = g.ceparts; e.N = g.N; e.ldo = g.ldo; e.ldo2 = g.ldo2; e.ldaux = g.ldaux; e.oseg = g.oseg;
+  e.out = g.out; e.out1 = g.out1; e.out2 = g.out2; e.aux = g.aux; e.rope = g.rope; e.tok = g.tok;
+  e.cepart = g.cepart; e.cetgt = g.cetgt;
+  return e;
+}
+
+__device__ __forceinline__ void tc_epilogue(const EpiRegs& g, const TcTile& ti, uint32_t trow, int m) {
   typedef __nv_bfloat16 bf;
   constexpr int NCH = TC_BN / 32;     // 32-column chunks per row
   switch (g.epi) {
     case EPI_ROPE: {
       // hd == 64: columns [64h, 64h+32) pair with [64h+32, 64h+64)
+      const float4* tab4 = reinterpret_cast<const float4*>(g.rope + (long long)(m % g.S) * 64);
       for (int h2 = 0; h2 < TC_BN / 64; ++h2) {
         float x[64];
         tmem_ld32(trow + h2 * 64, x);
         tmem_ld32(trow + h2 * 64 + 32, x + 32);
         const int n = ti.n0 + h2 * 64;
         if (n < 2 * g.hq) {
-          const int pos = m % g.S;
-          const float* tab = g.rope + (long long)pos * 32 * 2;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float c = tab[2 * i], s = tab[2 * i + 1];
-            const float x1 = x[i], x2 = x[i + 32];
-            x[i] = x1 * c - x2 * s;
-            x[i + 32] = x2 * c + x1 * s;
+          for (int i2 = 0; i2 < 16; ++i2) {
+            const float4 cs = tab4[i2];     // (cos, sin) of pairs 2*i2, 2*i2+1
+            const int i = 2 * i2;
+            float x1 = x[i], x2 = x[i + 32];
+            x[i] = x1 * cs.x - x2 * cs.y;
+            x[i + 32] = x2 * cs.x + x1 * cs.y;
+            x1 = x[i + 1];
+            x2 = x[i + 33];
+            x[i + 1] = x1 * cs.z - x2 * cs.w;
+            x[i + 33] = x2 * cs.z + x1 * cs.w;
           }
         }
         store_row_bf16<64>((bf*)g.out + (long long)m * g.ldo + n, x);
@@ -310,6 +348,8 @@ static __device__ __noinline__ void tc_epilogue(const GemmDesc& g, const TcTile&
     }
     case EPI_SWIGLU: {
       // each 128-column half = [64 gate | 64 up] of expert rows f0..f0+63
+      bf* gu = (bf*)g.out + (long long)m * g.ldo;
+      bf* act_row = (bf*)g.out2 + (long long)m * g.ldo2;
       for (int half = 0; half < TC_BN / 128; ++half) {
         const int f0 = ((ti.n0 >> 7) + half) * 64;
         for (int c = 0; c < 2; ++c) {
@@ -317,13 +357,12 @@ static __device__ __noinline__ void tc_epilogue(const GemmDesc& g, const TcTile&
           tmem_ld32(trow + half * 128 + c * 32, gg);
           tmem_ld32(trow + half * 128 + 64 + c * 32, uu);
           const int f = f0 + c * 32;
-          bf* gu = (bf*)g.out + (long long)m * g.ldo;
           store_row_bf16<32>(gu + f, gg);
           store_row_bf16<32>(gu + g.F + f, uu);
           float act[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) act[i] = silu_f(gg[i]) * uu[i];
-          store_row_bf16<32>((bf*)g.out2 + (long long)m * g.ldo2 + f, act);
+          store_row_bf16<32>(act_row + f, act);
         }
       }
       break;
@@ -339,57 +378,100 @@ static __device__ __noinline__ void tc_epilogue(const GemmDesc& g, const TcTile&
         load_row_bf16<32>(gu + g.F + n, uu);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          dg[i] = da[i] * uu[i] * silu_grad_f(gg[i]);
-          du[i] = da[i] * silu_f(gg[i]);
+          const float sg = 1.0f / (1.0f + __expf(-gg[i]));
+          du[i] = da[i] * gg[i] * sg;
+          dg[i] = da[i] * uu[i] * sg * (1.0f + gg[i] * (1.0f - sg));
         }
         store_row_bf16<32>(dgu + n, dg);
         store_row_bf16<32>(dgu + g.F + n, du);
       }
       break;
     }
-    case EPI_STORE_OP:
+    case EPI_STORE_OP: {
+      bf* o = (bf*)g.out + (long long)m * g.ldo + ti.n0;
       for (int c = 0; c < NCH; ++c) {
         float v[32];
         tmem_ld32(trow + c * 32, v);
-        store_row_bf16<32>((bf*)g.out + (long long)m * g.ldo + ti.n0 + c * 32, v);
-      }
-      break;
-    case EPI_STORE_OP_D: {
-      // 64-column heads
-      for (int h2 = 0; h2 < TC_BN / 64; ++h2) {
-        float x[64], o[64];
-        tmem_ld32(trow + h2 * 64, x);
-        tmem_ld32(trow + h2 * 64 + 32, x + 32);
-        const int n = ti.n0 + h2 * 64;
-        store_row_bf16<64>((bf*)g.out + (long long)m * g.ldo + n, x);
-        load_row_bf16<64>((const bf*)g.aux + (long long)m * g.ldaux + n, o);
-        float dot = 0.f;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) dot = fmaf(__bfloat162float(__float2bfloat16_rn(x[i])), o[i], dot);
-        ((float*)g.out2)[(long long)m * g.ldo2 + n / 64] = dot;
+        store_row_bf16<32>(o + c * 32, v);
       }
       break;
     }
-    case EPI_STORE_F32:
-      for (int c = 0; c < NCH; ++c) {
-        float v[32];
-        tmem_ld32(trow + c * 32, v);
-        store_row_f32<32>((float*)g.out + (long long)m * g.ldo + ti.n0 + c * 32, v);
+    case EPI_STORE_OP_D: {
+      // 64-column heads
+      bf* o = (bf*)g.out + (long long)m * g.ldo;
+      const bf* ao = (const bf*)g.aux + (long long)m * g.ldaux;
+      float* dsum = (float*)g.out2 + (long long)m * g.ldo2;
+      for (int h2 = 0; h2 < TC_BN / 64; ++h2) {
+        float x[64], oo[64];
+        tmem_ld32(trow + h2 * 64, x);
+        tmem_ld32(trow + h2 * 64 + 32, x + 32);
+        const int n = ti.n0 + h2 * 64;
+        store_row_bf16<64>(o + n, x);
+        load_row_bf16<64>(ao + n, oo);
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) dot = fmaf(__bfloat162float(__float2bfloat16_rn(x[i])), oo[i], dot);
+        dsum[n / 64] = dot;
       }
       break;
-    case EPI_RESID:
+    }
+    case EPI_LOGITS: {
+      int tgt = -1;
+      if (m % g.S != g.S - 1) {
+        tgt = g.tok[m + 1];
+        if (tgt < 0 || tgt >= g.N) tgt = 0;   // out-of-range ids are reported by the embedding job
+      }
+      bf* o = (bf*)g.out + (long long)m * g.ldo;
+      float mx = -INFINITY, sm = 0.f, tv = 0.f;
+      bool has_t = false;
       for (int c = 0; c < NCH; ++c) {
         float v[32];
         tmem_ld32(trow + c * 32, v);
-        const float* r = (const float*)g.aux + (long long)m * g.ldaux + ti.n0 + c * 32;
+        const int n = ti.n0 + c * 32;
+        store_row_bf16<32>(o + n, v);
+        float bm = mx;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          bm = fmaxf(bm, v[i]);
+          if (n + i == tgt) { tv = v[i]; has_t = true; }
+        }
+        float bs = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) bs += __expf(v[i] - bm);
+        sm = sm * __expf(mx - bm) + bs;
+        mx = bm;
+      }
+      if (has_t) g.cetgt[m] = tv;
+      float* pp = g.cepart + ((long long)m * g.ceparts + ti.n0 / TC_BN) * 2;
+      pp[0] = mx;
+      pp[1] = sm;
+      break;
+    }
+    case EPI_STORE_F32: {
+      float* o = (float*)g.out + (long long)m * g.ldo + ti.n0;
+      for (int c = 0; c < NCH; ++c) {
+        float v[32];
+        tmem_ld32(trow + c * 32, v);
+        store_row_f32<32>(o + c * 32, v);
+      }
+      break;
+    }
+    case EPI_RESID: {
+      float* o = (float*)g.out + (long long)m * g.ldo + ti.n0;
+      const float* rr = (const float*)g.aux + (long long)m * g.ldaux + ti.n0;
+      for (int c = 0; c < NCH; ++c) {
+        float v[32];
+        tmem_ld32(trow + c * 32, v);
+        const float* r = rr + c * 32;
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 q = *reinterpret_cast<const float4*>(r + i);
           v[i] += q.x; v[i + 1] += q.y; v[i + 2] += q.z; v[i + 3] += q.w;
         }
-        store_row_f32<32>((float*)g.out + (long long)m * g.ldo + ti.n0 + c * 32, v);
+        store_row_f32<32>(o + c * 32, v);
       }
       break;
+    }
     case EPI_GRAD: {
       float* out = (float*)g.out;
       int mm = m;
@@ -414,7 +496,7 @@ static __device__ __noinline__ void tc_epilogue(const GemmDesc& g, const TcTile&
 }
 
 // A weight-gradient tile whose expert received no rows: zero (or keep) the output.
-__device__ __forceinline__ void tc_epilogue_empty(const GemmDesc& g, const TcTile& ti, int m) {
+__device__ __forceinline__ void tc_epilogue_empty(const EpiRegs& g, const TcTile& ti, int m) {
   if (g.epi != EPI_GRAD || g.accumulate) return;
   float* out = (float*)g.out;
   int mm = m;
@@ -452,7 +534,7 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
   }
   __syncthreads();
   const TcShape sh = tc_shape(g);
-  const int items = gemm_items(g, TC_BM, TC_BN);
+  const int items = gemm_items(g, TC_BM, TC_BN) * sh.ksplit;
   const int first = s.first(), G = s.G;
 
   if (warp == 0) {
@@ -539,12 +621,13 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
     __syncwarp();
   } else if (warp >= 4) {
     const int q = warp - 4;
+    const EpiRegs er = epi_regs(g);
     uint32_t tcount = 0;
     for (int t = first; t < items; t += G) {
       const TcTile ti = tc_tile(sh, t);
       const int m = ti.m0 + q * 32 + lane;
       if (ti.nk == 0) {
-        tc_epilogue_empty(g, ti, m);
+        tc_epilogue_empty(er, ti, m);
         continue;
       }
       const int ab = tcount & 1;
@@ -556,7 +639,7 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
       __syncwarp();
       tc_fence_after();
       const uint32_t trow = tc.tmem_base + ab * TC_BN + ((uint32_t)(q * 32) << 16);
-      tc_epilogue(g, ti, trow, m);
+      tc_epilogue(er, ti, trow, m);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce + 8 * ab);

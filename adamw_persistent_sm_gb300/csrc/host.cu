@@ -47,6 +47,7 @@ int check_hparams(const mt_hparams* hp) {
   if (hp->d_ff % 64 != 0) return MT_ERR_UNSUPPORTED;
   if (hp->seq < 2) return MT_ERR_UNSUPPORTED;
   if (hp->vocab % 4 != 0) return MT_ERR_UNSUPPORTED;
+  if ((long long)hp->n_experts * hp->d_model * 4 > 160 * 1024) return MT_ERR_UNSUPPORTED;  // router staged in smem
   const long long T = (long long)hp->batch * hp->seq;
   if (T * hp->top_k + (long long)hp->n_experts * MT_TILE_M > (1LL << 30)) return MT_ERR_UNSUPPORTED;
   if ((long long)hp->vocab * T > (1LL << 40)) return MT_ERR_UNSUPPORTED;
@@ -96,7 +97,8 @@ void make_plan(const mt_hparams* hp, MtPlan* P) {
   sz[A_Y] = L * Pm * d * 4;
   sz[A_RF] = T * d * ob;
   sz[A_INVF] = T * 4;
-  sz[A_LOGITS] = T * D.V * 4;
+  sz[A_CEPART] = T * ((D.V + 127) / 128) * 2 * 4;
+  sz[A_CETGT] = T * 4;
   sz[A_DLOGITS] = T * D.V * ob;
   sz[A_TOKLOSS] = T * 4;
   sz[A_DX] = T * d * 4;
@@ -112,6 +114,7 @@ void make_plan(const mt_hparams* hp, MtPlan* P) {
   sz[A_DR] = T * d * 4;
   sz[A_DRF] = T * d * 4;
   sz[A_PART] = (long long)D.nch * (D.E + 2) * d * 4;
+  sz[A_KPART] = 8LL * 3 * D.hq * d * 4;
   sz[A_NORMPART] = (long long)D.nch * 8;
   sz[A_TRACE] = (long long)D.nch * MT_MAX_PHASES * 2 * 8;
   long long off = 0;
@@ -158,7 +161,7 @@ DevState g_dev[64];
 size_t smem_bytes(const MtDims& D, bool tc) {
   size_t attn = (size_t)(4 * 64 * 65 + 2 * 64 * 65 + 128) * 4;
   size_t simt = (size_t)SG_BM * SG_CPAD * 4;
-  size_t router = (size_t)8 * D.d * 4;
+  size_t router = (size_t)D.E * D.d * 4 + 64 * 4;
   size_t need = attn > simt ? attn : simt;
   if (router > need) need = router;
   if (tc && MT_TC_SMEM > need) need = MT_TC_SMEM;
@@ -349,7 +352,7 @@ int32_t mt_debug_view(const void* arena, const mt_hparams* hp, int32_t which, in
     case MT_VIEW_HIDDEN:
       *out = {base + P.aoff[A_X] + (long long)layer * T * D.d * 4, T * D.d, 4}; break;
     case MT_VIEW_LOGITS:
-      *out = {base + P.aoff[A_LOGITS], T * D.V, 4}; break;
+      *out = {base + P.aoff[A_DLOGITS], T * D.V, D.op_bytes}; break;
     default:
       return MT_ERR_ARG;
   }

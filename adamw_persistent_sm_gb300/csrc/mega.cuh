@@ -32,6 +32,27 @@ __device__ __forceinline__ const OP* pweight(const KArgs& a, int pid) {
 }
 __device__ __forceinline__ float* pgrad(const KArgs& a, int pid) { return a.grads + a.poff[pid]; }
 
+// Column tiles of the LM-head product (one cross-entropy partial each).
+template <class OP>
+__device__ __forceinline__ int ce_parts(const KArgs& a) {
+  const int w = (sizeof(OP) == 2 && a.use_tc) ? 256 : 128;
+  return (a.D.V + w - 1) / w;
+}
+
+// Slices of a weight-gradient reduction over K tokens on the tensor-core
+// path: enough tiles for every SM, K/64 divisible by the count, and the
+// slices must fit in A_KPART (8 x 3hq x d floats).
+__device__ __forceinline__ int ksplit_of(const KArgs& a, int M, int N, int K) {
+  if (!a.use_tc || M % 128 || N % 256 || K % 64) return 1;
+  const int tiles = (M / 128) * (N / 256);
+  int ks = (int)gridDim.x / tiles;
+  const long long cap = 8LL * 3 * a.D.hq * a.D.d / ((long long)M * N);
+  if (ks > cap) ks = (int)cap;
+  if (ks > 16) ks = 16;
+  while (ks > 1 && (K / 64) % ks) --ks;
+  return ks < 1 ? 1 : ks;
+}
+
 // token chunk owned by CTA c in chunked jobs (routing, column reductions)
 __device__ __forceinline__ int chunk_len(const MtDims& D, int G) { return (D.T + G - 1) / G; }
 
@@ -119,7 +140,12 @@ __device__ void job_router(const KArgs& a, int l, float* sm) {
   float* WGT = abuf<float>(a, A_WGT) + (long long)l * D.T * D.K;
   const float* g = pmaster(a, P_MOE_NORM) + (long long)l * D.d;
   const float* Wr = pmaster(a, P_ROUTER) + (long long)l * D.E * D.d;
-  (void)sm;
+  // router weights (fp32, E x d) staged once per CTA; per-expert counts after them
+  for (int i = threadIdx.x; i < D.E * D.d / 4; i += MT_THREADS)
+    reinterpret_cast<float4*>(sm)[i] = reinterpret_cast<const float4*>(Wr)[i];
+  int* s_cnt = reinterpret_cast<int*>(sm + (long long)D.E * D.d);
+  for (int e = threadIdx.x; e < D.E; e += MT_THREADS) s_cnt[e] = 0;
+  __syncthreads();
   const int n4 = D.d / 4;
   with_nc(D.d, [&](auto NCc) {
   constexpr int NC = decltype(NCc)::value;
@@ -133,7 +159,7 @@ __device__ void job_router(const KArgs& a, int l, float* sm) {
     if (lane == 0) inv2[t] = inv;
     float z0 = -INFINITY, z1 = -INFINITY;   // experts lane and lane + 32
     for (int e = 0; e < D.E; ++e) {
-      row_ld(w, Wr + (long long)e * D.d, n4);
+      row_ld(w, sm + (long long)e * D.d, n4);
       const float acc = row_dot(r, w);
       if (e == lane) z0 = acc;
       if (e == lane + 32) z1 = acc;
@@ -164,6 +190,7 @@ __device__ void job_router(const KArgs& a, int l, float* sm) {
       for (int k = 0; k < D.K; ++k) {
         IDX[(long long)t * D.K + k] = chosen_i[k];
         WGT[(long long)t * D.K + k] = chosen_p[k] / psum;
+        atomicAdd(&s_cnt[chosen_i[k]], 1);
       }
     }
   }
@@ -171,12 +198,9 @@ __device__ void job_router(const KArgs& a, int l, float* sm) {
   __syncthreads();
   if (t0 < D.T) {
     int* CNT = abuf<int>(a, A_CNT) + ((long long)l * D.nch + c) * D.E;
-    for (int e = threadIdx.x; e < D.E; e += MT_THREADS) {
-      int n = 0;
-      for (int j = t0 * D.K; j < t1 * D.K; ++j) n += (IDX[j] == e);
-      CNT[e] = n;
-    }
+    for (int e = threadIdx.x; e < D.E; e += MT_THREADS) CNT[e] = s_cnt[e];
   }
+  __syncthreads();
 }
 
 // route_order: stable counting sort of the T*K assignments by expert (the
@@ -248,20 +272,21 @@ __device__ void job_route(const KArgs& a, int l, int* ism) {
     }
   }
   __syncthreads();
-  // dispatch gather: XS[row] = R2[token]
+  // dispatch gather: XS[row] = R2[token], 16-byte chunks
+  const int n16 = D.d * (int)sizeof(OP) / 16;
   for (int j = a0 + warp; j < a1; j += MT_WARPS) {
     const int pos = INVM[j];
-    const OP* src = R2 + (long long)(j / D.K) * D.d;
-    OP* dst = XS + (long long)pos * D.d;
-    for (int i = lane; i < D.d; i += 32) dst[i] = src[i];
+    const uint4* src = reinterpret_cast<const uint4*>(R2 + (long long)(j / D.K) * D.d);
+    uint4* dst = reinterpret_cast<uint4*>(XS + (long long)pos * D.d);
+    for (int i = lane; i < n16; i += 32) dst[i] = src[i];
   }
   // zero the pad rows of every segment (spread over all CTAs)
   const int gw = c * MT_WARPS + warp, nw = G * MT_WARPS;
   for (int e = 0; e < D.E; ++e) {
     const int p0 = s_offs[e] + s_tot[e], p1 = s_offs[e + 1];
     for (int p = p0 + gw; p < p1; p += nw) {
-      OP* dst = XS + (long long)p * D.d;
-      for (int i = lane; i < D.d; i += 32) dst[i] = from_f<OP>(0.f);
+      uint4* dst = reinterpret_cast<uint4*>(XS + (long long)p * D.d);
+      for (int i = lane; i < n16; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
       if (lane == 0) PERM[p] = -1;
     }
   }
@@ -306,13 +331,22 @@ __device__ void job_combine(const KArgs& a, int l, Sched& s) {
   s.next(s.G);
 }
 
-// Fused softmax cross-entropy with its gradient: per position, lse over the
-// vocabulary, loss = coef * (lse - logit[target]) and
-// dlogits = coef * (softmax - onehot).  Position s predicts token s+1; the
-// last position of a sequence has no target (zero loss and gradient).
-// One warp per position; float4 loads, eight in flight per lane.
-__device__ __forceinline__ void ce_store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
-__device__ __forceinline__ void ce_store4(__nv_bfloat16* p, float4 v) {
+// Cross-entropy with its gradient, fused with the LM-head product: the
+// product's epilogue left the logits (operand type) and, per column tile,
+// the max and sum of exp(logit - max) of the fp32 accumulators, plus the
+// target's fp32 logit.  Per position: lse from the tile partials,
+// loss = coef * (lse - logit[target]), and the logits row is overwritten in
+// place by dlogits = coef * (softmax - onehot).  Position s predicts token
+// s+1; the last position of a sequence has no target (zero loss and gradient).
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
   __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
   uint2 u;
   u.x = *reinterpret_cast<uint32_t*>(&a);
@@ -323,44 +357,33 @@ template <class OP>
 __device__ void job_ce(const KArgs& a, Sched& s) {
   const MtDims& D = a.D;
   const int lane = threadIdx.x & 31;
-  const float* LOG = abuf<float>(a, A_LOGITS);
   OP* DL = abuf<OP>(a, A_DLOGITS);
+  const float* PART = abuf<float>(a, A_CEPART);
+  const float* TGT = abuf<float>(a, A_CETGT);
   float* TL = abuf<float>(a, A_TOKLOSS);
+  const int np = ce_parts<OP>(a);
   const int nw = s.G * MT_WARPS;
   const int v4 = D.V / 4;                 // V % 4 == 0 (checked on the host)
   constexpr int U = 8;
   for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
-    const float4* lg = reinterpret_cast<const float4*>(LOG + (long long)t * D.V);
-    OP* dl = DL + (long long)t * D.V;
+    OP* row = DL + (long long)t * D.V;
     const bool has = (t % D.S) != D.S - 1;
     if (!has) {
-      for (int j = lane; j < v4; j += 32) ce_store4(dl + 4 * j, make_float4(0.f, 0.f, 0.f, 0.f));
+      for (int j = lane; j < v4; j += 32) st4(row + 4 * j, make_float4(0.f, 0.f, 0.f, 0.f));
       if (lane == 0) TL[t] = 0.f;
       continue;
     }
     int target = a.tokens[t + 1];
     if (target < 0 || target >= D.V) target = 0;   // reported by job_embed; never read outside the row
     float m = -INFINITY, sum = 0.f;
-    for (int j0 = 0; j0 < v4; j0 += 32 * U) {
-      float4 q[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = j0 + lane + 32 * u;
-        q[u] = (j < v4) ? lg[j] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      }
-      float bm = m;
-#pragma unroll
-      for (int u = 0; u < U; ++u) bm = fmaxf(bm, fmaxf(fmaxf(q[u].x, q[u].y), fmaxf(q[u].z, q[u].w)));
-      if (bm == -INFINITY) continue;
-      float bs = 0.f;
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        bs += __expf(q[u].x - bm) + __expf(q[u].y - bm) + __expf(q[u].z - bm) + __expf(q[u].w - bm);
-      sum = sum * __expf(m - bm) + bs;
-      m = bm;
+    for (int i = lane; i < np; i += 32) {
+      const float pm = PART[((long long)t * np + i) * 2], ps = PART[((long long)t * np + i) * 2 + 1];
+      const float nm = fmaxf(m, pm);
+      sum = (m == -INFINITY ? 0.f : sum * expf(m - nm)) + (pm == -INFINITY ? 0.f : ps * expf(pm - nm));
+      m = nm;
     }
     const float M = warp_max(m);
-    sum = (m == -INFINITY) ? 0.f : sum * __expf(m - M);
+    sum = (m == -INFINITY) ? 0.f : sum * expf(m - M);
     sum = warp_sum(sum);
     const float lse = M + logf(sum);
     for (int j0 = 0; j0 < v4; j0 += 32 * U) {
@@ -368,7 +391,7 @@ __device__ void job_ce(const KArgs& a, Sched& s) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int j = j0 + lane + 32 * u;
-        if (j < v4) q[u] = lg[j];
+        if (j < v4) q[u] = ld4(row + 4 * j);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -383,11 +406,11 @@ __device__ void job_ce(const KArgs& a, Sched& s) {
             else if (c == 2) p.z -= a.coef;
             else p.w -= a.coef;
           }
-          ce_store4(dl + 4 * j, p);
+          st4(row + 4 * j, p);
         }
       }
     }
-    if (lane == 0) TL[t] = a.coef * (lse - LOG[(long long)t * D.V + target]);
+    if (lane == 0) TL[t] = a.coef * (lse - TGT[t]);
   }
   s.next(s.G);
 }
@@ -546,8 +569,10 @@ __device__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s) {
 // ===========================================================================
 // deterministic column reductions over tokens (norm gains, router weights)
 // ===========================================================================
-// Partial sums over CTA chunk c of the tokens, in token order, written to
-// PART[c][row][col]; a later phase adds the chunks in chunk order.
+// Partial sums over token chunks, each in token order, written to
+// PART[chunk][row][col]; a later phase adds the chunks in chunk order, so
+// the result does not depend on the grid size.  One thread owns one column
+// and every output row of it (ER accumulators, ER >= rows).
 enum ColKind { COL_GAIN = 0, COL_MOE = 1 };
 struct ColArgs {
   int kind;
@@ -559,59 +584,64 @@ struct ColArgs {
   int row0;           // first PART row written
 };
 
-static __device__ void job_colpart(const KArgs& a, const ColArgs& c, Sched& s, float* sm) {
+__device__ __forceinline__ int col_nchunks(const MtDims& D, int G) {
+  const int ncb = (D.d + MT_THREADS - 1) / MT_THREADS;
+  int n = (2 * G + ncb - 1) / ncb;
+  if (n > D.nch) n = D.nch;
+  if (n > D.T) n = D.T;
+  return n < 1 ? 1 : n;
+}
+
+template <int ER>
+__device__ void colpart_items(const KArgs& a, const ColArgs& c, Sched& s, float* sm) {
   const MtDims& D = a.D;
   const int G = s.G;
-  const int ch = chunk_len(D, G);
-  const int ncb = (D.d + 127) / 128;
-  const int items = G * ncb;
+  const int ncb = (D.d + MT_THREADS - 1) / MT_THREADS;
+  const int nchunk = col_nchunks(D, G);
+  const int ch = (D.T + nchunk - 1) / nchunk;
+  const int items = ncb * nchunk;
   const bool moe = (c.kind == COL_MOE);
-  const int nrows = moe ? D.E + 1 : 1;
+  const int E = moe ? D.E : 0;
   float* PART = abuf<float>(a, A_PART);
-  const int col_l = threadIdx.x & 127, rg = threadIdx.x >> 7;   // two row groups
-  const int jmax = (nrows - rg + 1) / 2;                         // rows rg, rg+2, ... < nrows
-  constexpr int SUB = 256;                                       // tokens staged at a time
-  float* s_inv = sm;               // [SUB]
-  float* s_dz = sm + SUB;          // [SUB][E]
+  constexpr int SUB = 256;           // tokens staged at a time
+  float* s_inv = sm;                 // [SUB]
+  float* s_dz = sm + SUB;            // [SUB][E]
   for (int it = s.first(); it < items; it += G) {
     const int chunk = it / ncb, cb = it % ncb;
-    const int col = cb * 128 + col_l;
+    const int col = cb * MT_THREADS + threadIdx.x;
     const int t0 = chunk * ch, t1 = min(D.T, t0 + ch);
-    float acc[33];
+    float acc[ER + 1];
 #pragma unroll
-    for (int j = 0; j < 33; ++j) acc[j] = 0.f;
+    for (int j = 0; j <= ER; ++j) acc[j] = 0.f;
     const float gcol = (moe && col < D.d) ? c.g[col] : 0.f;
     for (int s0 = t0; s0 < t1; s0 += SUB) {
       const int n = min(SUB, t1 - s0);
       __syncthreads();
       for (int i = threadIdx.x; i < n; i += MT_THREADS) s_inv[i] = c.inv[s0 + i];
       if (moe)
-        for (int i = threadIdx.x; i < n * D.E; i += MT_THREADS) s_dz[i] = c.dz[(long long)s0 * D.E + i];
+        for (int i = threadIdx.x; i < n * E; i += MT_THREADS) s_dz[i] = c.dz[(long long)s0 * E + i];
       __syncthreads();
       if (col >= D.d) continue;
-      for (int tb = 0; tb < n; tb += 8) {
-        float xv[8], dyv[8];
+      for (int tb = 0; tb < n; tb += 4) {
+        float xv[4], dyv[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 4; ++u) {
           const bool ok = tb + u < n;
           const long long off = (long long)(s0 + tb + u) * D.d + col;
           xv[u] = ok ? c.x[off] : 0.f;
           dyv[u] = ok ? c.dy[off] : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (tb + u >= n) break;
-          const float xh = xv[u] * s_inv[tb + u];
-          if (!moe) {
-            acc[0] = fmaf(dyv[u], xh, acc[0]);
-          } else {
-            const float r2 = xh * gcol;
-            const float* dz = s_dz + (tb + u) * D.E;
+        for (int u = 0; u < 4; ++u) {
+          if (tb + u < n) {
+            const float xh = xv[u] * s_inv[tb + u];
+            acc[ER] = fmaf(dyv[u], xh, acc[ER]);          // gain gradient row
+            if (ER > 0) {
+              const float r2 = xh * gcol;
+              const float* dz = s_dz + (tb + u) * E;
 #pragma unroll
-            for (int j = 0; j < 33; ++j) {
-              if (j >= jmax) break;
-              const int e = rg + 2 * j;
-              acc[j] = fmaf(e < D.E ? dz[e] : dyv[u], e < D.E ? r2 : xh, acc[j]);
+              for (int e = 0; e < ER; ++e)
+                if (e < E) acc[e] = fmaf(dz[e], r2, acc[e]);
             }
           }
         }
@@ -620,23 +650,30 @@ static __device__ void job_colpart(const KArgs& a, const ColArgs& c, Sched& s, f
     if (col < D.d) {
       float* out = PART + ((long long)chunk * (D.E + 2) + c.row0) * D.d + col;
 #pragma unroll
-      for (int j = 0; j < 33; ++j) {
-        const int r = rg + 2 * j;
-        if (r < nrows && (moe || rg == 0)) out[(long long)r * D.d] = acc[j];
-      }
+      for (int e = 0; e < ER; ++e)
+        if (e < E) out[(long long)e * D.d] = acc[e];
+      out[(long long)E * D.d] = acc[ER];
     }
   }
   __syncthreads();
   s.next(items);
 }
 
+static __device__ void job_colpart(const KArgs& a, const ColArgs& c, Sched& s, float* sm) {
+  const int E = (c.kind == COL_MOE) ? a.D.E : 0;
+  if (E == 0) colpart_items<0>(a, c, s, sm);
+  else if (E <= 4) colpart_items<4>(a, c, s, sm);
+  else if (E <= 16) colpart_items<16>(a, c, s, sm);
+  else if (E <= 32) colpart_items<32>(a, c, s, sm);
+  else colpart_items<64>(a, c, s, sm);
+}
+
 // out[r][col] (+)= sum over chunks of PART[chunk][row0 + r][col].
 static __device__ void job_colfinal(const KArgs& a, int row0, int nrows, float* out_rows, float* out_last,
-                             int last_is_separate, Sched& s) {
+                                    int last_is_separate, Sched& s) {
   const MtDims& D = a.D;
   const int G = s.G;
-  const int ch = chunk_len(D, G);
-  const int nused = (D.T + ch - 1) / ch;
+  const int nused = col_nchunks(D, G);
   const float* PART = abuf<float>(a, A_PART);
   const int n = nrows * D.d;
   const bool acc = a.micro_index > 0;
@@ -660,22 +697,44 @@ static __device__ void job_embed_bwd(const KArgs& a, int* ism) {
   const int v0 = (int)((long long)D.V * c / G), v1 = (int)((long long)D.V * (c + 1) / G);
   float* dE = pgrad(a, P_EMB);
   const float* DX = abuf<float>(a, A_DX);
+  const int n4 = D.d / 4;
   if (a.micro_index == 0) {
-    for (long long e = (long long)v0 * D.d + threadIdx.x; e < (long long)v1 * D.d; e += MT_THREADS) dE[e] = 0.f;
+    float4* z = reinterpret_cast<float4*>(dE + (long long)v0 * D.d);
+    const long long nz = (long long)(v1 - v0) * n4;
+    for (long long e = threadIdx.x; e < nz; e += MT_THREADS) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __syncthreads();
-  int* flag = ism;   // [256]
+  // matches of each 256-token block, compacted in ascending position order
+  int* list = ism;            // [256] positions
+  int* vid = ism + 256;       // [256] vocabulary rows
+  int* cnt = ism + 512;       // [8] per-warp counts
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int tb = 0; tb < D.T; tb += MT_THREADS) {
     const int t = tb + threadIdx.x;
-    int v = (t < D.T) ? a.tokens[t] : -1;
-    flag[threadIdx.x] = (v >= v0 && v < v1) ? v : -1;
+    const int v = (t < D.T) ? a.tokens[t] : -1;
+    const bool hit = v >= v0 && v < v1;
+    const unsigned m = __ballot_sync(0xffffffffu, hit);
+    if (lane == 0) cnt[warp] = __popc(m);
     __syncthreads();
-    for (int j = 0; j < MT_THREADS; ++j) {
-      const int vv = flag[j];
-      if (vv < 0) continue;
-      const float* dx = DX + (long long)(tb + j) * D.d;
-      float* row = dE + (long long)vv * D.d;
-      for (int i = threadIdx.x; i < D.d; i += MT_THREADS) row[i] += dx[i];
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += cnt[w];
+    int total = 0;
+    for (int w = 0; w < MT_WARPS; ++w) total += cnt[w];
+    if (hit) {
+      const int pos = base + __popc(m & ((1u << lane) - 1u));
+      list[pos] = t;
+      vid[pos] = v;
+    }
+    __syncthreads();
+    for (int j = 0; j < total; ++j) {
+      const float4* src = reinterpret_cast<const float4*>(DX + (long long)list[j] * D.d);
+      float4* row = reinterpret_cast<float4*>(dE + (long long)vid[j] * D.d);
+      for (int i = threadIdx.x; i < n4; i += MT_THREADS) {
+        const float4 x = src[i];
+        float4 y = row[i];
+        y.x += x.x; y.y += x.y; y.z += x.z; y.w += x.w;
+        row[i] = y;
+      }
     }
     __syncthreads();
   }
@@ -815,6 +874,7 @@ struct Gemms {
     g.out = g.out1 = g.out2 = nullptr; g.ldo = g.ldo2 = 0; g.oseg = 0; g.osplit = 0;
     g.aux = nullptr; g.ldaux = 0; g.accumulate = 0; g.F = D.F; g.S = D.S; g.hd = D.hd; g.hq = D.hq;
     g.rope = nullptr;
+    g.tok = nullptr; g.cepart = nullptr; g.cetgt = nullptr; g.ceparts = 0; g.ksplit = 1;
     return g;
   }
   __device__ const int* offs(int l) const { return abuf<int>(a, A_OFFS) + (long long)l * (D.E + 1); }
@@ -865,10 +925,12 @@ struct Gemms {
     return g;
   }
   __device__ GemmDesc lm() const {
-    GemmDesc g = base(D.T, D.V, D.d, EPI_STORE_F32);
+    GemmDesc g = base(D.T, D.V, D.d, EPI_LOGITS);
     g.A = opnd(abuf<OP>(a, A_RF), D.d, 0); g.A.map0 = MAP_RF;
     g.B = opnd(pweight<OP>(a, P_LM_HEAD), D.d, 0); g.B.map0 = MAP_WLM;
-    g.out = abuf<float>(a, A_LOGITS); g.ldo = D.V;
+    g.out = abuf<OP>(a, A_DLOGITS); g.ldo = D.V;
+    g.tok = a.tokens; g.cepart = abuf<float>(a, A_CEPART); g.cetgt = abuf<float>(a, A_CETGT);
+    g.ceparts = ce_parts<OP>(a);
     return g;
   }
   // backward
@@ -939,12 +1001,23 @@ struct Gemms {
     g.out2 = abuf<float>(a, A_DSUM); g.ldo2 = D.H;
     return g;
   }
+  // Weight gradients with few output tiles cut their token reduction into
+  // slices (tensor-core path); the slices land in A_KPART and job_ksplit_sum
+  // adds them in slice order.
+  __device__ void split(GemmDesc& g) const {
+    const int ks = ksplit_of(a, g.M, g.N, g.K);
+    if (ks <= 1) return;
+    g.ksplit = ks;
+    g.out = abuf<float>(a, A_KPART); g.out1 = nullptr; g.osplit = 0;
+    g.ldo = g.N; g.oseg = (long long)g.M * g.N; g.accumulate = 0;
+  }
   __device__ GemmDesc wo_wgrad(int l) const {
     GemmDesc g = base(D.d, D.hq, D.T, EPI_GRAD);
     g.A = opnd(abuf<OP>(a, A_DXO), D.d, 1); g.A.map0 = MAP_DXO;
     g.B = opnd(abuf<OP>(a, A_O) + (long long)l * D.T * D.hq, D.hq, 1);
     g.B.map0 = MAP_O; g.B.y0 = l * D.T;
     g.out = pgrad(a, P_WO) + (long long)l * D.d * D.hq; g.ldo = D.hq; g.accumulate = a.micro_index > 0;
+    split(g);
     return g;
   }
   __device__ GemmDesc qkv_dgrad(int l) const {
@@ -961,9 +1034,29 @@ struct Gemms {
     g.B = opnd(abuf<OP>(a, A_R) + (long long)l * D.T * D.d, D.d, 1);
     g.B.map0 = MAP_R; g.B.y0 = l * D.T;
     g.out = pgrad(a, P_WQKV) + (long long)l * 3 * D.hq * D.d; g.ldo = D.d; g.accumulate = a.micro_index > 0;
+    split(g);
     return g;
   }
 };
+
+// out[i] (+)= sum over slices s (in order) of KPART[s][i], i < M*N.
+static __device__ void job_ksplit_sum(const KArgs& a, float* out, int M, int N, Sched& s) {
+  const int ks = ksplit_of(a, M, N, a.D.T);
+  if (ks <= 1) return;
+  const float4* P = reinterpret_cast<const float4*>(abuf<float>(a, A_KPART));
+  float4* o = reinterpret_cast<float4*>(out);
+  const long long n4 = (long long)M * N / 4;
+  const bool acc = a.micro_index > 0;
+  for (long long i = (long long)s.first() * MT_THREADS + threadIdx.x; i < n4; i += (long long)s.G * MT_THREADS) {
+    float4 v = acc ? o[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < ks; ++k) {
+      const float4 p = P[(long long)k * n4 + i];
+      v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
+    }
+    o[i] = v;
+  }
+  s.next(s.G);
+}
 
 template <class OP>
 __device__ __forceinline__ void run_gemm(const KArgs& a, const GemmDesc& g, Sched& s, char* smem, TcState& tc) {
@@ -1038,105 +1131,121 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   int phase = 0;
   Gemms<OP> gm(a);
   const bool stall = (a.flags & MT_FLAG_TEST_STALL) && blockIdx.x == 0;
+  // per-job trace: (end time, job id) pairs in the second half of the CTA's trace
+  int nj = 0;
+  auto TJ = [&](int id) {
+    if (tr) {
+      __syncthreads();
+      if (threadIdx.x == 0 && nj < MT_MAX_PHASES / 2) {
+        tr[MT_MAX_PHASES + 2 * nj] = (long long)globaltimer();
+        tr[MT_MAX_PHASES + 2 * nj + 1] = id;
+      }
+      ++nj;
+    }
+  };
 
 #define MT_SYNC()                                                                                      \
   do {                                                                                                 \
-    if (!grid_barrier(hdr, G, a.timeout_ns, (tr && phase < MT_MAX_PHASES) ? tr + 2 * phase : nullptr, \
+    if (!grid_barrier(hdr, G, a.timeout_ns, (tr && phase < MT_MAX_PHASES / 2) ? tr + 2 * phase : nullptr, \
                       stall))                                                                          \
       return;                                                                                          \
     ++phase;                                                                                           \
+    TJ(0);                                                                                             \
   } while (0)
 
   // ---------------- forward ----------------
-  job_embed<OP>(a, s);
+  job_embed<OP>(a, s); TJ(1);
   MT_SYNC();
   for (int l = 0; l < D.L; ++l) {
-    run_gemm<OP>(a, gm.qkv(l), s, smem, tc);
+    run_gemm<OP>(a, gm.qkv(l), s, smem, tc); TJ(2);
     MT_SYNC();
-    run_attn_fwd<OP>(a, l, s, smem);
+    run_attn_fwd<OP>(a, l, s, smem); TJ(3);
     MT_SYNC();
-    run_gemm<OP>(a, gm.wo(l), s, smem, tc);
+    run_gemm<OP>(a, gm.wo(l), s, smem, tc); TJ(4);
     MT_SYNC();
-    job_router<OP>(a, l, (float*)smem);
+    job_router<OP>(a, l, (float*)smem); TJ(5);
     MT_SYNC();
-    job_route<OP>(a, l, (int*)smem);
+    job_route<OP>(a, l, (int*)smem); TJ(6);
     MT_SYNC();
-    run_gemm<OP>(a, gm.gateup(l), s, smem, tc);
+    run_gemm<OP>(a, gm.gateup(l), s, smem, tc); TJ(7);
     MT_SYNC();
-    run_gemm<OP>(a, gm.down(l), s, smem, tc);
+    run_gemm<OP>(a, gm.down(l), s, smem, tc); TJ(8);
     MT_SYNC();
-    job_combine<OP>(a, l, s);
+    job_combine<OP>(a, l, s); TJ(9);
     MT_SYNC();
   }
-  run_gemm<OP>(a, gm.lm(), s, smem, tc);
+  run_gemm<OP>(a, gm.lm(), s, smem, tc); TJ(10);
   MT_SYNC();
-  job_ce<OP>(a, s);
+  job_ce<OP>(a, s); TJ(11);
   MT_SYNC();
 
   // ---------------- backward ----------------
-  job_loss(a);
-  run_gemm<OP>(a, gm.lm_dgrad(), s, smem, tc);
-  run_gemm<OP>(a, gm.lm_wgrad(), s, smem, tc);
+  job_loss(a); TJ(12);
+  run_gemm<OP>(a, gm.lm_dgrad(), s, smem, tc); TJ(13);
+  run_gemm<OP>(a, gm.lm_wgrad(), s, smem, tc); TJ(14);
   MT_SYNC();
-  job_final_norm_bwd<OP>(a, s);
+  job_final_norm_bwd<OP>(a, s); TJ(15);
   MT_SYNC();
   {
     // final-norm gain partials (DRF stays valid until the next LM-head use)
     ColArgs c{COL_GAIN, abuf<float>(a, A_DRF), abuf<float>(a, A_X) + (long long)D.L * D.T * D.d,
               abuf<float>(a, A_INVF), nullptr, nullptr, D.E + 1};
-    job_colpart(a, c, s, (float*)smem);
+    job_colpart(a, c, s, (float*)smem); TJ(16);
   }
   for (int l = D.L - 1; l >= 0; --l) {
-    job_moe_bwd1<OP>(a, l, s);
+    job_moe_bwd1<OP>(a, l, s); TJ(17);
     if (l < D.L - 1) {
       // attention-norm gain partials of layer l+1 (DR of layer l+1 is still live)
       ColArgs c{COL_GAIN, abuf<float>(a, A_DR), abuf<float>(a, A_X) + (long long)(l + 1) * D.T * D.d,
                 abuf<float>(a, A_INV1) + (long long)(l + 1) * D.T, nullptr, nullptr, D.E + 1};
-      job_colpart(a, c, s, (float*)smem);
+      job_colpart(a, c, s, (float*)smem); TJ(16);
     }
     MT_SYNC();
     if (l == D.L - 1) job_colfinal(a, D.E + 1, 1, pgrad(a, P_FINAL_NORM), nullptr, 0, s);
     else job_colfinal(a, D.E + 1, 1, pgrad(a, P_ATTN_NORM) + (long long)(l + 1) * D.d, nullptr, 0, s);
-    run_gemm<OP>(a, gm.down_dgrad(l), s, smem, tc);
-    run_gemm<OP>(a, gm.down_wgrad(l), s, smem, tc);
+    TJ(18);
+    run_gemm<OP>(a, gm.down_dgrad(l), s, smem, tc); TJ(19);
+    run_gemm<OP>(a, gm.down_wgrad(l), s, smem, tc); TJ(20);
     MT_SYNC();
-    run_gemm<OP>(a, gm.gateup_dgrad(l), s, smem, tc);
-    run_gemm<OP>(a, gm.gateup_wgrad(l), s, smem, tc);
+    run_gemm<OP>(a, gm.gateup_dgrad(l), s, smem, tc); TJ(21);
+    run_gemm<OP>(a, gm.gateup_wgrad(l), s, smem, tc); TJ(22);
     MT_SYNC();
-    job_moe_bwd2<OP>(a, l, s);
+    job_moe_bwd2<OP>(a, l, s); TJ(23);
     MT_SYNC();
     {
       ColArgs c{COL_MOE, abuf<float>(a, A_DR2), abuf<float>(a, A_XM) + (long long)l * D.T * D.d,
                 abuf<float>(a, A_INV2) + (long long)l * D.T, pmaster(a, P_MOE_NORM) + (long long)l * D.d,
                 abuf<float>(a, A_DZ), 0};
-      job_colpart(a, c, s, (float*)smem);
+      job_colpart(a, c, s, (float*)smem); TJ(16);
     }
-    run_gemm<OP>(a, gm.wo_dgrad(l), s, smem, tc);
-    run_gemm<OP>(a, gm.wo_wgrad(l), s, smem, tc);
+    run_gemm<OP>(a, gm.wo_dgrad(l), s, smem, tc); TJ(24);
+    run_gemm<OP>(a, gm.wo_wgrad(l), s, smem, tc); TJ(25);
     MT_SYNC();
     job_colfinal(a, 0, D.E + 1, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d,
-                 pgrad(a, P_MOE_NORM) + (long long)l * D.d, 1, s);
-    run_attn_bwd<OP>(a, l, s, smem);
+                 pgrad(a, P_MOE_NORM) + (long long)l * D.d, 1, s); TJ(18);
+    job_ksplit_sum(a, pgrad(a, P_WO) + (long long)l * D.d * D.hq, D.d, D.hq, s); TJ(32);
+    run_attn_bwd<OP>(a, l, s, smem); TJ(26);
     MT_SYNC();
-    run_gemm<OP>(a, gm.qkv_dgrad(l), s, smem, tc);
-    run_gemm<OP>(a, gm.qkv_wgrad(l), s, smem, tc);
+    run_gemm<OP>(a, gm.qkv_dgrad(l), s, smem, tc); TJ(27);
+    run_gemm<OP>(a, gm.qkv_wgrad(l), s, smem, tc); TJ(28);
     MT_SYNC();
-    job_attn_norm_bwd<OP>(a, l, s);
+    job_attn_norm_bwd<OP>(a, l, s); TJ(29);
+    job_ksplit_sum(a, pgrad(a, P_WQKV) + (long long)l * 3 * D.hq * D.d, 3 * D.hq, D.d, s); TJ(33);
     MT_SYNC();
   }
   {
     ColArgs c{COL_GAIN, abuf<float>(a, A_DR), abuf<float>(a, A_X), abuf<float>(a, A_INV1), nullptr,
               nullptr, D.E + 1};
-    job_colpart(a, c, s, (float*)smem);
+    job_colpart(a, c, s, (float*)smem); TJ(16);
   }
-  job_embed_bwd(a, (int*)smem);
+  job_embed_bwd(a, (int*)smem); TJ(30);
   MT_SYNC();
-  job_colfinal(a, D.E + 1, 1, pgrad(a, P_ATTN_NORM), nullptr, 0, s);
+  job_colfinal(a, D.E + 1, 1, pgrad(a, P_ATTN_NORM), nullptr, 0, s); TJ(18);
 
   // ---------------- optimizer (last microbatch) ----------------
   if (a.run_opt) {
     MT_SYNC();
-    job_norm_partial(a, (double*)smem);
+    job_norm_partial(a, (double*)smem); TJ(31);
     MT_SYNC();
     job_adamw<OP>(a);
   }
@@ -1159,6 +1268,7 @@ __device__ void run_debug_gemm(const KArgs& a, char* smem, TcState& tc, Sched& s
   g.out = a.dbg_c; g.out1 = nullptr; g.out2 = nullptr; g.ldo = g.N; g.ldo2 = 0; g.osplit = 0;
   g.oseg = (long long)g.M * g.N; g.aux = nullptr; g.ldaux = 0; g.accumulate = 0;
   g.F = 0; g.S = 1; g.hd = 64; g.hq = 0; g.rope = nullptr;
+  g.tok = nullptr; g.cepart = nullptr; g.cetgt = nullptr; g.ceparts = 0; g.ksplit = 1;
   GOperand A, B;
   A.p0 = a.dbg_a; A.p1 = nullptr; A.mn = a.dbg_a_mn; A.ld = A.mn ? g.M : g.K; A.seg = 0; A.two = 0;
   A.split = 0; A.map0 = MAP_R; A.map1 = -1; A.y0 = 0; A.yseg = 0;

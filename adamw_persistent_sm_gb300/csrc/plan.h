@@ -44,8 +44,9 @@ enum ArenaId {
   A_Y,         // fp32 [L][Pmax][d] expert outputs
   A_RF,        // op   [T][d] final RMSNorm output
   A_INVF,      // fp32 [T]
-  A_LOGITS,    // fp32 [T][V]
-  A_DLOGITS,   // op   [T][V]
+  A_CEPART,    // fp32 [T][ceil(V/128)][2] per column tile (max, sum exp(l - max)) of the logits
+  A_CETGT,     // fp32 [T] logit of the target token
+  A_DLOGITS,   // op   [T][V] logits from the LM head, overwritten in place by dlogits
   A_TOKLOSS,   // fp32 [T]
   A_DX,        // fp32 [T][d] gradient wrt the residual stream
   A_DXO,       // op   [T][d] operand copy of A_DX
@@ -59,7 +60,8 @@ enum ArenaId {
   A_DQKV,      // op   [T][3hq] gradient wrt q,k,v (before RoPE)
   A_DR,        // fp32 [T][d] gradient wrt attention RMSNorm output
   A_DRF,       // fp32 [T][d] gradient wrt final RMSNorm output
-  A_PART,      // fp32 [NCH][E+1][d] column-reduction partials
+  A_PART,      // fp32 [NCH][E+2][d] column-reduction partials
+  A_KPART,     // fp32 [<= 8 x 3hq x d] split-K partial tiles of weight gradients
   A_NORMPART,  // fp32 [NCH] squared-norm partials (double precision accumulate)
   A_TRACE,     // i64  [NCH][MAXPH][2]
   A_COUNT

@@ -169,7 +169,8 @@ enum {
   MT_VIEW_TOK_LOSS = 5,       /* fp32 [T] coef * CE per position */
   MT_VIEW_TRACE = 6,          /* int64 [n_ctas, n_phases, 2] (t_arrive, t_leave) ns */
   MT_VIEW_HIDDEN = 7,         /* fp32 [T, d] residual stream entering `layer` (layer = L: final) */
-  MT_VIEW_LOGITS = 8          /* fp32 [T, V] */
+  MT_VIEW_LOGITS = 8          /* operand type [T, V]: LM-head logits (bf16 or fp32), overwritten
+                                 in place by dlogits during the same launch */
 };
 typedef struct mt_view {
   void* ptr;
