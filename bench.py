@@ -310,6 +310,83 @@ def run_ours(args, cfg, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# profiling helpers
+# ---------------------------------------------------------------------------
+JOB_NAMES = {0: "barrier wait", 1: "embed", 2: "qkv", 3: "attn_fwd", 4: "wo", 5: "router", 6: "route",
+             7: "gateup", 8: "down", 9: "combine", 10: "lm_head", 11: "ce", 12: "loss", 13: "lm_dgrad",
+             14: "lm_wgrad", 15: "final_norm_bwd", 16: "colpart", 17: "moe_bwd1", 18: "colfinal",
+             19: "down_dgrad", 20: "down_wgrad", 21: "gateup_dgrad", 22: "gateup_wgrad", 23: "moe_bwd2",
+             24: "wo_dgrad", 25: "wo_wgrad", 26: "attn_bwd", 27: "qkv_dgrad", 28: "qkv_wgrad",
+             29: "attn_norm_bwd", 30: "embed_bwd", 31: "norm_partial", 32: "wo_ksum", 33: "qkv_ksum"}
+
+
+def run_trace(args, cfg):
+    """Per-job time of one update from the in-kernel trace (MT_FLAG_TRACE):
+    each CTA stamps the end of every job; a job's time is the gap to the
+    previous stamp.  The first 256 stamps of the update are kept."""
+    import torch
+    from adamw_persistent_sm_gb300 import binding as B
+    from adamw_persistent_sm_gb300.trainer import MoETrainer
+    tr = MoETrainer(cfg, "cuda:0", flags=B.MT_FLAG_TRACE)
+    tr.load_params(mi.make_params(cfg))
+    toks = [torch.as_tensor(t).cuda() for t in mi.make_update_tokens(cfg)]
+    for it in range(max(1, args.warmup)):
+        tr.update(toks, step=it + 1)
+    out = tr.outputs()
+    assert out.status == B.MT_OK, B.status_string(out.status)
+    tv = tr.debug_view(B.MT_VIEW_TRACE, 0, torch.int64).cpu().numpy().reshape(-1, 1024)[:out.n_ctas]
+    jobs = tv[:, 512:].reshape(out.n_ctas, 256, 2)
+    nj = int((jobs[0, :, 0] > 0).sum())
+    t = jobs[:, :nj, 0].astype(np.float64)
+    ids = jobs[0, :nj, 1]
+    dur = np.diff(t, axis=1)
+    mean, mx = {}, {}
+    for j in range(1, nj):
+        k = JOB_NAMES.get(int(ids[j]), str(int(ids[j])))
+        mean[k] = mean.get(k, 0.0) + dur[:, j - 1].mean() / 1e6
+        mx[k] = mx.get(k, 0.0) + dur[:, j - 1].max() / 1e6
+    print(f"{args.config}: {nj} job stamps over {(t[:, -1] - t[:, 0]).mean() / 1e6:.2f} ms "
+          f"({out.n_phases} grid barriers, {out.n_ctas} CTAs)")
+    print(f"  {'job':16s} {'mean ms':>9s} {'max-over-CTAs ms':>18s}")
+    for k in sorted(mx, key=lambda k: -mx[k]):
+        print(f"  {k:16s} {mean[k]:9.3f} {mx[k]:18.3f}")
+
+
+def run_product(args):
+    """One matrix product C = A B^T through the megakernel's product engine
+    (mt_debug_gemm): --product M N K a_mn b_mn."""
+    import torch
+    from adamw_persistent_sm_gb300 import binding as B
+    M, N, K, amn, bmn = args.product
+    B.load(build_if_missing=True)
+    arena = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    B.mt_arena_init(arena.data_ptr(), arena.numel())
+    st = torch.cuda.current_stream().cuda_stream
+    A = (torch.randn(K, M, device="cuda") if amn else torch.randn(M, K, device="cuda")).bfloat16()
+    Bm = (torch.randn(K, N, device="cuda") if bmn else torch.randn(N, K, device="cuda")).bfloat16()
+    C = torch.empty(M, N, device="cuda")
+
+    def once():
+        r = B.mt_debug_gemm(A.data_ptr(), amn, Bm.data_ptr(), bmn, C.data_ptr(), M, N, K, 0, 0, 0,
+                            B.MT_PREC_BF16, 1, arena.data_ptr(), arena.numel(), st)
+        assert r == B.MT_OK, B.status_string(r)
+
+    for _ in range(args.warmup):
+        once()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        once()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / max(1, args.steps)
+    o = B.mt_read_outputs(arena.data_ptr(), st)
+    assert o.status == B.MT_OK
+    print(json.dumps({"product": [M, N, K, amn, bmn], "ms": ms, "tflops": 2.0 * M * N * K / ms / 1e9}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -321,8 +398,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--ref-tokens", type=int, default=256)
+    ap.add_argument("--trace", action="store_true", help="print the per-job time of one update")
+    ap.add_argument("--product", type=int, nargs=5, metavar=("M", "N", "K", "A_MN", "B_MN"),
+                    help="time one product through the tensor-core engine")
     args = ap.parse_args()
     cfg = mi.get_config(args.config)
+    if args.product:
+        run_product(args)
+        return
+    if args.trace:
+        run_trace(args, cfg)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
