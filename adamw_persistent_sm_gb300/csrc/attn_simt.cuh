@@ -272,7 +272,7 @@ __device__ void attn_bwd_dq_item(const AttnArgs& a, int b, int h, int qb, float*
 }
 
 template <class OP, int HD>
-__device__ void attn_fwd_job(const AttnArgs& a, Sched& s, float* sm) {
+__device__ __noinline__ void attn_fwd_job(const AttnArgs& a, Sched& s, float* sm) {
   const int nqb = (a.S + AT_B - 1) / AT_B;
   const int items = a.B * a.H * nqb;
   for (int it = s.first(); it < items; it += s.G) {
@@ -284,7 +284,7 @@ __device__ void attn_fwd_job(const AttnArgs& a, Sched& s, float* sm) {
 }
 
 template <class OP, int HD>
-__device__ void attn_bwd_job(const AttnArgs& a, Sched& s, float* sm) {
+__device__ __noinline__ void attn_bwd_job(const AttnArgs& a, Sched& s, float* sm) {
   const int nqb = (a.S + AT_B - 1) / AT_B;
   const int per = a.B * a.H * nqb;
   const int items = 2 * per;

@@ -317,7 +317,7 @@ __device__ __forceinline__ int gemm_items(const GemmDesc& g, int bm, int bn) {
 }
 
 template <class OP>
-__device__ void gemm_simt_job(const GemmDesc& g, Sched& s, float* sm) {
+__device__ __noinline__ void gemm_simt_job(const GemmDesc& g, Sched& s, float* sm) {
   const int nt = (g.N + SG_BN - 1) / SG_BN;
   const int items = gemm_items(g, SG_BM, SG_BN);
   for (int it = s.first(); it < items; it += s.G) {

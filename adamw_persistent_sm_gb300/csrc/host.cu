@@ -43,10 +43,10 @@ int check_hparams(const mt_hparams* hp) {
       hp->top_k > hp->n_experts)
     return MT_ERR_UNSUPPORTED;
   if (hp->head_dim != 16 && hp->head_dim != 64) return MT_ERR_UNSUPPORTED;
-  if (hp->d_model % 32 != 0 || hp->d_model > 2048) return MT_ERR_UNSUPPORTED;
+  if (hp->d_model % 32 != 0 || hp->d_model > 768) return MT_ERR_UNSUPPORTED;
   if (hp->d_ff % 64 != 0) return MT_ERR_UNSUPPORTED;
   if (hp->seq < 2) return MT_ERR_UNSUPPORTED;
-  if (hp->vocab % 4 != 0) return MT_ERR_UNSUPPORTED;
+  if (hp->vocab % 8 != 0) return MT_ERR_UNSUPPORTED;
   if ((long long)hp->n_experts * hp->d_model * 4 > 160 * 1024) return MT_ERR_UNSUPPORTED;  // router staged in smem
   const long long T = (long long)hp->batch * hp->seq;
   if (T * hp->top_k + (long long)hp->n_experts * MT_TILE_M > (1LL << 30)) return MT_ERR_UNSUPPORTED;

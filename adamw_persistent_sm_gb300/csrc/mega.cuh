@@ -70,7 +70,7 @@ __device__ __forceinline__ float warp_rms_inv(const float* x, int d, float eps) 
 // Rotary table (angles in double precision) and x0 = emb[tok], plus the
 // first layer's attention RMSNorm.
 template <class OP>
-__device__ void job_embed(const KArgs& a, Sched& s) {
+__device__ __noinline__ void job_embed(const KArgs& a, Sched& s) {
   const MtDims& D = a.D;
   const int half = D.hd / 2;
   float* rope = abuf<float>(a, A_ROPE);
@@ -126,7 +126,7 @@ __device__ __forceinline__ void warp_argmax(float& v, int& idx) {
 // top-k compares these fp32 logits (softmax is monotone), ties going to the
 // lower expert index.
 template <class OP>
-__device__ void job_router(const KArgs& a, int l, float* sm) {
+__device__ __noinline__ void job_router(const KArgs& a, int l, float* sm) {
   const MtDims& D = a.D;
   const int c = blockIdx.x, G = gridDim.x;
   const int ch = chunk_len(D, G);
@@ -158,11 +158,43 @@ __device__ void job_router(const KArgs& a, int l, float* sm) {
     row_st_op(R2 + (long long)t * D.d, r, n4);
     if (lane == 0) inv2[t] = inv;
     float z0 = -INFINITY, z1 = -INFINITY;   // experts lane and lane + 32
-    for (int e = 0; e < D.E; ++e) {
-      row_ld(w, sm + (long long)e * D.d, n4);
-      const float acc = row_dot(r, w);
-      if (e == lane) z0 = acc;
-      if (e == lane + 32) z1 = acc;
+    if (D.E <= 32) {
+      // lane-partial dot products for all experts, then one transpose-reduction
+      float p[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        float acc = 0.f;
+        if (e < D.E) {
+          row_ld(w, sm + (long long)e * D.d, n4);
+#pragma unroll
+          for (int i = 0; i < NC; ++i) {
+            acc = fmaf(r.v[i].x, w.v[i].x, acc);
+            acc = fmaf(r.v[i].y, w.v[i].y, acc);
+            acc = fmaf(r.v[i].z, w.v[i].z, acc);
+            acc = fmaf(r.v[i].w, w.v[i].w, acc);
+          }
+        }
+        p[e] = acc;
+      }
+      // after the step with offset o, lane l holds sums for the experts whose bit o matches l's bit o
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int e = 0; e < o; ++e) {
+          const float send = upper ? p[e] : p[e + o];
+          const float keep = upper ? p[e + o] : p[e];
+          p[e] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      if (lane < D.E) z0 = p[0];
+    } else {
+      for (int e = 0; e < D.E; ++e) {
+        row_ld(w, sm + (long long)e * D.d, n4);
+        const float acc = row_dot(r, w);
+        if (e == lane) z0 = acc;
+        if (e == lane + 32) z1 = acc;
+      }
     }
     if (lane < D.E) Z[(long long)t * D.E + lane] = z0;
     if (lane + 32 < D.E) Z[(long long)t * D.E + lane + 32] = z1;
@@ -208,7 +240,7 @@ __device__ void job_router(const KArgs& a, int l, float* sm) {
 // fused with the dispatch gather of the expert inputs.  Within an expert,
 // assignments keep ascending a = t*K + k.
 template <class OP>
-__device__ void job_route(const KArgs& a, int l, int* ism) {
+__device__ __noinline__ void job_route(const KArgs& a, int l, int* ism) {
   const MtDims& D = a.D;
   const int c = blockIdx.x, G = gridDim.x;
   const int ch = chunk_len(D, G);
@@ -225,10 +257,13 @@ __device__ void job_route(const KArgs& a, int l, int* ism) {
   int* s_tot = ism;                 // [E]
   int* s_base = ism + 64;           // [E]
   int* s_offs = ism + 128;          // [E+1]
+  int* s_cnt = ism + 256;           // [nused][E] chunk counts
+  for (int i = threadIdx.x; i < nused * D.E; i += MT_THREADS) s_cnt[i] = CNT[i];
+  __syncthreads();
   for (int e = threadIdx.x; e < D.E; e += MT_THREADS) {
     int tot = 0, before = 0;
     for (int cc = 0; cc < nused; ++cc) {
-      const int n = CNT[(long long)cc * D.E + e];
+      const int n = s_cnt[cc * D.E + e];
       tot += n;
       if (cc < c) before += n;
     }
@@ -295,7 +330,7 @@ __device__ void job_route(const KArgs& a, int l, int* ism) {
 // x_{l+1} = x_mid + sum_k w_k y_k (fixed slot order), then the next
 // RMSNorm (attention norm of layer l+1, or the final norm).
 template <class OP>
-__device__ void job_combine(const KArgs& a, int l, Sched& s) {
+__device__ __noinline__ void job_combine(const KArgs& a, int l, Sched& s) {
   const MtDims& D = a.D;
   const int lane = threadIdx.x & 31, n4 = D.d / 4;
   const float* XM = abuf<float>(a, A_XM) + (long long)l * D.T * D.d;
@@ -354,7 +389,7 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
   *reinterpret_cast<uint2*>(p) = u;
 }
 template <class OP>
-__device__ void job_ce(const KArgs& a, Sched& s) {
+__device__ __noinline__ void job_ce(const KArgs& a, Sched& s) {
   const MtDims& D = a.D;
   const int lane = threadIdx.x & 31;
   OP* DL = abuf<OP>(a, A_DLOGITS);
@@ -363,7 +398,7 @@ __device__ void job_ce(const KArgs& a, Sched& s) {
   float* TL = abuf<float>(a, A_TOKLOSS);
   const int np = ce_parts<OP>(a);
   const int nw = s.G * MT_WARPS;
-  const int v4 = D.V / 4;                 // V % 4 == 0 (checked on the host)
+  const int v4 = D.V / 4;                 // V % 8 == 0 (checked on the host)
   constexpr int U = 8;
   for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
     OP* row = DL + (long long)t * D.V;
@@ -420,7 +455,7 @@ __device__ void job_ce(const KArgs& a, Sched& s) {
 // ===========================================================================
 // dx = d(final RMSNorm) from d rf.
 template <class OP>
-__device__ void job_final_norm_bwd(const KArgs& a, Sched& s) {
+__device__ __noinline__ void job_final_norm_bwd(const KArgs& a, Sched& s) {
   const MtDims& D = a.D;
   const float* DRF = abuf<float>(a, A_DRF);
   const float* X = abuf<float>(a, A_X) + (long long)D.L * D.T * D.d;
@@ -446,7 +481,7 @@ __device__ void job_final_norm_bwd(const KArgs& a, Sched& s) {
 // experts (the renormalised weights are the softmax of the chosen logits),
 // and zero pad rows of dY.
 template <class OP>
-__device__ void job_moe_bwd1(const KArgs& a, int l, Sched& s) {
+__device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s) {
   const MtDims& D = a.D;
   const int lane = threadIdx.x & 31, n4 = D.d / 4;
   const float* DX = abuf<float>(a, A_DX);
@@ -498,7 +533,7 @@ __device__ void job_moe_bwd1(const KArgs& a, int l, Sched& s) {
 // atomics - "Open problems", Performance item 5), plus the router term
 // dz Wr, then the expert RMSNorm backward into dx, and the operand copy of dx.
 template <class OP>
-__device__ void job_moe_bwd2(const KArgs& a, int l, Sched& s) {
+__device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s) {
   const MtDims& D = a.D;
   const int n4 = D.d / 4;
   const float* DXS = abuf<float>(a, A_DXS);
@@ -543,7 +578,7 @@ __device__ void job_moe_bwd2(const KArgs& a, int l, Sched& s) {
 
 // Attention RMSNorm backward into dx.
 template <class OP>
-__device__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s) {
+__device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s) {
   const MtDims& D = a.D;
   const float* DR = abuf<float>(a, A_DR);
   const float* X = abuf<float>(a, A_X) + (long long)l * D.T * D.d;
@@ -659,7 +694,7 @@ __device__ void colpart_items(const KArgs& a, const ColArgs& c, Sched& s, float*
   s.next(items);
 }
 
-static __device__ void job_colpart(const KArgs& a, const ColArgs& c, Sched& s, float* sm) {
+static __device__ __noinline__ void job_colpart(const KArgs& a, const ColArgs& c, Sched& s, float* sm) {
   const int E = (c.kind == COL_MOE) ? a.D.E : 0;
   if (E == 0) colpart_items<0>(a, c, s, sm);
   else if (E <= 4) colpart_items<4>(a, c, s, sm);
@@ -669,7 +704,7 @@ static __device__ void job_colpart(const KArgs& a, const ColArgs& c, Sched& s, f
 }
 
 // out[r][col] (+)= sum over chunks of PART[chunk][row0 + r][col].
-static __device__ void job_colfinal(const KArgs& a, int row0, int nrows, float* out_rows, float* out_last,
+static __device__ __noinline__ void job_colfinal(const KArgs& a, int row0, int nrows, float* out_rows, float* out_last,
                                     int last_is_separate, Sched& s) {
   const MtDims& D = a.D;
   const int G = s.G;
@@ -691,7 +726,7 @@ static __device__ void job_colfinal(const KArgs& a, int row0, int nrows, float* 
 // embedding backward: dE[v] (+)= sum over positions t with tok[t] = v of dx_t,
 // in ascending t.  CTA c owns vocabulary rows [c*V/G, (c+1)*V/G).
 // ===========================================================================
-static __device__ void job_embed_bwd(const KArgs& a, int* ism) {
+static __device__ __noinline__ void job_embed_bwd(const KArgs& a, int* ism) {
   const MtDims& D = a.D;
   const int c = blockIdx.x, G = gridDim.x;
   const int v0 = (int)((long long)D.V * c / G), v1 = (int)((long long)D.V * (c + 1) / G);
@@ -743,7 +778,7 @@ static __device__ void job_embed_bwd(const KArgs& a, int* ism) {
 // ===========================================================================
 // loss reduction and optimizer
 // ===========================================================================
-static __device__ void job_loss(const KArgs& a) {
+static __device__ __noinline__ void job_loss(const KArgs& a) {
   if (blockIdx.x != 0 || threadIdx.x >= 32) return;
   const MtDims& D = a.D;
   const float* TL = abuf<float>(a, A_TOKLOSS);
@@ -759,7 +794,7 @@ static __device__ void job_loss(const KArgs& a) {
 }
 
 // Global gradient norm, first level: CTA c sums squares over its slice.
-static __device__ void job_norm_partial(const KArgs& a, double* dsm) {
+static __device__ __noinline__ void job_norm_partial(const KArgs& a, double* dsm) {
   const int c = blockIdx.x, G = gridDim.x;
   const long long n = a.n_params;
   const long long n4 = n / 4;
@@ -804,7 +839,7 @@ __device__ __forceinline__ void adamw_elem(const KArgs& a, float c, float& p, fl
 // Clip coefficient from the ordered sum of the partials, then the AdamW sweep
 // over CTA c's slice (float4 loads; writes p, m, v and the bf16 shadow).
 template <class OP>
-__device__ void job_adamw(const KArgs& a) {
+__device__ __noinline__ void job_adamw(const KArgs& a) {
   const int c = blockIdx.x, G = gridDim.x;
   const double* parts = reinterpret_cast<const double*>(abuf<float>(a, A_NORMPART));
   double tot = 0.0;
@@ -1040,7 +1075,7 @@ struct Gemms {
 };
 
 // out[i] (+)= sum over slices s (in order) of KPART[s][i], i < M*N.
-static __device__ void job_ksplit_sum(const KArgs& a, float* out, int M, int N, Sched& s) {
+static __device__ __noinline__ void job_ksplit_sum(const KArgs& a, float* out, int M, int N, Sched& s) {
   const int ks = ksplit_of(a, M, N, a.D.T);
   if (ks <= 1) return;
   const float4* P = reinterpret_cast<const float4*>(abuf<float>(a, A_KPART));

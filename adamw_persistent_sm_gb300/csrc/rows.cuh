@@ -4,7 +4,7 @@
 // used, so each warp keeps several 16-byte loads in flight per lane.
 //
 // NC is the number of chunks per lane (d/4/32 rounded up); the jobs are
-// instantiated for NC in {1, 6, 16} and dispatched on d.
+// instantiated for NC in {1, 6} (d <= 128 and d <= 768) and dispatched on d.
 #pragma once
 #include "common.cuh"
 
@@ -138,11 +138,11 @@ __device__ __forceinline__ float row_rms_inv(const Row<NC>& x, int d, float eps)
   return 1.0f / sqrtf(row_dot(x, x) / (float)d + eps);
 }
 
-// Run f(integral_constant<int, NC>) with the NC that covers d.
+// Run f(integral_constant<int, NC>) with the NC that covers d (d <= 768,
+// checked on the host: six rows of NC = 6 chunks still fit in registers).
 template <class F>
 __device__ __forceinline__ void with_nc(int d, F&& f) {
   const int n4 = d / 4;
   if (n4 <= 32) f(std::integral_constant<int, 1>());
-  else if (n4 <= 192) f(std::integral_constant<int, 6>());
-  else f(std::integral_constant<int, 16>());
+  else f(std::integral_constant<int, 6>());
 }

@@ -67,6 +67,12 @@ enum {
  * copied at call time).  Model: vocab V, d_model d, n_layers L, n_heads H of
  * head_dim hd (H*hd may differ from d), n_experts E, top_k K, expert width
  * d_ff F; this microbatch holds batch x seq tokens.
+ * Implemented shapes (else MT_ERR_UNSUPPORTED): d a multiple of 32 and at
+ * most 768; hd 16 or 64; F a multiple of 64; E <= 64 with E*d*4 <= 160 KiB;
+ * K <= min(8, E); V a multiple of 8; L <= 16; seq >= 2.  The tensor-core
+ * path (bf16) additionally needs batch*seq a multiple of 128, d, H*hd, V and
+ * F multiples of 256, and hd = 64; attention on tensor cores needs seq a
+ * multiple of 128.
  */
 typedef struct mt_hparams {
   int32_t vocab, d_model, n_layers, n_heads, head_dim, n_experts, top_k, d_ff;

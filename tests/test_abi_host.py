@@ -75,6 +75,7 @@ def _bad(cfg, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(vocab=0), B.MT_ERR_ARG),
     (dict(head_dim=32), B.MT_ERR_UNSUPPORTED),
+    (dict(d_model=1024), B.MT_ERR_UNSUPPORTED),
     (dict(top_k=9, n_experts=16), B.MT_ERR_UNSUPPORTED),
     (dict(n_experts=65), B.MT_ERR_UNSUPPORTED),
     (dict(d_ff=100), B.MT_ERR_UNSUPPORTED),
