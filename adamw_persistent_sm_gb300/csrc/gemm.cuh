@@ -23,6 +23,7 @@ enum EpiKind {
   EPI_GRAD,           // out(f32) = acc (+ out if accumulate); rows >= osplit go to out1
   EPI_STORE_OP_D,     // out(op) = acc, and out2(f32)[m][head] = sum over the head's 64 columns of
                       // op(acc) * aux(op)  (attention's D = rowsum(dO * O))
+  EPI_NONE,           // test harness: accumulators are read and dropped
   EPI_LOGITS          // out(op) = acc (LM-head logits); per row and column tile, (max, sum exp(acc -
                       // max)) into cepart[m][n0 / tile width]; the target token's fp32 logit into cetgt[m]
 };

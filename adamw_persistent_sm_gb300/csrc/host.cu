@@ -369,7 +369,9 @@ int32_t mt_debug_gemm(const void* A, int32_t a_mn, const void* B, int32_t b_mn, 
   if (rag == 1 && a_mn) return MT_ERR_ARG;
   if (rag == 2 && !(a_mn && b_mn)) return MT_ERR_ARG;
   const bool bf16 = precision == MT_PREC_BF16;
-  const bool tc = bf16 && use_tc && MT_TC_AVAILABLE;
+  const bool tc = bf16 && (use_tc & 1) && MT_TC_AVAILABLE;
+  const int out_mode = tc ? ((use_tc >> 1) & 3) : 0;     // use_tc bits 1-2: output mode (tensor cores only)
+  if (out_mode == 3) return MT_ERR_ARG;
   if (tc && (M % 128 || N % 256 || K % 64)) return MT_ERR_UNSUPPORTED;
   if (tc && (!aligned(A, 16) || !aligned(B, 16))) return MT_ERR_ARG;
   const size_t smem = tc ? (size_t)MT_TC_SMEM : (size_t)SG_BM * SG_CPAD * 4;
@@ -384,6 +386,7 @@ int32_t mt_debug_gemm(const void* A, int32_t a_mn, const void* B, int32_t b_mn, 
   a->dbg_a = A; a->dbg_b = B; a->dbg_c = C;
   a->dbg_m = M; a->dbg_n = N; a->dbg_k = K; a->dbg_a_mn = a_mn; a->dbg_b_mn = b_mn;
   a->dbg_rag = rag; a->dbg_nseg = rag ? nseg : 0; a->dbg_offs = offs;
+  a->dbg_out_mode = out_mode;
   a->use_tc = tc ? 1 : 0;
   if (tc) {
     const long long segs = rag == 1 ? nseg : 1;

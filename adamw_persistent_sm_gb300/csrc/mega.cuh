@@ -1299,7 +1299,8 @@ template <class OP>
 __device__ void run_debug_gemm(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   GemmDesc g;
   g.M = a.dbg_m; g.N = a.dbg_n; g.K = a.dbg_k; g.rag = a.dbg_rag; g.offs = a.dbg_offs; g.nseg = a.dbg_nseg;
-  g.epi = (g.rag == RAG_K) ? EPI_GRAD : EPI_STORE_F32;
+  g.epi = (g.rag == RAG_K) ? EPI_GRAD : (a.dbg_out_mode == 1 ? EPI_STORE_OP : EPI_STORE_F32);
+  if (a.dbg_out_mode == 2) g.epi = EPI_NONE;
   g.out = a.dbg_c; g.out1 = nullptr; g.out2 = nullptr; g.ldo = g.N; g.ldo2 = 0; g.osplit = 0;
   g.oseg = (long long)g.M * g.N; g.aux = nullptr; g.ldaux = 0; g.accumulate = 0;
   g.F = 0; g.S = 1; g.hd = 64; g.hq = 0; g.rope = nullptr;

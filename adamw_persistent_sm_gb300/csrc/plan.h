@@ -117,6 +117,7 @@ struct KArgs {
   int debug_gemm;               // test harness: run only the product described below
   const void* dbg_a; const void* dbg_b; float* dbg_c;
   int dbg_m, dbg_n, dbg_k, dbg_a_mn, dbg_b_mn, dbg_rag, dbg_nseg;
+  int dbg_out_mode;             // 0 fp32 C, 1 bf16 C (written over the fp32 buffer), 2 accumulators read only
   const int* dbg_offs;
   int use_tc;                   // tcgen05 GEMMs (bf16 only)
   int use_tc_attn;              // tensor-core attention (bf16 only)

@@ -359,6 +359,7 @@ def run_product(args):
     import torch
     from adamw_persistent_sm_gb300 import binding as B
     M, N, K, amn, bmn = args.product
+    out_mode = {"f32": 0, "bf16": 1, "none": 2}[args.product_out]
     B.load(build_if_missing=True)
     arena = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     B.mt_arena_init(arena.data_ptr(), arena.numel())
@@ -369,7 +370,7 @@ def run_product(args):
 
     def once():
         r = B.mt_debug_gemm(A.data_ptr(), amn, Bm.data_ptr(), bmn, C.data_ptr(), M, N, K, 0, 0, 0,
-                            B.MT_PREC_BF16, 1, arena.data_ptr(), arena.numel(), st)
+                            B.MT_PREC_BF16, 1 | (out_mode << 1), arena.data_ptr(), arena.numel(), st)
         assert r == B.MT_OK, B.status_string(r)
 
     for _ in range(args.warmup):
@@ -384,7 +385,8 @@ def run_product(args):
     ms = e0.elapsed_time(e1) / max(1, args.steps)
     o = B.mt_read_outputs(arena.data_ptr(), st)
     assert o.status == B.MT_OK
-    print(json.dumps({"product": [M, N, K, amn, bmn], "ms": ms, "tflops": 2.0 * M * N * K / ms / 1e9}))
+    print(json.dumps({"product": [M, N, K, amn, bmn], "out": args.product_out, "ms": ms,
+                      "tflops": 2.0 * M * N * K / ms / 1e9}))
 
 
 def main():
@@ -401,6 +403,8 @@ def main():
     ap.add_argument("--trace", action="store_true", help="print the per-job time of one update")
     ap.add_argument("--product", type=int, nargs=5, metavar=("M", "N", "K", "A_MN", "B_MN"),
                     help="time one product through the tensor-core engine")
+    ap.add_argument("--product-out", default="f32", choices=["f32", "bf16", "none"],
+                    help="output of --product: fp32, bf16, or accumulators read and dropped")
     args = ap.parse_args()
     cfg = mi.get_config(args.config)
     if args.product:
