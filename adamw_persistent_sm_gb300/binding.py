@@ -30,6 +30,7 @@ MT_FLAG_SIMT_GEMM = 1 << 1
 MT_FLAG_SIMT_ATTN = 1 << 2
 MT_FLAG_NO_OPTIMIZER = 1 << 3
 MT_FLAG_TEST_STALL = 1 << 4
+MT_FLAG_BARRIERS_ONLY = 1 << 5
 
 MT_MAX_LAYERS = 16
 MT_MAX_EXPERTS = 64
@@ -41,6 +42,9 @@ MT_VIEW_ROUTE_OFFS = 3
 MT_VIEW_ROUTE_PERM = 4
 MT_VIEW_TOK_LOSS = 5
 MT_VIEW_TRACE = 6
+MT_TRACE_PHASES = 512                 # per CTA: barrier (arrive, leave) pairs, then
+MT_TRACE_JOBS = 1024                  # (end time, job id) pairs
+MT_TRACE_WORDS = 2 * (MT_TRACE_PHASES + MT_TRACE_JOBS)
 MT_VIEW_HIDDEN = 7
 MT_VIEW_LOGITS = 8
 

@@ -412,25 +412,62 @@ static __device__ void dkdv_item(const Args& a, int b, int h, int kb, char* smem
 
 }  // namespace attn_tc
 
+// Dynamic scheduling and dependency counters of the attention jobs (all
+// null: static rotation, phases fenced by grid barriers).
+struct AttnDeps {
+  unsigned* ticket;        // item numbers are drawn from this counter
+  const unsigned* wait;    // per 128-row block of q,k,v: stored column tiles
+  unsigned wtarget;
+  unsigned* sig;           // per 128-row block of the output: +1 per stored head
+  ArenaHdr* hdr;
+  long long timeout_ns;
+};
+
+// Item number k of this CTA: a drawn ticket, or the static rotation.
+__device__ __forceinline__ int attn_next_item(const AttnDeps& dp, const Sched& s, int k) {
+  return dp.ticket ? draw_ticket(dp.ticket) : s.first() + k * s.G;
+}
+
 template <class OP>
-__device__ void attn_tc_fwd_job(const attn_tc::Args& a, Sched& s, char* smem) {
+__device__ void attn_tc_fwd_job(const attn_tc::Args& a, Sched& s, char* smem, const AttnDeps& dp) {
   const int nqb = a.S / 128;
   const int items = a.B * a.H * nqb;
-  for (int it = s.first(); it < items; it += s.G) {
-    const int qb = nqb - 1 - it / (a.B * a.H);       // longest rows first
-    const int bh = it % (a.B * a.H);
-    attn_tc::fwd_item(a, bh / a.H, bh % a.H, qb, smem);
+  for (int k = 0;; ++k) {
+    const int it = attn_next_item(dp, s, k);
+    if (it >= items) break;
+    int b, h, qb;
+    if (dp.ticket) {
+      // sequence by sequence (following the q,k,v product's row order),
+      // longest rows first within a sequence
+      b = it / (a.H * nqb);
+      const int r = it % (a.H * nqb);
+      qb = nqb - 1 - r / a.H; h = r % a.H;
+    } else {
+      // static rotation: longest rows first over the whole batch
+      qb = nqb - 1 - it / (a.B * a.H);
+      const int bh = it % (a.B * a.H);
+      b = bh / a.H; h = bh % a.H;
+    }
+    if (dp.wait) {
+      if (threadIdx.x <= qb) dep_wait(dp.hdr, dp.wait + b * nqb + threadIdx.x, dp.wtarget, dp.timeout_ns);
+      __syncthreads();
+    }
+    attn_tc::fwd_item(a, b, h, qb, smem);
     __syncthreads();
+    if (dp.sig && threadIdx.x == 0) dep_signal(dp.sig + b * nqb + qb);
   }
   s.next(items);
 }
 
 template <class OP>
-__device__ void attn_tc_bwd_job(const attn_tc::Args& a, Sched& s, char* smem) {
+__device__ void attn_tc_bwd_job(const attn_tc::Args& a, Sched& s, char* smem, const AttnDeps& dp) {
   const int nb = a.S / 128;
   const int per = a.B * a.H * nb;
   const int items = 2 * per;
-  for (int it = s.first(); it < items; it += s.G) {
+  for (int k = 0;; ++k) {
+    const int it = attn_next_item(dp, s, k);
+    if (it >= items) break;
+    // dK,dV items and dQ items alternate, longest first
     const int fam = it & 1, j = it >> 1;
     const int step = j / (a.B * a.H), bh = j % (a.B * a.H);
     if (fam == 0) attn_tc::dkdv_item(a, bh / a.H, bh % a.H, step, smem);

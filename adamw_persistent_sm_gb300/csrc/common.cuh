@@ -21,6 +21,7 @@ enum ErrSite {
   SITE_TC_ACC_EMPTY = 13,
   SITE_TC_DRAIN = 14,
   SITE_TC_ALIGN = 15,
+  SITE_DEP = 16,
   SITE_TEST_STALL = 20
 };
 
@@ -63,6 +64,42 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
+}
+
+// Bounded wait until a dependency counter reaches `target` (acquire, so the
+// producers' stores before their release are visible afterwards).  Returns
+// false at once when the status word holds an error, or after recording a
+// timeout; callers then carry on without the data (the results are void and
+// every CTA leaves at the next grid barrier).
+static __device__ __noinline__ bool dep_wait(ArenaHdr* h, const unsigned* c, unsigned target, long long timeout_ns) {
+  if (ld_acquire_gpu(c) >= target) return true;
+  const unsigned long long t0 = globaltimer();
+  unsigned ns = 32;
+  while (ld_acquire_gpu(c) < target) {
+    if (ld_volatile(&h->status) != 0) return false;
+    if ((long long)(globaltimer() - t0) > timeout_ns) {
+      set_error(h, MT_ERR_DEVICE_TIMEOUT, SITE_DEP);
+      return false;
+    }
+    __nanosleep(ns);
+    if (ns < 256) ns <<= 1;
+  }
+  return true;
+}
+// Publish a producer part: every store the calling thread has observed
+// (after a CTA or named barrier over the writers) is released with the add.
+__device__ __forceinline__ void dep_signal(unsigned* c) {
+  __threadfence();
+  atomicAdd(c, 1u);
+}
+// Next item of a dynamically scheduled job: thread 0 draws a ticket and the
+// CTA reads it after a CTA barrier.
+__device__ __forceinline__ int draw_ticket(unsigned* ticket) {
+  __shared__ int s_ticket;
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = (int)atomicAdd(ticket, 1u);
+  __syncthreads();
+  return s_ticket;
 }
 
 // Work distribution inside a phase: item i of the current job runs on CTA

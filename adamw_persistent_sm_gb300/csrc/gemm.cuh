@@ -67,6 +67,11 @@ struct GemmDesc {
   int ceparts;
   int ksplit;                                 // tensor-core path, dense products: the K range is cut
                                               // into ksplit slices, slice s writes out + s * oseg
+  // Dependency counters (tensor-core path; null where a grid barrier fences
+  // the product), one per 128-row block:
+  const unsigned* dwait; unsigned dtarget;    // A rows: wait before loading a tile's operands
+  const unsigned* dwait_aux; unsigned dtarget_aux;  // aux rows: wait before the epilogue reads aux
+  unsigned* dsig;                             // output rows: +1 per stored tile
 };
 
 // Target column of logits row m (next token), or -1 for the last position.

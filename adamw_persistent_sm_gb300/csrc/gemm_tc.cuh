@@ -540,6 +540,12 @@ __device__ __forceinline__ void tc_epilogue_empty(const EpiRegs& g, const TcTile
 // ---------------------------------------------------------------------------
 // the job
 // ---------------------------------------------------------------------------
+// All four epilogue warps have stored their rows of the tile: publish it.
+__device__ __forceinline__ void epi_signal(unsigned* c) {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  if (threadIdx.x == 128) dep_signal(c);
+}
+
 static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& g, Sched& s, char* smem, TcState& tc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
@@ -574,11 +580,19 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
       // make the generic-proxy writes of earlier phases visible to TMA reads
       asm volatile("fence.proxy.async;" ::: "memory");
       const TmaOp oa = tma_op(a, g.A), ob = tma_op(a, g.B);
+      const unsigned* dw = g.dwait;
+      const unsigned dtarget = g.dtarget;
       uint32_t it = 0;
       bool ok = true;
       for (int t = first; t < items && ok; t += G) {
         const TcTile ti = tc_tile(sh, t);
         const int bseg = (sh.rag == RAG_M) ? ti.seg * ob.yseg : 0;
+        if (dw) {
+          // the A rows of this tile come from another CTA's stores (generic
+          // proxy): acquire them, then order the TMA reads after the acquire
+          dep_wait(hdr, dw + (ti.m0 >> 7), dtarget, tmo);
+          asm volatile("fence.proxy.async;" ::: "memory");
+        }
         for (int kb = 0; kb < ti.nk; ++kb, ++it) {
           const int st = it % TC_STAGES;
           const uint32_t ph = (it / TC_STAGES) & 1;
@@ -655,27 +669,39 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
     const int q = warp - 4;
     const EpiRegs er = epi_regs(g);
     float* xst = reinterpret_cast<float*>(smem + TC_STAGE_OFF + q * TC_XPOSE_BYTES);
+    unsigned* const dsig = g.dsig;
+    const unsigned* const dwa = g.dwait_aux;
+    const unsigned dta = g.dtarget_aux;
     uint32_t tcount = 0;
+    bool dead = false;     // after a timed-out wait: skip the work, keep the named barriers paired
     for (int t = first; t < items; t += G) {
       const TcTile ti = tc_tile(sh, t);
       const int m = ti.m0 + q * 32 + lane;
+      if (dwa) {
+        if (lane == 0) dep_wait(hdr, dwa + (ti.m0 >> 7), dta, tmo);
+        __syncwarp();
+      }
       if (ti.nk == 0) {
         tc_epilogue_empty(er, ti, m);
+        if (dsig) epi_signal(dsig + (ti.m0 >> 7));
         continue;
       }
       const int ab = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
-      if (!mbar_wait(accf + 8 * ab, aph, tmo)) {
+      if (!dead && !mbar_wait(accf + 8 * ab, aph, tmo)) {
         set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_ACC_FULL);
-        break;
+        dead = true;
       }
-      __syncwarp();
-      tc_fence_after();
-      const uint32_t trow = tc.tmem_base + ab * TC_BN + ((uint32_t)(q * 32) << 16);
-      tc_epilogue(er, ti, trow, m, xst, (long long)(ti.m0 + q * 32));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce + 8 * ab);
+      if (!dead) {
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t trow = tc.tmem_base + ab * TC_BN + ((uint32_t)(q * 32) << 16);
+        tc_epilogue(er, ti, trow, m, xst, (long long)(ti.m0 + q * 32));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce + 8 * ab);
+      }
+      if (dsig) epi_signal(dsig + (ti.m0 >> 7));
       ++tcount;
     }
   }

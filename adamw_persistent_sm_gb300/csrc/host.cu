@@ -116,7 +116,8 @@ void make_plan(const mt_hparams* hp, MtPlan* P) {
   sz[A_PART] = (long long)D.nch * (D.E + 2) * d * 4;
   sz[A_KPART] = 8LL * 3 * D.hq * d * 4;
   sz[A_NORMPART] = (long long)D.nch * 8;
-  sz[A_TRACE] = (long long)D.nch * MT_MAX_PHASES * 2 * 8;
+  sz[A_DEP] = dep_words(D) * 4;
+  sz[A_TRACE] = (long long)D.nch * MT_TRACE_WORDS * 8;
   long long off = 0;
   for (int i = 0; i < A_COUNT; ++i) {
     P->aoff[i] = off;
@@ -289,6 +290,8 @@ int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m
   memcpy(a->aoff, P.aoff, sizeof(a->aoff));
   a->use_tc = want_tc ? 1 : 0;
   a->use_tc_attn = bf16 && !(hp->flags & MT_FLAG_SIMT_ATTN) && hp->head_dim == 64 && hp->seq % 128 == 0;
+  // counters need whole 128-row blocks on both sides of every hand-off
+  a->deps = a->use_tc && a->use_tc_attn && !(hp->flags & MT_FLAG_BARRIERS_ONLY);
   if (want_tc) {
     int ms = mt_build_tensor_maps(a, shadow);
     if (ms != MT_OK) { delete a; return ms; }
@@ -348,7 +351,7 @@ int32_t mt_debug_view(const void* arena, const mt_hparams* hp, int32_t which, in
     case MT_VIEW_TOK_LOSS:
       *out = {base + P.aoff[A_TOKLOSS], T, 4}; break;
     case MT_VIEW_TRACE:
-      *out = {base + P.aoff[A_TRACE], (long long)D.nch * MT_MAX_PHASES * 2, 8}; break;
+      *out = {base + P.aoff[A_TRACE], (long long)D.nch * MT_TRACE_WORDS, 8}; break;
     case MT_VIEW_HIDDEN:
       *out = {base + P.aoff[A_X] + (long long)layer * T * D.d * 4, T * D.d, 4}; break;
     case MT_VIEW_LOGITS:

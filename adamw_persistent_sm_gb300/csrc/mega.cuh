@@ -83,6 +83,11 @@ __device__ __noinline__ void job_embed(const KArgs& a, Sched& s) {
     rope[2 * e] = (float)cv;
     rope[2 * e + 1] = (float)sv;
   }
+  // dependency counters and tickets start at zero in every launch (first
+  // used after the first grid barrier)
+  unsigned* dep = abuf<unsigned>(a, A_DEP);
+  const long long ndep = dep_words(D);
+  for (long long i = (long long)me * MT_THREADS + threadIdx.x; i < ndep; i += (long long)s.G * MT_THREADS) dep[i] = 0u;
   ArenaHdr* hdr = abuf<ArenaHdr>(a, A_HDR);
   const float* emb = pmaster(a, P_EMB);
   float* X = abuf<float>(a, A_X);
@@ -126,7 +131,7 @@ __device__ __forceinline__ void warp_argmax(float& v, int& idx) {
 // top-k compares these fp32 logits (softmax is monotone), ties going to the
 // lower expert index.
 template <class OP>
-__device__ __noinline__ void job_router(const KArgs& a, int l, float* sm) {
+__device__ __noinline__ void job_router(const KArgs& a, int l, float* sm, const unsigned* dw, unsigned dtarget) {
   const MtDims& D = a.D;
   const int c = blockIdx.x, G = gridDim.x;
   const int ch = chunk_len(D, G);
@@ -145,6 +150,11 @@ __device__ __noinline__ void job_router(const KArgs& a, int l, float* sm) {
     reinterpret_cast<float4*>(sm)[i] = reinterpret_cast<const float4*>(Wr)[i];
   int* s_cnt = reinterpret_cast<int*>(sm + (long long)D.E * D.d);
   for (int e = threadIdx.x; e < D.E; e += MT_THREADS) s_cnt[e] = 0;
+  if (dw && t0 < t1) {
+    // the chunk's x_mid rows are stored by out-projection tiles of other CTAs
+    const int b0 = t0 / MT_TILE_M, nb = (t1 - 1) / MT_TILE_M - b0 + 1;
+    if (threadIdx.x < nb) dep_wait(abuf<ArenaHdr>(a, A_HDR), dw + b0 + threadIdx.x, dtarget, a.timeout_ns);
+  }
   __syncthreads();
   const int n4 = D.d / 4;
   with_nc(D.d, [&](auto NCc) {
@@ -330,7 +340,7 @@ __device__ __noinline__ void job_route(const KArgs& a, int l, int* ism) {
 // x_{l+1} = x_mid + sum_k w_k y_k (fixed slot order), then the next
 // RMSNorm (attention norm of layer l+1, or the final norm).
 template <class OP>
-__device__ __noinline__ void job_combine(const KArgs& a, int l, Sched& s) {
+__device__ __noinline__ void job_combine(const KArgs& a, int l, Sched& s, unsigned* dsig) {
   const MtDims& D = a.D;
   const int lane = threadIdx.x & 31, n4 = D.d / 4;
   const float* XM = abuf<float>(a, A_XM) + (long long)l * D.T * D.d;
@@ -342,12 +352,16 @@ __device__ __noinline__ void job_combine(const KArgs& a, int l, Sched& s) {
   const float* gp = last ? pmaster(a, P_FINAL_NORM) : pmaster(a, P_ATTN_NORM) + (long long)(l + 1) * D.d;
   OP* Rn = last ? abuf<OP>(a, A_RF) : abuf<OP>(a, A_R) + (long long)(l + 1) * D.T * D.d;
   float* invn = last ? abuf<float>(a, A_INVF) : abuf<float>(a, A_INV1) + (long long)(l + 1) * D.T;
-  const int nw = s.G * MT_WARPS;
+  // items: groups of MT_DEP_GROUP tokens (each warp takes every 8th token of
+  // its CTA's group); with counters on, each finished group is published
+  const int ng = (D.T + MT_DEP_GROUP - 1) / MT_DEP_GROUP;
   with_nc(D.d, [&](auto NCc) {
     constexpr int NC = decltype(NCc)::value;
     Row<NC> g, x, acc, y, r;
     row_ld(g, gp, n4);
-    for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
+    for (int gi = s.first(); gi < ng; gi += s.G) {
+    const int tend = min(D.T, (gi + 1) * MT_DEP_GROUP);
+    for (int t = gi * MT_DEP_GROUP + (threadIdx.x >> 5); t < tend; t += MT_WARPS) {
       row_ld(x, XM + (long long)t * D.d, n4);
       row_scale(acc, x, 0.f);
       for (int k = 0; k < D.K; ++k) {
@@ -362,8 +376,13 @@ __device__ __noinline__ void job_combine(const KArgs& a, int l, Sched& s) {
       row_st_op(Rn + (long long)t * D.d, r, n4);
       if (lane == 0) invn[t] = inv;
     }
+    if (dsig) {
+      __syncthreads();
+      if (threadIdx.x == 0) dep_signal(dsig + gi * MT_DEP_GROUP / MT_TILE_M);
+    }
+    }
   });
-  s.next(s.G);
+  s.next(ng);
 }
 
 // Cross-entropy with its gradient, fused with the LM-head product: the
@@ -910,6 +929,7 @@ struct Gemms {
     g.aux = nullptr; g.ldaux = 0; g.accumulate = 0; g.F = D.F; g.S = D.S; g.hd = D.hd; g.hq = D.hq;
     g.rope = nullptr;
     g.tok = nullptr; g.cepart = nullptr; g.cetgt = nullptr; g.ceparts = 0; g.ksplit = 1;
+    g.dwait = nullptr; g.dtarget = 0; g.dwait_aux = nullptr; g.dtarget_aux = 0; g.dsig = nullptr;
     return g;
   }
   __device__ const int* offs(int l) const { return abuf<int>(a, A_OFFS) + (long long)l * (D.E + 1); }
@@ -1133,18 +1153,18 @@ __device__ __forceinline__ attn_tc::Args attn_tc_args(const KArgs& a, int l) {
 }
 
 template <class OP>
-__device__ __forceinline__ void run_attn_fwd(const KArgs& a, int l, Sched& s, char* smem) {
+__device__ __forceinline__ void run_attn_fwd(const KArgs& a, int l, Sched& s, char* smem, const AttnDeps& dp) {
   if constexpr (sizeof(OP) == 2) {
-    if (a.use_tc_attn) { attn_tc_fwd_job<OP>(attn_tc_args<OP>(a, l), s, smem); return; }
+    if (a.use_tc_attn) { attn_tc_fwd_job<OP>(attn_tc_args<OP>(a, l), s, smem, dp); return; }
   }
   const AttnArgs t = attn_args<OP>(a, l);
   if (a.D.hd == 64) attn_fwd_job<OP, 64>(t, s, (float*)smem);
   else attn_fwd_job<OP, 16>(t, s, (float*)smem);
 }
 template <class OP>
-__device__ __forceinline__ void run_attn_bwd(const KArgs& a, int l, Sched& s, char* smem) {
+__device__ __forceinline__ void run_attn_bwd(const KArgs& a, int l, Sched& s, char* smem, const AttnDeps& dp) {
   if constexpr (sizeof(OP) == 2) {
-    if (a.use_tc_attn) { attn_tc_bwd_job<OP>(attn_tc_args<OP>(a, l), s, smem); return; }
+    if (a.use_tc_attn) { attn_tc_bwd_job<OP>(attn_tc_args<OP>(a, l), s, smem, dp); return; }
   }
   const AttnArgs t = attn_args<OP>(a, l);
   if (a.D.hd == 64) attn_bwd_job<OP, 64>(t, s, (float*)smem);
@@ -1162,7 +1182,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   ArenaHdr* hdr = abuf<ArenaHdr>(a, A_HDR);
   const unsigned G = gridDim.x;
   const bool trace = (a.flags & MT_FLAG_TRACE) != 0;
-  long long* tr = trace ? abuf<long long>(a, A_TRACE) + (long long)blockIdx.x * MT_MAX_PHASES * 2 : nullptr;
+  long long* tr = trace ? abuf<long long>(a, A_TRACE) + (long long)blockIdx.x * MT_TRACE_WORDS : nullptr;
   int phase = 0;
   Gemms<OP> gm(a);
   const bool stall = (a.flags & MT_FLAG_TEST_STALL) && blockIdx.x == 0;
@@ -1171,9 +1191,9 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   auto TJ = [&](int id) {
     if (tr) {
       __syncthreads();
-      if (threadIdx.x == 0 && nj < MT_MAX_PHASES / 2) {
-        tr[MT_MAX_PHASES + 2 * nj] = (long long)globaltimer();
-        tr[MT_MAX_PHASES + 2 * nj + 1] = id;
+      if (threadIdx.x == 0 && nj < MT_TRACE_JOBS) {
+        tr[2 * MT_TRACE_PHASES + 2 * nj] = (long long)globaltimer();
+        tr[2 * MT_TRACE_PHASES + 2 * nj + 1] = id;
       }
       ++nj;
     }
@@ -1181,35 +1201,81 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
 
 #define MT_SYNC()                                                                                      \
   do {                                                                                                 \
-    if (!grid_barrier(hdr, G, a.timeout_ns, (tr && phase < MT_MAX_PHASES / 2) ? tr + 2 * phase : nullptr, \
+    if (!grid_barrier(hdr, G, a.timeout_ns, (tr && phase < MT_TRACE_PHASES) ? tr + 2 * phase : nullptr, \
                       stall))                                                                          \
       return;                                                                                          \
     ++phase;                                                                                           \
     TJ(0);                                                                                             \
   } while (0)
 
+  // Hand-offs between consecutive phases either wait at a grid barrier or,
+  // with dependency counters, per 128-row block: the consumer waits only for
+  // the producer parts of the blocks it reads (a.deps is grid-uniform).
+  const bool dep = a.deps != 0;
+  unsigned* depc = abuf<unsigned>(a, A_DEP);
+  auto DEPC = [&](int l, int kind) { return depc + dep_offset(D, l, kind); };
+  auto attn_deps = [&](int l, int tk, bool fwd) {
+    AttnDeps dp{nullptr, nullptr, 0u, nullptr, hdr, a.timeout_ns};
+    if (dep) {
+      dp.ticket = depc + ticket_offset(D, l, tk);
+      if (fwd) {
+        dp.wait = DEPC(l, DEP_QKV); dp.wtarget = (unsigned)(3 * D.hq / TC_BN);
+        dp.sig = DEPC(l, DEP_O);
+      }
+    }
+    return dp;
+  };
+  const unsigned rn_target = MT_TILE_M / MT_DEP_GROUP;
+
   // ---------------- forward ----------------
   job_embed<OP>(a, s); TJ(1);
   MT_SYNC();
   for (int l = 0; l < D.L; ++l) {
-    run_gemm<OP>(a, gm.qkv(l), s, smem, tc); TJ(2);
-    MT_SYNC();
-    run_attn_fwd<OP>(a, l, s, smem); TJ(3);
-    MT_SYNC();
-    run_gemm<OP>(a, gm.wo(l), s, smem, tc); TJ(4);
-    MT_SYNC();
-    job_router<OP>(a, l, (float*)smem); TJ(5);
+    {
+      GemmDesc g = gm.qkv(l);
+      if (dep) {
+        if (l > 0) { g.dwait = DEPC(l - 1, DEP_RN); g.dtarget = rn_target; }
+        g.dsig = DEPC(l, DEP_QKV);
+      }
+      run_gemm<OP>(a, g, s, smem, tc); TJ(2);
+    }
+    if (!dep) MT_SYNC();
+    run_attn_fwd<OP>(a, l, s, smem, attn_deps(l, TK_ATTN_FWD, true)); TJ(3);
+    if (!dep) MT_SYNC();
+    {
+      GemmDesc g = gm.wo(l);
+      if (dep) {
+        g.dwait = DEPC(l, DEP_O); g.dtarget = (unsigned)D.H;
+        if (l > 0) { g.dwait_aux = DEPC(l - 1, DEP_RN); g.dtarget_aux = rn_target; }
+        g.dsig = DEPC(l, DEP_XMID);
+      }
+      run_gemm<OP>(a, g, s, smem, tc); TJ(4);
+    }
+    if (!dep) MT_SYNC();
+    job_router<OP>(a, l, (float*)smem, dep ? DEPC(l, DEP_XMID) : nullptr, (unsigned)(D.d / TC_BN)); TJ(5);
     MT_SYNC();
     job_route<OP>(a, l, (int*)smem); TJ(6);
     MT_SYNC();
-    run_gemm<OP>(a, gm.gateup(l), s, smem, tc); TJ(7);
+    {
+      GemmDesc g = gm.gateup(l);
+      if (dep) g.dsig = DEPC(l, DEP_ACT);
+      run_gemm<OP>(a, g, s, smem, tc); TJ(7);
+    }
+    if (!dep) MT_SYNC();
+    {
+      GemmDesc g = gm.down(l);
+      if (dep) { g.dwait = DEPC(l, DEP_ACT); g.dtarget = (unsigned)(2 * D.F / TC_BN); }
+      run_gemm<OP>(a, g, s, smem, tc); TJ(8);
+    }
     MT_SYNC();
-    run_gemm<OP>(a, gm.down(l), s, smem, tc); TJ(8);
-    MT_SYNC();
-    job_combine<OP>(a, l, s); TJ(9);
-    MT_SYNC();
+    job_combine<OP>(a, l, s, dep ? DEPC(l, DEP_RN) : nullptr); TJ(9);
+    if (!dep) MT_SYNC();
   }
-  run_gemm<OP>(a, gm.lm(), s, smem, tc); TJ(10);
+  {
+    GemmDesc g = gm.lm();
+    if (dep) { g.dwait = DEPC(D.L - 1, DEP_RN); g.dtarget = rn_target; }
+    run_gemm<OP>(a, g, s, smem, tc); TJ(10);
+  }
   MT_SYNC();
   job_ce<OP>(a, s); TJ(11);
   MT_SYNC();
@@ -1259,7 +1325,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     job_colfinal(a, 0, D.E + 1, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d,
                  pgrad(a, P_MOE_NORM) + (long long)l * D.d, 1, s); TJ(18);
     job_ksplit_sum(a, pgrad(a, P_WO) + (long long)l * D.d * D.hq, D.d, D.hq, s); TJ(32);
-    run_attn_bwd<OP>(a, l, s, smem); TJ(26);
+    run_attn_bwd<OP>(a, l, s, smem, attn_deps(l, TK_ATTN_BWD, false)); TJ(26);
     MT_SYNC();
     run_gemm<OP>(a, gm.qkv_dgrad(l), s, smem, tc); TJ(27);
     run_gemm<OP>(a, gm.qkv_wgrad(l), s, smem, tc); TJ(28);
@@ -1305,6 +1371,7 @@ __device__ void run_debug_gemm(const KArgs& a, char* smem, TcState& tc, Sched& s
   g.oseg = (long long)g.M * g.N; g.aux = nullptr; g.ldaux = 0; g.accumulate = 0;
   g.F = 0; g.S = 1; g.hd = 64; g.hq = 0; g.rope = nullptr;
   g.tok = nullptr; g.cepart = nullptr; g.cetgt = nullptr; g.ceparts = 0; g.ksplit = 1;
+  g.dwait = nullptr; g.dtarget = 0; g.dwait_aux = nullptr; g.dtarget_aux = 0; g.dsig = nullptr;
   GOperand A, B;
   A.p0 = a.dbg_a; A.p1 = nullptr; A.mn = a.dbg_a_mn; A.ld = A.mn ? g.M : g.K; A.seg = 0; A.two = 0;
   A.split = 0; A.map0 = MAP_R; A.map1 = -1; A.y0 = 0; A.yseg = 0;

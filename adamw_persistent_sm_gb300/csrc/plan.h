@@ -63,11 +63,11 @@ enum ArenaId {
   A_PART,      // fp32 [NCH][E+2][d] column-reduction partials
   A_KPART,     // fp32 [<= 8 x 3hq x d] split-K partial tiles of weight gradients
   A_NORMPART,  // fp32 [NCH] squared-norm partials (double precision accumulate)
-  A_TRACE,     // i64  [NCH][MAXPH][2]
+  A_DEP,       // u32  dependency counters and work tickets (layout below), zeroed by the first phase
+  A_TRACE,     // i64  [NCH][MT_TRACE_WORDS] barrier pairs, then job stamps
   A_COUNT
 };
 
-#define MT_MAX_PHASES 512
 
 // TMA tensor maps (bf16 operands of the tensor-core products), one per 2-D
 // buffer; per-layer and per-expert tensors are addressed through the outer
@@ -97,6 +97,38 @@ struct ArenaHdr {
   int expert_counts[16 * 64];
 };
 
+// Dependency counters.  Each layer owns one counter per 128-row block of
+// every hand-off that runs without a grid barrier; a producer adds 1 when it
+// has stored its part of a block, a consumer waits until the block's counter
+// reaches the number of producer parts.  After the L layers come the work
+// tickets (dynamically scheduled jobs take item numbers from them).
+enum DepKind {
+  DEP_QKV = 0,   // [T/128] q,k,v tiles stored (target: 3hq/256 column tiles)
+  DEP_O,         // [T/128] attention items stored (target: H)
+  DEP_XMID,      // [T/128] out-projection tiles stored (target: d/256)
+  DEP_RN,        // [T/128] 32-token combine groups stored (next layer's norm rows; target 4)
+  DEP_ACT,       // [Pmax/128] gate/up tiles stored (target: 2F/256)
+  DEP_KINDS
+};
+#define MT_DEP_GROUP 32         // tokens per combine item when counters are on
+#define MT_TICKETS 8            // ticket counters per layer (plus one set for the head)
+enum TicketId { TK_ATTN_FWD = 0, TK_ATTN_BWD };
+__host__ __device__ inline long long dep_blocks(const MtDims& D, int kind) {
+  return kind == DEP_ACT ? D.Pmax / MT_TILE_M : (D.T + MT_TILE_M - 1) / MT_TILE_M;
+}
+__host__ __device__ inline long long dep_layer_words(const MtDims& D) {
+  return (DEP_KINDS - 1) * dep_blocks(D, DEP_QKV) + dep_blocks(D, DEP_ACT);
+}
+__host__ __device__ inline long long dep_offset(const MtDims& D, int l, int kind) {
+  return (long long)l * dep_layer_words(D) + (long long)kind * dep_blocks(D, DEP_QKV);
+}
+__host__ __device__ inline long long ticket_offset(const MtDims& D, int l, int id) {
+  return (long long)D.L * dep_layer_words(D) + (long long)l * MT_TICKETS + id;
+}
+__host__ __device__ inline long long dep_words(const MtDims& D) {
+  return (long long)D.L * dep_layer_words(D) + (long long)(D.L + 1) * MT_TICKETS;
+}
+
 struct KArgs {
   MtDims D;
   float lr, beta1, beta2, eps, wd, clip, clip_eps, norm_eps, coef, rope_theta;
@@ -121,6 +153,7 @@ struct KArgs {
   const int* dbg_offs;
   int use_tc;                   // tcgen05 GEMMs (bf16 only)
   int use_tc_attn;              // tensor-core attention (bf16 only)
+  int deps;                     // dependency counters replace the grid barriers they cover
   CUtensorMap maps[MT_NMAPS];
 };
 

@@ -182,7 +182,7 @@ def run_ours(args, cfg, rank, world):
     B.load(build_if_missing=True)
     params = mi.make_params(cfg)
     host_toks = mi.make_update_tokens(cfg)
-    tr = MoETrainer(cfg, dev)
+    tr = MoETrainer(cfg, dev, flags=_sched_flags(args))
     tr.load_params(params)
     dtoks = [torch.as_tensor(t).to(dev) for t in host_toks]
     stream = torch.cuda.current_stream(dev)
@@ -321,22 +321,27 @@ JOB_NAMES = {0: "barrier wait", 1: "embed", 2: "qkv", 3: "attn_fwd", 4: "wo", 5:
              29: "attn_norm_bwd", 30: "embed_bwd", 31: "norm_partial", 32: "wo_ksum", 33: "qkv_ksum"}
 
 
+def _sched_flags(args):
+    from adamw_persistent_sm_gb300 import binding as B
+    return B.MT_FLAG_BARRIERS_ONLY if args.barriers_only else 0
+
+
 def run_trace(args, cfg):
     """Per-job time of one update from the in-kernel trace (MT_FLAG_TRACE):
     each CTA stamps the end of every job; a job's time is the gap to the
-    previous stamp.  The first 256 stamps of the update are kept."""
+    previous stamp."""
     import torch
     from adamw_persistent_sm_gb300 import binding as B
     from adamw_persistent_sm_gb300.trainer import MoETrainer
-    tr = MoETrainer(cfg, "cuda:0", flags=B.MT_FLAG_TRACE)
+    tr = MoETrainer(cfg, "cuda:0", flags=B.MT_FLAG_TRACE | _sched_flags(args))
     tr.load_params(mi.make_params(cfg))
     toks = [torch.as_tensor(t).cuda() for t in mi.make_update_tokens(cfg)]
     for it in range(max(1, args.warmup)):
         tr.update(toks, step=it + 1)
     out = tr.outputs()
     assert out.status == B.MT_OK, B.status_string(out.status)
-    tv = tr.debug_view(B.MT_VIEW_TRACE, 0, torch.int64).cpu().numpy().reshape(-1, 1024)[:out.n_ctas]
-    jobs = tv[:, 512:].reshape(out.n_ctas, 256, 2)
+    tv = tr.debug_view(B.MT_VIEW_TRACE, 0, torch.int64).cpu().numpy().reshape(-1, B.MT_TRACE_WORDS)
+    jobs = tv[:out.n_ctas, 2 * B.MT_TRACE_PHASES:].reshape(out.n_ctas, B.MT_TRACE_JOBS, 2)
     nj = int((jobs[0, :, 0] > 0).sum())
     t = jobs[:, :nj, 0].astype(np.float64)
     ids = jobs[0, :nj, 1]
@@ -401,6 +406,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--trace", action="store_true", help="print the per-job time of one update")
+    ap.add_argument("--barriers-only", action="store_true",
+                    help="grid barriers at every hand-off (no per-block dependency counters)")
     ap.add_argument("--product", type=int, nargs=5, metavar=("M", "N", "K", "A_MN", "B_MN"),
                     help="time one product through the tensor-core engine")
     ap.add_argument("--product-out", default="f32", choices=["f32", "bf16", "none"],

@@ -58,8 +58,11 @@ enum {
   MT_FLAG_SIMT_GEMM = 1u << 1,    /* bf16 mode: use the CUDA-core GEMM instead of tcgen05 */
   MT_FLAG_SIMT_ATTN = 1u << 2,    /* bf16 mode: use the CUDA-core attention */
   MT_FLAG_NO_OPTIMIZER = 1u << 3, /* skip clip + AdamW even on the last microbatch */
-  MT_FLAG_TEST_STALL = 1u << 4    /* test only: CTA 0 never arrives at the first grid
+  MT_FLAG_TEST_STALL = 1u << 4,   /* test only: CTA 0 never arrives at the first grid
                                      barrier, so the others' bounded waits run out */
+  MT_FLAG_BARRIERS_ONLY = 1u << 5 /* separate every phase by a grid barrier, even where
+                                     per-block dependency counters would do (same
+                                     results bit for bit; for comparison) */
 };
 
 /*
@@ -164,6 +167,9 @@ int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m
  * Returns out->status (MT_OK if the device side succeeded). */
 int32_t mt_read_outputs(const void* arena, mt_outputs* out, void* stream);
 
+/* Capacity of the per-CTA trace (MT_VIEW_TRACE) */
+enum { MT_TRACE_PHASES = 512, MT_TRACE_JOBS = 1024, MT_TRACE_WORDS = 2 * (512 + 1024) };
+
 /* Debug views into the arena after a launch (device pointers into the arena).
  * which: see MT_VIEW_* ; layer selects the layer for per-layer buffers. */
 enum {
@@ -173,7 +179,10 @@ enum {
   MT_VIEW_ROUTE_OFFS = 3,     /* int32 [E+1] padded segment starts (multiples of 128) */
   MT_VIEW_ROUTE_PERM = 4,     /* int32 [Pmax] assignment t*K+k at each sorted row, -1 = pad */
   MT_VIEW_TOK_LOSS = 5,       /* fp32 [T] coef * CE per position */
-  MT_VIEW_TRACE = 6,          /* int64 [n_ctas, n_phases, 2] (t_arrive, t_leave) ns */
+  MT_VIEW_TRACE = 6,          /* int64 [CTA][MT_TRACE_WORDS] (MT_FLAG_TRACE): per CTA, for
+                                 grid barrier p < MT_TRACE_PHASES the pair (t_arrive,
+                                 t_leave) at [2p], then from [2*MT_TRACE_PHASES] for job
+                                 stamp j < MT_TRACE_JOBS the pair (t_end, job id); ns */
   MT_VIEW_HIDDEN = 7,         /* fp32 [T, d] residual stream entering `layer` (layer = L: final) */
   MT_VIEW_LOGITS = 8          /* operand type [T, V]: LM-head logits (bf16 or fp32), overwritten
                                  in place by dlogits during the same launch */

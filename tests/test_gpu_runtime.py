@@ -59,7 +59,8 @@ def test_phase_trace():
     tr.update([torch.as_tensor(t).cuda() for t in mi.make_update_tokens(cfg)])
     out = tr.outputs()
     assert out.status == B.MT_OK
-    tv = tr.debug_view(B.MT_VIEW_TRACE, 0, torch.int64).cpu().numpy().reshape(-1, 512, 2)
+    tv = tr.debug_view(B.MT_VIEW_TRACE, 0, torch.int64).cpu().numpy().reshape(-1, B.MT_TRACE_WORDS)
+    tv = tv[:, :2 * B.MT_TRACE_PHASES].reshape(-1, B.MT_TRACE_PHASES, 2)
     tv = tv[:out.n_ctas, :out.n_phases]
     assert np.all(tv[:, :, 1] >= tv[:, :, 0])
     assert np.all(np.diff(tv[:, :, 0], axis=1) >= 0)
