@@ -42,6 +42,7 @@ MT_VIEW_ROUTE_OFFS = 3
 MT_VIEW_ROUTE_PERM = 4
 MT_VIEW_TOK_LOSS = 5
 MT_VIEW_TRACE = 6
+MT_MAX_CTAS = 512                     # arena buffers are sized for up to this many CTAs
 MT_TRACE_PHASES = 512                 # per CTA: barrier (arrive, leave) pairs, then
 MT_TRACE_JOBS = 1024                  # (end time, job id) pairs
 MT_TRACE_WORDS = 2 * (MT_TRACE_PHASES + MT_TRACE_JOBS)

@@ -117,7 +117,8 @@ void make_plan(const mt_hparams* hp, MtPlan* P) {
   sz[A_KPART] = 8LL * 3 * D.hq * d * 4;
   sz[A_NORMPART] = (long long)D.nch * 8;
   sz[A_DEP] = dep_words(D) * 4;
-  sz[A_TRACE] = (long long)D.nch * MT_TRACE_WORDS * 8;
+  // the per-CTA trace exists only in arenas sized for traced launches
+  sz[A_TRACE] = (hp->flags & MT_FLAG_TRACE) ? (long long)D.nch * MT_TRACE_WORDS * 8 : 0;
   long long off = 0;
   for (int i = 0; i < A_COUNT; ++i) {
     P->aoff[i] = off;
@@ -163,8 +164,13 @@ size_t smem_bytes(const MtDims& D, bool tc) {
   size_t attn = (size_t)(4 * 64 * 65 + 2 * 64 * 65 + 128) * 4;
   size_t simt = (size_t)SG_BM * SG_CPAD * 4;
   size_t router = (size_t)D.E * D.d * 4 + 64 * 4;
+  // column reductions: staged 1/rms and router gradients, token-lane partials
+  const int er = D.E <= 4 ? 4 : D.E <= 16 ? 16 : D.E <= 32 ? 32 : 64;
+  const int cw = D.E <= 16 ? 4 : D.E <= 32 ? 2 : 1;
+  size_t col = (size_t)(256 + 256 * D.E + 3 * (er + 1) * 64 * cw) * 4;
   size_t need = attn > simt ? attn : simt;
   if (router > need) need = router;
+  if (col > need) need = col;
   if (tc && MT_TC_SMEM > need) need = MT_TC_SMEM;
   return need;
 }
@@ -351,6 +357,7 @@ int32_t mt_debug_view(const void* arena, const mt_hparams* hp, int32_t which, in
     case MT_VIEW_TOK_LOSS:
       *out = {base + P.aoff[A_TOKLOSS], T, 4}; break;
     case MT_VIEW_TRACE:
+      if (!(hp->flags & MT_FLAG_TRACE)) return MT_ERR_ARG;
       *out = {base + P.aoff[A_TRACE], (long long)D.nch * MT_TRACE_WORDS, 8}; break;
     case MT_VIEW_HIDDEN:
       *out = {base + P.aoff[A_X] + (long long)layer * T * D.d * 4, T * D.d, 4}; break;

@@ -623,10 +623,13 @@ __device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s) 
 // ===========================================================================
 // deterministic column reductions over tokens (norm gains, router weights)
 // ===========================================================================
-// Partial sums over token chunks, each in token order, written to
-// PART[chunk][row][col]; a later phase adds the chunks in chunk order, so
-// the result does not depend on the grid size.  One thread owns one column
-// and every output row of it (ER accumulators, ER >= rows).
+// Partial sums over token chunks written to PART[chunk][row][col]; a later
+// phase adds the chunks in chunk order.  Inside a chunk, four token lanes
+// each sum every fourth token in token order and are then added in lane
+// order, so for a given grid the result is the same in every launch.  A
+// thread owns CW adjacent columns and every output row of them (ER router
+// rows plus the gain row); CW shrinks as the router rows grow so that the
+// accumulators stay in registers.
 enum ColKind { COL_GAIN = 0, COL_MOE = 1 };
 struct ColArgs {
   int kind;
@@ -638,36 +641,65 @@ struct ColArgs {
   int row0;           // first PART row written
 };
 
-__device__ __forceinline__ int col_nchunks(const MtDims& D, int G) {
-  const int ncb = (D.d + MT_THREADS - 1) / MT_THREADS;
+#define COL_LANES 4
+// columns per thread for a reduction with E router rows (0: gain only)
+__device__ __forceinline__ int col_width(int E) { return E <= 16 ? 4 : (E <= 32 ? 2 : 1); }
+// token chunks: about two items per CTA
+__device__ __forceinline__ int col_nchunks(const MtDims& D, int G, int E) {
+  const int cb = (MT_THREADS / COL_LANES) * col_width(E);
+  const int ncb = (D.d + cb - 1) / cb;
   int n = (2 * G + ncb - 1) / ncb;
   if (n > D.nch) n = D.nch;
   if (n > D.T) n = D.T;
   return n < 1 ? 1 : n;
 }
 
-template <int ER>
+template <int CW>
+__device__ __forceinline__ void ld_cols(float (&v)[CW], const float* p) {
+  if constexpr (CW == 4) {
+    const float4 q = *reinterpret_cast<const float4*>(p);
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  } else if constexpr (CW == 2) {
+    const float2 q = *reinterpret_cast<const float2*>(p);
+    v[0] = q.x; v[1] = q.y;
+  } else {
+    v[0] = *p;
+  }
+}
+
+template <int ER, int CW>
 __device__ void colpart_items(const KArgs& a, const ColArgs& c, Sched& s, float* sm) {
+  constexpr int TPL = MT_THREADS / COL_LANES;   // threads per token lane
+  constexpr int CB = TPL * CW;                  // columns per item
+  constexpr int U = 1;                          // tokens in flight per thread
+  constexpr int SUB = 256;                      // tokens staged at a time
   const MtDims& D = a.D;
   const int G = s.G;
-  const int ncb = (D.d + MT_THREADS - 1) / MT_THREADS;
-  const int nchunk = col_nchunks(D, G);
-  const int ch = (D.T + nchunk - 1) / nchunk;
-  const int items = ncb * nchunk;
   const bool moe = (c.kind == COL_MOE);
   const int E = moe ? D.E : 0;
+  const int ncb = (D.d + CB - 1) / CB;
+  const int nchunk = col_nchunks(D, G, E);
+  const int ch = (D.T + nchunk - 1) / nchunk;
+  const int items = ncb * nchunk;
   float* PART = abuf<float>(a, A_PART);
-  constexpr int SUB = 256;           // tokens staged at a time
-  float* s_inv = sm;                 // [SUB]
-  float* s_dz = sm + SUB;            // [SUB][E]
+  float* s_inv = sm;                            // [SUB]
+  float* s_dz = sm + SUB;                       // [SUB][E]
+  float* s_red = s_dz + SUB * E;                // [COL_LANES - 1][ER + 1][CB]
+  const int tl = threadIdx.x / TPL, tc = threadIdx.x % TPL;
   for (int it = s.first(); it < items; it += G) {
     const int chunk = it / ncb, cb = it % ncb;
-    const int col = cb * MT_THREADS + threadIdx.x;
+    const int col = cb * CB + tc * CW;
+    const bool active = col < D.d;
     const int t0 = chunk * ch, t1 = min(D.T, t0 + ch);
-    float acc[ER + 1];
+    float acc[ER + 1][CW];
 #pragma unroll
-    for (int j = 0; j <= ER; ++j) acc[j] = 0.f;
-    const float gcol = (moe && col < D.d) ? c.g[col] : 0.f;
+    for (int r = 0; r <= ER; ++r)
+#pragma unroll
+      for (int j = 0; j < CW; ++j) acc[r][j] = 0.f;
+    float gcol[CW];
+#pragma unroll
+    for (int j = 0; j < CW; ++j) gcol[j] = 0.f;
+    if (moe && active) ld_cols<CW>(gcol, c.g + col);
     for (int s0 = t0; s0 < t1; s0 += SUB) {
       const int n = min(SUB, t1 - s0);
       __syncthreads();
@@ -675,59 +707,84 @@ __device__ void colpart_items(const KArgs& a, const ColArgs& c, Sched& s, float*
       if (moe)
         for (int i = threadIdx.x; i < n * E; i += MT_THREADS) s_dz[i] = c.dz[(long long)s0 * E + i];
       __syncthreads();
-      if (col >= D.d) continue;
-      for (int tb = 0; tb < n; tb += 4) {
-        float xv[4], dyv[4];
+      if (!active) continue;
+      for (int tb = tl; tb < n; tb += COL_LANES * U) {
+        float xv[U][CW], dyv[U][CW];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const bool ok = tb + u < n;
-          const long long off = (long long)(s0 + tb + u) * D.d + col;
-          xv[u] = ok ? c.x[off] : 0.f;
-          dyv[u] = ok ? c.dy[off] : 0.f;
+        for (int u = 0; u < U; ++u) {
+          const int tk = tb + u * COL_LANES;
+          if (tk < n) {
+            const long long off = (long long)(s0 + tk) * D.d + col;
+            ld_cols<CW>(xv[u], c.x + off);
+            ld_cols<CW>(dyv[u], c.dy + off);
+          }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (tb + u < n) {
-            const float xh = xv[u] * s_inv[tb + u];
-            acc[ER] = fmaf(dyv[u], xh, acc[ER]);          // gain gradient row
-            if (ER > 0) {
-              const float r2 = xh * gcol;
-              const float* dz = s_dz + (tb + u) * E;
+        for (int u = 0; u < U; ++u) {
+          const int tk = tb + u * COL_LANES;
+          if (tk < n) {
+            const float iv = s_inv[tk];
 #pragma unroll
-              for (int e = 0; e < ER; ++e)
-                if (e < E) acc[e] = fmaf(dz[e], r2, acc[e]);
+            for (int j = 0; j < CW; ++j) {
+              const float xh = xv[u][j] * iv;
+              acc[ER][j] = fmaf(dyv[u][j], xh, acc[ER][j]);      // gain gradient row
+              if (ER > 0) {
+                const float r2 = xh * gcol[j];
+                const float* dz = s_dz + tk * E;
+#pragma unroll
+                for (int e = 0; e < ER; ++e)
+                  if (e < E) acc[e][j] = fmaf(dz[e], r2, acc[e][j]);
+              }
             }
           }
         }
       }
     }
-    if (col < D.d) {
+    // add the token lanes in lane order
+    if (tl > 0 && active) {
+#pragma unroll
+      for (int r = 0; r <= ER; ++r)
+#pragma unroll
+        for (int j = 0; j < CW; ++j) s_red[((tl - 1) * (ER + 1) + r) * CB + tc * CW + j] = acc[r][j];
+    }
+    __syncthreads();
+    if (tl == 0 && active) {
       float* out = PART + ((long long)chunk * (D.E + 2) + c.row0) * D.d + col;
 #pragma unroll
-      for (int e = 0; e < ER; ++e)
-        if (e < E) out[(long long)e * D.d] = acc[e];
-      out[(long long)E * D.d] = acc[ER];
+      for (int r = 0; r <= ER; ++r) {
+        if (r < ER && r >= E) continue;
+        const int orow = (r == ER) ? E : r;
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+          float v = acc[r][j];
+#pragma unroll
+          for (int q = 0; q < COL_LANES - 1; ++q) v += s_red[(q * (ER + 1) + r) * CB + tc * CW + j];
+          out[(long long)orow * D.d + j] = v;
+        }
+      }
     }
+    // the next item may be an empty chunk (no staging barrier) that writes s_red at once
+    __syncthreads();
   }
-  __syncthreads();
   s.next(items);
 }
 
 static __device__ __noinline__ void job_colpart(const KArgs& a, const ColArgs& c, Sched& s, float* sm) {
   const int E = (c.kind == COL_MOE) ? a.D.E : 0;
-  if (E == 0) colpart_items<0>(a, c, s, sm);
-  else if (E <= 4) colpart_items<4>(a, c, s, sm);
-  else if (E <= 16) colpart_items<16>(a, c, s, sm);
-  else if (E <= 32) colpart_items<32>(a, c, s, sm);
-  else colpart_items<64>(a, c, s, sm);
+  if (E == 0) colpart_items<0, 4>(a, c, s, sm);
+  else if (E <= 4) colpart_items<4, 4>(a, c, s, sm);
+  else if (E <= 16) colpart_items<16, 4>(a, c, s, sm);
+  else if (E <= 32) colpart_items<32, 2>(a, c, s, sm);
+  else colpart_items<64, 1>(a, c, s, sm);
 }
 
-// out[r][col] (+)= sum over chunks of PART[chunk][row0 + r][col].
-static __device__ __noinline__ void job_colfinal(const KArgs& a, int row0, int nrows, float* out_rows, float* out_last,
-                                    int last_is_separate, Sched& s) {
+// out[r][col] (+)= sum over chunks of PART[chunk][row0 + r][col]; E_kind is
+// the router-row count of the reduction that wrote those rows (0: gain only).
+static __device__ __noinline__ void job_colfinal(const KArgs& a, int row0, int nrows, int E_kind, float* out_rows,
+                                                 float* out_last, int last_is_separate, Sched& s) {
   const MtDims& D = a.D;
   const int G = s.G;
-  const int nused = col_nchunks(D, G);
+  const int nused = col_nchunks(D, G, E_kind);
   const float* PART = abuf<float>(a, A_PART);
   const int n = nrows * D.d;
   const bool acc = a.micro_index > 0;
@@ -1302,8 +1359,8 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
       job_colpart(a, c, s, (float*)smem); TJ(16);
     }
     MT_SYNC();
-    if (l == D.L - 1) job_colfinal(a, D.E + 1, 1, pgrad(a, P_FINAL_NORM), nullptr, 0, s);
-    else job_colfinal(a, D.E + 1, 1, pgrad(a, P_ATTN_NORM) + (long long)(l + 1) * D.d, nullptr, 0, s);
+    if (l == D.L - 1) job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_FINAL_NORM), nullptr, 0, s);
+    else job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM) + (long long)(l + 1) * D.d, nullptr, 0, s);
     TJ(18);
     run_gemm<OP>(a, gm.down_dgrad(l), s, smem, tc); TJ(19);
     run_gemm<OP>(a, gm.down_wgrad(l), s, smem, tc); TJ(20);
@@ -1322,7 +1379,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     run_gemm<OP>(a, gm.wo_dgrad(l), s, smem, tc); TJ(24);
     run_gemm<OP>(a, gm.wo_wgrad(l), s, smem, tc); TJ(25);
     MT_SYNC();
-    job_colfinal(a, 0, D.E + 1, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d,
+    job_colfinal(a, 0, D.E + 1, D.E, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d,
                  pgrad(a, P_MOE_NORM) + (long long)l * D.d, 1, s); TJ(18);
     job_ksplit_sum(a, pgrad(a, P_WO) + (long long)l * D.d * D.hq, D.d, D.hq, s); TJ(32);
     run_attn_bwd<OP>(a, l, s, smem, attn_deps(l, TK_ATTN_BWD, false)); TJ(26);
@@ -1341,7 +1398,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   }
   job_embed_bwd(a, (int*)smem); TJ(30);
   MT_SYNC();
-  job_colfinal(a, D.E + 1, 1, pgrad(a, P_ATTN_NORM), nullptr, 0, s); TJ(18);
+  job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM), nullptr, 0, s); TJ(18);
 
   // ---------------- optimizer (last microbatch) ----------------
   if (a.run_opt) {

@@ -33,7 +33,7 @@ class MoETrainer:
         self.device = torch.device(device)
         self.flags = flags
         self.wait_timeout_ns = wait_timeout_ns
-        hp = B.hparams(cfg)
+        hp = B.hparams(cfg, flags=flags)      # MT_FLAG_TRACE adds the trace to the arena
         n = B.mt_param_count(hp)
         if n < 0:
             raise StatusError(f"mt_param_count: {B.status_string(-n)}")

@@ -133,7 +133,9 @@ int64_t mt_param_count(const mt_hparams* hp);
 int32_t mt_param_layout(const mt_hparams* hp, mt_tensor_desc* out, int32_t cap);
 
 /* Bytes of caller-provided device arena the launch needs (worst case over
- * routing), or a negative mt_status. */
+ * routing), or a negative mt_status.  With MT_FLAG_TRACE in hp->flags the
+ * arena also holds the per-CTA trace (MT_VIEW_TRACE), so traced launches
+ * need an arena sized with that flag. */
 int64_t mt_arena_bytes(const mt_hparams* hp);
 
 /* Zero the arena's control header (barrier and status words).  Call once after
@@ -179,7 +181,8 @@ enum {
   MT_VIEW_ROUTE_OFFS = 3,     /* int32 [E+1] padded segment starts (multiples of 128) */
   MT_VIEW_ROUTE_PERM = 4,     /* int32 [Pmax] assignment t*K+k at each sorted row, -1 = pad */
   MT_VIEW_TOK_LOSS = 5,       /* fp32 [T] coef * CE per position */
-  MT_VIEW_TRACE = 6,          /* int64 [CTA][MT_TRACE_WORDS] (MT_FLAG_TRACE): per CTA, for
+  MT_VIEW_TRACE = 6,          /* int64 [CTA][MT_TRACE_WORDS] (hp->flags must hold
+                                 MT_FLAG_TRACE, else MT_ERR_ARG): per CTA, for
                                  grid barrier p < MT_TRACE_PHASES the pair (t_arrive,
                                  t_leave) at [2p], then from [2*MT_TRACE_PHASES] for job
                                  stamp j < MT_TRACE_JOBS the pair (t_end, job id); ns */

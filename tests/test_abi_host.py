@@ -110,3 +110,14 @@ def test_train_update_argument_checks(lib):
 def test_struct_sizes_match_header(lib):
     assert C.sizeof(B.mt_hparams) == 112
     assert C.sizeof(B.mt_outputs) == 40 + 4 * 16 * 64
+
+
+def test_trace_arena_is_sized_by_the_trace_flag():
+    from adamw_persistent_sm_gb300 import binding as B
+    cfg = mi.get_config("tiny")
+    plain = B.mt_arena_bytes(B.hparams(cfg))
+    traced = B.mt_arena_bytes(B.hparams(cfg, flags=B.MT_FLAG_TRACE))
+    per_cta = B.MT_TRACE_WORDS * 8
+    assert traced - plain >= B.MT_MAX_CTAS * per_cta
+    assert traced - plain < B.MT_MAX_CTAS * per_cta + 4096
+    assert plain <= B.MT_NOALLOC_ARENA_BYTES
