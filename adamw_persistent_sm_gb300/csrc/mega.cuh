@@ -440,27 +440,58 @@ __device__ __noinline__ void job_ce(const KArgs& a, Sched& s) {
     sum = (m == -INFINITY) ? 0.f : sum * expf(m - M);
     sum = warp_sum(sum);
     const float lse = M + logf(sum);
-    for (int j0 = 0; j0 < v4; j0 += 32 * U) {
-      float4 q[U];
+    if constexpr (sizeof(OP) == 2) {
+      // bf16 logits: 16-byte groups of 8, U groups in flight per lane
+      const int v8 = D.V / 8;
+      for (int j0 = 0; j0 < v8; j0 += 32 * U) {
+        uint4 q[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = j0 + lane + 32 * u;
-        if (j < v4) q[u] = ld4(row + 4 * j);
-      }
+        for (int u = 0; u < U; ++u) {
+          const int j = j0 + lane + 32 * u;
+          if (j < v8) q[u] = reinterpret_cast<const uint4*>(row)[j];
+        }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = j0 + lane + 32 * u;
-        if (j < v4) {
-          float4 p = make_float4(a.coef * __expf(q[u].x - lse), a.coef * __expf(q[u].y - lse),
-                                 a.coef * __expf(q[u].z - lse), a.coef * __expf(q[u].w - lse));
-          if ((target >> 2) == j) {
-            const int c = target & 3;
-            if (c == 0) p.x -= a.coef;
-            else if (c == 1) p.y -= a.coef;
-            else if (c == 2) p.z -= a.coef;
-            else p.w -= a.coef;
+        for (int u = 0; u < U; ++u) {
+          const int j = j0 + lane + 32 * u;
+          if (j < v8) {
+            const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[h]));
+              float p0 = a.coef * __expf(x.x - lse), p1 = a.coef * __expf(x.y - lse);
+              if (target == 8 * j + 2 * h) p0 -= a.coef;
+              if (target == 8 * j + 2 * h + 1) p1 -= a.coef;
+              __nv_bfloat162 r = __floats2bfloat162_rn(p0, p1);
+              o[h] = *reinterpret_cast<uint32_t*>(&r);
+            }
+            reinterpret_cast<uint4*>(row)[j] = make_uint4(o[0], o[1], o[2], o[3]);
           }
-          st4(row + 4 * j, p);
+        }
+      }
+    } else {
+      for (int j0 = 0; j0 < v4; j0 += 32 * U) {
+        float4 q[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int j = j0 + lane + 32 * u;
+          if (j < v4) q[u] = ld4(row + 4 * j);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int j = j0 + lane + 32 * u;
+          if (j < v4) {
+            float4 p = make_float4(a.coef * __expf(q[u].x - lse), a.coef * __expf(q[u].y - lse),
+                                   a.coef * __expf(q[u].z - lse), a.coef * __expf(q[u].w - lse));
+            if ((target >> 2) == j) {
+              const int c = target & 3;
+              if (c == 0) p.x -= a.coef;
+              else if (c == 1) p.y -= a.coef;
+              else if (c == 2) p.z -= a.coef;
+              else p.w -= a.coef;
+            }
+            st4(row + 4 * j, p);
+          }
         }
       }
     }
@@ -878,14 +909,29 @@ static __device__ __noinline__ void job_norm_partial(const KArgs& a, double* dsm
   const float4* g4 = reinterpret_cast<const float4*>(a.grads);
   double acc = 0.0;
   float facc = 0.f;
-  int cnt = 0;
-  for (long long i = b0 + threadIdx.x; i < b1; i += MT_THREADS) {
+  // four float4 loads in flight per thread; fp32 partial sums of 16 squares
+  // are added into the fp64 accumulator in a fixed order
+  long long i = b0 + threadIdx.x;
+  for (; i + 3 * MT_THREADS < b1; i += 4 * MT_THREADS) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = g4[i + u * MT_THREADS];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      facc = fmaf(v[u].x, v[u].x, facc);
+      facc = fmaf(v[u].y, v[u].y, facc);
+      facc = fmaf(v[u].z, v[u].z, facc);
+      facc = fmaf(v[u].w, v[u].w, facc);
+    }
+    acc += facc;
+    facc = 0.f;
+  }
+  for (; i < b1; i += MT_THREADS) {
     const float4 v = g4[i];
     facc = fmaf(v.x, v.x, facc);
     facc = fmaf(v.y, v.y, facc);
     facc = fmaf(v.z, v.z, facc);
     facc = fmaf(v.w, v.w, facc);
-    if (++cnt == 64) { acc += facc; facc = 0.f; cnt = 0; }
   }
   if (c == G - 1)
     for (long long i = n4 * 4 + threadIdx.x; i < n; i += MT_THREADS) facc = fmaf(a.grads[i], a.grads[i], facc);
@@ -936,22 +982,32 @@ __device__ __noinline__ void job_adamw(const KArgs& a) {
   float4* m4 = reinterpret_cast<float4*>(a.adam_m);
   float4* v4 = reinterpret_cast<float4*>(a.adam_v);
   __nv_bfloat16* sh = (sizeof(OP) == 2) ? (__nv_bfloat16*)a.shadow : nullptr;
-  for (long long i = b0 + threadIdx.x; i < b1; i += MT_THREADS) {
-    float4 p = p4[i], m = m4[i], v = v4[i];
-    const float4 g = g4[i];
+  // two float4 groups per iteration: eight 16-byte loads in flight per thread
+  auto step4 = [&](long long j, float4 p, const float4 g, float4 m, float4 v) {
     adamw_elem<OP>(a, coef, p.x, g.x, m.x, v.x);
     adamw_elem<OP>(a, coef, p.y, g.y, m.y, v.y);
     adamw_elem<OP>(a, coef, p.z, g.z, m.z, v.z);
     adamw_elem<OP>(a, coef, p.w, g.w, m.w, v.w);
-    p4[i] = p;
-    m4[i] = m;
-    v4[i] = v;
+    p4[j] = p;
+    m4[j] = m;
+    v4[j] = v;
     if (sh) {
+      uint2 u;
       __nv_bfloat162 lo = __floats2bfloat162_rn(p.x, p.y), hi = __floats2bfloat162_rn(p.z, p.w);
-      reinterpret_cast<__nv_bfloat162*>(sh)[2 * i] = lo;
-      reinterpret_cast<__nv_bfloat162*>(sh)[2 * i + 1] = hi;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(sh)[j] = u;
     }
+  };
+  long long i = b0 + threadIdx.x;
+  for (; i + MT_THREADS < b1; i += 2 * MT_THREADS) {
+    const long long j = i + MT_THREADS;
+    const float4 p0 = p4[i], m0 = m4[i], v0 = v4[i], g0 = g4[i];
+    const float4 p1 = p4[j], m1 = m4[j], v1 = v4[j], g1 = g4[j];
+    step4(i, p0, g0, m0, v0);
+    step4(j, p1, g1, m1, v1);
   }
+  if (i < b1) step4(i, p4[i], g4[i], m4[i], v4[i]);
   if (c == G - 1) {
     for (long long i = n4 * 4 + threadIdx.x; i < n; i += MT_THREADS) {
       float p = a.master[i], m = a.adam_m[i], v = a.adam_v[i];
