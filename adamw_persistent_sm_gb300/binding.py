@@ -31,6 +31,7 @@ MT_FLAG_SIMT_ATTN = 1 << 2
 MT_FLAG_NO_OPTIMIZER = 1 << 3
 MT_FLAG_TEST_STALL = 1 << 4
 MT_FLAG_BARRIERS_ONLY = 1 << 5
+MT_FLAG_MMA_SYNC_ATTN = 1 << 6
 
 MT_MAX_LAYERS = 16
 MT_MAX_EXPERTS = 64

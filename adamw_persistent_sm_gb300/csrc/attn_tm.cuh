@@ -1,0 +1,364 @@
+// attn_tm.cuh - causal attention forward on the 5th-generation tensor cores
+// (tcgen05) for head_dim 64: the pages' bf16_sdpa.sdpa forward ("How a
+// training megakernel works", section "1 - Describe the model and update").
+//
+// One item = 128 query rows of one (batch, head); keys in blocks of 128.
+//   warp 0 (one thread): TMA loads of Q (once per item) and of K, V blocks
+//                        into a two-stage ring (128-byte swizzled tiles);
+//   warp 1 (one thread): S_j = Q K_j^T into one of two TMEM buffers
+//                        (128 lanes x 128 fp32 columns), issued one block
+//                        ahead, and PV_j = P_j V_j into one of two 64-column
+//                        TMEM buffers;
+//   warps 4-7          : one query row per thread.  The row of S_j is read
+//                        from TMEM (tcgen05.ld), masked on the diagonal
+//                        block, exponentiated against the running maximum
+//                        (exp2 domain) and written as bf16 into a swizzled
+//                        shared tile P_j (the A operand of PV_j); PV_{j-1} is
+//                        read from TMEM and added into the row's output
+//                        registers after rescaling to the new maximum.
+// The output row is divided by the row sum and stored with the row
+// log-sum-exp (natural log), the same formats as the other attention paths.
+// P is rounded to bf16 before the PV product, as on the mma.sync path.
+#pragma once
+#include "common.cuh"
+#include "gemm_tc.cuh"
+
+struct AttnDeps;   // defined with the attention jobs
+
+namespace attn_tm {
+
+constexpr int BQ = 128, BKEY = 128, HD = 64;
+constexpr float LOG2E = 1.4426950408889634f;
+
+// shared memory (offsets from the 1024-aligned base)
+constexpr int KST = 3;                           // K and V ring stages
+constexpr uint32_t BAR_OFF = 0;                  // mbarriers
+constexpr uint32_t Q_OFF = 1024;                 // 2 x Q: 128 rows x 128 B
+constexpr uint32_t TILE = 16384;                 // one 128-row x 64-column bf16 tile
+constexpr uint32_t K_OFF = Q_OFF + 2 * TILE;     // KST x K tile
+constexpr uint32_t V_OFF = K_OFF + KST * TILE;   // KST x V tile
+constexpr uint32_t P_OFF = V_OFF + KST * TILE;   // 2 x P (128 rows x 128 keys bf16: two 16 KB boxes)
+constexpr uint32_t P_BUF = 2 * TILE;
+constexpr uint32_t SMEM_END = P_OFF + 2 * P_BUF;
+static_assert(SMEM_END <= MT_TC_SMEM, "attention tiles exceed the shared-memory window");
+
+// mbarrier slots (8 bytes each)
+enum { B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = B_KFULL + KST, B_VFULL = B_KEMPTY + KST,
+       B_VEMPTY = B_VFULL + KST, B_SFULL = B_VEMPTY + KST, B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2,
+       B_OFULL = B_PFULL + 2, B_OEMPTY = B_OFULL + 2, B_COUNT = B_OEMPTY + 2 };
+static_assert(B_COUNT * 8 <= 1024, "mbarriers exceed their slot");
+
+// TMEM columns: S buffers at 0 and 128, PV buffers at 256 and 320
+constexpr uint32_t TM_S = 0, TM_PV = 256;
+
+struct Job {
+  const CUtensorMap* map;    // q,k,v of all layers: rows l*T + t, columns [q | k | v]
+  int y0;                    // row of token 0 of this layer
+  __nv_bfloat16* o;          // [T][hq]
+  float* lse;                // [B*H][S]
+  int B, H, S, hq;
+  float scale;
+  // dependency counters (null: the phase is fenced by grid barriers)
+  const unsigned* wait; unsigned wtarget;
+  unsigned* sig;
+  ArenaHdr* hdr;
+  long long timeout_ns;
+};
+
+// Item k of this CTA: sequence-major (following the q,k,v product's row
+// order), longest query blocks first within a sequence.
+__device__ __forceinline__ void item_of(const Job& j, int it, int& b, int& h, int& qb) {
+  const int nqb = j.S / BQ;
+  b = it / (j.H * nqb);
+  const int r = it % (j.H * nqb);
+  qb = nqb - 1 - r / j.H;
+  h = r % j.H;
+}
+
+// Byte offset of element (row r, key k) in a P buffer: two 64-key boxes of
+// 128 rows x 128 B, 8-row groups of 1024 B, 16-byte chunks XOR-swizzled by
+// the row's position in its group (the layout a 128-byte-swizzled TMA tile
+// has, which the K-major operand descriptor expects).
+__device__ __forceinline__ uint32_t p_chunk_off(int r, int k) {
+  const int box = k >> 6, kk = k & 63;
+  return (uint32_t)(box * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + ((((kk >> 3) ^ r) & 7) << 4));
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane, without waiting:
+// several loads are issued back to back and completed by one tmem_wait_ld.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+// 2^x on the special-function unit (approximate, flush-to-zero)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, const TcState& tc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar = sbase + BAR_OFF;
+  auto B_ = [&](int i) { return bar + 8u * (uint32_t)i; };
+  const long long tmo = j.timeout_ns;
+  const int nqb = j.S / BQ;
+  const int items = j.B * j.H * nqb;
+  const int first = s.first(), G = s.G;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(B_(B_QFULL + i), 1);
+      mbar_init(B_(B_QEMPTY + i), 1);
+      mbar_init(B_(B_SFULL + i), 1);
+      mbar_init(B_(B_SEMPTY + i), 4);
+      mbar_init(B_(B_PFULL + i), 4);
+      mbar_init(B_(B_OFULL + i), 1);
+      mbar_init(B_(B_OEMPTY + i), 4);
+    }
+    for (int i = 0; i < KST; ++i) {
+      mbar_init(B_(B_KFULL + i), 1);
+      mbar_init(B_(B_KEMPTY + i), 1);
+      mbar_init(B_(B_VFULL + i), 1);
+      mbar_init(B_(B_VEMPTY + i), 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      asm volatile("fence.proxy.async;" ::: "memory");
+      uint32_t kvc = 0, ni = 0;
+      bool dead = false;
+      auto wait = [&](uint32_t b_, uint32_t par) {
+        if (!dead && !mbar_wait(b_, par, tmo)) { set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_EMPTY); dead = true; }
+      };
+      auto load_tile = [&](uint32_t dst, int x, int y, uint32_t fb) {
+        mbar_expect_tx(fb, TILE);
+        tma_load_2d(dst, j.map, x, y, fb);
+        tma_load_2d(dst + 8192, j.map, x, y + 64, fb);
+      };
+      for (int it = first; it < items; it += G, ++ni) {
+        int b, h, qb;
+        item_of(j, it, b, h, qb);
+        if (j.wait) {
+          for (int q = 0; q <= qb; ++q) dep_wait(j.hdr, j.wait + b * nqb + q, j.wtarget, tmo);
+          asm volatile("fence.proxy.async;" ::: "memory");
+        }
+        const int row0 = j.y0 + b * j.S;
+        const uint32_t qs = ni & 1;
+        wait(B_(B_QEMPTY + qs), ((ni >> 1) & 1) ^ 1);
+        load_tile(sbase + Q_OFF + qs * TILE, h * HD, row0 + qb * BQ, B_(B_QFULL + qs));
+        for (int kb = 0; kb <= qb; ++kb, ++kvc) {
+          const uint32_t st = kvc % KST, par = ((kvc / KST) & 1) ^ 1;
+          wait(B_(B_KEMPTY + st), par);
+          load_tile(sbase + K_OFF + st * TILE, j.hq + h * HD, row0 + kb * BKEY, B_(B_KFULL + st));
+          wait(B_(B_VEMPTY + st), par);
+          load_tile(sbase + V_OFF + st * TILE, 2 * j.hq + h * HD, row0 + kb * BKEY, B_(B_VFULL + st));
+        }
+      }
+      // every load issued must land before the shared memory is reused
+      if (!dead) {
+        const uint32_t lo = kvc > KST ? kvc - KST : 0;
+        for (uint32_t c = lo; c < kvc; ++c) {
+          wait(B_(B_KFULL + c % KST), (c / KST) & 1);
+          wait(B_(B_VFULL + c % KST), (c / KST) & 1);
+        }
+        for (uint32_t n = ni > 2 ? ni - 2 : 0; n < ni; ++n) wait(B_(B_QFULL + (n & 1)), (n >> 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16(BQ, BKEY, 0, 0);    // Q (K-major) x K^T (K-major)
+      const uint32_t id_pv = idesc_bf16(BQ, HD, 0, 1);     // P (K-major) x V (MN-major)
+      uint32_t sc = 0, ni = 0;
+      uint32_t last_bar = 0, last_par = 0;
+      bool dead = false;
+      auto wait = [&](uint32_t b_, uint32_t par, int site) {
+        if (!dead && !mbar_wait(b_, par, tmo)) { set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, site); dead = true; }
+      };
+      // S of global block c = Q (buffer qs) K_c^T into S buffer c & 1
+      auto issue_s = [&](uint32_t c, uint32_t qs) {
+        const uint32_t ks = c % KST, sb = c & 1;
+        wait(B_(B_KFULL + ks), (c / KST) & 1, SITE_TC_FULL);
+        wait(B_(B_SEMPTY + sb), ((c >> 1) & 1) ^ 1, SITE_TC_ACC_EMPTY);
+        tc_fence_after();
+        const uint32_t sq = sbase + Q_OFF + qs * TILE, sk = sbase + K_OFF + ks * TILE;
+        for (int kk = 0; kk < HD / 16; ++kk)
+          mma_bf16(tc.tmem_base + TM_S + sb * BKEY, sdesc(sq + kk * 32, 16, 1024), sdesc(sk + kk * 32, 16, 1024),
+                   id_s, kk > 0 ? 1u : 0u);
+        mma_commit(B_(B_SFULL + sb));
+        mma_commit(B_(B_KEMPTY + ks));                    // K_c is read
+      };
+      for (int it = first; it < items; it += G, ++ni) {
+        int b, h, qb;
+        item_of(j, it, b, h, qb);
+        const uint32_t qs = ni & 1;
+        wait(B_(B_QFULL + qs), (ni >> 1) & 1, SITE_TC_FULL);
+        issue_s(sc, qs);
+        for (int kb = 0; kb <= qb; ++kb, ++sc) {
+          if (kb < qb) issue_s(sc + 1, qs);
+          else mma_commit(B_(B_QEMPTY + qs));             // Q is free once the item's last S is done
+          const uint32_t pb = sc & 1, vs = sc % KST;
+          wait(B_(B_VFULL + vs), (sc / KST) & 1, SITE_TC_FULL);
+          wait(B_(B_PFULL + pb), (sc >> 1) & 1, SITE_TC_FULL);
+          wait(B_(B_OEMPTY + pb), ((sc >> 1) & 1) ^ 1, SITE_TC_ACC_EMPTY);
+          tc_fence_after();
+          const uint32_t sp = sbase + P_OFF + pb * P_BUF, sv = sbase + V_OFF + vs * TILE;
+          for (int kk = 0; kk < BKEY / 16; ++kk)
+            mma_bf16(tc.tmem_base + TM_PV + pb * HD, sdesc(sp + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                     sdesc(sv + kk * 2048, 8192, 1024), id_pv, kk > 0 ? 1u : 0u);
+          mma_commit(B_(B_OFULL + pb));
+          mma_commit(B_(B_VEMPTY + vs));
+          last_bar = B_(B_VEMPTY + vs);
+          last_par = (sc / KST) & 1;
+        }
+      }
+      // the tensor core must be idle before the job returns
+      if (last_bar && !dead && !mbar_wait(last_bar, last_par, tmo)) set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_DRAIN);
+      if (ni > 0 && !dead && !mbar_wait(B_(B_QEMPTY + ((ni - 1) & 1)), ((ni - 1) >> 1) & 1, tmo))
+        set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------- softmax and output: one query row per thread ----------------
+    const int q = warp - 4;
+    const int r = q * 32 + lane;                           // row within the item, TMEM lane
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const float sc_l2 = j.scale * LOG2E;
+    uint32_t sc = 0;
+    bool dead = false;
+    auto wait = [&](uint32_t b_, uint32_t par, int site) {
+      if (!dead && !mbar_wait(b_, par, tmo)) { set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, site); dead = true; }
+    };
+    // add the PV block with counter c (relative to maximum mc) into o (relative to m_o)
+    auto add_pv = [&](float* o, float& m_o, uint32_t c, float mc) {
+      const uint32_t pb = c & 1;
+      wait(B_(B_OFULL + pb), (c >> 1) & 1, SITE_TC_ACC_FULL);
+      __syncwarp();
+      tc_fence_after();
+      const float alpha = (m_o == -INFINITY) ? 0.f : exp2f(m_o - mc);
+      const uint32_t tp = tc.tmem_base + lane_off + TM_PV + pb * HD;
+      uint32_t v[HD];
+      tmem_ld32_async(tp, v);
+      tmem_ld32_async(tp + 32, v + 32);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < HD; ++i) o[i] = fmaf(o[i], alpha, __uint_as_float(v[i]));
+      m_o = mc;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B_(B_OEMPTY + pb));
+    };
+    for (int it = first; it < items; it += G) {
+      int b, h, qb;
+      item_of(j, it, b, h, qb);
+      float o[HD];
+#pragma unroll
+      for (int i = 0; i < HD; ++i) o[i] = 0.f;
+      float m = -INFINITY, lsum = 0.f, m_o = -INFINITY;
+      for (int kb = 0; kb <= qb; ++kb, ++sc) {
+        const uint32_t sb = sc & 1;
+        wait(B_(B_SFULL + sb), (sc >> 1) & 1, SITE_TC_ACC_FULL);
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t ts = tc.tmem_base + lane_off + TM_S + sb * BKEY;
+        const bool diag = (kb == qb);
+        // the whole row of S (128 fp32 columns) in four loads and one wait
+        uint32_t sr[BKEY];
+#pragma unroll
+        for (int c = 0; c < BKEY / 32; ++c) tmem_ld32_async(ts + c * 32, sr + c * 32);
+        tmem_wait_ld();
+        // diagonal block: keys after the row's query are masked as -inf (their
+        // probability is then exactly 0)
+        if (diag) {
+#pragma unroll
+          for (int i = 0; i < BKEY; ++i)
+            if (i > r) sr[i] = 0xff800000u;
+        }
+        // row maximum with eight independent partial maxima
+        float mx8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(sr[u]);
+#pragma unroll
+        for (int i = 8; i < BKEY; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float mn = fmaxf(m, mx * sc_l2);
+        // probabilities against the new maximum (eight partial row sums) and
+        // the bf16 P tile
+        float rs8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+        const uint32_t pbase = sbase + P_OFF + sb * P_BUF;
+#pragma unroll
+        for (int c = 0; c < BKEY / 32; ++c) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int k = c * 32 + i;
+            const float p0 = ex2(fmaf(__uint_as_float(sr[k]), sc_l2, -mn));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[k + 1]), sc_l2, -mn));
+            rs8[(k >> 1) & 7] += p0 + p1;
+            w[i >> 1] = pack2(p0, p1);
+          }
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            st_shared_v4(pbase + p_chunk_off(r, c * 32 + g * 8), w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+        }
+        const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+        // the S buffer is read and the P tile written (generic proxy -> tensor core)
+        tc_fence_before();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(B_(B_SEMPTY + sb));
+          mbar_arrive(B_(B_PFULL + sb));
+        }
+        const float m_prev = m;                    // the maximum P_{kb-1} was taken against
+        lsum = (m == -INFINITY ? 0.f : lsum * exp2f(m - mn)) + rs;
+        m = mn;
+        if (kb > 0) add_pv(o, m_o, sc - 1, m_prev);
+      }
+      add_pv(o, m_o, sc - 1, m);                   // the item's last block
+      // normalise, store the output row and the log-sum-exp
+      const float inv = 1.f / lsum;
+      const long long t = (long long)b * j.S + qb * BQ + r;
+      uint4* dst = reinterpret_cast<uint4*>(j.o + t * j.hq + h * HD);
+#pragma unroll
+      for (int g = 0; g < HD / 8; ++g)
+        dst[g] = make_uint4(pack2(o[8 * g] * inv, o[8 * g + 1] * inv), pack2(o[8 * g + 2] * inv, o[8 * g + 3] * inv),
+                            pack2(o[8 * g + 4] * inv, o[8 * g + 5] * inv), pack2(o[8 * g + 6] * inv, o[8 * g + 7] * inv));
+      j.lse[((long long)b * j.H + h) * j.S + qb * BQ + r] = (m + log2f(lsum)) / LOG2E;
+      if (j.sig) {
+        // every row of the block is stored: publish it
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        if (threadIdx.x == 128) dep_signal(j.sig + b * nqb + qb);
+      }
+    }
+  }
+  __syncthreads();
+  s.next(items);
+}
+
+}  // namespace attn_tm

@@ -296,6 +296,7 @@ int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m
   memcpy(a->aoff, P.aoff, sizeof(a->aoff));
   a->use_tc = want_tc ? 1 : 0;
   a->use_tc_attn = bf16 && !(hp->flags & MT_FLAG_SIMT_ATTN) && hp->head_dim == 64 && hp->seq % 128 == 0;
+  a->use_tm_attn = a->use_tc && a->use_tc_attn && !(hp->flags & MT_FLAG_MMA_SYNC_ATTN);
   // counters need whole 128-row blocks on both sides of every hand-off
   a->deps = a->use_tc && a->use_tc_attn && !(hp->flags & MT_FLAG_BARRIERS_ONLY);
   if (want_tc) {

@@ -17,6 +17,7 @@
 #include "attn_simt.cuh"
 #include "gemm_tc.cuh"
 #include "attn_tc.cuh"
+#include "attn_tm.cuh"
 #include "rows.cuh"
 #include <type_traits>
 
@@ -1266,8 +1267,17 @@ __device__ __forceinline__ attn_tc::Args attn_tc_args(const KArgs& a, int l) {
 }
 
 template <class OP>
-__device__ __forceinline__ void run_attn_fwd(const KArgs& a, int l, Sched& s, char* smem, const AttnDeps& dp) {
+__device__ __forceinline__ void run_attn_fwd(const KArgs& a, int l, Sched& s, char* smem, const TcState& tc,
+                                             const AttnDeps& dp) {
   if constexpr (sizeof(OP) == 2) {
+    if (a.use_tm_attn) {
+      const MtDims& D = a.D;
+      attn_tm::Job j{&a.maps[MAP_QKV], l * D.T, abuf<__nv_bfloat16>(a, A_O) + (long long)l * D.T * D.hq,
+                     abuf<float>(a, A_LSE) + (long long)l * D.B * D.H * D.S, D.B, D.H, D.S, D.hq,
+                     1.0f / sqrtf((float)D.hd), dp.wait, dp.wtarget, dp.sig, dp.hdr, dp.timeout_ns};
+      attn_tm::fwd_job(j, s, smem, tc);
+      return;
+    }
     if (a.use_tc_attn) { attn_tc_fwd_job<OP>(attn_tc_args<OP>(a, l), s, smem, dp); return; }
   }
   const AttnArgs t = attn_args<OP>(a, l);
@@ -1353,7 +1363,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
       run_gemm<OP>(a, g, s, smem, tc); TJ(2);
     }
     if (!dep) MT_SYNC();
-    run_attn_fwd<OP>(a, l, s, smem, attn_deps(l, TK_ATTN_FWD, true)); TJ(3);
+    run_attn_fwd<OP>(a, l, s, smem, tc, attn_deps(l, TK_ATTN_FWD, true)); TJ(3);
     if (!dep) MT_SYNC();
     {
       GemmDesc g = gm.wo(l);

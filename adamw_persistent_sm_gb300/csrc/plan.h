@@ -74,7 +74,7 @@ enum ArenaId {
 // coordinate of a map over the whole stack.
 enum MapId {
   MAP_R = 0, MAP_WQKV, MAP_O, MAP_WO, MAP_XS, MAP_WGATE, MAP_WUP, MAP_ACT, MAP_WDOWN, MAP_RF,
-  MAP_WLM, MAP_DLOGITS, MAP_DY, MAP_DGU, MAP_DXO, MAP_DQKV, MAP_COUNT
+  MAP_WLM, MAP_DLOGITS, MAP_DY, MAP_DGU, MAP_DXO, MAP_DQKV, MAP_QKV, MAP_DOUT, MAP_COUNT
 };
 
 struct MtDims {
@@ -153,6 +153,7 @@ struct KArgs {
   const int* dbg_offs;
   int use_tc;                   // tcgen05 GEMMs (bf16 only)
   int use_tc_attn;              // tensor-core attention (bf16 only)
+  int use_tm_attn;              // attention forward on tcgen05 with TMEM accumulators (needs use_tc)
   int deps;                     // dependency counters replace the grid barriers they cover
   CUtensorMap maps[MT_NMAPS];
 };

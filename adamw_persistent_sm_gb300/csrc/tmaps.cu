@@ -68,6 +68,8 @@ int mt_build_tensor_maps(KArgs* a, void* shadow) {
   ok &= encode(&a->maps[MAP_DGU], A(A_DGU), Pm, 2 * F);
   ok &= encode(&a->maps[MAP_DXO], A(A_DXO), T, d);
   ok &= encode(&a->maps[MAP_DQKV], A(A_DQKV), T, 3 * hq);
+  ok &= encode(&a->maps[MAP_QKV], A(A_QKV), L * T, 3 * hq);
+  ok &= encode(&a->maps[MAP_DOUT], A(A_DO), T, hq);
   return ok ? MT_OK : MT_ERR_ARG;
 }
 

@@ -60,9 +60,11 @@ enum {
   MT_FLAG_NO_OPTIMIZER = 1u << 3, /* skip clip + AdamW even on the last microbatch */
   MT_FLAG_TEST_STALL = 1u << 4,   /* test only: CTA 0 never arrives at the first grid
                                      barrier, so the others' bounded waits run out */
-  MT_FLAG_BARRIERS_ONLY = 1u << 5 /* separate every phase by a grid barrier, even where
+  MT_FLAG_BARRIERS_ONLY = 1u << 5, /* separate every phase by a grid barrier, even where
                                      per-block dependency counters would do (same
                                      results bit for bit; for comparison) */
+  MT_FLAG_MMA_SYNC_ATTN = 1u << 6 /* bf16 mode: attention forward on warp-level mma.sync
+                                     instead of tcgen05 with TMEM accumulators */
 };
 
 /*
