@@ -145,7 +145,7 @@ struct Args {
   bf* o;           // [T][hq]
   float* lse;      // [B*H][S]
   const bf* dout;  // [T][hq]
-  const float* dsum;  // [T][H] rowsum(dO * O)
+  const float* dsum;  // [B*H][S] rowsum(dO * O)
   bf* dqkv;        // [T][3hq]
   const float* rope;  // [S][32][2]
   int B, H, S, hq;
@@ -277,8 +277,8 @@ static __device__ void dq_item(const Args& a, int b, int h, int qb, char* smem) 
   fetch(0);
   const float* Lr = a.lse + ((long long)b * a.H + h) * a.S;
   const float lse0 = Lr[qw + g] * LOG2E, lse1 = Lr[qw + g + 8] * LOG2E;
-  const float* Dr = a.dsum + ((long long)b * a.S) * a.H + h;
-  const float D0 = Dr[(long long)(qw + g) * a.H], D1 = Dr[(long long)(qw + g + 8) * a.H];
+  const float* Dr = a.dsum + ((long long)b * a.H + h) * a.S;
+  const float D0 = Dr[qw + g], D1 = Dr[qw + g + 8];
   uint32_t qa[4][4], da[4][4];
   float dq[8][4];
   zero(dq);
@@ -337,7 +337,7 @@ static __device__ void dkdv_item(const Args& a, int b, int h, int kb, char* smem
   const bf* base = a.qkv + (long long)b * a.S * ld;
   const int k0 = kb * 128, kw = k0 + warp * 16;
   const float* Lr = a.lse + ((long long)b * a.H + h) * a.S;
-  const float* Dr = a.dsum + ((long long)b * a.S) * a.H + h;
+  const float* Dr = a.dsum + ((long long)b * a.H + h) * a.S;
   const int nqb = (a.S - k0) / 64;
   auto fetch = [&](int i) {
     const int q0 = k0 + i * 64;
@@ -348,7 +348,7 @@ static __device__ void dkdv_item(const Args& a, int b, int h, int kb, char* smem
     float* ldbuf = sLD + (i & 1) * 128;
     if (threadIdx.x < 64) {
       ldbuf[threadIdx.x] = Lr[q0 + threadIdx.x] * LOG2E;
-      ldbuf[64 + threadIdx.x] = Dr[(long long)(q0 + threadIdx.x) * a.H];
+      ldbuf[64 + threadIdx.x] = Dr[q0 + threadIdx.x];
     }
   };
   load_tile(sK, base + (long long)k0 * ld + a.hq + h * HD, ld, 128);

@@ -361,4 +361,462 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
   s.next(items);
 }
 
+
+// ===========================================================================
+// Backward ("How a training megakernel works", section "1 - Describe the
+// model and update": the backward of bf16_sdpa.sdpa).  P is recomputed from
+// the saved log-sum-exp; D = rowsum(dO * O) comes from the dO product's
+// epilogue.  Two item families, so that every output row is written once
+// and without atomics:
+//   dK/dV : 128 keys per item, 64-query steps.  S^T = K Q^T and
+//           dP^T = V dO^T go to TMEM (two buffers each); the softmax warps
+//           (one key row per thread) write P^T and dS^T = P^T (dP^T - D) as
+//           bf16 tiles; dV += P^T dO and dK += dS^T Q accumulate in TMEM.
+//   dQ    : 128 queries per item, 64-key steps.  S = Q K^T and dP = dO V^T
+//           in TMEM; the softmax warps (one query row per thread) write
+//           dS = P (dP - D); dQ += dS K accumulates in TMEM.
+// dK and dQ are scaled by the softmax scale and the rotary embedding is
+// undone on them before they are stored (bf16 rows of dqkv).
+// ===========================================================================
+struct BwdJob {
+  const CUtensorMap* map_qkv;  // q,k,v of all layers
+  const CUtensorMap* map_do;   // dO [T][hq]
+  int y0;                      // row of token 0 of this layer in map_qkv
+  const float* lse;            // [B*H][S] (natural log)
+  const float* dsum;           // [B*H][S]
+  __nv_bfloat16* dqkv;         // [T][3hq]
+  const float* rope;           // [S][32][2] cos, sin
+  int B, H, S, hq;
+  float scale;
+  ArenaHdr* hdr;
+  long long timeout_ns;
+};
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Undo the rotary embedding on a 64-wide gradient row at position pos and
+// store it as bf16 (dims i and i + 32 form a pair).
+__device__ __forceinline__ void store_grad_row(__nv_bfloat16* dst, float* g, const float* rope, int pos, float scale) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float cs = rope[((long long)pos * 32 + i) * 2 + 0], sn = rope[((long long)pos * 32 + i) * 2 + 1];
+    const float d1 = g[i] * scale, d2 = g[i + 32] * scale;
+    g[i] = d1 * cs + d2 * sn;
+    g[i + 32] = d2 * cs - d1 * sn;
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    d[q] = make_uint4(pack2(g[8 * q], g[8 * q + 1]), pack2(g[8 * q + 2], g[8 * q + 3]), pack2(g[8 * q + 4], g[8 * q + 5]),
+                      pack2(g[8 * q + 6], g[8 * q + 7]));
+}
+__device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const float* g) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    d[q] = make_uint4(pack2(g[8 * q], g[8 * q + 1]), pack2(g[8 * q + 2], g[8 * q + 3]), pack2(g[8 * q + 4], g[8 * q + 5]),
+                      pack2(g[8 * q + 6], g[8 * q + 7]));
+}
+
+namespace kv {   // dK/dV layout
+constexpr int NST = 4;                              // query-step ring stages
+constexpr uint32_t K_OFF = 1024, V_OFF = K_OFF + TILE;
+constexpr uint32_t ST_OFF = V_OFF + TILE;            // stage: Q 8 KB | dO 8 KB | lse 256 B | D 256 B
+constexpr uint32_t ST_BYTES = 17408;
+constexpr uint32_t P_OFF = ST_OFF + NST * ST_BYTES;   // 2 x P^T (128 keys x 64 queries)
+constexpr uint32_t DS_OFF = P_OFF + 2 * TILE;         // 2 x dS^T
+constexpr uint32_t END = DS_OFF + 2 * TILE;
+static_assert(END <= MT_TC_SMEM, "dK/dV tiles exceed the shared-memory window");
+static_assert(P_OFF % 1024 == 0 && ST_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+enum { KVFULL = 0, KVEMPTY, ACCFULL, ACCEMPTY, STFULL = 4, STEMPTY = STFULL + NST, SDFULL = STEMPTY + NST,
+       SDEMPTY = SDFULL + 2, PDFULL = SDEMPTY + 2, PDEMPTY = PDFULL + 2, COUNT = PDEMPTY + 2 };
+// TMEM: S^T at 0/64, dP^T at 128/192, dV at 256, dK at 320
+constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 320;
+}
+
+static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* smem, const TcState& tc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  auto B_ = [&](int i) { return sbase + 8u * (uint32_t)i; };
+  const long long tmo = j.timeout_ns;
+  const int nkb = j.S / 128;
+  const int items = j.B * j.H * nkb;
+  const int first = s.first(), G = s.G;
+  // item: longest (first key blocks) first
+  auto item_of = [&](int it, int& b, int& h, int& kb) {
+    kb = it / (j.B * j.H);
+    const int bh = it % (j.B * j.H);
+    b = bh / j.H; h = bh % j.H;
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(B_(kv::KVFULL), 1); mbar_init(B_(kv::KVEMPTY), 1);
+    mbar_init(B_(kv::ACCFULL), 1); mbar_init(B_(kv::ACCEMPTY), 4);
+    for (int i = 0; i < kv::NST; ++i) { mbar_init(B_(kv::STFULL + i), 1); mbar_init(B_(kv::STEMPTY + i), 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(B_(kv::SDFULL + i), 1); mbar_init(B_(kv::SDEMPTY + i), 4);
+      mbar_init(B_(kv::PDFULL + i), 4); mbar_init(B_(kv::PDEMPTY + i), 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  bool dead = false;
+  auto wait = [&](uint32_t b_, uint32_t par, int site) {
+    if (!dead && !mbar_wait(b_, par, tmo)) { set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, site); dead = true; }
+  };
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- loads ----------------
+      uint32_t c = 0, ni = 0;
+      for (int it = first; it < items; it += G, ++ni) {
+        int b, h, kb;
+        item_of(it, b, h, kb);
+        const int row0 = b * j.S;
+        wait(B_(kv::KVEMPTY), (ni & 1) ^ 1, SITE_TC_EMPTY);
+        mbar_expect_tx(B_(kv::KVFULL), 2 * TILE);
+        for (int half = 0; half < 2; ++half) {
+          tma_load_2d(sbase + kv::K_OFF + half * 8192, j.map_qkv, j.hq + h * HD, j.y0 + row0 + kb * 128 + half * 64, B_(kv::KVFULL));
+          tma_load_2d(sbase + kv::V_OFF + half * 8192, j.map_qkv, 2 * j.hq + h * HD, j.y0 + row0 + kb * 128 + half * 64,
+                      B_(kv::KVFULL));
+        }
+        const int nst = (j.S - kb * 128) / 64;
+        const float* lrow = j.lse + ((long long)b * j.H + h) * j.S;
+        const float* drow = j.dsum + ((long long)b * j.H + h) * j.S;
+        for (int i = 0; i < nst; ++i, ++c) {
+          const int q0 = kb * 128 + i * 64;
+          const uint32_t st = c % kv::NST, sa = sbase + kv::ST_OFF + st * kv::ST_BYTES;
+          wait(B_(kv::STEMPTY + st), ((c / kv::NST) & 1) ^ 1, SITE_TC_EMPTY);
+          mbar_expect_tx(B_(kv::STFULL + st), 2 * 8192 + 512);
+          tma_load_2d(sa, j.map_qkv, h * HD, j.y0 + row0 + q0, B_(kv::STFULL + st));
+          tma_load_2d(sa + 8192, j.map_do, h * HD, row0 + q0, B_(kv::STFULL + st));
+          bulk_load(sa + 16384, lrow + q0, 256, B_(kv::STFULL + st));
+          bulk_load(sa + 16640, drow + q0, 256, B_(kv::STFULL + st));
+        }
+      }
+      if (!dead) {
+        for (uint32_t x = c > kv::NST ? c - kv::NST : 0; x < c; ++x) wait(B_(kv::STFULL + x % kv::NST), (x / kv::NST) & 1, SITE_TC_DRAIN);
+        if (ni > 0) wait(B_(kv::KVFULL), (ni - 1) & 1, SITE_TC_DRAIN);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA ----------------
+      const uint32_t id_sd = idesc_bf16(128, 64, 0, 0);     // K (or V) x Q^T (or dO^T)
+      const uint32_t id_acc = idesc_bf16(128, 64, 0, 1);    // P^T (or dS^T) x dO (or Q), MN-major B
+      uint32_t c = 0, ni = 0, last_bar = 0, last_par = 0;
+      auto issue_sd = [&](uint32_t cc) {
+        const uint32_t st = cc % kv::NST, sb = cc & 1, sa = sbase + kv::ST_OFF + st * kv::ST_BYTES;
+        wait(B_(kv::STFULL + st), (cc / kv::NST) & 1, SITE_TC_FULL);
+        wait(B_(kv::SDEMPTY + sb), ((cc >> 1) & 1) ^ 1, SITE_TC_ACC_EMPTY);
+        tc_fence_after();
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          mma_bf16(tc.tmem_base + kv::TM_S + sb * 64, sdesc(sbase + kv::K_OFF + kk * 32, 16, 1024), sdesc(sa + kk * 32, 16, 1024),
+                   id_sd, kk > 0 ? 1u : 0u);
+          mma_bf16(tc.tmem_base + kv::TM_DP + sb * 64, sdesc(sbase + kv::V_OFF + kk * 32, 16, 1024),
+                   sdesc(sa + 8192 + kk * 32, 16, 1024), id_sd, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(B_(kv::SDFULL + sb));
+      };
+      for (int it = first; it < items; it += G, ++ni) {
+        int b, h, kb;
+        item_of(it, b, h, kb);
+        const int nst = (j.S - kb * 128) / 64;
+        wait(B_(kv::KVFULL), ni & 1, SITE_TC_FULL);
+        issue_sd(c);
+        for (int i = 0; i < nst; ++i, ++c) {
+          if (i + 1 < nst) issue_sd(c + 1);
+          const uint32_t st = c % kv::NST, sb = c & 1, sa = sbase + kv::ST_OFF + st * kv::ST_BYTES;
+          wait(B_(kv::PDFULL + sb), (c >> 1) & 1, SITE_TC_FULL);
+          if (i == 0) wait(B_(kv::ACCEMPTY), (ni & 1) ^ 1, SITE_TC_ACC_EMPTY);   // dK, dV of the last item are read
+          tc_fence_after();
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+            mma_bf16(tc.tmem_base + kv::TM_DV, sdesc(sbase + kv::P_OFF + sb * TILE + kk * 32, 16, 1024),
+                     sdesc(sa + 8192 + kk * 2048, 8192, 1024), id_acc, acc);
+            mma_bf16(tc.tmem_base + kv::TM_DK, sdesc(sbase + kv::DS_OFF + sb * TILE + kk * 32, 16, 1024),
+                     sdesc(sa + kk * 2048, 8192, 1024), id_acc, acc);
+          }
+          mma_commit(B_(kv::PDEMPTY + sb));
+          mma_commit(B_(kv::STEMPTY + st));
+          last_bar = B_(kv::STEMPTY + st);
+          last_par = (c / kv::NST) & 1;
+        }
+        mma_commit(B_(kv::ACCFULL));
+        mma_commit(B_(kv::KVEMPTY));
+      }
+      if (last_bar && !dead && !mbar_wait(last_bar, last_par, tmo)) set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_DRAIN);
+      if (ni > 0) wait(B_(kv::KVEMPTY), (ni - 1) & 1, SITE_TC_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------- softmax and output: one key row per thread ----------------
+    const int q = warp - 4, r = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const float sc_l2 = j.scale * LOG2E;
+    uint32_t c = 0, ni = 0;
+    for (int it = first; it < items; it += G, ++ni) {
+      int b, h, kb;
+      item_of(it, b, h, kb);
+      const int nst = (j.S - kb * 128) / 64;
+      for (int i = 0; i < nst; ++i, ++c) {
+        const uint32_t st = c % kv::NST, sb = c & 1, sa = sbase + kv::ST_OFF + st * kv::ST_BYTES;
+        wait(B_(kv::SDFULL + sb), (c >> 1) & 1, SITE_TC_ACC_FULL);
+        wait(B_(kv::STFULL + st), (c / kv::NST) & 1, SITE_TC_ACC_FULL);      // lse and D of the step
+        __syncwarp();
+        tc_fence_after();
+        uint32_t sv[64], dp[64];
+        tmem_ld32_async(tc.tmem_base + lane_off + kv::TM_S + sb * 64, sv);
+        tmem_ld32_async(tc.tmem_base + lane_off + kv::TM_S + sb * 64 + 32, sv + 32);
+        tmem_ld32_async(tc.tmem_base + lane_off + kv::TM_DP + sb * 64, dp);
+        tmem_ld32_async(tc.tmem_base + lane_off + kv::TM_DP + sb * 64 + 32, dp + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B_(kv::SDEMPTY + sb));
+        const float* sl = reinterpret_cast<const float*>(smem + kv::ST_OFF + st * kv::ST_BYTES + 16384);
+        const float* sd = sl + 64;
+        // queries q0 + x with q0 + x < key are masked (only the first two steps)
+        const int lim = r - i * 64;            // x < lim is masked
+        wait(B_(kv::PDEMPTY + sb), ((c >> 1) & 1) ^ 1, SITE_TC_EMPTY);
+        const uint32_t pb = sbase + kv::P_OFF + sb * TILE, db = sbase + kv::DS_OFF + sb * TILE;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          uint32_t wp[4], wd[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int x = g * 8 + e;
+            float p0 = ex2(fmaf(__uint_as_float(sv[x]), sc_l2, -sl[x] * LOG2E));
+            float p1 = ex2(fmaf(__uint_as_float(sv[x + 1]), sc_l2, -sl[x + 1] * LOG2E));
+            if (x < lim) p0 = 0.f;
+            if (x + 1 < lim) p1 = 0.f;
+            const float d0 = p0 * (__uint_as_float(dp[x]) - sd[x]);
+            const float d1 = p1 * (__uint_as_float(dp[x + 1]) - sd[x + 1]);
+            wp[e >> 1] = pack2(p0, p1);
+            wd[e >> 1] = pack2(d0, d1);
+          }
+          st_shared_v4(pb + p_chunk_off(r, g * 8), wp[0], wp[1], wp[2], wp[3]);
+          st_shared_v4(db + p_chunk_off(r, g * 8), wd[0], wd[1], wd[2], wd[3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B_(kv::PDFULL + sb));
+      }
+      // dK, dV of the item's 128 keys
+      wait(B_(kv::ACCFULL), ni & 1, SITE_TC_ACC_FULL);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t vk[64], vv[64];
+      tmem_ld32_async(tc.tmem_base + lane_off + kv::TM_DK, vk);
+      tmem_ld32_async(tc.tmem_base + lane_off + kv::TM_DK + 32, vk + 32);
+      tmem_ld32_async(tc.tmem_base + lane_off + kv::TM_DV, vv);
+      tmem_ld32_async(tc.tmem_base + lane_off + kv::TM_DV + 32, vv + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B_(kv::ACCEMPTY));
+      const int key = kb * 128 + r;
+      __nv_bfloat16* row = j.dqkv + ((long long)b * j.S + key) * (3LL * j.hq);
+      float g[64];
+#pragma unroll
+      for (int x = 0; x < 64; ++x) g[x] = __uint_as_float(vk[x]);
+      store_grad_row(row + j.hq + h * HD, g, j.rope, key, j.scale);
+#pragma unroll
+      for (int x = 0; x < 64; ++x) g[x] = __uint_as_float(vv[x]);
+      store_row64(row + 2 * j.hq + h * HD, g);
+    }
+  }
+  __syncthreads();
+  s.next(items);
+}
+
+namespace qd {   // dQ layout
+constexpr int NST = 4;                              // key-step ring stages: K 8 KB | V 8 KB
+constexpr uint32_t Q_OFF = 1024, DO_OFF = Q_OFF + TILE;
+constexpr uint32_t ST_OFF = DO_OFF + TILE;
+constexpr uint32_t ST_BYTES = 16384;
+constexpr uint32_t DS_OFF = ST_OFF + NST * ST_BYTES;  // 2 x dS (128 queries x 64 keys)
+constexpr uint32_t END = DS_OFF + 2 * TILE;
+static_assert(END <= MT_TC_SMEM, "dQ tiles exceed the shared-memory window");
+enum { QFULL = 0, QEMPTY, ACCFULL, ACCEMPTY, STFULL = 4, STEMPTY = STFULL + NST, SDFULL = STEMPTY + NST,
+       SDEMPTY = SDFULL + 2, DSFULL = SDEMPTY + 2, DSEMPTY = DSFULL + 2, COUNT = DSEMPTY + 2 };
+constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256;
+}
+
+static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem, const TcState& tc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  auto B_ = [&](int i) { return sbase + 8u * (uint32_t)i; };
+  const long long tmo = j.timeout_ns;
+  const int nqb = j.S / 128;
+  const int items = j.B * j.H * nqb;
+  const int first = s.first(), G = s.G;
+  // item: longest (last query blocks) first
+  auto item_of = [&](int it, int& b, int& h, int& qb) {
+    qb = nqb - 1 - it / (j.B * j.H);
+    const int bh = it % (j.B * j.H);
+    b = bh / j.H; h = bh % j.H;
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(B_(qd::QFULL), 1); mbar_init(B_(qd::QEMPTY), 1);
+    mbar_init(B_(qd::ACCFULL), 1); mbar_init(B_(qd::ACCEMPTY), 4);
+    for (int i = 0; i < qd::NST; ++i) { mbar_init(B_(qd::STFULL + i), 1); mbar_init(B_(qd::STEMPTY + i), 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(B_(qd::SDFULL + i), 1); mbar_init(B_(qd::SDEMPTY + i), 4);
+      mbar_init(B_(qd::DSFULL + i), 4); mbar_init(B_(qd::DSEMPTY + i), 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  bool dead = false;
+  auto wait = [&](uint32_t b_, uint32_t par, int site) {
+    if (!dead && !mbar_wait(b_, par, tmo)) { set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, site); dead = true; }
+  };
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t c = 0, ni = 0;
+      for (int it = first; it < items; it += G, ++ni) {
+        int b, h, qb;
+        item_of(it, b, h, qb);
+        const int row0 = b * j.S;
+        wait(B_(qd::QEMPTY), (ni & 1) ^ 1, SITE_TC_EMPTY);
+        mbar_expect_tx(B_(qd::QFULL), 2 * TILE);
+        for (int half = 0; half < 2; ++half) {
+          tma_load_2d(sbase + qd::Q_OFF + half * 8192, j.map_qkv, h * HD, j.y0 + row0 + qb * 128 + half * 64, B_(qd::QFULL));
+          tma_load_2d(sbase + qd::DO_OFF + half * 8192, j.map_do, h * HD, row0 + qb * 128 + half * 64, B_(qd::QFULL));
+        }
+        const int nst = 2 * (qb + 1);
+        for (int i = 0; i < nst; ++i, ++c) {
+          const uint32_t st = c % qd::NST, sa = sbase + qd::ST_OFF + st * qd::ST_BYTES;
+          wait(B_(qd::STEMPTY + st), ((c / qd::NST) & 1) ^ 1, SITE_TC_EMPTY);
+          mbar_expect_tx(B_(qd::STFULL + st), 2 * 8192);
+          tma_load_2d(sa, j.map_qkv, j.hq + h * HD, j.y0 + row0 + i * 64, B_(qd::STFULL + st));
+          tma_load_2d(sa + 8192, j.map_qkv, 2 * j.hq + h * HD, j.y0 + row0 + i * 64, B_(qd::STFULL + st));
+        }
+      }
+      if (!dead) {
+        for (uint32_t x = c > qd::NST ? c - qd::NST : 0; x < c; ++x) wait(B_(qd::STFULL + x % qd::NST), (x / qd::NST) & 1, SITE_TC_DRAIN);
+        if (ni > 0) wait(B_(qd::QFULL), (ni - 1) & 1, SITE_TC_DRAIN);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_sd = idesc_bf16(128, 64, 0, 0);     // Q (or dO) x K^T (or V^T)
+      const uint32_t id_acc = idesc_bf16(128, 64, 0, 1);    // dS x K, MN-major B
+      uint32_t c = 0, ni = 0, last_bar = 0, last_par = 0;
+      auto issue_sd = [&](uint32_t cc) {
+        const uint32_t st = cc % qd::NST, sb = cc & 1, sa = sbase + qd::ST_OFF + st * qd::ST_BYTES;
+        wait(B_(qd::STFULL + st), (cc / qd::NST) & 1, SITE_TC_FULL);
+        wait(B_(qd::SDEMPTY + sb), ((cc >> 1) & 1) ^ 1, SITE_TC_ACC_EMPTY);
+        tc_fence_after();
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          mma_bf16(tc.tmem_base + qd::TM_S + sb * 64, sdesc(sbase + qd::Q_OFF + kk * 32, 16, 1024), sdesc(sa + kk * 32, 16, 1024),
+                   id_sd, kk > 0 ? 1u : 0u);
+          mma_bf16(tc.tmem_base + qd::TM_DP + sb * 64, sdesc(sbase + qd::DO_OFF + kk * 32, 16, 1024),
+                   sdesc(sa + 8192 + kk * 32, 16, 1024), id_sd, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(B_(qd::SDFULL + sb));
+      };
+      for (int it = first; it < items; it += G, ++ni) {
+        int b, h, qb;
+        item_of(it, b, h, qb);
+        const int nst = 2 * (qb + 1);
+        wait(B_(qd::QFULL), ni & 1, SITE_TC_FULL);
+        issue_sd(c);
+        for (int i = 0; i < nst; ++i, ++c) {
+          if (i + 1 < nst) issue_sd(c + 1);
+          else mma_commit(B_(qd::QEMPTY));                    // Q and dO are free after the last S, dP
+          const uint32_t st = c % qd::NST, sb = c & 1, sa = sbase + qd::ST_OFF + st * qd::ST_BYTES;
+          wait(B_(qd::DSFULL + sb), (c >> 1) & 1, SITE_TC_FULL);
+          if (i == 0) wait(B_(qd::ACCEMPTY), (ni & 1) ^ 1, SITE_TC_ACC_EMPTY);
+          tc_fence_after();
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tc.tmem_base + qd::TM_DQ, sdesc(sbase + qd::DS_OFF + sb * TILE + kk * 32, 16, 1024),
+                     sdesc(sa + kk * 2048, 8192, 1024), id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(B_(qd::DSEMPTY + sb));
+          mma_commit(B_(qd::STEMPTY + st));
+          last_bar = B_(qd::STEMPTY + st);
+          last_par = (c / qd::NST) & 1;
+        }
+        mma_commit(B_(qd::ACCFULL));
+      }
+      if (last_bar && !dead && !mbar_wait(last_bar, last_par, tmo)) set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_DRAIN);
+      if (ni > 0) wait(B_(qd::QEMPTY), (ni - 1) & 1, SITE_TC_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------- softmax and output: one query row per thread ----------------
+    const int q = warp - 4, r = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const float sc_l2 = j.scale * LOG2E;
+    uint32_t c = 0, ni = 0;
+    for (int it = first; it < items; it += G, ++ni) {
+      int b, h, qb;
+      item_of(it, b, h, qb);
+      const int nst = 2 * (qb + 1);
+      const int query = qb * 128 + r;
+      const long long lrow = ((long long)b * j.H + h) * j.S + query;
+      const float lse2 = j.lse[lrow] * LOG2E, dd = j.dsum[lrow];
+      for (int i = 0; i < nst; ++i, ++c) {
+        const uint32_t sb = c & 1;
+        wait(B_(qd::SDFULL + sb), (c >> 1) & 1, SITE_TC_ACC_FULL);
+        __syncwarp();
+        tc_fence_after();
+        uint32_t sv[64], dp[64];
+        tmem_ld32_async(tc.tmem_base + lane_off + qd::TM_S + sb * 64, sv);
+        tmem_ld32_async(tc.tmem_base + lane_off + qd::TM_S + sb * 64 + 32, sv + 32);
+        tmem_ld32_async(tc.tmem_base + lane_off + qd::TM_DP + sb * 64, dp);
+        tmem_ld32_async(tc.tmem_base + lane_off + qd::TM_DP + sb * 64 + 32, dp + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B_(qd::SDEMPTY + sb));
+        // keys i*64 + x > query are masked
+        const int lim = query - i * 64;        // x > lim is masked
+        wait(B_(qd::DSEMPTY + sb), ((c >> 1) & 1) ^ 1, SITE_TC_EMPTY);
+        const uint32_t db = sbase + qd::DS_OFF + sb * TILE;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          uint32_t wd[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int x = g * 8 + e;
+            float p0 = ex2(fmaf(__uint_as_float(sv[x]), sc_l2, -lse2));
+            float p1 = ex2(fmaf(__uint_as_float(sv[x + 1]), sc_l2, -lse2));
+            if (x > lim) p0 = 0.f;
+            if (x + 1 > lim) p1 = 0.f;
+            wd[e >> 1] = pack2(p0 * (__uint_as_float(dp[x]) - dd), p1 * (__uint_as_float(dp[x + 1]) - dd));
+          }
+          st_shared_v4(db + p_chunk_off(r, g * 8), wd[0], wd[1], wd[2], wd[3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B_(qd::DSFULL + sb));
+      }
+      wait(B_(qd::ACCFULL), ni & 1, SITE_TC_ACC_FULL);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t vq[64];
+      tmem_ld32_async(tc.tmem_base + lane_off + qd::TM_DQ, vq);
+      tmem_ld32_async(tc.tmem_base + lane_off + qd::TM_DQ + 32, vq + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B_(qd::ACCEMPTY));
+      float g[64];
+#pragma unroll
+      for (int x = 0; x < 64; ++x) g[x] = __uint_as_float(vq[x]);
+      store_grad_row(j.dqkv + ((long long)b * j.S + query) * (3LL * j.hq) + h * HD, g, j.rope, query, j.scale);
+    }
+  }
+  __syncthreads();
+  s.next(items);
+}
+
 }  // namespace attn_tm

@@ -21,8 +21,9 @@ enum EpiKind {
   EPI_SWIGLU,         // tile = [64 gate | 64 up] columns -> g, u (out) and silu(g)*u (out2)
   EPI_SWIGLU_BWD,     // acc = d(silu(g)*u); aux = [g | u] -> out = [dg | du]
   EPI_GRAD,           // out(f32) = acc (+ out if accumulate); rows >= osplit go to out1
-  EPI_STORE_OP_D,     // out(op) = acc, and out2(f32)[m][head] = sum over the head's 64 columns of
-                      // op(acc) * aux(op)  (attention's D = rowsum(dO * O))
+  EPI_STORE_OP_D,     // out(op) = acc, and out2(f32)[batch][head][position] of row m = sum over the
+                      // head's 64 columns of op(acc) * aux(op)  (attention's D = rowsum(dO * O));
+                      // ldo2 = number of heads, S = positions per sequence
   EPI_NONE,           // test harness: accumulators are read and dropped
   EPI_LOGITS          // out(op) = acc (LM-head logits); per row and column tile, (max, sum exp(acc -
                       // max)) into cepart[m][n0 / tile width]; the target token's fp32 logit into cetgt[m]
@@ -242,7 +243,8 @@ __device__ void gemm_simt_tile(const GemmDesc& g, int seg, int m0, int n0, int k
         }
         dot = warp_sum(dot);
         const int n = n0 + hh * 64;
-        if (lane == 0 && n < g.N) ((float*)g.out2)[(long long)m * g.ldo2 + n / 64] = dot;
+        if (lane == 0 && n < g.N)
+          ((float*)g.out2)[((long long)(m / g.S) * g.ldo2 + n / 64) * g.S + (m % g.S)] = dot;
       }
     }
     __syncthreads();

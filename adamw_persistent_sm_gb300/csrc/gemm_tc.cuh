@@ -435,7 +435,8 @@ __device__ __forceinline__ void tc_epilogue(const EpiRegs& g, const TcTile& ti, 
       // 64-column heads
       bf* o = (bf*)g.out + (long long)m * g.ldo;
       const bf* ao = (const bf*)g.aux + (long long)m * g.ldaux;
-      float* dsum = (float*)g.out2 + (long long)m * g.ldo2;
+      // D is stored [batch][head][position] (the log-sum-exp's layout); ldo2 = heads
+      float* dsum = (float*)g.out2 + (long long)(m / g.S) * g.ldo2 * g.S + (m % g.S);
       for (int h2 = 0; h2 < TC_BN / 64; ++h2) {
         float x[64], oo[64];
         tmem_ld32(trow + h2 * 64, x);
@@ -446,7 +447,7 @@ __device__ __forceinline__ void tc_epilogue(const EpiRegs& g, const TcTile& ti, 
         float dot = 0.f;
 #pragma unroll
         for (int i = 0; i < 64; ++i) dot = fmaf(__bfloat162float(__float2bfloat16_rn(x[i])), oo[i], dot);
-        dsum[n / 64] = dot;
+        dsum[(long long)(n / 64) * g.S] = dot;
       }
       break;
     }

@@ -1285,8 +1285,19 @@ __device__ __forceinline__ void run_attn_fwd(const KArgs& a, int l, Sched& s, ch
   else attn_fwd_job<OP, 16>(t, s, (float*)smem);
 }
 template <class OP>
-__device__ __forceinline__ void run_attn_bwd(const KArgs& a, int l, Sched& s, char* smem, const AttnDeps& dp) {
+__device__ __forceinline__ void run_attn_bwd(const KArgs& a, int l, Sched& s, char* smem, const TcState& tc,
+                                             const AttnDeps& dp) {
   if constexpr (sizeof(OP) == 2) {
+    if (a.use_tm_attn) {
+      const MtDims& D = a.D;
+      attn_tm::BwdJob j{&a.maps[MAP_QKV], &a.maps[MAP_DOUT], l * D.T,
+                        abuf<float>(a, A_LSE) + (long long)l * D.B * D.H * D.S, abuf<float>(a, A_DSUM),
+                        abuf<__nv_bfloat16>(a, A_DQKV), abuf<float>(a, A_ROPE), D.B, D.H, D.S, D.hq,
+                        1.0f / sqrtf((float)D.hd), dp.hdr, dp.timeout_ns};
+      attn_tm::dkdv_job(j, s, smem, tc);
+      attn_tm::dq_job(j, s, smem, tc);
+      return;
+    }
     if (a.use_tc_attn) { attn_tc_bwd_job<OP>(attn_tc_args<OP>(a, l), s, smem, dp); return; }
   }
   const AttnArgs t = attn_args<OP>(a, l);
@@ -1448,7 +1459,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     job_colfinal(a, 0, D.E + 1, D.E, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d,
                  pgrad(a, P_MOE_NORM) + (long long)l * D.d, 1, s); TJ(18);
     job_ksplit_sum(a, pgrad(a, P_WO) + (long long)l * D.d * D.hq, D.d, D.hq, s); TJ(32);
-    run_attn_bwd<OP>(a, l, s, smem, attn_deps(l, TK_ATTN_BWD, false)); TJ(26);
+    run_attn_bwd<OP>(a, l, s, smem, tc, attn_deps(l, TK_ATTN_BWD, false)); TJ(26);
     MT_SYNC();
     run_gemm<OP>(a, gm.qkv_dgrad(l), s, smem, tc); TJ(27);
     run_gemm<OP>(a, gm.qkv_wgrad(l), s, smem, tc); TJ(28);

@@ -56,7 +56,7 @@ enum ArenaId {
   A_DXS,       // fp32 [Pmax][d] gradient wrt expert inputs
   A_DR2,       // fp32 [T][d] gradient wrt expert RMSNorm output
   A_DO,        // op   [T][hq] gradient wrt attention output
-  A_DSUM,      // fp32 [T][H] rowsum(dO * O) per head
+  A_DSUM,      // fp32 [B*H][S] rowsum(dO * O) of the attention backward
   A_DQKV,      // op   [T][3hq] gradient wrt q,k,v (before RoPE)
   A_DR,        // fp32 [T][d] gradient wrt attention RMSNorm output
   A_DRF,       // fp32 [T][d] gradient wrt final RMSNorm output

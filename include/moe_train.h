@@ -63,8 +63,8 @@ enum {
   MT_FLAG_BARRIERS_ONLY = 1u << 5, /* separate every phase by a grid barrier, even where
                                      per-block dependency counters would do (same
                                      results bit for bit; for comparison) */
-  MT_FLAG_MMA_SYNC_ATTN = 1u << 6 /* bf16 mode: attention forward on warp-level mma.sync
-                                     instead of tcgen05 with TMEM accumulators */
+  MT_FLAG_MMA_SYNC_ATTN = 1u << 6 /* bf16 mode: attention forward and backward on warp-level
+                                     mma.sync instead of tcgen05 with TMEM accumulators */
 };
 
 /*
