@@ -398,22 +398,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
-// Undo the rotary embedding on a 64-wide gradient row at position pos and
-// store it as bf16 (dims i and i + 32 form a pair).
-__device__ __forceinline__ void store_grad_row(__nv_bfloat16* dst, float* g, const float* rope, int pos, float scale) {
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float cs = rope[((long long)pos * 32 + i) * 2 + 0], sn = rope[((long long)pos * 32 + i) * 2 + 1];
-    const float d1 = g[i] * scale, d2 = g[i + 32] * scale;
-    g[i] = d1 * cs + d2 * sn;
-    g[i + 32] = d2 * cs - d1 * sn;
-  }
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-    d[q] = make_uint4(pack2(g[8 * q], g[8 * q + 1]), pack2(g[8 * q + 2], g[8 * q + 3]), pack2(g[8 * q + 4], g[8 * q + 5]),
-                      pack2(g[8 * q + 6], g[8 * q + 7]));
-}
 __device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const float* g) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -421,18 +405,39 @@ __device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const float* g) 
     d[q] = make_uint4(pack2(g[8 * q], g[8 * q + 1]), pack2(g[8 * q + 2], g[8 * q + 3]), pack2(g[8 * q + 4], g[8 * q + 5]),
                       pack2(g[8 * q + 6], g[8 * q + 7]));
 }
+// Undo the rotary embedding on a 64-wide gradient row at position pos (dims i
+// and i + 32 form a pair; table [pos][32][cos, sin]), scale, store as bf16.
+__device__ __forceinline__ void store_grad_row(__nv_bfloat16* dst, float* g, const float* rope, int pos, float scale) {
+  // all 32 (cos, sin) pairs of the position first: 16 independent 16-byte loads
+  const float4* tab = reinterpret_cast<const float4*>(rope + (long long)pos * 64);
+  float4 cs[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) cs[q] = tab[q];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int i = 2 * q;
+    float d1 = g[i] * scale, d2 = g[i + 32] * scale;
+    g[i] = d1 * cs[q].x + d2 * cs[q].y;
+    g[i + 32] = d2 * cs[q].x - d1 * cs[q].y;
+    d1 = g[i + 1] * scale;
+    d2 = g[i + 33] * scale;
+    g[i + 1] = d1 * cs[q].z + d2 * cs[q].w;
+    g[i + 33] = d2 * cs[q].z - d1 * cs[q].w;
+  }
+  store_row64(dst, g);
+}
 
 namespace kv {   // dK/dV layout
 constexpr int NST = 4;                              // query-step ring stages
-constexpr uint32_t K_OFF = 1024, V_OFF = K_OFF + TILE;
-constexpr uint32_t ST_OFF = V_OFF + TILE;            // stage: Q 8 KB | dO 8 KB | lse 256 B | D 256 B
+constexpr uint32_t KV_OFF = 1024;                    // 2 x (K 16 KB | V 16 KB): the next item's keys load early
+constexpr uint32_t ST_OFF = KV_OFF + 4 * TILE;       // stage: Q 8 KB | dO 8 KB | lse 256 B | D 256 B
 constexpr uint32_t ST_BYTES = 17408;
 constexpr uint32_t P_OFF = ST_OFF + NST * ST_BYTES;   // 2 x P^T (128 keys x 64 queries)
 constexpr uint32_t DS_OFF = P_OFF + 2 * TILE;         // 2 x dS^T
 constexpr uint32_t END = DS_OFF + 2 * TILE;
 static_assert(END <= MT_TC_SMEM, "dK/dV tiles exceed the shared-memory window");
-static_assert(P_OFF % 1024 == 0 && ST_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-enum { KVFULL = 0, KVEMPTY, ACCFULL, ACCEMPTY, STFULL = 4, STEMPTY = STFULL + NST, SDFULL = STEMPTY + NST,
+static_assert(P_OFF % 1024 == 0 && ST_OFF % 1024 == 0 && ST_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+enum { KVFULL = 0, KVEMPTY = 2, ACCFULL = 4, ACCEMPTY = 5, STFULL = 6, STEMPTY = STFULL + NST, SDFULL = STEMPTY + NST,
        SDEMPTY = SDFULL + 2, PDFULL = SDEMPTY + 2, PDEMPTY = PDFULL + 2, COUNT = PDEMPTY + 2 };
 // TMEM: S^T at 0/64, dP^T at 128/192, dV at 256, dK at 320
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 320;
@@ -453,7 +458,7 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
     b = bh / j.H; h = bh % j.H;
   };
   if (threadIdx.x == 0) {
-    mbar_init(B_(kv::KVFULL), 1); mbar_init(B_(kv::KVEMPTY), 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(B_(kv::KVFULL + i), 1); mbar_init(B_(kv::KVEMPTY + i), 1); }
     mbar_init(B_(kv::ACCFULL), 1); mbar_init(B_(kv::ACCEMPTY), 4);
     for (int i = 0; i < kv::NST; ++i) { mbar_init(B_(kv::STFULL + i), 1); mbar_init(B_(kv::STEMPTY + i), 1); }
     for (int i = 0; i < 2; ++i) {
@@ -476,12 +481,13 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
         int b, h, kb;
         item_of(it, b, h, kb);
         const int row0 = b * j.S;
-        wait(B_(kv::KVEMPTY), (ni & 1) ^ 1, SITE_TC_EMPTY);
-        mbar_expect_tx(B_(kv::KVFULL), 2 * TILE);
+        const uint32_t kbf = ni & 1, kva = sbase + kv::KV_OFF + kbf * 2 * TILE;
+        wait(B_(kv::KVEMPTY + kbf), ((ni >> 1) & 1) ^ 1, SITE_TC_EMPTY);
+        mbar_expect_tx(B_(kv::KVFULL + kbf), 2 * TILE);
         for (int half = 0; half < 2; ++half) {
-          tma_load_2d(sbase + kv::K_OFF + half * 8192, j.map_qkv, j.hq + h * HD, j.y0 + row0 + kb * 128 + half * 64, B_(kv::KVFULL));
-          tma_load_2d(sbase + kv::V_OFF + half * 8192, j.map_qkv, 2 * j.hq + h * HD, j.y0 + row0 + kb * 128 + half * 64,
-                      B_(kv::KVFULL));
+          tma_load_2d(kva + half * 8192, j.map_qkv, j.hq + h * HD, j.y0 + row0 + kb * 128 + half * 64, B_(kv::KVFULL + kbf));
+          tma_load_2d(kva + TILE + half * 8192, j.map_qkv, 2 * j.hq + h * HD, j.y0 + row0 + kb * 128 + half * 64,
+                      B_(kv::KVFULL + kbf));
         }
         const int nst = (j.S - kb * 128) / 64;
         const float* lrow = j.lse + ((long long)b * j.H + h) * j.S;
@@ -499,7 +505,7 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
       }
       if (!dead) {
         for (uint32_t x = c > kv::NST ? c - kv::NST : 0; x < c; ++x) wait(B_(kv::STFULL + x % kv::NST), (x / kv::NST) & 1, SITE_TC_DRAIN);
-        if (ni > 0) wait(B_(kv::KVFULL), (ni - 1) & 1, SITE_TC_DRAIN);
+        for (uint32_t n = ni > 2 ? ni - 2 : 0; n < ni; ++n) wait(B_(kv::KVFULL + (n & 1)), (n >> 1) & 1, SITE_TC_DRAIN);
       }
     }
     __syncwarp();
@@ -509,15 +515,16 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
       const uint32_t id_sd = idesc_bf16(128, 64, 0, 0);     // K (or V) x Q^T (or dO^T)
       const uint32_t id_acc = idesc_bf16(128, 64, 0, 1);    // P^T (or dS^T) x dO (or Q), MN-major B
       uint32_t c = 0, ni = 0, last_bar = 0, last_par = 0;
+      uint32_t kva = sbase + kv::KV_OFF;
       auto issue_sd = [&](uint32_t cc) {
         const uint32_t st = cc % kv::NST, sb = cc & 1, sa = sbase + kv::ST_OFF + st * kv::ST_BYTES;
         wait(B_(kv::STFULL + st), (cc / kv::NST) & 1, SITE_TC_FULL);
         wait(B_(kv::SDEMPTY + sb), ((cc >> 1) & 1) ^ 1, SITE_TC_ACC_EMPTY);
         tc_fence_after();
         for (int kk = 0; kk < HD / 16; ++kk) {
-          mma_bf16(tc.tmem_base + kv::TM_S + sb * 64, sdesc(sbase + kv::K_OFF + kk * 32, 16, 1024), sdesc(sa + kk * 32, 16, 1024),
+          mma_bf16(tc.tmem_base + kv::TM_S + sb * 64, sdesc(kva + kk * 32, 16, 1024), sdesc(sa + kk * 32, 16, 1024),
                    id_sd, kk > 0 ? 1u : 0u);
-          mma_bf16(tc.tmem_base + kv::TM_DP + sb * 64, sdesc(sbase + kv::V_OFF + kk * 32, 16, 1024),
+          mma_bf16(tc.tmem_base + kv::TM_DP + sb * 64, sdesc(kva + TILE + kk * 32, 16, 1024),
                    sdesc(sa + 8192 + kk * 32, 16, 1024), id_sd, kk > 0 ? 1u : 0u);
         }
         mma_commit(B_(kv::SDFULL + sb));
@@ -526,7 +533,9 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
         int b, h, kb;
         item_of(it, b, h, kb);
         const int nst = (j.S - kb * 128) / 64;
-        wait(B_(kv::KVFULL), ni & 1, SITE_TC_FULL);
+        const uint32_t kbf = ni & 1;
+        kva = sbase + kv::KV_OFF + kbf * 2 * TILE;
+        wait(B_(kv::KVFULL + kbf), (ni >> 1) & 1, SITE_TC_FULL);
         issue_sd(c);
         for (int i = 0; i < nst; ++i, ++c) {
           if (i + 1 < nst) issue_sd(c + 1);
@@ -547,10 +556,10 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
           last_par = (c / kv::NST) & 1;
         }
         mma_commit(B_(kv::ACCFULL));
-        mma_commit(B_(kv::KVEMPTY));
+        mma_commit(B_(kv::KVEMPTY + kbf));
       }
       if (last_bar && !dead && !mbar_wait(last_bar, last_par, tmo)) set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_DRAIN);
-      if (ni > 0) wait(B_(kv::KVEMPTY), (ni - 1) & 1, SITE_TC_DRAIN);
+      if (ni > 0) wait(B_(kv::KVEMPTY + ((ni - 1) & 1)), ((ni - 1) >> 1) & 1, SITE_TC_DRAIN);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -587,15 +596,19 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           uint32_t wp[4], wd[4];
+          const float4 la = reinterpret_cast<const float4*>(sl)[2 * g], lb = reinterpret_cast<const float4*>(sl)[2 * g + 1];
+          const float4 da = reinterpret_cast<const float4*>(sd)[2 * g], dbv = reinterpret_cast<const float4*>(sd)[2 * g + 1];
+          const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+          const float dv[8] = {da.x, da.y, da.z, da.w, dbv.x, dbv.y, dbv.z, dbv.w};
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
             const int x = g * 8 + e;
-            float p0 = ex2(fmaf(__uint_as_float(sv[x]), sc_l2, -sl[x] * LOG2E));
-            float p1 = ex2(fmaf(__uint_as_float(sv[x + 1]), sc_l2, -sl[x + 1] * LOG2E));
+            float p0 = ex2(fmaf(__uint_as_float(sv[x]), sc_l2, -lv[e] * LOG2E));
+            float p1 = ex2(fmaf(__uint_as_float(sv[x + 1]), sc_l2, -lv[e + 1] * LOG2E));
             if (x < lim) p0 = 0.f;
             if (x + 1 < lim) p1 = 0.f;
-            const float d0 = p0 * (__uint_as_float(dp[x]) - sd[x]);
-            const float d1 = p1 * (__uint_as_float(dp[x + 1]) - sd[x + 1]);
+            const float d0 = p0 * (__uint_as_float(dp[x]) - dv[e]);
+            const float d1 = p1 * (__uint_as_float(dp[x + 1]) - dv[e + 1]);
             wp[e >> 1] = pack2(p0, p1);
             wd[e >> 1] = pack2(d0, d1);
           }
@@ -636,13 +649,13 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
 
 namespace qd {   // dQ layout
 constexpr int NST = 4;                              // key-step ring stages: K 8 KB | V 8 KB
-constexpr uint32_t Q_OFF = 1024, DO_OFF = Q_OFF + TILE;
-constexpr uint32_t ST_OFF = DO_OFF + TILE;
+constexpr uint32_t QD_OFF = 1024;                    // 2 x (Q 16 KB | dO 16 KB): the next item's rows load early
+constexpr uint32_t ST_OFF = QD_OFF + 4 * TILE;
 constexpr uint32_t ST_BYTES = 16384;
 constexpr uint32_t DS_OFF = ST_OFF + NST * ST_BYTES;  // 2 x dS (128 queries x 64 keys)
 constexpr uint32_t END = DS_OFF + 2 * TILE;
 static_assert(END <= MT_TC_SMEM, "dQ tiles exceed the shared-memory window");
-enum { QFULL = 0, QEMPTY, ACCFULL, ACCEMPTY, STFULL = 4, STEMPTY = STFULL + NST, SDFULL = STEMPTY + NST,
+enum { QFULL = 0, QEMPTY = 2, ACCFULL = 4, ACCEMPTY = 5, STFULL = 6, STEMPTY = STFULL + NST, SDFULL = STEMPTY + NST,
        SDEMPTY = SDFULL + 2, DSFULL = SDEMPTY + 2, DSEMPTY = DSFULL + 2, COUNT = DSEMPTY + 2 };
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256;
 }
@@ -662,7 +675,7 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
     b = bh / j.H; h = bh % j.H;
   };
   if (threadIdx.x == 0) {
-    mbar_init(B_(qd::QFULL), 1); mbar_init(B_(qd::QEMPTY), 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(B_(qd::QFULL + i), 1); mbar_init(B_(qd::QEMPTY + i), 1); }
     mbar_init(B_(qd::ACCFULL), 1); mbar_init(B_(qd::ACCEMPTY), 4);
     for (int i = 0; i < qd::NST; ++i) { mbar_init(B_(qd::STFULL + i), 1); mbar_init(B_(qd::STEMPTY + i), 1); }
     for (int i = 0; i < 2; ++i) {
@@ -684,11 +697,12 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
         int b, h, qb;
         item_of(it, b, h, qb);
         const int row0 = b * j.S;
-        wait(B_(qd::QEMPTY), (ni & 1) ^ 1, SITE_TC_EMPTY);
-        mbar_expect_tx(B_(qd::QFULL), 2 * TILE);
+        const uint32_t qbf = ni & 1, qa = sbase + qd::QD_OFF + qbf * 2 * TILE;
+        wait(B_(qd::QEMPTY + qbf), ((ni >> 1) & 1) ^ 1, SITE_TC_EMPTY);
+        mbar_expect_tx(B_(qd::QFULL + qbf), 2 * TILE);
         for (int half = 0; half < 2; ++half) {
-          tma_load_2d(sbase + qd::Q_OFF + half * 8192, j.map_qkv, h * HD, j.y0 + row0 + qb * 128 + half * 64, B_(qd::QFULL));
-          tma_load_2d(sbase + qd::DO_OFF + half * 8192, j.map_do, h * HD, row0 + qb * 128 + half * 64, B_(qd::QFULL));
+          tma_load_2d(qa + half * 8192, j.map_qkv, h * HD, j.y0 + row0 + qb * 128 + half * 64, B_(qd::QFULL + qbf));
+          tma_load_2d(qa + TILE + half * 8192, j.map_do, h * HD, row0 + qb * 128 + half * 64, B_(qd::QFULL + qbf));
         }
         const int nst = 2 * (qb + 1);
         for (int i = 0; i < nst; ++i, ++c) {
@@ -701,7 +715,7 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
       }
       if (!dead) {
         for (uint32_t x = c > qd::NST ? c - qd::NST : 0; x < c; ++x) wait(B_(qd::STFULL + x % qd::NST), (x / qd::NST) & 1, SITE_TC_DRAIN);
-        if (ni > 0) wait(B_(qd::QFULL), (ni - 1) & 1, SITE_TC_DRAIN);
+        for (uint32_t n = ni > 2 ? ni - 2 : 0; n < ni; ++n) wait(B_(qd::QFULL + (n & 1)), (n >> 1) & 1, SITE_TC_DRAIN);
       }
     }
     __syncwarp();
@@ -710,15 +724,16 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
       const uint32_t id_sd = idesc_bf16(128, 64, 0, 0);     // Q (or dO) x K^T (or V^T)
       const uint32_t id_acc = idesc_bf16(128, 64, 0, 1);    // dS x K, MN-major B
       uint32_t c = 0, ni = 0, last_bar = 0, last_par = 0;
+      uint32_t qa = sbase + qd::QD_OFF;
       auto issue_sd = [&](uint32_t cc) {
         const uint32_t st = cc % qd::NST, sb = cc & 1, sa = sbase + qd::ST_OFF + st * qd::ST_BYTES;
         wait(B_(qd::STFULL + st), (cc / qd::NST) & 1, SITE_TC_FULL);
         wait(B_(qd::SDEMPTY + sb), ((cc >> 1) & 1) ^ 1, SITE_TC_ACC_EMPTY);
         tc_fence_after();
         for (int kk = 0; kk < HD / 16; ++kk) {
-          mma_bf16(tc.tmem_base + qd::TM_S + sb * 64, sdesc(sbase + qd::Q_OFF + kk * 32, 16, 1024), sdesc(sa + kk * 32, 16, 1024),
+          mma_bf16(tc.tmem_base + qd::TM_S + sb * 64, sdesc(qa + kk * 32, 16, 1024), sdesc(sa + kk * 32, 16, 1024),
                    id_sd, kk > 0 ? 1u : 0u);
-          mma_bf16(tc.tmem_base + qd::TM_DP + sb * 64, sdesc(sbase + qd::DO_OFF + kk * 32, 16, 1024),
+          mma_bf16(tc.tmem_base + qd::TM_DP + sb * 64, sdesc(qa + TILE + kk * 32, 16, 1024),
                    sdesc(sa + 8192 + kk * 32, 16, 1024), id_sd, kk > 0 ? 1u : 0u);
         }
         mma_commit(B_(qd::SDFULL + sb));
@@ -727,11 +742,13 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
         int b, h, qb;
         item_of(it, b, h, qb);
         const int nst = 2 * (qb + 1);
-        wait(B_(qd::QFULL), ni & 1, SITE_TC_FULL);
+        const uint32_t qbf = ni & 1;
+        qa = sbase + qd::QD_OFF + qbf * 2 * TILE;
+        wait(B_(qd::QFULL + qbf), (ni >> 1) & 1, SITE_TC_FULL);
         issue_sd(c);
         for (int i = 0; i < nst; ++i, ++c) {
           if (i + 1 < nst) issue_sd(c + 1);
-          else mma_commit(B_(qd::QEMPTY));                    // Q and dO are free after the last S, dP
+          else mma_commit(B_(qd::QEMPTY + qbf));              // Q and dO are free after the last S, dP
           const uint32_t st = c % qd::NST, sb = c & 1, sa = sbase + qd::ST_OFF + st * qd::ST_BYTES;
           wait(B_(qd::DSFULL + sb), (c >> 1) & 1, SITE_TC_FULL);
           if (i == 0) wait(B_(qd::ACCEMPTY), (ni & 1) ^ 1, SITE_TC_ACC_EMPTY);
@@ -747,7 +764,7 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
         mma_commit(B_(qd::ACCFULL));
       }
       if (last_bar && !dead && !mbar_wait(last_bar, last_par, tmo)) set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_DRAIN);
-      if (ni > 0) wait(B_(qd::QEMPTY), (ni - 1) & 1, SITE_TC_DRAIN);
+      if (ni > 0) wait(B_(qd::QEMPTY + ((ni - 1) & 1)), ((ni - 1) >> 1) & 1, SITE_TC_DRAIN);
     }
     __syncwarp();
   } else if (warp >= 4) {
