@@ -204,9 +204,11 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
         wait(B_(B_SEMPTY + sb), ((c >> 1) & 1) ^ 1, SITE_TC_ACC_EMPTY);
         tc_fence_after();
         const uint32_t sq = sbase + Q_OFF + qs * TILE, sk = sbase + K_OFF + ks * TILE;
+        const uint64_t dq = sdesc(sq, 16, 1024), dk = sdesc(sk, 16, 1024);
+#pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          mma_bf16(tc.tmem_base + TM_S + sb * BKEY, sdesc(sq + kk * 32, 16, 1024), sdesc(sk + kk * 32, 16, 1024),
-                   id_s, kk > 0 ? 1u : 0u);
+          mma_bf16(tc.tmem_base + TM_S + sb * BKEY, sdesc_add(dq, kk * 32), sdesc_add(dk, kk * 32), id_s,
+                   kk > 0 ? 1u : 0u);
         mma_commit(B_(B_SFULL + sb));
         mma_commit(B_(B_KEMPTY + ks));                    // K_c is read
       };
@@ -225,9 +227,11 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
           wait(B_(B_OEMPTY + pb), ((sc >> 1) & 1) ^ 1, SITE_TC_ACC_EMPTY);
           tc_fence_after();
           const uint32_t sp = sbase + P_OFF + pb * P_BUF, sv = sbase + V_OFF + vs * TILE;
+          const uint64_t dp0 = sdesc(sp, 16, 1024), dv0 = sdesc(sv, 8192, 1024);
+#pragma unroll
           for (int kk = 0; kk < BKEY / 16; ++kk)
-            mma_bf16(tc.tmem_base + TM_PV + pb * HD, sdesc(sp + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                     sdesc(sv + kk * 2048, 8192, 1024), id_pv, kk > 0 ? 1u : 0u);
+            mma_bf16(tc.tmem_base + TM_PV + pb * HD, sdesc_add(dp0, (kk >> 2) * 16384 + (kk & 3) * 32),
+                     sdesc_add(dv0, kk * 2048), id_pv, kk > 0 ? 1u : 0u);
           mma_commit(B_(B_OFULL + pb));
           mma_commit(B_(B_VEMPTY + vs));
           last_bar = B_(B_VEMPTY + vs);
@@ -521,11 +525,13 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
         wait(B_(kv::STFULL + st), (cc / kv::NST) & 1, SITE_TC_FULL);
         wait(B_(kv::SDEMPTY + sb), ((cc >> 1) & 1) ^ 1, SITE_TC_ACC_EMPTY);
         tc_fence_after();
+        const uint64_t dk = sdesc(kva, 16, 1024), dq = sdesc(sa, 16, 1024);
+#pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          mma_bf16(tc.tmem_base + kv::TM_S + sb * 64, sdesc(kva + kk * 32, 16, 1024), sdesc(sa + kk * 32, 16, 1024),
+          mma_bf16(tc.tmem_base + kv::TM_S + sb * 64, sdesc_add(dk, kk * 32), sdesc_add(dq, kk * 32), id_sd,
+                   kk > 0 ? 1u : 0u);
+          mma_bf16(tc.tmem_base + kv::TM_DP + sb * 64, sdesc_add(dk, TILE + kk * 32), sdesc_add(dq, 8192 + kk * 32),
                    id_sd, kk > 0 ? 1u : 0u);
-          mma_bf16(tc.tmem_base + kv::TM_DP + sb * 64, sdesc(kva + TILE + kk * 32, 16, 1024),
-                   sdesc(sa + 8192 + kk * 32, 16, 1024), id_sd, kk > 0 ? 1u : 0u);
         }
         mma_commit(B_(kv::SDFULL + sb));
       };
@@ -543,12 +549,14 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
           wait(B_(kv::PDFULL + sb), (c >> 1) & 1, SITE_TC_FULL);
           if (i == 0) wait(B_(kv::ACCEMPTY), (ni & 1) ^ 1, SITE_TC_ACC_EMPTY);   // dK, dV of the last item are read
           tc_fence_after();
+          const uint64_t dpt = sdesc(sbase + kv::P_OFF + sb * TILE, 16, 1024);
+          const uint64_t dst = sdesc(sbase + kv::DS_OFF + sb * TILE, 16, 1024);
+          const uint64_t dqm = sdesc(sa, 8192, 1024);
+#pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-            mma_bf16(tc.tmem_base + kv::TM_DV, sdesc(sbase + kv::P_OFF + sb * TILE + kk * 32, 16, 1024),
-                     sdesc(sa + 8192 + kk * 2048, 8192, 1024), id_acc, acc);
-            mma_bf16(tc.tmem_base + kv::TM_DK, sdesc(sbase + kv::DS_OFF + sb * TILE + kk * 32, 16, 1024),
-                     sdesc(sa + kk * 2048, 8192, 1024), id_acc, acc);
+            mma_bf16(tc.tmem_base + kv::TM_DV, sdesc_add(dpt, kk * 32), sdesc_add(dqm, 8192 + kk * 2048), id_acc, acc);
+            mma_bf16(tc.tmem_base + kv::TM_DK, sdesc_add(dst, kk * 32), sdesc_add(dqm, kk * 2048), id_acc, acc);
           }
           mma_commit(B_(kv::PDEMPTY + sb));
           mma_commit(B_(kv::STEMPTY + st));
@@ -730,11 +738,13 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
         wait(B_(qd::STFULL + st), (cc / qd::NST) & 1, SITE_TC_FULL);
         wait(B_(qd::SDEMPTY + sb), ((cc >> 1) & 1) ^ 1, SITE_TC_ACC_EMPTY);
         tc_fence_after();
+        const uint64_t dq = sdesc(qa, 16, 1024), dk = sdesc(sa, 16, 1024);
+#pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          mma_bf16(tc.tmem_base + qd::TM_S + sb * 64, sdesc(qa + kk * 32, 16, 1024), sdesc(sa + kk * 32, 16, 1024),
+          mma_bf16(tc.tmem_base + qd::TM_S + sb * 64, sdesc_add(dq, kk * 32), sdesc_add(dk, kk * 32), id_sd,
+                   kk > 0 ? 1u : 0u);
+          mma_bf16(tc.tmem_base + qd::TM_DP + sb * 64, sdesc_add(dq, TILE + kk * 32), sdesc_add(dk, 8192 + kk * 32),
                    id_sd, kk > 0 ? 1u : 0u);
-          mma_bf16(tc.tmem_base + qd::TM_DP + sb * 64, sdesc(qa + TILE + kk * 32, 16, 1024),
-                   sdesc(sa + 8192 + kk * 32, 16, 1024), id_sd, kk > 0 ? 1u : 0u);
         }
         mma_commit(B_(qd::SDFULL + sb));
       };
@@ -753,9 +763,11 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
           wait(B_(qd::DSFULL + sb), (c >> 1) & 1, SITE_TC_FULL);
           if (i == 0) wait(B_(qd::ACCEMPTY), (ni & 1) ^ 1, SITE_TC_ACC_EMPTY);
           tc_fence_after();
+          const uint64_t dds = sdesc(sbase + qd::DS_OFF + sb * TILE, 16, 1024), dkm = sdesc(sa, 8192, 1024);
+#pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tc.tmem_base + qd::TM_DQ, sdesc(sbase + qd::DS_OFF + sb * TILE + kk * 32, 16, 1024),
-                     sdesc(sa + kk * 2048, 8192, 1024), id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16(tc.tmem_base + qd::TM_DQ, sdesc_add(dds, kk * 32), sdesc_add(dkm, kk * 2048), id_acc,
+                     (i > 0 || kk > 0) ? 1u : 0u);
           mma_commit(B_(qd::DSEMPTY + sb));
           mma_commit(B_(qd::STEMPTY + st));
           last_bar = B_(qd::STEMPTY + st);

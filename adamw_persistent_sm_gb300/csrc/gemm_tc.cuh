@@ -116,6 +116,10 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo & 0x3FFFFu) >> 4) << 16) |
          ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
+// A descriptor advanced by `bytes` (a multiple of 16): the start-address
+// field holds addr >> 4 in its low bits and shared addresses stay below
+// 256 KB, so the advance is a plain add (no per-step rebuild).
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator.
 __device__ __forceinline__ uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
@@ -624,6 +628,8 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
       const uint32_t idesc = idesc_bf16(TC_BM, TC_BN, g.A.mn, g.B.mn);
       const uint32_t a_lbo = g.A.mn ? TC_BOX_BYTES : 16, b_lbo = g.B.mn ? TC_BOX_BYTES : 16;
       const uint32_t a_kstep = g.A.mn ? 16 * 128 : 32, b_kstep = g.B.mn ? 16 * 128 : 32;
+      // descriptors of stage 0; a stage and a K step are plain address advances
+      const uint64_t ad0 = sdesc(ring, a_lbo, 1024), bd0 = sdesc(ring + 2 * TC_BOX_BYTES, b_lbo, 1024);
       uint32_t it = 0, tcount = 0;
       bool ok = true;
       uint32_t last_bar = 0, last_par = 0;
@@ -647,13 +653,11 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
             break;
           }
           tc_fence_after();
-          const uint32_t sa = ring + st * TC_STAGE_BYTES, sb = sa + 2 * TC_BOX_BYTES;
+          const uint32_t soff = st * TC_STAGE_BYTES;
 #pragma unroll
-          for (int j = 0; j < TC_BK / 16; ++j) {
-            const uint64_t ad = sdesc(sa + j * a_kstep, a_lbo, 1024);
-            const uint64_t bd = sdesc(sb + j * b_kstep, b_lbo, 1024);
-            mma_bf16(dt, ad, bd, idesc, (kb > 0 || j > 0) ? 1u : 0u);
-          }
+          for (int j = 0; j < TC_BK / 16; ++j)
+            mma_bf16(dt, sdesc_add(ad0, soff + j * a_kstep), sdesc_add(bd0, soff + j * b_kstep), idesc,
+                     (kb > 0 || j > 0) ? 1u : 0u);
           mma_commit(empty + 8 * st);
           last_bar = empty + 8 * st;
           last_par = ph;
