@@ -163,7 +163,7 @@ DevState g_dev[64];
 size_t smem_bytes(const MtDims& D, bool tc) {
   size_t attn = (size_t)(4 * 64 * 65 + 2 * 64 * 65 + 128) * 4;
   size_t simt = (size_t)SG_BM * SG_CPAD * 4;
-  size_t router = (size_t)D.E * D.d * 4 + 64 * 4;
+  size_t router = 1024 + (size_t)D.E * D.d * 4 + 64 * 4;   // ring barriers, router weights, counts
   // column reductions: staged 1/rms and router gradients, token-lane partials
   const int er = D.E <= 4 ? 4 : D.E <= 16 ? 16 : D.E <= 32 ? 32 : 64;
   const int cw = D.E <= 16 ? 4 : D.E <= 32 ? 2 : 1;
@@ -299,6 +299,7 @@ int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m
   a->use_tm_attn = a->use_tc && a->use_tc_attn && !(hp->flags & MT_FLAG_MMA_SYNC_ATTN);
   // counters need whole 128-row blocks on both sides of every hand-off
   a->deps = a->use_tc && a->use_tc_attn && !(hp->flags & MT_FLAG_BARRIERS_ONLY);
+  a->smem_bytes = (int)smem;
   if (want_tc) {
     int ms = mt_build_tensor_maps(a, shadow);
     if (ms != MT_OK) { delete a; return ms; }

@@ -19,6 +19,7 @@
 #include "attn_tc.cuh"
 #include "attn_tm.cuh"
 #include "rows.cuh"
+#include "rowpipe.cuh"
 #include <type_traits>
 
 template <class T>
@@ -132,7 +133,7 @@ __device__ __forceinline__ void warp_argmax(float& v, int& idx) {
 // top-k compares these fp32 logits (softmax is monotone), ties going to the
 // lower expert index.
 template <class OP>
-__device__ __noinline__ void job_router(const KArgs& a, int l, float* sm, const unsigned* dw, unsigned dtarget) {
+__device__ __noinline__ void job_router(const KArgs& a, int l, char* smem, const unsigned* dw, unsigned dtarget) {
   const MtDims& D = a.D;
   const int c = blockIdx.x, G = gridDim.x;
   const int ch = chunk_len(D, G);
@@ -146,10 +147,17 @@ __device__ __noinline__ void job_router(const KArgs& a, int l, float* sm, const 
   float* WGT = abuf<float>(a, A_WGT) + (long long)l * D.T * D.K;
   const float* g = pmaster(a, P_MOE_NORM) + (long long)l * D.d;
   const float* Wr = pmaster(a, P_ROUTER) + (long long)l * D.E * D.d;
-  // router weights (fp32, E x d) staged once per CTA; per-expert counts after them
+  const uint32_t rowb = (uint32_t)D.d * 4u;
+  // shared memory: [mbarriers of the row rings | router weights (fp32, E x d)
+  // | per-expert counts | row rings]
+  float* sm = reinterpret_cast<float*>(smem + RP_WIN_OFF);
+  int* s_cnt = reinterpret_cast<int*>(sm + (long long)D.E * D.d);
+  const uint32_t win = (RP_WIN_OFF + (uint32_t)D.E * rowb + 4u * 64u + 127u) & ~127u;
+  const RowPipe p = rp_make(smem, win, (uint32_t)a.smem_bytes, rowb);
+  if (p.ns > 0) rp_begin(p);
+  else __syncthreads();
   for (int i = threadIdx.x; i < D.E * D.d / 4; i += MT_THREADS)
     reinterpret_cast<float4*>(sm)[i] = reinterpret_cast<const float4*>(Wr)[i];
-  int* s_cnt = reinterpret_cast<int*>(sm + (long long)D.E * D.d);
   for (int e = threadIdx.x; e < D.E; e += MT_THREADS) s_cnt[e] = 0;
   if (dw && t0 < t1) {
     // the chunk's x_mid rows are stored by out-projection tiles of other CTAs
@@ -157,13 +165,14 @@ __device__ __noinline__ void job_router(const KArgs& a, int l, float* sm, const 
     if (threadIdx.x < nb) dep_wait(abuf<ArenaHdr>(a, A_HDR), dw + b0 + threadIdx.x, dtarget, a.timeout_ns);
   }
   __syncthreads();
+  if (p.ns > 0 && lane == 0) asm volatile("fence.proxy.async;" ::: "memory");   // after the acquire
   const int n4 = D.d / 4;
+  bool ok = true;
   with_nc(D.d, [&](auto NCc) {
   constexpr int NC = decltype(NCc)::value;
   Row<NC> gr, x, r, w;
   row_ld(gr, g, n4);
-  for (int t = t0 + warp; t < t1; t += MT_WARPS) {
-    row_ld(x, XM + (long long)t * D.d, n4);
+  auto token = [&](int t) {
     const float inv = row_rms_inv(x, D.d, a.norm_eps);
     row_norm_apply(r, x, inv, gr);
     row_st_op(R2 + (long long)t * D.d, r, n4);
@@ -236,9 +245,32 @@ __device__ __noinline__ void job_router(const KArgs& a, int l, float* sm, const 
         atomicAdd(&s_cnt[chosen_i[k]], 1);
       }
     }
+  };
+  if (p.ns > 0) {
+    // staged: the x_mid row of each token; header: t
+    const int n = t0 + warp < t1 ? (t1 - 1 - t0 - warp) / MT_WARPS + 1 : 0;
+    ok = rp_run(
+        p, n, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 0,
+        [&](int j, uint32_t st, uint32_t bar) {
+          const int t = t0 + warp + j * MT_WARPS;
+          sts_i32(st, t);
+          mbar_expect_tx(bar, rowb);
+          bulk_g2s(st + RP_HDR, XM + (long long)t * D.d, rowb, bar);
+        },
+        [&](int j, uint32_t st) {
+          row_lds(x, st + RP_HDR, n4);
+          token(lds_i32(st));
+        },
+        [&](int) {});
+  } else {
+    for (int t = t0 + warp; t < t1; t += MT_WARPS) {
+      row_ld(x, XM + (long long)t * D.d, n4);
+      token(t);
+    }
   }
   });
-  __syncthreads();
+  if (p.ns > 0) rp_end(p, ok);
+  else __syncthreads();
   if (t0 < D.T) {
     int* CNT = abuf<int>(a, A_CNT) + ((long long)l * D.nch + c) * D.E;
     for (int e = threadIdx.x; e < D.E; e += MT_THREADS) CNT[e] = s_cnt[e];
@@ -251,7 +283,7 @@ __device__ __noinline__ void job_router(const KArgs& a, int l, float* sm, const 
 // fused with the dispatch gather of the expert inputs.  Within an expert,
 // assignments keep ascending a = t*K + k.
 template <class OP>
-__device__ __noinline__ void job_route(const KArgs& a, int l, int* ism) {
+__device__ __noinline__ void job_route(const KArgs& a, int l, char* smem) {
   const MtDims& D = a.D;
   const int c = blockIdx.x, G = gridDim.x;
   const int ch = chunk_len(D, G);
@@ -265,10 +297,16 @@ __device__ __noinline__ void job_route(const KArgs& a, int l, int* ism) {
   const int* IDX = abuf<int>(a, A_IDX) + (long long)l * D.T * D.K;
   const OP* R2 = abuf<OP>(a, A_R2) + (long long)l * D.T * D.d;
   OP* XS = abuf<OP>(a, A_XS) + (long long)l * D.Pmax * D.d;
+  // shared memory: [mbarriers of the row rings | counting-sort scratch | rings]
+  int* ism = reinterpret_cast<int*>(smem + RP_WIN_OFF);
   int* s_tot = ism;                 // [E]
   int* s_base = ism + 64;           // [E]
   int* s_offs = ism + 128;          // [E+1]
   int* s_cnt = ism + 256;           // [nused][E] chunk counts
+  const uint32_t rowb = (uint32_t)D.d * (uint32_t)sizeof(OP);
+  const uint32_t win = (RP_WIN_OFF + 4u * (256u + (uint32_t)(nused * D.E)) + 127u) & ~127u;
+  const RowPipe rp = rp_make(smem, win, (uint32_t)a.smem_bytes, rowb);
+  if (rp.ns > 0) rp_begin(rp);
   for (int i = threadIdx.x; i < nused * D.E; i += MT_THREADS) s_cnt[i] = CNT[i];
   __syncthreads();
   for (int e = threadIdx.x; e < D.E; e += MT_THREADS) {
@@ -318,13 +356,47 @@ __device__ __noinline__ void job_route(const KArgs& a, int l, int* ism) {
     }
   }
   __syncthreads();
-  // dispatch gather: XS[row] = R2[token], 16-byte chunks
   const int n16 = D.d * (int)sizeof(OP) / 16;
-  for (int j = a0 + warp; j < a1; j += MT_WARPS) {
-    const int pos = INVM[j];
-    const uint4* src = reinterpret_cast<const uint4*>(R2 + (long long)(j / D.K) * D.d);
-    uint4* dst = reinterpret_cast<uint4*>(XS + (long long)pos * D.d);
-    for (int i = lane; i < n16; i += 32) dst[i] = src[i];
+  // dispatch gather: XS[row] = R2[token].  With a ring, lane 0 of each warp
+  // copies the warp's token rows into shared memory (cp.async.bulk) and
+  // stores each to its K sorted rows with bulk stores; the stage of token j
+  // is refilled once the stores of token j have been read out.
+  if (rp.ns > 0) {
+    if (lane == 0) {
+      const int n = t0 + warp < t1 ? (t1 - 1 - t0 - warp) / MT_WARPS + 1 : 0;
+      auto load = [&](int j) {
+        mbar_expect_tx(rp.sbar(j), rowb);
+        bulk_g2s(rp.stage(j) + RP_HDR, R2 + (long long)(t0 + warp + j * MT_WARPS) * D.d, rowb, rp.sbar(j));
+      };
+      for (int j = 0; j < n && j < rp.ns; ++j) load(j);
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        if (!mbar_wait(rp.sbar(j), rp.parity(j), a.timeout_ns / 2)) {
+          set_error(abuf<ArenaHdr>(a, A_HDR), MT_ERR_DEVICE_TIMEOUT, SITE_ROWPIPE + 1);
+          ok = false;
+          break;
+        }
+        const int t = t0 + warp + j * MT_WARPS;
+        for (int k = 0; k < D.K; ++k)
+          bulk_s2g(XS + (long long)INVM[(long long)t * D.K + k] * D.d, rp.stage(j) + RP_HDR, rowb);
+        bulk_commit();
+        if (j + rp.ns < n) {
+          bulk_wait_read0();
+          load(j + rp.ns);
+        }
+      }
+      bulk_wait_all0();
+      // the bulk stores (async proxy) come before the release at the next barrier
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    __syncwarp();
+  } else {
+    for (int j = a0 + warp; j < a1; j += MT_WARPS) {
+      const int pos = INVM[j];
+      const uint4* src = reinterpret_cast<const uint4*>(R2 + (long long)(j / D.K) * D.d);
+      uint4* dst = reinterpret_cast<uint4*>(XS + (long long)pos * D.d);
+      for (int i = lane; i < n16; i += 32) dst[i] = src[i];
+    }
   }
   // zero the pad rows of every segment (spread over all CTAs)
   const int gw = c * MT_WARPS + warp, nw = G * MT_WARPS;
@@ -336,14 +408,15 @@ __device__ __noinline__ void job_route(const KArgs& a, int l, int* ism) {
       if (lane == 0) PERM[p] = -1;
     }
   }
+  if (rp.ns > 0) rp_end(rp, true);
 }
 
 // x_{l+1} = x_mid + sum_k w_k y_k (fixed slot order), then the next
 // RMSNorm (attention norm of layer l+1, or the final norm).
 template <class OP>
-__device__ __noinline__ void job_combine(const KArgs& a, int l, Sched& s, unsigned* dsig) {
+__device__ __noinline__ void job_combine(const KArgs& a, int l, Sched& s, unsigned* dsig, char* smem) {
   const MtDims& D = a.D;
-  const int lane = threadIdx.x & 31, n4 = D.d / 4;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n4 = D.d / 4;
   const float* XM = abuf<float>(a, A_XM) + (long long)l * D.T * D.d;
   const float* Y = abuf<float>(a, A_Y) + (long long)l * D.Pmax * D.d;
   const float* WGT = abuf<float>(a, A_WGT) + (long long)l * D.T * D.K;
@@ -356,6 +429,65 @@ __device__ __noinline__ void job_combine(const KArgs& a, int l, Sched& s, unsign
   // items: groups of MT_DEP_GROUP tokens (each warp takes every 8th token of
   // its CTA's group); with counters on, each finished group is published
   const int ng = (D.T + MT_DEP_GROUP - 1) / MT_DEP_GROUP;
+  const uint32_t rowb = (uint32_t)D.d * 4u;
+  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, (uint32_t)(1 + D.K) * rowb);
+  if (p.ns > 0 && D.K <= 8) {
+    // staged: x_mid row and the K expert-output rows of each token
+    constexpr int PER = MT_DEP_GROUP / MT_WARPS;
+    const int first = s.first();
+    const int mine = first < ng ? (ng - 1 - first) / s.G + 1 : 0;
+    auto tok = [&](int j) {
+      const int t = (first + (j / PER) * s.G) * MT_DEP_GROUP + warp + MT_WARPS * (j % PER);
+      return t < D.T ? t : -1;
+    };
+    rp_begin(p);
+    bool ok = true;
+    with_nc(D.d, [&](auto NCc) {
+      constexpr int NC = decltype(NCc)::value;
+      Row<NC> g, x, acc, y, r;
+      row_ld(g, gp, n4);
+      ok = rp_run(
+          p, mine * PER, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 2,
+          [&](int j, uint32_t st, uint32_t bar) {
+            // header: t, then K weights
+            const int t = tok(j);
+            sts_i32(st, t);
+            if (t < 0) { mbar_arrive(bar); return; }
+            mbar_expect_tx(bar, (uint32_t)(1 + D.K) * rowb);
+            bulk_g2s(st + RP_HDR, XM + (long long)t * D.d, rowb, bar);
+            for (int k = 0; k < D.K; ++k) {
+              const int pr = INVM[(long long)t * D.K + k];
+              sts_f32(st + 4u * (1 + k), WGT[(long long)t * D.K + k]);
+              bulk_g2s(st + RP_HDR + (1 + k) * rowb, Y + (long long)pr * D.d, rowb, bar);
+            }
+          },
+          [&](int j, uint32_t st) {
+            const int t = lds_i32(st);
+            if (t < 0) return;
+            row_lds(x, st + RP_HDR, n4);
+            row_scale(acc, x, 0.f);
+            for (int k = 0; k < D.K; ++k) {
+              row_lds(y, st + RP_HDR + (1 + k) * rowb, n4);
+              row_axpy(acc, y, lds_f32(st + 4u * (1 + k)));
+            }
+            row_add(x, acc);
+            row_st(Xn + (long long)t * D.d, x, n4);
+            const float inv = row_rms_inv(x, D.d, a.norm_eps);
+            row_norm_apply(r, x, inv, g);
+            row_st_op(Rn + (long long)t * D.d, r, n4);
+            if (lane == 0) invn[t] = inv;
+          },
+          [&](int j) {
+            if (dsig && j % PER == PER - 1) {
+              __syncthreads();
+              if (threadIdx.x == 0) dep_signal(dsig + (first + (j / PER) * s.G) * MT_DEP_GROUP / MT_TILE_M);
+            }
+          });
+    });
+    rp_end(p, ok);
+    s.next(ng);
+    return;
+  }
   with_nc(D.d, [&](auto NCc) {
     constexpr int NC = decltype(NCc)::value;
     Row<NC> g, x, acc, y, r;
@@ -419,7 +551,7 @@ __device__ __noinline__ void job_ce(const KArgs& a, Sched& s) {
   const int np = ce_parts<OP>(a);
   const int nw = s.G * MT_WARPS;
   const int v4 = D.V / 4;                 // V % 8 == 0 (checked on the host)
-  constexpr int U = 8;
+  constexpr int U = sizeof(OP) == 2 ? 16 : 8;   // 16-byte loads in flight per lane
   for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
     OP* row = DL + (long long)t * D.V;
     const bool has = (t % D.S) != D.S - 1;
@@ -532,7 +664,7 @@ __device__ __noinline__ void job_final_norm_bwd(const KArgs& a, Sched& s) {
 // experts (the renormalised weights are the softmax of the chosen logits),
 // and zero pad rows of dY.
 template <class OP>
-__device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s) {
+__device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char* smem) {
   const MtDims& D = a.D;
   const int lane = threadIdx.x & 31, n4 = D.d / 4;
   const float* DX = abuf<float>(a, A_DX);
@@ -546,27 +678,84 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s) {
   float* DZ = abuf<float>(a, A_DZ);
   const int nw = s.G * MT_WARPS;
   const int me = s.first() * MT_WARPS + (threadIdx.x >> 5);
+  const uint32_t rowb = (uint32_t)D.d * 4u;
+  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, (uint32_t)(1 + D.K) * rowb);
+  const bool piped = p.ns > 0 && D.K <= 8;
+  if (piped) rp_begin(p);
+  bool ok = true;
   with_nc(D.d, [&](auto NCc) {
     constexpr int NC = decltype(NCc)::value;
     Row<NC> dx, y, dy;
-    for (int t = me; t < D.T; t += nw) {
-      row_ld(dx, DX + (long long)t * D.d, n4);
-      float dw[8], w[8];
-      for (int k = 0; k < D.K; ++k) {
-        const int p = INVM[(long long)t * D.K + k];
-        w[k] = WGT[(long long)t * D.K + k];
-        row_ld(y, Y + (long long)p * D.d, n4);
-        dw[k] = row_dot(dx, y);
-        row_scale(dy, dx, w[k]);
-        row_st_op(DY + (long long)p * D.d, dy, n4);
-      }
-      float mean = 0.f;
-      for (int k = 0; k < D.K; ++k) mean = fmaf(w[k], dw[k], mean);
-      for (int e = lane; e < D.E; e += 32) {
-        float v = 0.f;
-        for (int k = 0; k < D.K; ++k)
-          if (IDX[(long long)t * D.K + k] == e) v = w[k] * (dw[k] - mean);
-        DZ[(long long)t * D.E + e] = v;
+    if (piped) {
+      // staged: the dx row and the K expert-output rows of each token;
+      // header: t, then K sorted rows, K weights, K experts
+      const int n = me < D.T ? (D.T - 1 - me) / nw + 1 : 0;
+      ok = rp_run(
+          p, n, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 3,
+          [&](int j, uint32_t st, uint32_t bar) {
+            const int t = me + j * nw;
+            sts_i32(st, t);
+            mbar_expect_tx(bar, (uint32_t)(1 + D.K) * rowb);
+            bulk_g2s(st + RP_HDR, DX + (long long)t * D.d, rowb, bar);
+            for (int k = 0; k < D.K; ++k) {
+              const int pr = INVM[(long long)t * D.K + k];
+              sts_i32(st + 4u * (1 + k), pr);
+              sts_f32(st + 4u * (1 + D.K + k), WGT[(long long)t * D.K + k]);
+              sts_i32(st + 4u * (1 + 2 * D.K + k), IDX[(long long)t * D.K + k]);
+              bulk_g2s(st + RP_HDR + (1 + k) * rowb, Y + (long long)pr * D.d, rowb, bar);
+            }
+          },
+          [&](int j, uint32_t st) {
+            const int t = lds_i32(st);
+            row_lds(dx, st + RP_HDR, n4);
+            // sum_k w_k dw_k, then dz_e = w_k (dw_k - mean) for the chosen e
+            float mean = 0.f;
+            float dzl = 0.f, dzh = 0.f;   // experts lane and lane + 32
+            float dwk[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (k < D.K) {
+                row_lds(y, st + RP_HDR + (1 + k) * rowb, n4);
+                const float w = lds_f32(st + 4u * (1 + D.K + k));
+                dwk[k] = row_dot(dx, y);
+                mean = fmaf(w, dwk[k], mean);
+                row_scale(dy, dx, w);
+                row_st_op(DY + (long long)lds_i32(st + 4u * (1 + k)) * D.d, dy, n4);
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (k < D.K) {
+                const int e = lds_i32(st + 4u * (1 + 2 * D.K + k));
+                const float v = lds_f32(st + 4u * (1 + D.K + k)) * (dwk[k] - mean);
+                if (e == lane) dzl = v;
+                if (e == lane + 32) dzh = v;
+              }
+            }
+            if (lane < D.E) DZ[(long long)t * D.E + lane] = dzl;
+            if (lane + 32 < D.E) DZ[(long long)t * D.E + lane + 32] = dzh;
+          },
+          [&](int) {});
+    } else {
+      for (int t = me; t < D.T; t += nw) {
+        row_ld(dx, DX + (long long)t * D.d, n4);
+        float dw[8], w[8];
+        for (int k = 0; k < D.K; ++k) {
+          const int p = INVM[(long long)t * D.K + k];
+          w[k] = WGT[(long long)t * D.K + k];
+          row_ld(y, Y + (long long)p * D.d, n4);
+          dw[k] = row_dot(dx, y);
+          row_scale(dy, dx, w[k]);
+          row_st_op(DY + (long long)p * D.d, dy, n4);
+        }
+        float mean = 0.f;
+        for (int k = 0; k < D.K; ++k) mean = fmaf(w[k], dw[k], mean);
+        for (int e = lane; e < D.E; e += 32) {
+          float v = 0.f;
+          for (int k = 0; k < D.K; ++k)
+            if (IDX[(long long)t * D.K + k] == e) v = w[k] * (dw[k] - mean);
+          DZ[(long long)t * D.E + e] = v;
+        }
       }
     }
     // pad rows of dY: PERM == -1 inside [0, OFFS[E])
@@ -576,6 +765,7 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s) {
     for (int p = me; p < nrows; p += nw)
       if (PERM[p] < 0) row_st_op(DY + (long long)p * D.d, dy, n4);
   });
+  if (piped) rp_end(p, ok);
   s.next(s.G);
 }
 
@@ -584,12 +774,13 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s) {
 // atomics - "Open problems", Performance item 5), plus the router term
 // dz Wr, then the expert RMSNorm backward into dx, and the operand copy of dx.
 template <class OP>
-__device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s) {
+__device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char* smem) {
   const MtDims& D = a.D;
   const int n4 = D.d / 4;
   const float* DXS = abuf<float>(a, A_DXS);
   const float* DZ = abuf<float>(a, A_DZ);
   const int* INVM = abuf<int>(a, A_INVM) + (long long)l * D.T * D.K;
+  const int* IDX = abuf<int>(a, A_IDX) + (long long)l * D.T * D.K;
   const float* Wr = pmaster(a, P_ROUTER) + (long long)l * D.E * D.d;
   const float* XM = abuf<float>(a, A_XM) + (long long)l * D.T * D.d;
   const float* inv2 = abuf<float>(a, A_INV2) + (long long)l * D.T;
@@ -597,58 +788,150 @@ __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s) {
   float* DX = abuf<float>(a, A_DX);
   OP* DXO = abuf<OP>(a, A_DXO);
   const int nw = s.G * MT_WARPS;
+  const int me = s.first() * MT_WARPS + (threadIdx.x >> 5);
+  const uint32_t rowb = (uint32_t)D.d * 4u;
+  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, (uint32_t)(D.K + 2) * rowb);
+  const bool piped = p.ns > 0 && D.K <= 8;
+  if (piped) rp_begin(p);
+  bool ok = true;
   with_nc(D.d, [&](auto NCc) {
     constexpr int NC = decltype(NCc)::value;
     Row<NC> g, dr2, tmp, x, dx, dxm;
     row_ld(g, pmaster(a, P_MOE_NORM) + (long long)l * D.d, n4);
-    for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
-      row_scale(dr2, g, 0.f);
-      for (int k = 0; k < D.K; ++k) {
-        row_ld(tmp, DXS + (long long)INVM[(long long)t * D.K + k] * D.d, n4);
-        row_add(dr2, tmp);
-      }
-      const float* dz = DZ + (long long)t * D.E;
-      for (int e = 0; e < D.E; ++e) {
-        const float ze = dz[e];
-        if (ze != 0.f) {
-          row_ld(tmp, Wr + (long long)e * D.d, n4);
-          row_axpy(dr2, tmp, ze);
+    if (piped) {
+      // staged: the K expert-input gradient rows, x_mid and dx of each token;
+      // header: t, 1/rms, then the chosen experts in ascending order with
+      // their router-logit gradients
+      const int n = me < D.T ? (D.T - 1 - me) / nw + 1 : 0;
+      ok = rp_run(
+          p, n, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 4,
+          [&](int j, uint32_t st, uint32_t bar) {
+            const int t = me + j * nw;
+            sts_i32(st, t);
+            sts_f32(st + 4u, inv2[t]);
+            mbar_expect_tx(bar, (uint32_t)(D.K + 2) * rowb);
+            for (int k = 0; k < D.K; ++k)
+              bulk_g2s(st + RP_HDR + k * rowb, DXS + (long long)INVM[(long long)t * D.K + k] * D.d, rowb, bar);
+            bulk_g2s(st + RP_HDR + D.K * rowb, XM + (long long)t * D.d, rowb, bar);
+            bulk_g2s(st + RP_HDR + (D.K + 1) * rowb, DX + (long long)t * D.d, rowb, bar);
+            // experts sorted ascending (insertion sort of K <= 8 values)
+            int ex[8];
+            for (int k = 0; k < D.K; ++k) {
+              int e = IDX[(long long)t * D.K + k], q = k;
+              while (q > 0 && ex[q - 1] > e) { ex[q] = ex[q - 1]; --q; }
+              ex[q] = e;
+            }
+            for (int k = 0; k < D.K; ++k) {
+              sts_i32(st + 4u * (2 + k), ex[k]);
+              sts_f32(st + 4u * (2 + D.K + k), DZ[(long long)t * D.E + ex[k]]);
+            }
+          },
+          [&](int j, uint32_t st) {
+            const int t = lds_i32(st);
+            row_lds(dr2, st + RP_HDR, n4);
+            for (int k = 1; k < D.K; ++k) {
+              row_lds(tmp, st + RP_HDR + k * rowb, n4);
+              row_add(dr2, tmp);
+            }
+            for (int k = 0; k < D.K; ++k) {
+              const float ze = lds_f32(st + 4u * (2 + D.K + k));
+              if (ze != 0.f) {
+                row_ld(tmp, Wr + (long long)lds_i32(st + 4u * (2 + k)) * D.d, n4);
+                row_axpy(dr2, tmp, ze);
+              }
+            }
+            row_st(DR2 + (long long)t * D.d, dr2, n4);
+            row_lds(x, st + RP_HDR + D.K * rowb, n4);
+            row_lds(dx, st + RP_HDR + (D.K + 1) * rowb, n4);
+            row_norm_bwd(dxm, dr2, x, lds_f32(st + 4u), g, D.d);
+            row_add(dx, dxm);
+            row_st(DX + (long long)t * D.d, dx, n4);
+            row_st_op(DXO + (long long)t * D.d, dx, n4);
+          },
+          [&](int) {});
+    } else {
+      for (int t = me; t < D.T; t += nw) {
+        row_scale(dr2, g, 0.f);
+        for (int k = 0; k < D.K; ++k) {
+          row_ld(tmp, DXS + (long long)INVM[(long long)t * D.K + k] * D.d, n4);
+          row_add(dr2, tmp);
         }
+        const float* dz = DZ + (long long)t * D.E;
+        for (int e = 0; e < D.E; ++e) {
+          const float ze = dz[e];
+          if (ze != 0.f) {
+            row_ld(tmp, Wr + (long long)e * D.d, n4);
+            row_axpy(dr2, tmp, ze);
+          }
+        }
+        row_st(DR2 + (long long)t * D.d, dr2, n4);
+        row_ld(x, XM + (long long)t * D.d, n4);
+        row_ld(dx, DX + (long long)t * D.d, n4);
+        row_norm_bwd(dxm, dr2, x, inv2[t], g, D.d);
+        row_add(dx, dxm);
+        row_st(DX + (long long)t * D.d, dx, n4);
+        row_st_op(DXO + (long long)t * D.d, dx, n4);
       }
-      row_st(DR2 + (long long)t * D.d, dr2, n4);
-      row_ld(x, XM + (long long)t * D.d, n4);
-      row_ld(dx, DX + (long long)t * D.d, n4);
-      row_norm_bwd(dxm, dr2, x, inv2[t], g, D.d);
-      row_add(dx, dxm);
-      row_st(DX + (long long)t * D.d, dx, n4);
-      row_st_op(DXO + (long long)t * D.d, dx, n4);
     }
   });
+  if (piped) rp_end(p, ok);
   s.next(s.G);
 }
 
 // Attention RMSNorm backward into dx.
 template <class OP>
-__device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s) {
+__device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s, char* smem) {
   const MtDims& D = a.D;
   const float* DR = abuf<float>(a, A_DR);
   const float* X = abuf<float>(a, A_X) + (long long)l * D.T * D.d;
   const float* inv = abuf<float>(a, A_INV1) + (long long)l * D.T;
   float* DX = abuf<float>(a, A_DX);
   const int n4 = D.d / 4, nw = s.G * MT_WARPS;
+  const int me = s.first() * MT_WARPS + (threadIdx.x >> 5);
+  const uint32_t rowb = (uint32_t)D.d * 4u;
+  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, 3u * rowb);
+  if (p.ns > 0) rp_begin(p);
+  bool ok = true;
   with_nc(D.d, [&](auto NCc) {
     constexpr int NC = decltype(NCc)::value;
     Row<NC> g, dy, x, dx, acc;
     row_ld(g, pmaster(a, P_ATTN_NORM) + (long long)l * D.d, n4);
-    for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
-      row_ld(dy, DR + (long long)t * D.d, n4);
-      row_ld(x, X + (long long)t * D.d, n4);
-      row_ld(acc, DX + (long long)t * D.d, n4);
-      row_norm_bwd(dx, dy, x, inv[t], g, D.d);
-      row_add(acc, dx);
-      row_st(DX + (long long)t * D.d, acc, n4);
+    if (p.ns > 0) {
+      // staged: dr, x and dx rows of each token; header: t, 1/rms
+      const int n = me < D.T ? (D.T - 1 - me) / nw + 1 : 0;
+      ok = rp_run(
+          p, n, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 5,
+          [&](int j, uint32_t st, uint32_t bar) {
+            const int t = me + j * nw;
+            sts_i32(st, t);
+            sts_f32(st + 4u, inv[t]);
+            mbar_expect_tx(bar, 3u * rowb);
+            bulk_g2s(st + RP_HDR, DR + (long long)t * D.d, rowb, bar);
+            bulk_g2s(st + RP_HDR + rowb, X + (long long)t * D.d, rowb, bar);
+            bulk_g2s(st + RP_HDR + 2u * rowb, DX + (long long)t * D.d, rowb, bar);
+          },
+          [&](int j, uint32_t st) {
+            const int t = lds_i32(st);
+            row_lds(dy, st + RP_HDR, n4);
+            row_lds(x, st + RP_HDR + rowb, n4);
+            row_lds(acc, st + RP_HDR + 2u * rowb, n4);
+            row_norm_bwd(dx, dy, x, lds_f32(st + 4u), g, D.d);
+            row_add(acc, dx);
+            row_st(DX + (long long)t * D.d, acc, n4);
+          },
+          [&](int) {});
+    } else {
+      for (int t = me; t < D.T; t += nw) {
+        row_ld(dy, DR + (long long)t * D.d, n4);
+        row_ld(x, X + (long long)t * D.d, n4);
+        row_ld(acc, DX + (long long)t * D.d, n4);
+        row_norm_bwd(dx, dy, x, inv[t], g, D.d);
+        row_add(acc, dx);
+        row_st(DX + (long long)t * D.d, acc, n4);
+      }
     }
   });
+  if (p.ns > 0) rp_end(p, ok);
   s.next(s.G);
 }
 
@@ -1386,9 +1669,9 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
       run_gemm<OP>(a, g, s, smem, tc); TJ(4);
     }
     if (!dep) MT_SYNC();
-    job_router<OP>(a, l, (float*)smem, dep ? DEPC(l, DEP_XMID) : nullptr, (unsigned)(D.d / TC_BN)); TJ(5);
+    job_router<OP>(a, l, smem, dep ? DEPC(l, DEP_XMID) : nullptr, (unsigned)(D.d / TC_BN)); TJ(5);
     MT_SYNC();
-    job_route<OP>(a, l, (int*)smem); TJ(6);
+    job_route<OP>(a, l, smem); TJ(6);
     MT_SYNC();
     {
       GemmDesc g = gm.gateup(l);
@@ -1402,7 +1685,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
       run_gemm<OP>(a, g, s, smem, tc); TJ(8);
     }
     MT_SYNC();
-    job_combine<OP>(a, l, s, dep ? DEPC(l, DEP_RN) : nullptr); TJ(9);
+    job_combine<OP>(a, l, s, dep ? DEPC(l, DEP_RN) : nullptr, smem); TJ(9);
     if (!dep) MT_SYNC();
   }
   {
@@ -1428,7 +1711,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     job_colpart(a, c, s, (float*)smem); TJ(16);
   }
   for (int l = D.L - 1; l >= 0; --l) {
-    job_moe_bwd1<OP>(a, l, s); TJ(17);
+    job_moe_bwd1<OP>(a, l, s, smem); TJ(17);
     if (l < D.L - 1) {
       // attention-norm gain partials of layer l+1 (DR of layer l+1 is still live)
       ColArgs c{COL_GAIN, abuf<float>(a, A_DR), abuf<float>(a, A_X) + (long long)(l + 1) * D.T * D.d,
@@ -1445,7 +1728,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     run_gemm<OP>(a, gm.gateup_dgrad(l), s, smem, tc); TJ(21);
     run_gemm<OP>(a, gm.gateup_wgrad(l), s, smem, tc); TJ(22);
     MT_SYNC();
-    job_moe_bwd2<OP>(a, l, s); TJ(23);
+    job_moe_bwd2<OP>(a, l, s, smem); TJ(23);
     MT_SYNC();
     {
       ColArgs c{COL_MOE, abuf<float>(a, A_DR2), abuf<float>(a, A_XM) + (long long)l * D.T * D.d,
@@ -1464,7 +1747,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     run_gemm<OP>(a, gm.qkv_dgrad(l), s, smem, tc); TJ(27);
     run_gemm<OP>(a, gm.qkv_wgrad(l), s, smem, tc); TJ(28);
     MT_SYNC();
-    job_attn_norm_bwd<OP>(a, l, s); TJ(29);
+    job_attn_norm_bwd<OP>(a, l, s, smem); TJ(29);
     job_ksplit_sum(a, pgrad(a, P_WQKV) + (long long)l * 3 * D.hq * D.d, 3 * D.hq, D.d, s); TJ(33);
     MT_SYNC();
   }

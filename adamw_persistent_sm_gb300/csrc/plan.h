@@ -155,6 +155,7 @@ struct KArgs {
   int use_tc_attn;              // tensor-core attention (bf16 only)
   int use_tm_attn;              // attention forward on tcgen05 with TMEM accumulators (needs use_tc)
   int deps;                     // dependency counters replace the grid barriers they cover
+  int smem_bytes;               // dynamic shared memory of the launch
   CUtensorMap maps[MT_NMAPS];
 };
 
