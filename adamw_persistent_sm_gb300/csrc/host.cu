@@ -167,7 +167,7 @@ size_t smem_bytes(const MtDims& D, bool tc) {
   // column reductions: staged 1/rms and router gradients, token-lane partials
   const int er = D.E <= 4 ? 4 : D.E <= 16 ? 16 : D.E <= 32 ? 32 : 64;
   const int cw = D.E <= 16 ? 4 : D.E <= 32 ? 2 : 1;
-  size_t col = (size_t)(256 + 256 * D.E + 3 * (er + 1) * 64 * cw) * 4;
+  size_t col = 1024 + (size_t)(256 + 256 * D.E + 3 * (er + 1) * 64 * cw) * 4;
   size_t need = attn > simt ? attn : simt;
   if (router > need) need = router;
   if (col > need) need = col;

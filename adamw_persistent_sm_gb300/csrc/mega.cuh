@@ -636,25 +636,91 @@ __device__ __noinline__ void job_ce(const KArgs& a, Sched& s) {
 // ===========================================================================
 // backward row jobs
 // ===========================================================================
+// Norm-gain gradient sum_t dy_t * xhat_t, fused with the norm backward:
+// each warp keeps a register partial over its tokens (token order); at the
+// end of the job the CTA adds its warps' partials in warp order and stores
+// them as PART[cta][E+1][:]; a later phase sums the CTAs in CTA order.
+template <int NC>
+__device__ __forceinline__ void row_gain_acc(Row<NC>& acc, const Row<NC>& dy, const Row<NC>& x, float inv) {
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    acc.v[i].x = fmaf(dy.v[i].x, x.v[i].x * inv, acc.v[i].x);
+    acc.v[i].y = fmaf(dy.v[i].y, x.v[i].y * inv, acc.v[i].y);
+    acc.v[i].z = fmaf(dy.v[i].z, x.v[i].z * inv, acc.v[i].z);
+    acc.v[i].w = fmaf(dy.v[i].w, x.v[i].w * inv, acc.v[i].w);
+  }
+}
+template <int NC>
+__device__ __forceinline__ void gain_partial_store(const KArgs& a, const Row<NC>& acc, char* smem) {
+  const MtDims& D = a.D;
+  const int warp = threadIdx.x >> 5, n4 = D.d / 4;
+  float* sw = reinterpret_cast<float*>(smem + RP_WIN_OFF);   // [MT_WARPS][d]
+  __syncthreads();
+  row_st(sw + warp * D.d, acc, n4);
+  __syncthreads();
+  float* out = abuf<float>(a, A_PART) + ((long long)blockIdx.x * (D.E + 2) + D.E + 1) * D.d;
+  for (int c = threadIdx.x; c < D.d; c += MT_THREADS) {
+    float v = 0.f;
+    for (int w = 0; w < MT_WARPS; ++w) v += sw[w * D.d + c];
+    out[c] = v;
+  }
+  __syncthreads();
+}
+
 // dx = d(final RMSNorm) from d rf.
 template <class OP>
-__device__ __noinline__ void job_final_norm_bwd(const KArgs& a, Sched& s) {
+__device__ __noinline__ void job_final_norm_bwd(const KArgs& a, Sched& s, char* smem) {
   const MtDims& D = a.D;
   const float* DRF = abuf<float>(a, A_DRF);
   const float* X = abuf<float>(a, A_X) + (long long)D.L * D.T * D.d;
   const float* inv = abuf<float>(a, A_INVF);
   float* DX = abuf<float>(a, A_DX);
   const int n4 = D.d / 4, nw = s.G * MT_WARPS;
+  const int me = s.first() * MT_WARPS + (threadIdx.x >> 5);
+  const uint32_t rowb = (uint32_t)D.d * 4u;
+  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, 2u * rowb);
+  if (p.ns > 0) rp_begin(p);
+  bool ok = true;
   with_nc(D.d, [&](auto NCc) {
     constexpr int NC = decltype(NCc)::value;
-    Row<NC> g, dy, x, dx;
+    Row<NC> g, dy, x, dx, acc;
     row_ld(g, pmaster(a, P_FINAL_NORM), n4);
-    for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
-      row_ld(dy, DRF + (long long)t * D.d, n4);
-      row_ld(x, X + (long long)t * D.d, n4);
-      row_norm_bwd(dx, dy, x, inv[t], g, D.d);
-      row_st(DX + (long long)t * D.d, dx, n4);
+    row_scale(acc, g, 0.f);
+    if (p.ns > 0) {
+      // staged: d rf and x rows of each token; header: t, 1/rms
+      const int n = me < D.T ? (D.T - 1 - me) / nw + 1 : 0;
+      ok = rp_run(
+          p, n, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 7,
+          [&](int j, uint32_t st, uint32_t bar) {
+            const int t = me + j * nw;
+            sts_i32(st, t);
+            sts_f32(st + 4u, inv[t]);
+            mbar_expect_tx(bar, 2u * rowb);
+            bulk_g2s(st + RP_HDR, DRF + (long long)t * D.d, rowb, bar);
+            bulk_g2s(st + RP_HDR + rowb, X + (long long)t * D.d, rowb, bar);
+          },
+          [&](int j, uint32_t st) {
+            const int t = lds_i32(st);
+            const float iv = lds_f32(st + 4u);
+            row_lds(dy, st + RP_HDR, n4);
+            row_lds(x, st + RP_HDR + rowb, n4);
+            row_norm_bwd(dx, dy, x, iv, g, D.d);
+            row_st(DX + (long long)t * D.d, dx, n4);
+            row_gain_acc(acc, dy, x, iv);
+          },
+          [&](int) {});
+    } else {
+      for (int t = me; t < D.T; t += nw) {
+        row_ld(dy, DRF + (long long)t * D.d, n4);
+        row_ld(x, X + (long long)t * D.d, n4);
+        const float iv = inv[t];
+        row_norm_bwd(dx, dy, x, iv, g, D.d);
+        row_st(DX + (long long)t * D.d, dx, n4);
+        row_gain_acc(acc, dy, x, iv);
+      }
     }
+    if (p.ns > 0) rp_end(p, ok);
+    gain_partial_store(a, acc, smem);
   });
   s.next(s.G);
 }
@@ -673,7 +739,6 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char*
   const int* IDX = abuf<int>(a, A_IDX) + (long long)l * D.T * D.K;
   const int* INVM = abuf<int>(a, A_INVM) + (long long)l * D.T * D.K;
   const int* OFFS = abuf<int>(a, A_OFFS) + (long long)l * (D.E + 1);
-  const int* PERM = abuf<int>(a, A_PERM) + (long long)l * D.Pmax;
   OP* DY = abuf<OP>(a, A_DY);
   float* DZ = abuf<float>(a, A_DZ);
   const int nw = s.G * MT_WARPS;
@@ -758,12 +823,20 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char*
         }
       }
     }
-    // pad rows of dY: PERM == -1 inside [0, OFFS[E])
+    // pad rows of dY: [OFFS[e] + n_e, OFFS[e+1]) of every expert segment,
+    // n_e = rows routed to e (the route job's totals); the segment bounds
+    // are read once per warp, two experts per lane
 #pragma unroll
     for (int i = 0; i < NC; ++i) dy.v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int nrows = OFFS[D.E];
-    for (int p = me; p < nrows; p += nw)
-      if (PERM[p] < 0) row_st_op(DY + (long long)p * D.d, dy, n4);
+    const int* ncnt = abuf<ArenaHdr>(a, A_HDR)->expert_counts + l * MT_MAX_EXPERTS;
+    int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
+    if (lane < D.E) { lo0 = OFFS[lane] + ncnt[lane]; hi0 = OFFS[lane + 1]; }
+    if (lane + 32 < D.E) { lo1 = OFFS[lane + 32] + ncnt[lane + 32]; hi1 = OFFS[lane + 33]; }
+    for (int e = 0; e < D.E; ++e) {
+      const int p0 = __shfl_sync(0xffffffffu, e < 32 ? lo0 : lo1, e & 31);
+      const int p1 = __shfl_sync(0xffffffffu, e < 32 ? hi0 : hi1, e & 31);
+      for (int p = p0 + me; p < p1; p += nw) row_st_op(DY + (long long)p * D.d, dy, n4);
+    }
   });
   if (piped) rp_end(p, ok);
   s.next(s.G);
@@ -784,7 +857,6 @@ __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char*
   const float* Wr = pmaster(a, P_ROUTER) + (long long)l * D.E * D.d;
   const float* XM = abuf<float>(a, A_XM) + (long long)l * D.T * D.d;
   const float* inv2 = abuf<float>(a, A_INV2) + (long long)l * D.T;
-  float* DR2 = abuf<float>(a, A_DR2);
   float* DX = abuf<float>(a, A_DX);
   OP* DXO = abuf<OP>(a, A_DXO);
   const int nw = s.G * MT_WARPS;
@@ -796,8 +868,9 @@ __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char*
   bool ok = true;
   with_nc(D.d, [&](auto NCc) {
     constexpr int NC = decltype(NCc)::value;
-    Row<NC> g, dr2, tmp, x, dx, dxm;
+    Row<NC> g, dr2, tmp, x, dx, gacc;
     row_ld(g, pmaster(a, P_MOE_NORM) + (long long)l * D.d, n4);
+    row_scale(gacc, g, 0.f);
     if (piped) {
       // staged: the K expert-input gradient rows, x_mid and dx of each token;
       // header: t, 1/rms, then the chosen experts in ascending order with
@@ -829,10 +902,7 @@ __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char*
           [&](int j, uint32_t st) {
             const int t = lds_i32(st);
             row_lds(dr2, st + RP_HDR, n4);
-            for (int k = 1; k < D.K; ++k) {
-              row_lds(tmp, st + RP_HDR + k * rowb, n4);
-              row_add(dr2, tmp);
-            }
+            for (int k = 1; k < D.K; ++k) row_add_lds(dr2, st + RP_HDR + k * rowb, n4);
             for (int k = 0; k < D.K; ++k) {
               const float ze = lds_f32(st + 4u * (2 + D.K + k));
               if (ze != 0.f) {
@@ -840,11 +910,11 @@ __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char*
                 row_axpy(dr2, tmp, ze);
               }
             }
-            row_st(DR2 + (long long)t * D.d, dr2, n4);
             row_lds(x, st + RP_HDR + D.K * rowb, n4);
+            const float iv = lds_f32(st + 4u);
+            row_gain_acc(gacc, dr2, x, iv);
             row_lds(dx, st + RP_HDR + (D.K + 1) * rowb, n4);
-            row_norm_bwd(dxm, dr2, x, lds_f32(st + 4u), g, D.d);
-            row_add(dx, dxm);
+            row_norm_bwd_add(dx, dr2, x, iv, g, D.d);
             row_st(DX + (long long)t * D.d, dx, n4);
             row_st_op(DXO + (long long)t * D.d, dx, n4);
           },
@@ -864,17 +934,18 @@ __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char*
             row_axpy(dr2, tmp, ze);
           }
         }
-        row_st(DR2 + (long long)t * D.d, dr2, n4);
         row_ld(x, XM + (long long)t * D.d, n4);
         row_ld(dx, DX + (long long)t * D.d, n4);
-        row_norm_bwd(dxm, dr2, x, inv2[t], g, D.d);
-        row_add(dx, dxm);
+        const float iv = inv2[t];
+        row_gain_acc(gacc, dr2, x, iv);
+        row_norm_bwd_add(dx, dr2, x, iv, g, D.d);
         row_st(DX + (long long)t * D.d, dx, n4);
         row_st_op(DXO + (long long)t * D.d, dx, n4);
       }
     }
+    if (piped) rp_end(p, ok);
+    gain_partial_store(a, gacc, smem);
   });
-  if (piped) rp_end(p, ok);
   s.next(s.G);
 }
 
@@ -894,8 +965,9 @@ __device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s, 
   bool ok = true;
   with_nc(D.d, [&](auto NCc) {
     constexpr int NC = decltype(NCc)::value;
-    Row<NC> g, dy, x, dx, acc;
+    Row<NC> g, dy, x, dx, acc, gacc;
     row_ld(g, pmaster(a, P_ATTN_NORM) + (long long)l * D.d, n4);
+    row_scale(gacc, g, 0.f);
     if (p.ns > 0) {
       // staged: dr, x and dx rows of each token; header: t, 1/rms
       const int n = me < D.T ? (D.T - 1 - me) / nw + 1 : 0;
@@ -915,9 +987,11 @@ __device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s, 
             row_lds(dy, st + RP_HDR, n4);
             row_lds(x, st + RP_HDR + rowb, n4);
             row_lds(acc, st + RP_HDR + 2u * rowb, n4);
-            row_norm_bwd(dx, dy, x, lds_f32(st + 4u), g, D.d);
+            const float iv = lds_f32(st + 4u);
+            row_norm_bwd(dx, dy, x, iv, g, D.d);
             row_add(acc, dx);
             row_st(DX + (long long)t * D.d, acc, n4);
+            row_gain_acc(gacc, dy, x, iv);
           },
           [&](int) {});
     } else {
@@ -925,13 +999,16 @@ __device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s, 
         row_ld(dy, DR + (long long)t * D.d, n4);
         row_ld(x, X + (long long)t * D.d, n4);
         row_ld(acc, DX + (long long)t * D.d, n4);
-        row_norm_bwd(dx, dy, x, inv[t], g, D.d);
+        const float iv = inv[t];
+        row_norm_bwd(dx, dy, x, iv, g, D.d);
         row_add(acc, dx);
         row_st(DX + (long long)t * D.d, acc, n4);
+        row_gain_acc(gacc, dy, x, iv);
       }
     }
+    if (p.ns > 0) rp_end(p, ok);
+    gain_partial_store(a, gacc, smem);
   });
-  if (p.ns > 0) rp_end(p, ok);
   s.next(s.G);
 }
 
@@ -983,7 +1060,7 @@ __device__ __forceinline__ void ld_cols(float (&v)[CW], const float* p) {
 }
 
 template <int ER, int CW>
-__device__ void colpart_items(const KArgs& a, const ColArgs& c, Sched& s, float* sm) {
+__device__ void colpart_items(const KArgs& a, const ColArgs& c, Sched& s, char* smem) {
   constexpr int TPL = MT_THREADS / COL_LANES;   // threads per token lane
   constexpr int CB = TPL * CW;                  // columns per item
   constexpr int U = 1;                          // tokens in flight per thread
@@ -991,14 +1068,15 @@ __device__ void colpart_items(const KArgs& a, const ColArgs& c, Sched& s, float*
   const MtDims& D = a.D;
   const int G = s.G;
   const bool moe = (c.kind == COL_MOE);
+  const bool gain = c.dy != nullptr;            // the gain row (else router rows only)
   const int E = moe ? D.E : 0;
   const int ncb = (D.d + CB - 1) / CB;
   const int nchunk = col_nchunks(D, G, E);
   const int ch = (D.T + nchunk - 1) / nchunk;
   const int items = ncb * nchunk;
   float* PART = abuf<float>(a, A_PART);
-  float* s_inv = sm;                            // [SUB]
-  float* s_dz = sm + SUB;                       // [SUB][E]
+  float* s_inv = reinterpret_cast<float*>(smem + RP_WIN_OFF);   // [SUB]
+  float* s_dz = s_inv + SUB;                    // [SUB][E]
   float* s_red = s_dz + SUB * E;                // [COL_LANES - 1][ER + 1][CB]
   const int tl = threadIdx.x / TPL, tc = threadIdx.x % TPL;
   for (int it = s.first(); it < items; it += G) {
@@ -1031,7 +1109,7 @@ __device__ void colpart_items(const KArgs& a, const ColArgs& c, Sched& s, float*
           if (tk < n) {
             const long long off = (long long)(s0 + tk) * D.d + col;
             ld_cols<CW>(xv[u], c.x + off);
-            ld_cols<CW>(dyv[u], c.dy + off);
+            if (gain) ld_cols<CW>(dyv[u], c.dy + off);
           }
         }
 #pragma unroll
@@ -1042,7 +1120,7 @@ __device__ void colpart_items(const KArgs& a, const ColArgs& c, Sched& s, float*
 #pragma unroll
             for (int j = 0; j < CW; ++j) {
               const float xh = xv[u][j] * iv;
-              acc[ER][j] = fmaf(dyv[u][j], xh, acc[ER][j]);      // gain gradient row
+              if (gain) acc[ER][j] = fmaf(dyv[u][j], xh, acc[ER][j]);      // gain gradient row
               if (ER > 0) {
                 const float r2 = xh * gcol[j];
                 const float* dz = s_dz + tk * E;
@@ -1068,6 +1146,7 @@ __device__ void colpart_items(const KArgs& a, const ColArgs& c, Sched& s, float*
 #pragma unroll
       for (int r = 0; r <= ER; ++r) {
         if (r < ER && r >= E) continue;
+        if (r == ER && !gain) continue;
         const int orow = (r == ER) ? E : r;
 #pragma unroll
         for (int j = 0; j < CW; ++j) {
@@ -1084,10 +1163,9 @@ __device__ void colpart_items(const KArgs& a, const ColArgs& c, Sched& s, float*
   s.next(items);
 }
 
-static __device__ __noinline__ void job_colpart(const KArgs& a, const ColArgs& c, Sched& s, float* sm) {
+static __device__ __noinline__ void job_colpart(const KArgs& a, const ColArgs& c, Sched& s, char* sm) {
   const int E = (c.kind == COL_MOE) ? a.D.E : 0;
-  if (E == 0) colpart_items<0, 4>(a, c, s, sm);
-  else if (E <= 4) colpart_items<4, 4>(a, c, s, sm);
+  if (E <= 4) colpart_items<4, 4>(a, c, s, sm);
   else if (E <= 16) colpart_items<16, 4>(a, c, s, sm);
   else if (E <= 32) colpart_items<32, 2>(a, c, s, sm);
   else colpart_items<64, 1>(a, c, s, sm);
@@ -1096,10 +1174,10 @@ static __device__ __noinline__ void job_colpart(const KArgs& a, const ColArgs& c
 // out[r][col] (+)= sum over chunks of PART[chunk][row0 + r][col]; E_kind is
 // the router-row count of the reduction that wrote those rows (0: gain only).
 static __device__ __noinline__ void job_colfinal(const KArgs& a, int row0, int nrows, int E_kind, float* out_rows,
-                                                 float* out_last, int last_is_separate, Sched& s) {
+                                                 float* out_last, int last_is_separate, Sched& s, int nchunks = 0) {
   const MtDims& D = a.D;
   const int G = s.G;
-  const int nused = col_nchunks(D, G, E_kind);
+  const int nused = nchunks > 0 ? nchunks : col_nchunks(D, G, E_kind);
   const float* PART = abuf<float>(a, A_PART);
   const int n = nrows * D.d;
   const bool acc = a.micro_index > 0;
@@ -1260,13 +1338,11 @@ __device__ __noinline__ void job_adamw(const KArgs& a) {
   }
   const long long n = a.n_params;
   const long long n4 = n / 4;
-  const long long b0 = n4 * c / G, b1 = n4 * (c + 1) / G;
   float4* p4 = reinterpret_cast<float4*>(a.master);
   const float4* g4 = reinterpret_cast<const float4*>(a.grads);
   float4* m4 = reinterpret_cast<float4*>(a.adam_m);
   float4* v4 = reinterpret_cast<float4*>(a.adam_v);
   __nv_bfloat16* sh = (sizeof(OP) == 2) ? (__nv_bfloat16*)a.shadow : nullptr;
-  // two float4 groups per iteration: eight 16-byte loads in flight per thread
   auto step4 = [&](long long j, float4 p, const float4 g, float4 m, float4 v) {
     adamw_elem<OP>(a, coef, p.x, g.x, m.x, v.x);
     adamw_elem<OP>(a, coef, p.y, g.y, m.y, v.y);
@@ -1283,15 +1359,35 @@ __device__ __noinline__ void job_adamw(const KArgs& a) {
       reinterpret_cast<uint2*>(sh)[j] = u;
     }
   };
-  long long i = b0 + threadIdx.x;
-  for (; i + MT_THREADS < b1; i += 2 * MT_THREADS) {
-    const long long j = i + MT_THREADS;
-    const float4 p0 = p4[i], m0 = m4[i], v0 = v4[i], g0 = g4[i];
-    const float4 p1 = p4[j], m1 = m4[j], v1 = v4[j], g1 = g4[j];
-    step4(i, p0, g0, m0, v0);
-    step4(j, p1, g1, m1, v1);
+  // The sweep is elementwise, so any split gives the same result: chunks of
+  // AW_CHUNK float4 groups are drawn from a ticket counter (zeroed at the
+  // start of the launch), so that SMs that stream faster take more chunks;
+  // the next ticket is drawn while the current chunk is processed.
+  constexpr long long AW_CHUNK = 4096;
+  constexpr int UA = 4;                 // float4 groups per thread in flight (16 loads)
+  const long long nchunk = (n4 + AW_CHUNK - 1) / AW_CHUNK;
+  unsigned* ticket = abuf<unsigned>(a, A_DEP) + ticket_offset(a.D, a.D.L, TK_ADAMW);
+  __shared__ int s_next;
+  long long cur = draw_ticket(ticket);
+  while (cur < nchunk) {
+    if (threadIdx.x == 0) s_next = (int)atomicAdd(ticket, 1u);
+    const long long b1 = min(n4, (cur + 1) * AW_CHUNK);
+    long long i = cur * AW_CHUNK + threadIdx.x;
+    for (; i + (UA - 1) * MT_THREADS < b1; i += UA * MT_THREADS) {
+      float4 pp[UA], mm[UA], vv[UA], gg[UA];
+#pragma unroll
+      for (int u = 0; u < UA; ++u) {
+        const long long j = i + u * MT_THREADS;
+        pp[u] = p4[j]; mm[u] = m4[j]; vv[u] = v4[j]; gg[u] = g4[j];
+      }
+#pragma unroll
+      for (int u = 0; u < UA; ++u) step4(i + u * MT_THREADS, pp[u], gg[u], mm[u], vv[u]);
+    }
+    for (; i < b1; i += MT_THREADS) step4(i, p4[i], g4[i], m4[i], v4[i]);
+    __syncthreads();
+    cur = s_next;
+    __syncthreads();
   }
-  if (i < b1) step4(i, p4[i], g4[i], m4[i], v4[i]);
   if (c == G - 1) {
     for (long long i = n4 * 4 + threadIdx.x; i < n; i += MT_THREADS) {
       float p = a.master[i], m = a.adam_m[i], v = a.adam_v[i];
@@ -1702,25 +1798,15 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   run_gemm<OP>(a, gm.lm_dgrad(), s, smem, tc); TJ(13);
   run_gemm<OP>(a, gm.lm_wgrad(), s, smem, tc); TJ(14);
   MT_SYNC();
-  job_final_norm_bwd<OP>(a, s); TJ(15);
+  // the norm-gain gradients: per-CTA partials (PART row E+1) left by the
+  // norm backward jobs, summed in CTA order by job_colfinal
+  job_final_norm_bwd<OP>(a, s, smem); TJ(15);
   MT_SYNC();
-  {
-    // final-norm gain partials (DRF stays valid until the next LM-head use)
-    ColArgs c{COL_GAIN, abuf<float>(a, A_DRF), abuf<float>(a, A_X) + (long long)D.L * D.T * D.d,
-              abuf<float>(a, A_INVF), nullptr, nullptr, D.E + 1};
-    job_colpart(a, c, s, (float*)smem); TJ(16);
-  }
   for (int l = D.L - 1; l >= 0; --l) {
     job_moe_bwd1<OP>(a, l, s, smem); TJ(17);
-    if (l < D.L - 1) {
-      // attention-norm gain partials of layer l+1 (DR of layer l+1 is still live)
-      ColArgs c{COL_GAIN, abuf<float>(a, A_DR), abuf<float>(a, A_X) + (long long)(l + 1) * D.T * D.d,
-                abuf<float>(a, A_INV1) + (long long)(l + 1) * D.T, nullptr, nullptr, D.E + 1};
-      job_colpart(a, c, s, (float*)smem); TJ(16);
-    }
     MT_SYNC();
-    if (l == D.L - 1) job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_FINAL_NORM), nullptr, 0, s);
-    else job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM) + (long long)(l + 1) * D.d, nullptr, 0, s);
+    if (l == D.L - 1) job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_FINAL_NORM), nullptr, 0, s, (int)G);
+    else job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM) + (long long)(l + 1) * D.d, nullptr, 0, s, (int)G);
     TJ(18);
     run_gemm<OP>(a, gm.down_dgrad(l), s, smem, tc); TJ(19);
     run_gemm<OP>(a, gm.down_wgrad(l), s, smem, tc); TJ(20);
@@ -1731,16 +1817,18 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     job_moe_bwd2<OP>(a, l, s, smem); TJ(23);
     MT_SYNC();
     {
-      ColArgs c{COL_MOE, abuf<float>(a, A_DR2), abuf<float>(a, A_XM) + (long long)l * D.T * D.d,
+      // router-weight gradient partials (rows 0..E-1); the expert-norm gain
+      // partial was left by job_moe_bwd2
+      ColArgs c{COL_MOE, nullptr, abuf<float>(a, A_XM) + (long long)l * D.T * D.d,
                 abuf<float>(a, A_INV2) + (long long)l * D.T, pmaster(a, P_MOE_NORM) + (long long)l * D.d,
                 abuf<float>(a, A_DZ), 0};
-      job_colpart(a, c, s, (float*)smem); TJ(16);
+      job_colpart(a, c, s, smem); TJ(16);
     }
     run_gemm<OP>(a, gm.wo_dgrad(l), s, smem, tc); TJ(24);
     run_gemm<OP>(a, gm.wo_wgrad(l), s, smem, tc); TJ(25);
     MT_SYNC();
-    job_colfinal(a, 0, D.E + 1, D.E, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d,
-                 pgrad(a, P_MOE_NORM) + (long long)l * D.d, 1, s); TJ(18);
+    job_colfinal(a, 0, D.E, D.E, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d, nullptr, 0, s);
+    job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_MOE_NORM) + (long long)l * D.d, nullptr, 0, s, (int)G); TJ(18);
     job_ksplit_sum(a, pgrad(a, P_WO) + (long long)l * D.d * D.hq, D.d, D.hq, s); TJ(32);
     run_attn_bwd<OP>(a, l, s, smem, tc, attn_deps(l, TK_ATTN_BWD, false)); TJ(26);
     MT_SYNC();
@@ -1751,21 +1839,16 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     job_ksplit_sum(a, pgrad(a, P_WQKV) + (long long)l * 3 * D.hq * D.d, 3 * D.hq, D.d, s); TJ(33);
     MT_SYNC();
   }
-  {
-    ColArgs c{COL_GAIN, abuf<float>(a, A_DR), abuf<float>(a, A_X), abuf<float>(a, A_INV1), nullptr,
-              nullptr, D.E + 1};
-    job_colpart(a, c, s, (float*)smem); TJ(16);
-  }
   job_embed_bwd(a, (int*)smem); TJ(30);
   MT_SYNC();
-  job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM), nullptr, 0, s); TJ(18);
+  job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM), nullptr, 0, s, (int)G); TJ(18);
 
   // ---------------- optimizer (last microbatch) ----------------
   if (a.run_opt) {
     MT_SYNC();
     job_norm_partial(a, (double*)smem); TJ(31);
     MT_SYNC();
-    job_adamw<OP>(a);
+    job_adamw<OP>(a); TJ(34);
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     hdr->micro_index = a.micro_index;

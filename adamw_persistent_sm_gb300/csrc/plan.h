@@ -112,7 +112,7 @@ enum DepKind {
 };
 #define MT_DEP_GROUP 32         // tokens per combine item when counters are on
 #define MT_TICKETS 8            // ticket counters per layer (plus one set for the head)
-enum TicketId { TK_ATTN_FWD = 0, TK_ATTN_BWD };
+enum TicketId { TK_ATTN_FWD = 0, TK_ATTN_BWD, TK_ADAMW };
 __host__ __device__ inline long long dep_blocks(const MtDims& D, int kind) {
   return kind == DEP_ACT ? D.Pmax / MT_TILE_M : (D.T + MT_TILE_M - 1) / MT_TILE_M;
 }

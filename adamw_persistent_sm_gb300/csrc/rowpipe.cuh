@@ -78,6 +78,20 @@ __device__ __forceinline__ void row_lds(Row<NC>& r, uint32_t a, int n4) {
 // start of a job and invalidate them at its end.
 static __shared__ __align__(8) unsigned long long rp_bars[MT_WARPS * RP_MAX_STAGES];
 
+// r += the staged row at shared address `a` (one float4 at a time)
+template <int NC>
+__device__ __forceinline__ void row_add_lds(Row<NC>& r, uint32_t a, int n4) {
+  const int l = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    const int c = l + 32 * i;
+    if (c < n4) {
+      const float4 v = lds4(a + 16u * (uint32_t)c);
+      r.v[i].x += v.x; r.v[i].y += v.y; r.v[i].z += v.z; r.v[i].w += v.w;
+    }
+  }
+}
+
 struct RowPipe {
   uint32_t ring;     // shared address of this warp's stage 0
   uint32_t bar;      // shared address of this warp's first mbarrier

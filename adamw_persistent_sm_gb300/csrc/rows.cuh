@@ -127,6 +127,27 @@ __device__ __forceinline__ void row_norm_bwd(Row<NC>& dx, const Row<NC>& dy, con
                           inv * (dy.v[i].z * g.v[i].z - x.v[i].z * inv * mean),
                           inv * (dy.v[i].w * g.v[i].w - x.v[i].w * inv * mean));
 }
+// dx += RMSNorm backward of dy (as row_norm_bwd, added in place)
+template <int NC>
+__device__ __forceinline__ void row_norm_bwd_add(Row<NC>& dx, const Row<NC>& dy, const Row<NC>& x, float inv,
+                                                 const Row<NC>& g, int d) {
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    s = fmaf(dy.v[i].x * g.v[i].x, x.v[i].x * inv, s);
+    s = fmaf(dy.v[i].y * g.v[i].y, x.v[i].y * inv, s);
+    s = fmaf(dy.v[i].z * g.v[i].z, x.v[i].z * inv, s);
+    s = fmaf(dy.v[i].w * g.v[i].w, x.v[i].w * inv, s);
+  }
+  const float mean = warp_sum(s) / (float)d;
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    dx.v[i].x += inv * (dy.v[i].x * g.v[i].x - x.v[i].x * inv * mean);
+    dx.v[i].y += inv * (dy.v[i].y * g.v[i].y - x.v[i].y * inv * mean);
+    dx.v[i].z += inv * (dy.v[i].z * g.v[i].z - x.v[i].z * inv * mean);
+    dx.v[i].w += inv * (dy.v[i].w * g.v[i].w - x.v[i].w * inv * mean);
+  }
+}
 template <int NC>
 __device__ __forceinline__ void row_add(Row<NC>& r, const Row<NC>& a) {
 #pragma unroll
