@@ -151,9 +151,12 @@ __device__ __noinline__ void job_router(const KArgs& a, int l, char* smem, const
   // shared memory: [mbarriers of the row rings | router weights (fp32, E x d)
   // | per-expert counts | row rings]
   float* sm = reinterpret_cast<float*>(smem + RP_WIN_OFF);
+  const uint32_t swr = smem_u32(sm);
   int* s_cnt = reinterpret_cast<int*>(sm + (long long)D.E * D.d);
   const uint32_t win = (RP_WIN_OFF + (uint32_t)D.E * rowb + 4u * 64u + 127u) & ~127u;
-  const RowPipe p = rp_make(smem, win, (uint32_t)a.smem_bytes, rowb);
+  // two tokens per stage: each router-weight value read from shared memory
+  // serves both (the logits are bound by shared-memory reads otherwise)
+  const RowPipe p = rp_make(smem, win, (uint32_t)a.smem_bytes, 2u * rowb);
   if (p.ns > 0) rp_begin(p);
   else __syncthreads();
   for (int i = threadIdx.x; i < D.E * D.d / 4; i += MT_THREADS)
@@ -170,102 +173,127 @@ __device__ __noinline__ void job_router(const KArgs& a, int l, char* smem, const
   bool ok = true;
   with_nc(D.d, [&](auto NCc) {
   constexpr int NC = decltype(NCc)::value;
-  Row<NC> gr, x, r, w;
+  Row<NC> gr, xa, xb;
   row_ld(gr, g, n4);
-  auto token = [&](int t) {
-    const float inv = row_rms_inv(x, D.d, a.norm_eps);
-    row_norm_apply(r, x, inv, gr);
-    row_st_op(R2 + (long long)t * D.d, r, n4);
-    if (lane == 0) inv2[t] = inv;
-    float z0 = -INFINITY, z1 = -INFINITY;   // experts lane and lane + 32
-    if (D.E <= 32) {
-      // lane-partial dot products for all experts, then one transpose-reduction
-      float p[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        float acc = 0.f;
-        if (e < D.E) {
-          row_ld(w, sm + (long long)e * D.d, n4);
-#pragma unroll
-          for (int i = 0; i < NC; ++i) {
-            acc = fmaf(r.v[i].x, w.v[i].x, acc);
-            acc = fmaf(r.v[i].y, w.v[i].y, acc);
-            acc = fmaf(r.v[i].z, w.v[i].z, acc);
-            acc = fmaf(r.v[i].w, w.v[i].w, acc);
-          }
-        }
-        p[e] = acc;
-      }
-      // after the step with offset o, lane l holds sums for the experts whose bit o matches l's bit o
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int e = 0; e < o; ++e) {
-          const float send = upper ? p[e] : p[e + o];
-          const float keep = upper ? p[e + o] : p[e];
-          p[e] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-      }
-      if (lane < D.E) z0 = p[0];
-    } else {
-      for (int e = 0; e < D.E; ++e) {
-        row_ld(w, sm + (long long)e * D.d, n4);
-        const float acc = row_dot(r, w);
-        if (e == lane) z0 = acc;
-        if (e == lane + 32) z1 = acc;
-      }
-    }
+  // softmax, token_topk and renormalised weights of one token from its logits
+  // (lane e holds expert e in z0, expert e + 32 in z1)
+  auto pick = [&](int t, float z0, float z1) {
     if (lane < D.E) Z[(long long)t * D.E + lane] = z0;
     if (lane + 32 < D.E) Z[(long long)t * D.E + lane + 32] = z1;
     const float zmax = warp_max(fmaxf(z0, z1));
     const float p0 = (lane < D.E) ? expf(z0 - zmax) : 0.f;
     const float p1 = (lane + 32 < D.E) ? expf(z1 - zmax) : 0.f;
-    // the softmax normaliser cancels in the renormalised weights
+    // the softmax normaliser cancels in the renormalised weights; slot k is
+    // kept by lane k
     float c0 = z0, c1 = z1;
-    float chosen_p[8];
-    int chosen_i[8];
+    float my_p = 0.f;
+    int my_i = 0;
     float psum = 0.f;
     for (int k = 0; k < D.K; ++k) {
       float v = c0;
       int idx = lane;
       if (c1 > v) { v = c1; idx = lane + 32; }
       warp_argmax(v, idx);
-      chosen_i[k] = idx;
       const float pk = __shfl_sync(0xffffffffu, idx < 32 ? p0 : p1, idx & 31);
-      chosen_p[k] = pk;
+      if (lane == k) { my_i = idx; my_p = pk; }
       psum += pk;
       if (idx == lane) c0 = -INFINITY;
       if (idx == lane + 32) c1 = -INFINITY;
     }
-    if (lane == 0) {
-      for (int k = 0; k < D.K; ++k) {
-        IDX[(long long)t * D.K + k] = chosen_i[k];
-        WGT[(long long)t * D.K + k] = chosen_p[k] / psum;
-        atomicAdd(&s_cnt[chosen_i[k]], 1);
-      }
+    if (lane < D.K) {
+      IDX[(long long)t * D.K + lane] = my_i;
+      WGT[(long long)t * D.K + lane] = my_p / psum;
+      atomicAdd(&s_cnt[my_i], 1);
     }
   };
+  // expert RMSNorm of tokens ta and tb (tb < 0: none), their operand rows,
+  // then the logits four experts per step: lane-partial dot products over the
+  // lane's columns and one warp sum each.  The expert loop is not unrolled,
+  // so that the code stays small in the instruction cache.
+  auto tokens2 = [&](int ta, int tb) {
+    const float inva = row_rms_inv(xa, D.d, a.norm_eps);
+    const float invb = row_rms_inv(xb, D.d, a.norm_eps);
+    row_norm_apply(xa, xa, inva, gr);
+    row_norm_apply(xb, xb, invb, gr);
+    row_st_op(R2 + (long long)ta * D.d, xa, n4);
+    if (lane == 0) inv2[ta] = inva;
+    if (tb >= 0) {
+      row_st_op(R2 + (long long)tb * D.d, xb, n4);
+      if (lane == 0) inv2[tb] = invb;
+    }
+    float za0 = -INFINITY, za1 = -INFINITY, zb0 = -INFINITY, zb1 = -INFINITY;
+#pragma unroll 1
+    for (int e0 = 0; e0 < D.E; e0 += 4) {
+      float aa[4], ab[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        aa[q] = 0.f;
+        ab[q] = 0.f;
+        if (e0 + q < D.E) {
+          const uint32_t wa = swr + (uint32_t)(e0 + q) * (uint32_t)D.d * 4u + 16u * (uint32_t)lane;
+#pragma unroll
+          for (int i = 0; i < NC; ++i) {
+            if (lane + 32 * i < n4) {
+              const float4 w4 = lds4(wa + 512u * (uint32_t)i);
+              aa[q] = fmaf(xa.v[i].x, w4.x, aa[q]);
+              aa[q] = fmaf(xa.v[i].y, w4.y, aa[q]);
+              aa[q] = fmaf(xa.v[i].z, w4.z, aa[q]);
+              aa[q] = fmaf(xa.v[i].w, w4.w, aa[q]);
+              ab[q] = fmaf(xb.v[i].x, w4.x, ab[q]);
+              ab[q] = fmaf(xb.v[i].y, w4.y, ab[q]);
+              ab[q] = fmaf(xb.v[i].z, w4.z, ab[q]);
+              ab[q] = fmaf(xb.v[i].w, w4.w, ab[q]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          aa[q] += __shfl_xor_sync(0xffffffffu, aa[q], o);
+          ab[q] += __shfl_xor_sync(0xffffffffu, ab[q], o);
+        }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (e0 + q == lane) { za0 = aa[q]; zb0 = ab[q]; }
+        if (e0 + q == lane + 32) { za1 = aa[q]; zb1 = ab[q]; }
+      }
+    }
+    pick(ta, za0, za1);
+    if (tb >= 0) pick(tb, zb0, zb1);
+  };
+  // this warp's tokens t0 + warp + 8 i, in pairs (i = 2j, 2j + 1)
+  const int nt = t0 + warp < t1 ? (t1 - 1 - t0 - warp) / MT_WARPS + 1 : 0;
   if (p.ns > 0) {
-    // staged: the x_mid row of each token; header: t
-    const int n = t0 + warp < t1 ? (t1 - 1 - t0 - warp) / MT_WARPS + 1 : 0;
+    // staged: the x_mid rows of a token pair; header: both tokens (-1: none)
     ok = rp_run(
-        p, n, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 0,
+        p, (nt + 1) / 2, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 0,
         [&](int j, uint32_t st, uint32_t bar) {
-          const int t = t0 + warp + j * MT_WARPS;
-          sts_i32(st, t);
-          mbar_expect_tx(bar, rowb);
-          bulk_g2s(st + RP_HDR, XM + (long long)t * D.d, rowb, bar);
+          const int ta = t0 + warp + 2 * j * MT_WARPS;
+          const int tb = (2 * j + 1 < nt) ? ta + MT_WARPS : -1;
+          sts_i32(st, ta);
+          sts_i32(st + 4u, tb);
+          mbar_expect_tx(bar, (tb >= 0 ? 2u : 1u) * rowb);
+          bulk_g2s(st + RP_HDR, XM + (long long)ta * D.d, rowb, bar);
+          if (tb >= 0) bulk_g2s(st + RP_HDR + rowb, XM + (long long)tb * D.d, rowb, bar);
         },
         [&](int j, uint32_t st) {
-          row_lds(x, st + RP_HDR, n4);
-          token(lds_i32(st));
+          const int ta = lds_i32(st), tb = lds_i32(st + 4u);
+          row_lds(xa, st + RP_HDR, n4);
+          if (tb >= 0) row_lds(xb, st + RP_HDR + rowb, n4);
+          else row_scale(xb, xa, 0.f);
+          tokens2(ta, tb);
         },
         [&](int) {});
   } else {
-    for (int t = t0 + warp; t < t1; t += MT_WARPS) {
-      row_ld(x, XM + (long long)t * D.d, n4);
-      token(t);
+    for (int i = 0; i < nt; i += 2) {
+      const int ta = t0 + warp + i * MT_WARPS;
+      const int tb = (i + 1 < nt) ? ta + MT_WARPS : -1;
+      row_ld(xa, XM + (long long)ta * D.d, n4);
+      if (tb >= 0) row_ld(xb, XM + (long long)tb * D.d, n4);
+      else row_scale(xb, xa, 0.f);
+      tokens2(ta, tb);
     }
   }
   });
@@ -430,7 +458,9 @@ __device__ __noinline__ void job_combine(const KArgs& a, int l, Sched& s, unsign
   // its CTA's group); with counters on, each finished group is published
   const int ng = (D.T + MT_DEP_GROUP - 1) / MT_DEP_GROUP;
   const uint32_t rowb = (uint32_t)D.d * 4u;
-  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, (uint32_t)(1 + D.K) * rowb);
+  // index table: per token of the warp (first RP_TBL), its K sorted rows and K weights
+  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, (uint32_t)(1 + D.K) * rowb,
+                            (uint32_t)(RP_TBL * 2 * D.K * 4));
   if (p.ns > 0 && D.K <= 8) {
     // staged: x_mid row and the K expert-output rows of each token
     constexpr int PER = MT_DEP_GROUP / MT_WARPS;
@@ -441,13 +471,24 @@ __device__ __noinline__ void job_combine(const KArgs& a, int l, Sched& s, unsign
       return t < D.T ? t : -1;
     };
     rp_begin(p);
+    const int n = mine * PER;
+    {
+      // index table: lane j reads token j's rows and weights (one round trip)
+      const int t = lane < n ? tok(lane) : -1;
+      if (lane < RP_TBL && t >= 0)
+        for (int k = 0; k < D.K; ++k) {
+          sts_i32(p.tbl + 4u * (uint32_t)(lane * 2 * D.K + k), INVM[(long long)t * D.K + k]);
+          sts_f32(p.tbl + 4u * (uint32_t)(lane * 2 * D.K + D.K + k), WGT[(long long)t * D.K + k]);
+        }
+      __syncwarp();
+    }
     bool ok = true;
     with_nc(D.d, [&](auto NCc) {
       constexpr int NC = decltype(NCc)::value;
       Row<NC> g, x, acc, y, r;
       row_ld(g, gp, n4);
       ok = rp_run(
-          p, mine * PER, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 2,
+          p, n, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 2,
           [&](int j, uint32_t st, uint32_t bar) {
             // header: t, then K weights
             const int t = tok(j);
@@ -456,8 +497,16 @@ __device__ __noinline__ void job_combine(const KArgs& a, int l, Sched& s, unsign
             mbar_expect_tx(bar, (uint32_t)(1 + D.K) * rowb);
             bulk_g2s(st + RP_HDR, XM + (long long)t * D.d, rowb, bar);
             for (int k = 0; k < D.K; ++k) {
-              const int pr = INVM[(long long)t * D.K + k];
-              sts_f32(st + 4u * (1 + k), WGT[(long long)t * D.K + k]);
+              int pr;
+              float w;
+              if (j < RP_TBL) {
+                pr = lds_i32(p.tbl + 4u * (uint32_t)(j * 2 * D.K + k));
+                w = lds_f32(p.tbl + 4u * (uint32_t)(j * 2 * D.K + D.K + k));
+              } else {
+                pr = INVM[(long long)t * D.K + k];
+                w = WGT[(long long)t * D.K + k];
+              }
+              sts_f32(st + 4u * (1 + k), w);
               bulk_g2s(st + RP_HDR + (1 + k) * rowb, Y + (long long)pr * D.d, rowb, bar);
             }
           },
@@ -744,7 +793,10 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char*
   const int nw = s.G * MT_WARPS;
   const int me = s.first() * MT_WARPS + (threadIdx.x >> 5);
   const uint32_t rowb = (uint32_t)D.d * 4u;
-  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, (uint32_t)(1 + D.K) * rowb);
+  // index table: per token of the warp (first RP_TBL), its K sorted rows,
+  // K weights and K experts (the layout of the stage header after t)
+  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, (uint32_t)(1 + D.K) * rowb,
+                            (uint32_t)(RP_TBL * 3 * D.K * 4));
   const bool piped = p.ns > 0 && D.K <= 8;
   if (piped) rp_begin(p);
   bool ok = true;
@@ -755,6 +807,15 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char*
       // staged: the dx row and the K expert-output rows of each token;
       // header: t, then K sorted rows, K weights, K experts
       const int n = me < D.T ? (D.T - 1 - me) / nw + 1 : 0;
+      if (lane < RP_TBL && lane < n) {
+        const int t = me + lane * nw;
+        for (int k = 0; k < D.K; ++k) {
+          sts_i32(p.tbl + 4u * (uint32_t)(lane * 3 * D.K + k), INVM[(long long)t * D.K + k]);
+          sts_f32(p.tbl + 4u * (uint32_t)(lane * 3 * D.K + D.K + k), WGT[(long long)t * D.K + k]);
+          sts_i32(p.tbl + 4u * (uint32_t)(lane * 3 * D.K + 2 * D.K + k), IDX[(long long)t * D.K + k]);
+        }
+      }
+      __syncwarp();
       ok = rp_run(
           p, n, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 3,
           [&](int j, uint32_t st, uint32_t bar) {
@@ -763,10 +824,21 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char*
             mbar_expect_tx(bar, (uint32_t)(1 + D.K) * rowb);
             bulk_g2s(st + RP_HDR, DX + (long long)t * D.d, rowb, bar);
             for (int k = 0; k < D.K; ++k) {
-              const int pr = INVM[(long long)t * D.K + k];
+              int pr, e;
+              float w;
+              if (j < RP_TBL) {
+                const uint32_t tr = p.tbl + 4u * (uint32_t)(j * 3 * D.K);
+                pr = lds_i32(tr + 4u * k);
+                w = lds_f32(tr + 4u * (D.K + k));
+                e = lds_i32(tr + 4u * (2 * D.K + k));
+              } else {
+                pr = INVM[(long long)t * D.K + k];
+                w = WGT[(long long)t * D.K + k];
+                e = IDX[(long long)t * D.K + k];
+              }
               sts_i32(st + 4u * (1 + k), pr);
-              sts_f32(st + 4u * (1 + D.K + k), WGT[(long long)t * D.K + k]);
-              sts_i32(st + 4u * (1 + 2 * D.K + k), IDX[(long long)t * D.K + k]);
+              sts_f32(st + 4u * (1 + D.K + k), w);
+              sts_i32(st + 4u * (1 + 2 * D.K + k), e);
               bulk_g2s(st + RP_HDR + (1 + k) * rowb, Y + (long long)pr * D.d, rowb, bar);
             }
           },
@@ -850,6 +922,7 @@ template <class OP>
 __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char* smem) {
   const MtDims& D = a.D;
   const int n4 = D.d / 4;
+  const int lane = threadIdx.x & 31;
   const float* DXS = abuf<float>(a, A_DXS);
   const float* DZ = abuf<float>(a, A_DZ);
   const int* INVM = abuf<int>(a, A_INVM) + (long long)l * D.T * D.K;
@@ -862,7 +935,10 @@ __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char*
   const int nw = s.G * MT_WARPS;
   const int me = s.first() * MT_WARPS + (threadIdx.x >> 5);
   const uint32_t rowb = (uint32_t)D.d * 4u;
-  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, (uint32_t)(D.K + 2) * rowb);
+  // index table: per token of the warp (first RP_TBL), 1/rms, then its K
+  // sorted rows, experts (ascending) and router-logit gradients
+  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, (uint32_t)(D.K + 2) * rowb,
+                            (uint32_t)(RP_TBL * (1 + 3 * D.K) * 4));
   const bool piped = p.ns > 0 && D.K <= 8;
   if (piped) rp_begin(p);
   bool ok = true;
@@ -876,27 +952,44 @@ __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char*
       // header: t, 1/rms, then the chosen experts in ascending order with
       // their router-logit gradients
       const int n = me < D.T ? (D.T - 1 - me) / nw + 1 : 0;
+      // index table row of token j: [1/rms, K sorted rows, K experts ascending,
+      // K router-logit gradients] - lane j fills row j (two round trips)
+      auto fill = [&](int j, uint32_t row) {
+        const int t = me + j * nw;
+        sts_f32(row, inv2[t]);
+        int ex[8];
+        for (int k = 0; k < D.K; ++k) {
+          sts_i32(row + 4u * (1 + k), INVM[(long long)t * D.K + k]);
+          int e = IDX[(long long)t * D.K + k], q = k;
+          while (q > 0 && ex[q - 1] > e) { ex[q] = ex[q - 1]; --q; }
+          ex[q] = e;
+        }
+        for (int k = 0; k < D.K; ++k) {
+          sts_i32(row + 4u * (1 + D.K + k), ex[k]);
+          sts_f32(row + 4u * (1 + 2 * D.K + k), DZ[(long long)t * D.E + ex[k]]);
+        }
+      };
+      const uint32_t tw = 4u * (uint32_t)(1 + 3 * D.K);   // table row bytes
+      if (lane < RP_TBL && lane < n) fill(lane, p.tbl + (uint32_t)lane * tw);
+      __syncwarp();
       ok = rp_run(
           p, n, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 4,
           [&](int j, uint32_t st, uint32_t bar) {
             const int t = me + j * nw;
+            // the header takes the table row; tokens past the table reuse row
+            // j % RP_TBL (its token was issued long before) and fill it here
+            const uint32_t row = p.tbl + (uint32_t)(j % RP_TBL) * tw;
+            if (j >= RP_TBL) fill(j, row);
             sts_i32(st, t);
-            sts_f32(st + 4u, inv2[t]);
+            sts_f32(st + 4u, lds_f32(row));
             mbar_expect_tx(bar, (uint32_t)(D.K + 2) * rowb);
             for (int k = 0; k < D.K; ++k)
-              bulk_g2s(st + RP_HDR + k * rowb, DXS + (long long)INVM[(long long)t * D.K + k] * D.d, rowb, bar);
+              bulk_g2s(st + RP_HDR + k * rowb, DXS + (long long)lds_i32(row + 4u * (1 + k)) * D.d, rowb, bar);
             bulk_g2s(st + RP_HDR + D.K * rowb, XM + (long long)t * D.d, rowb, bar);
             bulk_g2s(st + RP_HDR + (D.K + 1) * rowb, DX + (long long)t * D.d, rowb, bar);
-            // experts sorted ascending (insertion sort of K <= 8 values)
-            int ex[8];
             for (int k = 0; k < D.K; ++k) {
-              int e = IDX[(long long)t * D.K + k], q = k;
-              while (q > 0 && ex[q - 1] > e) { ex[q] = ex[q - 1]; --q; }
-              ex[q] = e;
-            }
-            for (int k = 0; k < D.K; ++k) {
-              sts_i32(st + 4u * (2 + k), ex[k]);
-              sts_f32(st + 4u * (2 + D.K + k), DZ[(long long)t * D.E + ex[k]]);
+              sts_i32(st + 4u * (2 + k), lds_i32(row + 4u * (1 + D.K + k)));
+              sts_f32(st + 4u * (2 + D.K + k), lds_f32(row + 4u * (1 + 2 * D.K + k)));
             }
           },
           [&](int j, uint32_t st) {
@@ -953,6 +1046,7 @@ __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char*
 template <class OP>
 __device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s, char* smem) {
   const MtDims& D = a.D;
+  const int lane = threadIdx.x & 31;
   const float* DR = abuf<float>(a, A_DR);
   const float* X = abuf<float>(a, A_X) + (long long)l * D.T * D.d;
   const float* inv = abuf<float>(a, A_INV1) + (long long)l * D.T;
@@ -960,7 +1054,7 @@ __device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s, 
   const int n4 = D.d / 4, nw = s.G * MT_WARPS;
   const int me = s.first() * MT_WARPS + (threadIdx.x >> 5);
   const uint32_t rowb = (uint32_t)D.d * 4u;
-  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, 3u * rowb);
+  const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, 3u * rowb, RP_TBL * 4u);
   if (p.ns > 0) rp_begin(p);
   bool ok = true;
   with_nc(D.d, [&](auto NCc) {
@@ -969,14 +1063,17 @@ __device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s, 
     row_ld(g, pmaster(a, P_ATTN_NORM) + (long long)l * D.d, n4);
     row_scale(gacc, g, 0.f);
     if (p.ns > 0) {
-      // staged: dr, x and dx rows of each token; header: t, 1/rms
+      // staged: dr, x and dx rows of each token; header: t, 1/rms (1/rms of
+      // the warp's first RP_TBL tokens read up front into the table)
       const int n = me < D.T ? (D.T - 1 - me) / nw + 1 : 0;
+      if (lane < RP_TBL && lane < n) sts_f32(p.tbl + 4u * lane, inv[me + lane * nw]);
+      __syncwarp();
       ok = rp_run(
           p, n, abuf<ArenaHdr>(a, A_HDR), a.timeout_ns / 2, SITE_ROWPIPE + 5,
           [&](int j, uint32_t st, uint32_t bar) {
             const int t = me + j * nw;
             sts_i32(st, t);
-            sts_f32(st + 4u, inv[t]);
+            sts_f32(st + 4u, j < RP_TBL ? lds_f32(p.tbl + 4u * j) : inv[t]);
             mbar_expect_tx(bar, 3u * rowb);
             bulk_g2s(st + RP_HDR, DR + (long long)t * D.d, rowb, bar);
             bulk_g2s(st + RP_HDR + rowb, X + (long long)t * D.d, rowb, bar);
@@ -1170,6 +1267,131 @@ static __device__ __noinline__ void job_colpart(const KArgs& a, const ColArgs& c
   else if (E <= 32) colpart_items<32, 2>(a, c, s, sm);
   else colpart_items<64, 1>(a, c, s, sm);
 }
+
+// Router-weight gradient partials dWr[e][c] = sum_t dz[t][e] r2[t][c] with
+// r2 = x_mid * (1/rms) * g in fp32.  CTA c takes the token chunk of the
+// routing jobs; its x_mid rows (and dz rows) are staged RG_TB tokens at a
+// time by cp.async.bulk into a ring of CTA-wide stages; warp w owns the
+// columns [w d/8, (w+1) d/8) and each lane keeps EM x 3 accumulators over
+// the chunk in token order, then stores PART[cta][e][col] (no cross-warp
+// reduction: the warps own disjoint columns).  Returns false when the ring
+// does not fit (the caller then takes the column pass).
+#define RG_TB 16
+template <int EM>
+__device__ __forceinline__ bool router_grad_cta(const KArgs& a, int l, char* smem) {
+  const MtDims& D = a.D;
+  const int c = blockIdx.x, G = gridDim.x;
+  const int ch = chunk_len(D, G);
+  const int t0 = c * ch, t1 = min(D.T, t0 + ch);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rowb = (uint32_t)D.d * 4u, dzb = (uint32_t)D.E * 4u;
+  const uint32_t stage_bytes = ((uint32_t)RG_TB * (rowb + dzb) + 127u) & ~127u;
+  int ns = (int)(((uint32_t)a.smem_bytes - RP_WIN_OFF) / stage_bytes);
+  if (ns > 3) ns = 3;
+  if (ns < 2 || (dzb & 15u)) return false;
+  const float* XM = abuf<float>(a, A_XM) + (long long)l * D.T * D.d;
+  const float* inv2 = abuf<float>(a, A_INV2) + (long long)l * D.T;
+  const float* DZ = abuf<float>(a, A_DZ);
+  const float* g = pmaster(a, P_MOE_NORM) + (long long)l * D.d;
+  constexpr int NCOL = 3;                       // columns per lane (d <= 768)
+  const int cpw = D.d / MT_WARPS;
+  int col[NCOL];
+  float gc[NCOL];
+#pragma unroll
+  for (int i = 0; i < NCOL; ++i) {
+    col[i] = warp * cpw + lane + 32 * i;
+    gc[i] = (lane + 32 * i < cpw) ? g[col[i]] : 0.f;
+  }
+  float acc[EM][NCOL];
+#pragma unroll
+  for (int e = 0; e < EM; ++e)
+#pragma unroll
+    for (int i = 0; i < NCOL; ++i) acc[e][i] = 0.f;
+  const uint32_t ring = smem_u32(smem) + RP_WIN_OFF, bar0 = smem_u32(&rp_bars[0]);
+  ArenaHdr* hdr = abuf<ArenaHdr>(a, A_HDR);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < ns; ++i) mbar_init(bar0 + 8u * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async;" ::: "memory");
+  }
+  __syncthreads();
+  const int nb = t1 > t0 ? (t1 - t0 + RG_TB - 1) / RG_TB : 0;
+  auto issue = [&](int b) {      // thread 0
+    const int tb = t0 + b * RG_TB, nt = min(RG_TB, t1 - tb);
+    const uint32_t st = ring + (uint32_t)(b % ns) * stage_bytes, bar = bar0 + 8u * (uint32_t)(b % ns);
+    mbar_expect_tx(bar, (uint32_t)nt * (rowb + dzb));
+    bulk_g2s(st + (uint32_t)RG_TB * rowb, DZ + (long long)tb * D.E, (uint32_t)nt * dzb, bar);
+    for (int r = 0; r < nt; ++r) bulk_g2s(st + (uint32_t)r * rowb, XM + (long long)(tb + r) * D.d, rowb, bar);
+  };
+  if (threadIdx.x == 0)
+    for (int b = 0; b < nb && b < ns; ++b) issue(b);
+  bool ok = true;
+  for (int b = 0; b < nb; ++b) {
+    const int tb = t0 + b * RG_TB, nt = min(RG_TB, t1 - tb);
+    const float ivl = lane < nt ? inv2[tb + lane] : 0.f;     // 1/rms of the batch, lane r holds token r
+    if (ok && !mbar_wait(bar0 + 8u * (uint32_t)(b % ns), (uint32_t)(b / ns) & 1u, a.timeout_ns)) {
+      set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_ROWPIPE + 8);
+      ok = false;
+    }
+    if (ok) {
+      const uint32_t st = ring + (uint32_t)(b % ns) * stage_bytes;
+      const uint32_t dzs = st + (uint32_t)RG_TB * rowb;
+      for (int r = 0; r < nt; ++r) {
+        const float iv = __shfl_sync(0xffffffffu, ivl, r);
+        float rr[NCOL];
+#pragma unroll
+        for (int i = 0; i < NCOL; ++i)
+          rr[i] = (lane + 32 * i < cpw) ? lds_f32(st + (uint32_t)r * rowb + 4u * (uint32_t)col[i]) * iv * gc[i] : 0.f;
+#pragma unroll
+        for (int e4 = 0; e4 < EM; e4 += 4) {
+          if (e4 < D.E) {
+            const float4 z = lds4(dzs + (uint32_t)(r * D.E + e4) * 4u);
+            const float zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int i = 0; i < NCOL; ++i) acc[e4 + q][i] = fmaf(zz[q], rr[i], acc[e4 + q][i]);
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (ok && threadIdx.x == 0 && b + ns < nb) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the reads of this stage come first
+      issue(b + ns);
+    }
+  }
+  if (threadIdx.x == 0 && ok)
+    for (int i = 0; i < ns; ++i) asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar0 + 8u * i) : "memory");
+  float* out = abuf<float>(a, A_PART) + (long long)c * (D.E + 2) * D.d;
+#pragma unroll
+  for (int e = 0; e < EM; ++e)
+    if (e < D.E)
+#pragma unroll
+      for (int i = 0; i < NCOL; ++i)
+        if (lane + 32 * i < cpw) out[(long long)e * D.d + col[i]] = acc[e][i];
+  __syncthreads();
+  return true;
+}
+// Router-weight gradient partials of layer l: per-CTA rows (PART[cta][0..E))
+// when the staged form fits, else the column pass (PART[chunk][0..E)).
+// Returns the number of partial chunks for job_colfinal.
+static __device__ __noinline__ int job_router_grad(const KArgs& a, int l, Sched& s, char* smem) {
+  const MtDims& D = a.D;
+  bool done = false;
+  if (D.E % 4 == 0 && D.d % (8 * MT_WARPS) == 0 && D.d <= 768) {
+    if (D.E <= 16) done = router_grad_cta<16>(a, l, smem);
+    else if (D.E <= 32) done = router_grad_cta<32>(a, l, smem);
+  }
+  if (done) return (int)gridDim.x;
+  ColArgs c{COL_MOE, nullptr, abuf<float>(a, A_XM) + (long long)l * D.T * D.d,
+            abuf<float>(a, A_INV2) + (long long)l * D.T, pmaster(a, P_MOE_NORM) + (long long)l * D.d,
+            abuf<float>(a, A_DZ), 0};
+  job_colpart(a, c, s, smem);
+  return 0;
+}
+
 
 // out[r][col] (+)= sum over chunks of PART[chunk][row0 + r][col]; E_kind is
 // the router-row count of the reduction that wrote those rows (0: gain only).
@@ -1816,18 +2038,13 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     MT_SYNC();
     job_moe_bwd2<OP>(a, l, s, smem); TJ(23);
     MT_SYNC();
-    {
-      // router-weight gradient partials (rows 0..E-1); the expert-norm gain
-      // partial was left by job_moe_bwd2
-      ColArgs c{COL_MOE, nullptr, abuf<float>(a, A_XM) + (long long)l * D.T * D.d,
-                abuf<float>(a, A_INV2) + (long long)l * D.T, pmaster(a, P_MOE_NORM) + (long long)l * D.d,
-                abuf<float>(a, A_DZ), 0};
-      job_colpart(a, c, s, smem); TJ(16);
-    }
+    // router-weight gradient partials (rows 0..E-1); the expert-norm gain
+    // partial was left by job_moe_bwd2
+    const int rg_chunks = job_router_grad(a, l, s, smem); TJ(16);
     run_gemm<OP>(a, gm.wo_dgrad(l), s, smem, tc); TJ(24);
     run_gemm<OP>(a, gm.wo_wgrad(l), s, smem, tc); TJ(25);
     MT_SYNC();
-    job_colfinal(a, 0, D.E, D.E, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d, nullptr, 0, s);
+    job_colfinal(a, 0, D.E, D.E, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d, nullptr, 0, s, rg_chunks);
     job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_MOE_NORM) + (long long)l * D.d, nullptr, 0, s, (int)G); TJ(18);
     job_ksplit_sum(a, pgrad(a, P_WO) + (long long)l * D.d * D.hq, D.d, D.hq, s); TJ(32);
     run_attn_bwd<OP>(a, l, s, smem, tc, attn_deps(l, TK_ATTN_BWD, false)); TJ(26);

@@ -20,6 +20,7 @@
 #define RP_MAX_STAGES 8
 #define RP_WIN_OFF 1024          // rings start here (the low kilobyte is left to the product jobs)
 #define RP_HDR 128               // stage header bytes
+#define RP_TBL 32                // tokens of a warp whose indices are read up front
 #define SITE_ROWPIPE 40           // + job: 0 router, 1 route, 2 combine, 3/4 combine bwd 1/2, 5 attention-norm bwd
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -95,6 +96,7 @@ __device__ __forceinline__ void row_add_lds(Row<NC>& r, uint32_t a, int n4) {
 struct RowPipe {
   uint32_t ring;     // shared address of this warp's stage 0
   uint32_t bar;      // shared address of this warp's first mbarrier
+  uint32_t tbl;      // shared address of this warp's index table (after its stages)
   uint32_t sbytes;   // bytes per stage
   int ns;            // stages; 0 when two stages do not fit (callers then take their register path)
   __device__ __forceinline__ uint32_t stage(int j) const { return ring + (uint32_t)(j % ns) * sbytes; }
@@ -103,17 +105,20 @@ struct RowPipe {
 };
 
 // Carve this warp's ring out of the shared-memory window [win_off, win_end)
-// for stages of `rows_bytes` bytes of rows.  Grid-uniform: every warp gets
-// the same number of stages.
-__device__ __forceinline__ RowPipe rp_make(char* smem, uint32_t win_off, uint32_t win_end, uint32_t rows_bytes) {
+// for stages of `rows_bytes` bytes of rows, plus `tbl_bytes` of index table
+// after the stages.  Grid-uniform: every warp gets the same number of stages.
+__device__ __forceinline__ RowPipe rp_make(char* smem, uint32_t win_off, uint32_t win_end, uint32_t rows_bytes,
+                                          uint32_t tbl_bytes = 0) {
   RowPipe p;
   const int warp = threadIdx.x >> 5;
   const uint32_t per = win_end > win_off ? ((win_end - win_off) / MT_WARPS) & ~127u : 0u;
   p.sbytes = (RP_HDR + rows_bytes + 127u) & ~127u;
-  int ns = (int)(per / p.sbytes);
+  const uint32_t tb = (tbl_bytes + 127u) & ~127u;
+  int ns = per > tb ? (int)((per - tb) / p.sbytes) : 0;
   if (ns > RP_MAX_STAGES) ns = RP_MAX_STAGES;
   p.ns = ns >= 2 ? ns : 0;
   p.ring = smem_u32(smem) + win_off + (uint32_t)warp * per;
+  p.tbl = p.ring + (uint32_t)p.ns * p.sbytes;
   p.bar = smem_u32(&rp_bars[warp * RP_MAX_STAGES]);
   return p;
 }
