@@ -22,6 +22,7 @@
 #pragma once
 #include "common.cuh"
 #include "gemm_tc.cuh"
+#include <type_traits>
 
 struct AttnDeps;   // defined with the attention jobs
 
@@ -353,7 +354,7 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
       for (int g = 0; g < HD / 8; ++g)
         dst[g] = make_uint4(pack2(o[8 * g] * inv, o[8 * g + 1] * inv), pack2(o[8 * g + 2] * inv, o[8 * g + 3] * inv),
                             pack2(o[8 * g + 4] * inv, o[8 * g + 5] * inv), pack2(o[8 * g + 6] * inv, o[8 * g + 7] * inv));
-      j.lse[((long long)b * j.H + h) * j.S + qb * BQ + r] = (m + log2f(lsum)) / LOG2E;
+      j.lse[((long long)b * j.H + h) * j.S + qb * BQ + r] = m + log2f(lsum);   // log2 units
       if (j.sig) {
         // every row of the block is stored: publish it
         asm volatile("bar.sync 2, 128;" ::: "memory");
@@ -386,7 +387,7 @@ struct BwdJob {
   const CUtensorMap* map_qkv;  // q,k,v of all layers
   const CUtensorMap* map_do;   // dO [T][hq]
   int y0;                      // row of token 0 of this layer in map_qkv
-  const float* lse;            // [B*H][S] (natural log)
+  const float* lse;            // [B*H][S] log2 of the row sum of exp2(scale log2(e) s) (this path's forward)
   const float* dsum;           // [B*H][S]
   __nv_bfloat16* dqkv;         // [T][3hq]
   const float* rope;           // [S][32][2] cos, sin
@@ -601,28 +602,37 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
         const int lim = r - i * 64;            // x < lim is masked
         wait(B_(kv::PDEMPTY + sb), ((c >> 1) & 1) ^ 1, SITE_TC_EMPTY);
         const uint32_t pb = sbase + kv::P_OFF + sb * TILE, db = sbase + kv::DS_OFF + sb * TILE;
+        // P^T and dS^T of the step; the mask only touches the first two steps,
+        // the others run without the compare and select
+        auto soft = [&](auto MASKc) {
+          constexpr bool MASK = decltype(MASKc)::value;
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          uint32_t wp[4], wd[4];
-          const float4 la = reinterpret_cast<const float4*>(sl)[2 * g], lb = reinterpret_cast<const float4*>(sl)[2 * g + 1];
-          const float4 da = reinterpret_cast<const float4*>(sd)[2 * g], dbv = reinterpret_cast<const float4*>(sd)[2 * g + 1];
-          const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
-          const float dv[8] = {da.x, da.y, da.z, da.w, dbv.x, dbv.y, dbv.z, dbv.w};
+          for (int g = 0; g < 8; ++g) {
+            uint32_t wp[4], wd[4];
+            const float4 la = reinterpret_cast<const float4*>(sl)[2 * g], lb = reinterpret_cast<const float4*>(sl)[2 * g + 1];
+            const float4 da = reinterpret_cast<const float4*>(sd)[2 * g], dbv = reinterpret_cast<const float4*>(sd)[2 * g + 1];
+            const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+            const float dv[8] = {da.x, da.y, da.z, da.w, dbv.x, dbv.y, dbv.z, dbv.w};
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int x = g * 8 + e;
-            float p0 = ex2(fmaf(__uint_as_float(sv[x]), sc_l2, -lv[e] * LOG2E));
-            float p1 = ex2(fmaf(__uint_as_float(sv[x + 1]), sc_l2, -lv[e + 1] * LOG2E));
-            if (x < lim) p0 = 0.f;
-            if (x + 1 < lim) p1 = 0.f;
-            const float d0 = p0 * (__uint_as_float(dp[x]) - dv[e]);
-            const float d1 = p1 * (__uint_as_float(dp[x + 1]) - dv[e + 1]);
-            wp[e >> 1] = pack2(p0, p1);
-            wd[e >> 1] = pack2(d0, d1);
+            for (int e = 0; e < 8; e += 2) {
+              const int x = g * 8 + e;
+              float p0 = ex2(fmaf(__uint_as_float(sv[x]), sc_l2, -lv[e]));
+              float p1 = ex2(fmaf(__uint_as_float(sv[x + 1]), sc_l2, -lv[e + 1]));
+              if (MASK) {
+                if (x < lim) p0 = 0.f;
+                if (x + 1 < lim) p1 = 0.f;
+              }
+              const float d0 = p0 * (__uint_as_float(dp[x]) - dv[e]);
+              const float d1 = p1 * (__uint_as_float(dp[x + 1]) - dv[e + 1]);
+              wp[e >> 1] = pack2(p0, p1);
+              wd[e >> 1] = pack2(d0, d1);
+            }
+            st_shared_v4(pb + p_chunk_off(r, g * 8), wp[0], wp[1], wp[2], wp[3]);
+            st_shared_v4(db + p_chunk_off(r, g * 8), wd[0], wd[1], wd[2], wd[3]);
           }
-          st_shared_v4(pb + p_chunk_off(r, g * 8), wp[0], wp[1], wp[2], wp[3]);
-          st_shared_v4(db + p_chunk_off(r, g * 8), wd[0], wd[1], wd[2], wd[3]);
-        }
+        };
+        if (i < 2) soft(std::true_type());
+        else soft(std::false_type());
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(B_(kv::PDFULL + sb));
@@ -791,7 +801,7 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
       const int nst = 2 * (qb + 1);
       const int query = qb * 128 + r;
       const long long lrow = ((long long)b * j.H + h) * j.S + query;
-      const float lse2 = j.lse[lrow] * LOG2E, dd = j.dsum[lrow];
+      const float lse2 = j.lse[lrow], dd = j.dsum[lrow];
       for (int i = 0; i < nst; ++i, ++c) {
         const uint32_t sb = c & 1;
         wait(B_(qd::SDFULL + sb), (c >> 1) & 1, SITE_TC_ACC_FULL);
@@ -810,20 +820,28 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
         const int lim = query - i * 64;        // x > lim is masked
         wait(B_(qd::DSEMPTY + sb), ((c >> 1) & 1) ^ 1, SITE_TC_EMPTY);
         const uint32_t db = sbase + qd::DS_OFF + sb * TILE;
+        // dS of the step; the mask only touches the last two steps
+        auto soft = [&](auto MASKc) {
+          constexpr bool MASK = decltype(MASKc)::value;
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          uint32_t wd[4];
+          for (int g = 0; g < 8; ++g) {
+            uint32_t wd[4];
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int x = g * 8 + e;
-            float p0 = ex2(fmaf(__uint_as_float(sv[x]), sc_l2, -lse2));
-            float p1 = ex2(fmaf(__uint_as_float(sv[x + 1]), sc_l2, -lse2));
-            if (x > lim) p0 = 0.f;
-            if (x + 1 > lim) p1 = 0.f;
-            wd[e >> 1] = pack2(p0 * (__uint_as_float(dp[x]) - dd), p1 * (__uint_as_float(dp[x + 1]) - dd));
+            for (int e = 0; e < 8; e += 2) {
+              const int x = g * 8 + e;
+              float p0 = ex2(fmaf(__uint_as_float(sv[x]), sc_l2, -lse2));
+              float p1 = ex2(fmaf(__uint_as_float(sv[x + 1]), sc_l2, -lse2));
+              if (MASK) {
+                if (x > lim) p0 = 0.f;
+                if (x + 1 > lim) p1 = 0.f;
+              }
+              wd[e >> 1] = pack2(p0 * (__uint_as_float(dp[x]) - dd), p1 * (__uint_as_float(dp[x + 1]) - dd));
+            }
+            st_shared_v4(db + p_chunk_off(r, g * 8), wd[0], wd[1], wd[2], wd[3]);
           }
-          st_shared_v4(db + p_chunk_off(r, g * 8), wd[0], wd[1], wd[2], wd[3]);
-        }
+        };
+        if (i >= nst - 2) soft(std::true_type());
+        else soft(std::false_type());
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(B_(qd::DSFULL + sb));
