@@ -590,7 +590,7 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
   *reinterpret_cast<uint2*>(p) = u;
 }
 template <class OP>
-__device__ __noinline__ void job_ce(const KArgs& a, Sched& s) {
+__device__ __noinline__ void job_ce(const KArgs& a, Sched& s, char* smem) {
   const MtDims& D = a.D;
   const int lane = threadIdx.x & 31;
   OP* DL = abuf<OP>(a, A_DLOGITS);
@@ -600,6 +600,114 @@ __device__ __noinline__ void job_ce(const KArgs& a, Sched& s) {
   const int np = ce_parts<OP>(a);
   const int nw = s.G * MT_WARPS;
   const int v4 = D.V / 4;                 // V % 8 == 0 (checked on the host)
+  if constexpr (sizeof(OP) == 2) {
+    // bf16 logits: each warp streams its rows in chunks of CK logits through
+    // a ring of shared-memory stages - bulk load, dlogits computed in place,
+    // bulk store back over the logits; the next row's column-tile partials
+    // are fetched into registers while the current row streams
+    constexpr int CK = 4096;
+    constexpr int PQ = 8;                 // partials per lane (np <= 256)
+    const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, CK * 2u);
+    if (p.ns > 0 && np <= 32 * PQ) {
+      const int nck = (D.V + CK - 1) / CK;
+      const int r0 = s.first() * MT_WARPS + (threadIdx.x >> 5);
+      const int nrow = r0 < D.T ? (D.T - 1 - r0) / nw + 1 : 0;
+      const int n = nrow * nck;
+      auto row_of = [&](int j) { return r0 + (j / nck) * nw; };
+      auto gptr = [&](int j) { return DL + (long long)row_of(j) * D.V + (long long)(j % nck) * CK; };
+      auto nbytes = [&](int j) { return (uint32_t)min(CK, D.V - (j % nck) * CK) * 2u; };
+      auto load = [&](int j) {              // lane 0
+        mbar_expect_tx(p.sbar(j), nbytes(j));
+        bulk_g2s(p.stage(j), gptr(j), nbytes(j), p.sbar(j));
+      };
+      float pm[PQ], ps[PQ];
+      auto fetch_parts = [&](int t) {
+#pragma unroll
+        for (int q = 0; q < PQ; ++q) {
+          const int i = lane + 32 * q;
+          pm[q] = (i < np) ? PART[((long long)t * np + i) * 2] : -INFINITY;
+          ps[q] = (i < np) ? PART[((long long)t * np + i) * 2 + 1] : 0.f;
+        }
+      };
+      rp_begin(p);
+      if (lane == 0)
+        for (int j = 0; j < n && j < p.ns; ++j) load(j);
+      __syncwarp();
+      if (nrow > 0) fetch_parts(r0);
+      bool ok = true;
+      float lse = 0.f;
+      int target = -1;
+      bool has = false;
+      for (int j = 0; j < n; ++j) {
+        const int k = j % nck, t = row_of(j);
+        if (k == 0) {
+          // log-sum-exp of row t from its partials (the same order as the
+          // register path), then the next row's partials
+          has = (t % D.S) != D.S - 1;
+          target = has ? a.tokens[t + 1] : -1;
+          if (has && (target < 0 || target >= D.V)) target = 0;
+          float m = -INFINITY, sum = 0.f;
+#pragma unroll
+          for (int q = 0; q < PQ; ++q) {
+            const float nm = fmaxf(m, pm[q]);
+            sum = (m == -INFINITY ? 0.f : sum * expf(m - nm)) + (pm[q] == -INFINITY ? 0.f : ps[q] * expf(pm[q] - nm));
+            m = nm;
+          }
+          const float M = warp_max(m);
+          sum = (m == -INFINITY) ? 0.f : sum * expf(m - M);
+          sum = warp_sum(sum);
+          lse = M + logf(sum);
+          if (j + nck < n) fetch_parts(row_of(j + nck));
+          if (lane == 0) TL[t] = has ? a.coef * (lse - TGT[t]) : 0.f;
+        }
+        if (ok && !mbar_wait(p.sbar(j), p.parity(j), a.timeout_ns)) {
+          set_error(abuf<ArenaHdr>(a, A_HDR), MT_ERR_DEVICE_TIMEOUT, SITE_ROWPIPE + 10);
+          ok = false;
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          const uint32_t st = p.stage(j);
+          const int nu = (int)(nbytes(j) / 16u), c0 = k * CK;
+          for (int u = lane; u < nu; u += 32) {
+            uint4 q;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w) : "r"(st + 16u * u));
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[h]));
+              float p0 = has ? a.coef * __expf(x.x - lse) : 0.f, p1 = has ? a.coef * __expf(x.y - lse) : 0.f;
+              const int col = c0 + 8 * u + 2 * h;
+              if (target == col) p0 -= a.coef;
+              if (target == col + 1) p1 -= a.coef;
+              __nv_bfloat162 r = __floats2bfloat162_rn(p0, p1);
+              o[h] = *reinterpret_cast<uint32_t*>(&r);
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(st + 16u * u), "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]) : "memory");
+          }
+          // the dlogits of the stage are read by the bulk store (async proxy)
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0 && ok) {
+          bulk_s2g(gptr(j), p.stage(j), nbytes(j));
+          bulk_commit();
+          if (j + p.ns < n) {
+            bulk_wait_read0();
+            load(j + p.ns);
+          }
+        }
+        __syncwarp();
+      }
+      if (lane == 0) {
+        bulk_wait_all0();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      rp_end(p, ok);
+      s.next(s.G);
+      return;
+    }
+  }
   constexpr int U = sizeof(OP) == 2 ? 16 : 8;   // 16-byte loads in flight per lane
   for (int t = s.first() * MT_WARPS + (threadIdx.x >> 5); t < D.T; t += nw) {
     OP* row = DL + (long long)t * D.V;
@@ -1545,7 +1653,7 @@ __device__ __forceinline__ void adamw_elem(const KArgs& a, float c, float& p, fl
 // Clip coefficient from the ordered sum of the partials, then the AdamW sweep
 // over CTA c's slice (float4 loads; writes p, m, v and the bf16 shadow).
 template <class OP>
-__device__ __noinline__ void job_adamw(const KArgs& a) {
+__device__ __noinline__ void job_adamw(const KArgs& a, char* smem) {
   const int c = blockIdx.x, G = gridDim.x;
   const double* parts = reinterpret_cast<const double*>(abuf<float>(a, A_NORMPART));
   double tot = 0.0;
@@ -1581,21 +1689,123 @@ __device__ __noinline__ void job_adamw(const KArgs& a) {
       reinterpret_cast<uint2*>(sh)[j] = u;
     }
   };
-  // The sweep is elementwise, so any split gives the same result: chunks of
-  // AW_CHUNK float4 groups are drawn from a ticket counter (zeroed at the
-  // start of the launch), so that SMs that stream faster take more chunks;
-  // the next ticket is drawn while the current chunk is processed.
-  constexpr long long AW_CHUNK = 4096;
-  constexpr int UA = 4;                 // float4 groups per thread in flight (16 loads)
-  const long long nchunk = (n4 + AW_CHUNK - 1) / AW_CHUNK;
+  // The sweep is elementwise, so any split gives the same result.  Chunks
+  // of AW_T float4 groups are drawn from a ticket counter (zeroed at the
+  // start of the launch; the next ticket is drawn one chunk ahead), so that
+  // SMs that stream faster take more chunks.  Each chunk streams through
+  // AW_NS shared-memory stages of AW_G groups: thread 0 copies a stage's p,
+  // m, v and g in with cp.async.bulk, every thread updates the stage in place
+  // (and writes the bf16 shadow next to it), and thread 0 stores p, m, v and
+  // the shadow back with bulk stores.  After the stores of iteration i are
+  // issued, the stage of iteration i-1 (whose stores have had a whole
+  // iteration to read it out) is refilled.  Groups past the last whole chunk
+  // take the register path on the last CTA.
+  constexpr int AW_G = 512, AW_NS = 4, AW_T = 4096;
+  const uint32_t SEG = (uint32_t)AW_G * 16u;
+  const uint32_t STB = 4u * SEG + (uint32_t)AW_G * 8u;   // p | m | v | g | shadow
+  const bool bulk = RP_WIN_OFF + (uint32_t)AW_NS * STB <= (uint32_t)a.smem_bytes;
+  const long long nfull = bulk ? n4 / AW_T : 0;          // whole chunks
   unsigned* ticket = abuf<unsigned>(a, A_DEP) + ticket_offset(a.D, a.D.L, TK_ADAMW);
-  __shared__ int s_next;
-  long long cur = draw_ticket(ticket);
-  while (cur < nchunk) {
-    if (threadIdx.x == 0) s_next = (int)atomicAdd(ticket, 1u);
-    const long long b1 = min(n4, (cur + 1) * AW_CHUNK);
-    long long i = cur * AW_CHUNK + threadIdx.x;
-    for (; i + (UA - 1) * MT_THREADS < b1; i += UA * MT_THREADS) {
+  if (bulk) {
+    const uint32_t ring = smem_u32(smem) + RP_WIN_OFF;
+    const uint32_t bar0 = smem_u32(&rp_bars[0]);
+    long long* s_g0 = reinterpret_cast<long long*>(smem + 64);   // first group of each stage (-1: none)
+    ArenaHdr* hdr = abuf<ArenaHdr>(a, A_HDR);
+    // thread 0's stream position: current chunk, next sub-chunk, prefetched ticket
+    long long cur = 0, nxt = 0;
+    int sub = AW_T / AW_G;
+    __syncthreads();
+    auto refill = [&](int st) {        // thread 0: the next sub-chunk into stage st
+      if (sub == AW_T / AW_G) {
+        cur = nxt;
+        if (cur < nfull) nxt = (long long)atomicAdd(ticket, 1u);
+        sub = 0;
+      }
+      if (cur >= nfull) { s_g0[st] = -1; return; }
+      const long long g0 = cur * AW_T + (long long)(sub++) * AW_G;
+      s_g0[st] = g0;
+      const uint32_t dst = ring + (uint32_t)st * STB, bar = bar0 + 8u * (uint32_t)st;
+      mbar_expect_tx(bar, 4u * SEG);
+      bulk_g2s(dst, p4 + g0, SEG, bar);
+      bulk_g2s(dst + SEG, m4 + g0, SEG, bar);
+      bulk_g2s(dst + 2u * SEG, v4 + g0, SEG, bar);
+      bulk_g2s(dst + 3u * SEG, g4 + g0, SEG, bar);
+    };
+    if (threadIdx.x == 0) {
+      for (int st = 0; st < AW_NS; ++st) mbar_init(bar0 + 8u * st, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      asm volatile("fence.proxy.async;" ::: "memory");
+      nxt = (long long)atomicAdd(ticket, 1u);
+      for (int st = 0; st < AW_NS; ++st) refill(st);
+    }
+    __syncthreads();
+    bool ok = true;
+    for (int it = 0;; ++it) {
+      const int st = it % AW_NS;
+      const long long g0 = s_g0[st];
+      if (g0 < 0) break;
+      if (ok && !mbar_wait(bar0 + 8u * (uint32_t)st, (uint32_t)(it / AW_NS) & 1u, a.timeout_ns)) {
+        set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_ROWPIPE + 9);
+        ok = false;
+      }
+      const uint32_t base = ring + (uint32_t)st * STB;
+      if (ok) {
+        for (int k = threadIdx.x; k < AW_G; k += MT_THREADS) {
+          const uint32_t o = 16u * (uint32_t)k;
+          float4 pp = lds4(base + o), mm = lds4(base + SEG + o), vv = lds4(base + 2u * SEG + o);
+          const float4 gg = lds4(base + 3u * SEG + o);
+          adamw_elem<OP>(a, coef, pp.x, gg.x, mm.x, vv.x);
+          adamw_elem<OP>(a, coef, pp.y, gg.y, mm.y, vv.y);
+          adamw_elem<OP>(a, coef, pp.z, gg.z, mm.z, vv.z);
+          adamw_elem<OP>(a, coef, pp.w, gg.w, mm.w, vv.w);
+          sts4(base + o, pp);
+          sts4(base + SEG + o, mm);
+          sts4(base + 2u * SEG + o, vv);
+          if (sh) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(pp.x, pp.y), hi = __floats2bfloat162_rn(pp.z, pp.w);
+            sts_u2(base + 4u * SEG + 8u * (uint32_t)k, *reinterpret_cast<uint32_t*>(&lo),
+                   *reinterpret_cast<uint32_t*>(&hi));
+          }
+        }
+      }
+      // the stage's new values are read by the bulk stores (async proxy)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        if (ok) {
+          bulk_s2g(p4 + g0, base, SEG);
+          bulk_s2g(m4 + g0, base + SEG, SEG);
+          bulk_s2g(v4 + g0, base + 2u * SEG, SEG);
+          if (sh) bulk_s2g(reinterpret_cast<uint2*>(sh) + g0, base + 4u * SEG, (uint32_t)AW_G * 8u);
+          bulk_commit();
+        }
+        if (it > 0) {
+          // the previous iteration's stores have read their stage: refill it
+          bulk_wait_read1();
+          const int pst = (it - 1) % AW_NS;
+          if (ok) refill(pst);
+          else s_g0[pst] = -1;
+        }
+        if (!ok) s_g0[st] = -1;
+      }
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      bulk_wait_all0();
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      if (ok)
+        for (int st = 0; st < AW_NS; ++st)
+          asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar0 + 8u * st) : "memory");
+    }
+    __syncthreads();
+  }
+  // groups past the last whole chunk (all groups when the stages do not fit)
+  constexpr int UA = 4;                 // float4 groups per thread in flight (16 loads)
+  const long long rest0 = nfull * AW_T;
+  if (!bulk || c == G - 1) {
+    const long long r0 = bulk ? rest0 : (n4 * c / G), r1 = bulk ? n4 : (n4 * (c + 1) / G);
+    long long i = r0 + threadIdx.x;
+    for (; i + (UA - 1) * MT_THREADS < r1; i += UA * MT_THREADS) {
       float4 pp[UA], mm[UA], vv[UA], gg[UA];
 #pragma unroll
       for (int u = 0; u < UA; ++u) {
@@ -1605,10 +1815,7 @@ __device__ __noinline__ void job_adamw(const KArgs& a) {
 #pragma unroll
       for (int u = 0; u < UA; ++u) step4(i + u * MT_THREADS, pp[u], gg[u], mm[u], vv[u]);
     }
-    for (; i < b1; i += MT_THREADS) step4(i, p4[i], g4[i], m4[i], v4[i]);
-    __syncthreads();
-    cur = s_next;
-    __syncthreads();
+    for (; i < r1; i += MT_THREADS) step4(i, p4[i], g4[i], m4[i], v4[i]);
   }
   if (c == G - 1) {
     for (long long i = n4 * 4 + threadIdx.x; i < n; i += MT_THREADS) {
@@ -2012,7 +2219,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     run_gemm<OP>(a, g, s, smem, tc); TJ(10);
   }
   MT_SYNC();
-  job_ce<OP>(a, s); TJ(11);
+  job_ce<OP>(a, s, smem); TJ(11);
   MT_SYNC();
 
   // ---------------- backward ----------------
@@ -2065,7 +2272,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     MT_SYNC();
     job_norm_partial(a, (double*)smem); TJ(31);
     MT_SYNC();
-    job_adamw<OP>(a); TJ(34);
+    job_adamw<OP>(a, smem); TJ(34);
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     hdr->micro_index = a.micro_index;
