@@ -22,6 +22,7 @@ enum ErrSite {
   SITE_TC_DRAIN = 14,
   SITE_TC_ALIGN = 15,
   SITE_DEP = 16,
+  SITE_TC_EPI = 17,
   SITE_TEST_STALL = 20
 };
 

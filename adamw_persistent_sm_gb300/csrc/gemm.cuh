@@ -73,6 +73,11 @@ struct GemmDesc {
   const unsigned* dwait; unsigned dtarget;    // A rows: wait before loading a tile's operands
   const unsigned* dwait_aux; unsigned dtarget_aux;  // aux rows: wait before the epilogue reads aux
   unsigned* dsig;                             // output rows: +1 per stored tile
+  // Epilogue tensor maps (tensor-core path; -1: plain stores / loads):
+  // out and out2 by bulk tensor stores, aux by bulk tensor loads.  Row m of
+  // the product is row y0 + m of the map.
+  int omap, omap2, amap;
+  int oy0, oy02, ay0;
 };
 
 // Target column of logits row m (next token), or -1 for the last position.

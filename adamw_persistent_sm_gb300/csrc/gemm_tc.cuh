@@ -24,9 +24,14 @@
 #define TC_BOX_BYTES (64 * 64 * 2)
 #define TC_STAGE_BYTES ((TC_BM + TC_BN) / 64 * TC_BOX_BYTES)
 #define TC_RING_OFF 1024
-#define TC_STAGE_OFF (TC_RING_OFF + TC_STAGES * TC_STAGE_BYTES)   // epilogue transpose tiles
-#define TC_XPOSE_BYTES (32 * 33 * 4)                              // one 32x32 fp32 tile per warp
-#define MT_TC_SMEM (TC_STAGE_OFF + 4 * TC_XPOSE_BYTES)
+#define TC_STAGE_OFF (TC_RING_OFF + TC_STAGES * TC_STAGE_BYTES)   // epilogue windows
+#define TC_EPI_WARP_BYTES 8192                                    // one window per epilogue warp
+#define TC_EPI_SLOT 2048                                          // one 32x32 bf16 box
+#define TC_EPI_MBAR 512                                           // aux-load mbarriers (2 per warp)
+#define TC_XPOSE_BYTES (32 * 33 * 4)                              // 32x32 fp32 transpose tile
+#define MT_TC_SMEM (TC_STAGE_OFF + 4 * TC_EPI_WARP_BYTES)
+static_assert(TC_XPOSE_BYTES <= TC_EPI_WARP_BYTES, "transpose tile exceeds the epilogue window");
+static_assert(MT_TC_SMEM <= 232448, "tensor-core shared memory exceeds 227 KB");
 #define TC_TMEM_COLS 512
 #define MT_TC_AVAILABLE 1
 
@@ -76,6 +81,36 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"((unsigned long long)map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// Bulk tensor store of a shared-memory box (one bulk group per commit).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   (unsigned long long)map),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most N of this thread's latest bulk groups still read shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// every bulk group of this thread has written global memory; later generic
+// accesses (after a release by any thread of the CTA) observe the writes
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// shared-memory writes of this thread become visible to bulk copies
+__device__ __forceinline__ void fence_smem_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -107,6 +142,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 64 consecutive fp32 columns of this thread's TMEM lane (one round trip).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, "
+      "%36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, "
+      "%57, %58, %59, %60, %61, %62, %63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.
@@ -333,6 +390,192 @@ __device__ __forceinline__ void xpose_store_f32_add(float* st, const float* v, f
 #pragma unroll
   for (int r = 0; r < 32; ++r) p[(long long)r * ld] = a[r] + st[r * 33 + l];
 }
+// ---------------------------------------------------------------------------
+// Bulk-copy epilogue.  Each epilogue warp owns an 8 KB shared-memory window
+// of four 2 KB slots.  A 32-row x 32-column output box (one row per lane)
+// is staged there with the swizzle of its tensor map - the 16-byte chunk j
+// of row r sits at chunk j ^ ((r >> 1) & 3) of the row (bf16, 64-byte rows)
+// or j ^ (r & 7) (fp32, 128-byte rows), so the eight lanes of every
+// 128-byte shared-memory wavefront hit distinct banks - and lane 0 writes it
+// to global memory with one bulk tensor store.  The warp goes on with the
+// next box while the copy engine drains the slot.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t sw64(int r, int j) { return r * 64 + ((j ^ ((r >> 1) & 3)) << 4); }
+__device__ __forceinline__ uint32_t sw128(int r, int j) { return r * 128 + ((j ^ (r & 7)) << 4); }
+__device__ __forceinline__ uint32_t bf2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ void box_put_bf16(uint32_t box, int r, const float* v) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    sts128(box + sw64(r, j), bf2(v[8 * j], v[8 * j + 1]), bf2(v[8 * j + 2], v[8 * j + 3]),
+           bf2(v[8 * j + 4], v[8 * j + 5]), bf2(v[8 * j + 6], v[8 * j + 7]));
+}
+__device__ __forceinline__ void box_get_bf16(uint32_t box, int r, float* v) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 u = lds128(box + sw64(r, j));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[8 * j + 2 * i] = __uint_as_float(w[i] << 16);
+      v[8 * j + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+__device__ __forceinline__ void box_put_f32(uint32_t box, int r, const float* v) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    sts128(box + sw128(r, j), __float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+           __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+}
+__device__ __forceinline__ void box_get_f32(uint32_t box, int r, float* v) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint4 u = lds128(box + sw128(r, j));
+    v[4 * j] = __uint_as_float(u.x); v[4 * j + 1] = __uint_as_float(u.y);
+    v[4 * j + 2] = __uint_as_float(u.z); v[4 * j + 3] = __uint_as_float(u.w);
+  }
+}
+
+// Epilogue arithmetic for bf16 outputs: 2^x by the special-function unit and
+// the logistic function with an approximate reciprocal (relative error a few
+// 1e-7, far below the bf16 rounding of the stored values).
+__device__ __forceinline__ float epi_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+#define EPI_LOG2E 1.4426950408889634f
+__device__ __forceinline__ float epi_sigmoid(float x) { return __fdividef(1.0f, 1.0f + epi_ex2(-x * EPI_LOG2E)); }
+
+// 32 columns at each of two TMEM addresses of this thread's lane, one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float* va, float* vb) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(ta));
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(tb));
+  // the wait takes the loaded registers as operands, so no use of them is
+  // scheduled before it
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+  asm volatile(""
+               : "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]),
+                 "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]),
+                 "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]),
+                 "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]),
+                 "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    va[i] = __uint_as_float(r[i]);
+    vb[i] = __uint_as_float(r[32 + i]);
+  }
+}
+
+// Per-warp state of the bulk-copy epilogue (warp-uniform).
+struct EpiSt {
+  uint32_t win;       // the warp's 8 KB window
+  uint32_t mbar;      // two aux-load mbarriers, 8 bytes apart
+  uint32_t nbox;      // boxes stored by the store-only epilogues
+  uint32_t use[2];    // completed phases of the two mbarriers
+  bool dead;          // an aux load timed out: skip the remaining work
+};
+
+// Store-only epilogues: stage box k in slot k & 3 (bf16) or half k & 1
+// (fp32) once the store four (two) boxes back has read it.
+__device__ __forceinline__ void epi_store_bf16(EpiSt& e, const CUtensorMap* map, int x, int y, const float* v) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t box = e.win + (e.nbox & 3) * TC_EPI_SLOT;
+  if (lane == 0) bulk_wait_read<3>();
+  __syncwarp();
+  box_put_bf16(box, lane, v);
+  fence_smem_async();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, box, x, y);
+    bulk_commit();
+  }
+  ++e.nbox;
+}
+__device__ __forceinline__ void epi_store_f32(EpiSt& e, const CUtensorMap* map, int x, int y, const float* v) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t box = e.win + (e.nbox & 1) * 2 * TC_EPI_SLOT;
+  if (lane == 0) bulk_wait_read<1>();
+  __syncwarp();
+  box_put_f32(box, lane, v);
+  fence_smem_async();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, box, x, y);
+    bulk_commit();
+  }
+  ++e.nbox;
+}
+
+// Epilogues with an input box per output box: chunk c of the tile uses half
+// c & 1 of the window.  Lane 0 loads the chunk's input boxes by TMA (two
+// chunks ahead), every lane replaces its row of them by the output rows, and
+// lane 0 stores them from the same slots.  issue(c, half, bar) and
+// store(c, half) run on lane 0; work(c, half) on every lane.
+template <class Issue, class Work, class Store>
+__device__ __forceinline__ void epi_aux_tile(EpiSt& e, int nch, long long tmo, ArenaHdr* hdr, Issue issue,
+                                             Work work, Store store) {
+  const int lane = threadIdx.x & 31;
+  if (e.dead) return;
+  if (lane == 0) {
+    bulk_wait_read<0>();
+    issue(0, e.win, e.mbar);
+    if (nch > 1) issue(1, e.win + 2 * TC_EPI_SLOT, e.mbar + 8);
+  }
+  __syncwarp();
+  for (int c = 0; c < nch; ++c) {
+    const int h = c & 1;
+    const uint32_t half = e.win + h * 2 * TC_EPI_SLOT, bar = e.mbar + 8 * h;
+    const uint32_t par = e.use[h] & 1;
+    ++e.use[h];
+    const bool late = !mbar_wait(bar, par, tmo);
+    if (__any_sync(0xffffffffu, late)) {
+      if (lane == 0) set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_EPI);
+      e.dead = true;
+      return;
+    }
+    work(c, half);
+    fence_smem_async();
+    __syncwarp();
+    if (lane == 0) {
+      store(c, half);
+      bulk_commit();
+      if (c + 2 < nch) {
+        bulk_wait_read<0>();
+        issue(c + 2, half, bar);
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // Epilogue parameters copied into registers once per job: stores through
 // the output pointers can then not force re-reads of the descriptor.
 struct EpiRegs {
@@ -346,14 +589,236 @@ struct EpiRegs {
   const int* tok;
   float* cepart;
   float* cetgt;
+  const CUtensorMap* om;     // bulk-store map of out (null: plain stores)
+  const CUtensorMap* om2;    // of out2
+  const CUtensorMap* am;     // bulk-load map of aux
+  int oy0, oy02, ay0;
 };
-__device__ __forceinline__ EpiRegs epi_regs(const GemmDesc& g) {
+__device__ __forceinline__ EpiRegs epi_regs(const KArgs& a, const GemmDesc& g) {
   EpiRegs e;
   e.epi = g.epi; e.S = g.S; e.hq = g.hq; e.F = g.F; e.accumulate = g.accumulate; e.osplit = g.osplit;
   e.ceparts = g.ceparts; e.N = g.N; e.ldo = g.ldo; e.ldo2 = g.ldo2; e.ldaux = g.ldaux; e.oseg = g.oseg;
   e.out = g.out; e.out1 = g.out1; e.out2 = g.out2; e.aux = g.aux; e.rope = g.rope; e.tok = g.tok;
   e.cepart = g.cepart; e.cetgt = g.cetgt;
+  e.om = g.omap >= 0 ? &a.maps[g.omap] : nullptr;
+  e.om2 = g.omap2 >= 0 ? &a.maps[g.omap2] : nullptr;
+  e.am = g.amap >= 0 ? &a.maps[g.amap] : nullptr;
+  e.oy0 = g.oy0; e.oy02 = g.oy02; e.ay0 = g.ay0;
+  // every tensor-map path of an epilogue needs all of its maps
+  if ((g.epi == EPI_SWIGLU && !e.om2) || ((g.epi == EPI_SWIGLU_BWD || g.epi == EPI_RESID ||
+                                            g.epi == EPI_STORE_OP_D) && !e.am))
+    e.om = nullptr;
   return e;
+}
+
+// The tensor-map paths of the epilogue (g.om set).  row0: first row of the
+// warp's 32 rows in the product; m = row0 + lane.
+__device__ __forceinline__ void tc_epilogue_tma(const EpiRegs& g, const TcTile& ti, uint32_t trow, int m,
+                                                int row0, EpiSt& es, long long tmo, ArenaHdr* hdr) {
+  constexpr int NCH = TC_BN / 32;
+  const int lane = threadIdx.x & 31;
+  const int y = g.oy0 + row0;
+  switch (g.epi) {
+    case EPI_ROPE: {
+      // hd == 64: columns [64h, 64h+32) pair with [64h+32, 64h+64)
+      const float4* tab4 = reinterpret_cast<const float4*>(g.rope + (long long)(m % g.S) * 64);
+      for (int h2 = 0; h2 < TC_BN / 64; ++h2) {
+        float x[64];
+        tmem_ld64(trow + h2 * 64, x);
+        const int n = ti.n0 + h2 * 64;
+        if (n < 2 * g.hq) {
+#pragma unroll
+          for (int i2 = 0; i2 < 16; ++i2) {
+            const float4 cs = tab4[i2];     // (cos, sin) of pairs 2*i2, 2*i2+1
+            const int i = 2 * i2;
+            float x1 = x[i], x2 = x[i + 32];
+            x[i] = x1 * cs.x - x2 * cs.y;
+            x[i + 32] = x2 * cs.x + x1 * cs.y;
+            x1 = x[i + 1];
+            x2 = x[i + 33];
+            x[i + 1] = x1 * cs.z - x2 * cs.w;
+            x[i + 33] = x2 * cs.z + x1 * cs.w;
+          }
+        }
+        epi_store_bf16(es, g.om, n, y, x);
+        epi_store_bf16(es, g.om, n + 32, y, x + 32);
+      }
+      break;
+    }
+    case EPI_SWIGLU: {
+      // each 128-column half = [64 gate | 64 up] of expert rows f0..f0+63
+      const int y2 = g.oy02 + row0;
+      for (int half = 0; half < TC_BN / 128; ++half) {
+        const int f0 = ((ti.n0 >> 7) + half) * 64;
+        for (int c = 0; c < 2; ++c) {
+          float gg[32], uu[32];
+          tmem_ld32x2(trow + half * 128 + c * 32, trow + half * 128 + 64 + c * 32, gg, uu);
+          const int f = f0 + c * 32;
+          epi_store_bf16(es, g.om, f, y, gg);
+          epi_store_bf16(es, g.om, g.F + f, y, uu);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) gg[i] = gg[i] * epi_sigmoid(gg[i]) * uu[i];
+          epi_store_bf16(es, g.om2, f, y2, gg);
+        }
+      }
+      break;
+    }
+    case EPI_SWIGLU_BWD: {
+      // aux = [g | u] boxes at columns n and F + n; out = [dg | du] in their slots
+      const int ya = g.ay0 + row0;
+      const CUtensorMap* am = g.am;
+      const CUtensorMap* om = g.om;
+      const int F = g.F, n0 = ti.n0;
+      epi_aux_tile(
+          es, NCH, tmo, hdr,
+          [&](int c, uint32_t half, uint32_t bar) {
+            mbar_expect_tx(bar, 2 * TC_EPI_SLOT);
+            tma_load_2d(half, am, n0 + 32 * c, ya, bar);
+            tma_load_2d(half + TC_EPI_SLOT, am, F + n0 + 32 * c, ya, bar);
+          },
+          [&](int c, uint32_t half) {
+            float da[32], gg[32], uu[32];
+            tmem_ld32(trow + c * 32, da);
+            box_get_bf16(half, lane, gg);
+            box_get_bf16(half + TC_EPI_SLOT, lane, uu);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float sg = epi_sigmoid(gg[i]);
+              const float du = da[i] * gg[i] * sg;
+              gg[i] = da[i] * uu[i] * sg * (1.0f + gg[i] * (1.0f - sg));
+              uu[i] = du;
+            }
+            box_put_bf16(half, lane, gg);
+            box_put_bf16(half + TC_EPI_SLOT, lane, uu);
+          },
+          [&](int c, uint32_t half) {
+            tma_store_2d(om, half, n0 + 32 * c, y);
+            tma_store_2d(om, half + TC_EPI_SLOT, F + n0 + 32 * c, y);
+          });
+      break;
+    }
+    case EPI_STORE_OP_D: {
+      // 64-column heads: out = dO (bf16); D = rowsum(bf16(dO) * O), O from aux
+      const int ya = g.ay0 + row0;
+      const CUtensorMap* am = g.am;
+      const CUtensorMap* om = g.om;
+      const int n0 = ti.n0;
+      float* dsum = (float*)g.out2 + (long long)(m / g.S) * g.ldo2 * g.S + (m % g.S);
+      epi_aux_tile(
+          es, TC_BN / 64, tmo, hdr,
+          [&](int c, uint32_t half, uint32_t bar) {
+            mbar_expect_tx(bar, 2 * TC_EPI_SLOT);
+            tma_load_2d(half, am, n0 + 64 * c, ya, bar);
+            tma_load_2d(half + TC_EPI_SLOT, am, n0 + 64 * c + 32, ya, bar);
+          },
+          [&](int c, uint32_t half) {
+            float x[32], oo[32];
+            float dot = 0.f;
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+              tmem_ld32(trow + c * 64 + p * 32, x);
+              box_get_bf16(half + p * TC_EPI_SLOT, lane, oo);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) dot = fmaf(__bfloat162float(__float2bfloat16_rn(x[i])), oo[i], dot);
+              box_put_bf16(half + p * TC_EPI_SLOT, lane, x);
+            }
+            dsum[(long long)((n0 + 64 * c) / 64) * g.S] = dot;
+          },
+          [&](int c, uint32_t half) {
+            tma_store_2d(om, half, n0 + 64 * c, y);
+            tma_store_2d(om, half + TC_EPI_SLOT, n0 + 64 * c + 32, y);
+          });
+      break;
+    }
+    case EPI_LOGITS: {
+      int tgt = -1;
+      if (m % g.S != g.S - 1) {
+        tgt = g.tok[m + 1];
+        if (tgt < 0 || tgt >= g.N) tgt = 0;   // out-of-range ids are reported by the embedding job
+      }
+      // running (max, sum of exp(l - max)) over the tile's columns, in base 2
+      // internally: sum_i 2^((l_i - max) log2 e) = sum_i exp(l_i - max)
+      float mx = -INFINITY, sm = 0.f, tv = 0.f;
+      bool has_t = false;
+      for (int c = 0; c < NCH; c += 2) {
+        float v[64];
+        tmem_ld64(trow + c * 32, v);
+        const int n = ti.n0 + c * 32;
+        epi_store_bf16(es, g.om, n, y, v);
+        epi_store_bf16(es, g.om, n + 32, y, v + 32);
+        const int off = tgt - n;
+        if ((unsigned)off < 64u) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i == off) tv = v[i];
+          has_t = true;
+        }
+        float m8[8], s8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = v[k];
+#pragma unroll
+        for (int i = 8; i < 64; ++i) m8[i & 7] = fmaxf(m8[i & 7], v[i]);
+        const float bm = fmaxf(fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))), mx);
+        const float bml = bm * EPI_LOG2E;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s8[k] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) s8[i & 7] += epi_ex2(fmaf(v[i], EPI_LOG2E, -bml));
+        const float bs = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+        sm = sm * epi_ex2((mx - bm) * EPI_LOG2E) + bs;
+        mx = bm;
+      }
+      if (has_t) g.cetgt[m] = tv;
+      float* pp = g.cepart + ((long long)m * g.ceparts + ti.n0 / TC_BN) * 2;
+      pp[0] = mx;
+      pp[1] = sm;
+      break;
+    }
+    case EPI_STORE_F32: {
+      for (int c = 0; c < NCH; c += 2) {
+        float v[64];
+        tmem_ld64(trow + c * 32, v);
+        epi_store_f32(es, g.om, ti.n0 + c * 32, y, v);
+        epi_store_f32(es, g.om, ti.n0 + c * 32 + 32, y, v + 32);
+      }
+      break;
+    }
+    case EPI_STORE_OP: {
+      for (int c = 0; c < NCH; c += 2) {
+        float v[64];
+        tmem_ld64(trow + c * 32, v);
+        epi_store_bf16(es, g.om, ti.n0 + c * 32, y, v);
+        epi_store_bf16(es, g.om, ti.n0 + c * 32 + 32, y, v + 32);
+      }
+      break;
+    }
+    case EPI_RESID: {
+      // out = aux + accumulator, fp32 boxes (one per half of the window)
+      const int ya = g.ay0 + row0;
+      const CUtensorMap* am = g.am;
+      const CUtensorMap* om = g.om;
+      const int n0 = ti.n0;
+      epi_aux_tile(
+          es, NCH, tmo, hdr,
+          [&](int c, uint32_t half, uint32_t bar) {
+            mbar_expect_tx(bar, 2 * TC_EPI_SLOT);
+            tma_load_2d(half, am, n0 + 32 * c, ya, bar);
+          },
+          [&](int c, uint32_t half) {
+            float v[32], x[32];
+            tmem_ld32(trow + c * 32, v);
+            box_get_f32(half, lane, x);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += x[i];
+            box_put_f32(half, lane, v);
+          },
+          [&](int c, uint32_t half) { tma_store_2d(om, half, n0 + 32 * c, y); });
+      break;
+    }
+    default:
+      break;
+  }
 }
 
 __device__ __forceinline__ void tc_epilogue(const EpiRegs& g, const TcTile& ti, uint32_t trow, int m, float* st,
@@ -572,6 +1037,7 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
       mbar_init(accf + 8 * i, 1);
       mbar_init(acce + 8 * i, 4);
     }
+    for (int i = 0; i < 8; ++i) mbar_init(sbase + TC_EPI_MBAR + 8 * i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -672,8 +1138,16 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
     __syncwarp();
   } else if (warp >= 4) {
     const int q = warp - 4;
-    const EpiRegs er = epi_regs(g);
-    float* xst = reinterpret_cast<float*>(smem + TC_STAGE_OFF + q * TC_XPOSE_BYTES);
+    const EpiRegs er = epi_regs(a, g);
+    float* xst = reinterpret_cast<float*>(smem + TC_STAGE_OFF + q * TC_EPI_WARP_BYTES);
+    EpiSt es;
+    es.win = sbase + TC_STAGE_OFF + q * TC_EPI_WARP_BYTES;
+    es.mbar = sbase + TC_EPI_MBAR + 16 * q;
+    es.nbox = 0; es.use[0] = es.use[1] = 0; es.dead = false;
+    const bool tma = er.om != nullptr;
+    // aux rows were stored by generic writes before this job: order the bulk
+    // loads after them
+    if (tma && lane == 0) asm volatile("fence.proxy.async;" ::: "memory");
     unsigned* const dsig = g.dsig;
     const unsigned* const dwa = g.dwait_aux;
     const unsigned dta = g.dtarget_aux;
@@ -683,7 +1157,10 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
       const TcTile ti = tc_tile(sh, t);
       const int m = ti.m0 + q * 32 + lane;
       if (dwa) {
-        if (lane == 0) dep_wait(hdr, dwa + (ti.m0 >> 7), dta, tmo);
+        if (lane == 0) {
+          dep_wait(hdr, dwa + (ti.m0 >> 7), dta, tmo);
+          asm volatile("fence.proxy.async;" ::: "memory");
+        }
         __syncwarp();
       }
       if (ti.nk == 0) {
@@ -701,14 +1178,26 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
         __syncwarp();
         tc_fence_after();
         const uint32_t trow = tc.tmem_base + ab * TC_BN + ((uint32_t)(q * 32) << 16);
-        tc_epilogue(er, ti, trow, m, xst, (long long)(ti.m0 + q * 32));
+        if (tma)
+          tc_epilogue_tma(er, ti, trow, m, ti.m0 + q * 32, es, tmo, hdr);
+        else
+          tc_epilogue(er, ti, trow, m, xst, (long long)(ti.m0 + q * 32));
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce + 8 * ab);
       }
-      if (dsig) epi_signal(dsig + (ti.m0 >> 7));
+      if (dsig) {
+        // the tile's bulk stores have landed before its counter moves
+        if (tma && lane == 0) bulk_wait_all();
+        __syncwarp();
+        epi_signal(dsig + (ti.m0 >> 7));
+      }
       ++tcount;
     }
+    // every bulk store of the job has landed before the job ends (the next
+    // hand-off is a grid barrier or a later counter) and the window is free
+    if (tma && lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   __syncthreads();
   s.next(items);

@@ -399,12 +399,13 @@ int32_t mt_debug_gemm(const void* A, int32_t a_mn, const void* B, int32_t b_mn, 
   a->dbg_m = M; a->dbg_n = N; a->dbg_k = K; a->dbg_a_mn = a_mn; a->dbg_b_mn = b_mn;
   a->dbg_rag = rag; a->dbg_nseg = rag ? nseg : 0; a->dbg_offs = offs;
   a->dbg_out_mode = out_mode;
+  a->dbg_tma = tc && (use_tc & 8) && rag != 2 && out_mode < 2;
   a->use_tc = tc ? 1 : 0;
   if (tc) {
     const long long segs = rag == 1 ? nseg : 1;
     const long long ar = a_mn ? K : M, ac = a_mn ? M : K;
     const long long br = (b_mn ? K : N) * segs, bc = b_mn ? N : K;
-    int ms = mt_build_debug_maps(a, A, ar, ac, B, br, bc);
+    int ms = mt_build_debug_maps(a, A, ar, ac, B, br, bc, a->dbg_tma ? C : nullptr, M, N, out_mode == 0);
     if (ms != MT_OK) { delete a; return ms; }
   }
   cudaError_t e = bf16 ? mt_launch_mega_bf16(*a, grid, smem, (cudaStream_t)stream)

@@ -1700,7 +1700,7 @@ __device__ __noinline__ void job_adamw(const KArgs& a, char* smem) {
   // issued, the stage of iteration i-1 (whose stores have had a whole
   // iteration to read it out) is refilled.  Groups past the last whole chunk
   // take the register path on the last CTA.
-  constexpr int AW_G = 512, AW_NS = 4, AW_T = 4096;
+  constexpr int AW_G = 512, AW_NS = 6, AW_T = 4096;
   const uint32_t SEG = (uint32_t)AW_G * 16u;
   const uint32_t STB = 4u * SEG + (uint32_t)AW_G * 8u;   // p | m | v | g | shadow
   const bool bulk = RP_WIN_OFF + (uint32_t)AW_NS * STB <= (uint32_t)a.smem_bytes;
@@ -1852,6 +1852,7 @@ struct Gemms {
     g.rope = nullptr;
     g.tok = nullptr; g.cepart = nullptr; g.cetgt = nullptr; g.ceparts = 0; g.ksplit = 1;
     g.dwait = nullptr; g.dtarget = 0; g.dwait_aux = nullptr; g.dtarget_aux = 0; g.dsig = nullptr;
+    g.omap = g.omap2 = g.amap = -1; g.oy0 = g.oy02 = g.ay0 = 0;
     return g;
   }
   __device__ const int* offs(int l) const { return abuf<int>(a, A_OFFS) + (long long)l * (D.E + 1); }
@@ -1864,6 +1865,7 @@ struct Gemms {
     g.B = opnd(pweight<OP>(a, P_WQKV) + (long long)l * 3 * D.hq * D.d, D.d, 0);
     g.B.map0 = MAP_WQKV; g.B.y0 = l * 3 * D.hq;
     g.out = abuf<OP>(a, A_QKV) + (long long)l * D.T * 3 * D.hq; g.ldo = 3 * D.hq;
+    g.omap = MAP_E_QKV; g.oy0 = l * D.T;
     g.rope = abuf<float>(a, A_ROPE);
     return g;
   }
@@ -1875,6 +1877,7 @@ struct Gemms {
     g.B.map0 = MAP_WO; g.B.y0 = l * D.d;
     g.out = abuf<float>(a, A_XM) + (long long)l * D.T * D.d; g.ldo = D.d;
     g.aux = abuf<float>(a, A_X) + (long long)l * D.T * D.d; g.ldaux = D.d;
+    g.omap = MAP_E_XM; g.oy0 = l * D.T; g.amap = MAP_E_X; g.ay0 = l * D.T;
     return g;
   }
   __device__ GemmDesc gateup(int l) const {
@@ -1888,6 +1891,7 @@ struct Gemms {
     g.B.map0 = MAP_WGATE; g.B.map1 = MAP_WUP; g.B.y0 = l * D.E * D.F; g.B.yseg = D.F;
     g.out = abuf<OP>(a, A_GU) + (long long)l * D.Pmax * 2 * D.F; g.ldo = 2 * D.F;
     g.out2 = abuf<OP>(a, A_ACT) + (long long)l * D.Pmax * D.F; g.ldo2 = D.F;
+    g.omap = MAP_E_GU; g.oy0 = l * D.Pmax; g.omap2 = MAP_E_ACT; g.oy02 = l * D.Pmax;
     return g;
   }
   __device__ GemmDesc down(int l) const {
@@ -1899,6 +1903,7 @@ struct Gemms {
     g.B.seg = (long long)D.d * D.F;
     g.B.map0 = MAP_WDOWN; g.B.y0 = l * D.E * D.d; g.B.yseg = D.d;
     g.out = abuf<float>(a, A_Y) + (long long)l * D.Pmax * D.d; g.ldo = D.d;
+    g.omap = MAP_E_Y; g.oy0 = l * D.Pmax;
     return g;
   }
   __device__ GemmDesc lm() const {
@@ -1908,6 +1913,7 @@ struct Gemms {
     g.out = abuf<OP>(a, A_DLOGITS); g.ldo = D.V;
     g.tok = a.tokens; g.cepart = abuf<float>(a, A_CEPART); g.cetgt = abuf<float>(a, A_CETGT);
     g.ceparts = ce_parts<OP>(a);
+    g.omap = MAP_E_DLOGITS;
     return g;
   }
   // backward
@@ -1916,6 +1922,7 @@ struct Gemms {
     g.A = opnd(abuf<OP>(a, A_DLOGITS), D.V, 0); g.A.map0 = MAP_DLOGITS;
     g.B = opnd(pweight<OP>(a, P_LM_HEAD), D.d, 1); g.B.map0 = MAP_WLM;
     g.out = abuf<float>(a, A_DRF); g.ldo = D.d;
+    g.omap = MAP_E_DRF;
     return g;
   }
   __device__ GemmDesc lm_wgrad() const {
@@ -1934,6 +1941,7 @@ struct Gemms {
     g.B.map0 = MAP_WDOWN; g.B.y0 = l * D.E * D.d; g.B.yseg = D.d;
     g.out = abuf<OP>(a, A_DGU); g.ldo = 2 * D.F;
     g.aux = abuf<OP>(a, A_GU) + (long long)l * D.Pmax * 2 * D.F; g.ldaux = 2 * D.F;
+    g.omap = MAP_E_DGU; g.amap = MAP_E_GU; g.ay0 = l * D.Pmax;
     return g;
   }
   __device__ GemmDesc down_wgrad(int l) const {
@@ -1955,6 +1963,7 @@ struct Gemms {
     g.B.two = 2; g.B.split = D.F; g.B.seg = (long long)D.F * D.d;
     g.B.map0 = MAP_WGATE; g.B.map1 = MAP_WUP; g.B.y0 = l * D.E * D.F; g.B.yseg = D.F;
     g.out = abuf<float>(a, A_DXS); g.ldo = D.d;
+    g.omap = MAP_E_DXS;
     return g;
   }
   __device__ GemmDesc gateup_wgrad(int l) const {
@@ -1976,6 +1985,7 @@ struct Gemms {
     g.out = abuf<OP>(a, A_DO); g.ldo = D.hq;
     g.aux = abuf<OP>(a, A_O) + (long long)l * D.T * D.hq; g.ldaux = D.hq;
     g.out2 = abuf<float>(a, A_DSUM); g.ldo2 = D.H;
+    g.omap = MAP_E_DO; g.amap = MAP_E_O; g.ay0 = l * D.T;
     return g;
   }
   // Weight gradients with few output tiles cut their token reduction into
@@ -2003,6 +2013,7 @@ struct Gemms {
     g.B = opnd(pweight<OP>(a, P_WQKV) + (long long)l * 3 * D.hq * D.d, D.d, 1);
     g.B.map0 = MAP_WQKV; g.B.y0 = l * 3 * D.hq;
     g.out = abuf<float>(a, A_DR); g.ldo = D.d;
+    g.omap = MAP_E_DR;
     return g;
   }
   __device__ GemmDesc qkv_wgrad(int l) const {
@@ -2296,6 +2307,8 @@ __device__ void run_debug_gemm(const KArgs& a, char* smem, TcState& tc, Sched& s
   g.F = 0; g.S = 1; g.hd = 64; g.hq = 0; g.rope = nullptr;
   g.tok = nullptr; g.cepart = nullptr; g.cetgt = nullptr; g.ceparts = 0; g.ksplit = 1;
   g.dwait = nullptr; g.dtarget = 0; g.dwait_aux = nullptr; g.dtarget_aux = 0; g.dsig = nullptr;
+  g.omap = g.omap2 = g.amap = -1; g.oy0 = g.oy02 = g.ay0 = 0;
+  if (a.dbg_tma && g.rag != RAG_K && a.dbg_out_mode < 2) g.omap = a.dbg_out_mode == 1 ? MAP_E_QKV : MAP_E_Y;
   GOperand A, B;
   A.p0 = a.dbg_a; A.p1 = nullptr; A.mn = a.dbg_a_mn; A.ld = A.mn ? g.M : g.K; A.seg = 0; A.two = 0;
   A.split = 0; A.map0 = MAP_R; A.map1 = -1; A.y0 = 0; A.yseg = 0;

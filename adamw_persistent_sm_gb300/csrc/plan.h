@@ -74,8 +74,14 @@ enum ArenaId {
 // coordinate of a map over the whole stack.
 enum MapId {
   MAP_R = 0, MAP_WQKV, MAP_O, MAP_WO, MAP_XS, MAP_WGATE, MAP_WUP, MAP_ACT, MAP_WDOWN, MAP_RF,
-  MAP_WLM, MAP_DLOGITS, MAP_DY, MAP_DGU, MAP_DXO, MAP_DQKV, MAP_QKV, MAP_DOUT, MAP_COUNT
+  MAP_WLM, MAP_DLOGITS, MAP_DY, MAP_DGU, MAP_DXO, MAP_DQKV, MAP_QKV, MAP_DOUT,
+  // 32 x 32 boxes of the epilogues' bulk stores and aux loads: bf16 with the
+  // 64-byte swizzle, fp32 with the 128-byte swizzle
+  MAP_E_QKV, MAP_E_GU, MAP_E_ACT, MAP_E_DGU, MAP_E_DLOGITS, MAP_E_DO, MAP_E_O,
+  MAP_E_Y, MAP_E_DRF, MAP_E_DXS, MAP_E_DR, MAP_E_XM, MAP_E_X,
+  MAP_COUNT
 };
+static_assert(MAP_COUNT <= MT_NMAPS, "too many tensor maps");
 
 struct MtDims {
   int V, d, L, H, hd, hq, E, K, F, B, S, T;
@@ -150,6 +156,7 @@ struct KArgs {
   const void* dbg_a; const void* dbg_b; float* dbg_c;
   int dbg_m, dbg_n, dbg_k, dbg_a_mn, dbg_b_mn, dbg_rag, dbg_nseg;
   int dbg_out_mode;             // 0 fp32 C, 1 bf16 C (written over the fp32 buffer), 2 accumulators read only
+  int dbg_tma;                  // C written by the bulk-store epilogue (map MAP_E_Y fp32 / MAP_E_QKV bf16)
   const int* dbg_offs;
   int use_tc;                   // tcgen05 GEMMs (bf16 only)
   int use_tc_attn;              // tensor-core attention (bf16 only)

@@ -365,7 +365,7 @@ def run_product(args):
     import torch
     from adamw_persistent_sm_gb300 import binding as B
     M, N, K, amn, bmn = args.product
-    out_mode = {"f32": 0, "bf16": 1, "none": 2}[args.product_out]
+    out_mode = {"f32": 0, "bf16": 1, "none": 2, "f32-bulk": 4, "bf16-bulk": 5}[args.product_out]
     B.load(build_if_missing=True)
     arena = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     B.mt_arena_init(arena.data_ptr(), arena.numel())
@@ -411,8 +411,9 @@ def main():
                     help="grid barriers at every hand-off (no per-block dependency counters)")
     ap.add_argument("--product", type=int, nargs=5, metavar=("M", "N", "K", "A_MN", "B_MN"),
                     help="time one product through the tensor-core engine")
-    ap.add_argument("--product-out", default="f32", choices=["f32", "bf16", "none"],
-                    help="output of --product: fp32, bf16, or accumulators read and dropped")
+    ap.add_argument("--product-out", default="f32", choices=["f32", "bf16", "none", "f32-bulk", "bf16-bulk"],
+                    help="output of --product: fp32, bf16, accumulators read and dropped, or fp32 / bf16 "
+                         "written by bulk tensor stores")
     args = ap.parse_args()
     cfg = mi.get_config(args.config)
     if args.product:

@@ -252,7 +252,9 @@ int32_t mt_train_update_noalloc(float* params, void* shadow, float* grads, float
  *            reduces rows offs[e]..offs[e+1] into C[e] ([nseg][M][N]).
  * use_tc: bit 0 selects the tensor cores; on that path bits 1-2 select the
  * output (0: fp32 C; 1: bf16 C written over the start of the C buffer; 2: the
- * accumulators are read from tensor memory and dropped - a timing mode).
+ * accumulators are read from tensor memory and dropped - a timing mode); bit 3
+ * writes an fp32 or bf16 C (rag 0 or 1) by bulk tensor stores from the
+ * epilogue's shared-memory window, the path the update's products take.
  * A and B are bf16 (MT_PREC_BF16) or fp32 (MT_PREC_FP32) device arrays.  The
  * tensor-core path needs M a multiple of 128, N a multiple of 256 and K a
  * multiple of 64.

@@ -101,3 +101,40 @@ def test_fp32_simt_exact():
     b = torch.randn(K, N, device="cuda")
     C = _run(a, 0, b, 1, M, N, K, use_tc=0)
     assert _rel(C, a.double() @ b.double()) < 1e-6
+
+
+@pytest.mark.parametrize("bf16_out", [0, 1])
+@pytest.mark.parametrize("rag", [0, 1])
+def test_bulk_store_epilogue(bf16_out, rag):
+    """C written by the bulk-store epilogue (swizzled shared-memory boxes and
+    bulk tensor stores, the path of the update's products) equals the plain
+    stores of the same product bit for bit, and matches the float64 product."""
+    from adamw_persistent_sm_gb300 import binding as B
+    torch.manual_seed(4)
+    N, K = 512, 320
+    offs = None
+    nseg = 0
+    if rag:
+        counts = [256, 0, 128]
+        nseg = len(counts)
+        offs_np = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        offs = torch.as_tensor(offs_np).cuda()
+        M = int(offs_np[-1])
+        w = torch.randn(nseg, N, K, device="cuda").bfloat16()
+    else:
+        M = 384
+        w = torch.randn(N, K, device="cuda").bfloat16()
+    a = torch.randn(M, K, device="cuda").bfloat16()
+    mode = 1 | (bf16_out << 1)
+    plain = _run(a, 0, w, 0, M, N, K, rag=rag, offs=offs, nseg=nseg, use_tc=mode)
+    bulk = _run(a, 0, w, 0, M, N, K, rag=rag, offs=offs, nseg=nseg, use_tc=mode | 8)
+    if bf16_out:
+        # bf16 C occupies the first M*N*2 bytes of the buffer
+        plain = plain.view(torch.bfloat16).reshape(-1)[:M * N].reshape(M, N).float()
+        bulk = bulk.view(torch.bfloat16).reshape(-1)[:M * N].reshape(M, N).float()
+    assert torch.equal(plain, bulk)
+    if rag:
+        ref = torch.cat([a[offs_np[e]:offs_np[e + 1]].double() @ w[e].double().t() for e in range(nseg)])
+    else:
+        ref = a.double() @ w.double().t()
+    assert _rel(bulk, ref) < (1e-2 if bf16_out else TOL)
