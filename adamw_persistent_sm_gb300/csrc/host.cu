@@ -281,8 +281,9 @@ int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m
   a->rope_theta = hp->rope_theta;
   const double ntargets = (double)hp->batch * (hp->seq - 1) * hp->micro_count;
   a->coef = hp->loss_coef > 0.f ? hp->loss_coef : (float)(1.0 / ntargets);
-  a->bc1 = (float)(1.0 - pow((double)hp->beta1, (double)hp->step));
-  a->bc2 = (float)(1.0 - pow((double)hp->beta2, (double)hp->step));
+  a->ibc1 = (float)(1.0 / (1.0 - pow((double)hp->beta1, (double)hp->step)));
+  a->ibc2 = (float)(1.0 / (1.0 - pow((double)hp->beta2, (double)hp->step)));
+  a->decay = (float)(1.0 - (double)hp->lr * (double)hp->weight_decay);
   a->micro_index = hp->micro_index;
   a->micro_count = hp->micro_count;
   a->run_opt = (hp->micro_index == hp->micro_count - 1) && !(hp->flags & MT_FLAG_NO_OPTIMIZER);

@@ -1639,15 +1639,32 @@ static __device__ __noinline__ void job_norm_partial(const KArgs& a, double* dsm
   }
 }
 
-template <class OP>
-__device__ __forceinline__ void adamw_elem(const KArgs& a, float c, float& p, float g, float& m, float& v) {
-  g *= c;
-  p *= 1.0f - a.lr * a.wd;
-  m = a.beta1 * m + (1.0f - a.beta1) * g;
-  v = a.beta2 * v + (1.0f - a.beta2) * g * g;
-  const float mh = m / a.bc1;
-  const float vh = v / a.bc2;
-  p -= a.lr * mh / (sqrtf(vh) + a.eps);
+// AdamW constants of one sweep, held in registers.
+struct AwConst {
+  float c;                  // clip coefficient
+  float decay;              // 1 - lr * wd (decoupled decay, applied first)
+  float b1, omb1, b2, omb2; // beta1, 1 - beta1, beta2, 1 - beta2
+  float ibc1, ibc2;         // 1 / (1 - beta^t)
+  float lr, eps;
+};
+__device__ __forceinline__ AwConst aw_const(const KArgs& a, float c) {
+  AwConst k;
+  k.c = c; k.decay = a.decay; k.b1 = a.beta1; k.omb1 = 1.0f - a.beta1; k.b2 = a.beta2; k.omb2 = 1.0f - a.beta2;
+  k.ibc1 = a.ibc1; k.ibc2 = a.ibc2; k.lr = a.lr; k.eps = a.eps;
+  return k;
+}
+// One parameter: g <- c g; p <- (1 - lr wd) p; m, v moving averages;
+// p <- p - lr m^ / (sqrt(v^) + eps) with the bias-corrected moments.  The
+// bias corrections multiply by host reciprocals and the step divides with
+// the fast division (relative error ~1e-7 on a step of ~lr).
+__device__ __forceinline__ void adamw_elem(const AwConst& k, float& p, float g, float& m, float& v) {
+  g *= k.c;
+  p *= k.decay;
+  m = k.b1 * m + k.omb1 * g;
+  v = k.b2 * v + k.omb2 * g * g;
+  const float mh = m * k.ibc1;
+  const float vh = v * k.ibc2;
+  p -= __fdividef(k.lr * mh, sqrtf(vh) + k.eps);
 }
 
 // Clip coefficient from the ordered sum of the partials, then the AdamW sweep
@@ -1660,6 +1677,7 @@ __device__ __noinline__ void job_adamw(const KArgs& a, char* smem) {
   for (int i = 0; i < G; ++i) tot += parts[i];
   const float norm = (float)sqrt(tot);
   const float coef = fminf(1.0f, a.clip / (norm + a.clip_eps));
+  const AwConst ak = aw_const(a, coef);
   if (c == 0 && threadIdx.x == 0) {
     ArenaHdr* h = abuf<ArenaHdr>(a, A_HDR);
     h->grad_norm = norm;
@@ -1674,10 +1692,10 @@ __device__ __noinline__ void job_adamw(const KArgs& a, char* smem) {
   float4* v4 = reinterpret_cast<float4*>(a.adam_v);
   __nv_bfloat16* sh = (sizeof(OP) == 2) ? (__nv_bfloat16*)a.shadow : nullptr;
   auto step4 = [&](long long j, float4 p, const float4 g, float4 m, float4 v) {
-    adamw_elem<OP>(a, coef, p.x, g.x, m.x, v.x);
-    adamw_elem<OP>(a, coef, p.y, g.y, m.y, v.y);
-    adamw_elem<OP>(a, coef, p.z, g.z, m.z, v.z);
-    adamw_elem<OP>(a, coef, p.w, g.w, m.w, v.w);
+    adamw_elem(ak, p.x, g.x, m.x, v.x);
+    adamw_elem(ak, p.y, g.y, m.y, v.y);
+    adamw_elem(ak, p.z, g.z, m.z, v.z);
+    adamw_elem(ak, p.w, g.w, m.w, v.w);
     p4[j] = p;
     m4[j] = m;
     v4[j] = v;
@@ -1754,10 +1772,10 @@ __device__ __noinline__ void job_adamw(const KArgs& a, char* smem) {
           const uint32_t o = 16u * (uint32_t)k;
           float4 pp = lds4(base + o), mm = lds4(base + SEG + o), vv = lds4(base + 2u * SEG + o);
           const float4 gg = lds4(base + 3u * SEG + o);
-          adamw_elem<OP>(a, coef, pp.x, gg.x, mm.x, vv.x);
-          adamw_elem<OP>(a, coef, pp.y, gg.y, mm.y, vv.y);
-          adamw_elem<OP>(a, coef, pp.z, gg.z, mm.z, vv.z);
-          adamw_elem<OP>(a, coef, pp.w, gg.w, mm.w, vv.w);
+          adamw_elem(ak, pp.x, gg.x, mm.x, vv.x);
+          adamw_elem(ak, pp.y, gg.y, mm.y, vv.y);
+          adamw_elem(ak, pp.z, gg.z, mm.z, vv.z);
+          adamw_elem(ak, pp.w, gg.w, mm.w, vv.w);
           sts4(base + o, pp);
           sts4(base + SEG + o, mm);
           sts4(base + 2u * SEG + o, vv);
@@ -1820,7 +1838,7 @@ __device__ __noinline__ void job_adamw(const KArgs& a, char* smem) {
   if (c == G - 1) {
     for (long long i = n4 * 4 + threadIdx.x; i < n; i += MT_THREADS) {
       float p = a.master[i], m = a.adam_m[i], v = a.adam_v[i];
-      adamw_elem<OP>(a, coef, p, a.grads[i], m, v);
+      adamw_elem(ak, p, a.grads[i], m, v);
       a.master[i] = p;
       a.adam_m[i] = m;
       a.adam_v[i] = v;
@@ -2103,9 +2121,9 @@ __device__ __forceinline__ void run_attn_fwd(const KArgs& a, int l, Sched& s, ch
   if (a.D.hd == 64) attn_fwd_job<OP, 64>(t, s, (float*)smem);
   else attn_fwd_job<OP, 16>(t, s, (float*)smem);
 }
-template <class OP>
+template <class OP, class Stamp>
 __device__ __forceinline__ void run_attn_bwd(const KArgs& a, int l, Sched& s, char* smem, const TcState& tc,
-                                             const AttnDeps& dp) {
+                                             const AttnDeps& dp, Stamp&& stamp) {
   if constexpr (sizeof(OP) == 2) {
     if (a.use_tm_attn) {
       const MtDims& D = a.D;
@@ -2114,6 +2132,7 @@ __device__ __forceinline__ void run_attn_bwd(const KArgs& a, int l, Sched& s, ch
                         abuf<__nv_bfloat16>(a, A_DQKV), abuf<float>(a, A_ROPE), D.B, D.H, D.S, D.hq,
                         1.0f / sqrtf((float)D.hd), dp.hdr, dp.timeout_ns};
       attn_tm::dkdv_job(j, s, smem, tc);
+      stamp();
       attn_tm::dq_job(j, s, smem, tc);
       return;
     }
@@ -2265,7 +2284,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     job_colfinal(a, 0, D.E, D.E, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d, nullptr, 0, s, rg_chunks);
     job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_MOE_NORM) + (long long)l * D.d, nullptr, 0, s, (int)G); TJ(18);
     job_ksplit_sum(a, pgrad(a, P_WO) + (long long)l * D.d * D.hq, D.d, D.hq, s); TJ(32);
-    run_attn_bwd<OP>(a, l, s, smem, tc, attn_deps(l, TK_ATTN_BWD, false)); TJ(26);
+    run_attn_bwd<OP>(a, l, s, smem, tc, attn_deps(l, TK_ATTN_BWD, false), [&] { TJ(35); }); TJ(26);
     MT_SYNC();
     run_gemm<OP>(a, gm.qkv_dgrad(l), s, smem, tc); TJ(27);
     run_gemm<OP>(a, gm.qkv_wgrad(l), s, smem, tc); TJ(28);

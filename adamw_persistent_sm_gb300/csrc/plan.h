@@ -138,7 +138,8 @@ __host__ __device__ inline long long dep_words(const MtDims& D) {
 struct KArgs {
   MtDims D;
   float lr, beta1, beta2, eps, wd, clip, clip_eps, norm_eps, coef, rope_theta;
-  float bc1, bc2;               // 1 - beta^t, computed on the host in double
+  float ibc1, ibc2;             // 1 / (1 - beta^t), computed on the host in double
+  float decay;                  // 1 - lr * weight_decay, in double on the host
   int micro_index, micro_count, run_opt;
   unsigned int flags;
   long long timeout_ns;
