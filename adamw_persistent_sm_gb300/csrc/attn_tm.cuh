@@ -386,6 +386,7 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
 struct BwdJob {
   const CUtensorMap* map_qkv;  // q,k,v of all layers
   const CUtensorMap* map_do;   // dO [T][hq]
+  const CUtensorMap* map_dqkv; // dq,dk,dv [T][3hq], 32-row x 64-column boxes (bulk stores)
   int y0;                      // row of token 0 of this layer in map_qkv
   const float* lse;            // [B*H][S] log2 of the row sum of exp2(scale log2(e) s) (this path's forward)
   const float* dsum;           // [B*H][S]
@@ -403,21 +404,40 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
-__device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const float* g) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-    d[q] = make_uint4(pack2(g[8 * q], g[8 * q + 1]), pack2(g[8 * q + 2], g[8 * q + 3]), pack2(g[8 * q + 4], g[8 * q + 5]),
-                      pack2(g[8 * q + 6], g[8 * q + 7]));
+// Packed pairs of fp32 (the two-wide fp32 instructions of this architecture;
+// each lane rounds as the scalar instruction does).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
 }
-// Undo the rotary embedding on a 64-wide gradient row at position pos (dims i
-// and i + 32 form a pair; table [pos][32][cos, sin]), scale, store as bf16.
-__device__ __forceinline__ void store_grad_row(__nv_bfloat16* dst, float* g, const float* rope, int pos, float scale) {
-  // all 32 (cos, sin) pairs of the position first: 16 independent 16-byte loads
-  const float4* tab = reinterpret_cast<const float4*>(rope + (long long)pos * 64);
-  float4 cs[16];
-#pragma unroll
-  for (int q = 0; q < 16; ++q) cs[q] = tab[q];
+__device__ __forceinline__ uint64_t u2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Undo the rotary embedding on a 64-wide gradient row (dims i and i + 32
+// form a pair; cs = the position's 32 (cos, sin) pairs) and scale it.
+__device__ __forceinline__ void rope_undo(float* g, const float4* cs, float scale) {
 #pragma unroll
   for (int q = 0; q < 16; ++q) {
     const int i = 2 * q;
@@ -429,7 +449,14 @@ __device__ __forceinline__ void store_grad_row(__nv_bfloat16* dst, float* g, con
     g[i + 1] = d1 * cs[q].z + d2 * cs[q].w;
     g[i + 33] = d2 * cs[q].z - d1 * cs[q].w;
   }
-  store_row64(dst, g);
+}
+// Row r of a 32-row x 64-column bf16 box with the 128-byte swizzle (16-byte
+// chunk j at chunk j ^ (r & 7) of the row) <- v[0..63]
+__device__ __forceinline__ void box_put_row64(uint32_t box, int r, const float* v) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    st_shared_v4(box + (uint32_t)r * 128u + ((uint32_t)(j ^ (r & 7)) << 4), pack2(v[8 * j], v[8 * j + 1]),
+                 pack2(v[8 * j + 2], v[8 * j + 3]), pack2(v[8 * j + 4], v[8 * j + 5]), pack2(v[8 * j + 6], v[8 * j + 7]));
 }
 
 namespace kv {   // dK/dV layout
@@ -576,6 +603,7 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
     const int q = warp - 4, r = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float sc_l2 = j.scale * LOG2E;
+    const uint64_t sc2 = f2(sc_l2, sc_l2);
     uint32_t c = 0, ni = 0;
     for (int it = first; it < items; it += G, ++ni) {
       int b, h, kb;
@@ -600,6 +628,11 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
         const float* sd = sl + 64;
         // queries q0 + x with q0 + x < key are masked (only the first two steps)
         const int lim = r - i * 64;            // x < lim is masked
+        if (i == 0) {
+          // the previous item's dK, dV bulk stores have read their staging rows
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+        }
         wait(B_(kv::PDEMPTY + sb), ((c >> 1) & 1) ^ 1, SITE_TC_EMPTY);
         const uint32_t pb = sbase + kv::P_OFF + sb * TILE, db = sbase + kv::DS_OFF + sb * TILE;
         // P^T and dS^T of the step; the mask only touches the first two steps,
@@ -611,19 +644,22 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
             uint32_t wp[4], wd[4];
             const float4 la = reinterpret_cast<const float4*>(sl)[2 * g], lb = reinterpret_cast<const float4*>(sl)[2 * g + 1];
             const float4 da = reinterpret_cast<const float4*>(sd)[2 * g], dbv = reinterpret_cast<const float4*>(sd)[2 * g + 1];
-            const float lv[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
-            const float dv[8] = {da.x, da.y, da.z, da.w, dbv.x, dbv.y, dbv.z, dbv.w};
+            const uint64_t z2 = f2(0.f, 0.f);
+            const uint64_t nl[4] = {sub2(z2, f2(la.x, la.y)), sub2(z2, f2(la.z, la.w)), sub2(z2, f2(lb.x, lb.y)),
+                                    sub2(z2, f2(lb.z, lb.w))};
+            const uint64_t dv[4] = {f2(da.x, da.y), f2(da.z, da.w), f2(dbv.x, dbv.y), f2(dbv.z, dbv.w)};
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
               const int x = g * 8 + e;
-              float p0 = ex2(fmaf(__uint_as_float(sv[x]), sc_l2, -lv[e]));
-              float p1 = ex2(fmaf(__uint_as_float(sv[x + 1]), sc_l2, -lv[e + 1]));
+              float t0, t1;
+              unf2(fma2(u2(sv[x], sv[x + 1]), sc2, nl[e >> 1]), t0, t1);
+              float p0 = ex2(t0), p1 = ex2(t1);
               if (MASK) {
                 if (x < lim) p0 = 0.f;
                 if (x + 1 < lim) p1 = 0.f;
               }
-              const float d0 = p0 * (__uint_as_float(dp[x]) - dv[e]);
-              const float d1 = p1 * (__uint_as_float(dp[x + 1]) - dv[e + 1]);
+              float d0, d1;
+              unf2(mul2(f2(p0, p1), sub2(u2(dp[x], dp[x + 1]), dv[e >> 1])), d0, d1);
               wp[e >> 1] = pack2(p0, p1);
               wd[e >> 1] = pack2(d0, d1);
             }
@@ -637,7 +673,17 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
         __syncwarp();
         if (lane == 0) mbar_arrive(B_(kv::PDFULL + sb));
       }
-      // dK, dV of the item's 128 keys
+      // dK, dV of the item's 128 keys: the key's rotary table row is loaded
+      // while the last products finish; the rows are staged in this warp's
+      // rows of P^T buffer 0 (dK) and dS^T buffer 0 (dV), free once every
+      // product of the item has completed, and written by bulk stores
+      const int key = kb * 128 + r;
+      float4 cs[16];
+      {
+        const float4* tab = reinterpret_cast<const float4*>(j.rope + (long long)key * 64);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) cs[x] = tab[x];
+      }
       wait(B_(kv::ACCFULL), ni & 1, SITE_TC_ACC_FULL);
       __syncwarp();
       tc_fence_after();
@@ -650,16 +696,28 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(B_(kv::ACCEMPTY));
-      const int key = kb * 128 + r;
-      __nv_bfloat16* row = j.dqkv + ((long long)b * j.S + key) * (3LL * j.hq);
+      const uint32_t bk = sbase + kv::P_OFF + (uint32_t)q * 4096u, bv = sbase + kv::DS_OFF + (uint32_t)q * 4096u;
       float g[64];
 #pragma unroll
       for (int x = 0; x < 64; ++x) g[x] = __uint_as_float(vk[x]);
-      store_grad_row(row + j.hq + h * HD, g, j.rope, key, j.scale);
+      rope_undo(g, cs, j.scale);
+      box_put_row64(bk, lane, g);
 #pragma unroll
       for (int x = 0; x < 64; ++x) g[x] = __uint_as_float(vv[x]);
-      store_row64(row + 2 * j.hq + h * HD, g);
+      box_put_row64(bv, lane, g);
+      fence_smem_async();
+      __syncwarp();
+      if (lane == 0 && !dead) {
+        const int y = b * j.S + kb * 128 + q * 32;
+        tma_store_2d(j.map_dqkv, bk, j.hq + h * HD, y);
+        tma_store_2d(j.map_dqkv, bv, 2 * j.hq + h * HD, y);
+        bulk_commit();
+      }
+      __syncwarp();
     }
+    // every dK, dV row has landed before the phase ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   __syncthreads();
   s.next(items);
@@ -671,8 +729,10 @@ constexpr uint32_t QD_OFF = 1024;                    // 2 x (Q 16 KB | dO 16 KB)
 constexpr uint32_t ST_OFF = QD_OFF + 4 * TILE;
 constexpr uint32_t ST_BYTES = 16384;
 constexpr uint32_t DS_OFF = ST_OFF + NST * ST_BYTES;  // 2 x dS (128 queries x 64 keys)
-constexpr uint32_t END = DS_OFF + 2 * TILE;
+constexpr uint32_t OUT_OFF = DS_OFF + 2 * TILE;   // 4 x 4 KB: each epilogue warp's dQ rows (bulk-store staging)
+constexpr uint32_t END = OUT_OFF + 4 * 4096;
 static_assert(END <= MT_TC_SMEM, "dQ tiles exceed the shared-memory window");
+static_assert(OUT_OFF % 1024 == 0, "swizzled staging needs 1024-byte alignment");
 enum { QFULL = 0, QEMPTY = 2, ACCFULL = 4, ACCEMPTY = 5, STFULL = 6, STEMPTY = STFULL + NST, SDFULL = STEMPTY + NST,
        SDEMPTY = SDFULL + 2, DSFULL = SDEMPTY + 2, DSEMPTY = DSFULL + 2, COUNT = DSEMPTY + 2 };
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256;
@@ -794,6 +854,7 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
     const int q = warp - 4, r = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float sc_l2 = j.scale * LOG2E;
+    const uint64_t sc2 = f2(sc_l2, sc_l2);
     uint32_t c = 0, ni = 0;
     for (int it = first; it < items; it += G, ++ni) {
       int b, h, qb;
@@ -802,6 +863,7 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
       const int query = qb * 128 + r;
       const long long lrow = ((long long)b * j.H + h) * j.S + query;
       const float lse2 = j.lse[lrow], dd = j.dsum[lrow];
+      const uint64_t nl2 = f2(-lse2, -lse2), dd2 = f2(dd, dd);
       for (int i = 0; i < nst; ++i, ++c) {
         const uint32_t sb = c & 1;
         wait(B_(qd::SDFULL + sb), (c >> 1) & 1, SITE_TC_ACC_FULL);
@@ -829,13 +891,16 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
               const int x = g * 8 + e;
-              float p0 = ex2(fmaf(__uint_as_float(sv[x]), sc_l2, -lse2));
-              float p1 = ex2(fmaf(__uint_as_float(sv[x + 1]), sc_l2, -lse2));
+              float t0, t1;
+              unf2(fma2(u2(sv[x], sv[x + 1]), sc2, nl2), t0, t1);
+              float p0 = ex2(t0), p1 = ex2(t1);
               if (MASK) {
                 if (x > lim) p0 = 0.f;
                 if (x + 1 > lim) p1 = 0.f;
               }
-              wd[e >> 1] = pack2(p0 * (__uint_as_float(dp[x]) - dd), p1 * (__uint_as_float(dp[x + 1]) - dd));
+              float d0, d1;
+              unf2(mul2(f2(p0, p1), sub2(u2(dp[x], dp[x + 1]), dd2)), d0, d1);
+              wd[e >> 1] = pack2(d0, d1);
             }
             st_shared_v4(db + p_chunk_off(r, g * 8), wd[0], wd[1], wd[2], wd[3]);
           }
@@ -859,8 +924,29 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
       float g[64];
 #pragma unroll
       for (int x = 0; x < 64; ++x) g[x] = __uint_as_float(vq[x]);
-      store_grad_row(j.dqkv + ((long long)b * j.S + query) * (3LL * j.hq) + h * HD, g, j.rope, query, j.scale);
+      float4 cs[16];
+      {
+        const float4* tab = reinterpret_cast<const float4*>(j.rope + (long long)query * 64);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) cs[x] = tab[x];
+      }
+      rope_undo(g, cs, j.scale);
+      // the previous item's bulk store has read the staging rows
+      const uint32_t bq = sbase + qd::OUT_OFF + (uint32_t)q * 4096u;
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
+      box_put_row64(bq, lane, g);
+      fence_smem_async();
+      __syncwarp();
+      if (lane == 0 && !dead) {
+        tma_store_2d(j.map_dqkv, bq, h * HD, b * j.S + qb * 128 + q * 32);
+        bulk_commit();
+      }
+      __syncwarp();
     }
+    // every dQ row has landed before the phase ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   __syncthreads();
   s.next(items);

@@ -2127,7 +2127,7 @@ __device__ __forceinline__ void run_attn_bwd(const KArgs& a, int l, Sched& s, ch
   if constexpr (sizeof(OP) == 2) {
     if (a.use_tm_attn) {
       const MtDims& D = a.D;
-      attn_tm::BwdJob j{&a.maps[MAP_QKV], &a.maps[MAP_DOUT], l * D.T,
+      attn_tm::BwdJob j{&a.maps[MAP_QKV], &a.maps[MAP_DOUT], &a.maps[MAP_E_DQKV], l * D.T,
                         abuf<float>(a, A_LSE) + (long long)l * D.B * D.H * D.S, abuf<float>(a, A_DSUM),
                         abuf<__nv_bfloat16>(a, A_DQKV), abuf<float>(a, A_ROPE), D.B, D.H, D.S, D.hq,
                         1.0f / sqrtf((float)D.hd), dp.hdr, dp.timeout_ns};

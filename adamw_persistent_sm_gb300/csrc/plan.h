@@ -79,6 +79,7 @@ enum MapId {
   // 64-byte swizzle, fp32 with the 128-byte swizzle
   MAP_E_QKV, MAP_E_GU, MAP_E_ACT, MAP_E_DGU, MAP_E_DLOGITS, MAP_E_DO, MAP_E_O,
   MAP_E_Y, MAP_E_DRF, MAP_E_DXS, MAP_E_DR, MAP_E_XM, MAP_E_X,
+  MAP_E_DQKV,   // 32 rows x 64 columns, 128-byte swizzle: the attention backward's dq, dk, dv rows
   MAP_COUNT
 };
 static_assert(MAP_COUNT <= MT_NMAPS, "too many tensor maps");
