@@ -40,7 +40,8 @@ constexpr uint32_t K_OFF = Q_OFF + 2 * TILE;     // KST x K tile
 constexpr uint32_t V_OFF = K_OFF + KST * TILE;   // KST x V tile
 constexpr uint32_t P_OFF = V_OFF + KST * TILE;   // 2 x P (128 rows x 128 keys bf16: two 16 KB boxes)
 constexpr uint32_t P_BUF = 2 * TILE;
-constexpr uint32_t SMEM_END = P_OFF + 2 * P_BUF;
+constexpr uint32_t OUT_OFF = P_OFF + 2 * P_BUF;   // 4 x 4 KB: each softmax warp's output rows (bulk-store staging)
+constexpr uint32_t SMEM_END = OUT_OFF + 4 * 4096;
 static_assert(SMEM_END <= MT_TC_SMEM, "attention tiles exceed the shared-memory window");
 
 // mbarrier slots (8 bytes each)
@@ -54,6 +55,7 @@ constexpr uint32_t TM_S = 0, TM_PV = 256;
 
 struct Job {
   const CUtensorMap* map;    // q,k,v of all layers: rows l*T + t, columns [q | k | v]
+  const CUtensorMap* map_o;  // o of all layers, 32-row x 64-column boxes (bulk stores)
   int y0;                    // row of token 0 of this layer
   __nv_bfloat16* o;          // [T][hq]
   float* lse;                // [B*H][S]
@@ -111,6 +113,42 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Packed pairs of fp32 (the two-wide fp32 instructions of this architecture;
+// each lane rounds as the scalar instruction does).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t u2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, const TcState& tc) {
@@ -251,6 +289,7 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
     const int r = q * 32 + lane;                           // row within the item, TMEM lane
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float sc_l2 = j.scale * LOG2E;
+    const uint64_t sc2 = f2(sc_l2, sc_l2);
     uint32_t sc = 0;
     bool dead = false;
     auto wait = [&](uint32_t b_, uint32_t par, int site) {
@@ -268,8 +307,9 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
       tmem_ld32_async(tp, v);
       tmem_ld32_async(tp + 32, v + 32);
       tmem_wait_ld();
+      const uint64_t al2 = f2(alpha, alpha);
 #pragma unroll
-      for (int i = 0; i < HD; ++i) o[i] = fmaf(o[i], alpha, __uint_as_float(v[i]));
+      for (int i = 0; i < HD; i += 2) unf2(fma2(f2(o[i], o[i + 1]), al2, u2(v[i], v[i + 1])), o[i], o[i + 1]);
       m_o = mc;
       tc_fence_before();
       __syncwarp();
@@ -312,9 +352,10 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
         const float mn = fmaxf(m, mx * sc_l2);
         // probabilities against the new maximum (eight partial row sums) and
         // the bf16 P tile
-        float rs8[8];
+        uint64_t rs2[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) rs8[u] = 0.f;
+        for (int u = 0; u < 4; ++u) rs2[u] = f2(0.f, 0.f);
+        const uint64_t nmn2 = f2(-mn, -mn);
         const uint32_t pbase = sbase + P_OFF + sb * P_BUF;
 #pragma unroll
         for (int c = 0; c < BKEY / 32; ++c) {
@@ -322,15 +363,19 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             const int k = c * 32 + i;
-            const float p0 = ex2(fmaf(__uint_as_float(sr[k]), sc_l2, -mn));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[k + 1]), sc_l2, -mn));
-            rs8[(k >> 1) & 7] += p0 + p1;
+            float t0, t1;
+            unf2(fma2(u2(sr[k], sr[k + 1]), sc2, nmn2), t0, t1);
+            const float p0 = ex2(t0), p1 = ex2(t1);
+            rs2[(k >> 1) & 3] = add2(rs2[(k >> 1) & 3], f2(p0, p1));
             w[i >> 1] = pack2(p0, p1);
           }
 #pragma unroll
           for (int g = 0; g < 4; ++g)
             st_shared_v4(pbase + p_chunk_off(r, c * 32 + g * 8), w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
         }
+        float rs8[8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) unf2(rs2[u], rs8[2 * u], rs8[2 * u + 1]);
         const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         // the S buffer is read and the P tile written (generic proxy -> tensor core)
         tc_fence_before();
@@ -348,19 +393,35 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
       add_pv(o, m_o, sc - 1, m);                   // the item's last block
       // normalise, store the output row and the log-sum-exp
       const float inv = 1.f / lsum;
-      const long long t = (long long)b * j.S + qb * BQ + r;
-      uint4* dst = reinterpret_cast<uint4*>(j.o + t * j.hq + h * HD);
+#pragma unroll
+      for (int i = 0; i < HD; ++i) o[i] *= inv;
+      // the output rows go out by one bulk store per warp (the previous
+      // item's store has read the staging rows first)
+      const uint32_t ob = sbase + OUT_OFF + (uint32_t)q * 4096u;
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
 #pragma unroll
       for (int g = 0; g < HD / 8; ++g)
-        dst[g] = make_uint4(pack2(o[8 * g] * inv, o[8 * g + 1] * inv), pack2(o[8 * g + 2] * inv, o[8 * g + 3] * inv),
-                            pack2(o[8 * g + 4] * inv, o[8 * g + 5] * inv), pack2(o[8 * g + 6] * inv, o[8 * g + 7] * inv));
+        st_shared_v4(ob + (uint32_t)lane * 128u + ((uint32_t)(g ^ (lane & 7)) << 4), pack2(o[8 * g], o[8 * g + 1]),
+                     pack2(o[8 * g + 2], o[8 * g + 3]), pack2(o[8 * g + 4], o[8 * g + 5]), pack2(o[8 * g + 6], o[8 * g + 7]));
+      fence_smem_async();
+      __syncwarp();
+      if (lane == 0 && !dead) {
+        tma_store_2d(j.map_o, ob, h * HD, j.y0 + b * j.S + qb * BQ + q * 32);
+        bulk_commit();
+      }
       j.lse[((long long)b * j.H + h) * j.S + qb * BQ + r] = m + log2f(lsum);   // log2 units
       if (j.sig) {
         // every row of the block is stored: publish it
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
         asm volatile("bar.sync 2, 128;" ::: "memory");
         if (threadIdx.x == 128) dep_signal(j.sig + b * nqb + qb);
       }
     }
+    // every output row has landed before the phase ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   __syncthreads();
   s.next(items);
@@ -402,37 +463,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
-}
-
-// Packed pairs of fp32 (the two-wide fp32 instructions of this architecture;
-// each lane rounds as the scalar instruction does).
-__device__ __forceinline__ uint64_t f2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ uint64_t u2(uint32_t lo, uint32_t hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-  return r;
-}
-__device__ __forceinline__ void unf2(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
 }
 
 // Undo the rotary embedding on a 64-wide gradient row (dims i and i + 32

@@ -2109,7 +2109,7 @@ __device__ __forceinline__ void run_attn_fwd(const KArgs& a, int l, Sched& s, ch
   if constexpr (sizeof(OP) == 2) {
     if (a.use_tm_attn) {
       const MtDims& D = a.D;
-      attn_tm::Job j{&a.maps[MAP_QKV], l * D.T, abuf<__nv_bfloat16>(a, A_O) + (long long)l * D.T * D.hq,
+      attn_tm::Job j{&a.maps[MAP_QKV], &a.maps[MAP_E_OROW], l * D.T, abuf<__nv_bfloat16>(a, A_O) + (long long)l * D.T * D.hq,
                      abuf<float>(a, A_LSE) + (long long)l * D.B * D.H * D.S, D.B, D.H, D.S, D.hq,
                      1.0f / sqrtf((float)D.hd), dp.wait, dp.wtarget, dp.sig, dp.hdr, dp.timeout_ns};
       attn_tm::fwd_job(j, s, smem, tc);

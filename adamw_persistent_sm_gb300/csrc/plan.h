@@ -10,7 +10,7 @@
 #include <cuda.h>
 
 #define MT_TILE_M 128           // routing pads each expert segment to this many rows
-#define MT_NMAPS 32
+#define MT_NMAPS 40
 
 // parameter tensors, in flat-buffer order
 enum ParamId {
@@ -80,6 +80,7 @@ enum MapId {
   MAP_E_QKV, MAP_E_GU, MAP_E_ACT, MAP_E_DGU, MAP_E_DLOGITS, MAP_E_DO, MAP_E_O,
   MAP_E_Y, MAP_E_DRF, MAP_E_DXS, MAP_E_DR, MAP_E_XM, MAP_E_X,
   MAP_E_DQKV,   // 32 rows x 64 columns, 128-byte swizzle: the attention backward's dq, dk, dv rows
+  MAP_E_OROW,   // 32 rows x 64 columns, 128-byte swizzle: the attention forward's output rows
   MAP_COUNT
 };
 static_assert(MAP_COUNT <= MT_NMAPS, "too many tensor maps");

@@ -357,6 +357,25 @@ def run_trace(args, cfg):
     print(f"  {'job':16s} {'mean ms':>9s} {'max-over-CTAs ms':>18s}")
     for k in sorted(mx, key=lambda k: -mx[k]):
         print(f"  {k:16s} {mean[k]:9.3f} {mx[k]:18.3f}")
+    # grid-barrier waits (arrival to release, mean over CTAs), grouped by the
+    # job that ran before each barrier
+    bars = tv[:out.n_ctas, :2 * B.MT_TRACE_PHASES].reshape(out.n_ctas, B.MT_TRACE_PHASES, 2).astype(np.float64)
+    nb = min(out.n_phases, B.MT_TRACE_PHASES)
+    waits = (bars[:, :nb, 1] - bars[:, :nb, 0]).mean(axis=0) / 1e6
+    before, last, k = {}, "start", 0
+    for jid in ids:
+        if int(jid) == 0:
+            if k < nb:
+                before[k] = last
+            k += 1
+        else:
+            last = JOB_NAMES.get(int(jid), str(int(jid)))
+    by = {}
+    for p_, w in enumerate(waits):
+        by[before.get(p_, "?")] = by.get(before.get(p_, "?"), 0.0) + w
+    print(f"  barrier wait by the job before the barrier ({nb} barriers, {waits.sum():.3f} ms):")
+    for k_ in sorted(by, key=lambda k_: -by[k_])[:12]:
+        print(f"    {k_:16s} {by[k_]:9.3f}")
 
 
 def run_product(args):
