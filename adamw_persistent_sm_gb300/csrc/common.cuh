@@ -23,6 +23,7 @@ enum ErrSite {
   SITE_TC_ALIGN = 15,
   SITE_DEP = 16,
   SITE_TC_EPI = 17,
+  SITE_TC_QUEUE = 18,
   SITE_TEST_STALL = 20
 };
 

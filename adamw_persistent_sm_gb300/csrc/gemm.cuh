@@ -78,6 +78,10 @@ struct GemmDesc {
   // the product is row y0 + m of the map.
   int omap, omap2, amap;
   int oy0, oy02, ay0;
+  // Tile order (tensor-core path): null - tile t on CTA (t + base) % G;
+  // else tiles are drawn from this counter (zero at the start of the launch)
+  // by the CTAs as they become free.
+  unsigned* ticket;
 };
 
 // Target column of logits row m (next token), or -1 for the last position.

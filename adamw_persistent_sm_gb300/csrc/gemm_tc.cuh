@@ -28,6 +28,10 @@
 #define TC_EPI_WARP_BYTES 8192                                    // one window per epilogue warp
 #define TC_EPI_SLOT 2048                                          // one 32x32 bf16 box
 #define TC_EPI_MBAR 512                                           // aux-load mbarriers (2 per warp)
+#define TC_Q_SLOTS 4                                              // drawn-tile queue: producer -> MMA, epilogue
+#define TC_Q_IDX 160                                              // tile indices (int per slot)
+#define TC_Q_FULL 576                                             // mbarriers: index written
+#define TC_Q_EMPTY 608                                            // mbarriers: index read by MMA + 4 epilogue warps
 #define TC_XPOSE_BYTES (32 * 33 * 4)                              // 32x32 fp32 transpose tile
 #define MT_TC_SMEM (TC_STAGE_OFF + 4 * TC_EPI_WARP_BYTES)
 static_assert(TC_XPOSE_BYTES <= TC_EPI_WARP_BYTES, "transpose tile exceeds the epilogue window");
@@ -1016,6 +1020,52 @@ __device__ __forceinline__ void epi_signal(unsigned* c) {
   if (threadIdx.x == 128) dep_signal(c);
 }
 
+// The tiles a role of this CTA works on, in order.  Static: first, first+G,
+// ...  Drawn: the producer takes the next ticket for every tile and passes
+// it through a TC_Q_SLOTS-entry shared-memory queue (mbarrier hand-off); the
+// MMA issuer and the epilogue warps read the same sequence.  -1 ends it.
+struct TileSeq {
+  unsigned* ticket;
+  uint32_t sbase;
+  int items, G, t, k;
+  bool producer;
+  // next tile; false at the end of the sequence or after a timed-out wait
+  __device__ __forceinline__ bool next(int& tile, ArenaHdr* hdr, long long tmo, int lane) {
+    if (!ticket) {
+      if (k++ > 0) t += G;
+      tile = t;
+      return t < items;
+    }
+    const uint32_t slot = (uint32_t)(k % TC_Q_SLOTS), par = (uint32_t)(k / TC_Q_SLOTS) & 1u;
+    const uint32_t idx = sbase + TC_Q_IDX + 4u * slot;
+    ++k;
+    int v = -1;
+    bool ok = true;
+    if (producer) {
+      // lane 0 alone
+      if (!mbar_wait(sbase + TC_Q_EMPTY + 8u * slot, par ^ 1u, tmo)) {
+        set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_QUEUE);
+        ok = false;
+      } else {
+        v = (int)atomicAdd(ticket, 1u);
+        if (v >= items) v = -1;
+      }
+      asm volatile("st.shared.b32 [%0], %1;" ::"r"(idx), "r"(v) : "memory");
+      mbar_arrive(sbase + TC_Q_FULL + 8u * slot);
+    } else {
+      if (!mbar_wait(sbase + TC_Q_FULL + 8u * slot, par, tmo)) {
+        set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_QUEUE);
+        ok = false;
+      } else {
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(idx) : "memory");
+      }
+      if (lane == 0) mbar_arrive(sbase + TC_Q_EMPTY + 8u * slot);
+    }
+    tile = v;
+    return ok && v >= 0;
+  }
+};
+
 static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& g, Sched& s, char* smem, TcState& tc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
@@ -1038,6 +1088,10 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
       mbar_init(acce + 8 * i, 4);
     }
     for (int i = 0; i < 8; ++i) mbar_init(sbase + TC_EPI_MBAR + 8 * i, 1);
+    for (int i = 0; i < TC_Q_SLOTS; ++i) {
+      mbar_init(sbase + TC_Q_FULL + 8 * i, 1);
+      mbar_init(sbase + TC_Q_EMPTY + 8 * i, 5);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -1045,6 +1099,7 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
   const TcShape sh = tc_shape(g);
   const int items = gemm_items(g, TC_BM, TC_BN) * sh.ksplit;
   const int first = s.first(), G = s.G;
+  TileSeq seq{g.ticket, sbase, items, G, first, 0, warp == 0};
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1055,7 +1110,8 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
       const unsigned dtarget = g.dtarget;
       uint32_t it = 0;
       bool ok = true;
-      for (int t = first; t < items && ok; t += G) {
+      int t;
+      while (ok && seq.next(t, hdr, tmo, lane)) {
         const TcTile ti = tc_tile(sh, t);
         const int bseg = (sh.rag == RAG_M) ? ti.seg * ob.yseg : 0;
         if (dw) {
@@ -1099,7 +1155,8 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
       uint32_t it = 0, tcount = 0;
       bool ok = true;
       uint32_t last_bar = 0, last_par = 0;
-      for (int t = first; t < items && ok; t += G) {
+      int t;
+      while (ok && seq.next(t, hdr, tmo, lane)) {
         const TcTile ti = tc_tile(sh, t);
         if (ti.nk == 0) continue;
         const int ab = tcount & 1;
@@ -1153,7 +1210,19 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
     const unsigned dta = g.dtarget_aux;
     uint32_t tcount = 0;
     bool dead = false;     // after a timed-out wait: skip the work, keep the named barriers paired
-    for (int t = first; t < items; t += G) {
+    int t;
+    while (true) {
+      // a drawn sequence is read by lane 0 and shared with the warp
+      int tt = -1;
+      bool more = false;
+      if (lane == 0) more = seq.next(tt, hdr, tmo, 0);
+      else if (!seq.ticket) more = seq.next(tt, hdr, tmo, lane);
+      if (seq.ticket) {
+        more = __shfl_sync(0xffffffffu, more, 0);
+        tt = __shfl_sync(0xffffffffu, tt, 0);
+      }
+      if (!more) break;
+      t = tt;
       const TcTile ti = tc_tile(sh, t);
       const int m = ti.m0 + q * 32 + lane;
       if (dwa) {

@@ -1871,6 +1871,7 @@ struct Gemms {
     g.tok = nullptr; g.cepart = nullptr; g.cetgt = nullptr; g.ceparts = 0; g.ksplit = 1;
     g.dwait = nullptr; g.dtarget = 0; g.dwait_aux = nullptr; g.dtarget_aux = 0; g.dsig = nullptr;
     g.omap = g.omap2 = g.amap = -1; g.oy0 = g.oy02 = g.ay0 = 0;
+    g.ticket = nullptr;
     return g;
   }
   __device__ const int* offs(int l) const { return abuf<int>(a, A_OFFS) + (long long)l * (D.E + 1); }
@@ -2198,13 +2199,18 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     return dp;
   };
   const unsigned rn_target = MT_TILE_M / MT_DEP_GROUP;
+  // tensor-core products draw their tiles (longest products first in a phase)
+  auto TK = [&](GemmDesc g, int l, int id) {
+    g.ticket = depc + ticket_offset(D, l, id);
+    return g;
+  };
 
   // ---------------- forward ----------------
   job_embed<OP>(a, s); TJ(1);
   MT_SYNC();
   for (int l = 0; l < D.L; ++l) {
     {
-      GemmDesc g = gm.qkv(l);
+      GemmDesc g = TK(gm.qkv(l), l, TK_QKV);
       if (dep) {
         if (l > 0) { g.dwait = DEPC(l - 1, DEP_RN); g.dtarget = rn_target; }
         g.dsig = DEPC(l, DEP_QKV);
@@ -2215,7 +2221,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     run_attn_fwd<OP>(a, l, s, smem, tc, attn_deps(l, TK_ATTN_FWD, true)); TJ(3);
     if (!dep) MT_SYNC();
     {
-      GemmDesc g = gm.wo(l);
+      GemmDesc g = TK(gm.wo(l), l, TK_WO);
       if (dep) {
         g.dwait = DEPC(l, DEP_O); g.dtarget = (unsigned)D.H;
         if (l > 0) { g.dwait_aux = DEPC(l - 1, DEP_RN); g.dtarget_aux = rn_target; }
@@ -2229,13 +2235,13 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     job_route<OP>(a, l, smem); TJ(6);
     MT_SYNC();
     {
-      GemmDesc g = gm.gateup(l);
+      GemmDesc g = TK(gm.gateup(l), l, TK_GATEUP);
       if (dep) g.dsig = DEPC(l, DEP_ACT);
       run_gemm<OP>(a, g, s, smem, tc); TJ(7);
     }
     if (!dep) MT_SYNC();
     {
-      GemmDesc g = gm.down(l);
+      GemmDesc g = TK(gm.down(l), l, TK_DOWN);
       if (dep) { g.dwait = DEPC(l, DEP_ACT); g.dtarget = (unsigned)(2 * D.F / TC_BN); }
       run_gemm<OP>(a, g, s, smem, tc); TJ(8);
     }
@@ -2244,7 +2250,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     if (!dep) MT_SYNC();
   }
   {
-    GemmDesc g = gm.lm();
+    GemmDesc g = TK(gm.lm(), D.L, TK_LM);
     if (dep) { g.dwait = DEPC(D.L - 1, DEP_RN); g.dtarget = rn_target; }
     run_gemm<OP>(a, g, s, smem, tc); TJ(10);
   }
@@ -2254,8 +2260,8 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
 
   // ---------------- backward ----------------
   job_loss(a); TJ(12);
-  run_gemm<OP>(a, gm.lm_dgrad(), s, smem, tc); TJ(13);
-  run_gemm<OP>(a, gm.lm_wgrad(), s, smem, tc); TJ(14);
+  run_gemm<OP>(a, TK(gm.lm_wgrad(), D.L, TK_LM_WGRAD), s, smem, tc); TJ(14);
+  run_gemm<OP>(a, TK(gm.lm_dgrad(), D.L, TK_LM_DGRAD), s, smem, tc); TJ(13);
   MT_SYNC();
   // the norm-gain gradients: per-CTA partials (PART row E+1) left by the
   // norm backward jobs, summed in CTA order by job_colfinal
@@ -2267,27 +2273,27 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     if (l == D.L - 1) job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_FINAL_NORM), nullptr, 0, s, (int)G);
     else job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM) + (long long)(l + 1) * D.d, nullptr, 0, s, (int)G);
     TJ(18);
-    run_gemm<OP>(a, gm.down_dgrad(l), s, smem, tc); TJ(19);
-    run_gemm<OP>(a, gm.down_wgrad(l), s, smem, tc); TJ(20);
+    run_gemm<OP>(a, TK(gm.down_wgrad(l), l, TK_DOWN_WGRAD), s, smem, tc); TJ(20);
+    run_gemm<OP>(a, TK(gm.down_dgrad(l), l, TK_DOWN_DGRAD), s, smem, tc); TJ(19);
     MT_SYNC();
-    run_gemm<OP>(a, gm.gateup_dgrad(l), s, smem, tc); TJ(21);
-    run_gemm<OP>(a, gm.gateup_wgrad(l), s, smem, tc); TJ(22);
+    run_gemm<OP>(a, TK(gm.gateup_wgrad(l), l, TK_GU_WGRAD), s, smem, tc); TJ(22);
+    run_gemm<OP>(a, TK(gm.gateup_dgrad(l), l, TK_GU_DGRAD), s, smem, tc); TJ(21);
     MT_SYNC();
     job_moe_bwd2<OP>(a, l, s, smem); TJ(23);
     MT_SYNC();
     // router-weight gradient partials (rows 0..E-1); the expert-norm gain
     // partial was left by job_moe_bwd2
     const int rg_chunks = job_router_grad(a, l, s, smem); TJ(16);
-    run_gemm<OP>(a, gm.wo_dgrad(l), s, smem, tc); TJ(24);
-    run_gemm<OP>(a, gm.wo_wgrad(l), s, smem, tc); TJ(25);
+    run_gemm<OP>(a, TK(gm.wo_wgrad(l), l, TK_WO_WGRAD), s, smem, tc); TJ(25);
+    run_gemm<OP>(a, TK(gm.wo_dgrad(l), l, TK_WO_DGRAD), s, smem, tc); TJ(24);
     MT_SYNC();
     job_colfinal(a, 0, D.E, D.E, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d, nullptr, 0, s, rg_chunks);
     job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_MOE_NORM) + (long long)l * D.d, nullptr, 0, s, (int)G); TJ(18);
     job_ksplit_sum(a, pgrad(a, P_WO) + (long long)l * D.d * D.hq, D.d, D.hq, s); TJ(32);
     run_attn_bwd<OP>(a, l, s, smem, tc, attn_deps(l, TK_ATTN_BWD, false), [&] { TJ(35); }); TJ(26);
     MT_SYNC();
-    run_gemm<OP>(a, gm.qkv_dgrad(l), s, smem, tc); TJ(27);
-    run_gemm<OP>(a, gm.qkv_wgrad(l), s, smem, tc); TJ(28);
+    run_gemm<OP>(a, TK(gm.qkv_wgrad(l), l, TK_QKV_WGRAD), s, smem, tc); TJ(28);
+    run_gemm<OP>(a, TK(gm.qkv_dgrad(l), l, TK_QKV_DGRAD), s, smem, tc); TJ(27);
     MT_SYNC();
     job_attn_norm_bwd<OP>(a, l, s, smem); TJ(29);
     job_ksplit_sum(a, pgrad(a, P_WQKV) + (long long)l * 3 * D.hq * D.d, 3 * D.hq, D.d, s); TJ(33);
@@ -2327,6 +2333,7 @@ __device__ void run_debug_gemm(const KArgs& a, char* smem, TcState& tc, Sched& s
   g.tok = nullptr; g.cepart = nullptr; g.cetgt = nullptr; g.ceparts = 0; g.ksplit = 1;
   g.dwait = nullptr; g.dtarget = 0; g.dwait_aux = nullptr; g.dtarget_aux = 0; g.dsig = nullptr;
   g.omap = g.omap2 = g.amap = -1; g.oy0 = g.oy02 = g.ay0 = 0;
+  g.ticket = nullptr;
   if (a.dbg_tma && g.rag != RAG_K && a.dbg_out_mode < 2) g.omap = a.dbg_out_mode == 1 ? MAP_E_QKV : MAP_E_Y;
   GOperand A, B;
   A.p0 = a.dbg_a; A.p1 = nullptr; A.mn = a.dbg_a_mn; A.ld = A.mn ? g.M : g.K; A.seg = 0; A.two = 0;

@@ -119,8 +119,16 @@ enum DepKind {
   DEP_KINDS
 };
 #define MT_DEP_GROUP 32         // tokens per combine item when counters are on
-#define MT_TICKETS 8            // ticket counters per layer (plus one set for the head)
-enum TicketId { TK_ATTN_FWD = 0, TK_ATTN_BWD, TK_ADAMW };
+#define MT_TICKETS 16           // ticket counters per layer (plus one set for the head)
+// Work tickets.  Per layer: the attention jobs and every tensor-core product
+// (tiles drawn in index order by whichever CTA is free); the head's set (layer
+// index L) holds the LM-head products and the optimizer sweep.
+enum TicketId {
+  TK_ATTN_FWD = 0, TK_ATTN_BWD, TK_ADAMW,
+  TK_QKV, TK_WO, TK_GATEUP, TK_DOWN,
+  TK_DOWN_DGRAD, TK_DOWN_WGRAD, TK_GU_DGRAD, TK_GU_WGRAD, TK_WO_DGRAD, TK_WO_WGRAD, TK_QKV_DGRAD, TK_QKV_WGRAD,
+  TK_LM = TK_QKV, TK_LM_DGRAD = TK_WO, TK_LM_WGRAD = TK_GATEUP
+};
 __host__ __device__ inline long long dep_blocks(const MtDims& D, int kind) {
   return kind == DEP_ACT ? D.Pmax / MT_TILE_M : (D.T + MT_TILE_M - 1) / MT_TILE_M;
 }
