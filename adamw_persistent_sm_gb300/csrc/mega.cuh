@@ -133,7 +133,8 @@ __device__ __forceinline__ void warp_argmax(float& v, int& idx) {
 // top-k compares these fp32 logits (softmax is monotone), ties going to the
 // lower expert index.
 template <class OP>
-__device__ __noinline__ void job_router(const KArgs& a, int l, char* smem, const unsigned* dw, unsigned dtarget) {
+__device__ __noinline__ void job_router(const KArgs& a, int l, char* smem, const unsigned* dw, unsigned dtarget,
+                                        long long* wait_stamp) {
   const MtDims& D = a.D;
   const int c = blockIdx.x, G = gridDim.x;
   const int ch = chunk_len(D, G);
@@ -168,6 +169,11 @@ __device__ __noinline__ void job_router(const KArgs& a, int l, char* smem, const
     if (threadIdx.x < nb) dep_wait(abuf<ArenaHdr>(a, A_HDR), dw + b0 + threadIdx.x, dtarget, a.timeout_ns);
   }
   __syncthreads();
+  if (wait_stamp && threadIdx.x == 0) {
+    // trace: the end of the wait for the out-projection tiles
+    wait_stamp[0] = (long long)globaltimer();
+    wait_stamp[1] = 36;
+  }
   if (p.ns > 0 && lane == 0) asm volatile("fence.proxy.async;" ::: "memory");   // after the acquire
   const int n4 = D.d / 4;
   bool ok = true;
@@ -668,22 +674,32 @@ __device__ __noinline__ void job_ce(const KArgs& a, Sched& s, char* smem) {
         if (ok) {
           const uint32_t st = p.stage(j);
           const int nu = (int)(nbytes(j) / 16u), c0 = k * CK;
+          // coef exp(x - lse) = 2^(x log2 e + (log2 coef - lse log2 e)): one
+          // two-wide FMA per pair of logits and the special-function unit's
+          // 2^x; a row without a target gets zeros
+          const float sh = has ? log2f(a.coef) - lse * EPI_LOG2E : -INFINITY;
+          const uint64_t l2e2 = attn_tm::f2(EPI_LOG2E, EPI_LOG2E), sh2 = attn_tm::f2(sh, sh);
+          const int tu = (target - c0) >> 3;     // the 16-byte group holding the target (if any)
           for (int u = lane; u < nu; u += 32) {
             uint4 q;
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w) : "r"(st + 16u * u));
             const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-            uint32_t o[4];
+            float pv[8];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-              const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[h]));
-              float p0 = has ? a.coef * __expf(x.x - lse) : 0.f, p1 = has ? a.coef * __expf(x.y - lse) : 0.f;
-              const int col = c0 + 8 * u + 2 * h;
-              if (target == col) p0 -= a.coef;
-              if (target == col + 1) p1 -= a.coef;
-              __nv_bfloat162 r = __floats2bfloat162_rn(p0, p1);
-              o[h] = *reinterpret_cast<uint32_t*>(&r);
+              float t0, t1;
+              attn_tm::unf2(attn_tm::fma2(attn_tm::f2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u)),
+                                          l2e2, sh2), t0, t1);
+              pv[2 * h] = epi_ex2(t0);
+              pv[2 * h + 1] = epi_ex2(t1);
             }
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(st + 16u * u), "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]) : "memory");
+            if (u == tu && target >= 0) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (c0 + 8 * u + i == target) pv[i] -= a.coef;
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(st + 16u * u), "r"(bf2(pv[0], pv[1])),
+                         "r"(bf2(pv[2], pv[3])), "r"(bf2(pv[4], pv[5])), "r"(bf2(pv[6], pv[7])) : "memory");
           }
           // the dlogits of the stage are read by the bulk store (async proxy)
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -2230,7 +2246,11 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
       run_gemm<OP>(a, g, s, smem, tc); TJ(4);
     }
     if (!dep) MT_SYNC();
-    job_router<OP>(a, l, smem, dep ? DEPC(l, DEP_XMID) : nullptr, (unsigned)(D.d / TC_BN)); TJ(5);
+    {
+      long long* ws = (tr && nj < MT_TRACE_JOBS) ? tr + 2 * MT_TRACE_PHASES + 2 * nj : nullptr;
+      if (tr) ++nj;
+      job_router<OP>(a, l, smem, dep ? DEPC(l, DEP_XMID) : nullptr, (unsigned)(D.d / TC_BN), ws); TJ(5);
+    }
     MT_SYNC();
     job_route<OP>(a, l, smem); TJ(6);
     MT_SYNC();

@@ -319,7 +319,7 @@ JOB_NAMES = {0: "barrier wait", 1: "embed", 2: "qkv", 3: "attn_fwd", 4: "wo", 5:
              19: "down_dgrad", 20: "down_wgrad", 21: "gateup_dgrad", 22: "gateup_wgrad", 23: "moe_bwd2",
              24: "wo_dgrad", 25: "wo_wgrad", 26: "attn_bwd_dq", 27: "qkv_dgrad", 28: "qkv_wgrad",
              29: "attn_norm_bwd", 30: "embed_bwd", 31: "norm_partial", 32: "wo_ksum", 33: "qkv_ksum",
-             34: "adamw", 35: "attn_bwd_dkdv"}
+             34: "adamw", 35: "attn_bwd_dkdv", 36: "router_wait"}
 
 
 def _sched_flags(args):
