@@ -678,7 +678,7 @@ __device__ __noinline__ void job_ce(const KArgs& a, Sched& s, char* smem) {
           // two-wide FMA per pair of logits and the special-function unit's
           // 2^x; a row without a target gets zeros
           const float sh = has ? log2f(a.coef) - lse * EPI_LOG2E : -INFINITY;
-          const uint64_t l2e2 = attn_tm::f2(EPI_LOG2E, EPI_LOG2E), sh2 = attn_tm::f2(sh, sh);
+          const uint64_t l2e2 = f2(EPI_LOG2E, EPI_LOG2E), sh2 = f2(sh, sh);
           const int tu = (target - c0) >> 3;     // the 16-byte group holding the target (if any)
           for (int u = lane; u < nu; u += 32) {
             uint4 q;
@@ -688,7 +688,7 @@ __device__ __noinline__ void job_ce(const KArgs& a, Sched& s, char* smem) {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
               float t0, t1;
-              attn_tm::unf2(attn_tm::fma2(attn_tm::f2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u)),
+              unf2(fma2(f2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u)),
                                           l2e2, sh2), t0, t1);
               pv[2 * h] = epi_ex2(t0);
               pv[2 * h + 1] = epi_ex2(t1);
@@ -815,13 +815,11 @@ __device__ __noinline__ void job_ce(const KArgs& a, Sched& s, char* smem) {
 // them as PART[cta][E+1][:]; a later phase sums the CTAs in CTA order.
 template <int NC>
 __device__ __forceinline__ void row_gain_acc(Row<NC>& acc, const Row<NC>& dy, const Row<NC>& x, float inv) {
+  const uint64_t i2 = f2(inv, inv);
 #pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    acc.v[i].x = fmaf(dy.v[i].x, x.v[i].x * inv, acc.v[i].x);
-    acc.v[i].y = fmaf(dy.v[i].y, x.v[i].y * inv, acc.v[i].y);
-    acc.v[i].z = fmaf(dy.v[i].z, x.v[i].z * inv, acc.v[i].z);
-    acc.v[i].w = fmaf(dy.v[i].w, x.v[i].w * inv, acc.v[i].w);
-  }
+  for (int i = 0; i < NC; ++i)
+    acc.v[i] = join2(fma2(lo2(dy.v[i]), mul2(lo2(x.v[i]), i2), lo2(acc.v[i])),
+                     fma2(hi2(dy.v[i]), mul2(hi2(x.v[i]), i2), hi2(acc.v[i])));
 }
 template <int NC>
 __device__ __forceinline__ void gain_partial_store(const KArgs& a, const Row<NC>& acc, char* smem) {

@@ -95,7 +95,7 @@ __device__ __forceinline__ void row_add_lds(Row<NC>& r, uint32_t a, int n4) {
     const int c = l + 32 * i;
     if (c < n4) {
       const float4 v = lds4(a + 16u * (uint32_t)c);
-      r.v[i].x += v.x; r.v[i].y += v.y; r.v[i].z += v.z; r.v[i].w += v.w;
+      r.v[i] = join2(add2(lo2(r.v[i]), lo2(v)), add2(hi2(r.v[i]), hi2(v)));
     }
   }
 }

@@ -70,89 +70,97 @@ __device__ __forceinline__ void row_st_op(__nv_bfloat16* p, const Row<NC>& r, in
     }
   }
 }
+// The arithmetic below runs on two-wide fp32 instructions: each float4 chunk
+// is two (x, y), (z, w) pairs.  Elementwise results equal the scalar ones;
+// dot products keep two partial sums (even and odd columns) per lane.
+__device__ __forceinline__ uint64_t lo2(const float4& v) { return f2(v.x, v.y); }
+__device__ __forceinline__ uint64_t hi2(const float4& v) { return f2(v.z, v.w); }
+__device__ __forceinline__ float4 join2(uint64_t lo, uint64_t hi) {
+  float4 r;
+  unf2(lo, r.x, r.y);
+  unf2(hi, r.z, r.w);
+  return r;
+}
+__device__ __forceinline__ float sum2(uint64_t v) {
+  float a, b;
+  unf2(v, a, b);
+  return a + b;
+}
 template <int NC>
 __device__ __forceinline__ float row_dot(const Row<NC>& a, const Row<NC>& b) {
-  float s = 0.f;
+  uint64_t s = f2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < NC; ++i) {
-    s = fmaf(a.v[i].x, b.v[i].x, s);
-    s = fmaf(a.v[i].y, b.v[i].y, s);
-    s = fmaf(a.v[i].z, b.v[i].z, s);
-    s = fmaf(a.v[i].w, b.v[i].w, s);
+    s = fma2(lo2(a.v[i]), lo2(b.v[i]), s);
+    s = fma2(hi2(a.v[i]), hi2(b.v[i]), s);
   }
-  return warp_sum(s);
+  return warp_sum(sum2(s));
 }
 // r = a * s (elementwise scalar)
 template <int NC>
 __device__ __forceinline__ void row_scale(Row<NC>& r, const Row<NC>& a, float s) {
+  const uint64_t s2 = f2(s, s);
 #pragma unroll
-  for (int i = 0; i < NC; ++i) r.v[i] = make_float4(a.v[i].x * s, a.v[i].y * s, a.v[i].z * s, a.v[i].w * s);
+  for (int i = 0; i < NC; ++i) r.v[i] = join2(mul2(lo2(a.v[i]), s2), mul2(hi2(a.v[i]), s2));
 }
 // r += a * s
 template <int NC>
 __device__ __forceinline__ void row_axpy(Row<NC>& r, const Row<NC>& a, float s) {
+  const uint64_t s2 = f2(s, s);
 #pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    r.v[i].x = fmaf(a.v[i].x, s, r.v[i].x);
-    r.v[i].y = fmaf(a.v[i].y, s, r.v[i].y);
-    r.v[i].z = fmaf(a.v[i].z, s, r.v[i].z);
-    r.v[i].w = fmaf(a.v[i].w, s, r.v[i].w);
-  }
+  for (int i = 0; i < NC; ++i)
+    r.v[i] = join2(fma2(lo2(a.v[i]), s2, lo2(r.v[i])), fma2(hi2(a.v[i]), s2, hi2(r.v[i])));
 }
 // y = x * inv * g
 template <int NC>
 __device__ __forceinline__ void row_norm_apply(Row<NC>& y, const Row<NC>& x, float inv, const Row<NC>& g) {
+  const uint64_t i2 = f2(inv, inv);
 #pragma unroll
   for (int i = 0; i < NC; ++i)
-    y.v[i] = make_float4(x.v[i].x * inv * g.v[i].x, x.v[i].y * inv * g.v[i].y, x.v[i].z * inv * g.v[i].z,
-                         x.v[i].w * inv * g.v[i].w);
+    y.v[i] = join2(mul2(mul2(lo2(x.v[i]), i2), lo2(g.v[i])), mul2(mul2(hi2(x.v[i]), i2), hi2(g.v[i])));
+}
+// sum over the row of (dy * g) * (x * inv), over the warp
+template <int NC>
+__device__ __forceinline__ float row_norm_dot(const Row<NC>& dy, const Row<NC>& x, float inv, const Row<NC>& g) {
+  const uint64_t i2 = f2(inv, inv);
+  uint64_t s = f2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    s = fma2(mul2(lo2(dy.v[i]), lo2(g.v[i])), mul2(lo2(x.v[i]), i2), s);
+    s = fma2(mul2(hi2(dy.v[i]), hi2(g.v[i])), mul2(hi2(x.v[i]), i2), s);
+  }
+  return warp_sum(sum2(s));
+}
+// inv * (dy * g - (x * inv) * mean) for one pair
+__device__ __forceinline__ uint64_t norm_bwd2(uint64_t dy, uint64_t g, uint64_t x, uint64_t i2, uint64_t m2) {
+  return mul2(i2, sub2(mul2(dy, g), mul2(mul2(x, i2), m2)));
 }
 // RMSNorm backward: returns dx = inv * (dy*g - xh * mean(dy*g*xh)), xh = x*inv
 template <int NC>
 __device__ __forceinline__ void row_norm_bwd(Row<NC>& dx, const Row<NC>& dy, const Row<NC>& x, float inv,
                                              const Row<NC>& g, int d) {
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    s = fmaf(dy.v[i].x * g.v[i].x, x.v[i].x * inv, s);
-    s = fmaf(dy.v[i].y * g.v[i].y, x.v[i].y * inv, s);
-    s = fmaf(dy.v[i].z * g.v[i].z, x.v[i].z * inv, s);
-    s = fmaf(dy.v[i].w * g.v[i].w, x.v[i].w * inv, s);
-  }
-  const float mean = warp_sum(s) / (float)d;
+  const float mean = row_norm_dot(dy, x, inv, g) / (float)d;
+  const uint64_t i2 = f2(inv, inv), m2 = f2(mean, mean);
 #pragma unroll
   for (int i = 0; i < NC; ++i)
-    dx.v[i] = make_float4(inv * (dy.v[i].x * g.v[i].x - x.v[i].x * inv * mean),
-                          inv * (dy.v[i].y * g.v[i].y - x.v[i].y * inv * mean),
-                          inv * (dy.v[i].z * g.v[i].z - x.v[i].z * inv * mean),
-                          inv * (dy.v[i].w * g.v[i].w - x.v[i].w * inv * mean));
+    dx.v[i] = join2(norm_bwd2(lo2(dy.v[i]), lo2(g.v[i]), lo2(x.v[i]), i2, m2),
+                    norm_bwd2(hi2(dy.v[i]), hi2(g.v[i]), hi2(x.v[i]), i2, m2));
 }
 // dx += RMSNorm backward of dy (as row_norm_bwd, added in place)
 template <int NC>
 __device__ __forceinline__ void row_norm_bwd_add(Row<NC>& dx, const Row<NC>& dy, const Row<NC>& x, float inv,
                                                  const Row<NC>& g, int d) {
-  float s = 0.f;
+  const float mean = row_norm_dot(dy, x, inv, g) / (float)d;
+  const uint64_t i2 = f2(inv, inv), m2 = f2(mean, mean);
 #pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    s = fmaf(dy.v[i].x * g.v[i].x, x.v[i].x * inv, s);
-    s = fmaf(dy.v[i].y * g.v[i].y, x.v[i].y * inv, s);
-    s = fmaf(dy.v[i].z * g.v[i].z, x.v[i].z * inv, s);
-    s = fmaf(dy.v[i].w * g.v[i].w, x.v[i].w * inv, s);
-  }
-  const float mean = warp_sum(s) / (float)d;
-#pragma unroll
-  for (int i = 0; i < NC; ++i) {
-    dx.v[i].x += inv * (dy.v[i].x * g.v[i].x - x.v[i].x * inv * mean);
-    dx.v[i].y += inv * (dy.v[i].y * g.v[i].y - x.v[i].y * inv * mean);
-    dx.v[i].z += inv * (dy.v[i].z * g.v[i].z - x.v[i].z * inv * mean);
-    dx.v[i].w += inv * (dy.v[i].w * g.v[i].w - x.v[i].w * inv * mean);
-  }
+  for (int i = 0; i < NC; ++i)
+    dx.v[i] = join2(add2(lo2(dx.v[i]), norm_bwd2(lo2(dy.v[i]), lo2(g.v[i]), lo2(x.v[i]), i2, m2)),
+                    add2(hi2(dx.v[i]), norm_bwd2(hi2(dy.v[i]), hi2(g.v[i]), hi2(x.v[i]), i2, m2)));
 }
 template <int NC>
 __device__ __forceinline__ void row_add(Row<NC>& r, const Row<NC>& a) {
 #pragma unroll
-  for (int i = 0; i < NC; ++i)
-    r.v[i] = make_float4(r.v[i].x + a.v[i].x, r.v[i].y + a.v[i].y, r.v[i].z + a.v[i].z, r.v[i].w + a.v[i].w);
+  for (int i = 0; i < NC; ++i) r.v[i] = join2(add2(lo2(r.v[i]), lo2(a.v[i])), add2(hi2(r.v[i]), hi2(a.v[i])));
 }
 template <int NC>
 __device__ __forceinline__ float row_rms_inv(const Row<NC>& x, int d, float eps) {
