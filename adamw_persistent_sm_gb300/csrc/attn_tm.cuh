@@ -412,6 +412,9 @@ struct BwdJob {
   const CUtensorMap* map_qkv;  // q,k,v of all layers
   const CUtensorMap* map_do;   // dO [T][hq]
   const CUtensorMap* map_dqkv; // dq,dk,dv [T][3hq], 32-row x 64-column boxes (bulk stores)
+  const CUtensorMap* map_ds;   // dS^T [B*H*S keys][S queries]: 32-row x 64-column boxes (stores)
+  const CUtensorMap* map_dsl;  // the same buffer, 64 x 64 boxes (loads of the dQ product)
+  int dsg;                     // dK/dV stores dS^T and dQ is a product over it (else dQ recomputes dS)
   int y0;                      // row of token 0 of this layer in map_qkv
   const float* lse;            // [B*H][S] log2 of the row sum of exp2(scale log2(e) s) (this path's forward)
   const float* dsum;           // [B*H][S]
@@ -626,6 +629,10 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
           // the previous item's dK, dV bulk stores have read their staging rows
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
+        } else if (j.dsg) {
+          // this warp's dS^T store of two steps back has read buffer sb
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
         }
         wait(B_(kv::PDEMPTY + sb), ((c >> 1) & 1) ^ 1, SITE_TC_EMPTY);
         const uint32_t pb = sbase + kv::P_OFF + sb * TILE, db = sbase + kv::DS_OFF + sb * TILE;
@@ -665,7 +672,16 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
         else soft(std::false_type());
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(B_(kv::PDFULL + sb));
+        if (lane == 0) {
+          mbar_arrive(B_(kv::PDFULL + sb));
+          if (j.dsg && !dead) {
+            // this warp's 32 key rows of dS^T are a 32 x 64 swizzled box: to HBM for the dQ product
+            tma_store_2d_hint(j.map_ds, db + (uint32_t)q * 4096u, kb * 128 + i * 64,
+                              (b * j.H + h) * j.S + kb * 128 + q * 32, l2_evict_first());
+            bulk_commit();
+          }
+        }
+        __syncwarp();
       }
       // dK, dV of the item's 128 keys: the key's rotary table row is loaded
       // while the last products finish; the rows are staged in this warp's
@@ -691,6 +707,11 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
       __syncwarp();
       if (lane == 0) mbar_arrive(B_(kv::ACCEMPTY));
       const uint32_t bk = sbase + kv::P_OFF + (uint32_t)q * 4096u, bv = sbase + kv::DS_OFF + (uint32_t)q * 4096u;
+      if (j.dsg) {
+        // the dS^T stores from these rows have read them
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+      }
       float g[64];
 #pragma unroll
       for (int x = 0; x < 64; ++x) g[x] = __uint_as_float(vk[x]);
@@ -927,6 +948,150 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
       rope_undo(g, cs, j.scale);
       // the previous item's bulk store has read the staging rows
       const uint32_t bq = sbase + qd::OUT_OFF + (uint32_t)q * 4096u;
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
+      box_put_row64(bq, lane, g);
+      fence_smem_async();
+      __syncwarp();
+      if (lane == 0 && !dead) {
+        tma_store_2d(j.map_dqkv, bq, h * HD, b * j.S + qb * 128 + q * 32);
+        bulk_commit();
+      }
+      __syncwarp();
+    }
+    // every dQ row has landed before the phase ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+  __syncthreads();
+  s.next(items);
+}
+
+// dQ as a product over the stored dS^T (the dK/dV job wrote every dS^T tile
+// of the layer, a grid barrier before this job): dQ = dS K for 128 queries
+// per item, 64-key steps.  dS is read MN-major in place (dS^T rows are keys),
+// K MN-major from the q,k,v buffer; no exponential is recomputed.
+namespace qs {
+constexpr int NST = 6;                                // stages: dS 2 x 8 KB (64 keys x 2 x 64 queries) | K 8 KB
+constexpr uint32_t ST_OFF = 1024;
+constexpr uint32_t ST_BYTES = 24576;
+constexpr uint32_t OUT_OFF = ST_OFF + NST * ST_BYTES; // 4 x 4 KB: each epilogue warp's dQ rows
+constexpr uint32_t END = OUT_OFF + 4 * 4096;
+static_assert(END <= MT_TC_SMEM, "dQ product tiles exceed the shared-memory window");
+static_assert(OUT_OFF % 1024 == 0 && ST_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+enum { STFULL = 0, STEMPTY = NST, ACCFULL = 2 * NST, ACCEMPTY = ACCFULL + 2, COUNT = ACCEMPTY + 2 };
+}
+
+static __device__ __noinline__ void dqs_job(const BwdJob& j, Sched& s, char* smem, const TcState& tc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  auto B_ = [&](int i) { return sbase + 8u * (uint32_t)i; };
+  const long long tmo = j.timeout_ns;
+  const int nqb = j.S / 128;
+  const int items = j.B * j.H * nqb;
+  const int first = s.first(), G = s.G;
+  auto item_of = [&](int it, int& b, int& h, int& qb) {   // longest (last query blocks) first
+    qb = nqb - 1 - it / (j.B * j.H);
+    const int bh = it % (j.B * j.H);
+    b = bh / j.H; h = bh % j.H;
+  };
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < qs::NST; ++i) { mbar_init(B_(qs::STFULL + i), 1); mbar_init(B_(qs::STEMPTY + i), 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(B_(qs::ACCFULL + i), 1); mbar_init(B_(qs::ACCEMPTY + i), 4); }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  bool dead = false;
+  auto wait = [&](uint32_t b_, uint32_t par, int site) {
+    if (!dead && !mbar_wait(b_, par, tmo)) { set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, site); dead = true; }
+  };
+  if (warp == 0) {
+    if (lane == 0) {
+      // the dS^T tiles were written by bulk stores of other CTAs before the barrier
+      asm volatile("fence.proxy.async;" ::: "memory");
+      const uint64_t pol = l2_evict_first();     // each dS^T tile is read once
+      uint32_t c = 0;
+      for (int it = first; it < items; it += G) {
+        int b, h, qb;
+        item_of(it, b, h, qb);
+        const int nst = 2 * (qb + 1), bh = b * j.H + h;
+        for (int i = 0; i < nst; ++i, ++c) {
+          const uint32_t st = c % qs::NST, sa = sbase + qs::ST_OFF + st * qs::ST_BYTES;
+          wait(B_(qs::STEMPTY + st), ((c / qs::NST) & 1) ^ 1, SITE_TC_EMPTY);
+          mbar_expect_tx(B_(qs::STFULL + st), qs::ST_BYTES);
+          tma_load_2d_hint(sa, j.map_dsl, qb * 128, bh * j.S + i * 64, B_(qs::STFULL + st), pol);
+          tma_load_2d_hint(sa + 8192, j.map_dsl, qb * 128 + 64, bh * j.S + i * 64, B_(qs::STFULL + st), pol);
+          tma_load_2d(sa + 16384, j.map_qkv, j.hq + h * HD, j.y0 + b * j.S + i * 64, B_(qs::STFULL + st));
+        }
+      }
+      if (!dead)
+        for (uint32_t x = c > qs::NST ? c - qs::NST : 0; x < c; ++x)
+          wait(B_(qs::STFULL + x % qs::NST), (x / qs::NST) & 1, SITE_TC_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_q = idesc_bf16(128, 64, 1, 1);     // dS (MN-major) x K (MN-major)
+      uint32_t c = 0, ni = 0, last_bar = 0, last_par = 0;
+      for (int it = first; it < items; it += G, ++ni) {
+        int b, h, qb;
+        item_of(it, b, h, qb);
+        const int nst = 2 * (qb + 1);
+        const uint32_t ab = ni & 1;
+        wait(B_(qs::ACCEMPTY + ab), ((ni >> 1) & 1) ^ 1, SITE_TC_ACC_EMPTY);
+        tc_fence_after();
+        for (int i = 0; i < nst; ++i, ++c) {
+          const uint32_t st = c % qs::NST, sa = sbase + qs::ST_OFF + st * qs::ST_BYTES;
+          wait(B_(qs::STFULL + st), (c / qs::NST) & 1, SITE_TC_FULL);
+          tc_fence_after();
+          const uint64_t da = sdesc(sa, 8192, 1024), dk = sdesc(sa + 16384, 8192, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tc.tmem_base + ab * 64, sdesc_add(da, kk * 2048), sdesc_add(dk, kk * 2048), id_q,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(B_(qs::STEMPTY + st));
+          last_bar = B_(qs::STEMPTY + st);
+          last_par = (c / qs::NST) & 1;
+        }
+        mma_commit(B_(qs::ACCFULL + ab));
+      }
+      // the tensor core must be idle before the job returns
+      if (last_bar && !dead && !mbar_wait(last_bar, last_par, tmo)) set_error(j.hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------- output: one query row per thread ----------------
+    const int q = warp - 4, r = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const uint32_t bq = sbase + qs::OUT_OFF + (uint32_t)q * 4096u;
+    uint32_t ni = 0;
+    for (int it = first; it < items; it += G, ++ni) {
+      int b, h, qb;
+      item_of(it, b, h, qb);
+      const int query = qb * 128 + r;
+      float4 cs[16];
+      {
+        const float4* tab = reinterpret_cast<const float4*>(j.rope + (long long)query * 64);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) cs[x] = tab[x];
+      }
+      const uint32_t ab = ni & 1;
+      wait(B_(qs::ACCFULL + ab), (ni >> 1) & 1, SITE_TC_ACC_FULL);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t vq[64];
+      tmem_ld32_async(tc.tmem_base + lane_off + ab * 64, vq);
+      tmem_ld32_async(tc.tmem_base + lane_off + ab * 64 + 32, vq + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B_(qs::ACCEMPTY + ab));
+      float g[64];
+#pragma unroll
+      for (int x = 0; x < 64; ++x) g[x] = __uint_as_float(vq[x]);
+      rope_undo(g, cs, j.scale);
+      // the previous item's bulk store has read the staging rows
       if (lane == 0) bulk_wait_read<0>();
       __syncwarp();
       box_put_row64(bq, lane, g);

@@ -111,6 +111,10 @@ void make_plan(const mt_hparams* hp, MtPlan* P) {
   sz[A_DO] = T * D.hq * ob;
   sz[A_DSUM] = T * D.H * 4;
   sz[A_DQKV] = T * 3 * D.hq * ob;
+  // dS^T of one layer for the dQ product of the tcgen05 attention backward
+  const bool tm_attn = hp->precision == MT_PREC_BF16 && tc_shapes_ok(hp) && hp->seq % 128 == 0 &&
+                       !(hp->flags & (MT_FLAG_SIMT_ATTN | MT_FLAG_MMA_SYNC_ATTN));
+  sz[A_DSG] = tm_attn ? (long long)D.B * D.H * D.S * D.S * 2 : 0;
   sz[A_DR] = T * d * 4;
   sz[A_DRF] = T * d * 4;
   sz[A_PART] = (long long)D.nch * (D.E + 2) * d * 4;
@@ -298,6 +302,7 @@ int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m
   a->use_tc = want_tc ? 1 : 0;
   a->use_tc_attn = bf16 && !(hp->flags & MT_FLAG_SIMT_ATTN) && hp->head_dim == 64 && hp->seq % 128 == 0;
   a->use_tm_attn = a->use_tc && a->use_tc_attn && !(hp->flags & MT_FLAG_MMA_SYNC_ATTN);
+  a->use_dsg = a->use_tm_attn && P.abytes[A_DSG] > 0;
   // counters need whole 128-row blocks on both sides of every hand-off
   a->deps = a->use_tc && a->use_tc_attn && !(hp->flags & MT_FLAG_BARRIERS_ONLY);
   a->smem_bytes = (int)smem;

@@ -2136,16 +2136,22 @@ __device__ __forceinline__ void run_attn_fwd(const KArgs& a, int l, Sched& s, ch
   if (a.D.hd == 64) attn_fwd_job<OP, 64>(t, s, (float*)smem);
   else attn_fwd_job<OP, 16>(t, s, (float*)smem);
 }
+// The tcgen05 attention backward's job description for layer l.
+__device__ __forceinline__ attn_tm::BwdJob tm_bwd_job(const KArgs& a, int l, const AttnDeps& dp) {
+  const MtDims& D = a.D;
+  return attn_tm::BwdJob{&a.maps[MAP_QKV], &a.maps[MAP_DOUT], &a.maps[MAP_E_DQKV], &a.maps[MAP_E_DS],
+                         &a.maps[MAP_E_DSL], a.use_dsg, l * D.T,
+                         abuf<float>(a, A_LSE) + (long long)l * D.B * D.H * D.S, abuf<float>(a, A_DSUM),
+                         abuf<__nv_bfloat16>(a, A_DQKV), abuf<float>(a, A_ROPE), D.B, D.H, D.S, D.hq,
+                         1.0f / sqrtf((float)D.hd), dp.hdr, dp.timeout_ns};
+}
+
 template <class OP, class Stamp>
 __device__ __forceinline__ void run_attn_bwd(const KArgs& a, int l, Sched& s, char* smem, const TcState& tc,
                                              const AttnDeps& dp, Stamp&& stamp) {
   if constexpr (sizeof(OP) == 2) {
     if (a.use_tm_attn) {
-      const MtDims& D = a.D;
-      attn_tm::BwdJob j{&a.maps[MAP_QKV], &a.maps[MAP_DOUT], &a.maps[MAP_E_DQKV], l * D.T,
-                        abuf<float>(a, A_LSE) + (long long)l * D.B * D.H * D.S, abuf<float>(a, A_DSUM),
-                        abuf<__nv_bfloat16>(a, A_DQKV), abuf<float>(a, A_ROPE), D.B, D.H, D.S, D.hq,
-                        1.0f / sqrtf((float)D.hd), dp.hdr, dp.timeout_ns};
+      const attn_tm::BwdJob j = tm_bwd_job(a, l, dp);
       attn_tm::dkdv_job(j, s, smem, tc);
       stamp();
       attn_tm::dq_job(j, s, smem, tc);
@@ -2308,7 +2314,16 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     job_colfinal(a, 0, D.E, D.E, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d, nullptr, 0, s, rg_chunks);
     job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_MOE_NORM) + (long long)l * D.d, nullptr, 0, s, (int)G); TJ(18);
     job_ksplit_sum(a, pgrad(a, P_WO) + (long long)l * D.d * D.hq, D.d, D.hq, s); TJ(32);
-    run_attn_bwd<OP>(a, l, s, smem, tc, attn_deps(l, TK_ATTN_BWD, false), [&] { TJ(35); }); TJ(26);
+    if constexpr (sizeof(OP) == 2) {
+      if (a.use_dsg) {
+        // dK/dV stores dS^T; after a grid barrier dQ is a product over it
+        const attn_tm::BwdJob j = tm_bwd_job(a, l, attn_deps(l, TK_ATTN_BWD, false));
+        attn_tm::dkdv_job(j, s, smem, tc); TJ(35);
+        MT_SYNC();
+        attn_tm::dqs_job(j, s, smem, tc); TJ(26);
+      }
+    }
+    if (!a.use_dsg) { run_attn_bwd<OP>(a, l, s, smem, tc, attn_deps(l, TK_ATTN_BWD, false), [&] { TJ(35); }); TJ(26); }
     MT_SYNC();
     run_gemm<OP>(a, TK(gm.qkv_wgrad(l), l, TK_QKV_WGRAD), s, smem, tc); TJ(28);
     run_gemm<OP>(a, TK(gm.qkv_dgrad(l), l, TK_QKV_DGRAD), s, smem, tc); TJ(27);

@@ -58,6 +58,7 @@ enum ArenaId {
   A_DO,        // op   [T][hq] gradient wrt attention output
   A_DSUM,      // fp32 [B*H][S] rowsum(dO * O) of the attention backward
   A_DQKV,      // op   [T][3hq] gradient wrt q,k,v (before RoPE)
+  A_DSG,       // bf16 [B*H*S][S] dS^T of one layer's attention backward (keys x queries; tensor-core path)
   A_DR,        // fp32 [T][d] gradient wrt attention RMSNorm output
   A_DRF,       // fp32 [T][d] gradient wrt final RMSNorm output
   A_PART,      // fp32 [NCH][E+2][d] column-reduction partials
@@ -81,6 +82,8 @@ enum MapId {
   MAP_E_Y, MAP_E_DRF, MAP_E_DXS, MAP_E_DR, MAP_E_XM, MAP_E_X,
   MAP_E_DQKV,   // 32 rows x 64 columns, 128-byte swizzle: the attention backward's dq, dk, dv rows
   MAP_E_OROW,   // 32 rows x 64 columns, 128-byte swizzle: the attention forward's output rows
+  MAP_E_DS,     // 32 rows x 64 columns, 128-byte swizzle: dS^T rows stored by the dK/dV softmax warps
+  MAP_E_DSL,    // 64 x 64, 128-byte swizzle: dS^T boxes loaded by the dQ product
   MAP_COUNT
 };
 static_assert(MAP_COUNT <= MT_NMAPS, "too many tensor maps");
@@ -172,6 +175,7 @@ struct KArgs {
   int use_tc;                   // tcgen05 GEMMs (bf16 only)
   int use_tc_attn;              // tensor-core attention (bf16 only)
   int use_tm_attn;              // attention forward on tcgen05 with TMEM accumulators (needs use_tc)
+  int use_dsg;                  // dQ as a product over stored dS^T (A_DSG, MAP_E_DS/DSL; needs use_tm_attn)
   int deps;                     // dependency counters replace the grid barriers they cover
   int smem_bytes;               // dynamic shared memory of the launch
   CUtensorMap maps[MT_NMAPS];

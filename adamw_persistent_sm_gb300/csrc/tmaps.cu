@@ -98,6 +98,11 @@ int mt_build_tensor_maps(KArgs* a, void* shadow) {
   ok &= encode_epi(&a->maps[MAP_E_X], A(A_X), (L + 1) * T, d, true);
   ok &= encode_box(&a->maps[MAP_E_DQKV], A(A_DQKV), T, 3 * hq, false, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   ok &= encode_box(&a->maps[MAP_E_OROW], A(A_O), L * T, hq, false, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (a->use_dsg) {
+    const long long rows = (long long)D.B * D.H * D.S;
+    ok &= encode_box(&a->maps[MAP_E_DS], A(A_DSG), rows, D.S, false, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= encode_box(&a->maps[MAP_E_DSL], A(A_DSG), rows, D.S, false, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   return ok ? MT_OK : MT_ERR_ARG;
 }
 
