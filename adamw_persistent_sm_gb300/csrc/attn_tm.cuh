@@ -412,7 +412,7 @@ struct BwdJob {
   const CUtensorMap* map_qkv;  // q,k,v of all layers
   const CUtensorMap* map_do;   // dO [T][hq]
   const CUtensorMap* map_dqkv; // dq,dk,dv [T][3hq], 32-row x 64-column boxes (bulk stores)
-  const CUtensorMap* map_ds;   // dS^T [B*H*S keys][S queries]: 32-row x 64-column boxes (stores)
+  const CUtensorMap* map_ds;   // dS^T [B*H*S keys][S queries]: 128-row x 64-column boxes (stores)
   const CUtensorMap* map_dsl;  // the same buffer, 64 x 64 boxes (loads of the dQ product)
   int dsg;                     // dK/dV stores dS^T and dQ is a product over it (else dQ recomputes dS)
   int y0;                      // row of token 0 of this layer in map_qkv
@@ -463,11 +463,12 @@ constexpr uint32_t ST_OFF = KV_OFF + 4 * TILE;       // stage: Q 8 KB | dO 8 KB 
 constexpr uint32_t ST_BYTES = 17408;
 constexpr uint32_t P_OFF = ST_OFF + NST * ST_BYTES;   // 2 x P^T (128 keys x 64 queries)
 constexpr uint32_t DS_OFF = P_OFF + 2 * TILE;         // 2 x dS^T
-constexpr uint32_t END = DS_OFF + 2 * TILE;
+constexpr uint32_t DV_OFF = DS_OFF + 2 * TILE;        // 4 x 4 KB: each softmax warp's dV rows (bulk-store staging)
+constexpr uint32_t END = DV_OFF + 4 * 4096;
 static_assert(END <= MT_TC_SMEM, "dK/dV tiles exceed the shared-memory window");
 static_assert(P_OFF % 1024 == 0 && ST_OFF % 1024 == 0 && ST_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 enum { KVFULL = 0, KVEMPTY = 2, ACCFULL = 4, ACCEMPTY = 5, STFULL = 6, STEMPTY = STFULL + NST, SDFULL = STEMPTY + NST,
-       SDEMPTY = SDFULL + 2, PDFULL = SDEMPTY + 2, PDEMPTY = PDFULL + 2, COUNT = PDEMPTY + 2 };
+       SDEMPTY = SDFULL + 2, PDFULL = SDEMPTY + 2, PDEMPTY = PDFULL + 2, DSFREE = PDEMPTY + 2, COUNT = DSFREE + 2 };
 // TMEM: S^T at 0/64, dP^T at 128/192, dV at 256, dK at 320
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 320;
 }
@@ -493,6 +494,7 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
     for (int i = 0; i < 2; ++i) {
       mbar_init(B_(kv::SDFULL + i), 1); mbar_init(B_(kv::SDEMPTY + i), 4);
       mbar_init(B_(kv::PDFULL + i), 4); mbar_init(B_(kv::PDEMPTY + i), 1);
+      mbar_init(B_(kv::DSFREE + i), 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -595,6 +597,36 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
       if (ni > 0) wait(B_(kv::KVEMPTY + ((ni - 1) & 1)), ((ni - 1) >> 1) & 1, SITE_TC_DRAIN);
     }
     __syncwarp();
+  } else if (warp == 2) {
+    if (lane == 0 && j.dsg) {
+      // ---------------- dS^T stores ----------------
+      // each step's dS^T tile (128 keys x 64 queries, swizzled) goes to HBM
+      // for the dQ product with one bulk store; the buffer is free again once
+      // the store has read it
+      const uint64_t pol = l2_evict_first();
+      uint32_t c = 0;
+      for (int it = first; it < items; it += G) {
+        int b, h, kb;
+        item_of(it, b, h, kb);
+        const int nst = (j.S - kb * 128) / 64;
+        for (int i = 0; i < nst; ++i, ++c) {
+          const uint32_t sb = c & 1;
+          wait(B_(kv::PDFULL + sb), (c >> 1) & 1, SITE_TC_FULL);
+          if (!dead) {
+            tma_store_2d_hint(j.map_ds, sbase + kv::DS_OFF + sb * TILE, kb * 128 + i * 64, (b * j.H + h) * j.S + kb * 128,
+                              pol);
+            bulk_commit();
+          }
+          if (c > 0) {
+            bulk_wait_read<1>();
+            mbar_arrive(B_(kv::DSFREE + ((c - 1) & 1)));
+          }
+        }
+      }
+      bulk_wait_all();
+      if (c > 0) mbar_arrive(B_(kv::DSFREE + ((c - 1) & 1)));
+    }
+    __syncwarp();
   } else if (warp >= 4) {
     // ---------------- softmax and output: one key row per thread ----------------
     const int q = warp - 4, r = q * 32 + lane;
@@ -629,12 +661,10 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
           // the previous item's dK, dV bulk stores have read their staging rows
           if (lane == 0) bulk_wait_read<0>();
           __syncwarp();
-        } else if (j.dsg) {
-          // this warp's dS^T store of two steps back has read buffer sb
-          if (lane == 0) bulk_wait_read<1>();
-          __syncwarp();
         }
         wait(B_(kv::PDEMPTY + sb), ((c >> 1) & 1) ^ 1, SITE_TC_EMPTY);
+        // the dS^T store of two steps back has read buffer sb
+        if (j.dsg) wait(B_(kv::DSFREE + sb), ((c >> 1) & 1) ^ 1, SITE_TC_EMPTY);
         const uint32_t pb = sbase + kv::P_OFF + sb * TILE, db = sbase + kv::DS_OFF + sb * TILE;
         // P^T and dS^T of the step; the mask only touches the first two steps,
         // the others run without the compare and select
@@ -672,16 +702,7 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
         else soft(std::false_type());
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(B_(kv::PDFULL + sb));
-          if (j.dsg && !dead) {
-            // this warp's 32 key rows of dS^T are a 32 x 64 swizzled box: to HBM for the dQ product
-            tma_store_2d_hint(j.map_ds, db + (uint32_t)q * 4096u, kb * 128 + i * 64,
-                              (b * j.H + h) * j.S + kb * 128 + q * 32, l2_evict_first());
-            bulk_commit();
-          }
-        }
-        __syncwarp();
+        if (lane == 0) mbar_arrive(B_(kv::PDFULL + sb));
       }
       // dK, dV of the item's 128 keys: the key's rotary table row is loaded
       // while the last products finish; the rows are staged in this warp's
@@ -706,12 +727,7 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(B_(kv::ACCEMPTY));
-      const uint32_t bk = sbase + kv::P_OFF + (uint32_t)q * 4096u, bv = sbase + kv::DS_OFF + (uint32_t)q * 4096u;
-      if (j.dsg) {
-        // the dS^T stores from these rows have read them
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
-      }
+      const uint32_t bk = sbase + kv::P_OFF + (uint32_t)q * 4096u, bv = sbase + kv::DV_OFF + (uint32_t)q * 4096u;
       float g[64];
 #pragma unroll
       for (int x = 0; x < 64; ++x) g[x] = __uint_as_float(vk[x]);

@@ -82,7 +82,7 @@ enum MapId {
   MAP_E_Y, MAP_E_DRF, MAP_E_DXS, MAP_E_DR, MAP_E_XM, MAP_E_X,
   MAP_E_DQKV,   // 32 rows x 64 columns, 128-byte swizzle: the attention backward's dq, dk, dv rows
   MAP_E_OROW,   // 32 rows x 64 columns, 128-byte swizzle: the attention forward's output rows
-  MAP_E_DS,     // 32 rows x 64 columns, 128-byte swizzle: dS^T rows stored by the dK/dV softmax warps
+  MAP_E_DS,     // 128 rows x 64 columns, 128-byte swizzle: dS^T tiles stored by the dK/dV job
   MAP_E_DSL,    // 64 x 64, 128-byte swizzle: dS^T boxes loaded by the dQ product
   MAP_COUNT
 };

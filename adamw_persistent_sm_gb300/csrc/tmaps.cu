@@ -100,7 +100,7 @@ int mt_build_tensor_maps(KArgs* a, void* shadow) {
   ok &= encode_box(&a->maps[MAP_E_OROW], A(A_O), L * T, hq, false, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (a->use_dsg) {
     const long long rows = (long long)D.B * D.H * D.S;
-    ok &= encode_box(&a->maps[MAP_E_DS], A(A_DSG), rows, D.S, false, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= encode_box(&a->maps[MAP_E_DS], A(A_DSG), rows, D.S, false, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     ok &= encode_box(&a->maps[MAP_E_DSL], A(A_DSG), rows, D.S, false, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   return ok ? MT_OK : MT_ERR_ARG;
