@@ -543,6 +543,25 @@ __device__ __forceinline__ void epi_store_bf16(EpiSt& e, const CUtensorMap* map,
   }
   ++e.nbox;
 }
+// 64 bf16 columns per row: a 32 x 64 box (128-byte rows, chunk j of row r at
+// j ^ (r & 7)) in half k & 1 of the window
+__device__ __forceinline__ void epi_store_bf16_64(EpiSt& e, const CUtensorMap* map, int x, int y, const float* v) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t box = e.win + (e.nbox & 1) * 2 * TC_EPI_SLOT;
+  if (lane == 0) bulk_wait_read<1>();
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    sts128(box + sw128(lane, j), bf2(v[8 * j], v[8 * j + 1]), bf2(v[8 * j + 2], v[8 * j + 3]),
+           bf2(v[8 * j + 4], v[8 * j + 5]), bf2(v[8 * j + 6], v[8 * j + 7]));
+  fence_smem_async();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, box, x, y);
+    bulk_commit();
+  }
+  ++e.nbox;
+}
 __device__ __forceinline__ void epi_store_f32(EpiSt& e, const CUtensorMap* map, int x, int y, const float* v) {
   const int lane = threadIdx.x & 31;
   const uint32_t box = e.win + (e.nbox & 1) * 2 * TC_EPI_SLOT;
@@ -664,8 +683,7 @@ __device__ __forceinline__ void tc_epilogue_tma(const EpiRegs& g, const TcTile& 
             x[i + 33] = x2 * cs.z + x1 * cs.w;
           }
         }
-        epi_store_bf16(es, g.om, n, y, x);
-        epi_store_bf16(es, g.om, n + 32, y, x + 32);
+        epi_store_bf16_64(es, g.om, n, y, x);
       }
       break;
     }
@@ -768,8 +786,7 @@ __device__ __forceinline__ void tc_epilogue_tma(const EpiRegs& g, const TcTile& 
         float v[64];
         tmem_ld64(trow + c * 32, v);
         const int n = ti.n0 + c * 32;
-        epi_store_bf16(es, g.om, n, y, v);
-        epi_store_bf16(es, g.om, n + 32, y, v + 32);
+        epi_store_bf16_64(es, g.om, n, y, v);
         const int off = tgt - n;
         if ((unsigned)off < 64u) {
 #pragma unroll
@@ -785,10 +802,18 @@ __device__ __forceinline__ void tc_epilogue_tma(const EpiRegs& g, const TcTile& 
         const float bm = fmaxf(fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                      fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))), mx);
         const float bml = bm * EPI_LOG2E;
+        const uint64_t l2 = f2(EPI_LOG2E, EPI_LOG2E), nb2 = f2(-bml, -bml);
+        uint64_t s2[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) s8[k] = 0.f;
+        for (int k = 0; k < 4; ++k) s2[k] = f2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) s8[i & 7] += epi_ex2(fmaf(v[i], EPI_LOG2E, -bml));
+        for (int i = 0; i < 64; i += 2) {
+          float t0, t1;
+          unf2(fma2(f2(v[i], v[i + 1]), l2, nb2), t0, t1);
+          s2[(i >> 1) & 3] = add2(s2[(i >> 1) & 3], f2(epi_ex2(t0), epi_ex2(t1)));
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) unf2(s2[k], s8[2 * k], s8[2 * k + 1]);
         const float bs = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
         sm = sm * epi_ex2((mx - bm) * EPI_LOG2E) + bs;
         mx = bm;

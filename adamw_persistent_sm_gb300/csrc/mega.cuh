@@ -1898,7 +1898,7 @@ struct Gemms {
     g.B = opnd(pweight<OP>(a, P_WQKV) + (long long)l * 3 * D.hq * D.d, D.d, 0);
     g.B.map0 = MAP_WQKV; g.B.y0 = l * 3 * D.hq;
     g.out = abuf<OP>(a, A_QKV) + (long long)l * D.T * 3 * D.hq; g.ldo = 3 * D.hq;
-    g.omap = MAP_E_QKV; g.oy0 = l * D.T;
+    g.omap = MAP_E_QKV64; g.oy0 = l * D.T;
     g.rope = abuf<float>(a, A_ROPE);
     return g;
   }

@@ -78,12 +78,15 @@ enum MapId {
   MAP_WLM, MAP_DLOGITS, MAP_DY, MAP_DGU, MAP_DXO, MAP_DQKV, MAP_QKV, MAP_DOUT,
   // 32 x 32 boxes of the epilogues' bulk stores and aux loads: bf16 with the
   // 64-byte swizzle, fp32 with the 128-byte swizzle
-  MAP_E_QKV, MAP_E_GU, MAP_E_ACT, MAP_E_DGU, MAP_E_DLOGITS, MAP_E_DO, MAP_E_O,
+  MAP_E_QKV, MAP_E_GU, MAP_E_ACT, MAP_E_DGU,
+  MAP_E_DLOGITS,  // (32 rows x 64 columns, 128-byte swizzle)
+  MAP_E_DO, MAP_E_O,
   MAP_E_Y, MAP_E_DRF, MAP_E_DXS, MAP_E_DR, MAP_E_XM, MAP_E_X,
   MAP_E_DQKV,   // 32 rows x 64 columns, 128-byte swizzle: the attention backward's dq, dk, dv rows
   MAP_E_OROW,   // 32 rows x 64 columns, 128-byte swizzle: the attention forward's output rows
   MAP_E_DS,     // 128 rows x 64 columns, 128-byte swizzle: dS^T tiles stored by the dK/dV job
   MAP_E_DSL,    // 64 x 64, 128-byte swizzle: dS^T boxes loaded by the dQ product
+  MAP_E_QKV64,  // 32 rows x 64 columns, 128-byte swizzle: q,k,v rows of the qkv product
   MAP_COUNT
 };
 static_assert(MAP_COUNT <= MT_NMAPS, "too many tensor maps");

@@ -87,7 +87,8 @@ int mt_build_tensor_maps(KArgs* a, void* shadow) {
   ok &= encode_epi(&a->maps[MAP_E_GU], A(A_GU), L * Pm, 2 * F, false);
   ok &= encode_epi(&a->maps[MAP_E_ACT], A(A_ACT), L * Pm, F, false);
   ok &= encode_epi(&a->maps[MAP_E_DGU], A(A_DGU), Pm, 2 * F, false);
-  ok &= encode_epi(&a->maps[MAP_E_DLOGITS], A(A_DLOGITS), T, V, false);
+  ok &= encode_box(&a->maps[MAP_E_DLOGITS], A(A_DLOGITS), T, V, false, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok &= encode_box(&a->maps[MAP_E_QKV64], A(A_QKV), L * T, 3 * hq, false, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   ok &= encode_epi(&a->maps[MAP_E_DO], A(A_DO), T, hq, false);
   ok &= encode_epi(&a->maps[MAP_E_O], A(A_O), L * T, hq, false);
   ok &= encode_epi(&a->maps[MAP_E_Y], A(A_Y), L * Pm, d, true);
