@@ -137,7 +137,11 @@ int32_t mt_param_layout(const mt_hparams* hp, mt_tensor_desc* out, int32_t cap);
 /* Bytes of caller-provided device arena the launch needs (worst case over
  * routing), or a negative mt_status.  With MT_FLAG_TRACE in hp->flags the
  * arena also holds the per-CTA trace (MT_VIEW_TRACE), so traced launches
- * need an arena sized with that flag. */
+ * need an arena sized with that flag.  bf16 models on the tensor-core
+ * attention path (neither MT_FLAG_SIMT_ATTN nor MT_FLAG_MMA_SYNC_ATTN) also
+ * hold one layer's attention-backward dS^T, batch * heads * seq^2 bf16
+ * values, so an arena must be sized with the flags of the launches that
+ * use it. */
 int64_t mt_arena_bytes(const mt_hparams* hp);
 
 /* Zero the arena's control header (barrier and status words).  Call once after

@@ -121,3 +121,18 @@ def test_trace_arena_is_sized_by_the_trace_flag():
     assert traced - plain >= B.MT_MAX_CTAS * per_cta
     assert traced - plain < B.MT_MAX_CTAS * per_cta + 4096
     assert plain <= B.MT_NOALLOC_ARENA_BYTES
+
+
+def test_arena_holds_the_attention_ds_buffer_on_the_tensor_core_path():
+    """bf16 models on the tcgen05 attention path keep one layer's dS^T
+    (batch x heads x seq^2 bf16) for the dQ product; the CUDA-core and
+    warp-MMA attention paths and the fp32 model do not."""
+    from adamw_persistent_sm_gb300 import binding as B
+    cfg = mi.get_config("b2")
+    ds = cfg.batch * cfg.n_heads * cfg.seq * cfg.seq * 2
+    tm = B.mt_arena_bytes(B.hparams(cfg))
+    for flag in (B.MT_FLAG_SIMT_ATTN, B.MT_FLAG_MMA_SYNC_ATTN):
+        other = B.mt_arena_bytes(B.hparams(cfg, flags=flag))
+        assert ds <= tm - other < ds + 4096
+    tiny = B.mt_arena_bytes(B.hparams(mi.get_config("tiny")))
+    assert tiny <= B.MT_NOALLOC_ARENA_BYTES
