@@ -698,8 +698,17 @@ __device__ __forceinline__ void tc_epilogue_tma(const EpiRegs& g, const TcTile& 
           const int f = f0 + c * 32;
           epi_store_bf16(es, g.om, f, y, gg);
           epi_store_bf16(es, g.om, g.F + f, y, uu);
+          const uint64_t nl2 = f2(-EPI_LOG2E, -EPI_LOG2E), one2 = f2(1.f, 1.f);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) gg[i] = gg[i] * epi_sigmoid(gg[i]) * uu[i];
+          for (int i = 0; i < 32; i += 2) {
+            // silu(g) u = g u / (1 + 2^(-g log2 e)), two columns per step
+            const uint64_t g2 = f2(gg[i], gg[i + 1]);
+            float e0, e1;
+            unf2(mul2(g2, nl2), e0, e1);
+            float d0, d1;
+            unf2(add2(one2, f2(epi_ex2(e0), epi_ex2(e1))), d0, d1);
+            unf2(mul2(mul2(g2, f2(uu[i], uu[i + 1])), f2(__fdividef(1.0f, d0), __fdividef(1.0f, d1))), gg[i], gg[i + 1]);
+          }
           epi_store_bf16(es, g.om2, f, y2, gg);
         }
       }

@@ -187,8 +187,8 @@ __device__ __noinline__ void job_router(const KArgs& a, int l, char* smem, const
     if (lane < D.E) Z[(long long)t * D.E + lane] = z0;
     if (lane + 32 < D.E) Z[(long long)t * D.E + lane + 32] = z1;
     const float zmax = warp_max(fmaxf(z0, z1));
-    const float p0 = (lane < D.E) ? expf(z0 - zmax) : 0.f;
-    const float p1 = (lane + 32 < D.E) ? expf(z1 - zmax) : 0.f;
+    const float p0 = (lane < D.E) ? __expf(z0 - zmax) : 0.f;
+    const float p1 = (lane + 32 < D.E) ? __expf(z1 - zmax) : 0.f;
     // the softmax normaliser cancels in the renormalised weights; slot k is
     // kept by lane k
     float c0 = z0, c1 = z1;
