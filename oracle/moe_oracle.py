@@ -232,12 +232,26 @@ def to64(params: dict) -> dict:
     return {k: np.asarray(v, dtype=F64) for k, v in params.items()}
 
 
-def moe_forward(r2, l, P, D: Dims):
+def moe_forward(r2, l, P, D: Dims, route_z=None):
     """Router, top-k, route_order and the per-expert SwiGLU products of one
-    expert layer.  Returns the weighted combination [T, d] and a cache."""
+    expert layer.  Returns the weighted combination [T, d] and a cache.
+
+    ``route_z`` (optional, [T, E]): logits on which the top-k *choice* is made
+    instead of this layer's own logits.  The weights are still the oracle's
+    own softmax probabilities of the chosen experts, renormalised over them,
+    so only the discrete choice comes from ``route_z``.  This is the check
+    the pages' routing statement implies ("token_topk" then "route_order" on a
+    given set of router logits): with another implementation's logits the
+    oracle reproduces that implementation's expert choices, and every other
+    step stays the plain fp64 definition.
+    """
     T = r2.shape[0]
     z = r2 @ P["router"][l].T                        # [T, E]
-    idx, w, _ = token_topk(z, D.K)
+    idx, w, p = token_topk(z, D.K)
+    if route_z is not None:
+        idx, _, _ = token_topk(np.asarray(route_z), D.K)
+        pk = np.take_along_axis(p, idx, axis=1)
+        w = pk / pk.sum(axis=1, keepdims=True)
     perm, counts, offsets, inv = route_order(idx, D.E)
     xs = r2[perm // D.K]                              # rows in expert order
     g = np.zeros((T * D.K, D.F))
@@ -297,10 +311,12 @@ def moe_backward(dout, r2, c, l, P, D: Dims, grads):
 
 
 def forward_backward(P: dict, tokens: np.ndarray, D: Dims, coef: float, grads: dict,
-                     keep_cache: bool = False, backward: bool = True):
+                     keep_cache: bool = False, backward: bool = True, route_logits=None):
     """Loss of one block of independent sequences and its gradients, added to
     ``grads``.  ``tokens`` is int [B, S]; ``coef`` multiplies every target's
-    cross-entropy.  Returns (loss, per_token_loss [B*S], debug)."""
+    cross-entropy.  ``route_logits`` (optional) is a per-layer list of [B*S, E]
+    logits on which each layer's expert choice is made (see
+    :func:`moe_forward`).  Returns (loss, per_token_loss [B*S], debug)."""
     B, S = tokens.shape
     T = B * S
     tok = tokens.reshape(-1)
@@ -325,7 +341,8 @@ def forward_backward(P: dict, tokens: np.ndarray, D: Dims, coef: float, grads: d
         o = unheads(causal_attention(q, k, v))
         x_mid = x_in + o @ P["wo"][l].T
         r2, inv2 = rmsnorm(x_mid, P["moe_norm"][l], D.eps)
-        moe_out, mc = moe_forward(r2, l, P, D)
+        moe_out, mc = moe_forward(r2, l, P, D,
+                                  None if route_logits is None else route_logits[l])
         x = x_mid + moe_out
         caches.append(dict(x_in=x_in, r=r, inv=inv, q=q, k=k, v=v, o=o,
                            x_mid=x_mid, r2=r2, inv2=inv2, moe=mc))
@@ -443,7 +460,8 @@ def n_targets(batch, seq) -> int:
 
 
 def train_update(params: dict, micro_tokens: list, cfg, m=None, v=None,
-                 seqs_per_block: int | None = None, keep_cache=False) -> UpdateResult:
+                 seqs_per_block: int | None = None, keep_cache=False,
+                 route_logits=None) -> UpdateResult:
     """Forward, loss, backward over every microbatch (gradients summed), then
     one clipped AdamW step.
 
@@ -451,6 +469,9 @@ def train_update(params: dict, micro_tokens: list, cfg, m=None, v=None,
     so the reported loss is the mean next-token cross-entropy of the update.
     ``seqs_per_block`` optionally evaluates a microbatch a few sequences at a
     time; sequences never interact in this model, so the sum is unchanged.
+    ``route_logits`` (optional): per microbatch, a per-layer list of
+    [batch*seq, E] logits on which the expert choices are made (see
+    :func:`moe_forward`).
     """
     D = Dims.of(cfg)
     P = to64(params)
@@ -459,13 +480,17 @@ def train_update(params: dict, micro_tokens: list, cfg, m=None, v=None,
     grads = {k: np.zeros_like(p) for k, p in P.items()}
     loss = 0.0
     tok_losses, debugs = [], []
-    for tokens in micro_tokens:
-        B = tokens.shape[0]
+    for mi_, tokens in enumerate(micro_tokens):
+        B, S = tokens.shape
         step_b = B if seqs_per_block is None else seqs_per_block
         parts = []
         for b0 in range(0, B, step_b):
+            rz = None
+            if route_logits is not None:
+                rows = slice(b0 * S, min(b0 + step_b, B) * S)
+                rz = [np.asarray(z)[rows] for z in route_logits[mi_]]
             lo, tl, dbg = forward_backward(P, tokens[b0:b0 + step_b], D, coef, grads,
-                                           keep_cache=keep_cache)
+                                           keep_cache=keep_cache, route_logits=rz)
             loss += lo
             parts.append(tl)
             debugs.append(dbg)
@@ -482,11 +507,13 @@ def train_update(params: dict, micro_tokens: list, cfg, m=None, v=None,
                         m=new_m, v=new_v, tok_loss=tok_losses, debug=debugs)
 
 
-def loss_only(params: dict, tokens: np.ndarray, cfg, coef: float | None = None) -> float:
+def loss_only(params: dict, tokens: np.ndarray, cfg, coef: float | None = None,
+              route_logits=None) -> float:
     """Loss of one microbatch (for finite differences)."""
     D = Dims.of(cfg)
     P = to64(params)
     if coef is None:
         coef = 1.0 / n_targets(*tokens.shape)
-    loss, _, _ = forward_backward(P, tokens, D, coef, {}, backward=False)
+    loss, _, _ = forward_backward(P, tokens, D, coef, {}, backward=False,
+                                  route_logits=route_logits)
     return loss

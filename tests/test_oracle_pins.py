@@ -345,3 +345,86 @@ def test_unrouted_expert_gets_zero_gradient():
         for e in range(3):
             assert np.any(grads[name][0, e]) == (c["counts"][e] > 0)
     assert not np.any(grads["router"][0, 3])
+
+
+# --------------------------------------------------------------------------
+# Expert choice made on given router logits (the GPU's, in the parity tests)
+# --------------------------------------------------------------------------
+def _own_logits(P, tok, cfg):
+    D = oracle.Dims.of(cfg)
+    _, _, dbg = oracle.forward_backward(oracle.to64(P), tok, D, 1.0, {}, keep_cache=True,
+                                        backward=False)
+    return [c["moe"]["z"] for c in dbg["caches"]]
+
+
+def test_route_logits_equal_to_own_logits_change_nothing(tiny_setup):
+    cfg, P, tok = tiny_setup
+    own = oracle.train_update(P, [tok], cfg)
+    forced = oracle.train_update(P, [tok], cfg, route_logits=[_own_logits(P, tok, cfg)])
+    assert forced.loss == own.loss
+    for k in own.grads:
+        np.testing.assert_array_equal(forced.grads[k], own.grads[k], err_msg=k)
+        np.testing.assert_array_equal(forced.params[k], own.params[k], err_msg=k)
+
+
+def test_route_logits_choose_experts_and_backward_matches_finite_differences(tiny_setup):
+    """With other logits deciding the choice, (1) each layer's chosen experts
+    are token_topk of those logits, (2) the weights are the oracle's own
+    probabilities renormalised over that choice, and (3) the hand backward is
+    the derivative of the loss with that choice held fixed (central
+    differences in float64)."""
+    cfg, P, tok = tiny_setup
+    D = oracle.Dims.of(cfg)
+    rng = np.random.default_rng(21)
+    T = tok.size
+    rz = [rng.normal(size=(T, cfg.n_experts)) for _ in range(cfg.n_layers)]
+    own_z = _own_logits(P, tok, cfg)
+    P64 = oracle.to64(P)
+    _, _, dbg = oracle.forward_backward(P64, tok, D, 1.0, {}, keep_cache=True, backward=False,
+                                        route_logits=rz)
+    n_diff = 0
+    for l, c in enumerate(dbg["caches"]):
+        idx, _, _ = oracle.token_topk(rz[l], cfg.top_k)
+        np.testing.assert_array_equal(c["moe"]["idx"], idx)
+        own_idx, _, _ = oracle.token_topk(own_z[l] if l == 0 else c["moe"]["z"], cfg.top_k)
+        n_diff += int(np.sum(np.any(np.sort(own_idx, 1) != np.sort(idx, 1), axis=1)))
+        p = oracle.softmax(c["moe"]["z"])
+        pk = np.take_along_axis(p, idx, axis=1)
+        np.testing.assert_allclose(c["moe"]["w"], pk / pk.sum(1, keepdims=True), rtol=1e-14)
+    assert n_diff > T // 2          # the given logits really change the choices
+    r = oracle.train_update(P, [tok], cfg, route_logits=[rz])
+    h = 1e-5
+    for name, arr in P64.items():
+        flat = arr.reshape(-1)
+        g = r.grads[name].reshape(-1)
+        picks = list(rng.choice(flat.size, size=min(3, flat.size), replace=False))
+        picks.append(int(np.argmax(np.abs(g))))
+        for i in picks:
+            old = flat[i]
+            flat[i] = old + h
+            lp = oracle.loss_only(P64, tok, cfg, route_logits=rz)
+            flat[i] = old - h
+            lm = oracle.loss_only(P64, tok, cfg, route_logits=rz)
+            flat[i] = old
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - g[i]) <= 1e-6 * abs(g[i]) + 2e-9, (name, i, fd, g[i])
+
+
+def test_pooled_oracle_equals_serial_oracle():
+    """The tests' process-pool evaluation of the oracle (one block of
+    sequences per worker, gradients summed, one clip + AdamW) gives the serial
+    oracle's update."""
+    from parity_util import pooled_oracle_update
+    cfg = tiny(batch=3, micro_count=2)
+    P = mi.make_params(cfg)
+    toks = mi.make_update_tokens(cfg)
+    serial = oracle.train_update(P, toks, cfg)
+    pooled = pooled_oracle_update(cfg, toks, workers=2)
+    assert pooled.loss == pytest.approx(serial.loss, rel=1e-13)
+    assert pooled.grad_norm == pytest.approx(serial.grad_norm, rel=1e-13)
+    for k in serial.grads:
+        np.testing.assert_allclose(pooled.grads[k], serial.grads[k], rtol=1e-11, atol=1e-16)
+        # Adam divides by sqrt(v): summation-order rounding of tiny gradients is amplified
+        np.testing.assert_allclose(pooled.params[k], serial.params[k], rtol=1e-9, atol=1e-16)
+    for a, b in zip(pooled.tok_loss, serial.tok_loss):
+        np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-16)
