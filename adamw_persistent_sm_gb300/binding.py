@@ -26,12 +26,10 @@ MT_PREC_FP32 = 0
 MT_PREC_BF16 = 1
 
 MT_FLAG_TRACE = 1 << 0
-MT_FLAG_SIMT_GEMM = 1 << 1
-MT_FLAG_SIMT_ATTN = 1 << 2
 MT_FLAG_NO_OPTIMIZER = 1 << 3
 MT_FLAG_TEST_STALL = 1 << 4
 MT_FLAG_BARRIERS_ONLY = 1 << 5
-MT_FLAG_MMA_SYNC_ATTN = 1 << 6
+MT_FLAG_RECOMPUTE_ATTN_DS = 1 << 7
 
 MT_MAX_LAYERS = 16
 MT_MAX_EXPERTS = 64
@@ -49,6 +47,22 @@ MT_TRACE_JOBS = 1024                  # (end time, job id) pairs
 MT_TRACE_WORDS = 2 * (MT_TRACE_PHASES + MT_TRACE_JOBS)
 MT_VIEW_HIDDEN = 7
 MT_VIEW_LOGITS = 8
+MT_VIEW_QKV = 9
+MT_VIEW_ATTN_O = 10
+MT_VIEW_LSE = 11
+MT_VIEW_DOUT = 12
+MT_VIEW_DSUM = 13
+MT_VIEW_DQKV = 14
+MT_VIEW_XMID = 15
+MT_VIEW_R2 = 16
+MT_VIEW_EXPERT_IN = 17
+MT_VIEW_FINAL_NORM = 18
+
+MT_OP_ATTN_FWD = 1
+MT_OP_ATTN_BWD = 2
+MT_OP_ROUTER = 3
+MT_OP_LM_CE = 4
+MT_OP_CLIP_ADAMW = 5
 
 
 class mt_hparams(C.Structure):
@@ -95,6 +109,8 @@ _SIGNATURES = {
     "mt_status_string": (C.c_char_p, [C.c_int32]),
     "mt_train_update_noalloc": (C.c_int32, [_P, _P, _P, _P, _P, _P, C.POINTER(mt_hparams),
                                             C.POINTER(mt_outputs), _P]),
+    "mt_debug_run": (C.c_int32, [C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P, C.POINTER(mt_hparams), _P,
+                                 C.c_int64, _P]),
     "mt_debug_gemm": (C.c_int32, [_P, C.c_int32, _P, C.c_int32, _P, C.c_int32, C.c_int32, C.c_int32,
                                   C.c_int32, _P, C.c_int32, C.c_int32, C.c_int32, _P, C.c_int64, _P]),
 }
@@ -202,6 +218,12 @@ def mt_debug_view(arena: int, hp: mt_hparams, which: int, layer: int = 0) -> mt_
     if st != MT_OK:
         raise ValueError(f"mt_debug_view: {status_string(st)}")
     return v
+
+
+def mt_debug_run(op: int, layer: int, params: int, shadow: int, grads: int, adam_m: int, adam_v: int,
+                 tokens: int, hp: mt_hparams, arena: int, arena_bytes: int, stream: int = 0) -> int:
+    return load().mt_debug_run(op, layer, params, shadow, grads, adam_m, adam_v, tokens, C.byref(hp),
+                               arena, arena_bytes, stream)
 
 
 def mt_debug_gemm(A: int, a_mn: int, B_: int, b_mn: int, C_: int, M: int, N: int, K: int, rag: int,

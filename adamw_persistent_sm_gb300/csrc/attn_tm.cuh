@@ -24,7 +24,15 @@
 #include "gemm_tc.cuh"
 #include <type_traits>
 
-struct AttnDeps;   // defined with the attention jobs
+// Dependency counters of the attention forward (all null: phases fenced by
+// grid barriers).
+struct AttnDeps {
+  const unsigned* wait;    // per 128-row block of q,k,v: stored column tiles
+  unsigned wtarget;
+  unsigned* sig;           // per 128-row block of the output: +1 per stored head
+  ArenaHdr* hdr;
+  long long timeout_ns;
+};
 
 namespace attn_tm {
 

@@ -32,6 +32,7 @@ int check_hparams(const mt_hparams* hp) {
       hp->batch <= 0 || hp->seq <= 0)
     return MT_ERR_ARG;
   if (hp->precision != MT_PREC_FP32 && hp->precision != MT_PREC_BF16) return MT_ERR_ARG;
+  if (hp->flags & ~(uint32_t)MT_FLAGS_ALL) return MT_ERR_ARG;
   if (hp->micro_count <= 0 || hp->micro_index < 0 || hp->micro_index >= hp->micro_count) return MT_ERR_ARG;
   if (hp->step < 1) return MT_ERR_ARG;
   if (!(hp->lr >= 0.f) || !(hp->beta1 >= 0.f && hp->beta1 < 1.f) || !(hp->beta2 >= 0.f && hp->beta2 < 1.f) ||
@@ -54,13 +55,14 @@ int check_hparams(const mt_hparams* hp) {
   return MT_OK;
 }
 
-// tcgen05 tiles are 128 x 128: every product dimension must be a multiple.
+// The bf16 model runs only on the tensor-core path: 128-row tiles over tokens
+// and expert rows, 256-column tiles over features, 128-query / 128-key
+// attention blocks of head_dim 64.  Other bf16 shapes are refused.
 bool tc_shapes_ok(const mt_hparams* hp) {
   const long long T = (long long)hp->batch * hp->seq;
   const int hq = hp->n_heads * hp->head_dim;
-  // 128-row tiles over tokens and expert rows, 256-column tiles over features
   return T % 128 == 0 && hp->d_model % 256 == 0 && hq % 256 == 0 && hp->vocab % 256 == 0 &&
-         hp->d_ff % 256 == 0 && hp->head_dim == 64;
+         hp->d_ff % 256 == 0 && hp->head_dim == 64 && hp->seq % 128 == 0;
 }
 
 void make_plan(const mt_hparams* hp, MtPlan* P) {
@@ -112,9 +114,9 @@ void make_plan(const mt_hparams* hp, MtPlan* P) {
   sz[A_DSUM] = T * D.H * 4;
   sz[A_DQKV] = T * 3 * D.hq * ob;
   // dS^T of one layer for the dQ product of the tcgen05 attention backward
-  const bool tm_attn = hp->precision == MT_PREC_BF16 && tc_shapes_ok(hp) && hp->seq % 128 == 0 &&
-                       !(hp->flags & (MT_FLAG_SIMT_ATTN | MT_FLAG_MMA_SYNC_ATTN));
-  sz[A_DSG] = tm_attn ? (long long)D.B * D.H * D.S * D.S * 2 : 0;
+  // (memory rule MT_FLAG_RECOMPUTE_ATTN_DS: not kept, dQ recomputes it)
+  const bool keep_ds = hp->precision == MT_PREC_BF16 && !(hp->flags & MT_FLAG_RECOMPUTE_ATTN_DS);
+  sz[A_DSG] = keep_ds ? (long long)D.B * D.H * D.S * D.S * 2 : 0;
   sz[A_DR] = T * d * 4;
   sz[A_DRF] = T * d * 4;
   sz[A_PART] = (long long)D.nch * (D.E + 2) * d * 4;
@@ -205,6 +207,9 @@ int prepare_launch(bool bf16, size_t smem, int* grid) {
   return MT_OK;
 }
 
+int launch_update(int op, int layer, float* params, void* shadow, float* grads, float* adam_m, float* adam_v,
+                  const int32_t* tokens, const mt_hparams* hp, void* arena, int64_t arena_bytes, void* stream);
+
 }  // namespace
 
 extern "C" {
@@ -258,6 +263,25 @@ int32_t mt_arena_init(void* arena, int64_t arena_bytes, void* stream) {
 int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m, float* adam_v,
                         const int32_t* tokens, const mt_hparams* hp, void* arena, int64_t arena_bytes,
                         void* stream) {
+  return launch_update(0, 0, params, shadow, grads, adam_m, adam_v, tokens, hp, arena, arena_bytes, stream);
+}
+
+int32_t mt_debug_run(int32_t op, int32_t layer, float* params, void* shadow, float* grads, float* adam_m,
+                     float* adam_v, const int32_t* tokens, const mt_hparams* hp, void* arena,
+                     int64_t arena_bytes, void* stream) {
+  if (op < MT_OP_ATTN_FWD || op > MT_OP_CLIP_ADAMW) return MT_ERR_ARG;
+  int st = check_hparams(hp);
+  if (st) return st;
+  if (layer < 0 || layer >= hp->n_layers) return MT_ERR_ARG;
+  return launch_update(op, layer, params, shadow, grads, adam_m, adam_v, tokens, hp, arena, arena_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+// One launch of the update (op == 0) or of one op of the single-op harness.
+int launch_update(int op, int layer, float* params, void* shadow, float* grads, float* adam_m, float* adam_v,
+                  const int32_t* tokens, const mt_hparams* hp, void* arena, int64_t arena_bytes, void* stream) {
   int st = check_hparams(hp);
   if (st) return st;
   const bool bf16 = hp->precision == MT_PREC_BF16;
@@ -269,8 +293,8 @@ int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m
   MtPlan P;
   make_plan(hp, &P);
   if (arena_bytes < P.arena_bytes) return MT_ERR_ARENA_SMALL;
-  const bool want_tc = bf16 && !(hp->flags & MT_FLAG_SIMT_GEMM) && MT_TC_AVAILABLE;
-  if (want_tc && !tc_shapes_ok(hp)) return MT_ERR_UNSUPPORTED;
+  const bool want_tc = bf16;
+  if (bf16 && !tc_shapes_ok(hp)) return MT_ERR_UNSUPPORTED;
 
   int grid = 0;
   st = prepare_launch(bf16, smem_bytes(P.D, want_tc), &grid);
@@ -300,18 +324,20 @@ int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m
   memcpy(a->poff, P.poff, sizeof(a->poff));
   memcpy(a->aoff, P.aoff, sizeof(a->aoff));
   a->use_tc = want_tc ? 1 : 0;
-  a->use_tc_attn = bf16 && !(hp->flags & MT_FLAG_SIMT_ATTN) && hp->head_dim == 64 && hp->seq % 128 == 0;
-  a->use_tm_attn = a->use_tc && a->use_tc_attn && !(hp->flags & MT_FLAG_MMA_SYNC_ATTN);
-  a->use_dsg = a->use_tm_attn && P.abytes[A_DSG] > 0;
+  a->use_dsg = bf16 && P.abytes[A_DSG] > 0;
   // counters need whole 128-row blocks on both sides of every hand-off
-  a->deps = a->use_tc && a->use_tc_attn && !(hp->flags & MT_FLAG_BARRIERS_ONLY);
+  a->deps = bf16 && !(hp->flags & MT_FLAG_BARRIERS_ONLY);
   a->smem_bytes = (int)smem;
   if (want_tc) {
     int ms = mt_build_tensor_maps(a, shadow);
     if (ms != MT_OK) { delete a; return ms; }
   }
-  cudaError_t e = bf16 ? mt_launch_mega_bf16(*a, grid, smem, (cudaStream_t)stream)
-                       : mt_launch_mega_f32(*a, grid, smem, (cudaStream_t)stream);
+  a->debug_op = op;
+  a->dbg_layer = layer;
+  cudaError_t e = op ? (bf16 ? mt_launch_op_bf16(*a, grid, smem, (cudaStream_t)stream)
+                             : mt_launch_op_f32(*a, grid, smem, (cudaStream_t)stream))
+                     : (bf16 ? mt_launch_mega_bf16(*a, grid, smem, (cudaStream_t)stream)
+                             : mt_launch_mega_f32(*a, grid, smem, (cudaStream_t)stream));
   delete a;
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -319,6 +345,9 @@ int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m
   }
   return MT_OK;
 }
+}  // namespace
+
+extern "C" {
 
 int32_t mt_read_outputs(const void* arena, mt_outputs* out, void* stream) {
   if (!arena || !out) return MT_ERR_ARG;
@@ -371,6 +400,27 @@ int32_t mt_debug_view(const void* arena, const mt_hparams* hp, int32_t which, in
       *out = {base + P.aoff[A_X] + (long long)layer * T * D.d * 4, T * D.d, 4}; break;
     case MT_VIEW_LOGITS:
       *out = {base + P.aoff[A_DLOGITS], T * D.V, D.op_bytes}; break;
+    case MT_VIEW_QKV:
+      *out = {base + P.aoff[A_QKV] + (long long)layer * T * 3 * D.hq * D.op_bytes, T * 3 * D.hq, D.op_bytes}; break;
+    case MT_VIEW_ATTN_O:
+      *out = {base + P.aoff[A_O] + (long long)layer * T * D.hq * D.op_bytes, T * D.hq, D.op_bytes}; break;
+    case MT_VIEW_LSE:
+      *out = {base + P.aoff[A_LSE] + (long long)layer * D.B * D.H * D.S * 4, (long long)D.B * D.H * D.S, 4}; break;
+    case MT_VIEW_DOUT:
+      *out = {base + P.aoff[A_DO], T * D.hq, D.op_bytes}; break;
+    case MT_VIEW_DSUM:
+      *out = {base + P.aoff[A_DSUM], (long long)D.B * D.H * D.S, 4}; break;
+    case MT_VIEW_DQKV:
+      *out = {base + P.aoff[A_DQKV], T * 3 * D.hq, D.op_bytes}; break;
+    case MT_VIEW_XMID:
+      *out = {base + P.aoff[A_XM] + (long long)layer * T * D.d * 4, T * D.d, 4}; break;
+    case MT_VIEW_R2:
+      *out = {base + P.aoff[A_R2] + (long long)layer * T * D.d * D.op_bytes, T * D.d, D.op_bytes}; break;
+    case MT_VIEW_EXPERT_IN:
+      *out = {base + P.aoff[A_XS] + (long long)layer * D.Pmax * D.d * D.op_bytes, (long long)D.Pmax * D.d,
+              D.op_bytes}; break;
+    case MT_VIEW_FINAL_NORM:
+      *out = {base + P.aoff[A_RF], T * D.d, D.op_bytes}; break;
     default:
       return MT_ERR_ARG;
   }
@@ -387,7 +437,10 @@ int32_t mt_debug_gemm(const void* A, int32_t a_mn, const void* B, int32_t b_mn, 
   if (rag == 1 && a_mn) return MT_ERR_ARG;
   if (rag == 2 && !(a_mn && b_mn)) return MT_ERR_ARG;
   const bool bf16 = precision == MT_PREC_BF16;
-  const bool tc = bf16 && (use_tc & 1) && MT_TC_AVAILABLE;
+  // bf16 operands run on the tensor cores only; the CUDA-core engine is the
+  // fp32 model's
+  if (bf16 && !(use_tc & 1)) return MT_ERR_UNSUPPORTED;
+  const bool tc = bf16;
   const int out_mode = tc ? ((use_tc >> 1) & 3) : 0;     // use_tc bits 1-2: output mode (tensor cores only)
   if (out_mode == 3) return MT_ERR_ARG;
   if (tc && (M % 128 || N % 256 || K % 64)) return MT_ERR_UNSUPPORTED;

@@ -16,7 +16,6 @@
 #include "gemm.cuh"
 #include "attn_simt.cuh"
 #include "gemm_tc.cuh"
-#include "attn_tc.cuh"
 #include "attn_tm.cuh"
 #include "rows.cuh"
 #include "rowpipe.cuh"
@@ -71,13 +70,15 @@ __device__ __forceinline__ float warp_rms_inv(const float* x, int d, float eps) 
 // ===========================================================================
 // Rotary table (angles in double precision) and x0 = emb[tok], plus the
 // first layer's attention RMSNorm.
-template <class OP>
-__device__ __noinline__ void job_embed(const KArgs& a, Sched& s) {
+// CTA me's share of the rotary table (cos, sin of pos * theta^(-2i/hd), in
+// double precision) and of the zeroing of the dependency counters and
+// tickets, which start at zero in every launch (first used after the first
+// grid barrier).
+__device__ __forceinline__ void launch_prologue(const KArgs& a, int me, int G) {
   const MtDims& D = a.D;
   const int half = D.hd / 2;
   float* rope = abuf<float>(a, A_ROPE);
-  const int me = s.first();
-  for (int e = me * MT_THREADS + threadIdx.x; e < D.S * half; e += s.G * MT_THREADS) {
+  for (int e = me * MT_THREADS + threadIdx.x; e < D.S * half; e += G * MT_THREADS) {
     const int pos = e / half, i = e % half;
     const double freq = pow((double)a.rope_theta, -2.0 * (double)i / (double)D.hd);
     double sv, cv;
@@ -85,11 +86,16 @@ __device__ __noinline__ void job_embed(const KArgs& a, Sched& s) {
     rope[2 * e] = (float)cv;
     rope[2 * e + 1] = (float)sv;
   }
-  // dependency counters and tickets start at zero in every launch (first
-  // used after the first grid barrier)
   unsigned* dep = abuf<unsigned>(a, A_DEP);
   const long long ndep = dep_words(D);
-  for (long long i = (long long)me * MT_THREADS + threadIdx.x; i < ndep; i += (long long)s.G * MT_THREADS) dep[i] = 0u;
+  for (long long i = (long long)me * MT_THREADS + threadIdx.x; i < ndep; i += (long long)G * MT_THREADS) dep[i] = 0u;
+}
+
+template <class OP>
+__device__ __noinline__ void job_embed(const KArgs& a, Sched& s) {
+  const MtDims& D = a.D;
+  const int me = s.first();
+  launch_prologue(a, me, s.G);
   ArenaHdr* hdr = abuf<ArenaHdr>(a, A_HDR);
   const float* emb = pmaster(a, P_EMB);
   float* X = abuf<float>(a, A_X);
@@ -2079,12 +2085,13 @@ static __device__ __noinline__ void job_ksplit_sum(const KArgs& a, float* out, i
   s.next(s.G);
 }
 
+// Products: tcgen05 for bf16 operands, exact fp32 FMAs on the CUDA cores for
+// the fp32 model.  There is no other path: bf16 shapes the tensor-core tiles
+// do not cover are refused on the host.
 template <class OP>
 __device__ __forceinline__ void run_gemm(const KArgs& a, const GemmDesc& g, Sched& s, char* smem, TcState& tc) {
-  if constexpr (sizeof(OP) == 2) {
-    if (a.use_tc) { gemm_tc_job(a, g, s, smem, tc); return; }
-  }
-  gemm_simt_job<OP>(g, s, reinterpret_cast<float*>(smem));
+  if constexpr (sizeof(OP) == 2) gemm_tc_job(a, g, s, smem, tc);
+  else gemm_simt_job<OP>(g, s, reinterpret_cast<float*>(smem));
 }
 
 template <class OP>
@@ -2103,38 +2110,19 @@ __device__ __forceinline__ AttnArgs attn_args(const KArgs& a, int l) {
 }
 
 template <class OP>
-__device__ __forceinline__ attn_tc::Args attn_tc_args(const KArgs& a, int l) {
-  const MtDims& D = a.D;
-  attn_tc::Args t;
-  t.qkv = abuf<__nv_bfloat16>(a, A_QKV) + (long long)l * D.T * 3 * D.hq;
-  t.o = abuf<__nv_bfloat16>(a, A_O) + (long long)l * D.T * D.hq;
-  t.lse = abuf<float>(a, A_LSE) + (long long)l * D.B * D.H * D.S;
-  t.dout = abuf<__nv_bfloat16>(a, A_DO);
-  t.dsum = abuf<float>(a, A_DSUM);
-  t.dqkv = abuf<__nv_bfloat16>(a, A_DQKV);
-  t.rope = abuf<float>(a, A_ROPE);
-  t.B = D.B; t.H = D.H; t.S = D.S; t.hq = D.hq;
-  t.scale = 1.0f / sqrtf((float)D.hd);
-  return t;
-}
-
-template <class OP>
 __device__ __forceinline__ void run_attn_fwd(const KArgs& a, int l, Sched& s, char* smem, const TcState& tc,
                                              const AttnDeps& dp) {
   if constexpr (sizeof(OP) == 2) {
-    if (a.use_tm_attn) {
-      const MtDims& D = a.D;
-      attn_tm::Job j{&a.maps[MAP_QKV], &a.maps[MAP_E_OROW], l * D.T, abuf<__nv_bfloat16>(a, A_O) + (long long)l * D.T * D.hq,
-                     abuf<float>(a, A_LSE) + (long long)l * D.B * D.H * D.S, D.B, D.H, D.S, D.hq,
-                     1.0f / sqrtf((float)D.hd), dp.wait, dp.wtarget, dp.sig, dp.hdr, dp.timeout_ns};
-      attn_tm::fwd_job(j, s, smem, tc);
-      return;
-    }
-    if (a.use_tc_attn) { attn_tc_fwd_job<OP>(attn_tc_args<OP>(a, l), s, smem, dp); return; }
+    const MtDims& D = a.D;
+    attn_tm::Job j{&a.maps[MAP_QKV], &a.maps[MAP_E_OROW], l * D.T, abuf<__nv_bfloat16>(a, A_O) + (long long)l * D.T * D.hq,
+                   abuf<float>(a, A_LSE) + (long long)l * D.B * D.H * D.S, D.B, D.H, D.S, D.hq,
+                   1.0f / sqrtf((float)D.hd), dp.wait, dp.wtarget, dp.sig, dp.hdr, dp.timeout_ns};
+    attn_tm::fwd_job(j, s, smem, tc);
+  } else {
+    const AttnArgs t = attn_args<OP>(a, l);
+    if (a.D.hd == 64) attn_fwd_job<OP, 64>(t, s, (float*)smem);
+    else attn_fwd_job<OP, 16>(t, s, (float*)smem);
   }
-  const AttnArgs t = attn_args<OP>(a, l);
-  if (a.D.hd == 64) attn_fwd_job<OP, 64>(t, s, (float*)smem);
-  else attn_fwd_job<OP, 16>(t, s, (float*)smem);
 }
 // The tcgen05 attention backward's job description for layer l.
 __device__ __forceinline__ attn_tm::BwdJob tm_bwd_job(const KArgs& a, int l, const AttnDeps& dp) {
@@ -2150,18 +2138,15 @@ template <class OP, class Stamp>
 __device__ __forceinline__ void run_attn_bwd(const KArgs& a, int l, Sched& s, char* smem, const TcState& tc,
                                              const AttnDeps& dp, Stamp&& stamp) {
   if constexpr (sizeof(OP) == 2) {
-    if (a.use_tm_attn) {
-      const attn_tm::BwdJob j = tm_bwd_job(a, l, dp);
-      attn_tm::dkdv_job(j, s, smem, tc);
-      stamp();
-      attn_tm::dq_job(j, s, smem, tc);
-      return;
-    }
-    if (a.use_tc_attn) { attn_tc_bwd_job<OP>(attn_tc_args<OP>(a, l), s, smem, dp); return; }
+    const attn_tm::BwdJob j = tm_bwd_job(a, l, dp);
+    attn_tm::dkdv_job(j, s, smem, tc);
+    stamp();
+    attn_tm::dq_job(j, s, smem, tc);
+  } else {
+    const AttnArgs t = attn_args<OP>(a, l);
+    if (a.D.hd == 64) attn_bwd_job<OP, 64>(t, s, (float*)smem);
+    else attn_bwd_job<OP, 16>(t, s, (float*)smem);
   }
-  const AttnArgs t = attn_args<OP>(a, l);
-  if (a.D.hd == 64) attn_bwd_job<OP, 64>(t, s, (float*)smem);
-  else attn_bwd_job<OP, 16>(t, s, (float*)smem);
 }
 
 // ===========================================================================
@@ -2207,10 +2192,9 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   const bool dep = a.deps != 0;
   unsigned* depc = abuf<unsigned>(a, A_DEP);
   auto DEPC = [&](int l, int kind) { return depc + dep_offset(D, l, kind); };
-  auto attn_deps = [&](int l, int tk, bool fwd) {
-    AttnDeps dp{nullptr, nullptr, 0u, nullptr, hdr, a.timeout_ns};
+  auto attn_deps = [&](int l, bool fwd) {
+    AttnDeps dp{nullptr, 0u, nullptr, hdr, a.timeout_ns};
     if (dep) {
-      dp.ticket = depc + ticket_offset(D, l, tk);
       if (fwd) {
         dp.wait = DEPC(l, DEP_QKV); dp.wtarget = (unsigned)(3 * D.hq / TC_BN);
         dp.sig = DEPC(l, DEP_O);
@@ -2238,7 +2222,7 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
       run_gemm<OP>(a, g, s, smem, tc); TJ(2);
     }
     if (!dep) MT_SYNC();
-    run_attn_fwd<OP>(a, l, s, smem, tc, attn_deps(l, TK_ATTN_FWD, true)); TJ(3);
+    run_attn_fwd<OP>(a, l, s, smem, tc, attn_deps(l, true)); TJ(3);
     if (!dep) MT_SYNC();
     {
       GemmDesc g = TK(gm.wo(l), l, TK_WO);
@@ -2317,13 +2301,13 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     if constexpr (sizeof(OP) == 2) {
       if (a.use_dsg) {
         // dK/dV stores dS^T; after a grid barrier dQ is a product over it
-        const attn_tm::BwdJob j = tm_bwd_job(a, l, attn_deps(l, TK_ATTN_BWD, false));
+        const attn_tm::BwdJob j = tm_bwd_job(a, l, attn_deps(l, false));
         attn_tm::dkdv_job(j, s, smem, tc); TJ(35);
         MT_SYNC();
         attn_tm::dqs_job(j, s, smem, tc); TJ(26);
       }
     }
-    if (!a.use_dsg) { run_attn_bwd<OP>(a, l, s, smem, tc, attn_deps(l, TK_ATTN_BWD, false), [&] { TJ(35); }); TJ(26); }
+    if (!a.use_dsg) { run_attn_bwd<OP>(a, l, s, smem, tc, attn_deps(l, false), [&] { TJ(35); }); TJ(26); }
     MT_SYNC();
     run_gemm<OP>(a, TK(gm.qkv_wgrad(l), l, TK_QKV_WGRAD), s, smem, tc); TJ(28);
     run_gemm<OP>(a, TK(gm.qkv_dgrad(l), l, TK_QKV_DGRAD), s, smem, tc); TJ(27);
@@ -2382,6 +2366,110 @@ __device__ void run_debug_gemm(const KArgs& a, char* smem, TcState& tc, Sched& s
     hdr->n_ctas = (int)gridDim.x;
     hdr->n_phases = 0;
   }
+}
+
+// ===========================================================================
+// single-op harness (mt_debug_run): one step of the update on inputs the
+// caller placed in the arena, run by the same jobs as the update
+// ===========================================================================
+// D = rowsum(dO * O) per (batch, head, position) from the stored dO and O
+// (the update forms it in the epilogue of the product that makes dO).
+template <class OP>
+__device__ __noinline__ void job_dsum(const KArgs& a, int l, Sched& s) {
+  const MtDims& D = a.D;
+  const OP* O = abuf<OP>(a, A_O) + (long long)l * D.T * D.hq;
+  const OP* dO = abuf<OP>(a, A_DO);
+  float* Ds = abuf<float>(a, A_DSUM);
+  const int lane = threadIdx.x & 31;
+  const long long n = (long long)D.T * D.H;
+  for (long long i = (long long)s.first() * MT_WARPS + (threadIdx.x >> 5); i < n; i += (long long)s.G * MT_WARPS) {
+    const int t = (int)(i / D.H), h = (int)(i % D.H);
+    float dot = 0.f;
+    for (int j = lane; j < D.hd; j += 32) {
+      const long long o = (long long)t * D.hq + (long long)h * D.hd + j;
+      dot = fmaf(to_f(dO[o]), to_f(O[o]), dot);
+    }
+    dot = warp_sum(dot);
+    if (lane == 0) Ds[((long long)(t / D.S) * D.H + h) * D.S + (t % D.S)] = dot;
+  }
+  s.next(s.G);
+}
+
+template <class OP>
+__device__ __noinline__ void run_op(const KArgs& a, char* smem, TcState& tc, Sched& s) {
+  const MtDims& D = a.D;
+  ArenaHdr* hdr = abuf<ArenaHdr>(a, A_HDR);
+  const unsigned G = gridDim.x;
+  const int l = a.dbg_layer;
+  int phase = 0;
+#define OP_SYNC()                                                          \
+  do {                                                                     \
+    if (!grid_barrier(hdr, G, a.timeout_ns, nullptr, false)) return;       \
+    ++phase;                                                               \
+  } while (0)
+  launch_prologue(a, s.first(), s.G);
+  OP_SYNC();
+  Gemms<OP> gm(a);
+  const AttnDeps nodeps{nullptr, 0u, nullptr, hdr, a.timeout_ns};
+  switch (a.debug_op) {
+    case MT_OP_ATTN_FWD:
+      run_attn_fwd<OP>(a, l, s, smem, tc, nodeps);
+      break;
+    case MT_OP_ATTN_BWD:
+      job_dsum<OP>(a, l, s);
+      OP_SYNC();
+      if constexpr (sizeof(OP) == 2) {
+        if (a.use_dsg) {
+          const attn_tm::BwdJob j = tm_bwd_job(a, l, nodeps);
+          attn_tm::dkdv_job(j, s, smem, tc);
+          OP_SYNC();
+          attn_tm::dqs_job(j, s, smem, tc);
+          break;
+        }
+      }
+      run_attn_bwd<OP>(a, l, s, smem, tc, nodeps, [] {});
+      break;
+    case MT_OP_ROUTER:
+      job_router<OP>(a, l, smem, nullptr, 0u, nullptr);
+      OP_SYNC();
+      job_route<OP>(a, l, smem);
+      break;
+    case MT_OP_LM_CE: {
+      GemmDesc g = gm.lm();
+      g.ticket = abuf<unsigned>(a, A_DEP) + ticket_offset(D, D.L, TK_LM);
+      run_gemm<OP>(a, g, s, smem, tc);
+      OP_SYNC();
+      job_ce<OP>(a, s, smem);
+      OP_SYNC();
+      job_loss(a);
+      break;
+    }
+    case MT_OP_CLIP_ADAMW:
+      job_norm_partial(a, (double*)smem);
+      OP_SYNC();
+      job_adamw<OP>(a, smem);
+      break;
+    default:
+      break;
+  }
+#undef OP_SYNC
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    hdr->micro_index = a.micro_index;
+    hdr->n_ctas = (int)G;
+    hdr->n_phases = phase;
+  }
+}
+
+// The single-op harness is its own kernel, so the update kernel's code is
+// the same with or without it.
+template <class OP>
+__global__ void __launch_bounds__(MT_THREADS, 1) mt_opkernel(const __grid_constant__ KArgs a) {
+  extern __shared__ __align__(1024) char smem[];
+  Sched s{(int)blockIdx.x, (int)gridDim.x, 0};
+  TcState tc;
+  tc_setup<OP>(a, smem, tc);
+  run_op<OP>(a, smem, tc, s);
+  tc_teardown<OP>(a, smem, tc);
 }
 
 template <class OP>

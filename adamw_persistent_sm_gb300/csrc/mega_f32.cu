@@ -6,6 +6,8 @@ cudaError_t mt_prepare_mega_f32(size_t smem, int* blocks_per_sm) {
   cudaError_t e = cudaFuncSetAttribute(mt_megakernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(mt_opkernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, mt_megakernel<float>, MT_THREADS, smem);
 }
 
@@ -21,4 +23,18 @@ cudaError_t mt_launch_mega_f32(const KArgs& a, int grid, size_t smem, cudaStream
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, mt_megakernel<float>, a);
+}
+
+cudaError_t mt_launch_op_f32(const KArgs& a, int grid, size_t smem, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(MT_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mt_opkernel<float>, a);
 }

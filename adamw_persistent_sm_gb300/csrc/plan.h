@@ -130,7 +130,7 @@ enum DepKind {
 // (tiles drawn in index order by whichever CTA is free); the head's set (layer
 // index L) holds the LM-head products and the optimizer sweep.
 enum TicketId {
-  TK_ATTN_FWD = 0, TK_ATTN_BWD, TK_ADAMW,
+  TK_ADAMW = 0,
   TK_QKV, TK_WO, TK_GATEUP, TK_DOWN,
   TK_DOWN_DGRAD, TK_DOWN_WGRAD, TK_GU_DGRAD, TK_GU_WGRAD, TK_WO_DGRAD, TK_WO_WGRAD, TK_QKV_DGRAD, TK_QKV_WGRAD,
   TK_LM = TK_QKV, TK_LM_DGRAD = TK_WO, TK_LM_WGRAD = TK_GATEUP
@@ -169,6 +169,8 @@ struct KArgs {
   char* arena;
   long long poff[P_COUNT];      // element offsets of each tensor in the flat buffers
   long long aoff[A_COUNT];      // byte offsets of each arena buffer
+  int debug_op;                 // single-op harness (mt_opkernel): MT_OP_* and its layer
+  int dbg_layer;
   int debug_gemm;               // test harness: run only the product described below
   const void* dbg_a; const void* dbg_b; float* dbg_c;
   int dbg_m, dbg_n, dbg_k, dbg_a_mn, dbg_b_mn, dbg_rag, dbg_nseg;
@@ -176,9 +178,7 @@ struct KArgs {
   int dbg_tma;                  // C written by the bulk-store epilogue (map MAP_E_Y fp32 / MAP_E_QKV bf16)
   const int* dbg_offs;
   int use_tc;                   // tcgen05 GEMMs (bf16 only)
-  int use_tc_attn;              // tensor-core attention (bf16 only)
-  int use_tm_attn;              // attention forward on tcgen05 with TMEM accumulators (needs use_tc)
-  int use_dsg;                  // dQ as a product over stored dS^T (A_DSG, MAP_E_DS/DSL; needs use_tm_attn)
+  int use_dsg;                  // dQ as a product over stored dS^T (A_DSG, MAP_E_DS/DSL; bf16 only)
   int deps;                     // dependency counters replace the grid barriers they cover
   int smem_bytes;               // dynamic shared memory of the launch
   CUtensorMap maps[MT_NMAPS];

@@ -102,6 +102,19 @@ class MoETrainer:
         for i, tok in enumerate(micro_tokens):
             self.micro_step(tok, i, step, flags)
 
+    def debug_run(self, op: int, layer: int = 0, tokens: torch.Tensor | None = None,
+                  step: int | None = None) -> None:
+        """One op of the single-op harness on the buffers of this trainer."""
+        if tokens is None:           # ops that read no token ids still take a valid buffer
+            tokens = torch.zeros(self.cfg.batch, self.cfg.seq, dtype=torch.int32, device=self.device)
+        tok = tokens.data_ptr()
+        hp = self.hparams(0, step)
+        st = B.mt_debug_run(op, layer, self.params.data_ptr(),
+                            self.shadow.data_ptr() if self.shadow is not None else 0,
+                            self.grads.data_ptr(), self.adam_m.data_ptr(), self.adam_v.data_ptr(),
+                            tok, hp, self.arena.data_ptr(), self.arena_bytes, self.stream)
+        _check(st, "mt_debug_run")
+
     def outputs(self) -> B.mt_outputs:
         return B.mt_read_outputs(self.arena.data_ptr(), self.stream)
 

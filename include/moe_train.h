@@ -52,19 +52,22 @@ typedef enum mt_status {
 
 enum { MT_PREC_FP32 = 0, MT_PREC_BF16 = 1 };
 
-/* hp.flags bits */
+/* hp.flags bits (any other bit is MT_ERR_ARG) */
 enum {
   MT_FLAG_TRACE = 1u << 0,        /* record per-CTA phase timestamps in the arena */
-  MT_FLAG_SIMT_GEMM = 1u << 1,    /* bf16 mode: use the CUDA-core GEMM instead of tcgen05 */
-  MT_FLAG_SIMT_ATTN = 1u << 2,    /* bf16 mode: use the CUDA-core attention */
   MT_FLAG_NO_OPTIMIZER = 1u << 3, /* skip clip + AdamW even on the last microbatch */
   MT_FLAG_TEST_STALL = 1u << 4,   /* test only: CTA 0 never arrives at the first grid
                                      barrier, so the others' bounded waits run out */
   MT_FLAG_BARRIERS_ONLY = 1u << 5, /* separate every phase by a grid barrier, even where
                                      per-block dependency counters would do (same
                                      results bit for bit; for comparison) */
-  MT_FLAG_MMA_SYNC_ATTN = 1u << 6 /* bf16 mode: attention forward and backward on warp-level
-                                     mma.sync instead of tcgen05 with TMEM accumulators */
+  /* Memory rules ("Open problems", Generality 2: what is stored and what is
+   * recomputed).  Each trades arena bytes for work; results are bit for bit
+   * those of the default plan. */
+  MT_FLAG_RECOMPUTE_ATTN_DS = 1u << 7, /* bf16: keep no dS^T of the attention backward
+                                          (batch*heads*seq^2 bf16 per launch); the dQ items
+                                          recompute P and dS instead of reading it */
+  MT_FLAGS_ALL = (1u << 0) | (1u << 3) | (1u << 4) | (1u << 5) | (1u << 7)
 };
 
 /*
@@ -74,10 +77,10 @@ enum {
  * d_ff F; this microbatch holds batch x seq tokens.
  * Implemented shapes (else MT_ERR_UNSUPPORTED): d a multiple of 32 and at
  * most 768; hd 16 or 64; F a multiple of 64; E <= 64 with E*d*4 <= 160 KiB;
- * K <= min(8, E); V a multiple of 8; L <= 16; seq >= 2.  The tensor-core
- * path (bf16) additionally needs batch*seq a multiple of 128, d, H*hd, V and
- * F multiples of 256, and hd = 64; attention on tensor cores needs seq a
- * multiple of 128.
+ * K <= min(8, E); V a multiple of 8; L <= 16; seq >= 2.  The bf16 model
+ * runs on the tensor cores only (tcgen05 products and attention) and
+ * additionally needs seq a multiple of 128, d, H*hd, V and F multiples of
+ * 256, and hd = 64.
  */
 typedef struct mt_hparams {
   int32_t vocab, d_model, n_layers, n_heads, head_dim, n_experts, top_k, d_ff;
@@ -137,11 +140,10 @@ int32_t mt_param_layout(const mt_hparams* hp, mt_tensor_desc* out, int32_t cap);
 /* Bytes of caller-provided device arena the launch needs (worst case over
  * routing), or a negative mt_status.  With MT_FLAG_TRACE in hp->flags the
  * arena also holds the per-CTA trace (MT_VIEW_TRACE), so traced launches
- * need an arena sized with that flag.  bf16 models on the tensor-core
- * attention path (neither MT_FLAG_SIMT_ATTN nor MT_FLAG_MMA_SYNC_ATTN) also
- * hold one layer's attention-backward dS^T, batch * heads * seq^2 bf16
- * values, so an arena must be sized with the flags of the launches that
- * use it. */
+ * need an arena sized with that flag.  bf16 models also hold one layer's
+ * attention-backward dS^T, batch * heads * seq^2 bf16 values, unless the
+ * memory rule MT_FLAG_RECOMPUTE_ATTN_DS is set; an arena must be sized with
+ * the flags of the launches that use it. */
 int64_t mt_arena_bytes(const mt_hparams* hp);
 
 /* Zero the arena's control header (barrier and status words).  Call once after
@@ -193,8 +195,24 @@ enum {
                                  t_leave) at [2p], then from [2*MT_TRACE_PHASES] for job
                                  stamp j < MT_TRACE_JOBS the pair (t_end, job id); ns */
   MT_VIEW_HIDDEN = 7,         /* fp32 [T, d] residual stream entering `layer` (layer = L: final) */
-  MT_VIEW_LOGITS = 8          /* operand type [T, V]: LM-head logits (bf16 or fp32), overwritten
+  MT_VIEW_LOGITS = 8,         /* operand type [T, V]: LM-head logits (bf16 or fp32), overwritten
                                  in place by dlogits during the same launch */
+  /* Buffers the single-op harness (mt_debug_run) reads and writes.  "op" is
+   * the operand type: bf16 for MT_PREC_BF16, fp32 for MT_PREC_FP32. */
+  MT_VIEW_QKV = 9,            /* op [T, 3*H*hd] of `layer`: q and k after RoPE, v; head h owns
+                                 columns h*hd..(h+1)*hd-1 of each of the three blocks */
+  MT_VIEW_ATTN_O = 10,        /* op [T, H*hd] of `layer`: attention output */
+  MT_VIEW_LSE = 11,           /* fp32 [B*H, S] of `layer`: row log-sum-exp of the scaled scores;
+                                 natural log for MT_PREC_FP32, base-2 log for MT_PREC_BF16
+                                 (log2 of the row sum of exp2(log2(e) q.k / sqrt(hd))) */
+  MT_VIEW_DOUT = 12,          /* op [T, H*hd]: gradient wrt the attention output (one layer at a time) */
+  MT_VIEW_DSUM = 13,          /* fp32 [B*H, S]: rowsum(dO * O) of the attention backward */
+  MT_VIEW_DQKV = 14,          /* op [T, 3*H*hd]: gradient wrt q, k (before RoPE) and v */
+  MT_VIEW_XMID = 15,          /* fp32 [T, d] of `layer`: residual stream after attention */
+  MT_VIEW_R2 = 16,            /* op [T, d] of `layer`: expert RMSNorm output (router input) */
+  MT_VIEW_EXPERT_IN = 17,     /* op [Pmax, d] of `layer`: expert inputs in expert order (rows of
+                                 MT_VIEW_ROUTE_PERM; pad rows zero) */
+  MT_VIEW_FINAL_NORM = 18     /* op [T, d]: final RMSNorm output (LM-head input) */
 };
 typedef struct mt_view {
   void* ptr;
@@ -203,6 +221,44 @@ typedef struct mt_view {
 } mt_view;
 int32_t mt_debug_view(const void* arena, const mt_hparams* hp, int32_t which, int32_t layer,
                       mt_view* out);
+
+/*
+ * Single-op parity harness (tests): run ONE step of the update on inputs the
+ * caller has written into the arena (through mt_debug_view pointers) and into
+ * the parameter buffers, with the same device code the update uses.  Every
+ * op is one cooperative launch on `stream`; its outputs are read back through
+ * mt_debug_view and mt_read_outputs.  Arguments are those of mt_train_update
+ * (hp describes the model and the microbatch; the arena must be initialised
+ * with mt_arena_init and sized by mt_arena_bytes(hp)) plus:
+ *   op     one of MT_OP_*;
+ *   layer  the layer whose per-layer buffers the op reads and writes.
+ * Errors as mt_train_update; MT_ERR_ARG for an unknown op or layer.
+ */
+enum {
+  /* Causal attention forward ("1 - Describe the model and update": bf16
+   * attention): MT_VIEW_QKV -> MT_VIEW_ATTN_O, MT_VIEW_LSE. */
+  MT_OP_ATTN_FWD = 1,
+  /* Causal attention backward: MT_VIEW_QKV, MT_VIEW_ATTN_O, MT_VIEW_LSE (as the
+   * forward left them) and MT_VIEW_DOUT -> MT_VIEW_DSUM, MT_VIEW_DQKV. */
+  MT_OP_ATTN_BWD = 2,
+  /* Expert RMSNorm, router logits, token_topk and route_order with the
+   * dispatch gather (same section): MT_VIEW_XMID and the moe_norm / router
+   * parameters -> MT_VIEW_R2, MT_VIEW_ROUTER_LOGITS, MT_VIEW_TOPK_IDX,
+   * MT_VIEW_TOPK_W, MT_VIEW_ROUTE_OFFS, MT_VIEW_ROUTE_PERM, MT_VIEW_EXPERT_IN
+   * and the expert counts of mt_outputs. */
+  MT_OP_ROUTER = 3,
+  /* LM head and fused next-token cross-entropy ("2 - Capture": labels and
+   * coefficients): MT_VIEW_FINAL_NORM, lm_head, tokens -> MT_VIEW_TOK_LOSS,
+   * the loss of mt_outputs and dlogits in MT_VIEW_LOGITS. */
+  MT_OP_LM_CE = 4,
+  /* Global-norm clipping and AdamW ("1 - Describe the model and update"):
+   * params, grads, adam_m, adam_v (hp->step, lr, ...) -> updated params, m, v,
+   * the bf16 shadow, and grad_norm / clip_coef of mt_outputs. */
+  MT_OP_CLIP_ADAMW = 5
+};
+int32_t mt_debug_run(int32_t op, int32_t layer, float* params, void* shadow, float* grads, float* adam_m,
+                     float* adam_v, const int32_t* tokens, const mt_hparams* hp, void* arena,
+                     int64_t arena_bytes, void* stream);
 
 /*
  * mt_train_update_noalloc - the same launch as mt_train_update, but with no
@@ -242,8 +298,9 @@ int32_t mt_train_update_noalloc(float* params, void* shadow, float* grads, float
 
 /*
  * Test harness: one matrix product C = A * B^T through the megakernel's product
- * engine (tcgen05 tensor cores when precision == MT_PREC_BF16 and use_tc != 0,
- * CUDA cores otherwise), fp32 accumulation, fp32 C.  Used by the tests to check
+ * engine (tcgen05 tensor cores for MT_PREC_BF16, which then needs bit 0 of
+ * use_tc set, else MT_ERR_UNSUPPORTED; the fp32 model's CUDA-core engine for
+ * MT_PREC_FP32), fp32 accumulation, fp32 C.  Used by the tests to check
  * every operand layout of the update's products ("1 - Describe the model and
  * update": dense products and ragged_mm) in isolation.
  *   rag = 0: A is [M,K] (a_mn = 0) or [K,M] (a_mn = 1); B is [N,K] (b_mn = 0)

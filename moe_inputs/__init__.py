@@ -173,3 +173,21 @@ def make_update_tokens(cfg: MoEConfig) -> list[np.ndarray]:
 
 def zeros_like_params(cfg: MoEConfig) -> dict[str, np.ndarray]:
     return {name: np.zeros(shape, dtype=np.float32) for name, shape in param_shapes(cfg)}
+
+
+# ---------------------------------------------------------------------------
+# Seeded operands for the single-op tests (draws only)
+# ---------------------------------------------------------------------------
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """fp32 copy of x holding the nearest bfloat16 values (ties to even), so
+    that a bf16 device buffer and a float64 host copy hold the same numbers."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16 << 16
+    return (b & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
+
+
+def normal_operand(shape, seed: int, std: float = 1.0, mean: float = 0.0,
+                   bf16: bool = False) -> np.ndarray:
+    """Seeded N(mean, std) fp32 array; bf16-representable when ``bf16``."""
+    x = np.random.default_rng(seed).normal(mean, std, size=shape).astype(np.float32)
+    return round_to_bf16(x) if bf16 else x

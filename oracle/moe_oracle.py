@@ -131,6 +131,16 @@ def causal_attention(q, k, v):
     return o
 
 
+def causal_logsumexp(q, k):
+    """Row log-sum-exp of the scaled causal scores q k^T / sqrt(hd) (keys
+    j <= i) for one (batch, head): the normaliser of the attention softmax."""
+    S, hd = q.shape
+    s = (q @ k.T) / math.sqrt(hd)
+    s = np.where(np.tril(np.ones((S, S), dtype=bool)), s, -np.inf)
+    m = s.max(axis=1)
+    return m + np.log(np.sum(np.exp(s - m[:, None]), axis=1))
+
+
 def causal_attention_backward(do, q, k, v):
     """Gradients of :func:`causal_attention` wrt q, k, v (P recomputed)."""
     B, H, S, hd = q.shape

@@ -123,16 +123,33 @@ def test_trace_arena_is_sized_by_the_trace_flag():
     assert plain <= B.MT_NOALLOC_ARENA_BYTES
 
 
-def test_arena_holds_the_attention_ds_buffer_on_the_tensor_core_path():
-    """bf16 models on the tcgen05 attention path keep one layer's dS^T
-    (batch x heads x seq^2 bf16) for the dQ product; the CUDA-core and
-    warp-MMA attention paths and the fp32 model do not."""
+def test_arena_holds_the_attention_ds_buffer_unless_recomputed():
+    """bf16 models keep one layer's dS^T (batch x heads x seq^2 bf16) for the
+    dQ product; the memory rule MT_FLAG_RECOMPUTE_ATTN_DS drops it, and the
+    fp32 model never holds it."""
     from adamw_persistent_sm_gb300 import binding as B
     cfg = mi.get_config("b2")
     ds = cfg.batch * cfg.n_heads * cfg.seq * cfg.seq * 2
-    tm = B.mt_arena_bytes(B.hparams(cfg))
-    for flag in (B.MT_FLAG_SIMT_ATTN, B.MT_FLAG_MMA_SYNC_ATTN):
-        other = B.mt_arena_bytes(B.hparams(cfg, flags=flag))
-        assert ds <= tm - other < ds + 4096
+    keep = B.mt_arena_bytes(B.hparams(cfg))
+    drop = B.mt_arena_bytes(B.hparams(cfg, flags=B.MT_FLAG_RECOMPUTE_ATTN_DS))
+    assert ds <= keep - drop < ds + 4096
     tiny = B.mt_arena_bytes(B.hparams(mi.get_config("tiny")))
     assert tiny <= B.MT_NOALLOC_ARENA_BYTES
+
+
+def test_unknown_flags_and_untiled_bf16_shapes_are_refused():
+    """Retired or unknown flag bits are argument errors; a bf16 model whose
+    shapes the tensor-core tiles do not cover is refused (there is no
+    CUDA-core fallback for bf16)."""
+    from adamw_persistent_sm_gb300 import binding as B
+    cfg = mi.get_config("b2")
+    for bit in (1, 2, 6, 8, 31):
+        assert B.mt_arena_bytes(B.hparams(cfg, flags=1 << bit)) == -B.MT_ERR_ARG
+    fake = 1 << 20
+    args = (fake, fake, fake, fake, fake, fake)
+    bad = B.hparams(cfg.replace(seq=1000))          # not a multiple of 128
+    need = B.mt_arena_bytes(bad)
+    assert need > 0
+    assert B.mt_train_update(*args, bad, fake, need) == B.MT_ERR_UNSUPPORTED
+    bad = B.hparams(cfg.replace(d_ff=320))          # not a multiple of 256
+    assert B.mt_train_update(*args, bad, fake, B.mt_arena_bytes(bad)) == B.MT_ERR_UNSUPPORTED

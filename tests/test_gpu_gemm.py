@@ -1,8 +1,8 @@
 """The product engine in isolation (mt_debug_gemm): every operand layout the
 update uses - K-major and MN-major A and B, ragged rows (expert segments of
 ragged_mm) and ragged reductions (expert weight gradients) - on the
-tensor-core path and on the CUDA-core path, against a float64 product of the
-same bf16 inputs."""
+tensor-core path (bf16 operands) and on the CUDA-core path of the fp32 model
+(the same bf16-valued inputs held in fp32), against a float64 product."""
 import numpy as np
 import pytest
 import torch
@@ -22,6 +22,8 @@ def _arena():
 def _run(A, a_mn, Bm, b_mn, M, N, K, rag=0, offs=None, nseg=0, use_tc=1, out_shape=None):
     from adamw_persistent_sm_gb300 import binding as B
     arena = _arena()
+    if not (use_tc & 1):                 # the CUDA-core engine is the fp32 model's
+        A, Bm = A.float(), Bm.float()
     C = torch.full(out_shape or (M, N), float("nan"), dtype=torch.float32, device="cuda")
     prec = B.MT_PREC_BF16 if A.dtype == torch.bfloat16 else B.MT_PREC_FP32
     st = B.mt_debug_gemm(A.data_ptr(), a_mn, Bm.data_ptr(), b_mn, C.data_ptr(), M, N, K, rag,
@@ -138,3 +140,15 @@ def test_bulk_store_epilogue(bf16_out, rag):
     else:
         ref = a.double() @ w.double().t()
     assert _rel(bulk, ref) < (1e-2 if bf16_out else TOL)
+
+
+def test_bf16_operands_have_no_cuda_core_path():
+    from adamw_persistent_sm_gb300 import binding as B
+    arena = _arena()
+    a = torch.zeros(128, 64, dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros(256, 64, dtype=torch.bfloat16, device="cuda")
+    c = torch.zeros(128, 256, dtype=torch.float32, device="cuda")
+    st = B.mt_debug_gemm(a.data_ptr(), 0, b.data_ptr(), 0, c.data_ptr(), 128, 256, 64, 0, 0, 0,
+                         B.MT_PREC_BF16, 0, arena.data_ptr(), arena.numel(),
+                         torch.cuda.current_stream().cuda_stream)
+    assert st == B.MT_ERR_UNSUPPORTED

@@ -76,6 +76,18 @@ def test_causal_attention_backward_matches_autograd():
         np.testing.assert_allclose(a, b.grad.numpy(), rtol=1e-10, atol=1e-12)
 
 
+def test_causal_logsumexp_matches_torch():
+    rng = np.random.default_rng(22)
+    q, k = rng.normal(size=(9, 16)), rng.normal(size=(9, 16))
+    lse = oracle.causal_logsumexp(q, k)
+    s = torch.tensor(q @ k.T / 4.0)
+    s = s.masked_fill(~torch.tril(torch.ones(9, 9, dtype=torch.bool)), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=1).numpy(), rtol=1e-14)
+    # p = exp(s - lse) is the oracle's softmax
+    p = oracle.moe_oracle._causal_probs(q, k)
+    np.testing.assert_allclose(p, np.exp(s.numpy() - lse[:, None]), rtol=1e-12, atol=1e-300)
+
+
 def test_first_query_attends_only_to_itself():
     rng = np.random.default_rng(4)
     q, k, v = (rng.normal(size=(1, 1, 9, 4)) for _ in range(3))
