@@ -30,6 +30,7 @@ MT_FLAG_NO_OPTIMIZER = 1 << 3
 MT_FLAG_TEST_STALL = 1 << 4
 MT_FLAG_BARRIERS_ONLY = 1 << 5
 MT_FLAG_RECOMPUTE_ATTN_DS = 1 << 7
+MT_FLAG_SELECTIVE_EXPERTS = 1 << 8
 
 MT_MAX_LAYERS = 16
 MT_MAX_EXPERTS = 64
@@ -75,7 +76,7 @@ class mt_hparams(C.Structure):
         ("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float),
         ("weight_decay", C.c_float), ("clip_norm", C.c_float), ("clip_eps", C.c_float),
         ("norm_eps", C.c_float), ("rope_theta", C.c_float), ("loss_coef", C.c_float),
-        ("wait_timeout_ns", C.c_int64),
+        ("wait_timeout_ns", C.c_int64), ("expert_step", C.c_int64),
     ]
 
 
@@ -89,7 +90,9 @@ class mt_outputs(C.Structure):
                 ("optimizer_ran", C.c_int32), ("loss", C.c_float), ("loss_update", C.c_float),
                 ("grad_norm", C.c_float), ("clip_coef", C.c_float), ("n_ctas", C.c_int32),
                 ("n_phases", C.c_int32),
-                ("expert_counts", C.c_int32 * (MT_MAX_LAYERS * MT_MAX_EXPERTS))]
+                ("expert_counts", C.c_int32 * (MT_MAX_LAYERS * MT_MAX_EXPERTS)),
+                ("experts_updated", C.c_int32), ("expert_grad_norm", C.c_float),
+                ("expert_clip_coef", C.c_float)]
 
 
 class mt_view(C.Structure):
@@ -141,7 +144,7 @@ def load(build_if_missing: bool = False) -> C.CDLL:
 
 
 def hparams(cfg, micro_index: int = 0, flags: int = 0, step: int | None = None,
-            wait_timeout_ns: int = 0, loss_coef: float = 0.0) -> mt_hparams:
+            wait_timeout_ns: int = 0, loss_coef: float = 0.0, expert_step: int = 1) -> mt_hparams:
     """mt_hparams from any object with the configuration's attribute names."""
     hp = mt_hparams()
     hp.vocab, hp.d_model, hp.n_layers = cfg.vocab, cfg.d_model, cfg.n_layers
@@ -156,6 +159,7 @@ def hparams(cfg, micro_index: int = 0, flags: int = 0, step: int | None = None,
     hp.norm_eps, hp.rope_theta = cfg.norm_eps, cfg.rope_theta
     hp.loss_coef = loss_coef
     hp.wait_timeout_ns = wait_timeout_ns
+    hp.expert_step = expert_step
     return hp
 
 

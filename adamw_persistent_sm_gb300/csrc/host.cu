@@ -15,6 +15,9 @@
 #include "tmaps.h"
 #include "gemm_tc.cuh"
 
+static_assert(sizeof(mt_hparams) == 120, "mt_hparams layout is part of the ABI");
+static_assert(sizeof(mt_outputs) == 40 + 4 * MT_MAX_LAYERS * MT_MAX_EXPERTS + 12, "mt_outputs layout");
+
 namespace {
 
 constexpr long long kAlign = 1024;
@@ -35,6 +38,7 @@ int check_hparams(const mt_hparams* hp) {
   if (hp->flags & ~(uint32_t)MT_FLAGS_ALL) return MT_ERR_ARG;
   if (hp->micro_count <= 0 || hp->micro_index < 0 || hp->micro_index >= hp->micro_count) return MT_ERR_ARG;
   if (hp->step < 1) return MT_ERR_ARG;
+  if ((hp->flags & MT_FLAG_SELECTIVE_EXPERTS) && hp->expert_step < 1) return MT_ERR_ARG;
   if (!(hp->lr >= 0.f) || !(hp->beta1 >= 0.f && hp->beta1 < 1.f) || !(hp->beta2 >= 0.f && hp->beta2 < 1.f) ||
       !(hp->eps > 0.f) || !(hp->weight_decay >= 0.f) || !(hp->clip_norm > 0.f) || !(hp->clip_eps >= 0.f) ||
       !(hp->norm_eps > 0.f) || !(hp->rope_theta > 0.f) || !(hp->loss_coef >= 0.f) || hp->wait_timeout_ns < 0)
@@ -121,7 +125,7 @@ void make_plan(const mt_hparams* hp, MtPlan* P) {
   sz[A_DRF] = T * d * 4;
   sz[A_PART] = (long long)D.nch * (D.E + 2) * d * 4;
   sz[A_KPART] = 8LL * 3 * D.hq * d * 4;
-  sz[A_NORMPART] = (long long)D.nch * 8;
+  sz[A_NORMPART] = (long long)MT_OPT_RANGES * D.nch * 8;
   sz[A_DEP] = dep_words(D) * 4;
   // the per-CTA trace exists only in arenas sized for traced launches
   sz[A_TRACE] = (hp->flags & MT_FLAG_TRACE) ? (long long)D.nch * MT_TRACE_WORDS * 8 : 0;
@@ -212,6 +216,26 @@ int launch_update(int op, int layer, float* params, void* shadow, float* grads, 
 
 }  // namespace
 
+// Every host-side check of a training-update launch, in the order the launch
+// makes them; nothing is enqueued.
+int mt_check_update_args(const float* params, const void* shadow, const float* grads, const float* adam_m,
+                         const float* adam_v, const int32_t* tokens, const mt_hparams* hp, const void* arena,
+                         int64_t arena_bytes) {
+  int st = check_hparams(hp);
+  if (st) return st;
+  const bool bf16 = hp->precision == MT_PREC_BF16;
+  if (!params || !grads || !adam_m || !adam_v || !tokens || !arena) return MT_ERR_ARG;
+  if (bf16 && !shadow) return MT_ERR_ARG;
+  if (!aligned(params, 256) || !aligned(grads, 256) || !aligned(adam_m, 256) || !aligned(adam_v, 256) ||
+      !aligned(arena, 256) || !aligned(tokens, 16) || (shadow && !aligned(shadow, 256)))
+    return MT_ERR_ARG;
+  MtPlan P;
+  make_plan(hp, &P);
+  if (arena_bytes < P.arena_bytes) return MT_ERR_ARENA_SMALL;
+  if (bf16 && !tc_shapes_ok(hp)) return MT_ERR_UNSUPPORTED;
+  return MT_OK;
+}
+
 extern "C" {
 
 int64_t mt_param_count(const mt_hparams* hp) {
@@ -282,19 +306,12 @@ namespace {
 // One launch of the update (op == 0) or of one op of the single-op harness.
 int launch_update(int op, int layer, float* params, void* shadow, float* grads, float* adam_m, float* adam_v,
                   const int32_t* tokens, const mt_hparams* hp, void* arena, int64_t arena_bytes, void* stream) {
-  int st = check_hparams(hp);
+  int st = mt_check_update_args(params, shadow, grads, adam_m, adam_v, tokens, hp, arena, arena_bytes);
   if (st) return st;
   const bool bf16 = hp->precision == MT_PREC_BF16;
-  if (!params || !grads || !adam_m || !adam_v || !tokens || !arena) return MT_ERR_ARG;
-  if (bf16 && !shadow) return MT_ERR_ARG;
-  if (!aligned(params, 256) || !aligned(grads, 256) || !aligned(adam_m, 256) || !aligned(adam_v, 256) ||
-      !aligned(arena, 256) || !aligned(tokens, 16) || (shadow && !aligned(shadow, 256)))
-    return MT_ERR_ARG;
   MtPlan P;
   make_plan(hp, &P);
-  if (arena_bytes < P.arena_bytes) return MT_ERR_ARENA_SMALL;
   const bool want_tc = bf16;
-  if (bf16 && !tc_shapes_ok(hp)) return MT_ERR_UNSUPPORTED;
 
   int grid = 0;
   st = prepare_launch(bf16, smem_bytes(P.D, want_tc), &grid);
@@ -307,14 +324,58 @@ int launch_update(int op, int layer, float* params, void* shadow, float* grads, 
   a->lr = hp->lr; a->beta1 = hp->beta1; a->beta2 = hp->beta2; a->eps = hp->eps; a->wd = hp->weight_decay;
   a->clip = hp->clip_norm; a->clip_eps = hp->clip_eps; a->norm_eps = hp->norm_eps;
   a->rope_theta = hp->rope_theta;
-  const double ntargets = (double)hp->batch * (hp->seq - 1) * hp->micro_count;
+  const bool selective = (hp->flags & MT_FLAG_SELECTIVE_EXPERTS) != 0;
+  // every target of an update weighs 1 / (its targets); under selective
+  // updates each microbatch is an update of the shared tensors
+  const double ntargets = (double)hp->batch * (hp->seq - 1) * (selective ? 1 : hp->micro_count);
   a->coef = hp->loss_coef > 0.f ? hp->loss_coef : (float)(1.0 / ntargets);
-  a->ibc1 = (float)(1.0 / (1.0 - pow((double)hp->beta1, (double)hp->step)));
-  a->ibc2 = (float)(1.0 / (1.0 - pow((double)hp->beta2, (double)hp->step)));
   a->decay = (float)(1.0 - (double)hp->lr * (double)hp->weight_decay);
   a->micro_index = hp->micro_index;
   a->micro_count = hp->micro_count;
-  a->run_opt = (hp->micro_index == hp->micro_count - 1) && !(hp->flags & MT_FLAG_NO_OPTIMIZER);
+  const bool last = hp->micro_index == hp->micro_count - 1;
+  const bool opt = !(hp->flags & MT_FLAG_NO_OPTIMIZER);
+  a->run_opt = opt && (last || selective);
+  auto group = [&](int gi, long long step, float gscale, int r0, int nr) {
+    OptGroup& g = a->ogrp[gi];
+    g.ibc1 = (float)(1.0 / (1.0 - pow((double)hp->beta1, (double)step)));
+    g.ibc2 = (float)(1.0 / (1.0 - pow((double)hp->beta2, (double)step)));
+    g.gscale = gscale;
+    g.r0 = r0;
+    g.nr = nr;
+  };
+  auto range = [&](int ri, long long off, long long n, int gi, int first) {
+    a->orng[ri] = OptRange{off, n, gi, first};
+  };
+  const unsigned all = (1u << P_COUNT) - 1u;
+  const unsigned experts = (1u << P_WGATE) | (1u << P_WUP) | (1u << P_WDOWN);
+  if (!selective) {
+    // one clipped AdamW step over every tensor after the last microbatch
+    a->acc_mask = hp->micro_index > 0 ? all : 0u;
+    a->n_ranges = 0;
+    if (a->run_opt) {
+      range(0, 0, P.n_params, 0, 1);
+      group(0, hp->step, 1.0f, 0, 1);
+      a->n_ranges = 1;
+    }
+  } else {
+    // shared tensors (all but the expert products): a step after every
+    // microbatch; expert tensors: gradients summed over micro_count
+    // microbatches, a step on their mean after the last
+    a->acc_mask = hp->micro_index > 0 ? experts : 0u;
+    a->n_ranges = 0;
+    if (opt) {
+      const long long e0 = P.poff[P_WGATE], e1 = P.poff[P_FINAL_NORM];
+      range(0, 0, e0, 0, 1);
+      range(1, e1, P.n_params - e1, 0, 0);
+      group(0, hp->step, 1.0f, 0, 2);
+      a->n_ranges = 2;
+      if (last) {
+        range(2, e0, e1 - e0, 1, 1);
+        group(1, hp->expert_step, 1.0f / (float)hp->micro_count, 2, 1);
+        a->n_ranges = 3;
+      }
+    }
+  }
   a->flags = hp->flags;
   a->timeout_ns = hp->wait_timeout_ns > 0 ? hp->wait_timeout_ns : 4000000000LL;
   a->n_params = P.n_params;
@@ -366,6 +427,9 @@ int32_t mt_read_outputs(const void* arena, mt_outputs* out, void* stream) {
   out->n_ctas = h.n_ctas;
   out->n_phases = h.n_phases;
   memcpy(out->expert_counts, h.expert_counts, sizeof(out->expert_counts));
+  out->experts_updated = h.experts_updated;
+  out->expert_grad_norm = h.expert_grad_norm;
+  out->expert_clip_coef = h.expert_clip_coef;
   return h.status;
 }
 

@@ -32,6 +32,10 @@ __device__ __forceinline__ const OP* pweight(const KArgs& a, int pid) {
   else return (const OP*)a.shadow + a.poff[pid];
 }
 __device__ __forceinline__ float* pgrad(const KArgs& a, int pid) { return a.grads + a.poff[pid]; }
+// Whether this launch adds tensor pid's gradient into the buffer (else it
+// overwrites it): every tensor after the first microbatch of an update, and
+// under selective updates only the expert tensors.
+__device__ __forceinline__ bool acc_of(const KArgs& a, int pid) { return (a.acc_mask >> pid) & 1u; }
 
 // Column tiles of the LM-head product (one cross-entropy partial each).
 template <class OP>
@@ -1524,13 +1528,14 @@ static __device__ __noinline__ int job_router_grad(const KArgs& a, int l, Sched&
 // out[r][col] (+)= sum over chunks of PART[chunk][row0 + r][col]; E_kind is
 // the router-row count of the reduction that wrote those rows (0: gain only).
 static __device__ __noinline__ void job_colfinal(const KArgs& a, int row0, int nrows, int E_kind, float* out_rows,
-                                                 float* out_last, int last_is_separate, Sched& s, int nchunks = 0) {
+                                                 float* out_last, int last_is_separate, Sched& s, int nchunks,
+                                                 int pid) {
   const MtDims& D = a.D;
   const int G = s.G;
   const int nused = nchunks > 0 ? nchunks : col_nchunks(D, G, E_kind);
   const float* PART = abuf<float>(a, A_PART);
   const int n = nrows * D.d;
-  const bool acc = a.micro_index > 0;
+  const bool acc = acc_of(a, pid);
   for (int e = s.first() * MT_THREADS + threadIdx.x; e < n; e += G * MT_THREADS) {
     const int r = e / D.d, col = e % D.d;
     float v = 0.f;
@@ -1552,7 +1557,7 @@ static __device__ __noinline__ void job_embed_bwd(const KArgs& a, int* ism) {
   float* dE = pgrad(a, P_EMB);
   const float* DX = abuf<float>(a, A_DX);
   const int n4 = D.d / 4;
-  if (a.micro_index == 0) {
+  if (!acc_of(a, P_EMB)) {
     float4* z = reinterpret_cast<float4*>(dE + (long long)v0 * D.d);
     const long long nz = (long long)(v1 - v0) * n4;
     for (long long e = threadIdx.x; e < nz; e += MT_THREADS) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1612,13 +1617,16 @@ static __device__ __noinline__ void job_loss(const KArgs& a) {
   }
 }
 
-// Global gradient norm, first level: CTA c sums squares over its slice.
-static __device__ __noinline__ void job_norm_partial(const KArgs& a, double* dsm) {
+// Global gradient norm, first level: CTA c sums squares over its slice of
+// optimizer range ri (the range's partials go to slot ri).
+static __device__ __noinline__ void job_norm_partial(const KArgs& a, double* dsm, int ri) {
   const int c = blockIdx.x, G = gridDim.x;
-  const long long n = a.n_params;
+  const OptRange& R = a.orng[ri];
+  const float* gr = a.grads + R.off;
+  const long long n = R.n;
   const long long n4 = n / 4;
   const long long b0 = n4 * c / G, b1 = n4 * (c + 1) / G;
-  const float4* g4 = reinterpret_cast<const float4*>(a.grads);
+  const float4* g4 = reinterpret_cast<const float4*>(gr);
   double acc = 0.0;
   float facc = 0.f;
   // four float4 loads in flight per thread; fp32 partial sums of 16 squares
@@ -1646,7 +1654,7 @@ static __device__ __noinline__ void job_norm_partial(const KArgs& a, double* dsm
     facc = fmaf(v.w, v.w, facc);
   }
   if (c == G - 1)
-    for (long long i = n4 * 4 + threadIdx.x; i < n; i += MT_THREADS) facc = fmaf(a.grads[i], a.grads[i], facc);
+    for (long long i = n4 * 4 + threadIdx.x; i < n; i += MT_THREADS) facc = fmaf(gr[i], gr[i], facc);
   acc += facc;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -1655,7 +1663,7 @@ static __device__ __noinline__ void job_norm_partial(const KArgs& a, double* dsm
   if (threadIdx.x == 0) {
     double t = 0.0;
     for (int w = 0; w < MT_WARPS; ++w) t += dsm[w];
-    reinterpret_cast<double*>(abuf<float>(a, A_NORMPART))[c] = t;
+    reinterpret_cast<double*>(abuf<float>(a, A_NORMPART))[(long long)ri * MT_MAX_CTAS + c] = t;
   }
 }
 
@@ -1667,10 +1675,10 @@ struct AwConst {
   float ibc1, ibc2;         // 1 / (1 - beta^t)
   float lr, eps;
 };
-__device__ __forceinline__ AwConst aw_const(const KArgs& a, float c) {
+__device__ __forceinline__ AwConst aw_const(const KArgs& a, const OptGroup& og, float c) {
   AwConst k;
   k.c = c; k.decay = a.decay; k.b1 = a.beta1; k.omb1 = 1.0f - a.beta1; k.b2 = a.beta2; k.omb2 = 1.0f - a.beta2;
-  k.ibc1 = a.ibc1; k.ibc2 = a.ibc2; k.lr = a.lr; k.eps = a.eps;
+  k.ibc1 = og.ibc1; k.ibc2 = og.ibc2; k.lr = a.lr; k.eps = a.eps;
   return k;
 }
 // One parameter: g <- c g; p <- (1 - lr wd) p; m, v moving averages;
@@ -1687,30 +1695,44 @@ __device__ __forceinline__ void adamw_elem(const AwConst& k, float& p, float g, 
   p -= __fdividef(k.lr * mh, sqrtf(vh) + k.eps);
 }
 
-// Clip coefficient from the ordered sum of the partials, then the AdamW sweep
-// over CTA c's slice (float4 loads; writes p, m, v and the bf16 shadow).
+// Clip coefficient of range ri's group from the ordered sum of the group's
+// partials, then the AdamW sweep over the range (float4 loads; writes p, m, v
+// and the bf16 shadow).  The group's step uses gscale * g, clipped.
 template <class OP>
-__device__ __noinline__ void job_adamw(const KArgs& a, char* smem) {
+__device__ __noinline__ void job_adamw(const KArgs& a, char* smem, int ri) {
   const int c = blockIdx.x, G = gridDim.x;
+  const OptRange& R = a.orng[ri];
+  const OptGroup& og = a.ogrp[R.group];
   const double* parts = reinterpret_cast<const double*>(abuf<float>(a, A_NORMPART));
   double tot = 0.0;
-  for (int i = 0; i < G; ++i) tot += parts[i];
-  const float norm = (float)sqrt(tot);
+  for (int r = og.r0; r < og.r0 + og.nr; ++r)
+    for (int i = 0; i < G; ++i) tot += parts[(long long)r * MT_MAX_CTAS + i];
+  const float norm = (float)sqrt(tot) * og.gscale;
   const float coef = fminf(1.0f, a.clip / (norm + a.clip_eps));
-  const AwConst ak = aw_const(a, coef);
-  if (c == 0 && threadIdx.x == 0) {
+  const AwConst ak = aw_const(a, og, coef * og.gscale);
+  if (c == 0 && threadIdx.x == 0 && R.first) {
     ArenaHdr* h = abuf<ArenaHdr>(a, A_HDR);
-    h->grad_norm = norm;
-    h->clip_coef = coef;
-    h->optimizer_ran = 1;
+    if (R.group == 0) {
+      h->grad_norm = norm;
+      h->clip_coef = coef;
+      h->optimizer_ran = 1;
+    } else {
+      h->expert_grad_norm = norm;
+      h->expert_clip_coef = coef;
+      h->experts_updated = 1;
+    }
   }
-  const long long n = a.n_params;
+  const long long n = R.n;
   const long long n4 = n / 4;
-  float4* p4 = reinterpret_cast<float4*>(a.master);
-  const float4* g4 = reinterpret_cast<const float4*>(a.grads);
-  float4* m4 = reinterpret_cast<float4*>(a.adam_m);
-  float4* v4 = reinterpret_cast<float4*>(a.adam_v);
-  __nv_bfloat16* sh = (sizeof(OP) == 2) ? (__nv_bfloat16*)a.shadow : nullptr;
+  float* const pm = a.master + R.off;
+  const float* const gr = a.grads + R.off;
+  float* const mm_ = a.adam_m + R.off;
+  float* const vv_ = a.adam_v + R.off;
+  float4* p4 = reinterpret_cast<float4*>(pm);
+  const float4* g4 = reinterpret_cast<const float4*>(gr);
+  float4* m4 = reinterpret_cast<float4*>(mm_);
+  float4* v4 = reinterpret_cast<float4*>(vv_);
+  __nv_bfloat16* sh = (sizeof(OP) == 2) ? (__nv_bfloat16*)a.shadow + R.off : nullptr;
   auto step4 = [&](long long j, float4 p, const float4 g, float4 m, float4 v) {
     adamw_elem(ak, p.x, g.x, m.x, v.x);
     adamw_elem(ak, p.y, g.y, m.y, v.y);
@@ -1743,7 +1765,7 @@ __device__ __noinline__ void job_adamw(const KArgs& a, char* smem) {
   const uint32_t STB = 4u * SEG + (uint32_t)AW_G * 8u;   // p | m | v | g | shadow
   const bool bulk = RP_WIN_OFF + (uint32_t)AW_NS * STB <= (uint32_t)a.smem_bytes;
   const long long nfull = bulk ? n4 / AW_T : 0;          // whole chunks
-  unsigned* ticket = abuf<unsigned>(a, A_DEP) + ticket_offset(a.D, a.D.L, TK_ADAMW);
+  unsigned* ticket = abuf<unsigned>(a, A_DEP) + ticket_offset(a.D, a.D.L, ri == 0 ? TK_ADAMW : ri == 1 ? TK_ADAMW_R1 : TK_ADAMW_R2);
   if (bulk) {
     const uint32_t ring = smem_u32(smem) + RP_WIN_OFF;
     const uint32_t bar0 = smem_u32(&rp_bars[0]);
@@ -1857,11 +1879,11 @@ __device__ __noinline__ void job_adamw(const KArgs& a, char* smem) {
   }
   if (c == G - 1) {
     for (long long i = n4 * 4 + threadIdx.x; i < n; i += MT_THREADS) {
-      float p = a.master[i], m = a.adam_m[i], v = a.adam_v[i];
-      adamw_elem(ak, p, a.grads[i], m, v);
-      a.master[i] = p;
-      a.adam_m[i] = m;
-      a.adam_v[i] = v;
+      float p = pm[i], m = mm_[i], v = vv_[i];
+      adamw_elem(ak, p, gr[i], m, v);
+      pm[i] = p;
+      mm_[i] = m;
+      vv_[i] = v;
       if (sh) sh[i] = __float2bfloat16_rn(p);
     }
   }
@@ -1968,7 +1990,7 @@ struct Gemms {
     GemmDesc g = base(D.V, D.d, D.T, EPI_GRAD);
     g.A = opnd(abuf<OP>(a, A_DLOGITS), D.V, 1); g.A.map0 = MAP_DLOGITS;
     g.B = opnd(abuf<OP>(a, A_RF), D.d, 1); g.B.map0 = MAP_RF;
-    g.out = pgrad(a, P_LM_HEAD); g.ldo = D.d; g.accumulate = a.micro_index > 0;
+    g.out = pgrad(a, P_LM_HEAD); g.ldo = D.d; g.accumulate = acc_of(a, P_LM_HEAD);
     return g;
   }
   __device__ GemmDesc down_dgrad(int l) const {
@@ -1990,7 +2012,7 @@ struct Gemms {
     g.B = opnd(abuf<OP>(a, A_ACT) + (long long)l * D.Pmax * D.F, D.F, 1);
     g.B.map0 = MAP_ACT; g.B.y0 = l * D.Pmax;
     g.out = pgrad(a, P_WDOWN) + (long long)l * D.E * D.d * D.F; g.ldo = D.F;
-    g.oseg = (long long)D.d * D.F; g.accumulate = a.micro_index > 0;
+    g.oseg = (long long)D.d * D.F; g.accumulate = acc_of(a, P_WDOWN);
     return g;
   }
   __device__ GemmDesc gateup_dgrad(int l) const {
@@ -2013,7 +2035,7 @@ struct Gemms {
     g.B.map0 = MAP_XS; g.B.y0 = l * D.Pmax;
     g.out = pgrad(a, P_WGATE) + (long long)l * D.E * D.F * D.d;
     g.out1 = pgrad(a, P_WUP) + (long long)l * D.E * D.F * D.d;
-    g.osplit = D.F; g.ldo = D.d; g.oseg = (long long)D.F * D.d; g.accumulate = a.micro_index > 0;
+    g.osplit = D.F; g.ldo = D.d; g.oseg = (long long)D.F * D.d; g.accumulate = acc_of(a, P_WGATE);
     return g;
   }
   __device__ GemmDesc wo_dgrad(int l) const {
@@ -2042,7 +2064,7 @@ struct Gemms {
     g.A = opnd(abuf<OP>(a, A_DXO), D.d, 1); g.A.map0 = MAP_DXO;
     g.B = opnd(abuf<OP>(a, A_O) + (long long)l * D.T * D.hq, D.hq, 1);
     g.B.map0 = MAP_O; g.B.y0 = l * D.T;
-    g.out = pgrad(a, P_WO) + (long long)l * D.d * D.hq; g.ldo = D.hq; g.accumulate = a.micro_index > 0;
+    g.out = pgrad(a, P_WO) + (long long)l * D.d * D.hq; g.ldo = D.hq; g.accumulate = acc_of(a, P_WO);
     split(g);
     return g;
   }
@@ -2060,20 +2082,20 @@ struct Gemms {
     g.A = opnd(abuf<OP>(a, A_DQKV), 3 * D.hq, 1); g.A.map0 = MAP_DQKV;
     g.B = opnd(abuf<OP>(a, A_R) + (long long)l * D.T * D.d, D.d, 1);
     g.B.map0 = MAP_R; g.B.y0 = l * D.T;
-    g.out = pgrad(a, P_WQKV) + (long long)l * 3 * D.hq * D.d; g.ldo = D.d; g.accumulate = a.micro_index > 0;
+    g.out = pgrad(a, P_WQKV) + (long long)l * 3 * D.hq * D.d; g.ldo = D.d; g.accumulate = acc_of(a, P_WQKV);
     split(g);
     return g;
   }
 };
 
 // out[i] (+)= sum over slices s (in order) of KPART[s][i], i < M*N.
-static __device__ __noinline__ void job_ksplit_sum(const KArgs& a, float* out, int M, int N, Sched& s) {
+static __device__ __noinline__ void job_ksplit_sum(const KArgs& a, float* out, int M, int N, Sched& s, int pid) {
   const int ks = ksplit_of(a, M, N, a.D.T);
   if (ks <= 1) return;
   const float4* P = reinterpret_cast<const float4*>(abuf<float>(a, A_KPART));
   float4* o = reinterpret_cast<float4*>(out);
   const long long n4 = (long long)M * N / 4;
-  const bool acc = a.micro_index > 0;
+  const bool acc = acc_of(a, pid);
   for (long long i = (long long)s.first() * MT_THREADS + threadIdx.x; i < n4; i += (long long)s.G * MT_THREADS) {
     float4 v = acc ? o[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < ks; ++k) {
@@ -2278,8 +2300,9 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   for (int l = D.L - 1; l >= 0; --l) {
     job_moe_bwd1<OP>(a, l, s, smem); TJ(17);
     MT_SYNC();
-    if (l == D.L - 1) job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_FINAL_NORM), nullptr, 0, s, (int)G);
-    else job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM) + (long long)(l + 1) * D.d, nullptr, 0, s, (int)G);
+    if (l == D.L - 1) job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_FINAL_NORM), nullptr, 0, s, (int)G, P_FINAL_NORM);
+    else job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM) + (long long)(l + 1) * D.d, nullptr, 0, s, (int)G,
+                      P_ATTN_NORM);
     TJ(18);
     run_gemm<OP>(a, TK(gm.down_wgrad(l), l, TK_DOWN_WGRAD), s, smem, tc); TJ(20);
     run_gemm<OP>(a, TK(gm.down_dgrad(l), l, TK_DOWN_DGRAD), s, smem, tc); TJ(19);
@@ -2295,9 +2318,9 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     run_gemm<OP>(a, TK(gm.wo_wgrad(l), l, TK_WO_WGRAD), s, smem, tc); TJ(25);
     run_gemm<OP>(a, TK(gm.wo_dgrad(l), l, TK_WO_DGRAD), s, smem, tc); TJ(24);
     MT_SYNC();
-    job_colfinal(a, 0, D.E, D.E, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d, nullptr, 0, s, rg_chunks);
-    job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_MOE_NORM) + (long long)l * D.d, nullptr, 0, s, (int)G); TJ(18);
-    job_ksplit_sum(a, pgrad(a, P_WO) + (long long)l * D.d * D.hq, D.d, D.hq, s); TJ(32);
+    job_colfinal(a, 0, D.E, D.E, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d, nullptr, 0, s, rg_chunks, P_ROUTER);
+    job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_MOE_NORM) + (long long)l * D.d, nullptr, 0, s, (int)G, P_MOE_NORM); TJ(18);
+    job_ksplit_sum(a, pgrad(a, P_WO) + (long long)l * D.d * D.hq, D.d, D.hq, s, P_WO); TJ(32);
     if constexpr (sizeof(OP) == 2) {
       if (a.use_dsg) {
         // dK/dV stores dS^T; after a grid barrier dQ is a product over it
@@ -2313,23 +2336,28 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     run_gemm<OP>(a, TK(gm.qkv_dgrad(l), l, TK_QKV_DGRAD), s, smem, tc); TJ(27);
     MT_SYNC();
     job_attn_norm_bwd<OP>(a, l, s, smem); TJ(29);
-    job_ksplit_sum(a, pgrad(a, P_WQKV) + (long long)l * 3 * D.hq * D.d, 3 * D.hq, D.d, s); TJ(33);
+    job_ksplit_sum(a, pgrad(a, P_WQKV) + (long long)l * 3 * D.hq * D.d, 3 * D.hq, D.d, s, P_WQKV); TJ(33);
     MT_SYNC();
   }
   job_embed_bwd(a, (int*)smem); TJ(30);
   MT_SYNC();
-  job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM), nullptr, 0, s, (int)G); TJ(18);
+  job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM), nullptr, 0, s, (int)G, P_ATTN_NORM); TJ(18);
 
   // ---------------- optimizer (last microbatch) ----------------
-  if (a.run_opt) {
+  if (a.n_ranges > 0) {
     MT_SYNC();
-    job_norm_partial(a, (double*)smem); TJ(31);
+    for (int r = 0; r < a.n_ranges; ++r) job_norm_partial(a, (double*)smem, r);
+    TJ(31);
     MT_SYNC();
-    job_adamw<OP>(a, smem); TJ(34);
+    for (int r = 0; r < a.n_ranges; ++r) job_adamw<OP>(a, smem, r);
+    TJ(34);
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     hdr->micro_index = a.micro_index;
-    if (!a.run_opt) hdr->optimizer_ran = 0;
+    bool g0 = false, g1 = false;
+    for (int r = 0; r < a.n_ranges; ++r) (a.orng[r].group ? g1 : g0) = true;
+    if (!g0) hdr->optimizer_ran = 0;
+    if (!g1) hdr->experts_updated = 0;
     hdr->n_ctas = (int)G;
     hdr->n_phases = phase;
   }
@@ -2445,9 +2473,9 @@ __device__ __noinline__ void run_op(const KArgs& a, char* smem, TcState& tc, Sch
       break;
     }
     case MT_OP_CLIP_ADAMW:
-      job_norm_partial(a, (double*)smem);
+      for (int r = 0; r < a.n_ranges; ++r) job_norm_partial(a, (double*)smem, r);
       OP_SYNC();
-      job_adamw<OP>(a, smem);
+      for (int r = 0; r < a.n_ranges; ++r) job_adamw<OP>(a, smem, r);
       break;
     default:
       break;

@@ -7,38 +7,28 @@
 // loaded on a device, and it stays there until the process exits.  Host code
 // must not pass the array's name to a kernel: on the host that name is only a
 // stand-in symbol, not a device address.  The device address is looked up
-// once per device with cudaGetSymbolAddress (with that device current) and
-// cached.
+// with cudaGetSymbolAddress on every call, with the caller's device current,
+// so it stays right after a cudaDeviceReset reloads the module.
 #include <cuda_runtime.h>
 #include <string.h>
 
-#include <mutex>
-
 #include "../../include/moe_train.h"
+#include "launch.h"
 #include "plan.h"
 
 static __device__ __align__(256) unsigned char g_noalloc_arena[MT_NOALLOC_ARENA_BYTES];
 
 namespace {
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64] = {};
-
-// Device address of the array on the current device (looked up once per device).
+// Device address of the array on the current device.
 int noalloc_arena(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MT_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_arena);
-    if (e != cudaSuccess || !p) {
-      cudaGetLastError();
-      return MT_ERR_CUDA;
-    }
-    g_noalloc_addr[dev] = p;
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_arena);
+  if (e != cudaSuccess || !p) {
+    cudaGetLastError();
+    return MT_ERR_CUDA;
   }
-  *out = g_noalloc_addr[dev];
+  *out = p;
   return MT_OK;
 }
 
@@ -52,6 +42,10 @@ extern "C" int32_t mt_train_update_noalloc(float* params, void* shadow, float* g
   if (need > (int64_t)MT_NOALLOC_ARENA_BYTES) return MT_ERR_ARENA_SMALL;
   void* arena = nullptr;
   int st = noalloc_arena(&arena);
+  if (st) return st;
+  // every check of the launch comes before anything is enqueued
+  st = mt_check_update_args(params, shadow, grads, adam_m, adam_v, tokens, hp, arena,
+                            (int64_t)MT_NOALLOC_ARENA_BYTES);
   if (st) return st;
   // The array keeps whatever the previous call left in it.  The barrier
   // words and the status word must start at zero; the rest of the header

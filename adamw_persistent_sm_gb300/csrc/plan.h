@@ -109,6 +109,9 @@ struct ArenaHdr {
   float loss, loss_update, grad_norm, clip_coef;
   int n_ctas, n_phases;
   int expert_counts[16 * 64];
+  // second optimizer group (expert tensors under MT_FLAG_SELECTIVE_EXPERTS)
+  int experts_updated;
+  float expert_grad_norm, expert_clip_coef;
 };
 
 // Dependency counters.  Each layer owns one counter per 128-row block of
@@ -133,8 +136,12 @@ enum TicketId {
   TK_ADAMW = 0,
   TK_QKV, TK_WO, TK_GATEUP, TK_DOWN,
   TK_DOWN_DGRAD, TK_DOWN_WGRAD, TK_GU_DGRAD, TK_GU_WGRAD, TK_WO_DGRAD, TK_WO_WGRAD, TK_QKV_DGRAD, TK_QKV_WGRAD,
-  TK_LM = TK_QKV, TK_LM_DGRAD = TK_WO, TK_LM_WGRAD = TK_GATEUP
+  TK_COUNT_,
+  // the head's set: LM-head products and the optimizer ranges
+  TK_LM = TK_QKV, TK_LM_DGRAD = TK_WO, TK_LM_WGRAD = TK_GATEUP,
+  TK_ADAMW_R1 = TK_DOWN, TK_ADAMW_R2 = TK_DOWN_DGRAD
 };
+static_assert(TK_COUNT_ <= MT_TICKETS, "ticket ids exceed a layer's ticket set");
 __host__ __device__ inline long long dep_blocks(const MtDims& D, int kind) {
   return kind == DEP_ACT ? D.Pmax / MT_TILE_M : (D.T + MT_TILE_M - 1) / MT_TILE_M;
 }
@@ -151,12 +158,31 @@ __host__ __device__ inline long long dep_words(const MtDims& D) {
   return (long long)D.L * dep_layer_words(D) + (long long)(D.L + 1) * MT_TICKETS;
 }
 
+// The optimizer of one launch: up to MT_OPT_RANGES contiguous ranges of the
+// flat parameter / gradient / moment buffers, each in one of two groups.  A
+// group is one clipped AdamW step: its own global norm (over the gradients of
+// its ranges, times gscale), its own bias corrections.
+#define MT_OPT_RANGES 3
+struct OptRange {
+  long long off, n;             // element range (off and n multiples of 4)
+  int group;                    // 0 or 1
+  int first;                    // the group's first range (writes the group's outputs)
+};
+struct OptGroup {
+  float ibc1, ibc2;             // 1 / (1 - beta^t) for this group's step t
+  float gscale;                 // the step uses gscale * (summed gradient)
+  int r0, nr;                   // its ranges: orng[r0 .. r0+nr-1] (norm partial slots alike)
+};
+
 struct KArgs {
   MtDims D;
   float lr, beta1, beta2, eps, wd, clip, clip_eps, norm_eps, coef, rope_theta;
-  float ibc1, ibc2;             // 1 / (1 - beta^t), computed on the host in double
   float decay;                  // 1 - lr * weight_decay, in double on the host
   int micro_index, micro_count, run_opt;
+  unsigned acc_mask;            // bit p: parameter tensor p's gradient is added to the buffer (else overwritten)
+  int n_ranges;                 // optimizer ranges this launch (0: no optimizer)
+  OptRange orng[MT_OPT_RANGES];
+  OptGroup ogrp[2];
   unsigned int flags;
   long long timeout_ns;
   long long n_params;

@@ -80,17 +80,18 @@ class MoETrainer:
     def named(self, buf: torch.Tensor) -> dict:
         return {name: self.view(buf, name) for name in self.layout}
 
-    def hparams(self, micro_index: int = 0, step: int | None = None, flags: int | None = None):
+    def hparams(self, micro_index: int = 0, step: int | None = None, flags: int | None = None,
+                expert_step: int = 1):
         return B.hparams(self.cfg, micro_index=micro_index, step=step,
                          flags=self.flags if flags is None else flags,
-                         wait_timeout_ns=self.wait_timeout_ns)
+                         wait_timeout_ns=self.wait_timeout_ns, expert_step=expert_step)
 
     # ---- the update ---------------------------------------------------------
     def micro_step(self, tokens: torch.Tensor, micro_index: int = 0, step: int | None = None,
-                   flags: int | None = None) -> None:
+                   flags: int | None = None, expert_step: int = 1) -> None:
         """Enqueue one microbatch launch (tokens: int32 [batch, seq] on the device)."""
         assert tokens.dtype == torch.int32 and tokens.is_cuda and tokens.is_contiguous()
-        hp = self.hparams(micro_index, step, flags)
+        hp = self.hparams(micro_index, step, flags, expert_step)
         st = B.mt_train_update(self.params.data_ptr(),
                                self.shadow.data_ptr() if self.shadow is not None else 0,
                                self.grads.data_ptr(), self.adam_m.data_ptr(), self.adam_v.data_ptr(),

@@ -67,7 +67,19 @@ enum {
   MT_FLAG_RECOMPUTE_ATTN_DS = 1u << 7, /* bf16: keep no dS^T of the attention backward
                                           (batch*heads*seq^2 bf16 per launch); the dQ items
                                           recompute P and dS instead of reading it */
-  MT_FLAGS_ALL = (1u << 0) | (1u << 3) | (1u << 4) | (1u << 5) | (1u << 7)
+  /* Selective updates ("Results", "Other measured compiler work": shared
+   * weights update every microbatch, experts every 16).  The shared tensors
+   * (every tensor but w_gate, w_up, w_down) get their gradients overwritten
+   * and a clipped AdamW step (step t = hp.step, norm over the shared
+   * gradients) after EVERY microbatch, each microbatch weighing its targets
+   * 1 / (batch*(seq-1)).  The expert tensors' gradients are summed over the
+   * micro_count microbatches of a period (overwritten at micro_index 0); after
+   * the last one they get a clipped AdamW step (t = hp.expert_step, norm over
+   * their gradients) on the mean, sum / micro_count.  mt_outputs reports the
+   * shared step in grad_norm / clip_coef and the expert step in
+   * expert_grad_norm / expert_clip_coef / experts_updated. */
+  MT_FLAG_SELECTIVE_EXPERTS = 1u << 8,
+  MT_FLAGS_ALL = (1u << 0) | (1u << 3) | (1u << 4) | (1u << 5) | (1u << 7) | (1u << 8)
 };
 
 /*
@@ -96,6 +108,7 @@ typedef struct mt_hparams {
   float rope_theta;           /* rotary base */
   float loss_coef;            /* per-target CE coefficient; 0 -> 1/(batch*(seq-1)*micro_count) */
   int64_t wait_timeout_ns;    /* bound on every device-side wait; 0 -> 4e9 ns */
+  int64_t expert_step;        /* MT_FLAG_SELECTIVE_EXPERTS: AdamW step t of the expert tensors */
 } mt_hparams;
 
 /* One parameter tensor inside the flat fp32 parameter buffer. */
@@ -125,19 +138,30 @@ typedef struct mt_outputs {
   int32_t n_ctas;             /* grid size of the launch */
   int32_t n_phases;           /* grid-wide barriers passed */
   int32_t expert_counts[MT_MAX_LAYERS * MT_MAX_EXPERTS]; /* tokens routed to [layer][expert] */
+  int32_t experts_updated;    /* MT_FLAG_SELECTIVE_EXPERTS: 1 if the expert step ran */
+  float expert_grad_norm;     /* its norm of the mean expert gradient, before clipping */
+  float expert_clip_coef;     /* and its clip coefficient */
 } mt_outputs;
 
-/* Number of parameters (elements of the flat fp32 buffers params/grads/m/v). */
+/* Number of parameters (elements of the flat fp32 buffers params/grads/m/v).
+ * Defined by: "How a training megakernel works", "From two weights to 200
+ * million" (the model's weights: attention and expert layers) with the sizes
+ * of hp.  Errors: a negative mt_status (see check rules above). */
 int64_t mt_param_count(const mt_hparams* hp);
 
-/* Fill out[0..min(cap, n)-1] with the parameter layout; returns the number of
+/* Defined by: "How a training megakernel works", "From two weights to 200
+ * million" (attention + expert layers with a router) and "1 - Describe the
+ * model and update" (the model's parameter names are kept).
+ * Fill out[0..min(cap, n)-1] with the parameter layout; returns the number of
  * tensors n (11) or a negative mt_status.  Order: emb [V,d], attn_norm [L,d],
  * wqkv [L,3*H*hd,d], wo [L,d,H*hd], moe_norm [L,d], router [L,E,d],
  * w_gate [L,E,F,d], w_up [L,E,F,d], w_down [L,E,d,F], final_norm [d],
  * lm_head [V,d]; every matrix is [out, in]. */
 int32_t mt_param_layout(const mt_hparams* hp, mt_tensor_desc* out, int32_t cap);
 
-/* Bytes of caller-provided device arena the launch needs (worst case over
+/* Defined by: "How a training megakernel works", "4 - Scheduling and storage"
+ * (values passed between phases live in a planned GPU-memory arena).
+ * Bytes of caller-provided device arena the launch needs (worst case over
  * routing), or a negative mt_status.  With MT_FLAG_TRACE in hp->flags the
  * arena also holds the per-CTA trace (MT_VIEW_TRACE), so traced launches
  * need an arena sized with that flag.  bf16 models also hold one layer's
@@ -147,15 +171,28 @@ int32_t mt_param_layout(const mt_hparams* hp, mt_tensor_desc* out, int32_t cap);
 int64_t mt_arena_bytes(const mt_hparams* hp);
 
 /* Zero the arena's control header (barrier and status words).  Call once after
- * allocating an arena, and again after a device-side error. */
+ * allocating an arena, and again after a device-side error.  Defined by: same
+ * section (the grid-wide barriers between phases); the pages' per-update
+ * scalar fills are not needed because the barrier resets itself.
+ * Errors: MT_ERR_ARG (null or misaligned arena), MT_ERR_CUDA. */
 int32_t mt_arena_init(void* arena, int64_t arena_bytes, void* stream);
 
 /* Write the bf16 compute copy of the fp32 master parameters:
- * shadow[i] = bf16(master[i]) for i < n (round to nearest even). */
+ * shadow[i] = bf16(master[i]) for i < n (round to nearest even).  Defined by:
+ * "4 - Scheduling and storage" (FP32 master weights, BF16 matrix products).
+ * Both pointers are caller-owned device memory.  Errors: MT_ERR_ARG,
+ * MT_ERR_LAUNCH. */
 int32_t mt_sync_shadow(const float* master, void* shadow_bf16, int64_t n, void* stream);
 
 /*
  * One microbatch of the training update, as one persistent kernel launch.
+ * Defined by: "How a training megakernel works", "One training update"
+ * (forward, loss, backward, optimizer step), "What Latch does" (one
+ * persistent GPU program resident across the SMs; steps 1-4: bf16 attention,
+ * token_topk, route_order, ragged_mm, global-norm clipping and AdamW, phases
+ * with grid-wide barriers, the arena, FP32 master weights and moments with
+ * BF16 products) and "How GPUs usually run it" (one kernel per microbatch,
+ * one optimizer update after the last microbatch of the published batch).
  *   params  fp32 [n]   master weights (updated in place by the optimizer)
  *   shadow  bf16 [n]   compute copy (read by bf16 products, rewritten by AdamW);
  *                      may be NULL when hp->precision == MT_PREC_FP32
@@ -174,14 +211,21 @@ int32_t mt_train_update(float* params, void* shadow, float* grads, float* adam_m
                         void* arena, int64_t arena_bytes, void* stream);
 
 /* Synchronise `stream` and copy the outputs block of the arena to *out.
- * Returns out->status (MT_OK if the device side succeeded). */
+ * Returns out->status (MT_OK if the device side succeeded), or MT_ERR_ARG /
+ * MT_ERR_CUDA for host-side failures.  Defined by: "One training update" (the
+ * loss) and "1 - Describe the model and update" (global-norm clipping: the
+ * norm and coefficient). */
 int32_t mt_read_outputs(const void* arena, mt_outputs* out, void* stream);
 
 /* Capacity of the per-CTA trace (MT_VIEW_TRACE) */
 enum { MT_TRACE_PHASES = 512, MT_TRACE_JOBS = 1024, MT_TRACE_WORDS = 2 * (512 + 1024) };
 
-/* Debug views into the arena after a launch (device pointers into the arena).
- * which: see MT_VIEW_* ; layer selects the layer for per-layer buffers. */
+/* Debug views into the arena after a launch (device pointers into the arena,
+ * owned by the arena's owner).  which: see MT_VIEW_* ; layer selects the
+ * layer for per-layer buffers.  Defined by: "5 - Generation and compilation"
+ * (the generated program's comparison and numerical-check commands).
+ * Errors: MT_ERR_ARG (unknown view or layer, trace view of an untraced
+ * arena). */
 enum {
   MT_VIEW_ROUTER_LOGITS = 0,  /* fp32 [T, E] */
   MT_VIEW_TOPK_IDX = 1,       /* int32 [T, K] */
@@ -280,9 +324,12 @@ int32_t mt_debug_run(int32_t op, int32_t layer, float* params, void* shadow, flo
  *    larger ones return MT_ERR_ARENA_SMALL and nothing is enqueued.
  *  - The array occupies MT_NOALLOC_ARENA_BYTES on every device where the
  *    library's code is loaded, until the process exits.
- *  - The first call on a device looks up the array's device address (with that
- *    device current) and caches it; make that first call before any stream
- *    capture.
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress), so the address stays right after a
+ *    cudaDeviceReset reloads the library's module; the first call on a device
+ *    also loads the module there, so make it before any stream capture.
+ *  - Every argument check (as mt_train_update's) runs before anything is
+ *    enqueued: a call that returns an error has written nothing.
  *  - Every call uses the same array, which keeps what the previous call left
  *    in it; each call clears the barrier and status words it needs at zero.
  *    Calls whose execution overlaps on the GPU (different streams, or

@@ -191,3 +191,10 @@ def normal_operand(shape, seed: int, std: float = 1.0, mean: float = 0.0,
     """Seeded N(mean, std) fp32 array; bf16-representable when ``bf16``."""
     x = np.random.default_rng(seed).normal(mean, std, size=shape).astype(np.float32)
     return round_to_bf16(x) if bf16 else x
+
+
+def make_step_tokens(cfg: MoEConfig, step: int) -> list[np.ndarray]:
+    """Token ids of every microbatch of update number ``step`` (1-based) of a
+    multi-step run; step 1 draws the same ids as :func:`make_update_tokens`."""
+    base = 0 if step == 1 else 100003 * step
+    return [make_tokens(cfg, base + i) for i in range(cfg.micro_count)]

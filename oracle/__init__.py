@@ -8,4 +8,5 @@ from .moe_oracle import (worked_example, rmsnorm, rmsnorm_backward, rope_tables,
                          rope_backward, causal_attention, causal_attention_backward, causal_logsumexp,
                          token_topk, route_order, moe_forward, forward_backward,
                          clip_adamw, global_norm, train_update, loss_only, Dims,
-                         UpdateResult, n_targets, to64, softmax, silu, silu_grad)
+                         UpdateResult, n_targets, to64, softmax, silu, silu_grad,
+                         selective_updates, SelectiveResult, EXPERT_TENSORS)

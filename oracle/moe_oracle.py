@@ -527,3 +527,73 @@ def loss_only(params: dict, tokens: np.ndarray, cfg, coef: float | None = None,
     loss, _, _ = forward_backward(P, tokens, D, coef, {}, backward=False,
                                   route_logits=route_logits)
     return loss
+
+
+# ---------------------------------------------------------------------------
+# Selective updates (*Results*, "Other measured compiler work": shared weights
+# update every microbatch, experts every 16)
+# ---------------------------------------------------------------------------
+EXPERT_TENSORS = ("w_gate", "w_up", "w_down")
+
+
+@dataclass
+class SelectiveResult:
+    params: dict
+    m: dict
+    v: dict
+    losses: list            # loss of each microbatch (mean CE over its targets)
+    shared_norms: list      # ||g|| of the shared tensors at each microbatch
+    shared_coefs: list
+    expert_norm: float      # ||mean expert gradient|| at the end of the period
+    expert_coef: float
+    shared_grads: dict      # shared gradients of the last microbatch
+    expert_grads: dict      # expert gradients summed over the period
+
+
+def selective_updates(params: dict, micro_tokens: list, cfg, m=None, v=None, step: int = 1,
+                      expert_step: int = 1, expert_names=EXPERT_TENSORS,
+                      route_logits=None) -> SelectiveResult:
+    """One period of selective updates over ``micro_tokens``.
+
+    Every microbatch i: forward and backward at the current weights, every
+    target weighing 1 / (targets of the microbatch); the shared tensors (all
+    but ``expert_names``) take one clipped AdamW step at step index step + i
+    (norm over the shared gradients).  The expert tensors' gradients are
+    summed over the microbatches; after the last one the experts take one
+    clipped AdamW step at ``expert_step`` on the mean (sum / number of
+    microbatches, norm over that mean).
+    """
+    D = Dims.of(cfg)
+    P = to64(params)
+    m = {k: np.zeros_like(p) for k, p in P.items()} if m is None else to64(m)
+    v = {k: np.zeros_like(p) for k, p in P.items()} if v is None else to64(v)
+    shared = [k for k in P if k not in expert_names]
+    experts = [k for k in P if k in expert_names]
+    hyper = dict(lr=cfg.lr, beta1=cfg.beta1, beta2=cfg.beta2, eps=cfg.eps,
+                 weight_decay=cfg.weight_decay, clip_norm=cfg.clip_norm, clip_eps=cfg.clip_eps)
+    acc = {k: np.zeros_like(P[k]) for k in experts}
+    losses, norms, coefs = [], [], []
+    grads = {}
+    for i, tokens in enumerate(micro_tokens):
+        grads = {k: np.zeros_like(p) for k, p in P.items()}
+        coef = 1.0 / n_targets(*tokens.shape)
+        rz = None if route_logits is None else route_logits[i]
+        loss, _, _ = forward_backward(P, tokens, D, coef, grads, route_logits=rz)
+        losses.append(loss)
+        for k in experts:
+            acc[k] += grads[k]
+        if shared:
+            sp, sm, sv, n, c = clip_adamw({k: P[k] for k in shared}, {k: grads[k] for k in shared},
+                                          {k: m[k] for k in shared}, {k: v[k] for k in shared},
+                                          step=step + i, **hyper)
+            P.update(sp); m.update(sm); v.update(sv)
+            norms.append(n); coefs.append(c)
+    n_e, c_e = 0.0, 1.0
+    if experts:
+        mean = {k: acc[k] / len(micro_tokens) for k in experts}
+        ep, em, ev, n_e, c_e = clip_adamw({k: P[k] for k in experts}, mean, {k: m[k] for k in experts},
+                                          {k: v[k] for k in experts}, step=expert_step, **hyper)
+        P.update(ep); m.update(em); v.update(ev)
+    return SelectiveResult(params=P, m=m, v=v, losses=losses, shared_norms=norms, shared_coefs=coefs,
+                           expert_norm=n_e, expert_coef=c_e,
+                           shared_grads={k: grads[k] for k in shared}, expert_grads=acc)

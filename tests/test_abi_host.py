@@ -108,8 +108,8 @@ def test_train_update_argument_checks(lib):
 
 
 def test_struct_sizes_match_header(lib):
-    assert C.sizeof(B.mt_hparams) == 112
-    assert C.sizeof(B.mt_outputs) == 40 + 4 * 16 * 64
+    assert C.sizeof(B.mt_hparams) == 120
+    assert C.sizeof(B.mt_outputs) == 40 + 4 * 16 * 64 + 12
 
 
 def test_trace_arena_is_sized_by_the_trace_flag():
@@ -143,7 +143,7 @@ def test_unknown_flags_and_untiled_bf16_shapes_are_refused():
     CUDA-core fallback for bf16)."""
     from adamw_persistent_sm_gb300 import binding as B
     cfg = mi.get_config("b2")
-    for bit in (1, 2, 6, 8, 31):
+    for bit in (1, 2, 6, 9, 31):
         assert B.mt_arena_bytes(B.hparams(cfg, flags=1 << bit)) == -B.MT_ERR_ARG
     fake = 1 << 20
     args = (fake, fake, fake, fake, fake, fake)

@@ -440,3 +440,62 @@ def test_pooled_oracle_equals_serial_oracle():
         np.testing.assert_allclose(pooled.params[k], serial.params[k], rtol=1e-9, atol=1e-16)
     for a, b in zip(pooled.tok_loss, serial.tok_loss):
         np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-16)
+
+
+# --------------------------------------------------------------------------
+# Selective updates: the two special cases are plain updates
+# --------------------------------------------------------------------------
+def test_selective_all_experts_is_gradient_accumulation():
+    """With every tensor in the expert group nothing updates until the end,
+    and the step on the mean gradient is the accumulated update's step."""
+    cfg = tiny(batch=1, micro_count=3)
+    P = mi.make_params(cfg)
+    toks = mi.make_update_tokens(cfg)
+    acc = oracle.train_update(P, toks, cfg)
+    sel = oracle.selective_updates(P, toks, cfg, expert_names=tuple(P))
+    for k in P:
+        # coefficient 1/31 per microbatch, then / 3, against 1/93: rounding only
+        np.testing.assert_allclose(sel.expert_grads[k] / 3, acc.grads[k], rtol=1e-10, atol=1e-16)
+        np.testing.assert_allclose(sel.params[k], acc.params[k], rtol=1e-9, atol=1e-15)
+    assert sel.expert_norm == pytest.approx(acc.grad_norm, rel=1e-12)
+
+
+def test_selective_all_shared_is_one_update_per_microbatch():
+    """With no expert group every microbatch is one whole update at step
+    index 1, 2, 3 with the state carried over."""
+    cfg = tiny(batch=1, micro_count=3)
+    P = mi.make_params(cfg)
+    toks = mi.make_update_tokens(cfg)
+    sel = oracle.selective_updates(P, toks, cfg, expert_names=())
+    st, m, v = P, None, None
+    for i, t in enumerate(toks):
+        r = oracle.train_update(st, [t], cfg.replace(micro_count=1, step=i + 1), m=m, v=v)
+        st, m, v = r.params, r.m, r.v
+        assert sel.losses[i] == pytest.approx(r.loss, rel=1e-12)
+        assert sel.shared_norms[i] == pytest.approx(r.grad_norm, rel=1e-12)
+    for k in P:
+        np.testing.assert_allclose(sel.params[k], st[k], rtol=1e-12, atol=1e-16)
+
+
+def test_selective_first_shared_step_and_expert_step():
+    """The first microbatch's shared step is the plain single-microbatch
+    update's step on those tensors (clipping off: the norm is then over
+    different sets but unused), and the expert step is one AdamW step at
+    t = 1 on the mean of the period's expert gradients: with clipping off,
+    -lr * sign(mean g) - lr * wd * p up to eps."""
+    cfg = tiny(batch=1, micro_count=3, clip_norm=1e6)
+    P = mi.make_params(cfg)
+    toks = mi.make_update_tokens(cfg)
+    one = oracle.selective_updates(P, toks[:1], cfg)
+    plain = oracle.train_update(P, toks[:1], cfg.replace(micro_count=1))
+    for k in P:
+        if k not in oracle.EXPERT_TENSORS:
+            np.testing.assert_allclose(one.params[k], plain.params[k], rtol=1e-12, atol=1e-16)
+    full = oracle.selective_updates(P, toks, cfg)
+    for k in oracle.EXPERT_TENSORS:
+        g = full.expert_grads[k] / 3
+        p0 = P[k].astype(np.float64)
+        expect = p0 * (1 - cfg.lr * cfg.weight_decay) - cfg.lr * g / (np.abs(g) + cfg.eps)
+        np.testing.assert_allclose(full.params[k], expect, rtol=1e-9, atol=1e-15)
+        # and differs from stepping on the sum by the eps term only where |g| ~ eps
+        assert np.any(full.expert_grads[k])
