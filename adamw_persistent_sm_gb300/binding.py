@@ -31,6 +31,7 @@ MT_FLAG_TEST_STALL = 1 << 4
 MT_FLAG_BARRIERS_ONLY = 1 << 5
 MT_FLAG_RECOMPUTE_ATTN_DS = 1 << 7
 MT_FLAG_SELECTIVE_EXPERTS = 1 << 8
+MT_FLAG_RECOMPUTE_EXPERT_ACT = 1 << 9
 
 MT_MAX_LAYERS = 16
 MT_MAX_EXPERTS = 64
@@ -77,6 +78,7 @@ class mt_hparams(C.Structure):
         ("weight_decay", C.c_float), ("clip_norm", C.c_float), ("clip_eps", C.c_float),
         ("norm_eps", C.c_float), ("rope_theta", C.c_float), ("loss_coef", C.c_float),
         ("wait_timeout_ns", C.c_int64), ("expert_step", C.c_int64),
+        ("n_unique_layers", C.c_int32), ("reserved0", C.c_int32),
     ]
 
 
@@ -160,6 +162,7 @@ def hparams(cfg, micro_index: int = 0, flags: int = 0, step: int | None = None,
     hp.loss_coef = loss_coef
     hp.wait_timeout_ns = wait_timeout_ns
     hp.expert_step = expert_step
+    hp.n_unique_layers = getattr(cfg, "n_unique_layers", 0)
     return hp
 
 

@@ -15,7 +15,7 @@
 #include "tmaps.h"
 #include "gemm_tc.cuh"
 
-static_assert(sizeof(mt_hparams) == 120, "mt_hparams layout is part of the ABI");
+static_assert(sizeof(mt_hparams) == 128, "mt_hparams layout is part of the ABI");
 static_assert(sizeof(mt_outputs) == 40 + 4 * MT_MAX_LAYERS * MT_MAX_EXPERTS + 12, "mt_outputs layout");
 
 namespace {
@@ -39,6 +39,7 @@ int check_hparams(const mt_hparams* hp) {
   if (hp->micro_count <= 0 || hp->micro_index < 0 || hp->micro_index >= hp->micro_count) return MT_ERR_ARG;
   if (hp->step < 1) return MT_ERR_ARG;
   if ((hp->flags & MT_FLAG_SELECTIVE_EXPERTS) && hp->expert_step < 1) return MT_ERR_ARG;
+  if (hp->n_unique_layers < 0 || hp->n_unique_layers > hp->n_layers || hp->reserved0 != 0) return MT_ERR_ARG;
   if (!(hp->lr >= 0.f) || !(hp->beta1 >= 0.f && hp->beta1 < 1.f) || !(hp->beta2 >= 0.f && hp->beta2 < 1.f) ||
       !(hp->eps > 0.f) || !(hp->weight_decay >= 0.f) || !(hp->clip_norm > 0.f) || !(hp->clip_eps >= 0.f) ||
       !(hp->norm_eps > 0.f) || !(hp->rope_theta > 0.f) || !(hp->loss_coef >= 0.f) || hp->wait_timeout_ns < 0)
@@ -74,6 +75,7 @@ void make_plan(const mt_hparams* hp, MtPlan* P) {
   D.V = hp->vocab; D.d = hp->d_model; D.L = hp->n_layers; D.H = hp->n_heads; D.hd = hp->head_dim;
   D.hq = D.H * D.hd; D.E = hp->n_experts; D.K = hp->top_k; D.F = hp->d_ff; D.B = hp->batch;
   D.S = hp->seq; D.T = D.B * D.S;
+  D.U = hp->n_unique_layers > 0 ? hp->n_unique_layers : hp->n_layers;
   D.Pmax = (int)round_up((long long)D.T * D.K + (long long)D.E * (MT_TILE_M - 1), MT_TILE_M);
   D.nch = kNch;
   D.op_bytes = hp->precision == MT_PREC_BF16 ? 2 : 4;
@@ -98,8 +100,10 @@ void make_plan(const mt_hparams* hp, MtPlan* P) {
   sz[A_PERM] = L * Pm * 4;
   sz[A_INVM] = L * T * D.K * 4;
   sz[A_XS] = L * Pm * d * ob;
-  sz[A_GU] = L * Pm * 2 * D.F * ob;
-  sz[A_ACT] = L * Pm * D.F * ob;
+  // memory rule MT_FLAG_RECOMPUTE_EXPERT_ACT: one layer of expert activations
+  const long long AL = (hp->flags & MT_FLAG_RECOMPUTE_EXPERT_ACT) ? 1 : L;
+  sz[A_GU] = AL * Pm * 2 * D.F * ob;
+  sz[A_ACT] = AL * Pm * D.F * ob;
   sz[A_Y] = L * Pm * d * 4;
   sz[A_RF] = T * d * ob;
   sz[A_INVF] = T * 4;
@@ -136,18 +140,18 @@ void make_plan(const mt_hparams* hp, MtPlan* P) {
     off = round_up(off + sz[i], kAlign);
   }
   P->arena_bytes = off;
-  // parameters
-  const long long V = D.V, E = D.E, F = D.F, hq = D.hq;
+  // parameters: per-layer tensors are stacked over the U weight slots
+  const long long V = D.V, E = D.E, F = D.F, hq = D.hq, U = D.U;
   long long pn[P_COUNT];
   pn[P_EMB] = V * d;
-  pn[P_ATTN_NORM] = L * d;
-  pn[P_WQKV] = L * 3 * hq * d;
-  pn[P_WO] = L * d * hq;
-  pn[P_MOE_NORM] = L * d;
-  pn[P_ROUTER] = L * E * d;
-  pn[P_WGATE] = L * E * F * d;
-  pn[P_WUP] = L * E * F * d;
-  pn[P_WDOWN] = L * E * d * F;
+  pn[P_ATTN_NORM] = U * d;
+  pn[P_WQKV] = U * 3 * hq * d;
+  pn[P_WO] = U * d * hq;
+  pn[P_MOE_NORM] = U * d;
+  pn[P_ROUTER] = U * E * d;
+  pn[P_WGATE] = U * E * F * d;
+  pn[P_WUP] = U * E * F * d;
+  pn[P_WDOWN] = U * E * d * F;
   pn[P_FINAL_NORM] = d;
   pn[P_LM_HEAD] = V * d;
   long long po = 0;
@@ -252,8 +256,9 @@ int32_t mt_param_layout(const mt_hparams* hp, mt_tensor_desc* out, int32_t cap) 
   if (cap > 0 && !out) return -MT_ERR_ARG;
   MtPlan P;
   make_plan(hp, &P);
-  const long long L = hp->n_layers, d = hp->d_model, E = hp->n_experts, F = hp->d_ff, V = hp->vocab;
+  const long long L = P.D.U, d = hp->d_model, E = hp->n_experts, F = hp->d_ff, V = hp->vocab;
   const long long hq = (long long)hp->n_heads * hp->head_dim;
+  // per-layer tensors have one slot per distinct layer (U = n_layers unless looped)
   const long long shapes[P_COUNT][4] = {{V, d}, {L, d}, {L, 3 * hq, d}, {L, d, hq}, {L, d}, {L, E, d},
                                         {L, E, F, d}, {L, E, F, d}, {L, E, d, F}, {d}, {V, d}};
   const int ndims[P_COUNT] = {2, 2, 3, 3, 2, 3, 4, 4, 4, 1, 2};
@@ -386,6 +391,7 @@ int launch_update(int op, int layer, float* params, void* shadow, float* grads, 
   memcpy(a->aoff, P.aoff, sizeof(a->aoff));
   a->use_tc = want_tc ? 1 : 0;
   a->use_dsg = bf16 && P.abytes[A_DSG] > 0;
+  a->act_layers = (hp->flags & MT_FLAG_RECOMPUTE_EXPERT_ACT) ? 1 : hp->n_layers;
   // counters need whole 128-row blocks on both sides of every hand-off
   a->deps = bf16 && !(hp->flags & MT_FLAG_BARRIERS_ONLY);
   a->smem_bytes = (int)smem;

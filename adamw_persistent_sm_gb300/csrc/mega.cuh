@@ -36,6 +36,15 @@ __device__ __forceinline__ float* pgrad(const KArgs& a, int pid) { return a.grad
 // overwrites it): every tensor after the first microbatch of an update, and
 // under selective updates only the expert tensors.
 __device__ __forceinline__ bool acc_of(const KArgs& a, int pid) { return (a.acc_mask >> pid) & 1u; }
+// Weight slot of layer visit l: the looped model applies its U distinct
+// layers in turn (visit l uses slot l mod U; U = L without looping).
+__device__ __forceinline__ int wslot(const KArgs& a, int l) { return l % a.D.U; }
+// Gradient write of layer visit l into its slot: the backward meets the
+// visits in decreasing order, so every visit but the last U (the first ones
+// processed) adds into what a later visit already wrote.
+__device__ __forceinline__ bool acc_visit(const KArgs& a, int pid, int l) {
+  return acc_of(a, pid) || l < a.D.L - a.D.U;
+}
 
 // Column tiles of the LM-head product (one cross-entropy partial each).
 template <class OP>
@@ -156,8 +165,8 @@ __device__ __noinline__ void job_router(const KArgs& a, int l, char* smem, const
   float* Z = abuf<float>(a, A_Z) + (long long)l * D.T * D.E;
   int* IDX = abuf<int>(a, A_IDX) + (long long)l * D.T * D.K;
   float* WGT = abuf<float>(a, A_WGT) + (long long)l * D.T * D.K;
-  const float* g = pmaster(a, P_MOE_NORM) + (long long)l * D.d;
-  const float* Wr = pmaster(a, P_ROUTER) + (long long)l * D.E * D.d;
+  const float* g = pmaster(a, P_MOE_NORM) + (long long)wslot(a, l) * D.d;
+  const float* Wr = pmaster(a, P_ROUTER) + (long long)wslot(a, l) * D.E * D.d;
   const uint32_t rowb = (uint32_t)D.d * 4u;
   // shared memory: [mbarriers of the row rings | router weights (fp32, E x d)
   // | per-expert counts | row rings]
@@ -467,7 +476,7 @@ __device__ __noinline__ void job_combine(const KArgs& a, int l, Sched& s, unsign
   const int* INVM = abuf<int>(a, A_INVM) + (long long)l * D.T * D.K;
   float* Xn = abuf<float>(a, A_X) + (long long)(l + 1) * D.T * D.d;
   const bool last = (l + 1 == D.L);
-  const float* gp = last ? pmaster(a, P_FINAL_NORM) : pmaster(a, P_ATTN_NORM) + (long long)(l + 1) * D.d;
+  const float* gp = last ? pmaster(a, P_FINAL_NORM) : pmaster(a, P_ATTN_NORM) + (long long)wslot(a, l + 1) * D.d;
   OP* Rn = last ? abuf<OP>(a, A_RF) : abuf<OP>(a, A_R) + (long long)(l + 1) * D.T * D.d;
   float* invn = last ? abuf<float>(a, A_INVF) : abuf<float>(a, A_INV1) + (long long)(l + 1) * D.T;
   // items: groups of MT_DEP_GROUP tokens (each warp takes every 8th token of
@@ -1059,7 +1068,7 @@ __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char*
   const float* DZ = abuf<float>(a, A_DZ);
   const int* INVM = abuf<int>(a, A_INVM) + (long long)l * D.T * D.K;
   const int* IDX = abuf<int>(a, A_IDX) + (long long)l * D.T * D.K;
-  const float* Wr = pmaster(a, P_ROUTER) + (long long)l * D.E * D.d;
+  const float* Wr = pmaster(a, P_ROUTER) + (long long)wslot(a, l) * D.E * D.d;
   const float* XM = abuf<float>(a, A_XM) + (long long)l * D.T * D.d;
   const float* inv2 = abuf<float>(a, A_INV2) + (long long)l * D.T;
   float* DX = abuf<float>(a, A_DX);
@@ -1077,7 +1086,7 @@ __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char*
   with_nc(D.d, [&](auto NCc) {
     constexpr int NC = decltype(NCc)::value;
     Row<NC> g, dr2, tmp, x, dx, gacc;
-    row_ld(g, pmaster(a, P_MOE_NORM) + (long long)l * D.d, n4);
+    row_ld(g, pmaster(a, P_MOE_NORM) + (long long)wslot(a, l) * D.d, n4);
     row_scale(gacc, g, 0.f);
     if (piped) {
       // staged: the K expert-input gradient rows, x_mid and dx of each token;
@@ -1192,7 +1201,7 @@ __device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s, 
   with_nc(D.d, [&](auto NCc) {
     constexpr int NC = decltype(NCc)::value;
     Row<NC> g, dy, x, dx, acc, gacc;
-    row_ld(g, pmaster(a, P_ATTN_NORM) + (long long)l * D.d, n4);
+    row_ld(g, pmaster(a, P_ATTN_NORM) + (long long)wslot(a, l) * D.d, n4);
     row_scale(gacc, g, 0.f);
     if (p.ns > 0) {
       // staged: dr, x and dx rows of each token; header: t, 1/rms (1/rms of
@@ -1424,7 +1433,7 @@ __device__ __forceinline__ bool router_grad_cta(const KArgs& a, int l, char* sme
   const float* XM = abuf<float>(a, A_XM) + (long long)l * D.T * D.d;
   const float* inv2 = abuf<float>(a, A_INV2) + (long long)l * D.T;
   const float* DZ = abuf<float>(a, A_DZ);
-  const float* g = pmaster(a, P_MOE_NORM) + (long long)l * D.d;
+  const float* g = pmaster(a, P_MOE_NORM) + (long long)wslot(a, l) * D.d;
   constexpr int NCOL = 3;                       // columns per lane (d <= 768)
   const int cpw = D.d / MT_WARPS;
   int col[NCOL];
@@ -1518,7 +1527,7 @@ static __device__ __noinline__ int job_router_grad(const KArgs& a, int l, Sched&
   }
   if (done) return (int)gridDim.x;
   ColArgs c{COL_MOE, nullptr, abuf<float>(a, A_XM) + (long long)l * D.T * D.d,
-            abuf<float>(a, A_INV2) + (long long)l * D.T, pmaster(a, P_MOE_NORM) + (long long)l * D.d,
+            abuf<float>(a, A_INV2) + (long long)l * D.T, pmaster(a, P_MOE_NORM) + (long long)wslot(a, l) * D.d,
             abuf<float>(a, A_DZ), 0};
   job_colpart(a, c, s, smem);
   return 0;
@@ -1529,13 +1538,12 @@ static __device__ __noinline__ int job_router_grad(const KArgs& a, int l, Sched&
 // the router-row count of the reduction that wrote those rows (0: gain only).
 static __device__ __noinline__ void job_colfinal(const KArgs& a, int row0, int nrows, int E_kind, float* out_rows,
                                                  float* out_last, int last_is_separate, Sched& s, int nchunks,
-                                                 int pid) {
+                                                 bool acc) {
   const MtDims& D = a.D;
   const int G = s.G;
   const int nused = nchunks > 0 ? nchunks : col_nchunks(D, G, E_kind);
   const float* PART = abuf<float>(a, A_PART);
   const int n = nrows * D.d;
-  const bool acc = acc_of(a, pid);
   for (int e = s.first() * MT_THREADS + threadIdx.x; e < n; e += G * MT_THREADS) {
     const int r = e / D.d, col = e % D.d;
     float v = 0.f;
@@ -1897,6 +1905,8 @@ struct Gemms {
   const KArgs& a;
   const MtDims& D;
   __device__ Gemms(const KArgs& a_) : a(a_), D(a_.D) {}
+  // slot of layer l in the expert-activation buffers [g | u] and silu(g) u
+  __device__ int al(int l) const { return a.act_layers == D.L ? l : 0; }
 
   __device__ GOperand opnd(const void* p, long long ld, int mn) const {
     GOperand o;
@@ -1923,8 +1933,8 @@ struct Gemms {
     GemmDesc g = base(D.T, 3 * D.hq, D.d, EPI_ROPE);
     g.A = opnd(abuf<OP>(a, A_R) + (long long)l * D.T * D.d, D.d, 0);
     g.A.map0 = MAP_R; g.A.y0 = l * D.T;
-    g.B = opnd(pweight<OP>(a, P_WQKV) + (long long)l * 3 * D.hq * D.d, D.d, 0);
-    g.B.map0 = MAP_WQKV; g.B.y0 = l * 3 * D.hq;
+    g.B = opnd(pweight<OP>(a, P_WQKV) + (long long)wslot(a, l) * 3 * D.hq * D.d, D.d, 0);
+    g.B.map0 = MAP_WQKV; g.B.y0 = wslot(a, l) * 3 * D.hq;
     g.out = abuf<OP>(a, A_QKV) + (long long)l * D.T * 3 * D.hq; g.ldo = 3 * D.hq;
     g.omap = MAP_E_QKV64; g.oy0 = l * D.T;
     g.rope = abuf<float>(a, A_ROPE);
@@ -1934,8 +1944,8 @@ struct Gemms {
     GemmDesc g = base(D.T, D.d, D.hq, EPI_RESID);
     g.A = opnd(abuf<OP>(a, A_O) + (long long)l * D.T * D.hq, D.hq, 0);
     g.A.map0 = MAP_O; g.A.y0 = l * D.T;
-    g.B = opnd(pweight<OP>(a, P_WO) + (long long)l * D.d * D.hq, D.hq, 0);
-    g.B.map0 = MAP_WO; g.B.y0 = l * D.d;
+    g.B = opnd(pweight<OP>(a, P_WO) + (long long)wslot(a, l) * D.d * D.hq, D.hq, 0);
+    g.B.map0 = MAP_WO; g.B.y0 = wslot(a, l) * D.d;
     g.out = abuf<float>(a, A_XM) + (long long)l * D.T * D.d; g.ldo = D.d;
     g.aux = abuf<float>(a, A_X) + (long long)l * D.T * D.d; g.ldaux = D.d;
     g.omap = MAP_E_XM; g.oy0 = l * D.T; g.amap = MAP_E_X; g.ay0 = l * D.T;
@@ -1946,23 +1956,23 @@ struct Gemms {
     g.rag = RAG_M; g.offs = offs(l); g.nseg = D.E;
     g.A = opnd(abuf<OP>(a, A_XS) + (long long)l * D.Pmax * D.d, D.d, 0);
     g.A.map0 = MAP_XS; g.A.y0 = l * D.Pmax;
-    g.B = opnd(pweight<OP>(a, P_WGATE) + (long long)l * D.E * D.F * D.d, D.d, 0);
-    g.B.p1 = pweight<OP>(a, P_WUP) + (long long)l * D.E * D.F * D.d;
+    g.B = opnd(pweight<OP>(a, P_WGATE) + (long long)wslot(a, l) * D.E * D.F * D.d, D.d, 0);
+    g.B.p1 = pweight<OP>(a, P_WUP) + (long long)wslot(a, l) * D.E * D.F * D.d;
     g.B.two = 1; g.B.seg = (long long)D.F * D.d;
-    g.B.map0 = MAP_WGATE; g.B.map1 = MAP_WUP; g.B.y0 = l * D.E * D.F; g.B.yseg = D.F;
-    g.out = abuf<OP>(a, A_GU) + (long long)l * D.Pmax * 2 * D.F; g.ldo = 2 * D.F;
-    g.out2 = abuf<OP>(a, A_ACT) + (long long)l * D.Pmax * D.F; g.ldo2 = D.F;
-    g.omap = MAP_E_GU; g.oy0 = l * D.Pmax; g.omap2 = MAP_E_ACT; g.oy02 = l * D.Pmax;
+    g.B.map0 = MAP_WGATE; g.B.map1 = MAP_WUP; g.B.y0 = wslot(a, l) * D.E * D.F; g.B.yseg = D.F;
+    g.out = abuf<OP>(a, A_GU) + (long long)al(l) * D.Pmax * 2 * D.F; g.ldo = 2 * D.F;
+    g.out2 = abuf<OP>(a, A_ACT) + (long long)al(l) * D.Pmax * D.F; g.ldo2 = D.F;
+    g.omap = MAP_E_GU; g.oy0 = al(l) * D.Pmax; g.omap2 = MAP_E_ACT; g.oy02 = al(l) * D.Pmax;
     return g;
   }
   __device__ GemmDesc down(int l) const {
     GemmDesc g = base(D.Pmax, D.d, D.F, EPI_STORE_F32);
     g.rag = RAG_M; g.offs = offs(l); g.nseg = D.E;
-    g.A = opnd(abuf<OP>(a, A_ACT) + (long long)l * D.Pmax * D.F, D.F, 0);
-    g.A.map0 = MAP_ACT; g.A.y0 = l * D.Pmax;
-    g.B = opnd(pweight<OP>(a, P_WDOWN) + (long long)l * D.E * D.d * D.F, D.F, 0);
+    g.A = opnd(abuf<OP>(a, A_ACT) + (long long)al(l) * D.Pmax * D.F, D.F, 0);
+    g.A.map0 = MAP_ACT; g.A.y0 = al(l) * D.Pmax;
+    g.B = opnd(pweight<OP>(a, P_WDOWN) + (long long)wslot(a, l) * D.E * D.d * D.F, D.F, 0);
     g.B.seg = (long long)D.d * D.F;
-    g.B.map0 = MAP_WDOWN; g.B.y0 = l * D.E * D.d; g.B.yseg = D.d;
+    g.B.map0 = MAP_WDOWN; g.B.y0 = wslot(a, l) * D.E * D.d; g.B.yseg = D.d;
     g.out = abuf<float>(a, A_Y) + (long long)l * D.Pmax * D.d; g.ldo = D.d;
     g.omap = MAP_E_Y; g.oy0 = l * D.Pmax;
     return g;
@@ -1997,32 +2007,32 @@ struct Gemms {
     GemmDesc g = base(D.Pmax, D.F, D.d, EPI_SWIGLU_BWD);
     g.rag = RAG_M; g.offs = offs(l); g.nseg = D.E;
     g.A = opnd(abuf<OP>(a, A_DY), D.d, 0); g.A.map0 = MAP_DY;
-    g.B = opnd(pweight<OP>(a, P_WDOWN) + (long long)l * D.E * D.d * D.F, D.F, 1);
+    g.B = opnd(pweight<OP>(a, P_WDOWN) + (long long)wslot(a, l) * D.E * D.d * D.F, D.F, 1);
     g.B.seg = (long long)D.d * D.F;
-    g.B.map0 = MAP_WDOWN; g.B.y0 = l * D.E * D.d; g.B.yseg = D.d;
+    g.B.map0 = MAP_WDOWN; g.B.y0 = wslot(a, l) * D.E * D.d; g.B.yseg = D.d;
     g.out = abuf<OP>(a, A_DGU); g.ldo = 2 * D.F;
-    g.aux = abuf<OP>(a, A_GU) + (long long)l * D.Pmax * 2 * D.F; g.ldaux = 2 * D.F;
-    g.omap = MAP_E_DGU; g.amap = MAP_E_GU; g.ay0 = l * D.Pmax;
+    g.aux = abuf<OP>(a, A_GU) + (long long)al(l) * D.Pmax * 2 * D.F; g.ldaux = 2 * D.F;
+    g.omap = MAP_E_DGU; g.amap = MAP_E_GU; g.ay0 = al(l) * D.Pmax;
     return g;
   }
   __device__ GemmDesc down_wgrad(int l) const {
     GemmDesc g = base(D.d, D.F, 0, EPI_GRAD);
     g.rag = RAG_K; g.offs = offs(l); g.nseg = D.E;
     g.A = opnd(abuf<OP>(a, A_DY), D.d, 1); g.A.map0 = MAP_DY;
-    g.B = opnd(abuf<OP>(a, A_ACT) + (long long)l * D.Pmax * D.F, D.F, 1);
-    g.B.map0 = MAP_ACT; g.B.y0 = l * D.Pmax;
-    g.out = pgrad(a, P_WDOWN) + (long long)l * D.E * D.d * D.F; g.ldo = D.F;
-    g.oseg = (long long)D.d * D.F; g.accumulate = acc_of(a, P_WDOWN);
+    g.B = opnd(abuf<OP>(a, A_ACT) + (long long)al(l) * D.Pmax * D.F, D.F, 1);
+    g.B.map0 = MAP_ACT; g.B.y0 = al(l) * D.Pmax;
+    g.out = pgrad(a, P_WDOWN) + (long long)wslot(a, l) * D.E * D.d * D.F; g.ldo = D.F;
+    g.oseg = (long long)D.d * D.F; g.accumulate = acc_visit(a, P_WDOWN, l);
     return g;
   }
   __device__ GemmDesc gateup_dgrad(int l) const {
     GemmDesc g = base(D.Pmax, D.d, 2 * D.F, EPI_STORE_F32);
     g.rag = RAG_M; g.offs = offs(l); g.nseg = D.E;
     g.A = opnd(abuf<OP>(a, A_DGU), 2 * D.F, 0); g.A.map0 = MAP_DGU;
-    g.B = opnd(pweight<OP>(a, P_WGATE) + (long long)l * D.E * D.F * D.d, D.d, 1);
-    g.B.p1 = pweight<OP>(a, P_WUP) + (long long)l * D.E * D.F * D.d;
+    g.B = opnd(pweight<OP>(a, P_WGATE) + (long long)wslot(a, l) * D.E * D.F * D.d, D.d, 1);
+    g.B.p1 = pweight<OP>(a, P_WUP) + (long long)wslot(a, l) * D.E * D.F * D.d;
     g.B.two = 2; g.B.split = D.F; g.B.seg = (long long)D.F * D.d;
-    g.B.map0 = MAP_WGATE; g.B.map1 = MAP_WUP; g.B.y0 = l * D.E * D.F; g.B.yseg = D.F;
+    g.B.map0 = MAP_WGATE; g.B.map1 = MAP_WUP; g.B.y0 = wslot(a, l) * D.E * D.F; g.B.yseg = D.F;
     g.out = abuf<float>(a, A_DXS); g.ldo = D.d;
     g.omap = MAP_E_DXS;
     return g;
@@ -2033,16 +2043,16 @@ struct Gemms {
     g.A = opnd(abuf<OP>(a, A_DGU), 2 * D.F, 1); g.A.map0 = MAP_DGU;
     g.B = opnd(abuf<OP>(a, A_XS) + (long long)l * D.Pmax * D.d, D.d, 1);
     g.B.map0 = MAP_XS; g.B.y0 = l * D.Pmax;
-    g.out = pgrad(a, P_WGATE) + (long long)l * D.E * D.F * D.d;
-    g.out1 = pgrad(a, P_WUP) + (long long)l * D.E * D.F * D.d;
-    g.osplit = D.F; g.ldo = D.d; g.oseg = (long long)D.F * D.d; g.accumulate = acc_of(a, P_WGATE);
+    g.out = pgrad(a, P_WGATE) + (long long)wslot(a, l) * D.E * D.F * D.d;
+    g.out1 = pgrad(a, P_WUP) + (long long)wslot(a, l) * D.E * D.F * D.d;
+    g.osplit = D.F; g.ldo = D.d; g.oseg = (long long)D.F * D.d; g.accumulate = acc_visit(a, P_WGATE, l);
     return g;
   }
   __device__ GemmDesc wo_dgrad(int l) const {
     GemmDesc g = base(D.T, D.hq, D.d, EPI_STORE_OP_D);
     g.A = opnd(abuf<OP>(a, A_DXO), D.d, 0); g.A.map0 = MAP_DXO;
-    g.B = opnd(pweight<OP>(a, P_WO) + (long long)l * D.d * D.hq, D.hq, 1);
-    g.B.map0 = MAP_WO; g.B.y0 = l * D.d;
+    g.B = opnd(pweight<OP>(a, P_WO) + (long long)wslot(a, l) * D.d * D.hq, D.hq, 1);
+    g.B.map0 = MAP_WO; g.B.y0 = wslot(a, l) * D.d;
     g.out = abuf<OP>(a, A_DO); g.ldo = D.hq;
     g.aux = abuf<OP>(a, A_O) + (long long)l * D.T * D.hq; g.ldaux = D.hq;
     g.out2 = abuf<float>(a, A_DSUM); g.ldo2 = D.H;
@@ -2064,15 +2074,15 @@ struct Gemms {
     g.A = opnd(abuf<OP>(a, A_DXO), D.d, 1); g.A.map0 = MAP_DXO;
     g.B = opnd(abuf<OP>(a, A_O) + (long long)l * D.T * D.hq, D.hq, 1);
     g.B.map0 = MAP_O; g.B.y0 = l * D.T;
-    g.out = pgrad(a, P_WO) + (long long)l * D.d * D.hq; g.ldo = D.hq; g.accumulate = acc_of(a, P_WO);
+    g.out = pgrad(a, P_WO) + (long long)wslot(a, l) * D.d * D.hq; g.ldo = D.hq; g.accumulate = acc_visit(a, P_WO, l);
     split(g);
     return g;
   }
   __device__ GemmDesc qkv_dgrad(int l) const {
     GemmDesc g = base(D.T, D.d, 3 * D.hq, EPI_STORE_F32);
     g.A = opnd(abuf<OP>(a, A_DQKV), 3 * D.hq, 0); g.A.map0 = MAP_DQKV;
-    g.B = opnd(pweight<OP>(a, P_WQKV) + (long long)l * 3 * D.hq * D.d, D.d, 1);
-    g.B.map0 = MAP_WQKV; g.B.y0 = l * 3 * D.hq;
+    g.B = opnd(pweight<OP>(a, P_WQKV) + (long long)wslot(a, l) * 3 * D.hq * D.d, D.d, 1);
+    g.B.map0 = MAP_WQKV; g.B.y0 = wslot(a, l) * 3 * D.hq;
     g.out = abuf<float>(a, A_DR); g.ldo = D.d;
     g.omap = MAP_E_DR;
     return g;
@@ -2082,20 +2092,19 @@ struct Gemms {
     g.A = opnd(abuf<OP>(a, A_DQKV), 3 * D.hq, 1); g.A.map0 = MAP_DQKV;
     g.B = opnd(abuf<OP>(a, A_R) + (long long)l * D.T * D.d, D.d, 1);
     g.B.map0 = MAP_R; g.B.y0 = l * D.T;
-    g.out = pgrad(a, P_WQKV) + (long long)l * 3 * D.hq * D.d; g.ldo = D.d; g.accumulate = acc_of(a, P_WQKV);
+    g.out = pgrad(a, P_WQKV) + (long long)wslot(a, l) * 3 * D.hq * D.d; g.ldo = D.d; g.accumulate = acc_visit(a, P_WQKV, l);
     split(g);
     return g;
   }
 };
 
 // out[i] (+)= sum over slices s (in order) of KPART[s][i], i < M*N.
-static __device__ __noinline__ void job_ksplit_sum(const KArgs& a, float* out, int M, int N, Sched& s, int pid) {
+static __device__ __noinline__ void job_ksplit_sum(const KArgs& a, float* out, int M, int N, Sched& s, bool acc) {
   const int ks = ksplit_of(a, M, N, a.D.T);
   if (ks <= 1) return;
   const float4* P = reinterpret_cast<const float4*>(abuf<float>(a, A_KPART));
   float4* o = reinterpret_cast<float4*>(out);
   const long long n4 = (long long)M * N / 4;
-  const bool acc = acc_of(a, pid);
   for (long long i = (long long)s.first() * MT_THREADS + threadIdx.x; i < n4; i += (long long)s.G * MT_THREADS) {
     float4 v = acc ? o[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < ks; ++k) {
@@ -2299,10 +2308,19 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   MT_SYNC();
   for (int l = D.L - 1; l >= 0; --l) {
     job_moe_bwd1<OP>(a, l, s, smem); TJ(17);
+    // memory rule: the arena keeps one layer's expert activations; re-run
+    // this layer's gate/up product (same inputs, same tiles: the same values).
+    // Its tiles come from a ticket; the rotating item map of the later jobs
+    // (whose per-CTA partial sums follow it) is left as without the rule.
+    if (a.act_layers != D.L) {
+      const int rot = s.base;
+      run_gemm<OP>(a, TK(gm.gateup(l), l, TK_GATEUP_AGAIN), s, smem, tc); TJ(37);
+      s.base = rot;
+    }
     MT_SYNC();
-    if (l == D.L - 1) job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_FINAL_NORM), nullptr, 0, s, (int)G, P_FINAL_NORM);
-    else job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM) + (long long)(l + 1) * D.d, nullptr, 0, s, (int)G,
-                      P_ATTN_NORM);
+    if (l == D.L - 1) job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_FINAL_NORM), nullptr, 0, s, (int)G, acc_of(a, P_FINAL_NORM));
+    else job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM) + (long long)wslot(a, l + 1) * D.d, nullptr, 0, s, (int)G,
+                      acc_visit(a, P_ATTN_NORM, l + 1));
     TJ(18);
     run_gemm<OP>(a, TK(gm.down_wgrad(l), l, TK_DOWN_WGRAD), s, smem, tc); TJ(20);
     run_gemm<OP>(a, TK(gm.down_dgrad(l), l, TK_DOWN_DGRAD), s, smem, tc); TJ(19);
@@ -2318,9 +2336,11 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     run_gemm<OP>(a, TK(gm.wo_wgrad(l), l, TK_WO_WGRAD), s, smem, tc); TJ(25);
     run_gemm<OP>(a, TK(gm.wo_dgrad(l), l, TK_WO_DGRAD), s, smem, tc); TJ(24);
     MT_SYNC();
-    job_colfinal(a, 0, D.E, D.E, pgrad(a, P_ROUTER) + (long long)l * D.E * D.d, nullptr, 0, s, rg_chunks, P_ROUTER);
-    job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_MOE_NORM) + (long long)l * D.d, nullptr, 0, s, (int)G, P_MOE_NORM); TJ(18);
-    job_ksplit_sum(a, pgrad(a, P_WO) + (long long)l * D.d * D.hq, D.d, D.hq, s, P_WO); TJ(32);
+    job_colfinal(a, 0, D.E, D.E, pgrad(a, P_ROUTER) + (long long)wslot(a, l) * D.E * D.d, nullptr, 0, s, rg_chunks,
+                 acc_visit(a, P_ROUTER, l));
+    job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_MOE_NORM) + (long long)wslot(a, l) * D.d, nullptr, 0, s, (int)G,
+                 acc_visit(a, P_MOE_NORM, l)); TJ(18);
+    job_ksplit_sum(a, pgrad(a, P_WO) + (long long)wslot(a, l) * D.d * D.hq, D.d, D.hq, s, acc_visit(a, P_WO, l)); TJ(32);
     if constexpr (sizeof(OP) == 2) {
       if (a.use_dsg) {
         // dK/dV stores dS^T; after a grid barrier dQ is a product over it
@@ -2336,12 +2356,13 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     run_gemm<OP>(a, TK(gm.qkv_dgrad(l), l, TK_QKV_DGRAD), s, smem, tc); TJ(27);
     MT_SYNC();
     job_attn_norm_bwd<OP>(a, l, s, smem); TJ(29);
-    job_ksplit_sum(a, pgrad(a, P_WQKV) + (long long)l * 3 * D.hq * D.d, 3 * D.hq, D.d, s, P_WQKV); TJ(33);
+    job_ksplit_sum(a, pgrad(a, P_WQKV) + (long long)wslot(a, l) * 3 * D.hq * D.d, 3 * D.hq, D.d, s,
+                   acc_visit(a, P_WQKV, l)); TJ(33);
     MT_SYNC();
   }
   job_embed_bwd(a, (int*)smem); TJ(30);
   MT_SYNC();
-  job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM), nullptr, 0, s, (int)G, P_ATTN_NORM); TJ(18);
+  job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM), nullptr, 0, s, (int)G, acc_visit(a, P_ATTN_NORM, 0)); TJ(18);
 
   // ---------------- optimizer (last microbatch) ----------------
   if (a.n_ranges > 0) {

@@ -93,6 +93,7 @@ static_assert(MAP_COUNT <= MT_NMAPS, "too many tensor maps");
 
 struct MtDims {
   int V, d, L, H, hd, hq, E, K, F, B, S, T;
+  int U;       // distinct layers (weight slots); layer visit l uses slot l % U
   int Pmax;    // rows of expert-ordered buffers: T*K + E*(MT_TILE_M-1), rounded up to MT_TILE_M
   int nch;     // maximum number of CTAs (chunks) the arena was sized for
   int op_bytes;
@@ -136,6 +137,7 @@ enum TicketId {
   TK_ADAMW = 0,
   TK_QKV, TK_WO, TK_GATEUP, TK_DOWN,
   TK_DOWN_DGRAD, TK_DOWN_WGRAD, TK_GU_DGRAD, TK_GU_WGRAD, TK_WO_DGRAD, TK_WO_WGRAD, TK_QKV_DGRAD, TK_QKV_WGRAD,
+  TK_GATEUP_AGAIN,              // the gate/up product re-run in the backward (memory rule)
   TK_COUNT_,
   // the head's set: LM-head products and the optimizer ranges
   TK_LM = TK_QKV, TK_LM_DGRAD = TK_WO, TK_LM_WGRAD = TK_GATEUP,
@@ -206,6 +208,8 @@ struct KArgs {
   int use_tc;                   // tcgen05 GEMMs (bf16 only)
   int use_dsg;                  // dQ as a product over stored dS^T (A_DSG, MAP_E_DS/DSL; bf16 only)
   int deps;                     // dependency counters replace the grid barriers they cover
+  int act_layers;               // layers of [g | u] and silu(g) u the arena keeps: L, or 1 when the
+                                // backward re-runs each layer's gate/up product (memory rule)
   int smem_bytes;               // dynamic shared memory of the launch
   CUtensorMap maps[MT_NMAPS];
 };

@@ -60,20 +60,22 @@ int mt_build_tensor_maps(KArgs* a, void* shadow) {
   if (!g_encode) return MT_ERR_CUDA;
   const MtDims& D = a->D;
   const long long L = D.L, T = D.T, d = D.d, hq = D.hq, E = D.E, F = D.F, V = D.V, Pm = D.Pmax;
+  const long long AL = a->act_layers;       // layers of expert activations the arena keeps
+  const long long U = D.U;                  // weight slots of the per-layer tensors
   char* ar = a->arena;
   const char* w = (const char*)shadow;
   auto P = [&](int pid) { return (const void*)(w + a->poff[pid] * 2); };
   auto A = [&](int id) { return (const void*)(ar + a->aoff[id]); };
   bool ok = true;
   ok &= encode(&a->maps[MAP_R], A(A_R), L * T, d);
-  ok &= encode(&a->maps[MAP_WQKV], P(P_WQKV), L * 3 * hq, d);
+  ok &= encode(&a->maps[MAP_WQKV], P(P_WQKV), U * 3 * hq, d);
   ok &= encode(&a->maps[MAP_O], A(A_O), L * T, hq);
-  ok &= encode(&a->maps[MAP_WO], P(P_WO), L * d, hq);
+  ok &= encode(&a->maps[MAP_WO], P(P_WO), U * d, hq);
   ok &= encode(&a->maps[MAP_XS], A(A_XS), L * Pm, d);
-  ok &= encode(&a->maps[MAP_WGATE], P(P_WGATE), L * E * F, d);
-  ok &= encode(&a->maps[MAP_WUP], P(P_WUP), L * E * F, d);
-  ok &= encode(&a->maps[MAP_ACT], A(A_ACT), L * Pm, F);
-  ok &= encode(&a->maps[MAP_WDOWN], P(P_WDOWN), L * E * d, F);
+  ok &= encode(&a->maps[MAP_WGATE], P(P_WGATE), U * E * F, d);
+  ok &= encode(&a->maps[MAP_WUP], P(P_WUP), U * E * F, d);
+  ok &= encode(&a->maps[MAP_ACT], A(A_ACT), AL * Pm, F);
+  ok &= encode(&a->maps[MAP_WDOWN], P(P_WDOWN), U * E * d, F);
   ok &= encode(&a->maps[MAP_RF], A(A_RF), T, d);
   ok &= encode(&a->maps[MAP_WLM], P(P_LM_HEAD), V, d);
   ok &= encode(&a->maps[MAP_DLOGITS], A(A_DLOGITS), T, V);
@@ -84,8 +86,8 @@ int mt_build_tensor_maps(KArgs* a, void* shadow) {
   ok &= encode(&a->maps[MAP_QKV], A(A_QKV), L * T, 3 * hq);
   ok &= encode(&a->maps[MAP_DOUT], A(A_DO), T, hq);
   ok &= encode_epi(&a->maps[MAP_E_QKV], A(A_QKV), L * T, 3 * hq, false);
-  ok &= encode_epi(&a->maps[MAP_E_GU], A(A_GU), L * Pm, 2 * F, false);
-  ok &= encode_epi(&a->maps[MAP_E_ACT], A(A_ACT), L * Pm, F, false);
+  ok &= encode_epi(&a->maps[MAP_E_GU], A(A_GU), AL * Pm, 2 * F, false);
+  ok &= encode_epi(&a->maps[MAP_E_ACT], A(A_ACT), AL * Pm, F, false);
   ok &= encode_epi(&a->maps[MAP_E_DGU], A(A_DGU), Pm, 2 * F, false);
   ok &= encode_box(&a->maps[MAP_E_DLOGITS], A(A_DLOGITS), T, V, false, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   ok &= encode_box(&a->maps[MAP_E_QKV64], A(A_QKV), L * T, 3 * hq, false, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);

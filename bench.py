@@ -33,7 +33,30 @@ WORKLOADS = {
     "accum16": "16 microbatches of 8 x 1024 tokens, one optimizer step, 219M-param MoE",
     "top8": "1 x 4096 Zipf tokens, top-8-of-32 experts d_ff 256, 219M-param MoE",
     "tiny": "2 x 32 tokens, tiny fp32 MoE (d 64, 2 layers, 4 experts)",
+    "looped": "32 x 1024 tokens, looped MoE: 4 distinct layers each visited twice (8 layer visits)",
+    "selective": "selective updates: 16 microbatches of 2 x 1024 tokens, shared tensors stepped after "
+                 "each microbatch, experts after the 16th",
+    "b32_lowmem": "b32 with both memory rules (no attention dS^T kept, one layer of expert activations)",
 }
+NOMINAL_BF16_TFLOPS = 2250.0   # GB300 dense bf16 tensor peak (vendor figure, without sparsity)
+
+
+def workload_config(name):
+    """The model configuration and launch flags of a bench workload."""
+    from adamw_persistent_sm_gb300 import binding as B
+    if name == "selective":
+        return mi.get_config("b2", micro_count=16), B.MT_FLAG_SELECTIVE_EXPERTS
+    if name == "b32_lowmem":
+        return mi.get_config("b32"), B.MT_FLAG_RECOMPUTE_ATTN_DS | B.MT_FLAG_RECOMPUTE_EXPERT_ACT
+    return mi.get_config(name), 0
+
+
+def param_bytes_per_update(n_params: int, micro_count: int = 1) -> float:
+    """Algorithmic HBM bytes of the parameter term: gradient write 4, AdamW
+    reads p, g, m, v 16 and writes p, m, v 12 plus the bf16 shadow 2, bf16
+    weight reads in the forward and the dgrad products 4 (38 B/param); each
+    later microbatch adds a read-modify-write of the gradient (8 B/param)."""
+    return n_params * (38.0 + 8.0 * (micro_count - 1))
 METRIC = "MoE train-update ms & tokens/s (B2x1024, B32x1024); % bf16 tensor peak"
 ARENA_HDR_BYTES = 4512   # mt_read_outputs copies the arena's control header
 
@@ -46,6 +69,37 @@ def flops_per_update(cfg) -> float:
     toks = cfg.tokens_per_update
     attn = 3 * 2 * cfg.batch * cfg.seq ** 2 * hq * L * cfg.micro_count
     return 6.0 * active * toks + attn
+
+
+def source_digest() -> str:
+    """sha256 over the CUDA sources and the C header: the kernel a profile
+    was taken from."""
+    import hashlib
+    h = hashlib.sha256()
+    for d in (os.path.join(ROOT, "adamw_persistent_sm_gb300", "csrc"), os.path.join(ROOT, "include")):
+        for f in sorted(os.listdir(d)):
+            if f.endswith((".cu", ".cuh", ".h")):
+                with open(os.path.join(d, f), "rb") as fh:
+                    h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config: str):
+    """DRAM bytes (read + write) per launch from the committed ncu summary of
+    this workload, or None when there is none or the kernel's sources have
+    changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"megakernel_{config}_dram.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- source_digest:") or line.startswith("- dram_bytes_per_launch:"):
+                k, v = line[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_digest") != source_digest() or "dram_bytes_per_launch" not in vals:
+        return None
+    return float(vals["dram_bytes_per_launch"])
 
 
 def load_peaks() -> dict:
@@ -144,7 +198,11 @@ def cpu_cores() -> int:
 
 # ---------------------------------------------------------------------------
 def run_reference(args, cfg, rank):
-    """The oracle as the reference arm: rank 0 only, host cores."""
+    """The oracle as the reference arm: rank 0 only, host cores.  A step is a
+    bounded sample of the workload (one sequence prefix of --ref-tokens
+    positions plus its share of the optimizer sweep); ms_per_step is that
+    measured sample time, and the time of a whole update at the same rate is
+    reported apart as an extrapolation."""
     if rank != 0:
         return
     params = mi.make_params(cfg)
@@ -162,7 +220,9 @@ def run_reference(args, cfg, rank):
     ms_update = cfg.tokens_per_update / tps * 1e3
     line = {
         "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_update,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / len(times) * 1e3,
+        "step_is": f"one bounded sample of {seq_tokens} tokens (measured)",
+        "ms_per_update_extrapolated": ms_update, "extrapolated_from_tokens": seq_tokens,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": f"{args.config}: {WORKLOADS[args.config]}"},
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
@@ -172,7 +232,96 @@ def run_reference(args, cfg, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, cfg, rank, world):
+def make_update_fn(tr, cfg, flags, dtoks):
+    """One step of a workload: the update's microbatch launches (under
+    selective updates one period: a shared step per microbatch, the expert
+    step after the last)."""
+    from adamw_persistent_sm_gb300 import binding as B
+
+    def one_update(step):
+        if flags & B.MT_FLAG_SELECTIVE_EXPERTS:
+            n = cfg.micro_count
+            for i, t in enumerate(dtoks):
+                tr.micro_step(t, i, step=(step - 1) * n + i + 1, flags=flags, expert_step=step)
+        else:
+            tr.update(dtoks, step=step, flags=flags)
+    return one_update
+
+
+def measure_workload(name, dev, steps=5, warmup=3):
+    """ms per update of another workload, timed with CUDA events on the
+    launching stream after warm-up (inputs resident in HBM)."""
+    import torch
+    from adamw_persistent_sm_gb300 import binding as B
+    from adamw_persistent_sm_gb300.trainer import MoETrainer
+    cfg, flags = workload_config(name)
+    tr = MoETrainer(cfg, dev, flags=flags)
+    tr.load_params(mi.make_params(cfg))
+    dtoks = [torch.as_tensor(t).to(dev) for t in mi.make_update_tokens(cfg)]
+    one = make_update_fn(tr, cfg, flags, dtoks)
+    for k in range(warmup):
+        one(k + 1)
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    evs = []
+    for k in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one(warmup + k + 1)
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize(dev)
+    out = tr.outputs()
+    if out.status != B.MT_OK:
+        raise RuntimeError(f"{name}: {B.status_string(out.status)}")
+    ms = [a.elapsed_time(b) for a, b in evs]
+    med = statistics.median(ms)
+    peaks = load_peaks()
+    flops = flops_per_update(cfg)
+    r = {"workload": WORKLOADS[name], "ms_per_update": med, "ms_min": min(ms), "ms_max": max(ms),
+         "tokens_per_s": cfg.tokens_per_update / (med / 1e3), "launches_per_update": cfg.micro_count,
+         "tflops": flops / (med / 1e3) / 1e12, "frac_of_measured_bf16": flops / (med / 1e3) / 1e12 / peaks["bf16"],
+         "arena_gb": tr.arena_bytes / 1e9, "timed_updates": steps}
+    if flags & B.MT_FLAG_SELECTIVE_EXPERTS:
+        r["ms_per_microbatch"] = med / cfg.micro_count
+        r["context_h100_ms_per_microbatch"] = 10.28
+    pb = param_bytes_per_update(tr.n_params, 1 if flags & B.MT_FLAG_SELECTIVE_EXPERTS else cfg.micro_count)
+    r["hbm_param_term_frac"] = pb / (med / 1e3) / 1e9 / peaks["hbm"]
+    r["hbm_param_term_note"] = ("38 B/param parameter term only (a lower bound on the algorithmic "
+                                "bytes) over the measured copy bandwidth")
+    del tr, dtoks
+    torch.cuda.empty_cache()
+    return r
+
+
+def barrier_idle_fraction(cfg, flags, dev):
+    """Mean over CTAs of the time spent waiting at grid barriers over the
+    launch's duration, from one traced update (MT_FLAG_TRACE)."""
+    import torch
+    from adamw_persistent_sm_gb300 import binding as B
+    from adamw_persistent_sm_gb300.trainer import MoETrainer
+    tr = MoETrainer(cfg, dev, flags=flags | B.MT_FLAG_TRACE)
+    tr.load_params(mi.make_params(cfg))
+    dtoks = [torch.as_tensor(t).to(dev) for t in mi.make_update_tokens(cfg)]
+    for k in range(2):
+        tr.update(dtoks, step=k + 1)
+    out = tr.outputs()
+    tv = tr.debug_view(B.MT_VIEW_TRACE, 0, torch.int64).cpu().numpy().reshape(-1, B.MT_TRACE_WORDS)
+    G = out.n_ctas
+    nb = min(out.n_phases, B.MT_TRACE_PHASES)
+    bars = tv[:G, :2 * B.MT_TRACE_PHASES].reshape(G, B.MT_TRACE_PHASES, 2)[:, :nb].astype(np.float64)
+    jobs = tv[:G, 2 * B.MT_TRACE_PHASES:].reshape(G, B.MT_TRACE_JOBS, 2)
+    nj = int((jobs[0, :, 0] > 0).sum())
+    span = (jobs[:, nj - 1, 0] - jobs[:, 0, 0]).astype(np.float64)
+    wait = (bars[:, :, 1] - bars[:, :, 0]).sum(axis=1)
+    del tr
+    torch.cuda.empty_cache()
+    return {"mean": float(np.mean(wait / span)), "max": float(np.max(wait / span)), "barriers": nb,
+            "source": "in-kernel trace of one traced update (MT_FLAG_TRACE), per CTA: "
+                      "sum of (release - arrival) at grid barriers / launch span"}
+
+
+def run_ours(args, cfg, rank, world, wflags=0):
     import torch
     from adamw_persistent_sm_gb300 import binding as B
     from adamw_persistent_sm_gb300.trainer import MoETrainer
@@ -182,7 +331,8 @@ def run_ours(args, cfg, rank, world):
     B.load(build_if_missing=True)
     params = mi.make_params(cfg)
     host_toks = mi.make_update_tokens(cfg)
-    tr = MoETrainer(cfg, dev, flags=_sched_flags(args))
+    flags = wflags | _sched_flags(args)
+    tr = MoETrainer(cfg, dev, flags=flags)
     tr.load_params(params)
     dtoks = [torch.as_tensor(t).to(dev) for t in host_toks]
     stream = torch.cuda.current_stream(dev)
@@ -193,8 +343,7 @@ def run_ours(args, cfg, rank, world):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def one_update(step):
-        tr.update(dtoks, step=step)
+    one_update = make_update_fn(tr, cfg, flags, dtoks)
 
     step = 1
     for _ in range(args.warmup):
@@ -262,14 +411,28 @@ def run_ours(args, cfg, rank, world):
 
     if rank != 0:
         return
+    n_params = tr.n_params
+    arena_gb = tr.arena_bytes / 1e9
+    del tr
+    torch.cuda.empty_cache()
     peaks = load_peaks()
     flops = flops_per_update(cfg)
     launch_ms = statistics.mean(upd_ms) / cfg.micro_count
     achieved = flops / cfg.micro_count / (launch_ms / 1e3) / 1e12
+    traffic = profiled_traffic(args.config)
     roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
-            "frac": achieved / peaks["bf16"], "traffic": None,
+            "frac": achieved / peaks["bf16"], "traffic": traffic,
             "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)",
+            "frac_of_nominal_dense_bf16": achieved / NOMINAL_BF16_TFLOPS,
+            "nominal_peak": NOMINAL_BF16_TFLOPS,
+            "algorithmic_bytes_param_term": param_bytes_per_update(n_params, cfg.micro_count) / cfg.micro_count,
             "kernel": "mt_megakernel<__nv_bfloat16> (the only kernel of the step)"}
+    extra = {}
+    idle = None
+    if not args.no_extra and args.config == "b32" and world == 1:
+        idle = barrier_idle_fraction(cfg, flags, dev)
+        for name in ("b2", "top8", "accum16", "selective", "looped", "b32_lowmem"):
+            extra[name] = measure_workload(name, dev)
     cpu = None
     if not args.no_cpu_baseline:
         dt, desc = oracle_sample_time(cfg, params, host_toks, min(cfg.seq, args.cpu_tokens))
@@ -294,7 +457,7 @@ def run_ours(args, cfg, rank, world):
                    "tokens_per_update": cfg.tokens_per_update,
                    "flops_per_update": flops,
                    "l2": "inputs larger than L2 (arena %.1f GB, params %.2f GB)" % (
-                       tr.arena_bytes / 1e9, tr.n_params * 4 / 1e9),
+                       arena_gb, n_params * 4 / 1e9),
                    "replicas": world,
                    "context_h100_ms_per_update": {"b2": [13.63, 13.77], "b32": [68.27, 68.61]}.get(args.config)},
         "tflops": achieved,
@@ -302,6 +465,8 @@ def run_ours(args, cfg, rank, world):
         "launches_per_update": cfg.micro_count,
         "grid_barriers_per_launch": out.n_phases,
         "roofline": roof,
+        "barrier_idle_frac": idle,
+        "other_workloads": extra or None,
         "clocks": clock_info,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -319,7 +484,7 @@ JOB_NAMES = {0: "barrier wait", 1: "embed", 2: "qkv", 3: "attn_fwd", 4: "wo", 5:
              19: "down_dgrad", 20: "down_wgrad", 21: "gateup_dgrad", 22: "gateup_wgrad", 23: "moe_bwd2",
              24: "wo_dgrad", 25: "wo_wgrad", 26: "attn_bwd_dq", 27: "qkv_dgrad", 28: "qkv_wgrad",
              29: "attn_norm_bwd", 30: "embed_bwd", 31: "norm_partial", 32: "wo_ksum", 33: "qkv_ksum",
-             34: "adamw", 35: "attn_bwd_dkdv", 36: "router_wait"}
+             34: "adamw", 35: "attn_bwd_dkdv", 36: "router_wait", 37: "gateup_again"}
 
 
 def _sched_flags(args):
@@ -426,6 +591,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--trace", action="store_true", help="print the per-job time of one update")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="b32 only: skip the other workloads and the traced barrier-idle measurement")
     ap.add_argument("--barriers-only", action="store_true",
                     help="grid barriers at every hand-off (no per-block dependency counters)")
     ap.add_argument("--product", type=int, nargs=5, metavar=("M", "N", "K", "A_MN", "B_MN"),
@@ -434,7 +601,7 @@ def main():
                     help="output of --product: fp32, bf16, accumulators read and dropped, or fp32 / bf16 "
                          "written by bulk tensor stores")
     args = ap.parse_args()
-    cfg = mi.get_config(args.config)
+    cfg, wflags = workload_config(args.config)
     if args.product:
         run_product(args)
         return
@@ -452,7 +619,7 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
     try:
-        run_ours(args, cfg, rank, world)
+        run_ours(args, cfg, rank, world, wflags)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -62,11 +62,16 @@ enum {
                                      per-block dependency counters would do (same
                                      results bit for bit; for comparison) */
   /* Memory rules ("Open problems", Generality 2: what is stored and what is
-   * recomputed).  Each trades arena bytes for work; results are bit for bit
-   * those of the default plan. */
+   * recomputed).  Each trades arena bytes for work. */
   MT_FLAG_RECOMPUTE_ATTN_DS = 1u << 7, /* bf16: keep no dS^T of the attention backward
                                           (batch*heads*seq^2 bf16 per launch); the dQ items
-                                          recompute P and dS instead of reading it */
+                                          recompute P and dS instead of reading it (same
+                                          values up to fp32 summation order) */
+  MT_FLAG_RECOMPUTE_EXPERT_ACT = 1u << 9, /* keep the expert activations [g | u] and
+                                          silu(g) u of one layer instead of all L
+                                          ((L-1) * Pmax * 3 * d_ff operands fewer); the backward
+                                          re-runs each layer's gate/up product first (bit for
+                                          bit the same values) */
   /* Selective updates ("Results", "Other measured compiler work": shared
    * weights update every microbatch, experts every 16).  The shared tensors
    * (every tensor but w_gate, w_up, w_down) get their gradients overwritten
@@ -79,7 +84,7 @@ enum {
    * shared step in grad_norm / clip_coef and the expert step in
    * expert_grad_norm / expert_clip_coef / experts_updated. */
   MT_FLAG_SELECTIVE_EXPERTS = 1u << 8,
-  MT_FLAGS_ALL = (1u << 0) | (1u << 3) | (1u << 4) | (1u << 5) | (1u << 7) | (1u << 8)
+  MT_FLAGS_ALL = (1u << 0) | (1u << 3) | (1u << 4) | (1u << 5) | (1u << 7) | (1u << 8) | (1u << 9)
 };
 
 /*
@@ -109,6 +114,13 @@ typedef struct mt_hparams {
   float loss_coef;            /* per-target CE coefficient; 0 -> 1/(batch*(seq-1)*micro_count) */
   int64_t wait_timeout_ns;    /* bound on every device-side wait; 0 -> 4e9 ns */
   int64_t expert_step;        /* MT_FLAG_SELECTIVE_EXPERTS: AdamW step t of the expert tensors */
+  int32_t n_unique_layers;    /* looped model ("Results", "Other measured compiler work": repeated
+                                 layers share weights and accumulate gradients across visits):
+                                 U distinct layers, layer visit l (0 <= l < n_layers) uses weight
+                                 slot l mod U, and each slot's gradient is the sum over its visits.
+                                 0 = n_layers (no looping); else 1 <= U <= n_layers.  The per-layer
+                                 parameter tensors are stacked over the U slots. */
+  int32_t reserved0;          /* must be 0 */
 } mt_hparams;
 
 /* One parameter tensor inside the flat fp32 parameter buffer. */

@@ -16,6 +16,8 @@ Workloads (one GPU, one update each):
 * ``accum16`` - as ``b2`` with 16 microbatches of 8 x 1024, one optimizer step.
 * ``top8``    - as ``b2`` but 32 experts of d_ff 256, top-8, batch 1 x 4096,
                 Zipf(1.1) token ids.
+* ``looped``  - as ``b32`` with 4 distinct layers visited twice each (8 layer
+                visits; visit l uses the weights of layer l mod 4).
 
 The model is the pages' "TinyMoE" stand-in ("How a training megakernel works",
 section "From two weights to 200 million": attention plus expert layers whose
@@ -62,6 +64,7 @@ class MoEConfig:
     out_std: float = 0.02            # attention out-proj and expert down-proj
     token_dist: str = "uniform"      # "uniform" | "zipf1.1"
     step: int = 1                    # AdamW step index t (1-based)
+    n_unique_layers: int = 0         # looped model: distinct layers (0 = n_layers)
 
     @property
     def tokens_per_micro(self) -> int:
@@ -96,6 +99,9 @@ CONFIGS: dict[str, MoEConfig] = {
     "accum16": MoEConfig(name="accum16", batch=8, seq=1024, micro_count=16, **_BASE),
     "top8": MoEConfig(name="top8", batch=1, seq=4096, token_dist="zipf1.1",
                       **{**_BASE, "n_experts": 32, "top_k": 8, "d_ff": 256}),
+    # looped ("SMELT-style") model: the same trunk with 4 distinct layers,
+    # each visited twice (visit l uses the weights of layer l mod 4)
+    "looped": MoEConfig(name="looped", batch=32, seq=1024, n_unique_layers=4, **_BASE),
 }
 
 
@@ -109,7 +115,8 @@ def param_shapes(cfg: MoEConfig) -> list[tuple[str, tuple[int, ...]]]:
     ``wqkv`` rows are [q; k; v], head h owning rows h*head_dim..(h+1)*head_dim-1
     inside each block; every matrix is stored [out, in] (row = output feature).
     """
-    V, d, L, E, F = cfg.vocab, cfg.d_model, cfg.n_layers, cfg.n_experts, cfg.d_ff
+    V, d, E, F = cfg.vocab, cfg.d_model, cfg.n_experts, cfg.d_ff
+    L = cfg.n_unique_layers or cfg.n_layers          # per-layer tensors: one slot per distinct layer
     hq = cfg.n_heads * cfg.head_dim
     return [
         ("emb", (V, d)),

@@ -231,11 +231,19 @@ class Dims:
     F: int
     eps: float
     theta: float
+    U: int = 0          # looped model: distinct layers; visit l uses weights l mod U (0: U = L)
 
     @staticmethod
     def of(cfg) -> "Dims":
         return Dims(cfg.vocab, cfg.d_model, cfg.n_layers, cfg.n_heads, cfg.head_dim,
-                    cfg.n_experts, cfg.top_k, cfg.d_ff, cfg.norm_eps, cfg.rope_theta)
+                    cfg.n_experts, cfg.top_k, cfg.d_ff, cfg.norm_eps, cfg.rope_theta,
+                    getattr(cfg, "n_unique_layers", 0))
+
+    def slot(self, l: int) -> int:
+        """Weights of layer visit l ("Results", "Other measured compiler work":
+        the looped model's repeated layers share weights; gradients of a
+        slot accumulate over its visits)."""
+        return l % (self.U or self.L)
 
 
 def to64(params: dict) -> dict:
@@ -244,7 +252,8 @@ def to64(params: dict) -> dict:
 
 def moe_forward(r2, l, P, D: Dims, route_z=None):
     """Router, top-k, route_order and the per-expert SwiGLU products of one
-    expert layer.  Returns the weighted combination [T, d] and a cache.
+    expert layer (weights of layer slot l).  Returns the weighted combination
+    [T, d] and a cache.
 
     ``route_z`` (optional, [T, E]): logits on which the top-k *choice* is made
     instead of this layer's own logits.  The weights are still the oracle's
@@ -343,15 +352,16 @@ def forward_backward(P: dict, tokens: np.ndarray, D: Dims, coef: float, grads: d
     caches = []
     for l in range(D.L):
         x_in = x
-        r, inv = rmsnorm(x_in, P["attn_norm"][l], D.eps)
-        qkv = r @ P["wqkv"][l].T
+        w = D.slot(l)                                # weights of this layer visit
+        r, inv = rmsnorm(x_in, P["attn_norm"][w], D.eps)
+        qkv = r @ P["wqkv"][w].T
         q = rope(heads(qkv[:, :hq]), cos, sin)
         k = rope(heads(qkv[:, hq:2 * hq]), cos, sin)
         v = heads(qkv[:, 2 * hq:])
         o = unheads(causal_attention(q, k, v))
-        x_mid = x_in + o @ P["wo"][l].T
-        r2, inv2 = rmsnorm(x_mid, P["moe_norm"][l], D.eps)
-        moe_out, mc = moe_forward(r2, l, P, D,
+        x_mid = x_in + o @ P["wo"][w].T
+        r2, inv2 = rmsnorm(x_mid, P["moe_norm"][w], D.eps)
+        moe_out, mc = moe_forward(r2, w, P, D,
                                   None if route_logits is None else route_logits[l])
         x = x_mid + moe_out
         caches.append(dict(x_in=x_in, r=r, inv=inv, q=q, k=k, v=v, o=o,
@@ -389,22 +399,23 @@ def forward_backward(P: dict, tokens: np.ndarray, D: Dims, coef: float, grads: d
     grads["final_norm"] += dgf
     for l in reversed(range(D.L)):
         c = caches[l]
+        w = D.slot(l)                                # gradients of a slot add over its visits
         # expert half: x = x_mid + moe(rmsnorm(x_mid))
-        dr2 = moe_backward(dx, c["r2"], c["moe"], l, P, D, grads)
-        dxm, dg2 = rmsnorm_backward(dr2, c["x_mid"], c["inv2"], P["moe_norm"][l])
-        grads["moe_norm"][l] += dg2
+        dr2 = moe_backward(dx, c["r2"], c["moe"], w, P, D, grads)
+        dxm, dg2 = rmsnorm_backward(dr2, c["x_mid"], c["inv2"], P["moe_norm"][w])
+        grads["moe_norm"][w] += dg2
         dx = dx + dxm
         # attention half: x_mid = x_in + attn(rmsnorm(x_in)) Wo^T
-        grads["wo"][l] += dx.T @ c["o"]
-        do = heads(dx @ P["wo"][l])
+        grads["wo"][w] += dx.T @ c["o"]
+        do = heads(dx @ P["wo"][w])
         dq, dk, dv = causal_attention_backward(do, c["q"], c["k"], c["v"])
         dqkv = np.concatenate([unheads(rope_backward(dq, cos, sin)),
                                unheads(rope_backward(dk, cos, sin)),
                                unheads(dv)], axis=1)
-        grads["wqkv"][l] += dqkv.T @ c["r"]
-        dr = dqkv @ P["wqkv"][l]
-        dxa, dg1 = rmsnorm_backward(dr, c["x_in"], c["inv"], P["attn_norm"][l])
-        grads["attn_norm"][l] += dg1
+        grads["wqkv"][w] += dqkv.T @ c["r"]
+        dr = dqkv @ P["wqkv"][w]
+        dxa, dg1 = rmsnorm_backward(dr, c["x_in"], c["inv"], P["attn_norm"][w])
+        grads["attn_norm"][w] += dg1
         dx = dx + dxa
     np.add.at(grads["emb"], tok, dx)
 

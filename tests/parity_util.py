@@ -59,7 +59,7 @@ _WORKER_P = {}
 def _oracle_block(job):
     import oracle
     cfg, tokens, coef, route_rows = job
-    key = (cfg.name, cfg.n_experts, cfg.top_k, cfg.d_ff)
+    key = (cfg.name, cfg.n_experts, cfg.top_k, cfg.d_ff, cfg.n_layers, cfg.n_unique_layers)
     if key not in _WORKER_P:
         _WORKER_P.clear()
         _WORKER_P[key] = oracle.to64(mi.make_params(cfg))

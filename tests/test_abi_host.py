@@ -108,7 +108,7 @@ def test_train_update_argument_checks(lib):
 
 
 def test_struct_sizes_match_header(lib):
-    assert C.sizeof(B.mt_hparams) == 120
+    assert C.sizeof(B.mt_hparams) == 128
     assert C.sizeof(B.mt_outputs) == 40 + 4 * 16 * 64 + 12
 
 
@@ -143,7 +143,7 @@ def test_unknown_flags_and_untiled_bf16_shapes_are_refused():
     CUDA-core fallback for bf16)."""
     from adamw_persistent_sm_gb300 import binding as B
     cfg = mi.get_config("b2")
-    for bit in (1, 2, 6, 9, 31):
+    for bit in (1, 2, 6, 10, 31):
         assert B.mt_arena_bytes(B.hparams(cfg, flags=1 << bit)) == -B.MT_ERR_ARG
     fake = 1 << 20
     args = (fake, fake, fake, fake, fake, fake)
@@ -153,3 +153,18 @@ def test_unknown_flags_and_untiled_bf16_shapes_are_refused():
     assert B.mt_train_update(*args, bad, fake, need) == B.MT_ERR_UNSUPPORTED
     bad = B.hparams(cfg.replace(d_ff=320))          # not a multiple of 256
     assert B.mt_train_update(*args, bad, fake, B.mt_arena_bytes(bad)) == B.MT_ERR_UNSUPPORTED
+
+
+def test_memory_rule_keeps_one_layer_of_expert_activations():
+    """MT_FLAG_RECOMPUTE_EXPERT_ACT drops (L-1) layers of [g | u] and
+    silu(g) u: (L-1) * Pmax * 3 * d_ff operand values."""
+    from adamw_persistent_sm_gb300 import binding as B
+    for name in ("b2", "b32", "tiny"):
+        cfg = mi.get_config(name)
+        keep = B.mt_arena_bytes(B.hparams(cfg))
+        drop = B.mt_arena_bytes(B.hparams(cfg, flags=B.MT_FLAG_RECOMPUTE_EXPERT_ACT))
+        T, K, E = cfg.tokens_per_micro, cfg.top_k, cfg.n_experts
+        pmax = -(-(T * K + E * 127) // 128) * 128
+        ob = 2 if cfg.precision == "bf16" else 4
+        saved = (cfg.n_layers - 1) * pmax * 3 * cfg.d_ff * ob
+        assert saved - 4096 < keep - drop <= saved + 4096, (name, keep - drop, saved)

@@ -29,12 +29,12 @@ from parity_util import (BF16_GRAD_TOL, BF16_LOSS_TOL, BF16_PARAM_TOL, pooled_or
 pytestmark = pytest.mark.gpu
 
 
-def run_with_logits(cfg, params, micro_tokens):
+def run_with_logits(cfg, params, micro_tokens, flags=0):
     """Run the update microbatch by microbatch, reading every layer's router
     logits after each launch (the next launch overwrites them)."""
     from adamw_persistent_sm_gb300 import binding as B
     from adamw_persistent_sm_gb300.trainer import MoETrainer
-    tr = MoETrainer(cfg, "cuda:0")
+    tr = MoETrainer(cfg, "cuda:0", flags=flags)
     tr.load_params(params)
     T, E = cfg.tokens_per_micro, cfg.n_experts
     logits, tok_loss = [], []
@@ -48,12 +48,17 @@ def run_with_logits(cfg, params, micro_tokens):
     return tr, out, logits, tok_loss
 
 
-@pytest.mark.parametrize("name", ["b2", "b32", "accum16"])
-def test_bf16_update_with_gpu_routing(name):
+@pytest.mark.parametrize("name,rule", [("b2", None), ("b32", None), ("accum16", None),
+                                       ("b2", "RECOMPUTE_ATTN_DS")])
+def test_bf16_update_with_gpu_routing(name, rule):
+    """rule: a memory rule whose path differs from the default (dQ recomputes
+    P and dS instead of reading the stored dS^T)."""
+    from adamw_persistent_sm_gb300 import binding as B
     cfg = mi.get_config(name)
     params = mi.make_params(cfg)
     toks = mi.make_update_tokens(cfg)
-    tr, out, logits, tok_loss = run_with_logits(cfg, params, toks)
+    flags = getattr(B, "MT_FLAG_" + rule) if rule else 0
+    tr, out, logits, tok_loss = run_with_logits(cfg, params, toks, flags)
     ref = pooled_oracle_update(cfg, toks, route_logits=logits)
     print(f"\n{name} (GPU routing): loss {out.loss_update:.6f} (oracle {ref.loss:.6f}), "
           f"|g| {out.grad_norm:.5f} (oracle {ref.grad_norm:.5f})")

@@ -47,3 +47,17 @@ def test_counters_are_deterministic_across_launches():
     t2, o2 = _run(cfg, 0)
     assert o1.loss == o2.loss
     assert torch.equal(t1.params, t2.params)
+
+
+@pytest.mark.parametrize("name", ["b2", "tiny"])
+def test_expert_activation_recompute_is_bit_identical(name):
+    """The memory rule that re-runs each layer's gate/up product in the
+    backward (one layer of expert activations kept) gives the default plan's
+    update bit for bit: same tiles, same inputs, same accumulation order."""
+    from adamw_persistent_sm_gb300 import binding as B
+    cfg = mi.get_config(name)
+    base, _ = _run(cfg, 0)
+    rule, _ = _run(cfg, B.MT_FLAG_RECOMPUTE_EXPERT_ACT)
+    assert rule.arena_bytes < base.arena_bytes
+    for buf in ("grads", "params", "adam_m", "adam_v"):
+        assert torch.equal(getattr(base, buf), getattr(rule, buf)), buf

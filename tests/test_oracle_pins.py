@@ -499,3 +499,49 @@ def test_selective_first_shared_step_and_expert_step():
         np.testing.assert_allclose(full.params[k], expect, rtol=1e-9, atol=1e-15)
         # and differs from stepping on the sum by the eps term only where |g| ~ eps
         assert np.any(full.expert_grads[k])
+
+
+# --------------------------------------------------------------------------
+# Looped model: repeated layers share weights, gradients add over visits
+# --------------------------------------------------------------------------
+def test_looped_model_is_the_unrolled_model_with_tied_weights():
+    """A model of U distinct layers visited L times equals the L-layer model
+    whose layer l holds a copy of slot l mod U: same loss, and each slot's
+    gradient is the sum of the unrolled layers' gradients over its visits."""
+    cfg = tiny(n_layers=4, n_unique_layers=2)
+    P = mi.make_params(cfg)
+    tok = mi.make_tokens(cfg, 0)
+    looped = oracle.train_update(P, [tok], cfg)
+    unrolled_cfg = cfg.replace(n_unique_layers=0)
+    U = {k: (np.stack([v[l % 2] for l in range(4)]) if v.ndim >= 2 and k not in ("emb", "lm_head") else v)
+         for k, v in P.items()}
+    un = oracle.train_update(U, [tok], unrolled_cfg)
+    assert looped.loss == pytest.approx(un.loss, rel=1e-13)
+    for k, g in looped.grads.items():
+        if k in ("emb", "lm_head", "final_norm"):
+            np.testing.assert_allclose(g, un.grads[k], rtol=1e-11, atol=1e-16)
+        else:
+            # visits 0, 2 use slot 0 and visits 1, 3 slot 1
+            np.testing.assert_allclose(g, un.grads[k][0:2] + un.grads[k][2:4], rtol=1e-10, atol=1e-15, err_msg=k)
+
+
+def test_looped_backward_finite_differences():
+    """Central differences on the looped model (one layer visited twice)."""
+    cfg = tiny(n_layers=2, n_unique_layers=1)
+    P = oracle.to64(mi.make_params(cfg))
+    tok = mi.make_tokens(cfg, 0)
+    r = oracle.train_update(P, [tok], cfg)
+    rng = np.random.default_rng(31)
+    h = 1e-5
+    for name in ("wqkv", "wo", "moe_norm", "router", "w_gate", "w_down", "attn_norm"):
+        flat = P[name].reshape(-1)
+        g = r.grads[name].reshape(-1)
+        for i in [int(np.argmax(np.abs(g))), *rng.choice(flat.size, size=2, replace=False)]:
+            old = flat[i]
+            flat[i] = old + h
+            lp = oracle.loss_only(P, tok, cfg)
+            flat[i] = old - h
+            lm = oracle.loss_only(P, tok, cfg)
+            flat[i] = old
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - g[i]) <= 1e-6 * abs(g[i]) + 2e-9, (name, i, fd, g[i])
