@@ -247,7 +247,11 @@ __device__ __noinline__ void job_router(const KArgs& a, int l, char* smem, const
       if (lane == 0) inv2[tb] = invb;
     }
     float za0 = -INFINITY, za1 = -INFINITY, zb0 = -INFINITY, zb1 = -INFINITY;
-#pragma unroll 1
+    // Lane l's logit sums of group e0 end up in red: the eight partials
+    // (token a: experts e0..e0+3, token b: the same) are reduce-scattered over
+    // lane bits 4, 3, 2 (one value left per lane) and summed over bits 1, 0:
+    // lane l holds partial index ((l >> 4) & 1) * 4 + ((l >> 3) & 1) * 2 + ((l >> 2) & 1).
+#pragma unroll 2
     for (int e0 = 0; e0 < D.E; e0 += 4) {
       float aa[4], ab[4];
 #pragma unroll
@@ -272,18 +276,31 @@ __device__ __noinline__ void job_router(const KArgs& a, int l, char* smem, const
           }
         }
       }
+      float v8[8] = {aa[0], aa[1], aa[2], aa[3], ab[0], ab[1], ab[2], ab[3]};
+      const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          aa[q] += __shfl_xor_sync(0xffffffffu, aa[q], o);
-          ab[q] += __shfl_xor_sync(0xffffffffu, ab[q], o);
-        }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (e0 + q == lane) { za0 = aa[q]; zb0 = ab[q]; }
-        if (e0 + q == lane + 32) { za1 = aa[q]; zb1 = ab[q]; }
+      for (int i = 0; i < 4; ++i) {        // bit 4: keep the half of index bit 2
+        const float send = b4 ? v8[i] : v8[i + 4], keep = b4 ? v8[i + 4] : v8[i];
+        v8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
       }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {        // bit 3
+        const float send = b3 ? v8[i] : v8[i + 2], keep = b3 ? v8[i + 2] : v8[i];
+        v8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+      {                                    // bit 2
+        const float send = b2 ? v8[0] : v8[1], keep = b2 ? v8[1] : v8[0];
+        v8[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+      v8[0] += __shfl_xor_sync(0xffffffffu, v8[0], 2);
+      v8[0] += __shfl_xor_sync(0xffffffffu, v8[0], 1);
+      // lane e (and e + 32) collects expert e of both tokens: index (e & 3)
+      // of token a lives in lane 8 ((e >> 1) & 1) + 4 (e & 1), of token b 16 lanes up
+      const int src = 8 * ((lane >> 1) & 1) + 4 * (lane & 1);
+      const float ga = __shfl_sync(0xffffffffu, v8[0], src);
+      const float gb = __shfl_sync(0xffffffffu, v8[0], src + 16);
+      if ((lane & ~3) == e0 && lane < D.E) { za0 = ga; zb0 = gb; }
+      if (((lane + 32) & ~3) == e0 && lane + 32 < D.E) { za1 = ga; zb1 = gb; }
     }
     pick(ta, za0, za1);
     if (tb >= 0) pick(tb, zb0, zb1);

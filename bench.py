@@ -543,6 +543,86 @@ def run_trace(args, cfg):
         print(f"    {k_:16s} {by[k_]:9.3f}")
 
 
+OPS = ("attn_fwd", "attn_bwd", "router", "lm_ce", "adamw")
+
+
+def run_op(args, cfg):
+    """One step of the update alone (mt_debug_run: the update's own device
+    code in the single-op kernel) on seeded inputs, timed with CUDA events:
+    --op attn_fwd|attn_bwd|router|lm_ce|adamw.  Prints ms per launch and the
+    algorithmic rate (FLOP/s for the tensor-core steps, bytes/s for the
+    others)."""
+    import torch
+    from adamw_persistent_sm_gb300 import binding as B
+    from adamw_persistent_sm_gb300.trainer import MoETrainer
+    if args.batch:
+        cfg = cfg.replace(batch=args.batch)
+    B.load(build_if_missing=True)
+    tr = MoETrainer(cfg, "cuda:0")
+    T, d, hq, V = cfg.tokens_per_micro, cfg.d_model, cfg.n_heads * cfg.head_dim, cfg.vocab
+    dt = torch.bfloat16 if cfg.precision == "bf16" else torch.float32
+    g = torch.Generator(device="cuda").manual_seed(11)
+
+    def fill(which, n, std=1.0, dtype=dt):
+        v = tr.debug_view(which, 0, dtype)
+        v.copy_((torch.randn(n, device="cuda", generator=g) * std).to(dtype))
+
+    opid = {"attn_fwd": B.MT_OP_ATTN_FWD, "attn_bwd": B.MT_OP_ATTN_BWD, "router": B.MT_OP_ROUTER,
+            "lm_ce": B.MT_OP_LM_CE, "adamw": B.MT_OP_CLIP_ADAMW}[args.op]
+    toks = torch.as_tensor(mi.make_tokens(cfg, 0)).cuda()
+    causal_pairs = cfg.batch * cfg.n_heads * cfg.seq * (cfg.seq + 1) / 2
+    if args.op in ("attn_fwd", "attn_bwd"):
+        fill(B.MT_VIEW_QKV, T * 3 * hq)
+        tr.debug_run(B.MT_OP_ATTN_FWD)
+        fill(B.MT_VIEW_DOUT, T * hq)
+        work, unit = (2 if args.op == "attn_fwd" else 4) * 2 * causal_pairs * cfg.head_dim, "TFLOP/s"
+        note = "causal score/probability products: QK^T and PV (forward); S, dP, dV, dK recomputed or " \
+               "accumulated plus dQ counted as twice the forward (backward)"
+    elif args.op == "router":
+        fill(B.MT_VIEW_XMID, T * d, 0.05, torch.float32)
+        ob = 2 if cfg.precision == "bf16" else 4
+        work, unit = T * (4 * d + ob * d + 4 * cfg.n_experts + 8 * cfg.top_k + ob * d + cfg.top_k * ob * d), "GB/s"
+        note = ("bytes per token: x_mid read 4d, r2 write, logits 4E, choices and weights 8K, the "
+                "dispatch gather's r2 read and K expert-row writes")
+    elif args.op == "lm_ce":
+        fill(B.MT_VIEW_FINAL_NORM, T * d)
+        tr.params.normal_(0.0, 0.02, generator=g)
+        tr.sync_shadow()
+        work, unit = 2.0 * T * V * d, "TFLOP/s"
+        note = "LM-head product 2 T V d (the fused cross-entropy rides on its epilogue and one pass)"
+    else:
+        n = tr.n_params
+        for buf, std in ((tr.params, 0.02), (tr.grads, 1e-4), (tr.adam_m, 1e-5), (tr.adam_v, 1e-9)):
+            buf.normal_(0.0, std, generator=g)
+        tr.adam_v.abs_()
+        work, unit = 34.0 * n, "GB/s"
+        note = "34 B/param: norm pass reads g (4); AdamW reads p, g, m, v (16), writes p, m, v (12) " \
+               "and the bf16 shadow (2)"
+
+    def once():
+        tr.debug_run(opid, 0, tokens=toks, step=3 if args.op == "adamw" else None)
+
+    for _ in range(args.warmup):
+        once()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(args.steps):
+        once()
+    e1.record(st)
+    torch.cuda.synchronize()
+    out = tr.outputs()
+    assert out.status == B.MT_OK, B.status_string(out.status)
+    ms = e0.elapsed_time(e1) / max(1, args.steps)
+    rate = work / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    peaks = load_peaks()
+    peak = peaks["bf16"] if unit == "TFLOP/s" else peaks["hbm"]
+    print(json.dumps({"op": args.op, "config": cfg.name, "batch": cfg.batch, "ms": ms, "rate": rate,
+                      "unit": unit, "frac_of_measured_peak": rate / peak, "work": work, "note": note,
+                      "launches": args.steps}))
+
+
 def run_product(args):
     """One matrix product C = A B^T through the megakernel's product engine
     (mt_debug_gemm): --product M N K a_mn b_mn."""
@@ -591,6 +671,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--trace", action="store_true", help="print the per-job time of one update")
+    ap.add_argument("--op", choices=OPS, help="time one step of the update alone (single-op kernel)")
+    ap.add_argument("--batch", type=int, default=0, help="--op: override the workload's batch")
     ap.add_argument("--no-extra", action="store_true",
                     help="b32 only: skip the other workloads and the traced barrier-idle measurement")
     ap.add_argument("--barriers-only", action="store_true",
@@ -607,6 +689,9 @@ def main():
         return
     if args.trace:
         run_trace(args, cfg)
+        return
+    if args.op:
+        run_op(args, cfg)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
