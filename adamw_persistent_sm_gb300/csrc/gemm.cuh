@@ -45,6 +45,7 @@ struct GOperand {
   int map0, map1;
   int y0;               // outer (row) coordinate of element (0,0) in map0/map1
   int yseg;             // outer-coordinate step per expert segment
+  int rows_per_box = 64; // K-major single-source operands: rows per TMA box of map0 (64, 128 or 256)
 };
 
 struct GemmDesc {

@@ -297,13 +297,14 @@ __device__ __forceinline__ TcTile tc_tile(const TcShape& g, int t) {
 struct TmaOp {
   const CUtensorMap* m0;
   const CUtensorMap* m1;
-  int mn, two, split, y0, yseg;
+  int mn, two, split, y0, yseg, rpb;
 };
 __device__ __forceinline__ TmaOp tma_op(const KArgs& a, const GOperand& o) {
   TmaOp t;
   t.m0 = &a.maps[o.map0];
   t.m1 = (o.map1 >= 0) ? &a.maps[o.map1] : t.m0;
   t.mn = o.mn; t.two = o.two; t.split = o.split; t.y0 = o.y0; t.yseg = o.yseg;
+  t.rpb = (!o.mn && o.two != 1) ? o.rows_per_box : 64;
   return t;
 }
 
@@ -312,6 +313,13 @@ __device__ __forceinline__ TmaOp tma_op(const KArgs& a, const GOperand& o) {
 template <int NBOX>
 __device__ __forceinline__ void tc_load_operand(const TmaOp& o, int r0, int k0, int yseg_off, uint32_t dst,
                                                 uint32_t bar) {
+  if (o.rpb > 64) {
+    // K-major, one source: taller boxes of the same 128-byte-swizzled rows
+    // (a 128-row box lands exactly where two 64-row boxes would)
+    for (int rr = 0; rr < NBOX * 64; rr += o.rpb)
+      tma_load_2d(dst + (uint32_t)rr * 128u, o.m0, k0, o.y0 + yseg_off + r0 + rr, bar);
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < NBOX; ++i) {
     const CUtensorMap* map = o.m0;

@@ -534,7 +534,12 @@ int32_t mt_debug_gemm(const void* A, int32_t a_mn, const void* B, int32_t b_mn, 
     const long long segs = rag == 1 ? nseg : 1;
     const long long ar = a_mn ? K : M, ac = a_mn ? M : K;
     const long long br = (b_mn ? K : N) * segs, bc = b_mn ? N : K;
-    int ms = mt_build_debug_maps(a, A, ar, ac, B, br, bc, a->dbg_tma ? C : nullptr, M, N, out_mode == 0);
+    // use_tc bit 4: K-major operands in one 128-row (A) / 256-row (B) box per K block
+    const bool tall = (use_tc & 16) != 0;
+    a->dbg_a_rpb = (tall && !a_mn && rag != 2) ? 128 : 64;
+    a->dbg_b_rpb = (tall && !b_mn && rag != 2) ? 256 : 64;
+    int ms = mt_build_debug_maps(a, A, ar, ac, B, br, bc, a->dbg_tma ? C : nullptr, M, N, out_mode == 0,
+                                 a->dbg_a_rpb, a->dbg_b_rpb);
     if (ms != MT_OK) { delete a; return ms; }
   }
   cudaError_t e = bf16 ? mt_launch_mega_bf16(*a, grid, smem, (cudaStream_t)stream)

@@ -2424,6 +2424,8 @@ __device__ void run_debug_gemm(const KArgs& a, char* smem, TcState& tc, Sched& s
   B.p0 = a.dbg_b; B.p1 = nullptr; B.mn = a.dbg_b_mn; B.ld = B.mn ? g.N : g.K;
   B.seg = (long long)g.N * g.K; B.two = 0; B.split = 0; B.map0 = MAP_WQKV; B.map1 = -1; B.y0 = 0;
   B.yseg = B.mn ? g.K : g.N;
+  A.rows_per_box = a.dbg_a_rpb > 0 ? a.dbg_a_rpb : 64;
+  B.rows_per_box = a.dbg_b_rpb > 0 ? a.dbg_b_rpb : 64;
   g.A = A;
   g.B = B;
   run_gemm<OP>(a, g, s, smem, tc);

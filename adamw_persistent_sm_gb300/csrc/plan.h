@@ -204,6 +204,7 @@ struct KArgs {
   int dbg_m, dbg_n, dbg_k, dbg_a_mn, dbg_b_mn, dbg_rag, dbg_nseg;
   int dbg_out_mode;             // 0 fp32 C, 1 bf16 C (written over the fp32 buffer), 2 accumulators read only
   int dbg_tma;                  // C written by the bulk-store epilogue (map MAP_E_Y fp32 / MAP_E_QKV bf16)
+  int dbg_a_rpb, dbg_b_rpb;     // rows per TMA box of the harness's A and B maps
   const int* dbg_offs;
   int use_tc;                   // tcgen05 GEMMs (bf16 only)
   int use_dsg;                  // dQ as a product over stored dS^T (A_DSG, MAP_E_DS/DSL; bf16 only)

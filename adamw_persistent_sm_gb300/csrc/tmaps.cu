@@ -111,11 +111,11 @@ int mt_build_tensor_maps(KArgs* a, void* shadow) {
 
 int mt_build_debug_maps(KArgs* a, const void* A, long long a_rows, long long a_cols, const void* B,
                         long long b_rows, long long b_cols, const void* C, long long c_rows, long long c_cols,
-                        bool c_f32) {
+                        bool c_f32, int a_rpb, int b_rpb) {
   std::call_once(g_once, resolve);
   if (!g_encode) return MT_ERR_CUDA;
-  bool ok = encode(&a->maps[MAP_R], A, a_rows, a_cols);
-  ok &= encode(&a->maps[MAP_WQKV], B, b_rows, b_cols);
+  bool ok = encode_box(&a->maps[MAP_R], A, a_rows, a_cols, false, 64, (unsigned)a_rpb, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok &= encode_box(&a->maps[MAP_WQKV], B, b_rows, b_cols, false, 64, (unsigned)b_rpb, CU_TENSOR_MAP_SWIZZLE_128B);
   if (C) ok &= encode_epi(&a->maps[c_f32 ? MAP_E_Y : MAP_E_QKV], C, c_rows, c_cols, c_f32);
   return ok ? MT_OK : MT_ERR_ARG;
 }

@@ -557,6 +557,8 @@ def run_op(args, cfg):
     from adamw_persistent_sm_gb300.trainer import MoETrainer
     if args.batch:
         cfg = cfg.replace(batch=args.batch)
+    if args.layers:
+        cfg = cfg.replace(n_layers=args.layers, n_unique_layers=0)
     B.load(build_if_missing=True)
     tr = MoETrainer(cfg, "cuda:0")
     T, d, hq, V = cfg.tokens_per_micro, cfg.d_model, cfg.n_heads * cfg.head_dim, cfg.vocab
@@ -618,7 +620,7 @@ def run_op(args, cfg):
     rate = work / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
     peaks = load_peaks()
     peak = peaks["bf16"] if unit == "TFLOP/s" else peaks["hbm"]
-    print(json.dumps({"op": args.op, "config": cfg.name, "batch": cfg.batch, "ms": ms, "rate": rate,
+    print(json.dumps({"op": args.op, "config": cfg.name, "batch": cfg.batch, "layers": cfg.n_layers, "ms": ms, "rate": rate,
                       "unit": unit, "frac_of_measured_peak": rate / peak, "work": work, "note": note,
                       "launches": args.steps}))
 
@@ -640,7 +642,8 @@ def run_product(args):
 
     def once():
         r = B.mt_debug_gemm(A.data_ptr(), amn, Bm.data_ptr(), bmn, C.data_ptr(), M, N, K, 0, 0, 0,
-                            B.MT_PREC_BF16, 1 | (out_mode << 1), arena.data_ptr(), arena.numel(), st)
+                            B.MT_PREC_BF16, 1 | (out_mode << 1) | (16 if args.product_tall else 0),
+                            arena.data_ptr(), arena.numel(), st)
         assert r == B.MT_OK, B.status_string(r)
 
     for _ in range(args.warmup):
@@ -655,7 +658,7 @@ def run_product(args):
     ms = e0.elapsed_time(e1) / max(1, args.steps)
     o = B.mt_read_outputs(arena.data_ptr(), st)
     assert o.status == B.MT_OK
-    print(json.dumps({"product": [M, N, K, amn, bmn], "out": args.product_out, "ms": ms,
+    print(json.dumps({"product": [M, N, K, amn, bmn], "out": args.product_out, "tall": args.product_tall, "ms": ms,
                       "tflops": 2.0 * M * N * K / ms / 1e9}))
 
 
@@ -673,12 +676,15 @@ def main():
     ap.add_argument("--trace", action="store_true", help="print the per-job time of one update")
     ap.add_argument("--op", choices=OPS, help="time one step of the update alone (single-op kernel)")
     ap.add_argument("--batch", type=int, default=0, help="--op: override the workload's batch")
+    ap.add_argument("--layers", type=int, default=0, help="--op: override the workload's layer count")
     ap.add_argument("--no-extra", action="store_true",
                     help="b32 only: skip the other workloads and the traced barrier-idle measurement")
     ap.add_argument("--barriers-only", action="store_true",
                     help="grid barriers at every hand-off (no per-block dependency counters)")
     ap.add_argument("--product", type=int, nargs=5, metavar=("M", "N", "K", "A_MN", "B_MN"),
                     help="time one product through the tensor-core engine")
+    ap.add_argument("--product-tall", action="store_true",
+                    help="--product: K-major operands in 128-row (A) / 256-row (B) TMA boxes")
     ap.add_argument("--product-out", default="f32", choices=["f32", "bf16", "none", "f32-bulk", "bf16-bulk"],
                     help="output of --product: fp32, bf16, accumulators read and dropped, or fp32 / bf16 "
                          "written by bulk tensor stores")
