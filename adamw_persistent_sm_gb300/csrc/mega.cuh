@@ -1445,7 +1445,7 @@ __device__ __forceinline__ bool router_grad_cta(const KArgs& a, int l, char* sme
   const uint32_t rowb = (uint32_t)D.d * 4u, dzb = (uint32_t)D.E * 4u;
   const uint32_t stage_bytes = ((uint32_t)RG_TB * (rowb + dzb) + 127u) & ~127u;
   int ns = (int)(((uint32_t)a.smem_bytes - RP_WIN_OFF) / stage_bytes);
-  if (ns > 3) ns = 3;
+  if (ns > 4) ns = 4;
   if (ns < 2 || (dzb & 15u)) return false;
   const float* XM = abuf<float>(a, A_XM) + (long long)l * D.T * D.d;
   const float* inv2 = abuf<float>(a, A_INV2) + (long long)l * D.T;
@@ -1480,7 +1480,7 @@ __device__ __forceinline__ bool router_grad_cta(const KArgs& a, int l, char* sme
     const uint32_t st = ring + (uint32_t)(b % ns) * stage_bytes, bar = bar0 + 8u * (uint32_t)(b % ns);
     mbar_expect_tx(bar, (uint32_t)nt * (rowb + dzb));
     bulk_g2s(st + (uint32_t)RG_TB * rowb, DZ + (long long)tb * D.E, (uint32_t)nt * dzb, bar);
-    for (int r = 0; r < nt; ++r) bulk_g2s(st + (uint32_t)r * rowb, XM + (long long)(tb + r) * D.d, rowb, bar);
+    bulk_g2s(st, XM + (long long)tb * D.d, (uint32_t)nt * rowb, bar);    // the batch's rows are contiguous
   };
   if (threadIdx.x == 0)
     for (int b = 0; b < nb && b < ns; ++b) issue(b);
@@ -1561,12 +1561,28 @@ static __device__ __noinline__ void job_colfinal(const KArgs& a, int row0, int n
   const int nused = nchunks > 0 ? nchunks : col_nchunks(D, G, E_kind);
   const float* PART = abuf<float>(a, A_PART);
   const int n = nrows * D.d;
-  for (int e = s.first() * MT_THREADS + threadIdx.x; e < n; e += G * MT_THREADS) {
-    const int r = e / D.d, col = e % D.d;
+  // eight lanes per output: lane j of the group adds chunks j, j+8, ... in
+  // order, then the group sums its eight partials by a fixed butterfly (so
+  // every CTA takes part; a whole warp steps together for the shuffles)
+  const long long total = (long long)n * 8;
+  const long long nthr = (long long)G * MT_THREADS;
+  const int lane = threadIdx.x & 31;
+  for (long long base = (long long)s.first() * MT_THREADS + (threadIdx.x & ~31); base < total; base += nthr) {
+    const long long w = base + lane;
+    const int e = (int)(w >> 3), sub = (int)(w & 7);
     float v = 0.f;
-    for (int cc = 0; cc < nused; ++cc) v += PART[((long long)cc * (D.E + 2) + row0 + r) * D.d + col];
-    float* dst = (last_is_separate && r == nrows - 1) ? out_last + col : out_rows + e;
-    *dst = acc ? *dst + v : v;
+    if (e < n) {
+      const int r = e / D.d, col = e % D.d;
+      for (int cc = sub; cc < nused; cc += 8) v += PART[((long long)cc * (D.E + 2) + row0 + r) * D.d + col];
+    }
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    if (sub == 0 && e < n) {
+      const int r = e / D.d, col = e % D.d;
+      float* dst = (last_is_separate && r == nrows - 1) ? out_last + col : out_rows + e;
+      *dst = acc ? *dst + v : v;
+    }
   }
   s.next(G);
 }
