@@ -470,13 +470,13 @@ constexpr uint32_t KV_OFF = 1024;                    // 2 x (K 16 KB | V 16 KB):
 constexpr uint32_t ST_OFF = KV_OFF + 4 * TILE;       // stage: Q 8 KB | dO 8 KB | lse 256 B | D 256 B
 constexpr uint32_t ST_BYTES = 17408;
 constexpr uint32_t P_OFF = ST_OFF + NST * ST_BYTES;   // 2 x P^T (128 keys x 64 queries)
-constexpr uint32_t DS_OFF = P_OFF + 2 * TILE;         // 2 x dS^T
-constexpr uint32_t DV_OFF = DS_OFF + 2 * TILE;        // 4 x 4 KB: each softmax warp's dV rows (bulk-store staging)
-constexpr uint32_t END = DV_OFF + 4 * 4096;
+constexpr uint32_t DS_OFF = P_OFF + 2 * TILE;         // 3 x dS^T (step c uses buffer c % 3)
+constexpr int NDS = 3;
+constexpr uint32_t END = DS_OFF + NDS * TILE;
 static_assert(END <= MT_TC_SMEM, "dK/dV tiles exceed the shared-memory window");
 static_assert(P_OFF % 1024 == 0 && ST_OFF % 1024 == 0 && ST_BYTES % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 enum { KVFULL = 0, KVEMPTY = 2, ACCFULL = 4, ACCEMPTY = 5, STFULL = 6, STEMPTY = STFULL + NST, SDFULL = STEMPTY + NST,
-       SDEMPTY = SDFULL + 2, PDFULL = SDEMPTY + 2, PDEMPTY = PDFULL + 2, DSFREE = PDEMPTY + 2, COUNT = DSFREE + 2 };
+       SDEMPTY = SDFULL + 2, PDFULL = SDEMPTY + 2, PDEMPTY = PDFULL + 2, DSFREE = PDEMPTY + 2, COUNT = DSFREE + NDS };
 // TMEM: S^T at 0/64, dP^T at 128/192, dV at 256, dK at 320
 constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 320;
 }
@@ -502,8 +502,8 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
     for (int i = 0; i < 2; ++i) {
       mbar_init(B_(kv::SDFULL + i), 1); mbar_init(B_(kv::SDEMPTY + i), 4);
       mbar_init(B_(kv::PDFULL + i), 4); mbar_init(B_(kv::PDEMPTY + i), 1);
-      mbar_init(B_(kv::DSFREE + i), 1);
     }
+    for (int i = 0; i < kv::NDS; ++i) mbar_init(B_(kv::DSFREE + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -585,7 +585,7 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
           if (i == 0) wait(B_(kv::ACCEMPTY), (ni & 1) ^ 1, SITE_TC_ACC_EMPTY);   // dK, dV of the last item are read
           tc_fence_after();
           const uint64_t dpt = sdesc(sbase + kv::P_OFF + sb * TILE, 16, 1024);
-          const uint64_t dst = sdesc(sbase + kv::DS_OFF + sb * TILE, 16, 1024);
+          const uint64_t dst = sdesc(sbase + kv::DS_OFF + (c % kv::NDS) * TILE, 16, 1024);
           const uint64_t dqm = sdesc(sa, 8192, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
@@ -609,8 +609,8 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
     if (lane == 0 && j.dsg) {
       // ---------------- dS^T stores ----------------
       // each step's dS^T tile (128 keys x 64 queries, swizzled) goes to HBM
-      // for the dQ product with one bulk store; the buffer is free again once
-      // the store has read it
+      // for the dQ product with one bulk store; its buffer (one of three) is
+      // released as soon as that store has read it
       const uint64_t pol = l2_evict_first();
       uint32_t c = 0;
       for (int it = first; it < items; it += G) {
@@ -618,21 +618,18 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
         item_of(it, b, h, kb);
         const int nst = (j.S - kb * 128) / 64;
         for (int i = 0; i < nst; ++i, ++c) {
-          const uint32_t sb = c & 1;
+          const uint32_t sb = c & 1, dsb = c % kv::NDS;
           wait(B_(kv::PDFULL + sb), (c >> 1) & 1, SITE_TC_FULL);
           if (!dead) {
-            tma_store_2d_hint(j.map_ds, sbase + kv::DS_OFF + sb * TILE, kb * 128 + i * 64, (b * j.H + h) * j.S + kb * 128,
+            tma_store_2d_hint(j.map_ds, sbase + kv::DS_OFF + dsb * TILE, kb * 128 + i * 64, (b * j.H + h) * j.S + kb * 128,
                               pol);
             bulk_commit();
           }
-          if (c > 0) {
-            bulk_wait_read<1>();
-            mbar_arrive(B_(kv::DSFREE + ((c - 1) & 1)));
-          }
+          bulk_wait_read<0>();
+          mbar_arrive(B_(kv::DSFREE + dsb));
         }
       }
       bulk_wait_all();
-      if (c > 0) mbar_arrive(B_(kv::DSFREE + ((c - 1) & 1)));
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -671,9 +668,10 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
           __syncwarp();
         }
         wait(B_(kv::PDEMPTY + sb), ((c >> 1) & 1) ^ 1, SITE_TC_EMPTY);
-        // the dS^T store of two steps back has read buffer sb
-        if (j.dsg) wait(B_(kv::DSFREE + sb), ((c >> 1) & 1) ^ 1, SITE_TC_EMPTY);
-        const uint32_t pb = sbase + kv::P_OFF + sb * TILE, db = sbase + kv::DS_OFF + sb * TILE;
+        // the dS^T store of three steps back has read this step's buffer
+        const uint32_t dsb = c % kv::NDS;
+        if (j.dsg) wait(B_(kv::DSFREE + dsb), ((c / kv::NDS) & 1) ^ 1, SITE_TC_EMPTY);
+        const uint32_t pb = sbase + kv::P_OFF + sb * TILE, db = sbase + kv::DS_OFF + dsb * TILE;
         // P^T and dS^T of the step; the mask only touches the first two steps,
         // the others run without the compare and select
         auto soft = [&](auto MASKc) {
@@ -714,7 +712,7 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
       }
       // dK, dV of the item's 128 keys: the key's rotary table row is loaded
       // while the last products finish; the rows are staged in this warp's
-      // rows of P^T buffer 0 (dK) and dS^T buffer 0 (dV), free once every
+      // rows of P^T buffer 0 (dK) and P^T buffer 1 (dV), free once every
       // product of the item has completed, and written by bulk stores
       const int key = kb * 128 + r;
       float4 cs[16];
@@ -735,7 +733,10 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(B_(kv::ACCEMPTY));
-      const uint32_t bk = sbase + kv::P_OFF + (uint32_t)q * 4096u, bv = sbase + kv::DV_OFF + (uint32_t)q * 4096u;
+      // dK rows in P^T buffer 0, dV rows in P^T buffer 1 (both free: every
+      // product of the item has completed, and the next item's first step
+      // waits for these stores to have read them before writing P^T)
+      const uint32_t bk = sbase + kv::P_OFF + (uint32_t)q * 4096u, bv = sbase + kv::P_OFF + TILE + (uint32_t)q * 4096u;
       float g[64];
 #pragma unroll
       for (int x = 0; x < 64; ++x) g[x] = __uint_as_float(vk[x]);
