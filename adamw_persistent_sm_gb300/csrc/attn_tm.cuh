@@ -36,6 +36,14 @@ struct AttnDeps {
 
 namespace attn_tm {
 
+// Item of round rnd for the CTA whose first item is `first`: the items are
+// ordered longest first and dealt to the G CTAs in alternating directions
+// (round 0: CTA c takes c, round 1: G - 1 - c, ...), so that no CTA takes the
+// longest item of every round.  Every CTA's role loops walk the same sequence.
+__device__ __forceinline__ int snake_item(int first, int G, int rnd) {
+  return rnd * G + ((rnd & 1) ? (G - 1 - first) : first);
+}
+
 constexpr int BQ = 128, BKEY = 128, HD = 64;
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -167,7 +175,7 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
         tma_load_2d(dst, j.map, x, y, fb);
         tma_load_2d(dst + 8192, j.map, x, y + 64, fb);
       };
-      for (int it = first; it < items; it += G, ++ni) {
+      for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_), ++ni) {
         int b, h, qb;
         item_of(j, it, b, h, qb);
         if (j.wait) {
@@ -223,7 +231,7 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
         mma_commit(B_(B_SFULL + sb));
         mma_commit(B_(B_KEMPTY + ks));                    // K_c is read
       };
-      for (int it = first; it < items; it += G, ++ni) {
+      for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_), ++ni) {
         int b, h, qb;
         item_of(j, it, b, h, qb);
         const uint32_t qs = ni & 1;
@@ -287,7 +295,7 @@ static __device__ __noinline__ void fwd_job(const Job& j, Sched& s, char* smem, 
       __syncwarp();
       if (lane == 0) mbar_arrive(B_(B_OEMPTY + pb));
     };
-    for (int it = first; it < items; it += G) {
+    for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_)) {
       int b, h, qb;
       item_of(j, it, b, h, qb);
       float o[HD];
@@ -516,7 +524,7 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
     if (lane == 0) {
       // ---------------- loads ----------------
       uint32_t c = 0, ni = 0;
-      for (int it = first; it < items; it += G, ++ni) {
+      for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_), ++ni) {
         int b, h, kb;
         item_of(it, b, h, kb);
         const int row0 = b * j.S;
@@ -570,7 +578,7 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
         }
         mma_commit(B_(kv::SDFULL + sb));
       };
-      for (int it = first; it < items; it += G, ++ni) {
+      for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_), ++ni) {
         int b, h, kb;
         item_of(it, b, h, kb);
         const int nst = (j.S - kb * 128) / 64;
@@ -613,7 +621,7 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
       // released as soon as that store has read it
       const uint64_t pol = l2_evict_first();
       uint32_t c = 0;
-      for (int it = first; it < items; it += G) {
+      for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_)) {
         int b, h, kb;
         item_of(it, b, h, kb);
         const int nst = (j.S - kb * 128) / 64;
@@ -639,7 +647,7 @@ static __device__ __noinline__ void dkdv_job(const BwdJob& j, Sched& s, char* sm
     const float sc_l2 = j.scale * LOG2E;
     const uint64_t sc2 = f2(sc_l2, sc_l2);
     uint32_t c = 0, ni = 0;
-    for (int it = first; it < items; it += G, ++ni) {
+    for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_), ++ni) {
       int b, h, kb;
       item_of(it, b, h, kb);
       const int nst = (j.S - kb * 128) / 64;
@@ -811,7 +819,7 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
   if (warp == 0) {
     if (lane == 0) {
       uint32_t c = 0, ni = 0;
-      for (int it = first; it < items; it += G, ++ni) {
+      for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_), ++ni) {
         int b, h, qb;
         item_of(it, b, h, qb);
         const int row0 = b * j.S;
@@ -858,7 +866,7 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
         }
         mma_commit(B_(qd::SDFULL + sb));
       };
-      for (int it = first; it < items; it += G, ++ni) {
+      for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_), ++ni) {
         int b, h, qb;
         item_of(it, b, h, qb);
         const int nst = 2 * (qb + 1);
@@ -896,7 +904,7 @@ static __device__ __noinline__ void dq_job(const BwdJob& j, Sched& s, char* smem
     const float sc_l2 = j.scale * LOG2E;
     const uint64_t sc2 = f2(sc_l2, sc_l2);
     uint32_t c = 0, ni = 0;
-    for (int it = first; it < items; it += G, ++ni) {
+    for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_), ++ni) {
       int b, h, qb;
       item_of(it, b, h, qb);
       const int nst = 2 * (qb + 1);
@@ -1037,7 +1045,7 @@ static __device__ __noinline__ void dqs_job(const BwdJob& j, Sched& s, char* sme
       asm volatile("fence.proxy.async;" ::: "memory");
       const uint64_t pol = l2_evict_first();     // each dS^T tile is read once
       uint32_t c = 0;
-      for (int it = first; it < items; it += G) {
+      for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_)) {
         int b, h, qb;
         item_of(it, b, h, qb);
         const int nst = 2 * (qb + 1), bh = b * j.H + h;
@@ -1059,7 +1067,7 @@ static __device__ __noinline__ void dqs_job(const BwdJob& j, Sched& s, char* sme
     if (lane == 0) {
       const uint32_t id_q = idesc_bf16(128, 64, 1, 1);     // dS (MN-major) x K (MN-major)
       uint32_t c = 0, ni = 0, last_bar = 0, last_par = 0;
-      for (int it = first; it < items; it += G, ++ni) {
+      for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_), ++ni) {
         int b, h, qb;
         item_of(it, b, h, qb);
         const int nst = 2 * (qb + 1);
@@ -1091,7 +1099,7 @@ static __device__ __noinline__ void dqs_job(const BwdJob& j, Sched& s, char* sme
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const uint32_t bq = sbase + qs::OUT_OFF + (uint32_t)q * 4096u;
     uint32_t ni = 0;
-    for (int it = first; it < items; it += G, ++ni) {
+    for (int rnd_ = 0, it = first; it < items; it = snake_item(first, G, ++rnd_), ++ni) {
       int b, h, qb;
       item_of(it, b, h, qb);
       const int query = qb * 128 + r;

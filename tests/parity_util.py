@@ -77,7 +77,7 @@ def _oracle_block(job):
 
 
 def oracle_workers() -> int:
-    """Worker count for the pooled oracle: half the host cores, bounded by
+    """Worker count for the pooled oracle: the host cores (at most 16), bounded by
     about 6 GB of host memory per worker (float64 weights, gradients and one
     sequence's activations at d 768, V 32000)."""
     cores = len(os.sched_getaffinity(0))
@@ -92,7 +92,7 @@ def oracle_workers() -> int:
             mem = min(mem, int(lim))
     except OSError:
         pass
-    return max(1, min(cores // 2, 8, int((mem - (16 << 30)) // (6 << 30))))
+    return max(1, min(cores, 16, int((mem - (16 << 30)) // (6 << 30))))
 
 
 def pooled_oracle_update(cfg, micro_tokens, route_logits=None, workers=None):

@@ -6,7 +6,8 @@ Both sides carry their own state - the GPU its fp32 master weights, bf16
 shadow and Adam moments in device memory, the oracle its float64 copies - so
 the bias corrections of steps t > 1, the non-zero moments and the round trip
 of the state through every launch are all compared.  New seeded tokens each
-step.  The tiny fp32 model runs 10 updates at 1e-4; the bf16 models run with
+step.  The tiny fp32 model runs 10 updates at 1e-4; the bf16 models (5 updates
+at 2x1024, 2 at 1x4096 top-8) run with
 the expert choices taken from the GPU's router logits (as in
 test_gpu_bf16_routed.py) under the bf16 gates.
 """
@@ -68,7 +69,7 @@ def test_tiny_ten_updates():
                 assert x < TINY_TOL, (t, k, x)
 
 
-@pytest.mark.parametrize("name,steps", [("b2", 5), ("top8", 3)])
+@pytest.mark.parametrize("name,steps", [("b2", 5), ("top8", 2)])
 def test_bf16_updates_with_gpu_routing(name, steps):
     _, rows = _run(name, steps, gpu_routing=True)
     for t, errs in enumerate(rows, 1):
