@@ -1202,18 +1202,30 @@ __device__ __noinline__ void job_moe_bwd2(const KArgs& a, int l, Sched& s, char*
 
 // Attention RMSNorm backward into dx.
 template <class OP>
-__device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s, char* smem) {
+__device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s, char* smem, const unsigned* dw,
+                                              unsigned dtarget) {
   const MtDims& D = a.D;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float* DR = abuf<float>(a, A_DR);
   const float* X = abuf<float>(a, A_X) + (long long)l * D.T * D.d;
   const float* inv = abuf<float>(a, A_INV1) + (long long)l * D.T;
   float* DX = abuf<float>(a, A_DX);
-  const int n4 = D.d / 4, nw = s.G * MT_WARPS;
-  const int me = s.first() * MT_WARPS + (threadIdx.x >> 5);
+  const int n4 = D.d / 4;
+  // CTA c takes the token chunk [c ch, (c+1) ch); warp w its tokens t0 + w + 8 j
+  const int c = blockIdx.x, ch = chunk_len(D, gridDim.x);
+  const int t0 = c * ch, t1 = min(D.T, t0 + ch);
+  const int me = t0 + warp, nw = MT_WARPS;
   const uint32_t rowb = (uint32_t)D.d * 4u;
   const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, 3u * rowb, RP_TBL * 4u);
   if (p.ns > 0) rp_begin(p);
+  else __syncthreads();
+  if (dw && t0 < t1) {
+    // the chunk's dR rows are stored by qkv dgrad tiles of other CTAs
+    const int b0 = t0 / MT_TILE_M, nb = (t1 - 1) / MT_TILE_M - b0 + 1;
+    if (threadIdx.x < nb) dep_wait(abuf<ArenaHdr>(a, A_HDR), dw + b0 + threadIdx.x, dtarget, a.timeout_ns);
+  }
+  __syncthreads();
+  if (dw && p.ns > 0 && lane == 0) asm volatile("fence.proxy.async;" ::: "memory");   // bulk loads after the acquire
   bool ok = true;
   with_nc(D.d, [&](auto NCc) {
     constexpr int NC = decltype(NCc)::value;
@@ -1223,7 +1235,7 @@ __device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s, 
     if (p.ns > 0) {
       // staged: dr, x and dx rows of each token; header: t, 1/rms (1/rms of
       // the warp's first RP_TBL tokens read up front into the table)
-      const int n = me < D.T ? (D.T - 1 - me) / nw + 1 : 0;
+      const int n = me < t1 ? (t1 - 1 - me) / nw + 1 : 0;
       if (lane < RP_TBL && lane < n) sts_f32(p.tbl + 4u * lane, inv[me + lane * nw]);
       __syncwarp();
       ok = rp_run(
@@ -1250,7 +1262,7 @@ __device__ __noinline__ void job_attn_norm_bwd(const KArgs& a, int l, Sched& s, 
           },
           [&](int) {});
     } else {
-      for (int t = me; t < D.T; t += nw) {
+      for (int t = me; t < t1; t += nw) {
         row_ld(dy, DR + (long long)t * D.d, n4);
         row_ld(x, X + (long long)t * D.d, n4);
         row_ld(acc, DX + (long long)t * D.d, n4);
@@ -2341,6 +2353,13 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   MT_SYNC();
   for (int l = D.L - 1; l >= 0; --l) {
     job_moe_bwd1<OP>(a, l, s, smem); TJ(17);
+    // the split-K slices of layer l+1's qkv weight gradient (stored before the
+    // last grid barrier; the buffer is next written by layer l's out-projection)
+    if (l + 1 < D.L) {
+      job_ksplit_sum(a, pgrad(a, P_WQKV) + (long long)wslot(a, l + 1) * 3 * D.hq * D.d, 3 * D.hq, D.d, s,
+                     acc_visit(a, P_WQKV, l + 1));
+      TJ(33);
+    }
     // memory rule: the arena keeps one layer's expert activations; re-run
     // this layer's gate/up product (same inputs, same tiles: the same values).
     // Its tiles come from a ticket; the rotating item map of the later jobs
@@ -2386,13 +2405,20 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     if (!a.use_dsg) { run_attn_bwd<OP>(a, l, s, smem, tc, attn_deps(l, false), [&] { TJ(35); }); TJ(26); }
     MT_SYNC();
     run_gemm<OP>(a, TK(gm.qkv_wgrad(l), l, TK_QKV_WGRAD), s, smem, tc); TJ(28);
-    run_gemm<OP>(a, TK(gm.qkv_dgrad(l), l, TK_QKV_DGRAD), s, smem, tc); TJ(27);
-    MT_SYNC();
-    job_attn_norm_bwd<OP>(a, l, s, smem); TJ(29);
-    job_ksplit_sum(a, pgrad(a, P_WQKV) + (long long)wslot(a, l) * 3 * D.hq * D.d, 3 * D.hq, D.d, s,
-                   acc_visit(a, P_WQKV, l)); TJ(33);
+    {
+      GemmDesc g = TK(gm.qkv_dgrad(l), l, TK_QKV_DGRAD);
+      if (dep) g.dsig = DEPC(l, DEP_DR);
+      run_gemm<OP>(a, g, s, smem, tc); TJ(27);
+    }
+    // the norm backward of a token chunk starts once the chunk's dR rows are
+    // stored (counters), else after a grid barrier
+    if (!dep) MT_SYNC();
+    job_attn_norm_bwd<OP>(a, l, s, smem, dep ? DEPC(l, DEP_DR) : nullptr, (unsigned)(D.d / TC_BN)); TJ(29);
     MT_SYNC();
   }
+  // the split-K slices of layer 0's qkv weight gradient (the other layers'
+  // are summed in the next layer's first backward phase)
+  job_ksplit_sum(a, pgrad(a, P_WQKV), 3 * D.hq, D.d, s, acc_visit(a, P_WQKV, 0)); TJ(33);
   job_embed_bwd(a, (int*)smem); TJ(30);
   MT_SYNC();
   job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM), nullptr, 0, s, (int)G, acc_visit(a, P_ATTN_NORM, 0)); TJ(18);

@@ -125,6 +125,7 @@ enum DepKind {
   DEP_O,         // [T/128] attention items stored (target: H)
   DEP_XMID,      // [T/128] out-projection tiles stored (target: d/256)
   DEP_RN,        // [T/128] 32-token combine groups stored (next layer's norm rows; target 4)
+  DEP_DR,        // [T/128] qkv dgrad tiles stored (attention-norm backward rows; target: d/256)
   DEP_ACT,       // [Pmax/128] gate/up tiles stored (target: 2F/256)
   DEP_KINDS
 };

@@ -1,7 +1,8 @@
 """Per-block dependency counters against grid barriers.  With counters on
 (the default wherever the tensor-core products and attention run), the
-hand-offs qkv -> attention -> out-projection -> router, gate/up -> down and
-combine -> next layer wait per 128-row block instead of at a grid barrier,
+hand-offs qkv -> attention -> out-projection -> router, gate/up -> down,
+combine -> next layer and (backward) qkv dgrad -> attention-norm backward
+wait per 128-row block instead of at a grid barrier,
 and attention items are drawn from ticket counters.  Every item still
 computes the same values in the same order, so the update must equal the
 barrier-only schedule bit for bit."""
@@ -37,8 +38,9 @@ def test_counters_equal_barriers_bit_for_bit(name):
     assert torch.equal(t_dep.params, t_bar.params)
     assert torch.equal(t_dep.adam_m, t_bar.adam_m)
     assert torch.equal(t_dep.adam_v, t_bar.adam_v)
-    # five forward barriers per layer are replaced by counters
-    assert o_bar.n_phases - o_dep.n_phases == 5 * cfg.n_layers
+    # five forward barriers per layer and the backward's qkv dgrad -> norm
+    # backward barrier are replaced by counters
+    assert o_bar.n_phases - o_dep.n_phases == 6 * cfg.n_layers
 
 
 def test_counters_are_deterministic_across_launches():
