@@ -151,6 +151,28 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
+// The same two instructions for a whole converged warp: every lane walks
+// the issue loop (so the operands are warp-uniform values) and one elected
+// lane - always the same one while all 32 are active - issues.  The commit
+// tracks the products of the lane that issued them, so both go through the
+// same election.
+__device__ __forceinline__ void mma_bf16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
@@ -1208,7 +1230,9 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
+    // the whole warp walks the tile sequence (warp-uniform operands); one
+    // elected lane issues the products and their commits
+    {
       const uint32_t idesc = idesc_bf16(TC_BM, TC_BN, g.A.mn, g.B.mn);
       const uint32_t a_lbo = g.A.mn ? TC_BOX_BYTES : 16, b_lbo = g.B.mn ? TC_BOX_BYTES : 16;
       const uint32_t a_kstep = g.A.mn ? 16 * 128 : 32, b_kstep = g.B.mn ? 16 * 128 : 32;
@@ -1217,23 +1241,34 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
       uint32_t it = 0, tcount = 0;
       bool ok = true;
       uint32_t last_bar = 0, last_par = 0;
-      int t;
-      while (ok && seq.next(t, hdr, tmo, lane)) {
+      // every lane waits; the outcome is made warp-uniform
+      auto wait = [&](uint32_t bar, uint32_t par, int site) {
+        const bool w = __all_sync(0xffffffffu, mbar_wait(bar, par, tmo));
+        if (!w && lane == 0) set_error(hdr, MT_ERR_DEVICE_TIMEOUT, site);
+        return w;
+      };
+      while (ok) {
+        // a drawn sequence is read by lane 0 and shared with the warp
+        int t = -1;
+        bool more = false;
+        if (lane == 0) more = seq.next(t, hdr, tmo, 0);
+        else if (!seq.ticket) more = seq.next(t, hdr, tmo, lane);
+        if (seq.ticket) {
+          more = __shfl_sync(0xffffffffu, more, 0);
+          t = __shfl_sync(0xffffffffu, t, 0);
+        }
+        if (!more) break;
         const TcTile ti = tc_tile(sh, t);
         if (ti.nk == 0) continue;
         const int ab = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
-        if (!mbar_wait(acce + 8 * ab, aph ^ 1, tmo)) {
-          set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_ACC_EMPTY);
-          break;
-        }
+        if (!wait(acce + 8 * ab, aph ^ 1, SITE_TC_ACC_EMPTY)) break;
         tc_fence_after();
         const uint32_t dt = tc.tmem_base + ab * TC_BN;
         for (int kb = 0; kb < ti.nk; ++kb, ++it) {
           const int st = it % TC_STAGES;
           const uint32_t ph = (it / TC_STAGES) & 1;
-          if (!mbar_wait(full + 8 * st, ph, tmo)) {
-            set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_FULL);
+          if (!wait(full + 8 * st, ph, SITE_TC_FULL)) {
             ok = false;
             break;
           }
@@ -1241,18 +1276,18 @@ static __device__ __noinline__ void gemm_tc_job(const KArgs& a, const GemmDesc& 
           const uint32_t soff = st * TC_STAGE_BYTES;
 #pragma unroll
           for (int j = 0; j < TC_BK / 16; ++j)
-            mma_bf16(dt, sdesc_add(ad0, soff + j * a_kstep), sdesc_add(bd0, soff + j * b_kstep), idesc,
-                     (kb > 0 || j > 0) ? 1u : 0u);
-          mma_commit(empty + 8 * st);
+            mma_bf16_warp(dt, sdesc_add(ad0, soff + j * a_kstep), sdesc_add(bd0, soff + j * b_kstep), idesc,
+                          (kb > 0 || j > 0) ? 1u : 0u);
+          mma_commit_warp(empty + 8 * st);
           last_bar = empty + 8 * st;
           last_par = ph;
         }
         if (!ok) break;
-        mma_commit(accf + 8 * ab);
+        mma_commit_warp(accf + 8 * ab);
         ++tcount;
       }
       // the tensor core must be idle before the job returns
-      if (last_bar && !mbar_wait(last_bar, last_par, tmo)) set_error(hdr, MT_ERR_DEVICE_TIMEOUT, SITE_TC_DRAIN);
+      if (last_bar) wait(last_bar, last_par, SITE_TC_DRAIN);
     }
     __syncwarp();
   } else if (warp >= 4) {

@@ -120,6 +120,41 @@ def test_attention_forward(name):
         assert np.max(np.abs(lse[b, h] - lref)) < (2e-4 if bf else 1e-5), (b, h)
 
 
+@pytest.mark.parametrize("name", ["b32", "top8"])
+def test_attention_forward_rising_scores(name):
+    """Keys whose scale grows along the sequence (1 at the first position, 6
+    at the last), so that a row's later key blocks exceed the maximum of its
+    first block by far more than 2^8 in exp2 units: the online softmax must
+    rescale the row's accumulated output and sum by large factors mid-item
+    (a stale or dropped rescale shows as an error of the size of o).  The
+    input is checked to force that (from the fp64 scores) and the output is
+    held to the bounds of the forward test."""
+    cfg = mi.get_config(name)
+    tr = _trainer(cfg)
+    qkv = _attn_inputs(cfg, 110).copy()
+    S, hq = cfg.seq, cfg.n_heads * cfg.head_dim
+    pos = np.arange(cfg.tokens_per_micro) % S
+    qkv[:, hq:2 * hq] *= (1.0 + 5.0 * pos / S)[:, None].astype(np.float32)
+    qkv = mi.round_to_bf16(qkv)
+    o, lse = _run_attn_fwd(cfg, tr, qkv)
+    q, k, v = (_heads(cfg, qkv.astype(np.float64), i) for i in range(3))
+    og = _heads(cfg, o, 0)
+    scale_l2 = 1.0 / math.sqrt(cfg.head_dim) / math.log(2.0)
+    moved = 0
+    for b, h in _pairs(cfg):
+        s = (q[b, h] @ k[b, h].T) * scale_l2
+        s = np.where(np.tril(np.ones((S, S), dtype=bool)), s, -np.inf)
+        first = s[:, :128].max(axis=1)
+        moved += int(np.sum(s.max(axis=1) > first + 8.0))
+        ref = oracle.causal_attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1])[0, 0]
+        err = np.abs(og[b, h] - ref)
+        assert np.all(err <= 8e-3 * np.abs(ref) + 8e-3), (b, h, float(err.max()))
+        assert rel_l2(og[b, h], ref) < 5e-3, (b, h)
+        lref = oracle.causal_logsumexp(q[b, h], k[b, h])
+        assert np.max(np.abs(lse[b, h] - lref)) < 2e-4 * max(1.0, float(np.max(np.abs(lref)))), (b, h)
+    assert moved > 100, moved
+
+
 @pytest.mark.parametrize("name", CASES)
 def test_attention_backward(name):
     """dq, dk (RoPE undone) and dv of the causal attention, from q, k, v, the
