@@ -935,7 +935,9 @@ __device__ __noinline__ void job_final_norm_bwd(const KArgs& a, Sched& s, char* 
 // Expert-combine backward, part 1: dY[row] = w_k dx, dw_k = <dx, y_k>,
 // router-logit gradient dz_i = w_i (dw_i - sum_j w_j dw_j) on the chosen
 // experts (the renormalised weights are the softmax of the chosen logits),
-// and zero pad rows of dY.
+// and zero pad rows of dY.  CTA c takes the token chunk the attention-norm
+// backward gives it, so that every dx row it reads was written by the same
+// CTA: the hand-off from the layer above needs no grid barrier.
 template <class OP>
 __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char* smem) {
   const MtDims& D = a.D;
@@ -948,15 +950,22 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char*
   const int* OFFS = abuf<int>(a, A_OFFS) + (long long)l * (D.E + 1);
   OP* DY = abuf<OP>(a, A_DY);
   float* DZ = abuf<float>(a, A_DZ);
-  const int nw = s.G * MT_WARPS;
-  const int me = s.first() * MT_WARPS + (threadIdx.x >> 5);
+  // tokens: the chunk [c ch, (c+1) ch) of CTA c, warp w its tokens t0 + w + 8 j
+  const int ch = chunk_len(D, gridDim.x);
+  const int t0 = (int)blockIdx.x * ch, t1 = min(D.T, t0 + ch);
+  const int me = t0 + (threadIdx.x >> 5), nw = MT_WARPS;
+  // pad rows of dY: spread over every warp of the grid
+  const int gnw = s.G * MT_WARPS, gme = s.first() * MT_WARPS + (threadIdx.x >> 5);
   const uint32_t rowb = (uint32_t)D.d * 4u;
   // index table: per token of the warp (first RP_TBL), its K sorted rows,
   // K weights and K experts (the layout of the stage header after t)
   const RowPipe p = rp_make(smem, RP_WIN_OFF, (uint32_t)a.smem_bytes, (uint32_t)(1 + D.K) * rowb,
                             (uint32_t)(RP_TBL * 3 * D.K * 4));
   const bool piped = p.ns > 0 && D.K <= 8;
+  // the chunk's dx rows were stored by this CTA's warps in the previous job
+  // (rp_begin also orders them before the bulk loads)
   if (piped) rp_begin(p);
+  else __syncthreads();
   bool ok = true;
   with_nc(D.d, [&](auto NCc) {
     constexpr int NC = decltype(NCc)::value;
@@ -964,7 +973,7 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char*
     if (piped) {
       // staged: the dx row and the K expert-output rows of each token;
       // header: t, then K sorted rows, K weights, K experts
-      const int n = me < D.T ? (D.T - 1 - me) / nw + 1 : 0;
+      const int n = me < t1 ? (t1 - 1 - me) / nw + 1 : 0;
       if (lane < RP_TBL && lane < n) {
         const int t = me + lane * nw;
         for (int k = 0; k < D.K; ++k) {
@@ -1032,7 +1041,7 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char*
           },
           [&](int) {});
     } else {
-      for (int t = me; t < D.T; t += nw) {
+      for (int t = me; t < t1; t += nw) {
         row_ld(dx, DX + (long long)t * D.d, n4);
         float dw[8], w[8];
         for (int k = 0; k < D.K; ++k) {
@@ -1065,7 +1074,7 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char*
     for (int e = 0; e < D.E; ++e) {
       const int p0 = __shfl_sync(0xffffffffu, e < 32 ? lo0 : lo1, e & 31);
       const int p1 = __shfl_sync(0xffffffffu, e < 32 ? hi0 : hi1, e & 31);
-      for (int p = p0 + me; p < p1; p += nw) row_st_op(DY + (long long)p * D.d, dy, n4);
+      for (int p = p0 + gme; p < p1; p += gnw) row_st_op(DY + (long long)p * D.d, dy, n4);
     }
   });
   if (piped) rp_end(p, ok);
@@ -2353,13 +2362,6 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
   MT_SYNC();
   for (int l = D.L - 1; l >= 0; --l) {
     job_moe_bwd1<OP>(a, l, s, smem); TJ(17);
-    // the split-K slices of layer l+1's qkv weight gradient (stored before the
-    // last grid barrier; the buffer is next written by layer l's out-projection)
-    if (l + 1 < D.L) {
-      job_ksplit_sum(a, pgrad(a, P_WQKV) + (long long)wslot(a, l + 1) * 3 * D.hq * D.d, 3 * D.hq, D.d, s,
-                     acc_visit(a, P_WQKV, l + 1));
-      TJ(33);
-    }
     // memory rule: the arena keeps one layer's expert activations; re-run
     // this layer's gate/up product (same inputs, same tiles: the same values).
     // Its tiles come from a ticket; the rotating item map of the later jobs
@@ -2370,6 +2372,14 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
       s.base = rot;
     }
     MT_SYNC();
+    // the split-K slices of layer l+1's qkv weight gradient (complete since
+    // the grid barrier above; the buffer is next written by layer l's
+    // out-projection weight gradient)
+    if (l + 1 < D.L) {
+      job_ksplit_sum(a, pgrad(a, P_WQKV) + (long long)wslot(a, l + 1) * 3 * D.hq * D.d, 3 * D.hq, D.d, s,
+                     acc_visit(a, P_WQKV, l + 1));
+      TJ(33);
+    }
     if (l == D.L - 1) job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_FINAL_NORM), nullptr, 0, s, (int)G, acc_of(a, P_FINAL_NORM));
     else job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_ATTN_NORM) + (long long)wslot(a, l + 1) * D.d, nullptr, 0, s, (int)G,
                       acc_visit(a, P_ATTN_NORM, l + 1));
@@ -2414,7 +2424,10 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     // stored (counters), else after a grid barrier
     if (!dep) MT_SYNC();
     job_attn_norm_bwd<OP>(a, l, s, smem, dep ? DEPC(l, DEP_DR) : nullptr, (unsigned)(D.d / TC_BN)); TJ(29);
-    MT_SYNC();
+    // the next layer's expert-combine backward reads only dx rows that this
+    // job stored on the same CTA (same token chunks); its other inputs are
+    // forward activations, and what it writes is read after a grid barrier
+    if (!dep || l == 0) MT_SYNC();
   }
   // the split-K slices of layer 0's qkv weight gradient (the other layers'
   // are summed in the next layer's first backward phase)

@@ -2,7 +2,9 @@
 (the default wherever the tensor-core products and attention run), the
 hand-offs qkv -> attention -> out-projection -> router, gate/up -> down,
 combine -> next layer and (backward) qkv dgrad -> attention-norm backward
-wait per 128-row block instead of at a grid barrier,
+wait per 128-row block instead of at a grid barrier, the attention-norm
+backward hands its rows to the next layer's expert-combine backward on the
+same CTA,
 and attention items are drawn from ticket counters.  Every item still
 computes the same values in the same order, so the update must equal the
 barrier-only schedule bit for bit."""
@@ -38,9 +40,11 @@ def test_counters_equal_barriers_bit_for_bit(name):
     assert torch.equal(t_dep.params, t_bar.params)
     assert torch.equal(t_dep.adam_m, t_bar.adam_m)
     assert torch.equal(t_dep.adam_v, t_bar.adam_v)
-    # five forward barriers per layer and the backward's qkv dgrad -> norm
-    # backward barrier are replaced by counters
-    assert o_bar.n_phases - o_dep.n_phases == 6 * cfg.n_layers
+    # five forward barriers per layer, the backward's qkv dgrad -> norm
+    # backward barrier (counters) and, above layer 0, the norm backward ->
+    # next layer's expert-combine backward barrier (same token chunk per CTA)
+    # are gone
+    assert o_bar.n_phases - o_dep.n_phases == 7 * cfg.n_layers - 1
 
 
 def test_counters_are_deterministic_across_launches():
