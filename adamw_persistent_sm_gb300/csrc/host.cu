@@ -115,6 +115,7 @@ void make_plan(const mt_hparams* hp, MtPlan* P) {
   sz[A_DXO] = T * d * ob;
   sz[A_DY] = Pm * d * ob;
   sz[A_DZ] = T * D.E * 4;
+  sz[A_DZB] = T * 64 * 2;
   sz[A_DGU] = Pm * 2 * D.F * ob;
   sz[A_DXS] = Pm * d * 4;
   sz[A_DR2] = T * d * 4;

@@ -950,6 +950,7 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char*
   const int* OFFS = abuf<int>(a, A_OFFS) + (long long)l * (D.E + 1);
   OP* DY = abuf<OP>(a, A_DY);
   float* DZ = abuf<float>(a, A_DZ);
+  __nv_bfloat16* DZB = abuf<__nv_bfloat16>(a, A_DZB);
   // tokens: the chunk [c ch, (c+1) ch) of CTA c, warp w its tokens t0 + w + 8 j
   const int ch = chunk_len(D, gridDim.x);
   const int t0 = (int)blockIdx.x * ch, t1 = min(D.T, t0 + ch);
@@ -1038,6 +1039,12 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char*
             }
             if (lane < D.E) DZ[(long long)t * D.E + lane] = dzl;
             if (lane + 32 < D.E) DZ[(long long)t * D.E + lane + 32] = dzh;
+            if constexpr (sizeof(OP) == 2) {
+              // bf16 operand copy for the router-weight gradient product
+              // (the lanes of absent experts hold 0)
+              DZB[(long long)t * 64 + lane] = __float2bfloat16_rn(dzl);
+              DZB[(long long)t * 64 + lane + 32] = __float2bfloat16_rn(dzh);
+            }
           },
           [&](int) {});
     } else {
@@ -1054,11 +1061,12 @@ __device__ __noinline__ void job_moe_bwd1(const KArgs& a, int l, Sched& s, char*
         }
         float mean = 0.f;
         for (int k = 0; k < D.K; ++k) mean = fmaf(w[k], dw[k], mean);
-        for (int e = lane; e < D.E; e += 32) {
+        for (int e = lane; e < 64; e += 32) {
           float v = 0.f;
           for (int k = 0; k < D.K; ++k)
             if (IDX[(long long)t * D.K + k] == e) v = w[k] * (dw[k] - mean);
-          DZ[(long long)t * D.E + e] = v;
+          if (e < D.E) DZ[(long long)t * D.E + e] = v;
+          if constexpr (sizeof(OP) == 2) DZB[(long long)t * 64 + e] = __float2bfloat16_rn(v);
         }
       }
     }
@@ -2141,6 +2149,19 @@ struct Gemms {
     g.omap = MAP_E_DR;
     return g;
   }
+  // Router-weight gradient dWr[e][c] = sum_t dz[t][e] r2[t][c] as a product
+  // over the tokens: the E rows padded to one 128-row tile (the operand
+  // columns beyond the bf16 dz copy's 64 read as zeros), the token reduction
+  // split into slices of 128 x d at `off` floats into A_KPART.
+  __device__ GemmDesc router_wgrad(int l, long long off) const {
+    GemmDesc g = base(TC_BM, D.d, D.T, EPI_GRAD);
+    g.A = opnd(abuf<__nv_bfloat16>(a, A_DZB), 64, 1); g.A.map0 = MAP_DZB;
+    g.B = opnd(abuf<OP>(a, A_R2) + (long long)l * D.T * D.d, D.d, 1);
+    g.B.map0 = MAP_R2; g.B.y0 = l * D.T;
+    g.ksplit = ksplit_of(a, TC_BM, D.d, D.T);
+    g.out = abuf<float>(a, A_KPART) + off; g.ldo = D.d; g.oseg = (long long)TC_BM * D.d; g.accumulate = 0;
+    return g;
+  }
   __device__ GemmDesc qkv_wgrad(int l) const {
     GemmDesc g = base(3 * D.hq, D.d, D.T, EPI_GRAD);
     g.A = opnd(abuf<OP>(a, A_DQKV), 3 * D.hq, 1); g.A.map0 = MAP_DQKV;
@@ -2152,22 +2173,40 @@ struct Gemms {
   }
 };
 
-// out[i] (+)= sum over slices s (in order) of KPART[s][i], i < M*N.
-static __device__ __noinline__ void job_ksplit_sum(const KArgs& a, float* out, int M, int N, Sched& s, bool acc) {
-  const int ks = ksplit_of(a, M, N, a.D.T);
-  if (ks <= 1) return;
-  const float4* P = reinterpret_cast<const float4*>(abuf<float>(a, A_KPART));
+// out[i] (+)= sum over slices k < ks (in order) of src[k * stride + i], i < n
+// (n and stride multiples of 4).
+static __device__ __noinline__ void job_slices_sum(float* out, const float* src, long long n, long long stride, int ks,
+                                                   Sched& s, bool acc) {
+  const float4* P = reinterpret_cast<const float4*>(src);
   float4* o = reinterpret_cast<float4*>(out);
-  const long long n4 = (long long)M * N / 4;
+  const long long n4 = n / 4, s4 = stride / 4;
   for (long long i = (long long)s.first() * MT_THREADS + threadIdx.x; i < n4; i += (long long)s.G * MT_THREADS) {
     float4 v = acc ? o[i] : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < ks; ++k) {
-      const float4 p = P[(long long)k * n4 + i];
+      const float4 p = P[(long long)k * s4 + i];
       v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
     }
     o[i] = v;
   }
   s.next(s.G);
+}
+// out[i] (+)= sum over slices s (in order) of KPART[s][i], i < M*N.
+static __device__ __forceinline__ void job_ksplit_sum(const KArgs& a, float* out, int M, int N, Sched& s, bool acc) {
+  const int ks = ksplit_of(a, M, N, a.D.T);
+  if (ks <= 1) return;
+  job_slices_sum(out, abuf<float>(a, A_KPART), (long long)M * N, (long long)M * N, ks, s, acc);
+}
+// Offset (floats) in A_KPART of the router-weight gradient's slices, after
+// the out-projection weight gradient's (both run in one phase), or -1 when
+// the product form does not apply (CUDA-core model, or the slices do not fit).
+__device__ __forceinline__ long long router_kpart_off(const KArgs& a) {
+  const MtDims& D = a.D;
+  const int ks = ksplit_of(a, TC_BM, D.d, D.T);
+  if (ks <= 1) return -1;
+  const int kw = ksplit_of(a, D.d, D.hq, D.T);
+  const long long off = kw > 1 ? (long long)kw * D.d * D.hq : 0;
+  if (off + (long long)ks * TC_BM * D.d > 8LL * 3 * D.hq * D.d) return -1;
+  return off;
 }
 
 // Products: tcgen05 for bf16 operands, exact fp32 FMAs on the CUDA cores for
@@ -2392,14 +2431,25 @@ __device__ void run_update(const KArgs& a, char* smem, TcState& tc, Sched& s) {
     MT_SYNC();
     job_moe_bwd2<OP>(a, l, s, smem); TJ(23);
     MT_SYNC();
-    // router-weight gradient partials (rows 0..E-1); the expert-norm gain
-    // partial was left by job_moe_bwd2
-    const int rg_chunks = job_router_grad(a, l, s, smem); TJ(16);
+    // router-weight gradient: a tensor-core product over the tokens whose
+    // slices are summed after the barrier, else (fp32 model) per-CTA partials
+    // on the CUDA cores (rows 0..E-1); the expert-norm gain partial was left
+    // by job_moe_bwd2
+    const long long rg_off = router_kpart_off(a);
+    int rg_chunks = 0;
+    if (rg_off >= 0) run_gemm<OP>(a, TK(gm.router_wgrad(l, rg_off), l, TK_ROUTER_WGRAD), s, smem, tc);
+    else rg_chunks = job_router_grad(a, l, s, smem);
+    TJ(16);
     run_gemm<OP>(a, TK(gm.wo_wgrad(l), l, TK_WO_WGRAD), s, smem, tc); TJ(25);
     run_gemm<OP>(a, TK(gm.wo_dgrad(l), l, TK_WO_DGRAD), s, smem, tc); TJ(24);
     MT_SYNC();
-    job_colfinal(a, 0, D.E, D.E, pgrad(a, P_ROUTER) + (long long)wslot(a, l) * D.E * D.d, nullptr, 0, s, rg_chunks,
-                 acc_visit(a, P_ROUTER, l));
+    if (rg_off >= 0)
+      job_slices_sum(pgrad(a, P_ROUTER) + (long long)wslot(a, l) * D.E * D.d, abuf<float>(a, A_KPART) + rg_off,
+                     (long long)D.E * D.d, (long long)TC_BM * D.d, ksplit_of(a, TC_BM, D.d, D.T), s,
+                     acc_visit(a, P_ROUTER, l));
+    else
+      job_colfinal(a, 0, D.E, D.E, pgrad(a, P_ROUTER) + (long long)wslot(a, l) * D.E * D.d, nullptr, 0, s, rg_chunks,
+                   acc_visit(a, P_ROUTER, l));
     job_colfinal(a, D.E + 1, 1, 0, pgrad(a, P_MOE_NORM) + (long long)wslot(a, l) * D.d, nullptr, 0, s, (int)G,
                  acc_visit(a, P_MOE_NORM, l)); TJ(18);
     job_ksplit_sum(a, pgrad(a, P_WO) + (long long)wslot(a, l) * D.d * D.hq, D.d, D.hq, s, acc_visit(a, P_WO, l)); TJ(32);

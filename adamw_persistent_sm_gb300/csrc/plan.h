@@ -52,6 +52,7 @@ enum ArenaId {
   A_DXO,       // op   [T][d] operand copy of A_DX
   A_DY,        // op   [Pmax][d] gradient wrt expert outputs
   A_DZ,        // fp32 [T][E] gradient wrt router logits
+  A_DZB,       // bf16 [T][64] A_DZ rounded to bf16, columns E..63 zero (operand of the router-weight gradient)
   A_DGU,       // op   [Pmax][2F] gradient wrt [g | u]
   A_DXS,       // fp32 [Pmax][d] gradient wrt expert inputs
   A_DR2,       // fp32 [T][d] gradient wrt expert RMSNorm output
@@ -75,7 +76,7 @@ enum ArenaId {
 // coordinate of a map over the whole stack.
 enum MapId {
   MAP_R = 0, MAP_WQKV, MAP_O, MAP_WO, MAP_XS, MAP_WGATE, MAP_WUP, MAP_ACT, MAP_WDOWN, MAP_RF,
-  MAP_WLM, MAP_DLOGITS, MAP_DY, MAP_DGU, MAP_DXO, MAP_DQKV, MAP_QKV, MAP_DOUT,
+  MAP_WLM, MAP_DLOGITS, MAP_DY, MAP_DGU, MAP_DXO, MAP_DQKV, MAP_QKV, MAP_DOUT, MAP_DZB, MAP_R2,
   // 32 x 32 boxes of the epilogues' bulk stores and aux loads: bf16 with the
   // 64-byte swizzle, fp32 with the 128-byte swizzle
   MAP_E_QKV, MAP_E_GU, MAP_E_ACT, MAP_E_DGU,
@@ -139,6 +140,7 @@ enum TicketId {
   TK_QKV, TK_WO, TK_GATEUP, TK_DOWN,
   TK_DOWN_DGRAD, TK_DOWN_WGRAD, TK_GU_DGRAD, TK_GU_WGRAD, TK_WO_DGRAD, TK_WO_WGRAD, TK_QKV_DGRAD, TK_QKV_WGRAD,
   TK_GATEUP_AGAIN,              // the gate/up product re-run in the backward (memory rule)
+  TK_ROUTER_WGRAD,              // the router-weight gradient product
   TK_COUNT_,
   // the head's set: LM-head products and the optimizer ranges
   TK_LM = TK_QKV, TK_LM_DGRAD = TK_WO, TK_LM_WGRAD = TK_GATEUP,

@@ -85,6 +85,8 @@ int mt_build_tensor_maps(KArgs* a, void* shadow) {
   ok &= encode(&a->maps[MAP_DQKV], A(A_DQKV), T, 3 * hq);
   ok &= encode(&a->maps[MAP_QKV], A(A_QKV), L * T, 3 * hq);
   ok &= encode(&a->maps[MAP_DOUT], A(A_DO), T, hq);
+  ok &= encode(&a->maps[MAP_DZB], A(A_DZB), T, 64);
+  ok &= encode(&a->maps[MAP_R2], A(A_R2), L * T, d);
   ok &= encode_epi(&a->maps[MAP_E_QKV], A(A_QKV), L * T, 3 * hq, false);
   ok &= encode_epi(&a->maps[MAP_E_GU], A(A_GU), AL * Pm, 2 * F, false);
   ok &= encode_epi(&a->maps[MAP_E_ACT], A(A_ACT), AL * Pm, F, false);

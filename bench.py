@@ -480,7 +480,7 @@ def run_ours(args, cfg, rank, world, wflags=0):
 # ---------------------------------------------------------------------------
 JOB_NAMES = {0: "barrier wait", 1: "embed", 2: "qkv", 3: "attn_fwd", 4: "wo", 5: "router", 6: "route",
              7: "gateup", 8: "down", 9: "combine", 10: "lm_head", 11: "ce", 12: "loss", 13: "lm_dgrad",
-             14: "lm_wgrad", 15: "final_norm_bwd", 16: "colpart", 17: "moe_bwd1", 18: "colfinal",
+             14: "lm_wgrad", 15: "final_norm_bwd", 16: "router_wgrad", 17: "moe_bwd1", 18: "colfinal",
              19: "down_dgrad", 20: "down_wgrad", 21: "gateup_dgrad", 22: "gateup_wgrad", 23: "moe_bwd2",
              24: "wo_dgrad", 25: "wo_wgrad", 26: "attn_bwd_dq", 27: "qkv_dgrad", 28: "qkv_wgrad",
              29: "attn_norm_bwd", 30: "embed_bwd", 31: "norm_partial", 32: "wo_ksum", 33: "qkv_ksum",
