@@ -183,8 +183,10 @@ size_t smem_bytes(const MtDims& D, bool tc) {
   const int er = D.E <= 4 ? 4 : D.E <= 16 ? 16 : D.E <= 32 ? 32 : 64;
   const int cw = D.E <= 16 ? 4 : D.E <= 32 ? 2 : 1;
   size_t col = 1024 + (size_t)(256 + 256 * D.E + 3 * (er + 1) * 64 * cw) * 4;
+  size_t embed = (size_t)(2 * 4096 + 8) * 4;                // embedding backward: match list
   size_t need = attn > simt ? attn : simt;
   if (router > need) need = router;
+  if (embed > need) need = embed;
   if (col > need) need = col;
   if (tc && MT_TC_SMEM > need) need = MT_TC_SMEM;
   return need;

@@ -1633,29 +1633,21 @@ static __device__ __noinline__ void job_embed_bwd(const KArgs& a, int* ism) {
     for (long long e = threadIdx.x; e < nz; e += MT_THREADS) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __syncthreads();
-  // matches of each 256-token block, compacted in ascending position order
-  int* list = ism;            // [256] positions
-  int* vid = ism + 256;       // [256] vocabulary rows
-  int* cnt = ism + 512;       // [8] per-warp counts
+  // The matches (tokens in this CTA's vocabulary rows) are compacted in
+  // ascending position order into a list of up to RB_CAP entries, eight
+  // consecutive token ids per thread and round (few rounds, each waiting on
+  // one load of ids); then the CTA adds them in list order, thread i taking
+  // float4 i of every row (a row's matches are summed in position order by
+  // the same threads, whatever the token distribution).
+  constexpr int RB_CAP = 4096, TPT = 8;
+  int* list = ism;                 // [RB_CAP] positions
+  int* vid = ism + RB_CAP;         // [RB_CAP] vocabulary rows
+  int* cnt = ism + 2 * RB_CAP;     // [8] per-warp match counts of a round
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int tb = 0; tb < D.T; tb += MT_THREADS) {
-    const int t = tb + threadIdx.x;
-    const int v = (t < D.T) ? a.tokens[t] : -1;
-    const bool hit = v >= v0 && v < v1;
-    const unsigned m = __ballot_sync(0xffffffffu, hit);
-    if (lane == 0) cnt[warp] = __popc(m);
+  int n = 0;                       // entries in the list (the same in every thread)
+  auto flush = [&]() {
     __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += cnt[w];
-    int total = 0;
-    for (int w = 0; w < MT_WARPS; ++w) total += cnt[w];
-    if (hit) {
-      const int pos = base + __popc(m & ((1u << lane) - 1u));
-      list[pos] = t;
-      vid[pos] = v;
-    }
-    __syncthreads();
-    for (int j = 0; j < total; ++j) {
+    for (int j = 0; j < n; ++j) {
       const float4* src = reinterpret_cast<const float4*>(DX + (long long)list[j] * D.d);
       float4* row = reinterpret_cast<float4*>(dE + (long long)vid[j] * D.d);
       for (int i = threadIdx.x; i < n4; i += MT_THREADS) {
@@ -1666,7 +1658,45 @@ static __device__ __noinline__ void job_embed_bwd(const KArgs& a, int* ism) {
       }
     }
     __syncthreads();
+    n = 0;
+  };
+  for (int tb = 0; tb < D.T; tb += MT_THREADS * TPT) {
+    const int tt = tb + (int)threadIdx.x * TPT;
+    int vv[TPT];
+    int nh = 0;
+#pragma unroll
+    for (int i = 0; i < TPT; ++i) {
+      vv[i] = (tt + i < D.T) ? a.tokens[tt + i] : -1;
+      nh += (vv[i] >= v0 && vv[i] < v1) ? 1 : 0;
+    }
+    // exclusive prefix of the match counts in thread order (= position order)
+    int incl = nh;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) cnt[warp] = incl;
+    __syncthreads();
+    int base = 0, total = 0;
+    for (int w = 0; w < MT_WARPS; ++w) {
+      const int cw = cnt[w];
+      if (w < warp) base += cw;
+      total += cw;
+    }
+    if (n + total > RB_CAP) flush();
+    int pos = n + base + incl - nh;
+#pragma unroll
+    for (int i = 0; i < TPT; ++i)
+      if (vv[i] >= v0 && vv[i] < v1) {
+        list[pos] = tt + i;
+        vid[pos] = vv[i];
+        ++pos;
+      }
+    n += total;
+    __syncthreads();
   }
+  flush();
 }
 
 // ===========================================================================
