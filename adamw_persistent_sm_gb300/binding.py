@@ -59,6 +59,7 @@ MT_VIEW_XMID = 15
 MT_VIEW_R2 = 16
 MT_VIEW_EXPERT_IN = 17
 MT_VIEW_FINAL_NORM = 18
+MT_VIEW_DX = 19
 
 MT_OP_ATTN_FWD = 1
 MT_OP_ATTN_BWD = 2

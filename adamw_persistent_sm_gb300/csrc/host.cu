@@ -494,6 +494,8 @@ int32_t mt_debug_view(const void* arena, const mt_hparams* hp, int32_t which, in
               D.op_bytes}; break;
     case MT_VIEW_FINAL_NORM:
       *out = {base + P.aoff[A_RF], T * D.d, D.op_bytes}; break;
+    case MT_VIEW_DX:
+      *out = {base + P.aoff[A_DX], T * D.d, 4}; break;
     default:
       return MT_ERR_ARG;
   }

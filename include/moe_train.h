@@ -268,7 +268,9 @@ enum {
   MT_VIEW_R2 = 16,            /* op [T, d] of `layer`: expert RMSNorm output (router input) */
   MT_VIEW_EXPERT_IN = 17,     /* op [Pmax, d] of `layer`: expert inputs in expert order (rows of
                                  MT_VIEW_ROUTE_PERM; pad rows zero) */
-  MT_VIEW_FINAL_NORM = 18     /* op [T, d]: final RMSNorm output (LM-head input) */
+  MT_VIEW_FINAL_NORM = 18,    /* op [T, d]: final RMSNorm output (LM-head input) */
+  MT_VIEW_DX = 19             /* fp32 [T, d]: gradient wrt the residual stream; after an update,
+                                 wrt the embedding output (the rows the embedding backward sums) */
 };
 typedef struct mt_view {
   void* ptr;
