@@ -168,3 +168,47 @@ def test_memory_rule_keeps_one_layer_of_expert_activations():
         ob = 2 if cfg.precision == "bf16" else 4
         saved = (cfg.n_layers - 1) * pmax * 3 * cfg.d_ff * ob
         assert saved - 4096 < keep - drop <= saved + 4096, (name, keep - drop, saved)
+
+
+@pytest.mark.parametrize("name", ["tiny", "b2", "top8"])
+def test_debug_views_are_disjoint_buffers_inside_the_arena(lib, name):
+    """Every debug view of the first and the last layer lies inside the arena
+    that mt_arena_bytes plans, with its documented shape; views of different
+    buffers do not overlap and start on 1024-byte boundaries; the trace view
+    exists only when the trace flag sizes the arena for it.  Host arithmetic
+    only: the arena address is never dereferenced."""
+    cfg = mi.get_config(name)
+    hp = B.hparams(cfg)
+    need = B.mt_arena_bytes(hp)
+    base = 1 << 40
+    T, d, E, K = cfg.batch * cfg.seq, cfg.d_model, cfg.n_experts, cfg.top_k
+    hq = cfg.n_heads * cfg.head_dim
+    op = 2 if cfg.precision == "bf16" else 4
+    shapes = {B.MT_VIEW_ROUTER_LOGITS: (T * E, 4), B.MT_VIEW_TOPK_IDX: (T * K, 4), B.MT_VIEW_TOPK_W: (T * K, 4),
+              B.MT_VIEW_ROUTE_OFFS: (E + 1, 4), B.MT_VIEW_TOK_LOSS: (T, 4), B.MT_VIEW_HIDDEN: (T * d, 4),
+              B.MT_VIEW_XMID: (T * d, 4), B.MT_VIEW_DX: (T * d, 4), B.MT_VIEW_QKV: (T * 3 * hq, op),
+              B.MT_VIEW_ATTN_O: (T * hq, op), B.MT_VIEW_R2: (T * d, op), B.MT_VIEW_FINAL_NORM: (T * d, op)}
+    views = [getattr(B, k) for k in dir(B) if k.startswith("MT_VIEW_") and k != "MT_VIEW_TRACE"]
+    spans = []
+    for which in views:
+        for layer in (0, cfg.n_layers - 1):
+            v = B.mt_debug_view(base, hp, which, layer)
+            lo = v.ptr - base
+            hi = lo + v.numel * v.elem_bytes
+            assert 0 <= lo < hi <= need, (which, layer)
+            if which in shapes:
+                assert (v.numel, v.elem_bytes) == shapes[which], which
+            if layer == 0:
+                assert lo % 1024 == 0, which
+                spans.append((lo, hi, which))
+    spans.sort()
+    for (_, a1, wa), (b0, _, wb) in zip(spans, spans[1:]):
+        assert a1 <= b0, (wa, wb)
+    # the residual stream entering the final norm (layer L) exists too
+    v = B.mt_debug_view(base, hp, B.MT_VIEW_HIDDEN, cfg.n_layers)
+    assert v.ptr - base + v.numel * v.elem_bytes <= need
+    with pytest.raises(ValueError):
+        B.mt_debug_view(base, hp, B.MT_VIEW_TRACE, 0)
+    ht = B.hparams(cfg, flags=B.MT_FLAG_TRACE)
+    v = B.mt_debug_view(base, ht, B.MT_VIEW_TRACE, 0)
+    assert 0 <= v.ptr - base and v.ptr - base + v.numel * v.elem_bytes <= B.mt_arena_bytes(ht)
